@@ -1,0 +1,342 @@
+"""Pins of the CPU oracle to facts the papers and the mathematics fix.
+
+None of these re-types the oracle's own formula: each compares it with a closed
+form, an invariant, a brute-force pure-Python evaluation on tiny inputs, a
+different decomposition (SVD, exhaustive search) or a hand-worked example.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bf16(a):
+    import torch
+    return torch.tensor(np.asarray(a, dtype=np.float32)).bfloat16().float().numpy().astype(np.float64)
+
+
+# ---------------------------------------------------------------- scores ----
+@pytest.mark.parametrize("Hq,Hkv,W,N,d", [(4, 2, 7, 19, 16), (1, 1, 5, 5, 8), (8, 2, 33, 40, 32)])
+def test_token_weight_mass_equals_rows(Hq, Hkv, W, N, d):
+    """Each softmax row sums to one, so sum_t w_t[g] = G * W   [RDKV §2.1]."""
+    rng = np.random.default_rng(1)
+    Q = rng.standard_normal((Hq, W, d)) * 2
+    K = rng.standard_normal((Hkv, N, d)) * 2
+    sc = O.attention_scores(Q, K, N - W)
+    np.testing.assert_allclose(sc["w_t"].sum(axis=1), (Hq // Hkv) * W, rtol=1e-12)
+
+
+@pytest.mark.parametrize("q_pos0", [0, 3, 10])
+def test_constant_keys_harmonic_closed_form(q_pos0):
+    """Equal keys give a_{r,t} = 1/(p_r+1) for t <= p_r, hence
+    w_t = G * sum_{r: p_r >= t} 1/(p_r+1) and lse_r = q_r.k/sqrt(d) + ln(p_r+1)."""
+    rng = np.random.default_rng(2)
+    Hq, Hkv, W, N, d = 6, 2, 5, 16, 8
+    N = max(N, q_pos0 + W)
+    Q = rng.standard_normal((Hq, W, d))
+    k = rng.standard_normal(d)
+    K = np.broadcast_to(k, (Hkv, N, d)).copy()
+    sc = O.attention_scores(Q, K, q_pos0)
+    G = Hq // Hkv
+    pos = q_pos0 + np.arange(W)
+    for t in range(N):
+        expect = G * sum(1.0 / (p + 1) for p in pos if p >= t)
+        np.testing.assert_allclose(sc["w_t"][:, t], expect, rtol=1e-12, atol=1e-15)
+    lse_expect = Q @ k / math.sqrt(d) + np.log(pos + 1)[None, :]
+    np.testing.assert_allclose(sc["lse"], lse_expect, rtol=1e-12)
+    # KVzip: every visible column max is the largest 1/(p+1) among rows that see t
+    for t in range(N):
+        seen = [1.0 / (p + 1) for p in pos if p >= t]
+        np.testing.assert_allclose(sc["kvzip"][:, t], max(seen) if seen else 0.0, rtol=1e-12)
+
+
+def test_single_key():
+    """N = 1: every row puts all its mass on key 0; lse equals the logit."""
+    rng = np.random.default_rng(3)
+    Q = rng.standard_normal((4, 3, 8))
+    K = rng.standard_normal((2, 1, 8))
+    sc = O.attention_scores(Q, K, 0)
+    np.testing.assert_allclose(sc["w_t"], 2 * 3, rtol=1e-14)
+    s = np.stack([Q[h] @ K[h // 2, 0] for h in range(4)]) / math.sqrt(8)
+    np.testing.assert_allclose(sc["lse"], s, rtol=1e-13)
+
+
+def _brute_scores(Q, K, V, h, WO, q_pos0):
+    """Pure-Python loops, straight from the definitions."""
+    Hq, W, d = Q.shape
+    Hkv, N, _ = K.shape
+    G = Hq // Hkv
+    D = h.shape[1]
+    lse = [[0.0] * W for _ in range(Hq)]
+    wt = [[0.0] * N for _ in range(Hkv)]
+    kz = [[0.0] * N for _ in range(Hkv)]
+    sp = [[0.0] * N for _ in range(Hkv)]
+    hn = [math.sqrt(math.fsum(float(h[r, i]) ** 2 for i in range(D))) for r in range(W)]
+    for hd in range(Hq):
+        g = hd // G
+        vn = []
+        for t in range(N):
+            acc = []
+            for i in range(D):
+                acc.append(math.fsum(float(WO[i, hd * d + c]) * float(V[g, t, c]) for c in range(d)) ** 2)
+            vn.append(math.sqrt(math.fsum(acc)))
+        for r in range(W):
+            p = q_pos0 + r
+            logits = {t: math.fsum(float(Q[hd, r, c]) * float(K[g, t, c]) for c in range(d)) / math.sqrt(d)
+                      for t in range(N) if t <= p}
+            mx = max(logits.values())
+            l = mx + math.log(math.fsum(math.exp(s - mx) for s in logits.values()))
+            lse[hd][r] = l
+            for t, s in logits.items():
+                a = math.exp(s - l)
+                wt[g][t] += a
+                kz[g][t] = max(kz[g][t], a)
+                sp[g][t] = max(sp[g][t], a / (vn[t] / hn[r]))
+    return np.array(lse), np.array(wt), np.array(kz), np.array(sp)
+
+
+@pytest.mark.parametrize("q_pos0,W,N", [(2, 4, 6), (0, 5, 5), (4, 3, 9)])
+def test_scores_brute_force(q_pos0, W, N):
+    """LSE [KVSculpt §2], w_t [RDKV §2.1], KVzip and KVzip+ [KVzap §2.1] by brute force."""
+    rng = np.random.default_rng(4 + W)
+    Hq, Hkv, d, D = 4, 2, 4, 3
+    Q = rng.standard_normal((Hq, W, d)) * 1.5
+    K = rng.standard_normal((Hkv, N, d)) * 1.5
+    V = rng.standard_normal((Hkv, N, d))
+    h = rng.standard_normal((W, D)) * np.exp(rng.standard_normal((W, 1)))
+    WO = rng.standard_normal((D, Hq * d))
+    sc = O.attention_scores(Q, K, q_pos0, V=V, h=h, W_O=WO)
+    lse, wt, kz, sp = _brute_scores(Q, K, V, h, WO, q_pos0)
+    np.testing.assert_allclose(sc["lse"], lse, rtol=1e-12)
+    np.testing.assert_allclose(sc["w_t"], wt, rtol=1e-11, atol=1e-15)
+    np.testing.assert_allclose(sc["kvzip"], kz, rtol=1e-11, atol=1e-15)
+    np.testing.assert_allclose(sc["s_plus"], sp, rtol=1e-11, atol=1e-15)
+
+
+def test_row_chunking_is_invisible():
+    rng = np.random.default_rng(5)
+    Q = rng.standard_normal((4, 37, 16))
+    K = rng.standard_normal((2, 50, 16))
+    a = O.attention_scores(Q, K, 13, row_chunk=7)
+    b = O.attention_scores(Q, K, 13, row_chunk=1000)
+    for k in ("lse", "w_t", "kvzip"):
+        np.testing.assert_allclose(a[k], b[k], rtol=1e-13)
+
+
+# ------------------------------------------------------- channel weights ----
+def test_channel_weight_is_spectral_norm_of_logit_change():
+    """w_c is the spectral norm of the logit deviation when channel c is zeroed
+    [RDKV §2.1]; the deviation is a rank-one outer product, so the bound is tight."""
+    rng = np.random.default_rng(6)
+    Hq, Hkv, W, N, d = 4, 2, 6, 11, 8
+    Q = rng.standard_normal((Hq, W, d))
+    K = rng.standard_normal((Hkv, N, d))
+    wc = O.channel_weights(Q, K)
+    G = Hq // Hkv
+    for g in range(Hkv):
+        Qg = Q[g * G:(g + 1) * G].reshape(G * W, d)
+        S = Qg @ K[g].T / math.sqrt(d)
+        for c in range(d):
+            Kz = K[g].copy()
+            Kz[:, c] = 0
+            dS = S - Qg @ Kz.T / math.sqrt(d)
+            np.testing.assert_allclose(wc[g, c], np.linalg.norm(dS, 2), rtol=1e-10)
+
+
+# --------------------------------------------------------------- sigma -----
+def test_unit_rms_brute_force():
+    rng = np.random.default_rng(7)
+    X = rng.standard_normal((2, 9, 4))
+    keep = rng.random((2, 9)) > 0.4
+    keep[1] = False
+    s0 = O.unit_rms(X, 0)
+    s1 = O.unit_rms(X, 1, keep)
+    for g in range(2):
+        for t in range(9):
+            assert math.isclose(s0[g, t], math.sqrt(math.fsum(X[g, t, c] ** 2 for c in range(4)) / 4), rel_tol=1e-13)
+        for c in range(4):
+            ts = [t for t in range(9) if keep[g, t]]
+            e = math.sqrt(math.fsum(X[g, t, c] ** 2 for t in ts) / len(ts)) if ts else 0.0
+            assert math.isclose(s1[g, c], e, rel_tol=1e-13, abs_tol=0.0)
+
+
+# ---------------------------------------------------------- allocation -----
+def test_allocation_hand_examples():
+    gold = json.load(open(os.path.join(GOLD, "alloc_hand_examples.json")))
+    for case in gold["cases"]:
+        got = O.allocate_bits(case["w"], case["sigma"], case["budget"])
+        assert got.tolist() == case["bits"], case["why"]
+
+
+def test_chord_slopes_exact():
+    assert O.chord_slopes((0, 2, 4, 8, 16)) == [3 / 8, 3 / 32, 15 / 1024, 255 / 524288]
+    assert O.chord_slopes((0, 16)) == [65535 / 1048576]
+
+
+def _exhaustive(key, widths, B):
+    best = None
+    for combo in itertools.product(widths, repeat=len(key)):
+        if sum(combo) <= B:
+            D = sum(k * 2.0 ** (-b) for k, b in zip(key, combo))
+            if best is None or D < best[0]:
+                best = (D, combo)
+    return best
+
+
+@pytest.mark.parametrize("U", [1, 3, 5, 7])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_allocation_vs_exhaustive(U, seed):
+    """Everett: the Lagrangian prefix is optimal at its own rate; the final
+    allocation fits B and sits between the exhaustive optimum and the prefix."""
+    rng = np.random.default_rng(100 * U + seed)
+    w = (rng.random(U) * rng.choice([1, 10, 100], U)).astype(np.float32)
+    s = rng.random(U).astype(np.float32) + np.float32(0.1)
+    key = (w.astype(np.float64) * s.astype(np.float64)).tolist()
+    widths = (0, 2, 4, 8, 16)
+    for B in range(0, 16 * U + 3, max(1, U)):
+        bits = O.allocate_bits(w, s, B)
+        assert int(bits.astype(int).sum()) <= B
+        D_final = O.distortion(w, s, bits)
+        D_opt, _ = _exhaustive(key, widths, B)
+        assert D_final >= D_opt * (1 - 1e-12)
+        # the prefix alone: recompute with the fix pass disabled by a budget equal to its own rate
+        c = O.chord_slopes(widths)
+        items = sorted(((-ck * k, u, j, widths[j + 1] - widths[j])
+                        for u, k in enumerate(key) for j, ck in enumerate(c) if ck * k > 0))
+        used, lvl = 0, [0] * U
+        for _, u, j, cost in items:
+            if used + cost > B:
+                break
+            used += cost
+            lvl[u] += 1
+        prefix_bits = [widths[l] for l in lvl]
+        D_prefix = sum(k * 2.0 ** (-b) for k, b in zip(key, prefix_bits))
+        assert D_final <= D_prefix * (1 + 1e-12)
+        D_at_rate, _ = _exhaustive(key, widths, used)
+        assert math.isclose(D_prefix, D_at_rate, rel_tol=1e-12), (B, prefix_bits)
+
+
+def test_allocation_extremes():
+    rng = np.random.default_rng(8)
+    w = rng.random(50).astype(np.float32)
+    s = rng.random(50).astype(np.float32) + np.float32(0.01)
+    assert (O.allocate_bits(w, s, 0) == 0).all()
+    assert (O.allocate_bits(w, s, 16 * 50) == 16).all()
+    assert (O.allocate_bits(w, s, 10 ** 9) == 16).all()
+
+
+def test_allocation_two_widths_is_topk():
+    """Widths {0,16}: keep the top-k keys (ties by lower index), k = floor(B/16)."""
+    rng = np.random.default_rng(9)
+    U = 300
+    w = rng.random(U).astype(np.float32)
+    w[::7] = w[3]                                     # plenty of ties
+    s = np.ones(U, dtype=np.float32)
+    for k in (0, 1, 17, 150, 299, 300):
+        bits = O.allocate_bits(w, s, 16 * k, widths=(0, 16))
+        key = w.astype(np.float64)
+        order = sorted(range(U), key=lambda u: (-key[u], u))
+        expect = np.zeros(U, dtype=np.uint8)
+        expect[order[:k]] = 16
+        assert (bits == expect).all()
+
+
+# --------------------------------------------------------- quantisation ----
+def test_quant_hand_examples():
+    gold = json.load(open(os.path.join(GOLD, "quant_hand_examples.json")))
+    for case in gold["cases"]:
+        wd = case["width"]
+        x = np.zeros(64)
+        x[:len(case["x"])] = case["x"]
+        X = x.reshape(1, 1, 64)
+        st = O.quantize_pack(X, 0, np.array([wd], np.uint8))[wd]
+        expect = np.zeros(case["n_bytes"], np.uint8)
+        for k, v in case["bytes_nonzero"].items():
+            expect[int(k)] = v
+        assert st["codes"].tolist() == expect.tolist(), case["why"]
+        if case["scale_bits"] is not None:
+            assert st["scales"].tolist() == [case["scale_bits"]], case["why"]
+        xh = O.dequantize({w: (st if w == wd else {"ids": np.zeros(0, np.int32)}) for w in (2, 4, 8, 16)},
+                          (1, 1, 64), 0, np.array([wd], np.uint8))
+        np.testing.assert_array_equal(xh[0, 0, :len(case["x_hat"])], np.float32(case["x_hat"]))
+
+
+def _unpack_bitloop(blk, wd):
+    """Independent unpack: walk the bits one at a time."""
+    vals = []
+    for e in range(64):
+        code = 0
+        for b in range(wd):
+            bit_index = wd * e + b
+            code |= ((int(blk[bit_index // 8]) >> (bit_index % 8)) & 1) << b
+        vals.append(code - (1 << wd) if code >= 1 << (wd - 1) else code)
+    return vals
+
+
+@pytest.mark.parametrize("wd", [2, 4, 8])
+def test_quant_bounds_and_bit_layout(wd):
+    rng = np.random.default_rng(10 + wd)
+    X = _bf16(rng.standard_normal((2, 5, 128)) * np.exp(rng.standard_normal((2, 5, 1)) * 3))
+    bits = np.full(10, wd, np.uint8)
+    st = O.quantize_pack(X, 0, bits)
+    qmax = 2 ** (wd - 1) - 1
+    s = st[wd]["scales"].view(np.float16).astype(np.float64)
+    groups = X.reshape(-1, 64)
+    a = np.abs(groups).max(axis=1)
+    assert (s * qmax >= a).all()                                              # s >= a/qmax
+    prev = np.nextafter(s.astype(np.float16), np.float16(-np.inf)).astype(np.float64)
+    assert (prev * qmax < a).all()                                            # s minimal
+    for gi in range(groups.shape[0]):
+        blk = st[wd]["codes"][gi * 8 * wd:(gi + 1) * 8 * wd]
+        q = np.array(_unpack_bitloop(blk, wd))
+        assert np.abs(q).max() <= qmax
+        xh = q * s[gi]
+        assert (np.abs(groups[gi] - xh) <= s[gi] / 2).all()                  # |x - x_hat| <= s/2
+    xh = O.dequantize(st, X.shape, 0, bits)
+    assert (np.abs(X - xh) <= np.repeat(s, 64).reshape(X.shape) / 2).all()
+
+
+def test_pack_axis1_kept_tokens_and_padding():
+    rng = np.random.default_rng(11)
+    X = _bf16(rng.standard_normal((2, 150, 64)))
+    keep = rng.random((2, 150)) > 0.3
+    bits = rng.choice([0, 2, 4, 8, 16], size=2 * 64).astype(np.uint8)
+    st = O.quantize_pack(X, 1, bits, keep)
+    xh = O.dequantize(st, X.shape, 1, bits, keep)
+    for g in range(2):
+        tk = np.nonzero(keep[g])[0]
+        ng = -(-tk.size // 64)
+        for c in range(64):
+            b = int(bits[g * 64 + c])
+            col = xh[g, :, c]
+            assert (col[~keep[g]] == 0).all()
+            if b == 0:
+                assert (col == 0).all()
+            elif b == 16:
+                np.testing.assert_array_equal(col[tk], X[g, tk, c].astype(np.float32))
+            else:
+                j = list(st[b]["ids"]).index(g * 64 + c)
+                g0 = st[b]["group_offsets"][j]
+                s = st[b]["scales"][g0:g0 + ng].view(np.float16).astype(np.float64)
+                err = np.abs(col[tk] - X[g, tk, c])
+                assert (err <= np.repeat(s, 64)[:tk.size] / 2).all()
+                last = st[b]["codes"][(g0 + ng - 1) * 8 * b:(g0 + ng) * 8 * b]
+                q = _unpack_bitloop(last, b)
+                assert all(v == 0 for v in q[tk.size - (ng - 1) * 64:])       # padding codes are 0
+
+
+def test_zero_group_and_overflow():
+    X = np.zeros((1, 1, 64))
+    st = O.quantize_pack(X, 0, np.array([4], np.uint8))
+    assert st[4]["scales"].tolist() == [0] and not st[4]["codes"].any()
+    Y = np.zeros((1, 1, 64))
+    Y[0, 0, 0] = 2.0 ** 100                                                   # bf16-exact, beyond fp16 range
+    with pytest.raises(OverflowError):
+        O.quantize_pack(Y, 0, np.array([8], np.uint8))
