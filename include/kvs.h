@@ -1,0 +1,207 @@
+/*
+ * kvs.h - C ABI of libkvs.so: attention-derived importance scoring and
+ * rate-distortion compression of a prefilled KV cache, for NVIDIA B300 (sm_103a).
+ *
+ * Sources (web summaries of the papers; section as printed there):
+ *   [RDKV]     "RDKV - Asignacion de Bits de Tasa-Distorsion para Eviccion y
+ *              Cuantizacion Conjunta de la Cache KV" (gist.science 2605.08317)
+ *   [KVzap]    "KVzap - Poda del KV Cache Rapida, Adaptativa y Fiel"
+ *              (gist.science 2601.07891)
+ *   [KVSculpt] "KVSculpt: KV Cache Compression as Distillation"
+ *              (gist.science 2603.27819)
+ *
+ * Conventions shared by every call
+ *  - Tensors are row-major and contiguous.  bf16 data is passed as its 16-bit
+ *    patterns (uint16_t).  Shapes:
+ *        Q    [Hq,  W, d]  queries of the observation window; row r is at
+ *                          absolute position q_pos0 + r
+ *        K, V [Hkv, N, d]  the cache; row t is at position t
+ *        h    [W, D]       hidden states of the window positions
+ *        W_O  [D, Hq*d]    output projection; head hd uses columns hd*d .. hd*d+d-1
+ *    Query head hd reads KV head hd / G with G = Hq / Hkv.  A query at
+ *    position p sees keys t <= p.  Logits are q.k / sqrt(d).
+ *  - Every pointer that is not marked "host" is a DEVICE pointer owned by the
+ *    caller.  The library allocates no device memory: scratch space is the
+ *    caller's workspace, sized by the matching *_workspace_size() call and
+ *    aligned to 256 bytes.  Workspace contents need not be initialised.
+ *  - Every call enqueues its kernels on `stream` (a cudaStream_t passed as
+ *    void*; NULL = the legacy default stream) and returns without
+ *    synchronising.  Outputs are valid once the stream reaches that point.
+ *  - Return value: KVS_OK or an error code.  Argument errors are detected on
+ *    the host before anything is enqueued.  Data-dependent errors found on
+ *    the device (non-finite weights, an fp16 scale overflow, a stream
+ *    capacity exceeded, a device wait that timed out) are recorded in a device
+ *    error word that kvs_get_device_error() reads; the kernels that detect
+ *    them skip the offending writes and return normally.
+ *  - Device waits are bounded: a wait that exceeds about two seconds sets
+ *    KVS_ERR_TIMEOUT in the error word and the kernel returns.
+ *  - Supported: d in {64, 128}; 1 <= G and (G <= 4 or G % 4 == 0);
+ *    0 <= q_pos0 and q_pos0 + W <= N; N, W >= 1; N < 2^31; Hkv*N < 2^31.
+ */
+#ifndef KVS_H_
+#define KVS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define KVS_OK               0
+#define KVS_ERR_INVALID_ARG  1  /* null pointer, negative or inconsistent size */
+#define KVS_ERR_UNSUPPORTED  2  /* shape outside the supported set */
+#define KVS_ERR_RANGE        3  /* non-finite / negative weight, fp16 scale overflow, capacity */
+#define KVS_ERR_CUDA         4  /* a CUDA runtime call failed */
+#define KVS_ERR_TIMEOUT      5  /* a bounded device wait ran out */
+#define KVS_ERR_WORKSPACE    6  /* workspace too small or misaligned */
+
+/* Human-readable name of a status code (static string). */
+const char* kvs_status_string(int status);
+
+/* Library ABI version (major*100 + minor). */
+int kvs_version(void);
+
+/* Reads and clears the device error word after synchronising `stream`.
+ * Returns KVS_OK when no kernel recorded an error since the last call,
+ * else the first recorded code; KVS_ERR_CUDA if the read itself failed. */
+int kvs_get_device_error(void* stream);
+
+/* ---- importance scoring ------------------------------------------------ */
+#define KVS_MODE_LSE         1u  /* lse[Hq, W]  = ln sum_{t<=p_r} exp(s_{r,t})         [KVSculpt §2, LSE term] */
+#define KVS_MODE_RDKV_WT     2u  /* w_t[Hkv, N] = sum over the group's heads and window rows of a_{r,t}
+                                                                                     [RDKV §2.1, w_t] */
+#define KVS_MODE_KVZIP       4u  /* s_plus[Hkv, N] = max over heads and rows of a_{r,t}  [KVzap §2.1, KVzip] */
+#define KVS_MODE_KVZIP_PLUS  8u  /* s_plus[Hkv, N] = max_heads max_r a^h_{r,t} |h_r| / |W_O^h v_t|
+                                                                                     [KVzap §2.1, KVzip+] */
+
+/* Bytes of workspace kvs_score_attention needs for these sizes and mode. */
+size_t kvs_score_workspace_size(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d,
+                                int64_t D, int64_t q_pos0, uint32_t mode);
+
+/* Attention-derived scores of a prefilled cache, without materialising the
+ * attention matrix.  Pass 1 computes every window row's log-sum-exp; pass 2
+ * recomputes the probabilities a = exp(s - lse) and reduces them per key.
+ *   mode    : KVS_MODE_LSE is implied; add KVS_MODE_RDKV_WT and at most one of
+ *             KVS_MODE_KVZIP / KVS_MODE_KVZIP_PLUS.
+ *   Q, K    : bf16, required.  V, h, W_O: bf16, required for KVZIP_PLUS only
+ *             (D = hidden size, ignored otherwise).
+ *   lse     : float [Hq, W], natural log, required.
+ *   w_t     : float [Hkv, N], required with RDKV_WT, else may be NULL.
+ *   s_plus  : float [Hkv, N], required with KVZIP or KVZIP_PLUS.  Keys no
+ *             query sees get w_t = 0 and s_plus = 0.
+ * Deterministic: the same inputs give the same bits. */
+int kvs_score_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                        const uint16_t* h, const uint16_t* W_O,
+                        int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t D,
+                        int64_t q_pos0, uint32_t mode,
+                        float* lse, float* w_t, float* s_plus,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Host-only: how kvs_score_attention splits its work for these sizes and
+ * mode (same rules as the call itself).  info: host int64[5] =
+ *   {key tiles per pass-1 CTA, pass-1 splits, query tiles per pass-2 CTA,
+ *    pass-2 splits, kernels the call launches}. */
+int kvs_score_plan_info(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t D,
+                        int64_t q_pos0, uint32_t mode, int64_t* info);
+
+/* Channel distortion weights  w_c[g, c] = |Q_{:,c}| |K_{:,c}| / sqrt(d)   [RDKV §2.1, w_c]
+ * The query column stacks the G heads' W window rows of group g; the key
+ * column spans all N tokens of KV head g.  w_c: float [Hkv, d]. */
+size_t kvs_channel_weights_workspace_size(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d);
+int kvs_channel_weights(const uint16_t* Q, const uint16_t* K,
+                        int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d,
+                        float* w_c, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Per-unit RMS sigma_u, the scale of a unit in the RD objective   [RDKV §2.1]
+ *   axis 0: unit = token row,  sigma[g*N + t] = sqrt(mean_c X[g,t,c]^2)      (V cache)
+ *   axis 1: unit = channel,    sigma[g*d + c] = sqrt(mean_{t kept} X[g,t,c]^2) (K cache)
+ *           token t of head g is kept iff keep_bits[g*N + t] != 0 (stage 2's
+ *           V widths; stage 3 allocates K over kept tokens only [RDKV §2.2]);
+ *           keep_bits NULL keeps every token; a head keeping none gives 0. */
+size_t kvs_unit_rms_workspace_size(int64_t Hkv, int64_t N, int64_t d, int axis);
+int kvs_unit_rms(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis,
+                 const uint8_t* keep_bits, float* sigma,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- bit allocation ---------------------------------------------------- */
+/* Width set as a bit mask: bit b set <=> width b allowed.  Width 0 (evict) is
+ * always allowed.  Allowed widths: 2, 4, 8, 16. */
+#define KVS_WIDTHS_ALL  ((1u << 2) | (1u << 4) | (1u << 8) | (1u << 16))
+#define KVS_WIDTHS_KEEP_OR_EVICT  (1u << 16)
+
+size_t kvs_allocate_workspace_size(int64_t U);
+
+/* min sum_u w_u sigma_u 2^-b_u  s.t.  sum_u b_u <= budget_bits, b_u in the
+ * width set   [RDKV §2.1 objective; §2.2 reverse water-filling / Lagrangian
+ * relaxation of the multiple-choice knapsack over {0,2,4,8,16}].
+ * key_u = (double)w_u * (double)sigma_u; the Lagrangian moves unit u from
+ * width b_k to b_{k+1} at multiplier theta = c_k * key_u (fp64), with c_k the
+ * chord slope of 2^-b.  Upgrades are taken in theta-descending order (ties:
+ * lower unit, then lower step) while they fit; a budget-fix scan then takes
+ * any later upgrade that still fits and whose previous step was taken.
+ *   w, sigma : float [U], finite and >= 0 (else KVS_ERR_RANGE in the error word)
+ *   bits     : uint8 [U] output widths.
+ * Bit-exact and deterministic. */
+int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t budget_bits,
+                      uint32_t width_mask, uint8_t* bits,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- quantise / pack / dequantise --------------------------------------- */
+/* Width-grouped streams, one per width 2, 4, 8, 16 (index 0..3)   [RDKV §2.3, TriZone].
+ * A unit is a token row (axis 0, V cache) or a channel over the kept tokens
+ * in ascending order (axis 1, K cache).  Its elements form groups of 64; a
+ * short last group is padded with code 0.  Units of one width are stored in
+ * ascending unit id (g*N + t, or g*d + c).
+ *   codes[i]         : uint8, 8*w bytes per group.  Widths 2/4/8: element e of
+ *                      a group is the w-bit two's-complement code q_e in bits
+ *                      [w*e, w*e + w) of the group's block, least significant
+ *                      first.  Width 16: the raw bf16 values, little-endian.
+ *   scales[i]        : fp16 bit patterns, one per group (widths 2/4/8 only):
+ *                      s = smallest fp16 >= absmax/qmax, qmax = 2^(w-1)-1,
+ *                      q = round-half-even(x / s); x_hat = q * s.
+ *   unit_ids[i]      : int32, the unit id of each stored unit.
+ *   group_offsets[i] : int64, the first group of each stored unit.
+ *   cap_units[i], cap_groups[i] : capacities (host values) of those arrays.
+ *   counts           : device int64[8]: units stored per width, then groups
+ *                      per width; written by kvs_quantize_pack.
+ * Overflowing a capacity records KVS_ERR_RANGE and drops the excess. */
+typedef struct kvs_stream_set {
+    uint8_t*  codes[4];
+    uint16_t* scales[4];
+    int32_t*  unit_ids[4];
+    int64_t*  group_offsets[4];
+    int64_t   cap_units[4];
+    int64_t   cap_groups[4];
+    int64_t*  counts;
+} kvs_stream_set;
+
+/* Host-only: capacities that always suffice for an allocation of at most
+ * budget_bits (a unit of width w costs w bits, so at most budget/w units of
+ * that width exist).  cap_units, cap_groups: host int64[4]. */
+int kvs_pack_capacity(int64_t Hkv, int64_t N, int64_t d, int axis, int64_t budget_bits,
+                      int64_t* cap_units, int64_t* cap_groups);
+
+size_t kvs_pack_workspace_size(int64_t Hkv, int64_t N, int64_t d, int axis);
+
+/* Quantise and pack X [Hkv, N, d] (bf16) at the widths `bits` (uint8, one per
+ * unit: Hkv*N for axis 0, Hkv*d for axis 1)   [RDKV §2.2 stages 2-3, §2.3].
+ * axis 1 needs keep_bits (uint8 [Hkv*N], nonzero = kept); axis 0 ignores it.
+ * `streams` is a HOST pointer to a struct of device pointers.  An fp16
+ * scale overflow records KVS_ERR_RANGE. */
+int kvs_quantize_pack(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis,
+                      const uint8_t* bits, const uint8_t* keep_bits,
+                      const kvs_stream_set* streams,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Inverse of kvs_quantize_pack: out float [Hkv, N, d], x_hat = q * s (exact in
+ * fp32), width 16 -> the bf16 value, width 0 and tokens not kept -> 0. */
+int kvs_dequantize(const kvs_stream_set* streams, int64_t Hkv, int64_t N, int64_t d, int axis,
+                   const uint8_t* bits, const uint8_t* keep_bits, float* out,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVS_H_ */

@@ -1,0 +1,276 @@
+"""ctypes binding of libkvs.so (C ABI in include/kvs.h).
+
+Argument marshalling only: every computation runs in the CUDA library.  Torch
+supplies device memory (outputs, workspaces, stream buffers) and the current
+CUDA stream.  There is no fallback: if the library is missing or a call fails,
+an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_int, c_int64, c_size_t, c_uint32, c_void_p
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvs.so")
+
+KVS_OK = 0
+STATUS = {0: "KVS_OK", 1: "KVS_ERR_INVALID_ARG", 2: "KVS_ERR_UNSUPPORTED", 3: "KVS_ERR_RANGE",
+          4: "KVS_ERR_CUDA", 5: "KVS_ERR_TIMEOUT", 6: "KVS_ERR_WORKSPACE"}
+
+MODE_LSE = 1
+MODE_RDKV_WT = 2
+MODE_KVZIP = 4
+MODE_KVZIP_PLUS = 8
+
+WIDTHS_ALL = (1 << 2) | (1 << 4) | (1 << 8) | (1 << 16)
+WIDTHS_KEEP_OR_EVICT = 1 << 16
+STREAM_WIDTHS = (2, 4, 8, 16)
+
+# every exported symbol the header declares, with its ctypes signature
+SIGNATURES = {
+    "kvs_status_string": (c_char_p, [c_int]),
+    "kvs_version": (c_int, []),
+    "kvs_get_device_error": (c_int, [c_void_p]),
+    "kvs_score_workspace_size": (c_size_t, [c_int64] * 7 + [c_uint32]),
+    "kvs_score_attention": (c_int, [c_void_p] * 5 + [c_int64] * 7 + [c_uint32] + [c_void_p] * 4 + [c_size_t, c_void_p]),
+    "kvs_score_plan_info": (c_int, [c_int64] * 7 + [c_uint32, POINTER(c_int64)]),
+    "kvs_channel_weights_workspace_size": (c_size_t, [c_int64] * 5),
+    "kvs_channel_weights": (c_int, [c_void_p, c_void_p] + [c_int64] * 5 + [c_void_p, c_void_p, c_size_t, c_void_p]),
+    "kvs_unit_rms_workspace_size": (c_size_t, [c_int64] * 3 + [c_int]),
+    "kvs_unit_rms": (c_int, [c_void_p] + [c_int64] * 3 + [c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "kvs_allocate_workspace_size": (c_size_t, [c_int64]),
+    "kvs_allocate_bits": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_uint32, c_void_p, c_void_p, c_size_t,
+                                  c_void_p]),
+    "kvs_pack_capacity": (c_int, [c_int64] * 3 + [c_int, c_int64, POINTER(c_int64), POINTER(c_int64)]),
+    "kvs_pack_workspace_size": (c_size_t, [c_int64] * 3 + [c_int]),
+    "kvs_quantize_pack": (c_int, [c_void_p] + [c_int64] * 3 + [c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                               c_size_t, c_void_p]),
+    "kvs_dequantize": (c_int, [c_void_p] + [c_int64] * 3 + [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                                            c_void_p]),
+}
+
+
+class KvsError(RuntimeError):
+    pass
+
+
+class StreamSetC(ctypes.Structure):
+    _fields_ = [("codes", c_void_p * 4), ("scales", c_void_p * 4), ("unit_ids", c_void_p * 4),
+                ("group_offsets", c_void_p * 4), ("cap_units", c_int64 * 4), ("cap_groups", c_int64 * 4),
+                ("counts", c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (raises when it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise KvsError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != KVS_OK:
+        raise KvsError(f"{what}: {STATUS.get(rc, rc)}")
+
+
+def _ptr(t):
+    return None if t is None else c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return c_void_p(s.cuda_stream)
+
+
+def _bf16(t, name):
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise KvsError(f"{name} must be a contiguous bf16 CUDA tensor")
+    return t
+
+
+class Workspace:
+    """A growable device scratch buffer (one per caller)."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes: int, device):
+        nbytes = max(int(nbytes), 256)
+        if self.buf is None or self.buf.numel() < nbytes or self.buf.device != device:
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        return self.buf
+
+
+_default_ws = {}
+
+
+def _ws(ws, key, nbytes, device):
+    if ws is None:
+        ws = _default_ws.setdefault(key, Workspace())
+    return ws.get(nbytes, device)
+
+
+def device_error(stream=None) -> int:
+    """Reads and clears the library's device error word (synchronises the stream)."""
+    return lib().kvs_get_device_error(_stream(stream))
+
+
+def score_attention(Q, K, *, q_pos0=None, mode=MODE_LSE | MODE_RDKV_WT, V=None, h=None, W_O=None,
+                    out=None, ws=None, stream=None):
+    """lse [Hq,W], w_t [Hkv,N], s_plus [Hkv,N] (per mode) from bf16 Q [Hq,W,d], K [Hkv,N,d]."""
+    _bf16(Q, "Q"), _bf16(K, "K")
+    Hq, W, d = Q.shape
+    Hkv, N, _ = K.shape
+    q_pos0 = N - W if q_pos0 is None else q_pos0
+    D = 0
+    if mode & MODE_KVZIP_PLUS:
+        _bf16(V, "V"), _bf16(h, "h"), _bf16(W_O, "W_O")
+        D = h.shape[1]
+    dev = Q.device
+    out = {} if out is None else out
+    lse = out.get("lse")
+    if lse is None:
+        lse = out["lse"] = torch.empty(Hq, W, dtype=torch.float32, device=dev)
+    w_t = s_plus = None
+    if mode & MODE_RDKV_WT:
+        w_t = out.get("w_t")
+        if w_t is None:
+            w_t = out["w_t"] = torch.empty(Hkv, N, dtype=torch.float32, device=dev)
+    if mode & (MODE_KVZIP | MODE_KVZIP_PLUS):
+        s_plus = out.get("s_plus")
+        if s_plus is None:
+            s_plus = out["s_plus"] = torch.empty(Hkv, N, dtype=torch.float32, device=dev)
+    L = lib()
+    nbytes = L.kvs_score_workspace_size(Hq, Hkv, W, N, d, D, q_pos0, mode)
+    if nbytes == 0:
+        raise KvsError("kvs_score_workspace_size: unsupported shape or mode")
+    buf = _ws(ws, "score", nbytes, dev)
+    _check(L.kvs_score_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(h), _ptr(W_O), Hq, Hkv, W, N, d, D, q_pos0,
+                                 mode, _ptr(lse), _ptr(w_t), _ptr(s_plus), _ptr(buf), buf.numel(),
+                                 _stream(stream)), "kvs_score_attention")
+    return out
+
+
+def score_plan_info(Hq, Hkv, W, N, d, D=0, q_pos0=None, mode=MODE_LSE | MODE_RDKV_WT):
+    """(kt_chunk, pass-1 splits, qt_chunk, pass-2 splits, kernels launched) of kvs_score_attention."""
+    info = (c_int64 * 5)()
+    q_pos0 = N - W if q_pos0 is None else q_pos0
+    _check(lib().kvs_score_plan_info(Hq, Hkv, W, N, d, D, q_pos0, mode, info), "kvs_score_plan_info")
+    return tuple(info)
+
+
+def channel_weights(Q, K, *, out=None, ws=None, stream=None):
+    _bf16(Q, "Q"), _bf16(K, "K")
+    Hq, W, d = Q.shape
+    Hkv, N, _ = K.shape
+    w_c = out if out is not None else torch.empty(Hkv, d, dtype=torch.float32, device=Q.device)
+    L = lib()
+    buf = _ws(ws, "cw", L.kvs_channel_weights_workspace_size(Hq, Hkv, W, N, d), Q.device)
+    _check(L.kvs_channel_weights(_ptr(Q), _ptr(K), Hq, Hkv, W, N, d, _ptr(w_c), _ptr(buf), buf.numel(),
+                                 _stream(stream)), "kvs_channel_weights")
+    return w_c
+
+
+def unit_rms(X, axis, keep_bits=None, *, out=None, ws=None, stream=None):
+    _bf16(X, "X")
+    Hkv, N, d = X.shape
+    shape = (Hkv, N) if axis == 0 else (Hkv, d)
+    sigma = out if out is not None else torch.empty(shape, dtype=torch.float32, device=X.device)
+    L = lib()
+    buf = _ws(ws, "rms", L.kvs_unit_rms_workspace_size(Hkv, N, d, axis), X.device)
+    _check(L.kvs_unit_rms(_ptr(X), Hkv, N, d, axis, _ptr(keep_bits), _ptr(sigma), _ptr(buf), buf.numel(),
+                          _stream(stream)), "kvs_unit_rms")
+    return sigma
+
+
+def allocate_bits(w, sigma, budget_bits, width_mask=WIDTHS_ALL, *, out=None, ws=None, stream=None):
+    w = w.reshape(-1)
+    sigma = sigma.reshape(-1)
+    if w.dtype != torch.float32 or sigma.dtype != torch.float32 or w.numel() != sigma.numel():
+        raise KvsError("w and sigma must be float32 of equal length")
+    U = w.numel()
+    bits = out if out is not None else torch.empty(U, dtype=torch.uint8, device=w.device)
+    L = lib()
+    buf = _ws(ws, "alloc", L.kvs_allocate_workspace_size(U), w.device)
+    _check(L.kvs_allocate_bits(_ptr(w), _ptr(sigma), U, int(budget_bits), width_mask, _ptr(bits), _ptr(buf),
+                               buf.numel(), _stream(stream)), "kvs_allocate_bits")
+    return bits
+
+
+class Streams:
+    """Device buffers of one width-grouped stream set (see kvs_stream_set)."""
+
+    def __init__(self, Hkv, N, d, axis, budget_bits, device):
+        cu = (c_int64 * 4)()
+        cg = (c_int64 * 4)()
+        _check(lib().kvs_pack_capacity(Hkv, N, d, axis, int(budget_bits), cu, cg), "kvs_pack_capacity")
+        self.shape, self.axis = (Hkv, N, d), axis
+        self.cap_units, self.cap_groups = list(cu), list(cg)
+        self.codes, self.scales, self.ids, self.goff = [], [], [], []
+        for i, wd in enumerate(STREAM_WIDTHS):
+            self.codes.append(torch.empty(max(1, cg[i] * 8 * wd), dtype=torch.uint8, device=device))
+            self.scales.append(torch.empty(max(1, cg[i]), dtype=torch.int16, device=device))
+            self.ids.append(torch.empty(max(1, cu[i]), dtype=torch.int32, device=device))
+            self.goff.append(torch.empty(max(1, cu[i]), dtype=torch.int64, device=device))
+        self.counts = torch.zeros(8, dtype=torch.int64, device=device)
+        c = StreamSetC()
+        for i in range(4):
+            c.codes[i] = self.codes[i].data_ptr()
+            c.scales[i] = self.scales[i].data_ptr()
+            c.unit_ids[i] = self.ids[i].data_ptr()
+            c.group_offsets[i] = self.goff[i].data_ptr()
+            c.cap_units[i] = cu[i]
+            c.cap_groups[i] = cg[i]
+        c.counts = self.counts.data_ptr()
+        self.c = c
+
+    def host_view(self):
+        """Copy the used part of every stream to host numpy arrays (width -> dict)."""
+        counts = self.counts.cpu().tolist()
+        out = {}
+        for i, wd in enumerate(STREAM_WIDTHS):
+            nu, ng = counts[i], counts[4 + i]
+            out[wd] = {
+                "ids": self.ids[i][:nu].cpu().numpy(),
+                "group_offsets": self.goff[i][:nu].cpu().numpy(),
+                "n_groups": ng,
+                "codes": self.codes[i][:ng * 8 * wd].cpu().numpy(),
+                "scales": self.scales[i][:ng].cpu().numpy().view("uint16") if wd != 16 else None,
+            }
+        return out
+
+
+def quantize_pack(X, axis, bits, keep_bits, streams: Streams, *, ws=None, stream=None):
+    _bf16(X, "X")
+    Hkv, N, d = X.shape
+    L = lib()
+    buf = _ws(ws, "pack%d" % axis, L.kvs_pack_workspace_size(Hkv, N, d, axis), X.device)
+    _check(L.kvs_quantize_pack(_ptr(X), Hkv, N, d, axis, _ptr(bits), _ptr(keep_bits), ctypes.byref(streams.c),
+                               _ptr(buf), buf.numel(), _stream(stream)), "kvs_quantize_pack")
+    return streams
+
+
+def dequantize(streams: Streams, bits, keep_bits, *, out=None, ws=None, stream=None):
+    Hkv, N, d = streams.shape
+    axis = streams.axis
+    dev = streams.counts.device
+    y = out if out is not None else torch.empty(Hkv, N, d, dtype=torch.float32, device=dev)
+    L = lib()
+    buf = _ws(ws, "deq%d" % axis, L.kvs_pack_workspace_size(Hkv, N, d, axis), dev)
+    _check(L.kvs_dequantize(ctypes.byref(streams.c), Hkv, N, d, axis, _ptr(bits), _ptr(keep_bits), _ptr(y),
+                            _ptr(buf), buf.numel(), _stream(stream)), "kvs_dequantize")
+    return y

@@ -1,0 +1,299 @@
+// Lagrangian (reverse water-filling) multiple-choice-knapsack bit allocation.
+//   min sum_u w_u sigma_u 2^-b_u  s.t.  sum_u b_u <= B,  b_u in a width set
+//   [RDKV §2.1 objective; §2.2 discrete widths {0,2,4,8,16}, Lagrangian relaxation]
+//
+// D_u(b) = key_u 2^-b is strictly convex in b, so the Lagrangian argmin of
+// D_u(b) + lambda b climbs the widths in order: unit u leaves width b_k when
+// lambda drops below theta_{u,k} = c_k key_u (c_k = chord slope of 2^-b,
+// key_u = w_u sigma_u exactly in fp64).  Sorting every "upgrade item" (u, k)
+// by theta descending (ties: u, then k ascending) and taking the longest
+// prefix that fits B is the Lagrangian solution at the critical multiplier
+// lambda* = theta of the first item that does not fit.  A budget-fix scan then
+// keeps taking later items that still fit and whose previous step was taken.
+//
+// B300 design: one cooperative launch, all blocks resident, grid barriers with
+// bounded waits.  lambda* is found exactly by an 8-pass radix select on the
+// fp64 bit patterns of theta (positive doubles order like their bit patterns),
+// each pass a cost-weighted 256-bin histogram; every block then decides the
+// digit redundantly so one barrier per pass suffices.  Ties at lambda* are
+// resolved in unit order by a grid-wide scan; the fix scan is an arg-max
+// (theta, then lowest unit) over each unit's next upgrade, repeated while the
+// leftover budget buys something (at most max_step/min_step rounds).
+#pragma once
+
+#include "common.cuh"
+
+namespace kvs {
+
+constexpr int kAllocThreads = 256;
+constexpr int kMaxFixRounds = 16;
+
+struct AllocHeader {
+  GridSync sync;
+  unsigned long long total;  // cost of every positive upgrade item
+  int bad;                   // a weight or sigma was negative or not finite
+  int pad_;
+  unsigned long long hist[8][256];
+  unsigned long long first_cut;  // B-side cost before the first item that did not fit
+};
+
+struct FixCand {
+  unsigned long long theta;  // fp64 bit pattern, 0 = no candidate
+  long long u;
+  int cost;
+  int pad_;
+};
+
+struct AllocParams {
+  const float* w;
+  const float* sigma;
+  uint8_t* bits;
+  long long U;
+  unsigned long long B;
+  int K;            // upgrade steps = allowed widths - 1
+  int min_cost;     // smallest step
+  double c[4];      // chord slopes, descending
+  int cost[4];      // step sizes b_{k+1} - b_k
+  int width[5];     // allowed widths, ascending, width[0] = 0
+  AllocHeader* hdr;
+  unsigned long long* tie_block;  // [gridDim.x]
+  FixCand* cand;                  // [kMaxFixRounds][gridDim.x]
+};
+
+__device__ __forceinline__ unsigned long long ld_vol(const unsigned long long* p) {
+  return *reinterpret_cast<const volatile unsigned long long*>(p);
+}
+
+template <class T>
+__device__ __forceinline__ T block_sum(T v, T* sbuf) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) sbuf[warp] = v;
+  __syncthreads();
+  T s = 0;
+  for (int i = 0; i < (kAllocThreads >> 5); ++i) s += sbuf[i];
+  return s;
+}
+
+// exclusive scan of v over the block in thread order; returns the block total in *total
+__device__ __forceinline__ unsigned long long block_exscan(unsigned long long v, unsigned long long* sbuf,
+                                                           unsigned long long* total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) sbuf[warp] = x;
+  __syncthreads();
+  unsigned long long before = 0, tot = 0;
+  for (int i = 0; i < (kAllocThreads >> 5); ++i) {
+    if (i < warp) before += sbuf[i];
+    tot += sbuf[i];
+  }
+  *total = tot;
+  return before + x - v;
+}
+
+__device__ __forceinline__ bool cand_better(const FixCand& a, const FixCand& b) {  // a before b in item order
+  if (a.theta != b.theta) return a.theta > b.theta;
+  return a.u < b.u;
+}
+
+__global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocParams p) {
+  __shared__ unsigned long long s_hist[256];
+  __shared__ unsigned long long s_red[kAllocThreads / 32];
+  __shared__ unsigned long long s_sel_above;
+  __shared__ int s_sel;
+  __shared__ int s_lvl_of_width[17];
+  __shared__ FixCand s_cand[kAllocThreads / 32];
+  __shared__ FixCand s_best;
+  __shared__ int s_flag;
+
+  const int nb = gridDim.x, b = blockIdx.x, tid = threadIdx.x;
+  const long long per = (p.U + nb - 1) / nb;
+  const long long u_begin = static_cast<long long>(b) * per;
+  const long long u_end = min(p.U, u_begin + per);
+  AllocHeader* H = p.hdr;
+
+  if (tid < 17) s_lvl_of_width[tid] = -1;
+  __syncthreads();
+  if (tid <= p.K) s_lvl_of_width[p.width[tid]] = tid;
+
+  // ---- phase 0: validate, total cost of positive items -------------------
+  unsigned long long my_total = 0;
+  int my_bad = 0;
+  const int full_cost = p.width[p.K];
+  for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) {
+    const float wf = p.w[u], sf = p.sigma[u];
+    if (!(isfinite(wf) && isfinite(sf) && wf >= 0.f && sf >= 0.f)) my_bad = 1;
+    const double key = static_cast<double>(wf) * static_cast<double>(sf);
+    if (key > 0.0) my_total += static_cast<unsigned long long>(full_cost);
+  }
+  const unsigned long long blk_total = block_sum(my_total, s_red);
+  const int blk_bad = __syncthreads_or(my_bad);
+  if (tid == 0) {
+    if (blk_total) atomicAdd(&H->total, blk_total);
+    if (blk_bad) atomicOr(&H->bad, 1);
+  }
+  if (!grid_barrier(&H->sync, nb)) return;
+  const unsigned long long total = ld_vol(&H->total);
+  const int bad = *reinterpret_cast<volatile int*>(&H->bad);
+  if (bad) {
+    if (b == 0 && tid == 0) record_error(KVS_ERR_RANGE);
+    for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) p.bits[u] = 0;
+    return;
+  }
+  if (total <= p.B) {  // every upgrade fits
+    for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) {
+      const double key = static_cast<double>(p.w[u]) * static_cast<double>(p.sigma[u]);
+      p.bits[u] = key > 0.0 ? static_cast<uint8_t>(full_cost) : 0;
+    }
+    return;
+  }
+
+  // ---- phase 1: radix select of lambda* on theta bit patterns ------------
+  unsigned long long prefix = 0, pmask = 0, above = 0;
+  for (int pass = 0; pass < 8; ++pass) {
+    const int shift = 56 - 8 * pass;
+    s_hist[tid] = 0;  // kAllocThreads == 256 bins
+    __syncthreads();
+    for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) {
+      const double key = static_cast<double>(p.w[u]) * static_cast<double>(p.sigma[u]);
+      if (key <= 0.0) continue;
+      for (int k = 0; k < p.K; ++k) {
+        const unsigned long long v = static_cast<unsigned long long>(__double_as_longlong(p.c[k] * key));
+        if ((v & pmask) == prefix) atomicAdd(&s_hist[(v >> shift) & 255ull], static_cast<unsigned long long>(p.cost[k]));
+      }
+    }
+    __syncthreads();
+    if (s_hist[tid]) atomicAdd(&H->hist[pass][tid], s_hist[tid]);
+    if (!grid_barrier(&H->sync, nb)) return;
+    if (tid == 0) {
+      unsigned long long a = above;
+      int sel = 0;
+      for (int dgt = 255; dgt >= 0; --dgt) {
+        const unsigned long long h = ld_vol(&H->hist[pass][dgt]);
+        if (a + h > p.B) {
+          sel = dgt;
+          break;
+        }
+        a += h;
+      }
+      s_sel = sel;
+      s_sel_above = a;
+    }
+    __syncthreads();
+    prefix |= static_cast<unsigned long long>(s_sel) << shift;
+    pmask |= 255ull << shift;
+    above = s_sel_above;
+    __syncthreads();
+  }
+  const unsigned long long lam = prefix;  // theta bits of the first item that does not fit
+
+  // ---- phase 2: prefix levels; ties at lambda* resolved in unit order -----
+  unsigned long long my_tie = 0;
+  for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) {
+    const double key = static_cast<double>(p.w[u]) * static_cast<double>(p.sigma[u]);
+    if (key <= 0.0) continue;
+    for (int k = 0; k < p.K; ++k)
+      if (static_cast<unsigned long long>(__double_as_longlong(p.c[k] * key)) == lam) my_tie += p.cost[k];
+  }
+  const unsigned long long blk_tie = block_sum(my_tie, s_red);
+  if (tid == 0) p.tie_block[b] = blk_tie;
+  if (!grid_barrier(&H->sync, nb)) return;
+  unsigned long long carry = above;
+  if (tid == 0) {
+    unsigned long long e = 0;
+    for (int i = 0; i < b; ++i) e += ld_vol(&p.tie_block[i]);
+    s_sel_above = e;
+  }
+  __syncthreads();
+  carry += s_sel_above;
+  for (long long base = u_begin; base < u_end; base += kAllocThreads) {
+    const long long u = base + tid;
+    int lvl = 0;
+    unsigned long long tie = 0;
+    if (u < u_end) {
+      const double key = static_cast<double>(p.w[u]) * static_cast<double>(p.sigma[u]);
+      if (key > 0.0) {
+        for (int k = 0; k < p.K; ++k) {
+          const unsigned long long v = static_cast<unsigned long long>(__double_as_longlong(p.c[k] * key));
+          if (v > lam) ++lvl;
+          else if (v == lam) tie = p.cost[k];
+        }
+      }
+    }
+    unsigned long long chunk_total;
+    const unsigned long long ex = block_exscan(tie, s_red, &chunk_total);
+    if (u < u_end) {
+      const unsigned long long cum = carry + ex + tie;  // cost through this item
+      if (tie) {
+        if (cum <= p.B) ++lvl;
+        else if (cum - tie <= p.B) H->first_cut = cum - tie;  // exactly one item: the first misfit
+      }
+      p.bits[u] = static_cast<uint8_t>(p.width[lvl]);
+    }
+    carry += chunk_total;
+  }
+  if (!grid_barrier(&H->sync, nb)) return;
+
+  // ---- phase 3: budget-fix rounds ------------------------------------------
+  long long R = static_cast<long long>(p.B) - static_cast<long long>(ld_vol(&H->first_cut));
+  for (int it = 0; it < kMaxFixRounds; ++it) {
+    if (R < p.min_cost) break;
+    FixCand best = {0ull, 0ll, 0, 0};
+    for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) {
+      const int lvl = s_lvl_of_width[p.bits[u]];
+      if (lvl < 0 || lvl >= p.K || p.cost[lvl] > R) continue;
+      const double key = static_cast<double>(p.w[u]) * static_cast<double>(p.sigma[u]);
+      const double th = p.c[lvl] * key;
+      if (!(th > 0.0)) continue;
+      FixCand c = {static_cast<unsigned long long>(__double_as_longlong(th)), u, p.cost[lvl], 0};
+      if (best.theta == 0ull || cand_better(c, best)) best = c;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      FixCand o_c;
+      o_c.theta = __shfl_xor_sync(0xFFFFFFFFu, best.theta, o);
+      o_c.u = __shfl_xor_sync(0xFFFFFFFFu, best.u, o);
+      o_c.cost = __shfl_xor_sync(0xFFFFFFFFu, best.cost, o);
+      o_c.pad_ = 0;
+      if (o_c.theta != 0ull && (best.theta == 0ull || cand_better(o_c, best))) best = o_c;
+    }
+    if ((tid & 31) == 0) s_cand[tid >> 5] = best;
+    __syncthreads();
+    if (tid == 0) {
+      FixCand bb = s_cand[0];
+      for (int i = 1; i < (kAllocThreads >> 5); ++i)
+        if (s_cand[i].theta != 0ull && (bb.theta == 0ull || cand_better(s_cand[i], bb))) bb = s_cand[i];
+      p.cand[it * nb + b] = bb;
+    }
+    if (!grid_barrier(&H->sync, nb)) return;
+    if (tid == 0) {
+      FixCand bb = {0ull, 0ll, 0, 0};
+      for (int i = 0; i < nb; ++i) {
+        const volatile FixCand* vc = &p.cand[it * nb + i];
+        FixCand c2 = {vc->theta, vc->u, vc->cost, 0};
+        if (c2.theta != 0ull && (bb.theta == 0ull || cand_better(c2, bb))) bb = c2;
+      }
+      s_best = bb;
+      s_flag = bb.theta != 0ull;
+    }
+    __syncthreads();
+    if (!s_flag) break;
+    const long long ub = s_best.u;
+    if (ub >= u_begin && ub < u_end && tid == static_cast<int>((ub - u_begin) % kAllocThreads)) {
+      const int lvl = s_lvl_of_width[p.bits[ub]];
+      p.bits[ub] = static_cast<uint8_t>(p.width[lvl + 1]);
+    }
+    R -= s_best.cost;
+    __syncthreads();
+  }
+}
+
+}  // namespace kvs

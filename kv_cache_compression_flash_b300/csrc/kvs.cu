@@ -1,0 +1,614 @@
+// libkvs.so: host side of the C ABI declared in include/kvs.h.  Validates
+// arguments, carves the caller's workspace, encodes TMA tensor maps and
+// enqueues the kernels of score.cuh, norms.cuh, alloc.cuh and pack.cuh on the
+// caller's stream.  One translation unit, so every kernel shares the device
+// error word.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "alloc.cuh"
+#include "common.cuh"
+#include "norms.cuh"
+#include "pack.cuh"
+#include "score.cuh"
+
+using namespace kvs;
+
+namespace {
+
+constexpr int kVersion = 100;
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+// ---- TMA tensor maps ---------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 map over [dim2][dim1][dim0] (dim0 contiguous), 128-byte swizzle,
+// out-of-range elements read as zero.
+int make_map_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2, uint32_t box0,
+                uint32_t box1, uint32_t box2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return KVS_ERR_CUDA;
+  const cuuint64_t gdim[3] = {dim0, dim1, dim2};
+  const cuuint64_t gstride[2] = {dim0 * 2, dim0 * dim1 * 2};
+  const cuuint32_t box[3] = {box0, box1, box2};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box,
+                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KVS_OK : KVS_ERR_CUDA;
+}
+
+// ---- scoring plan -------------------------------------------------------------
+constexpr int kGramSlices = 8;
+
+struct ScorePlan {
+  ScoreGeom geo;
+  int d, D;
+  int kt_chunk, n_split1;
+  int qt_chunk, n_split2;
+  int gram_slice_len;
+  bool want_wt, want_max, want_plus;
+};
+
+int validate_shape(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t q_pos0) {
+  if (Hq <= 0 || Hkv <= 0 || W <= 0 || N <= 0 || d <= 0 || q_pos0 < 0) return KVS_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || q_pos0 + W > N) return KVS_ERR_INVALID_ARG;
+  const int64_t G = Hq / Hkv;
+  if (d != 64 && d != 128) return KVS_ERR_UNSUPPORTED;
+  if (!(G <= 4 || G % 4 == 0)) return KVS_ERR_UNSUPPORTED;
+  if (N >= (1ll << 31) || Hkv * N >= (1ll << 31) || Hq * W >= (1ll << 31) || Hq >= (1 << 16))
+    return KVS_ERR_UNSUPPORTED;
+  return KVS_OK;
+}
+
+int plan_score(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t D, int64_t q_pos0,
+               uint32_t mode, ScorePlan* pl) {
+  int st = validate_shape(Hq, Hkv, W, N, d, q_pos0);
+  if (st) return st;
+  if ((mode & ~(KVS_MODE_LSE | KVS_MODE_RDKV_WT | KVS_MODE_KVZIP | KVS_MODE_KVZIP_PLUS)) != 0)
+    return KVS_ERR_INVALID_ARG;
+  if ((mode & KVS_MODE_KVZIP) && (mode & KVS_MODE_KVZIP_PLUS)) return KVS_ERR_INVALID_ARG;
+  if ((mode & KVS_MODE_KVZIP_PLUS) && (D <= 0 || D % 8 != 0)) return KVS_ERR_INVALID_ARG;
+  ScoreGeom& g = pl->geo;
+  g.Hq = static_cast<int>(Hq);
+  g.Hkv = static_cast<int>(Hkv);
+  g.G = static_cast<int>(Hq / Hkv);
+  g.Gt = g.G <= 4 ? g.G : 4;
+  g.P = 128 / g.Gt;
+  g.W = static_cast<int>(W);
+  g.N = static_cast<int>(N);
+  g.q_pos0 = static_cast<int>(q_pos0);
+  g.n_hc = g.G / g.Gt;
+  g.n_pb = static_cast<int>(cdiv(W, g.P));
+  g.n_rt = g.Hkv * g.n_hc * g.n_pb;
+  g.n_kt = static_cast<int>(cdiv(N, 128));
+  g.c_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  pl->d = static_cast<int>(d);
+  pl->D = static_cast<int>(D);
+  pl->want_wt = (mode & KVS_MODE_RDKV_WT) != 0;
+  pl->want_plus = (mode & KVS_MODE_KVZIP_PLUS) != 0;
+  pl->want_max = (mode & (KVS_MODE_KVZIP | KVS_MODE_KVZIP_PLUS)) != 0;
+  const long long target = static_cast<long long>(sm_count()) * 2 * 4;
+  long long w1 = 0;
+  for (int pb = 0; pb < g.n_pb; ++pb) w1 += pb_nkt(g, pb);
+  w1 *= static_cast<long long>(g.Hkv) * g.n_hc;
+  pl->kt_chunk = static_cast<int>(std::max<long long>(4, cdiv(w1, target)));
+  pl->n_split1 = static_cast<int>(cdiv(pb_nkt(g, g.n_pb - 1), pl->kt_chunk));
+  long long w2 = 0;
+  for (int kt = 0; kt < g.n_kt; ++kt) w2 += kt_nvis(g, kt);
+  w2 *= static_cast<long long>(g.Hkv) * g.n_hc;
+  pl->qt_chunk = static_cast<int>(std::max<long long>(4, cdiv(w2, target)));
+  pl->n_split2 = static_cast<int>(cdiv(static_cast<long long>(kt_nvis(g, 0)) * g.n_hc, pl->qt_chunk));
+  if (pl->n_split2 < 1) pl->n_split2 = 1;
+  pl->gram_slice_len = static_cast<int>(cdiv(cdiv(std::max<int64_t>(D, 1), kGramSlices), 32) * 32);
+  return KVS_OK;
+}
+
+struct ScoreWs {
+  float2* part1;
+  float* b_plain;
+  float* b_scaled;
+  float* part_sum;
+  float* part_max;
+  float* hn;
+  float* gram;
+  float* vn;
+};
+
+size_t carve_score(const ScorePlan& pl, void* base, size_t cap, ScoreWs* w) {
+  WsCarver c{static_cast<char*>(base), 0, cap};
+  const ScoreGeom& g = pl.geo;
+  w->part1 = c.take<float2>(static_cast<size_t>(g.n_rt) * pl.n_split1 * 128);
+  w->b_plain = (pl.want_wt || (pl.want_max && !pl.want_plus)) ? c.take<float>(static_cast<size_t>(g.n_rt) * 128)
+                                                              : nullptr;
+  w->b_scaled = pl.want_plus ? c.take<float>(static_cast<size_t>(g.n_rt) * 128) : nullptr;
+  const size_t kn = static_cast<size_t>(g.Hkv) * g.N;
+  w->part_sum = (pl.want_wt && pl.n_split2 > 1) ? c.take<float>(kn * pl.n_split2) : nullptr;
+  w->part_max = (pl.want_max && pl.n_split2 > 1) ? c.take<float>(kn * pl.n_split2) : nullptr;
+  w->hn = pl.want_plus ? c.take<float>(g.W) : nullptr;
+  w->gram = pl.want_plus ? c.take<float>(static_cast<size_t>(kGramSlices) * g.Hq * pl.d * pl.d) : nullptr;
+  w->vn = pl.want_plus ? c.take<float>(static_cast<size_t>(g.Hq) * g.N) : nullptr;
+  return c.used;
+}
+
+template <class K>
+cudaError_t allow_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
+constexpr int kStages = 2;
+// Each scoring CTA holds 256 TMEM columns; 512 exist per SM.  Asking for at
+// least this much shared memory keeps residency at two CTAs per SM.
+constexpr size_t kScoreMinSmem = 80 * 1024;
+
+template <int DH>
+int launch_lse(const ScorePlan& pl, const CUtensorMap& mq, const CUtensorMap& mk, float2* part,
+               cudaStream_t st) {
+  auto kern = lse_pass_kernel<DH, kStages>;
+  const size_t smem = std::max(sizeof(LseSmem<DH, kStages>) + 1024, kScoreMinSmem);
+  KVS_CUDA_TRY(allow_smem(kern, smem));
+  dim3 grid(pl.n_split1, pl.geo.n_rt);
+  kern<<<grid, kScoreThreads, smem, st>>>(mq, mk, pl.geo, pl.kt_chunk, pl.n_split1, part);
+  return KVS_OK;
+}
+
+template <int DH, int GT, bool MAXM>
+int launch_col_gt(const ScorePlan& pl, const CUtensorMap& mq, const CUtensorMap& mk, const float* bvals,
+                  const float* vn, float* out, float* part, cudaStream_t st) {
+  auto kern = colreduce_pass_kernel<DH, kStages, GT, MAXM>;
+  const size_t smem = std::max(sizeof(ColSmem<DH, kStages>) + 1024, kScoreMinSmem);
+  KVS_CUDA_TRY(allow_smem(kern, smem));
+  dim3 grid(pl.n_split2, pl.geo.n_kt * pl.geo.Hkv);
+  kern<<<grid, kScoreThreads, smem, st>>>(mq, mk, pl.geo, pl.qt_chunk, pl.n_split2, bvals, vn, out, part);
+  if (pl.n_split2 > 1) {
+    const int total = pl.geo.Hkv * pl.geo.N;
+    colreduce_finalize_kernel<MAXM><<<static_cast<int>(cdiv(total, 256)), 256, 0, st>>>(
+        pl.geo, pl.qt_chunk, pl.n_split2, part, out);
+  }
+  return KVS_OK;
+}
+
+template <int DH, bool MAXM>
+int launch_col(const ScorePlan& pl, const CUtensorMap& mq, const CUtensorMap& mk, const float* bvals,
+               const float* vn, float* out, float* part, cudaStream_t st) {
+  switch (pl.geo.Gt) {
+    case 1: return launch_col_gt<DH, 1, MAXM>(pl, mq, mk, bvals, vn, out, part, st);
+    case 2: return launch_col_gt<DH, 2, MAXM>(pl, mq, mk, bvals, vn, out, part, st);
+    case 4: return launch_col_gt<DH, 4, MAXM>(pl, mq, mk, bvals, vn, out, part, st);
+    default: return KVS_ERR_UNSUPPORTED;
+  }
+}
+
+template <int DH>
+int score_dh(const ScorePlan& pl, const uint16_t* Q, const uint16_t* K, const uint16_t* V, const uint16_t* h,
+             const uint16_t* WO, float* lse, float* w_t, float* s_plus, const ScoreWs& w, cudaStream_t st) {
+  const ScoreGeom& g = pl.geo;
+  CUtensorMap mq, mk;
+  int rc = make_map_3d(&mq, Q, DH, g.W, g.Hq, 64, g.P, g.Gt);
+  if (rc) return rc;
+  rc = make_map_3d(&mk, K, DH, g.N, g.Hkv, 64, 128, 1);
+  if (rc) return rc;
+  if (pl.want_plus) {
+    row_norm_kernel<<<static_cast<int>(cdiv(g.W, 8)), 256, 0, st>>>(h, g.W, pl.D, w.hn);
+    gram_kernel<DH><<<dim3(kGramSlices, g.Hq, DH / 64), 256, 0, st>>>(WO, pl.D, g.Hq, pl.gram_slice_len, w.gram);
+    const size_t vsmem = (static_cast<size_t>(DH) * DH + static_cast<size_t>(DH) * 64) * sizeof(float);
+    KVS_CUDA_TRY(allow_smem(vnorm_kernel<DH>, vsmem));
+    vnorm_kernel<DH><<<dim3(static_cast<unsigned>(cdiv(g.N, 64)), g.Hq), 256, vsmem, st>>>(
+        V, w.gram, kGramSlices, g.Hq, g.G, g.N, w.vn);
+  }
+  rc = launch_lse<DH>(pl, mq, mk, w.part1, st);
+  if (rc) return rc;
+  lse_finalize_kernel<<<g.n_rt, 128, 0, st>>>(g, pl.kt_chunk, pl.n_split1, w.part1, w.hn, lse, w.b_plain,
+                                               w.b_scaled);
+  if (pl.want_wt) {
+    rc = launch_col<DH, false>(pl, mq, mk, w.b_plain, nullptr, w_t, w.part_sum, st);
+    if (rc) return rc;
+  }
+  if (pl.want_max) {
+    rc = launch_col<DH, true>(pl, mq, mk, pl.want_plus ? w.b_scaled : w.b_plain, pl.want_plus ? w.vn : nullptr,
+                              s_plus, w.part_max, st);
+    if (rc) return rc;
+  }
+  return KVS_OK;
+}
+
+// ---- allocation ---------------------------------------------------------------
+int alloc_blocks_max() { return sm_count() * 8; }
+
+size_t alloc_ws_bytes(int nb) {
+  WsCarver c{nullptr, 0, 0};
+  c.take<AllocHeader>(1);
+  c.take<unsigned long long>(nb);
+  c.take<FixCand>(static_cast<size_t>(kMaxFixRounds) * nb);
+  return c.used;
+}
+
+// ---- packing --------------------------------------------------------------------
+StreamPtrs to_ptrs(const kvs_stream_set* s, bool with_counts) {
+  StreamPtrs p;
+  for (int i = 0; i < 4; ++i) {
+    p.codes[i] = s->codes[i];
+    p.scales[i] = s->scales[i];
+    p.ids[i] = s->unit_ids[i];
+    p.goff[i] = s->group_offsets[i];
+    p.cap_units[i] = s->cap_units[i];
+    p.cap_groups[i] = s->cap_groups[i];
+  }
+  p.counts = with_counts ? s->counts : nullptr;
+  return p;
+}
+
+bool streams_ok(const kvs_stream_set* s) {
+  if (!s) return false;
+  for (int i = 0; i < 4; ++i) {
+    if (s->cap_units[i] < 0 || s->cap_groups[i] < 0) return false;
+    if (s->cap_units[i] > 0 && (!s->unit_ids[i] || !s->group_offsets[i])) return false;
+    if (s->cap_groups[i] > 0 && !s->codes[i]) return false;
+    if (s->cap_groups[i] > 0 && i < 3 && !s->scales[i]) return false;
+    if ((reinterpret_cast<uintptr_t>(s->codes[i]) & 7u) != 0) return false;
+  }
+  return true;
+}
+
+struct PackWs {
+  int* chunk;
+  int* rank;
+  int* kept;
+  int* n_kept;
+};
+
+size_t carve_pack(int64_t Hkv, int64_t N, int64_t d, int axis, void* base, size_t cap, PackWs* w) {
+  WsCarver c{static_cast<char*>(base), 0, cap};
+  if (axis == 0) {
+    const long long U = Hkv * N;
+    w->chunk = c.take<int>(static_cast<size_t>(cdiv(U, kPlanChunk)) * 4);
+    w->rank = c.take<int>(static_cast<size_t>(U));
+    w->kept = w->n_kept = nullptr;
+  } else {
+    w->chunk = nullptr;
+    w->rank = c.take<int>(static_cast<size_t>(Hkv * d));
+    w->kept = c.take<int>(static_cast<size_t>(Hkv * N));
+    w->n_kept = c.take<int>(static_cast<size_t>(Hkv));
+  }
+  return c.used;
+}
+
+int pack_shape_ok(int64_t Hkv, int64_t N, int64_t d, int axis) {
+  if (Hkv <= 0 || N <= 0 || d <= 0 || (axis != 0 && axis != 1)) return KVS_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return KVS_ERR_UNSUPPORTED;
+  if (Hkv * N >= (1ll << 31)) return KVS_ERR_UNSUPPORTED;
+  return KVS_OK;
+}
+
+template <int DH>
+int pack_dh(const uint16_t* X, int64_t Hkv, int64_t N, int axis, const uint8_t* bits, const uint8_t* keep,
+            const kvs_stream_set* s, const PackWs& w, cudaStream_t st, bool dequant, float* out) {
+  const int sms = sm_count();
+  if (axis == 0) {
+    const long long U = Hkv * N;
+    const int nchunk = static_cast<int>(cdiv(U, kPlanChunk));
+    const StreamPtrs sp = to_ptrs(s, !dequant);
+    plan_count_kernel<<<nchunk, kPlanThreads, 0, st>>>(bits, U, w.chunk);
+    plan_scan_kernel<<<1, 1024, 0, st>>>(w.chunk, nchunk, DH / 64, sp);
+    plan_rank_kernel<<<nchunk, kPlanThreads, 0, st>>>(bits, U, w.chunk, DH / 64, w.rank, sp, dequant ? 0 : 1);
+    const long long ngroups = U * (DH / 64);
+    const int blocks = static_cast<int>(std::min<long long>(cdiv(ngroups, 16), static_cast<long long>(sms) * 16));
+    if (dequant)
+      dequant_rows_kernel<DH><<<blocks, 256, 0, st>>>(sp, bits, w.rank, U, out);
+    else
+      pack_rows_kernel<DH><<<blocks, 256, 0, st>>>(X, bits, w.rank, U, sp);
+  } else {
+    const StreamPtrs sp = to_ptrs(s, !dequant);
+    kept_index_kernel<<<static_cast<int>(Hkv), 1024, 0, st>>>(keep, static_cast<int>(N), w.kept, w.n_kept);
+    plan_channels_kernel<<<1, kPlanThreads, 0, st>>>(bits, static_cast<int>(Hkv * DH), DH, w.n_kept, w.rank, sp,
+                                                     dequant ? 0 : 1);
+    const dim3 grid(static_cast<unsigned>(cdiv(N, 64)), static_cast<unsigned>(Hkv));
+    if (dequant) {
+      const long long rows = Hkv * N;
+      const int zb = static_cast<int>(std::min<long long>(cdiv(rows * (DH / 4), 256), static_cast<long long>(sms) * 16));
+      zero_dropped_rows_kernel<DH><<<zb, 256, 0, st>>>(keep, rows, out);
+      dequant_channels_kernel<DH><<<grid, 256, 0, st>>>(sp, static_cast<int>(N), bits, w.rank, w.kept, w.n_kept,
+                                                        out);
+    } else {
+      pack_channels_kernel<DH><<<grid, 256, 0, st>>>(X, static_cast<int>(N), bits, w.rank, w.kept, w.n_kept, sp);
+    }
+  }
+  return KVS_OK;
+}
+
+int pack_common(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis, const uint8_t* bits,
+                const uint8_t* keep, const kvs_stream_set* s, void* ws, size_t ws_bytes, void* stream,
+                bool dequant, float* out) {
+  int rc = pack_shape_ok(Hkv, N, d, axis);
+  if (rc) return rc;
+  if (!bits || !streams_ok(s) || (axis == 1 && !keep) || (dequant ? !out : !X)) return KVS_ERR_INVALID_ARG;
+  if (!dequant && !s->counts) return KVS_ERR_INVALID_ARG;
+  if (X && !aligned16(X)) return KVS_ERR_INVALID_ARG;
+  if (out && !aligned16(out)) return KVS_ERR_INVALID_ARG;
+  PackWs w;
+  if (carve_pack(Hkv, N, d, axis, ws, ws_bytes, &w) > ws_bytes || (!ws && ws_bytes == 0)) return KVS_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KVS_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  rc = d == 64 ? pack_dh<64>(X, Hkv, N, axis, bits, keep, s, w, st, dequant, out)
+               : pack_dh<128>(X, Hkv, N, axis, bits, keep, s, w, st, dequant, out);
+  if (rc) return rc;
+  KVS_CUDA_TRY(cudaGetLastError());
+  return KVS_OK;
+}
+
+}  // namespace
+
+// =============================================================================
+// C ABI
+// =============================================================================
+extern "C" {
+
+const char* kvs_status_string(int status) {
+  switch (status) {
+    case KVS_OK: return "KVS_OK";
+    case KVS_ERR_INVALID_ARG: return "KVS_ERR_INVALID_ARG";
+    case KVS_ERR_UNSUPPORTED: return "KVS_ERR_UNSUPPORTED";
+    case KVS_ERR_RANGE: return "KVS_ERR_RANGE";
+    case KVS_ERR_CUDA: return "KVS_ERR_CUDA";
+    case KVS_ERR_TIMEOUT: return "KVS_ERR_TIMEOUT";
+    case KVS_ERR_WORKSPACE: return "KVS_ERR_WORKSPACE";
+    default: return "KVS_ERR_UNKNOWN";
+  }
+}
+
+int kvs_version(void) { return kVersion; }
+
+int kvs_get_device_error(void* stream) {
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return KVS_ERR_CUDA;
+  }
+  int v = 0;
+  const int zero = 0;
+  KVS_CUDA_TRY(cudaMemcpyFromSymbol(&v, kvs::g_device_error, sizeof(int)));
+  KVS_CUDA_TRY(cudaMemcpyToSymbol(kvs::g_device_error, &zero, sizeof(int)));
+  return v;
+}
+
+size_t kvs_score_workspace_size(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t D,
+                                int64_t q_pos0, uint32_t mode) {
+  ScorePlan pl;
+  if (plan_score(Hq, Hkv, W, N, d, D, q_pos0, mode, &pl) != KVS_OK) return 0;
+  ScoreWs w;
+  return carve_score(pl, nullptr, 0, &w);
+}
+
+int kvs_score_plan_info(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t D, int64_t q_pos0,
+                        uint32_t mode, int64_t* info) {
+  if (!info) return KVS_ERR_INVALID_ARG;
+  ScorePlan pl;
+  const int rc = plan_score(Hq, Hkv, W, N, d, D, q_pos0, mode, &pl);
+  if (rc) return rc;
+  info[0] = pl.kt_chunk;
+  info[1] = pl.n_split1;
+  info[2] = pl.qt_chunk;
+  info[3] = pl.n_split2;
+  const int per_col = 1 + (pl.n_split2 > 1 ? 1 : 0);
+  info[4] = (pl.want_plus ? 3 : 0) + 2 + (pl.want_wt ? per_col : 0) + (pl.want_max ? per_col : 0);
+  return KVS_OK;
+}
+
+int kvs_score_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const uint16_t* h,
+                        const uint16_t* W_O, int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t D,
+                        int64_t q_pos0, uint32_t mode, float* lse, float* w_t, float* s_plus, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  ScorePlan pl;
+  int rc = plan_score(Hq, Hkv, W, N, d, D, q_pos0, mode, &pl);
+  if (rc) return rc;
+  if (!Q || !K || !lse) return KVS_ERR_INVALID_ARG;
+  if (pl.want_wt && !w_t) return KVS_ERR_INVALID_ARG;
+  if (pl.want_max && !s_plus) return KVS_ERR_INVALID_ARG;
+  if (pl.want_plus && (!V || !h || !W_O)) return KVS_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || (pl.want_plus && (!aligned16(V) || !aligned16(h))))
+    return KVS_ERR_INVALID_ARG;
+  ScoreWs w;
+  if (carve_score(pl, workspace, workspace_bytes, &w) > workspace_bytes || !workspace) return KVS_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KVS_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  rc = d == 64 ? score_dh<64>(pl, Q, K, V, h, W_O, lse, w_t, s_plus, w, st)
+               : score_dh<128>(pl, Q, K, V, h, W_O, lse, w_t, s_plus, w, st);
+  if (rc) return rc;
+  KVS_CUDA_TRY(cudaGetLastError());
+  return KVS_OK;
+}
+
+size_t kvs_channel_weights_workspace_size(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d) {
+  if (Hq <= 0 || Hkv <= 0 || W <= 0 || N <= 0 || Hq % Hkv) return 0;
+  WsCarver c{nullptr, 0, 0};
+  const long long nq = cdiv((Hq / Hkv) * W, kColChunkRows), nk = cdiv(N, kColChunkRows);
+  c.take<float>(static_cast<size_t>(Hkv * nq * d));
+  c.take<float>(static_cast<size_t>(Hkv * nk * d));
+  return c.used;
+}
+
+int kvs_channel_weights(const uint16_t* Q, const uint16_t* K, int64_t Hq, int64_t Hkv, int64_t W, int64_t N,
+                        int64_t d, float* w_c, void* workspace, size_t workspace_bytes, void* stream) {
+  if (Hq <= 0 || Hkv <= 0 || W <= 0 || N <= 0 || d <= 0 || Hq % Hkv) return KVS_ERR_INVALID_ARG;
+  if (!Q || !K || !w_c || !aligned16(Q) || !aligned16(K)) return KVS_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return KVS_ERR_UNSUPPORTED;
+  if (Hkv * N >= (1ll << 31) || Hq * W >= (1ll << 31)) return KVS_ERR_UNSUPPORTED;
+  const long long rq = (Hq / Hkv) * W;
+  const long long nq = cdiv(rq, kColChunkRows), nk = cdiv(N, kColChunkRows);
+  WsCarver c{static_cast<char*>(workspace), 0, workspace_bytes};
+  float* qp = c.take<float>(static_cast<size_t>(Hkv * nq * d));
+  float* kp = c.take<float>(static_cast<size_t>(Hkv * nk * d));
+  if (!c.ok() || !workspace) return KVS_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  const dim3 gq(static_cast<unsigned>(nq), static_cast<unsigned>(Hkv)), gk(static_cast<unsigned>(nk), static_cast<unsigned>(Hkv));
+  if (d == 64) {
+    colsumsq_kernel<64><<<gq, kNormThreads, 0, st>>>(Q, static_cast<int>(rq), nullptr, qp, nullptr);
+    colsumsq_kernel<64><<<gk, kNormThreads, 0, st>>>(K, static_cast<int>(N), nullptr, kp, nullptr);
+  } else {
+    colsumsq_kernel<128><<<gq, kNormThreads, 0, st>>>(Q, static_cast<int>(rq), nullptr, qp, nullptr);
+    colsumsq_kernel<128><<<gk, kNormThreads, 0, st>>>(K, static_cast<int>(N), nullptr, kp, nullptr);
+  }
+  const int n = static_cast<int>(Hkv * d);
+  channel_weight_finalize_kernel<<<static_cast<int>(cdiv(n, 256)), 256, 0, st>>>(
+      qp, static_cast<int>(nq), kp, static_cast<int>(nk), static_cast<int>(Hkv), static_cast<int>(d),
+      static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))), w_c);
+  KVS_CUDA_TRY(cudaGetLastError());
+  return KVS_OK;
+}
+
+size_t kvs_unit_rms_workspace_size(int64_t Hkv, int64_t N, int64_t d, int axis) {
+  if (axis == 0) return 0;
+  WsCarver c{nullptr, 0, 0};
+  const long long nk = cdiv(N, kColChunkRows);
+  c.take<float>(static_cast<size_t>(Hkv * nk * d));
+  c.take<int>(static_cast<size_t>(Hkv * nk));
+  return c.used;
+}
+
+int kvs_unit_rms(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis, const uint8_t* keep_bits,
+                 float* sigma, void* workspace, size_t workspace_bytes, void* stream) {
+  if (Hkv <= 0 || N <= 0 || d <= 0 || (axis != 0 && axis != 1)) return KVS_ERR_INVALID_ARG;
+  if (!X || !sigma || !aligned16(X)) return KVS_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return KVS_ERR_UNSUPPORTED;
+  if (Hkv * N >= (1ll << 31)) return KVS_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  const int sms = sm_count();
+  if (axis == 0) {
+    const long long rows = Hkv * N;
+    const int rpb = kNormThreads / (static_cast<int>(d) / 8);
+    const int blocks = static_cast<int>(std::min<long long>(cdiv(rows, rpb), static_cast<long long>(sms) * 16));
+    if (d == 64)
+      row_rms_kernel<64><<<blocks, kNormThreads, 0, st>>>(X, static_cast<int>(rows), sigma);
+    else
+      row_rms_kernel<128><<<blocks, kNormThreads, 0, st>>>(X, static_cast<int>(rows), sigma);
+  } else {
+    const long long nk = cdiv(N, kColChunkRows);
+    WsCarver c{static_cast<char*>(workspace), 0, workspace_bytes};
+    float* part = c.take<float>(static_cast<size_t>(Hkv * nk * d));
+    int* cnt = c.take<int>(static_cast<size_t>(Hkv * nk));
+    if (!c.ok() || !workspace) return KVS_ERR_WORKSPACE;
+    const dim3 grid(static_cast<unsigned>(nk), static_cast<unsigned>(Hkv));
+    if (d == 64)
+      colsumsq_kernel<64><<<grid, kNormThreads, 0, st>>>(X, static_cast<int>(N), keep_bits, part, cnt);
+    else
+      colsumsq_kernel<128><<<grid, kNormThreads, 0, st>>>(X, static_cast<int>(N), keep_bits, part, cnt);
+    const int n = static_cast<int>(Hkv * d);
+    masked_rms_finalize_kernel<<<static_cast<int>(cdiv(n, 256)), 256, 0, st>>>(
+        part, cnt, static_cast<int>(nk), static_cast<int>(Hkv), static_cast<int>(d), sigma);
+  }
+  KVS_CUDA_TRY(cudaGetLastError());
+  return KVS_OK;
+}
+
+size_t kvs_allocate_workspace_size(int64_t U) {
+  (void)U;
+  return alloc_ws_bytes(alloc_blocks_max());
+}
+
+int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t budget_bits, uint32_t width_mask,
+                      uint8_t* bits, void* workspace, size_t workspace_bytes, void* stream) {
+  if (U < 0 || budget_bits < 0) return KVS_ERR_INVALID_ARG;
+  if ((width_mask & ~KVS_WIDTHS_ALL & ~1u) != 0) return KVS_ERR_INVALID_ARG;
+  if (U == 0) return KVS_OK;
+  if (!w || !sigma || !bits) return KVS_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  AllocParams p;
+  std::memset(&p, 0, sizeof(p));
+  int nw = 1;
+  p.width[0] = 0;
+  for (int b : {2, 4, 8, 16})
+    if (width_mask & (1u << b)) p.width[nw++] = b;
+  p.K = nw - 1;
+  if (p.K == 0) {
+    KVS_CUDA_TRY(cudaMemsetAsync(bits, 0, static_cast<size_t>(U), st));
+    return KVS_OK;
+  }
+  p.min_cost = 1 << 30;
+  for (int k = 0; k < p.K; ++k) {
+    const int b0 = p.width[k], b1 = p.width[k + 1];
+    p.cost[k] = b1 - b0;
+    p.min_cost = std::min(p.min_cost, p.cost[k]);
+    p.c[k] = (std::ldexp(1.0, -b0) - std::ldexp(1.0, -b1)) / static_cast<double>(b1 - b0);
+  }
+  int occ = 0;
+  KVS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, allocate_kernel, kAllocThreads, 0));
+  const int nb_cap = std::min(std::max(occ, 1) * sm_count(), alloc_blocks_max());
+  const int nb = static_cast<int>(std::max<long long>(1, std::min<long long>(nb_cap, cdiv(U, kAllocThreads))));
+  WsCarver c{static_cast<char*>(workspace), 0, workspace_bytes};
+  p.hdr = c.take<AllocHeader>(1);
+  p.tie_block = c.take<unsigned long long>(nb);
+  p.cand = c.take<FixCand>(static_cast<size_t>(kMaxFixRounds) * nb);
+  if (!c.ok() || !workspace) return KVS_ERR_WORKSPACE;
+  p.w = w;
+  p.sigma = sigma;
+  p.bits = bits;
+  p.U = U;
+  p.B = static_cast<unsigned long long>(budget_bits);
+  KVS_CUDA_TRY(cudaMemsetAsync(p.hdr, 0, sizeof(AllocHeader), st));
+  void* args[] = {&p};
+  KVS_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(allocate_kernel), dim3(nb),
+                                           dim3(kAllocThreads), args, 0, st));
+  return KVS_OK;
+}
+
+int kvs_pack_capacity(int64_t Hkv, int64_t N, int64_t d, int axis, int64_t budget_bits, int64_t* cap_units,
+                      int64_t* cap_groups) {
+  const int rc = pack_shape_ok(Hkv, N, d, axis);
+  if (rc) return rc;
+  if (budget_bits < 0 || !cap_units || !cap_groups) return KVS_ERR_INVALID_ARG;
+  const long long U = axis == 0 ? Hkv * N : Hkv * d;
+  const long long gpu = axis == 0 ? d / 64 : cdiv(N, 64);
+  const int widths[4] = {2, 4, 8, 16};
+  for (int i = 0; i < 4; ++i) {
+    cap_units[i] = std::min<long long>(U, budget_bits / widths[i]);
+    cap_groups[i] = cap_units[i] * gpu;
+  }
+  return KVS_OK;
+}
+
+size_t kvs_pack_workspace_size(int64_t Hkv, int64_t N, int64_t d, int axis) {
+  if (pack_shape_ok(Hkv, N, d, axis)) return 0;
+  PackWs w;
+  return carve_pack(Hkv, N, d, axis, nullptr, 0, &w);
+}
+
+int kvs_quantize_pack(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis, const uint8_t* bits,
+                      const uint8_t* keep_bits, const kvs_stream_set* streams, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  return pack_common(X, Hkv, N, d, axis, bits, keep_bits, streams, workspace, workspace_bytes, stream, false,
+                     nullptr);
+}
+
+int kvs_dequantize(const kvs_stream_set* streams, int64_t Hkv, int64_t N, int64_t d, int axis, const uint8_t* bits,
+                   const uint8_t* keep_bits, float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return pack_common(nullptr, Hkv, N, d, axis, bits, keep_bits, streams, workspace, workspace_bytes, stream, true,
+                     out);
+}
+
+}  // extern "C"

@@ -1,0 +1,647 @@
+// Attention-derived importance scores of a prefilled KV cache.
+//
+//   pass 1 (lse_pass_kernel):  lse_r = ln sum_{t<=p_r} exp(s_{r,t})
+//       [KVSculpt: KV Cache Compression as Distillation, §2 loss, LSE term]
+//   pass 2 (colreduce_pass_kernel), probabilities recomputed as a = exp(s - lse):
+//       sum mode:  w_t = sum over the group's heads and rows of a_{r,t}
+//                  [RDKV, §2.1, token distortion weight w_t = sum_tau a_{tau,t}]
+//       max mode:  s_t = max_heads max_r a_{r,t} |h_r| / |W_O^h v_t|
+//                  [KVzap, §2.1, KVzip and KVzip+ scores]
+//
+// Both passes are flash-style: 128x128 logit tiles S = Q K^T are produced by
+// tcgen05.mma into tensor memory (fp32) from 128-byte-swizzled bf16 tiles that
+// TMA streams into shared memory; the N x N matrix never exists in HBM.
+// Roles per CTA: warps 0-3 reduce the tiles (one TMEM lane, i.e. one tile row,
+// per thread), warp 4 issues TMA, warp 5 issues the MMAs.  Two TMEM buffers
+// let the MMA of tile i+1 run while tile i is being reduced.
+//
+// GQA packing: a 128-row query tile holds P = 128/Gt consecutive window rows
+// of Gt heads of one KV group (row j = head (j / P), position pmin + j % P), so
+// every K tile that TMA brings in serves Gt heads at once.
+//
+// Pass 1 is Q-stationary (one tile of query rows per CTA, looping over key
+// tiles, online max / sum in the log2 domain).  Pass 2 is K-stationary
+// (S^T = K Q^T: one tile of keys per CTA looping over query tiles) so the
+// per-key reduction over queries is a per-thread reduction along the TMEM
+// row: no shuffles or atomics.  Long loops are split across CTAs and merged in
+// a fixed order by small finalize kernels, so results are deterministic.
+#pragma once
+
+#include "common.cuh"
+
+namespace kvs {
+
+constexpr int kScoreThreads = 192;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+struct ScoreGeom {
+  int Hq, Hkv, G, Gt, P, W, N, q_pos0;
+  int n_hc;   // G / Gt head chunks per group
+  int n_pb;   // ceil(W / P) position blocks
+  int n_rt;   // Hkv * n_hc * n_pb query-row tiles
+  int n_kt;   // ceil(N / 128) key tiles
+  float c_log2;  // log2(e) / sqrt(d)
+};
+
+__host__ __device__ inline int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+// last position of position block pb, and the key tiles it needs
+__host__ __device__ inline int pb_pmax(const ScoreGeom& g, int pb) {
+  int r1 = (pb + 1) * g.P;
+  if (r1 > g.W) r1 = g.W;
+  return g.q_pos0 + r1 - 1;
+}
+__host__ __device__ inline int pb_nkt(const ScoreGeom& g, int pb) { return pb_pmax(g, pb) / 128 + 1; }
+
+// first position block that any key of key tile kt is visible to
+__host__ __device__ inline int kt_pb_lo(const ScoreGeom& g, int kt) {
+  const int t0 = kt * 128;
+  const int num = t0 - g.q_pos0 - g.P + 1;
+  return num <= 0 ? 0 : ceil_div_i(num, g.P);
+}
+__host__ __device__ inline int kt_nvis(const ScoreGeom& g, int kt) {
+  const int t0 = kt * 128;
+  if (t0 > g.q_pos0 + g.W - 1) return 0;
+  const int lo = kt_pb_lo(g, kt);
+  return lo < g.n_pb ? g.n_pb - lo : 0;
+}
+
+template <int DH>
+struct TileCfg {
+  static constexpr int kPanels = DH / 64;           // 64-column (128-byte) panels per row
+  static constexpr int kTileBytes = kPanels * 16384;  // 128 rows x DH bf16
+  static constexpr int kKSteps = DH / 16;           // MMA K=16 steps
+};
+
+template <int DH>
+__device__ __forceinline__ void issue_tile_mma(uint32_t d_tmem, uint32_t a_base, uint32_t b_base) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+#pragma unroll
+  for (int kk = 0; kk < TileCfg<DH>::kKSteps; ++kk) {
+    const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
+    umma_bf16(d_tmem, sdesc_kmajor_sw128(a_base + off), sdesc_kmajor_sw128(b_base + off), idesc,
+              kk > 0 ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+// ---------------------------------------------------------------------------
+// pass 1: row log-sum-exp
+// ---------------------------------------------------------------------------
+template <int DH, int NS>
+struct LseSmem {
+  uint8_t q[TileCfg<DH>::kTileBytes];
+  uint8_t k[NS][TileCfg<DH>::kTileBytes];
+  uint64_t q_full, k_full[NS], k_empty[NS], s_full[2], s_empty[2], drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// partial[(rt * n_split + split) * 128 + row] = (running max m, sum l), log2 domain:
+// the rows' 2^(x - m) summed over the split's key tiles, x = s * log2(e)/sqrt(d).
+template <int DH, int NS>
+__global__ void __launch_bounds__(kScoreThreads, 2)
+    lse_pass_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                    const ScoreGeom geo, const int kt_chunk, const int n_split, float2* __restrict__ partial) {
+  extern __shared__ uint8_t smem_raw[];
+  LseSmem<DH, NS>& S = *reinterpret_cast<LseSmem<DH, NS>*>(align1024(smem_raw));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x;
+  const int jy = blockIdx.y;
+  const int pb = geo.n_pb - 1 - (jy % geo.n_pb);  // longest rows launch first
+  const int gh = jy / geo.n_pb;
+  const int g = gh / geo.n_hc, hc = gh % geo.n_hc;
+  const int rt = gh * geo.n_pb + pb;
+  const int pmin = geo.q_pos0 + pb * geo.P;
+  const int kt0 = split * kt_chunk;
+  const int kt1 = min(pb_nkt(geo, pb), kt0 + kt_chunk);
+  if (kt0 >= kt1 || timeout_recorded()) return;  // uniform over the CTA, before any barrier
+  const int niter = kt1 - kt0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&S.q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&S.k_full[s], 1);
+      mbar_init(&S.k_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.s_full[b], 1);
+      mbar_init(&S.s_empty[b], 4);
+    }
+    mbar_init(&S.drain, 1);
+    S.abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&S.tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  volatile int* abort_flag = &S.abort_flag;
+
+  if (warp == 4) {
+    if (lane == 0) {  // TMA producer
+      prefetch_tensormap(&mapQ);
+      prefetch_tensormap(&mapK);
+      constexpr uint32_t kBytes = TileCfg<DH>::kTileBytes;
+      mbar_arrive_expect_tx(&S.q_full, kBytes);
+#pragma unroll
+      for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
+        tma_load_3d(S.q + p * 16384, &mapQ, &S.q_full, p * 64, pb * geo.P, g * geo.G + hc * geo.Gt);
+      int issued = 0;
+      for (int i = 0; i < niter; ++i) {
+        const int s = i % NS;
+        const uint32_t ph = (i / NS) & 1;
+        if (!mbar_wait(&S.k_empty[s], ph ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(&S.k_full[s], kBytes);
+#pragma unroll
+        for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
+          tma_load_3d(S.k[s] + p * 16384, &mapK, &S.k_full[s], p * 64, (kt0 + i) * 128, g);
+        issued = i + 1;
+      }
+      if (*abort_flag) {  // let our copies land before the CTA goes away
+        volatile int never = 0;
+        mbar_wait(&S.q_full, 0, &never);
+        for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(&S.k_full[i % NS], (i / NS) & 1, &never);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {  // MMA issuer
+      if (mbar_wait(&S.q_full, 0, abort_flag)) {
+        for (int i = 0; i < niter; ++i) {
+          const int s = i % NS, b = i & 1;
+          if (!mbar_wait(&S.k_full[s], (i / NS) & 1, abort_flag)) break;
+          if (!mbar_wait(&S.s_empty[b], ((i >> 1) & 1) ^ 1u, abort_flag)) break;
+          tc_fence_after();
+          issue_tile_mma<DH>(tmem + b * 128, smem_u32(S.q), smem_u32(S.k[s]));
+          umma_commit(&S.k_empty[s]);
+          umma_commit(&S.s_full[b]);
+        }
+      }
+      if (*abort_flag) {
+        volatile int never = 0;
+        umma_commit(&S.drain);
+        mbar_wait(&S.drain, 0, &never);
+      }
+    }
+  } else {  // warps 0-3: one tile row per thread
+    const int row = warp * 32 + lane;
+    const int pos = pmin + row % geo.P;
+    const float c = geo.c_log2;
+    float m = -INFINITY, l = 0.f;
+    for (int i = 0; i < niter; ++i) {
+      const int b = i & 1;
+      if (!mbar_wait(&S.s_full[b], (i >> 1) & 1, abort_flag)) break;
+      tc_fence_after();
+      const int t0 = (kt0 + i) * 128;
+      const bool diag = t0 + 127 > pmin;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        float v[32];
+        tmem_load32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * 128 + ch * 32, v);
+        if (diag) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (t0 + ch * 32 + j > pos) v[j] = -INFINITY;
+        }
+        float cm0 = fmaxf(v[0], v[1]), cm1 = fmaxf(v[2], v[3]);
+#pragma unroll
+        for (int j = 4; j < 32; j += 4) {
+          cm0 = fmaxf(cm0, fmaxf(v[j], v[j + 1]));
+          cm1 = fmaxf(cm1, fmaxf(v[j + 2], v[j + 3]));
+        }
+        const float m_new = fmaxf(m, fmaxf(cm0, cm1) * c);
+        if (m_new != -INFINITY) {
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            a0 += ex2_approx(fmaf(v[j], c, -m_new));
+            a1 += ex2_approx(fmaf(v[j + 1], c, -m_new));
+            a2 += ex2_approx(fmaf(v[j + 2], c, -m_new));
+            a3 += ex2_approx(fmaf(v[j + 3], c, -m_new));
+          }
+          l = l * ex2_approx(m - m_new) + ((a0 + a1) + (a2 + a3));
+          m = m_new;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.s_empty[b]);
+    }
+    partial[(static_cast<size_t>(rt) * n_split + split) * 128 + row] = make_float2(m, l);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// Merges pass-1 partials in split order.  Writes lse (natural log) for the
+// valid rows and, per query tile, the pass-2 offsets
+//     b[rt][row] = lse2 - log2|h_r|   (|h_r| = 1 when hn is null; +inf for padding rows)
+// so that pass 2 computes a_{r,t} |h_r| = 2^(s c - b).
+__global__ void lse_finalize_kernel(const ScoreGeom geo, const int kt_chunk, const int n_split,
+                                    const float2* __restrict__ partial, const float* __restrict__ hn,
+                                    float* __restrict__ lse, float* __restrict__ b_plain,
+                                    float* __restrict__ b_scaled) {
+  const int rt = blockIdx.x, row = threadIdx.x;
+  const int pb = rt % geo.n_pb;
+  const int gh = rt / geo.n_pb;
+  const int g = gh / geo.n_hc, hc = gh % geo.n_hc;
+  const int ns = ceil_div_i(pb_nkt(geo, pb), kt_chunk);
+  const float2* p = partial + static_cast<size_t>(rt) * n_split * 128 + row;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, p[s * 128].x);
+  float L = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float2 v = p[s * 128];
+    if (v.x != -INFINITY) L += v.y * ex2_approx(v.x - M);
+  }
+  const float l2 = M + lg2_approx(L);
+  const int hl = row / geo.P, r = pb * geo.P + row % geo.P;
+  const bool valid = r < geo.W;
+  if (valid) lse[static_cast<size_t>(g * geo.G + hc * geo.Gt + hl) * geo.W + r] = l2 * kLn2;
+  if (b_plain) b_plain[static_cast<size_t>(rt) * 128 + row] = valid ? l2 : INFINITY;
+  if (b_scaled) b_scaled[static_cast<size_t>(rt) * 128 + row] = valid ? l2 - lg2_approx(hn[r]) : INFINITY;
+}
+
+// ---------------------------------------------------------------------------
+// pass 2: per-key reductions over queries (K-stationary)
+// ---------------------------------------------------------------------------
+template <int DH, int NS>
+struct ColSmem {
+  uint8_t k[TileCfg<DH>::kTileBytes];
+  uint8_t q[NS][TileCfg<DH>::kTileBytes];
+  float bv[NS][128];
+  uint64_t k_full, q_full[NS], q_empty[NS], s_full[2], s_empty[2], drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// One CTA: 128 keys (kt) of KV head g, query tiles [q0, q1) of that key tile's
+// visible list (head chunk major, position block minor).
+//   MAXMODE = false: out = sum_j 2^(s_j c - b_j)               (w_t)
+//   MAXMODE = true : out = max_heads 2^(max_j (s_j c - b_j)) / vn[head][t]   (vn null: / 1)
+// Output goes to out_direct (n_split == 1) or out_partial[split][g*N + t].
+template <int DH, int NS, int GT, bool MAXMODE>
+__global__ void __launch_bounds__(kScoreThreads, 2)
+    colreduce_pass_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                          const ScoreGeom geo, const int qt_chunk, const int n_split,
+                          const float* __restrict__ bvals, const float* __restrict__ vn,
+                          float* __restrict__ out_direct, float* __restrict__ out_partial) {
+  constexpr int P = 128 / GT;
+  extern __shared__ uint8_t smem_raw[];
+  ColSmem<DH, NS>& S = *reinterpret_cast<ColSmem<DH, NS>*>(align1024(smem_raw));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x;
+  const int kt = blockIdx.y / geo.Hkv, g = blockIdx.y % geo.Hkv;
+  const int t0 = kt * 128;
+  const int nvis = kt_nvis(geo, kt);
+  const int pb_lo = geo.n_pb - nvis;
+  const int nq = nvis * geo.n_hc;
+  const int q0 = split * qt_chunk;
+  const int q1 = min(nq, q0 + qt_chunk);
+  if (q0 >= q1 || timeout_recorded()) return;
+  const int niter = q1 - q0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&S.k_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&S.q_full[s], 1);
+      mbar_init(&S.q_empty[s], 1 + 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.s_full[b], 1);
+      mbar_init(&S.s_empty[b], 4);
+    }
+    mbar_init(&S.drain, 1);
+    S.abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&S.tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  volatile int* abort_flag = &S.abort_flag;
+
+  if (warp == 4) {
+    if (lane == 0) {  // TMA producer
+      prefetch_tensormap(&mapQ);
+      prefetch_tensormap(&mapK);
+      constexpr uint32_t kBytes = TileCfg<DH>::kTileBytes;
+      mbar_arrive_expect_tx(&S.k_full, kBytes);
+#pragma unroll
+      for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
+        tma_load_3d(S.k + p * 16384, &mapK, &S.k_full, p * 64, t0, g);
+      int issued = 0;
+      for (int i = 0; i < niter; ++i) {
+        const int s = i % NS;
+        if (!mbar_wait(&S.q_empty[s], ((i / NS) & 1) ^ 1u, abort_flag)) break;
+        const int q = q0 + i;
+        const int hc = q / nvis, pb = pb_lo + q % nvis;
+        const int rt = (g * geo.n_hc + hc) * geo.n_pb + pb;
+        mbar_arrive_expect_tx(&S.q_full[s], kBytes + 512u);
+#pragma unroll
+        for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
+          tma_load_3d(S.q[s] + p * 16384, &mapQ, &S.q_full[s], p * 64, pb * P, g * geo.G + hc * GT);
+        bulk_load(S.bv[s], bvals + static_cast<size_t>(rt) * 128, 512u, &S.q_full[s]);
+        issued = i + 1;
+      }
+      if (*abort_flag) {
+        volatile int never = 0;
+        mbar_wait(&S.k_full, 0, &never);
+        for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(&S.q_full[i % NS], (i / NS) & 1, &never);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {  // MMA issuer: S^T tile = K_tile (M = 128 keys) x Q_tile^T (N = 128 rows)
+      if (mbar_wait(&S.k_full, 0, abort_flag)) {
+        for (int i = 0; i < niter; ++i) {
+          const int s = i % NS, b = i & 1;
+          if (!mbar_wait(&S.q_full[s], (i / NS) & 1, abort_flag)) break;
+          if (!mbar_wait(&S.s_empty[b], ((i >> 1) & 1) ^ 1u, abort_flag)) break;
+          tc_fence_after();
+          issue_tile_mma<DH>(tmem + b * 128, smem_u32(S.k), smem_u32(S.q[s]));
+          umma_commit(&S.q_empty[s]);
+          umma_commit(&S.s_full[b]);
+        }
+      }
+      if (*abort_flag) {
+        volatile int never = 0;
+        umma_commit(&S.drain);
+        mbar_wait(&S.drain, 0, &never);
+      }
+    }
+  } else {  // warps 0-3: one key per thread
+    const int krow = warp * 32 + lane;
+    const int t = t0 + krow;
+    const float c = geo.c_log2;
+    float acc = 0.f;
+    float best = 0.f;
+    float mx[GT];
+#pragma unroll
+    for (int h = 0; h < GT; ++h) mx[h] = -INFINITY;
+    int cur_hc = -1;
+    auto flush = [&](int hc) {
+#pragma unroll
+      for (int h = 0; h < GT; ++h) {
+        if (mx[h] != -INFINITY && t < geo.N) {
+          float r = ex2_approx(mx[h]);
+          if (vn) r = r / vn[static_cast<size_t>(g * geo.G + hc * GT + h) * geo.N + t];
+          best = fmaxf(best, r);
+        }
+        mx[h] = -INFINITY;
+      }
+    };
+    for (int i = 0; i < niter; ++i) {
+      const int s = i % NS, b = i & 1;
+      const int q = q0 + i;
+      const int hc = q / nvis, pb = pb_lo + q % nvis;
+      if (MAXMODE && hc != cur_hc) {
+        if (cur_hc >= 0) flush(cur_hc);
+        cur_hc = hc;
+      }
+      if (!mbar_wait(&S.s_full[b], (i >> 1) & 1, abort_flag)) break;
+      // the staged offsets bv[s] arrived with the query tile
+      if (!mbar_wait(&S.q_full[s], (i / NS) & 1, abort_flag)) break;
+      tc_fence_after();
+      const int pmin = geo.q_pos0 + pb * P;
+      const bool diag = pmin < t0 + 127;
+      const float4* bvs = reinterpret_cast<const float4*>(S.bv[s]);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        float v[32];
+        tmem_load32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * 128 + ch * 32, v);
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 bb = bvs[ch * 8 + j4];
+          v[4 * j4 + 0] = fmaf(v[4 * j4 + 0], c, -bb.x);
+          v[4 * j4 + 1] = fmaf(v[4 * j4 + 1], c, -bb.y);
+          v[4 * j4 + 2] = fmaf(v[4 * j4 + 2], c, -bb.z);
+          v[4 * j4 + 3] = fmaf(v[4 * j4 + 3], c, -bb.w);
+        }
+        if (diag) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (pmin + ((ch * 32 + j) % P) < t) v[j] = -INFINITY;
+        }
+        if (MAXMODE) {
+          float m0 = fmaxf(v[0], v[1]), m1 = fmaxf(v[2], v[3]);
+#pragma unroll
+          for (int j = 4; j < 32; j += 4) {
+            m0 = fmaxf(m0, fmaxf(v[j], v[j + 1]));
+            m1 = fmaxf(m1, fmaxf(v[j + 2], v[j + 3]));
+          }
+          const int hl = (ch * 32) / P;  // P >= 32: the chunk lies in one head
+#pragma unroll
+          for (int h = 0; h < GT; ++h)
+            if (h == hl) mx[h] = fmaxf(mx[h], fmaxf(m0, m1));
+        } else {
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            a0 += ex2_approx(v[j]);
+            a1 += ex2_approx(v[j + 1]);
+            a2 += ex2_approx(v[j + 2]);
+            a3 += ex2_approx(v[j + 3]);
+          }
+          acc += (a0 + a1) + (a2 + a3);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&S.s_empty[b]);
+        mbar_arrive(&S.q_empty[s]);
+      }
+    }
+    if (MAXMODE && cur_hc >= 0) flush(cur_hc);
+    const float res = MAXMODE ? best : acc;
+    if (t < geo.N) {
+      const size_t o = static_cast<size_t>(g) * geo.N + t;
+      if (n_split == 1)
+        out_direct[o] = res;
+      else
+        out_partial[static_cast<size_t>(split) * geo.Hkv * geo.N + o] = res;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// Sums (or maxes) pass-2 partials over the key tile's splits, in split order.
+template <bool MAXMODE>
+__global__ void colreduce_finalize_kernel(const ScoreGeom geo, const int qt_chunk, const int n_split,
+                                          const float* __restrict__ part, float* __restrict__ out) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  const int total = geo.Hkv * geo.N;
+  if (idx >= total) return;
+  const int t = idx % geo.N;
+  const int ns = ceil_div_i(kt_nvis(geo, t / 128) * geo.n_hc, qt_chunk);
+  float r = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float v = part[static_cast<size_t>(s) * total + idx];
+    r = MAXMODE ? fmaxf(r, v) : r + v;
+  }
+  out[idx] = r;
+}
+
+// ---------------------------------------------------------------------------
+// KVzip+ norms   [KVzap §2.1: |h_j| and |W_O v_i|]
+// ---------------------------------------------------------------------------
+// out[r] = |X[r, :]|_2, one warp per row, 16-byte loads, fixed-order reduction
+__global__ void row_norm_kernel(const uint16_t* __restrict__ X, const int rows, const int cols,
+                                float* __restrict__ out) {
+  const int warps = blockDim.x >> 5;
+  const int r = blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const uint4* p = reinterpret_cast<const uint4*>(X + static_cast<size_t>(r) * cols);
+  const int n16 = cols / 8;
+  float acc = 0.f;
+  for (int i = lane; i < n16; i += 32) {
+    const uint4 u = __ldg(p + i);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
+      acc = fmaf(lo, lo, acc);
+      acc = fmaf(hi, hi, acc);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  if (lane == 0) out[r] = sqrtf(acc);
+}
+
+// Partial Gram matrices of the per-head output projections:
+//   gram[s][h][c1][c2] = sum_{i in slice s} W_O[i, h*DH + c1] W_O[i, h*DH + c2]
+// grid (n_slices, Hq, DH/64); 256 threads; each thread 4 x (DH/16) outputs.
+template <int DH>
+__global__ void __launch_bounds__(256) gram_kernel(const uint16_t* __restrict__ WO, const int D, const int Hq,
+                                                   const int slice_len, float* __restrict__ gram) {
+  constexpr int CPT = DH / 16;
+  __shared__ float T[32][DH + 4];
+  const int s = blockIdx.x, h = blockIdx.y, c1b = blockIdx.z * 64;
+  const int tid = threadIdx.x;
+  const int r4 = (tid / 16) * 4, cg = (tid % 16) * CPT;
+  float acc[4][CPT];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < CPT; ++b) acc[a][b] = 0.f;
+  const int i_begin = s * slice_len, i_end = min(D, i_begin + slice_len);
+  const size_t ld = static_cast<size_t>(Hq) * DH;
+  for (int i0 = i_begin; i0 < i_end; i0 += 32) {
+    for (int e = tid; e < 32 * DH; e += 256) {
+      const int rr = e / DH, cc = e % DH;
+      const int i = i0 + rr;
+      float v = 0.f;
+      if (i < i_end) v = __uint_as_float(static_cast<uint32_t>(WO[i * ld + h * DH + cc]) << 16);
+      T[rr][cc] = v;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int k = 0; k < 32; ++k) {
+      float a[4], b[CPT];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) a[x] = T[k][c1b + r4 + x];
+#pragma unroll
+      for (int y = 0; y < CPT; ++y) b[y] = T[k][cg + y];
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < CPT; ++y) acc[x][y] = fmaf(a[x], b[y], acc[x][y]);
+    }
+    __syncthreads();
+  }
+  float* out = gram + ((static_cast<size_t>(s) * Hq + h) * DH) * DH;
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < CPT; ++y) out[(c1b + r4 + x) * DH + cg + y] = acc[x][y];
+}
+
+// vn[h][t] = sqrt(v_t^T G_h v_t) = |W_O^h v_t|, G_h = sum of the Gram slices
+// (fixed order).  grid (ceil(N/64), Hq); 256 threads: 16 token quads x 16 column groups.
+template <int DH>
+__global__ void __launch_bounds__(256) vnorm_kernel(const uint16_t* __restrict__ V,
+                                                    const float* __restrict__ gram, const int n_slices,
+                                                    const int Hq, const int G, const int N,
+                                                    float* __restrict__ vn) {
+  constexpr int CPT = DH / 16;
+  extern __shared__ uint8_t smem_raw[];
+  float* Gs = reinterpret_cast<float*>(smem_raw);  // [DH][DH]
+  float* Vs = Gs + DH * DH;                        // [DH][64] (transposed tile)
+  const int h = blockIdx.y, t0 = blockIdx.x * 64, tid = threadIdx.x;
+  const int g = h / G;
+  for (int e = tid; e < DH * DH; e += 256) {
+    float a = 0.f;
+    for (int s = 0; s < n_slices; ++s) a += gram[(static_cast<size_t>(s) * Hq + h) * DH * DH + e];
+    Gs[e] = a;
+  }
+  for (int e = tid; e < 64 * DH; e += 256) {
+    const int tt = e / DH, cc = e % DH;
+    const int t = t0 + tt;
+    float v = 0.f;
+    if (t < N) v = __uint_as_float(static_cast<uint32_t>(V[(static_cast<size_t>(g) * N + t) * DH + cc]) << 16);
+    Vs[cc * 64 + tt] = v;
+  }
+  __syncthreads();
+  const int tq = (tid / 16) * 4, cg = (tid % 16) * CPT;
+  float acc[4][CPT];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < CPT; ++b) acc[a][b] = 0.f;
+#pragma unroll 4
+  for (int k = 0; k < DH; ++k) {
+    const float4 a4 = *reinterpret_cast<const float4*>(&Vs[k * 64 + tq]);
+    const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+    float b[CPT];
+#pragma unroll
+    for (int y = 0; y < CPT; ++y) b[y] = Gs[k * DH + cg + y];
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < CPT; ++y) acc[x][y] = fmaf(a[x], b[y], acc[x][y]);
+  }
+  float part[4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    float p = 0.f;
+#pragma unroll
+    for (int y = 0; y < CPT; ++y) p = fmaf(acc[x][y], Vs[(cg + y) * 64 + tq + x], p);
+    part[x] = p;
+  }
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) part[x] += __shfl_xor_sync(0xFFFFFFFFu, part[x], o);
+  if ((tid % 16) == 0) {
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int t = t0 + tq + x;
+      if (t < N) vn[static_cast<size_t>(h) * N + t] = sqrtf(fmaxf(part[x], 0.f));
+    }
+  }
+}
+
+}  // namespace kvs

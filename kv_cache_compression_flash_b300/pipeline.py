@@ -1,0 +1,85 @@
+"""One pass of the RDKV hot path over one (layer, sequence) pool.
+
+Stage 1 weights, stage 2 V allocation, stage 3 K allocation over the kept
+tokens, then packing (and optionally dequantisation), each step a call into
+libkvs.so.   [RDKV §2.2 pipeline; §2.3 TriZone streams]
+
+Buffers are allocated once per shape so a step allocates nothing and can be
+replayed inside a CUDA graph.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib as K_
+
+
+class RdkvLayerStep:
+    """Preallocated outputs and workspaces for one pool shape."""
+
+    def __init__(self, Hq, Hkv, N, W, d, avg_bits, device="cuda", width_mask=K_.WIDTHS_ALL, dequant=True):
+        self.shape = (Hq, Hkv, N, W, d)
+        self.dequant = dequant
+        self.width_mask = width_mask
+        dev = torch.device(device)
+        self.U_v, self.U_k = Hkv * N, Hkv * d
+        self.B_v = int(math.floor(avg_bits * self.U_v))
+        self.B_k = int(math.floor(avg_bits * self.U_k))
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.out = {"lse": torch.empty(Hq, W, **f32), "w_t": torch.empty(Hkv, N, **f32)}
+        self.w_c = torch.empty(Hkv, d, **f32)
+        self.sig_t = torch.empty(Hkv, N, **f32)
+        self.sig_c = torch.empty(Hkv, d, **f32)
+        self.bits_v = torch.empty(self.U_v, dtype=torch.uint8, device=dev)
+        self.bits_k = torch.empty(self.U_k, dtype=torch.uint8, device=dev)
+        self.v_streams = K_.Streams(Hkv, N, d, 0, self.B_v, dev)
+        self.k_streams = K_.Streams(Hkv, N, d, 1, self.B_k, dev)
+        self.v_hat = torch.empty(Hkv, N, d, **f32) if dequant else None
+        self.k_hat = torch.empty(Hkv, N, d, **f32) if dequant else None
+        self.ws = {k: K_.Workspace() for k in ("score", "cw", "rms0", "rms1", "av", "ak", "pv", "pk", "dv", "dk")}
+        # size every workspace now so run() allocates nothing
+        L = K_.lib()
+        sizes = {
+            "score": L.kvs_score_workspace_size(Hq, Hkv, W, N, d, 0, N - W, K_.MODE_LSE | K_.MODE_RDKV_WT),
+            "cw": L.kvs_channel_weights_workspace_size(Hq, Hkv, W, N, d),
+            "rms0": 256, "rms1": L.kvs_unit_rms_workspace_size(Hkv, N, d, 1),
+            "av": L.kvs_allocate_workspace_size(self.U_v), "ak": L.kvs_allocate_workspace_size(self.U_k),
+            "pv": L.kvs_pack_workspace_size(Hkv, N, d, 0), "pk": L.kvs_pack_workspace_size(Hkv, N, d, 1),
+            "dv": L.kvs_pack_workspace_size(Hkv, N, d, 0), "dk": L.kvs_pack_workspace_size(Hkv, N, d, 1),
+        }
+        for k, n in sizes.items():
+            self.ws[k].get(n, dev)
+
+    # number of kernels one run() launches (memset nodes excluded)
+    def kernel_launches(self) -> int:
+        Hq, Hkv, N, W, d = self.shape
+        n = K_.score_plan_info(Hq, Hkv, W, N, d, mode=K_.MODE_LSE | K_.MODE_RDKV_WT)[4]
+        n += 3          # channel weights: 2 column passes + finalize
+        n += 1          # sigma_t
+        n += 1 + 2      # V allocation, sigma_c (pass + finalize)
+        n += 1          # K allocation
+        n += 4 + 3      # V pack (count, scan, rank, pack), K pack (kept, plan, pack)
+        if self.dequant:
+            n += 4 + 4  # V dequant (count, scan, rank, dequant), K dequant (kept, plan, zero, dequant)
+        return n
+
+    def run(self, Q, K, V, stream=None):
+        Hq, Hkv, N, W, d = self.shape
+        ws = self.ws
+        K_.score_attention(Q, K, q_pos0=N - W, mode=K_.MODE_LSE | K_.MODE_RDKV_WT, out=self.out, ws=ws["score"],
+                           stream=stream)
+        K_.channel_weights(Q, K, out=self.w_c, ws=ws["cw"], stream=stream)
+        K_.unit_rms(V, 0, out=self.sig_t, ws=ws["rms0"], stream=stream)
+        K_.allocate_bits(self.out["w_t"], self.sig_t, self.B_v, self.width_mask, out=self.bits_v, ws=ws["av"],
+                         stream=stream)
+        K_.unit_rms(K, 1, keep_bits=self.bits_v, out=self.sig_c, ws=ws["rms1"], stream=stream)
+        K_.allocate_bits(self.w_c, self.sig_c, self.B_k, self.width_mask, out=self.bits_k, ws=ws["ak"],
+                         stream=stream)
+        K_.quantize_pack(V, 0, self.bits_v, None, self.v_streams, ws=ws["pv"], stream=stream)
+        K_.quantize_pack(K, 1, self.bits_k, self.bits_v, self.k_streams, ws=ws["pk"], stream=stream)
+        if self.dequant:
+            K_.dequantize(self.v_streams, self.bits_v, None, out=self.v_hat, ws=ws["dv"], stream=stream)
+            K_.dequantize(self.k_streams, self.bits_k, self.bits_v, out=self.k_hat, ws=ws["dk"], stream=stream)
+        return self

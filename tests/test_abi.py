@@ -1,0 +1,96 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, and rejects bad arguments on the host before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from kv_cache_compression_flash_b300 import _lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvs.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvs_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return L.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in L.SIGNATURES, f"binding lacks {n}"
+
+
+def test_status_strings_and_version(lib):
+    assert lib.kvs_version() == 100
+    for code, name in L.STATUS.items():
+        assert lib.kvs_status_string(code).decode() == name
+
+
+def _score(lib, **kw):
+    a = dict(Q=1 << 20, K=1 << 20, V=None, h=None, W_O=None, Hq=8, Hkv=2, W=16, N=64, d=128, D=0, q_pos0=48,
+             mode=L.MODE_LSE | L.MODE_RDKV_WT, lse=1 << 20, w_t=1 << 20, s_plus=None, ws=1 << 20, wsb=1 << 30)
+    a.update(kw)
+    v = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.kvs_score_attention(v(a["Q"]), v(a["K"]), v(a["V"]), v(a["h"]), v(a["W_O"]), a["Hq"], a["Hkv"],
+                                   a["W"], a["N"], a["d"], a["D"], a["q_pos0"], a["mode"], v(a["lse"]),
+                                   v(a["w_t"]), v(a["s_plus"]), v(a["ws"]), a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Q=None), 1), (dict(lse=None), 1), (dict(w_t=None), 1),
+    (dict(Hq=7), 1), (dict(q_pos0=49), 1), (dict(q_pos0=-1), 1), (dict(N=0), 1), (dict(W=0), 1),
+    (dict(d=96), 2), (dict(Hq=12, Hkv=2), 2),
+    (dict(mode=L.MODE_LSE | L.MODE_KVZIP | L.MODE_KVZIP_PLUS, s_plus=1 << 20), 1),
+    (dict(mode=L.MODE_LSE | L.MODE_KVZIP_PLUS, s_plus=1 << 20, D=64), 1),   # V, h, W_O missing
+    (dict(mode=1 << 9), 1),
+    (dict(Q=(1 << 20) + 2), 1),                                             # TMA needs 16-byte alignment
+    (dict(wsb=16), 6), (dict(ws=(1 << 20) + 64), 6),
+])
+def test_score_argument_errors(lib, kw, code):
+    assert _score(lib, **kw) == code
+
+
+def test_workspace_sizes_and_plan(lib):
+    assert lib.kvs_score_workspace_size(32, 8, 512, 8192, 128, 0, 7680, 3) > 0
+    assert lib.kvs_score_workspace_size(32, 8, 512, 8192, 96, 0, 7680, 3) == 0
+    info = L.score_plan_info(32, 8, 512, 8192, 128)
+    assert info[0] >= 4 and info[1] >= 1 and info[2] >= 4 and info[3] >= 1 and info[4] >= 3
+    assert lib.kvs_allocate_workspace_size(1000) > 0
+    assert lib.kvs_pack_workspace_size(8, 8192, 128, 0) >= 8 * 8192 * 4
+    assert lib.kvs_pack_workspace_size(8, 8192, 128, 1) >= 8 * 8192 * 4
+
+
+def test_pack_capacity(lib):
+    cu, cg = (ctypes.c_int64 * 4)(), (ctypes.c_int64 * 4)()
+    assert lib.kvs_pack_capacity(8, 8192, 128, 0, 3 * 65536, cu, cg) == 0
+    assert list(cu) == [65536, 49152, 24576, 12288]
+    assert list(cg) == [2 * x for x in cu]
+    assert lib.kvs_pack_capacity(8, 8192, 128, 1, 3 * 1024, cu, cg) == 0
+    assert list(cu) == [1024, 768, 384, 192]
+    assert list(cg) == [x * 128 for x in cu]
+    assert lib.kvs_pack_capacity(8, 8192, 96, 0, 10, cu, cg) == 2
+
+
+def test_alloc_and_pack_argument_errors(lib):
+    p = ctypes.c_void_p(1 << 20)
+    assert lib.kvs_allocate_bits(p, p, 10, -1, L.WIDTHS_ALL, p, p, 1 << 20, None) == 1
+    assert lib.kvs_allocate_bits(p, p, 10, 5, 1 << 3, p, p, 1 << 20, None) == 1       # width 3 is not a width
+    assert lib.kvs_allocate_bits(None, p, 10, 5, L.WIDTHS_ALL, p, p, 1 << 20, None) == 1
+    assert lib.kvs_allocate_bits(p, p, 0, 5, L.WIDTHS_ALL, p, p, 1 << 20, None) == 0  # nothing to do
+    s = L.StreamSetC()
+    assert lib.kvs_quantize_pack(p, 8, 64, 128, 0, p, None, ctypes.byref(s), p, 1 << 20, None) == 1  # no counts
+    assert lib.kvs_quantize_pack(p, 8, 64, 128, 2, p, None, ctypes.byref(s), p, 1 << 20, None) == 1  # bad axis
+    assert lib.kvs_quantize_pack(p, 8, 64, 96, 0, p, None, ctypes.byref(s), p, 1 << 20, None) == 2
+    assert lib.kvs_unit_rms(p, 8, 64, 128, 3, None, p, p, 1 << 20, None) == 1
+    assert lib.kvs_channel_weights(p, p, 8, 3, 16, 64, 128, p, p, 1 << 20, None) == 1

@@ -1,0 +1,248 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Scores and LSE: within the relative 2e-3 the method's accuracy target states
+(fp32 accumulation of bf16 products); allocations, packed bytes and the
+dequantised values: bit-exact when the GPU is fed the oracle's own weights.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from kv_cache_compression_flash_b300 import _lib as L
+from kv_cache_compression_flash_b300 import synth
+from kv_cache_compression_flash_b300.pipeline import RdkvLayerStep
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+TOL = 2e-3
+
+
+def f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def assert_scores_close(got, ref, what):
+    """|g - o| <= 2e-3 * max(|o|, 1e-4 * max|o|) per element; 2e-3 on the vector norm."""
+    got = np.asarray(got, dtype=np.float64)
+    floor = 1e-4 * np.abs(ref).max()
+    bad = np.abs(got - ref) > TOL * np.maximum(np.abs(ref), floor)
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst at " \
+                          f"{np.unravel_index(np.argmax(np.abs(got - ref)), ref.shape)}"
+    assert np.linalg.norm(got - ref) <= TOL * np.linalg.norm(ref) + 1e-30
+
+
+def assert_lse_close(got, ref):
+    err = np.abs(np.asarray(got, np.float64) - ref)
+    assert (err <= TOL * np.maximum(1.0, np.abs(ref))).all(), f"lse worst error {err.max()}"
+
+
+def rand_layer(Hq, Hkv, W, N, d, seed, scale=1.0, sinks=0):
+    g = torch.Generator().manual_seed(seed)
+    Q = torch.randn(Hq, W, d, generator=g) * scale
+    K = torch.randn(Hkv, N, d, generator=g) * scale
+    V = torch.randn(Hkv, N, d, generator=g)
+    if sinks:
+        K[:, :sinks] *= 4
+    return Q.bfloat16(), K.bfloat16(), V.bfloat16()
+
+
+SCORE_SHAPES = [
+    # Hq, Hkv, W, N, d
+    (1, 1, 512, 512, 64),      # single head, every position a query
+    (4, 2, 100, 300, 128),     # G=2, ragged key tail, ragged window
+    (8, 2, 130, 700, 128),     # G=4, window not a multiple of the 32-row position block
+    (4, 4, 1, 1, 64),          # one key, one query
+    (2, 1, 1, 129, 128),       # one query row, a key tile plus one
+    (16, 4, 200, 1000, 64),    # d=64, G=4
+    (8, 1, 64, 2000, 128),     # G=8: two head chunks per group
+    (2, 2, 257, 257, 128),     # full causal, G=1, 3 position blocks
+]
+
+
+@pytest.mark.parametrize("shape", SCORE_SHAPES)
+def test_scores_rdkv_and_kvzip(shape):
+    Hq, Hkv, W, N, d = shape
+    Q, K, V = rand_layer(Hq, Hkv, W, N, d, seed=sum(shape), scale=1.5, sinks=2)
+    q_pos0 = N - W
+    ref = O.attention_scores(f64(Q), f64(K), q_pos0)
+    out = L.score_attention(Q.to(DEV), K.to(DEV), q_pos0=q_pos0,
+                            mode=L.MODE_LSE | L.MODE_RDKV_WT | L.MODE_KVZIP)
+    torch.cuda.synchronize()
+    assert L.device_error() == 0
+    assert_lse_close(out["lse"].cpu().numpy(), ref["lse"])
+    assert_scores_close(out["w_t"].cpu().numpy(), ref["w_t"], "w_t")
+    assert_scores_close(out["s_plus"].cpu().numpy(), ref["kvzip"], "kvzip")
+
+
+@pytest.mark.parametrize("shape", [(4, 2, 100, 300, 128), (8, 2, 96, 96, 64), (4, 1, 70, 333, 128)])
+def test_scores_kvzip_plus(shape):
+    Hq, Hkv, W, N, d = shape
+    D = 256
+    Q, K, V = rand_layer(Hq, Hkv, W, N, d, seed=7 + sum(shape))
+    g = torch.Generator().manual_seed(99)
+    h = (torch.randn(W, D, generator=g) * torch.exp(0.5 * torch.randn(W, 1, generator=g))).bfloat16()
+    WO = (torch.randn(D, Hq * d, generator=g) / math.sqrt(D)).bfloat16()
+    ref = O.attention_scores(f64(Q), f64(K), N - W, V=f64(V), h=f64(h), W_O=f64(WO))
+    out = L.score_attention(Q.to(DEV), K.to(DEV), mode=L.MODE_LSE | L.MODE_KVZIP_PLUS, V=V.to(DEV),
+                            h=h.to(DEV), W_O=WO.to(DEV))
+    torch.cuda.synchronize()
+    assert L.device_error() == 0
+    assert_lse_close(out["lse"].cpu().numpy(), ref["lse"])
+    assert_scores_close(out["s_plus"].cpu().numpy(), ref["s_plus"], "s_plus")
+
+
+def test_scores_deterministic():
+    Q, K, _ = rand_layer(8, 2, 300, 3000, 128, seed=5)
+    Qd, Kd = Q.to(DEV), K.to(DEV)
+    a = L.score_attention(Qd, Kd)
+    a = {k: v.clone() for k, v in a.items()}
+    b = L.score_attention(Qd, Kd)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("shape", [(32, 8, 512, 8192, 128), (1, 1, 512, 512, 64), (8, 2, 130, 700, 128)])
+def test_channel_weights_and_rms(shape):
+    Hq, Hkv, W, N, d = shape
+    Q, K, V = rand_layer(Hq, Hkv, W, N, d, seed=11)
+    wc = L.channel_weights(Q.to(DEV), K.to(DEV))
+    np.testing.assert_allclose(wc.cpu().numpy(), O.channel_weights(f64(Q), f64(K)), rtol=TOL)
+    st = L.unit_rms(V.to(DEV), 0)
+    np.testing.assert_allclose(st.cpu().numpy(), O.unit_rms(f64(V), 0), rtol=TOL)
+    keep = torch.rand(Hkv, N, generator=torch.Generator().manual_seed(3)) > 0.6
+    keep[0] = False
+    sc = L.unit_rms(K.to(DEV), 1, keep_bits=keep.to(torch.uint8).reshape(-1).to(DEV))
+    np.testing.assert_allclose(sc.cpu().numpy(), O.unit_rms(f64(K), 1, keep.numpy()), rtol=TOL, atol=0)
+
+
+def gpu_alloc(w, s, B, mask=L.WIDTHS_ALL):
+    bits = L.allocate_bits(torch.from_numpy(w).to(DEV), torch.from_numpy(s).to(DEV), B, mask)
+    torch.cuda.synchronize()
+    return bits.cpu().numpy()
+
+
+MASKS = {(0, 2, 4, 8, 16): L.WIDTHS_ALL, (0, 16): L.WIDTHS_KEEP_OR_EVICT, (0, 4, 16): (1 << 4) | (1 << 16),
+         (0, 2, 8): (1 << 2) | (1 << 8)}
+
+
+@pytest.mark.parametrize("U", [1, 3, 17, 1000, 70000])
+@pytest.mark.parametrize("widths", list(MASKS))
+def test_allocation_bit_exact(U, widths):
+    rng = np.random.default_rng(U + len(widths))
+    w = (rng.random(U) ** 3 * 10).astype(np.float32)
+    s = (rng.random(U) + 0.05).astype(np.float32)
+    w[rng.random(U) < 0.05] = 0                       # zero keys
+    w[::11] = w[5 % U]                                # ties
+    s[::11] = s[5 % U]
+    for avg in (0.0, 0.3, 1.7, 3.0, 4.0, 9.5, 16.0, 20.0):
+        B = int(math.floor(avg * U))
+        ref = O.allocate_bits(w, s, B, widths)
+        got = gpu_alloc(w, s, B, MASKS[widths])
+        assert (got == ref).all(), (avg, np.nonzero(got != ref)[0][:10])
+    assert L.device_error() == 0
+
+
+def test_allocation_power_of_two_ties():
+    """key_v = 4 key_u makes theta(u, 0) == theta(v, 1): ties across steps."""
+    w = np.array([1, 4, 1, 4, 2, 8, 0.5, 16, 1, 4] * 30, dtype=np.float32)
+    s = np.ones_like(w)
+    for B in range(0, 16 * w.size + 1, 7):
+        assert (gpu_alloc(w, s, B) == O.allocate_bits(w, s, B)).all(), B
+
+
+def test_allocation_rejects_bad_weights():
+    w = np.ones(100, np.float32)
+    w[7] = np.nan
+    gpu_alloc(w, np.ones(100, np.float32), 300)
+    assert L.device_error() == 3
+
+
+def _cmp_streams(dev_streams, ref):
+    got = dev_streams.host_view()
+    for wd in (2, 4, 8, 16):
+        assert (got[wd]["ids"] == ref[wd]["ids"]).all(), wd
+        assert (got[wd]["group_offsets"] == ref[wd]["group_offsets"]).all(), wd
+        assert got[wd]["n_groups"] == ref[wd]["n_groups"], wd
+        assert np.array_equal(got[wd]["codes"], ref[wd]["codes"]), wd
+        if wd != 16:
+            assert np.array_equal(got[wd]["scales"], ref[wd]["scales"]), wd
+
+
+@pytest.mark.parametrize("Hkv,N,d", [(2, 300, 128), (1, 64, 64), (3, 1000, 64), (8, 8192, 128)])
+def test_pack_dequant_bit_exact(Hkv, N, d):
+    rng = np.random.default_rng(N)
+    g = torch.Generator().manual_seed(N)
+    X = (torch.randn(Hkv, N, d, generator=g) * torch.exp(torch.randn(Hkv, N, 1, generator=g))).bfloat16()
+    X[0, 0, :] = 0                                   # an all-zero group
+    Xd = X.to(DEV)
+    x64 = f64(X)
+    # V: per token
+    bits_v = rng.choice([0, 2, 4, 8, 16], size=Hkv * N).astype(np.uint8)
+    B_v = int(bits_v.astype(int).sum())
+    st = L.Streams(Hkv, N, d, 0, B_v, DEV)
+    bv = torch.from_numpy(bits_v).to(DEV)
+    L.quantize_pack(Xd, 0, bv, None, st)
+    ref_v = O.quantize_pack(x64, 0, bits_v)
+    _cmp_streams(st, ref_v)
+    xh = L.dequantize(st, bv, None)
+    assert np.array_equal(xh.cpu().numpy(), O.dequantize(ref_v, X.shape, 0, bits_v))
+    # K: per channel over kept tokens
+    keep = (bits_v > 0).reshape(Hkv, N)
+    bits_k = rng.choice([0, 2, 4, 8, 16], size=Hkv * d).astype(np.uint8)
+    B_k = int(bits_k.astype(int).sum())
+    sk = L.Streams(Hkv, N, d, 1, B_k, DEV)
+    bk = torch.from_numpy(bits_k).to(DEV)
+    L.quantize_pack(Xd, 1, bk, bv, sk)
+    ref_k = O.quantize_pack(x64, 1, bits_k, keep)
+    _cmp_streams(sk, ref_k)
+    kh = L.dequantize(sk, bk, bv)
+    assert np.array_equal(kh.cpu().numpy(), O.dequantize(ref_k, X.shape, 1, bits_k, keep))
+    assert L.device_error() == 0
+
+
+def test_pack_scale_overflow_is_reported():
+    X = torch.zeros(1, 64, 64)
+    X[0, 3, 5] = 2.0 ** 100
+    st = L.Streams(1, 64, 64, 0, 64 * 8, DEV)
+    L.quantize_pack(X.bfloat16().to(DEV), 0, torch.full((64,), 8, dtype=torch.uint8, device=DEV), None, st)
+    assert L.device_error() == 3
+
+
+@pytest.mark.parametrize("name", ["single_head_n512_d64", "llama3_8b_layer_n8192_w512"])
+def test_pipeline_vs_oracle(name):
+    """The whole RDKV pass on the synthetic workload: scores within tolerance;
+    allocation and packing bit-exact when fed the oracle's weights."""
+    wl = synth.WORKLOADS[name]
+    t = synth.make_layer(wl)
+    Q, K, V = (t[k].to(DEV) for k in ("Q", "K", "V"))
+    avg = wl.avg_bits[0]
+    step = RdkvLayerStep(wl.Hq, wl.Hkv, wl.N, wl.W, wl.d, avg, device=DEV)
+    step.run(Q, K, V)
+    torch.cuda.synchronize()
+    assert L.device_error() == 0
+    x = {k: f64(t[k]) for k in ("Q", "K", "V")}
+    ref = O.rdkv_compress(x["Q"], x["K"], x["V"], wl.q_pos0, avg)
+    assert_lse_close(step.out["lse"].cpu().numpy(), ref["scores"]["lse"])
+    assert_scores_close(step.out["w_t"].cpu().numpy(), ref["scores"]["w_t"], "w_t")
+    np.testing.assert_allclose(step.w_c.cpu().numpy(), ref["w_c"], rtol=TOL)
+    np.testing.assert_allclose(step.sig_t.cpu().numpy(), ref["sigma_t"], rtol=TOL)
+    # stage 2/3 fed the oracle's weights
+    bits_v = gpu_alloc(ref["scores"]["w_t"].astype(np.float32).ravel(), ref["sigma_t"].ravel(), step.B_v)
+    assert (bits_v == ref["bits_v"]).all()
+    bits_k = gpu_alloc(ref["w_c"].ravel(), ref["sigma_c"].ravel(), step.B_k)
+    assert (bits_k == ref["bits_k"]).all()
+    bv, bk = torch.from_numpy(bits_v).to(DEV), torch.from_numpy(bits_k).to(DEV)
+    sv = L.Streams(wl.Hkv, wl.N, wl.d, 0, step.B_v, DEV)
+    L.quantize_pack(V, 0, bv, None, sv)
+    _cmp_streams(sv, ref["v_streams"])
+    sk = L.Streams(wl.Hkv, wl.N, wl.d, 1, step.B_k, DEV)
+    L.quantize_pack(K, 1, bk, bv, sk)
+    _cmp_streams(sk, ref["k_streams"])
+    # sigma_c on the oracle's kept set
+    sc = L.unit_rms(K, 1, keep_bits=bv)
+    np.testing.assert_allclose(sc.cpu().numpy(), ref["sigma_c"], rtol=TOL)
+    assert L.device_error() == 0
