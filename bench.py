@@ -1,0 +1,405 @@
+#!/usr/bin/env python
+"""Throughput of the RDKV hot path on one B300: KV tokens scored + compressed
+per second per layer.
+
+A step is one pass of the whole path over one (layer, sequence) pool of the
+synthetic Llama-3-8B-shaped layer (32 query heads, 8 KV heads, d = 128,
+N = 8192 keys, window of the last 512 queries, 3 bits on average):
+row LSE (pass 1), token weights (pass 2), channel weights, sigma_t, V
+allocation, sigma_c over kept tokens, K allocation, V and K quantise/pack,
+V and K dequantise.  Inputs are resident in HBM; L2 is flushed (256 MB write)
+between timed steps and the flush is not timed.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own synthetic layer (no data-path
+collective: the pools are independent) and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV tokens scored+compressed/s per layer (M tok/s) and % of tensor/HBM roofline"
+UNIT = "M tok/s"
+DEFAULT_WORKLOAD = "llama3_8b_layer_n8192_w512"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-s", type=float, default=1.0, help="untimed replays before timing (clock samples)")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# multi-process plumbing (barrier and max over ranks only; no data exchange)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_group(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def reduce_max(dist, x: float, device=None) -> float:
+    """Max of x over ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx.append(float(f[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(self.NAMES, f[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+            os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# roofline helpers
+# ---------------------------------------------------------------------------
+def pass_flops(wl) -> float:
+    """2 d flops per visible (query row, key) pair per query head; masked work not counted."""
+    pairs = wl.W * (wl.q_pos0 + 1) + wl.W * (wl.W - 1) // 2
+    return 2.0 * wl.d * pairs * wl.Hq
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("bf16_tflops"), d.get("hbm_gbs"), "measured"
+    return 1800.0, 6400.0, "fallback"
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    cdir = os.path.join(ROOT, "kv_cache_compression_flash_b300", "csrc")
+    for f in sorted(os.listdir(cdir)):
+        h.update(open(os.path.join(cdir, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on this source."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    cur = csrc_hash()
+    for line in open(PROFILE_TRAFFIC):
+        f = line.split()
+        if len(f) == 4 and f[0] == kernel and f[1] == workload and f[3] == cur:
+            return float(f[2])
+    return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+def oracle_cores():
+    """Threads the oracle uses: its BLAS pool (elementwise NumPy work is single-threaded)."""
+    import numpy as np
+    np.ones((64, 64)) @ np.ones((64, 64))           # loads the BLAS library
+    try:
+        import threadpoolctl
+        blas = [i["num_threads"] for i in threadpoolctl.threadpool_info() if i.get("user_api") == "blas"]
+        if blas:
+            return max(blas)
+    except ImportError:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def oracle_group_step(wl, host, g):
+    """The oracle's RDKV pass over KV group g alone (G query heads, one KV head)."""
+    import numpy as np
+    import oracle as O
+    G = wl.G
+    Q = host["Q"][g * G:(g + 1) * G].float().numpy().astype(np.float64)
+    Kx = host["K"][g:g + 1].float().numpy().astype(np.float64)
+    Vx = host["V"][g:g + 1].float().numpy().astype(np.float64)
+    O.rdkv_compress(Q, Kx, Vx, wl.q_pos0, wl.avg_bits[0])
+
+
+def time_oracle(wl, host, min_seconds=10.0):
+    """Runs the oracle group by group until min_seconds; returns (layer tokens/s, groups, seconds)."""
+    groups, t0 = 0, time.perf_counter()
+    while True:
+        oracle_group_step(wl, host, groups % wl.Hkv)
+        groups += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return wl.N * groups / wl.Hkv / dt, groups, dt
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "Hq": wl.Hq, "Hkv": wl.Hkv, "N": wl.N, "W": wl.W, "d": wl.d,
+            "avg_bits": wl.avg_bits[0], "widths": list(wl.widths), "pools_per_step_per_gpu": 1,
+            "l2": "flushed between timed steps (256 MB write, untimed)", "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from kv_cache_compression_flash_b300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    host = synth.make_layer(wl, layer=0)
+    for i in range(args.warmup):
+        oracle_group_step(wl, host, i % wl.Hkv)
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_group_step(wl, host, i % wl.Hkv)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = wl.N / wl.Hkv * args.steps / total / 1e6
+    sample = (f"each step = the fp64 oracle's full RDKV pass (scores, weights, allocation, packing) over one "
+              f"KV group ({wl.G} query heads, 1 of {wl.Hkv} KV heads, N={wl.N}, W={wl.W}); "
+              f"counted as N/Hkv layer tokens")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    from kv_cache_compression_flash_b300 import _lib as L
+    from kv_cache_compression_flash_b300 import synth
+    from kv_cache_compression_flash_b300.pipeline import RdkvLayerStep
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_group(world, "nccl")
+    L.lib()
+
+    wl = synth.WORKLOADS[args.workload]
+    host = synth.make_layer(wl, layer=rank)                  # each rank: its own pool
+    pinned = {k: host[k].pin_memory() for k in ("Q", "K", "V")}
+    Q, K, V = (pinned[k].to(dev) for k in ("Q", "K", "V"))
+    step = RdkvLayerStep(wl.Hq, wl.Hkv, wl.N, wl.W, wl.d, wl.avg_bits[0], device=dev)
+    step.capture(Q, K, V)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step.replay()
+    torch.cuda.synchronize()
+    if L.device_error() != 0:
+        raise SystemExit("device error during warm-up")
+
+    clocks = ClockSampler(local).start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak_s:  # clocks under load before the timed region
+        for _ in range(20):
+            flush.zero_()
+            step.replay()
+        torch.cuda.synchronize()
+
+    barrier(dist, dev)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        step.replay(evs[i])
+    torch.cuda.synchronize()
+    barrier(dist, dev)
+    clk = clocks.stop()
+    if L.device_error() != 0:
+        raise SystemExit("device error during the timed region")
+
+    seg = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)] for i in range(args.steps)]
+    step_ms = [sum(s) for s in seg]
+    total_s = reduce_max(dist, sum(step_ms) / 1e3, dev)
+    value = world * args.steps * wl.N / total_s / 1e6
+    seg_avg = [statistics.fmean(s[j] for s in seg) for j in range(3)]
+
+    # ---- roofline of the dominant kernel (the slower scoring pass) -------------
+    peak_tf, _, peak_kind = measured_peaks()
+    dom = 0 if seg_avg[0] >= seg_avg[1] else 1
+    kname = ("lse_pass_kernel", "colreduce_pass_kernel")[dom]
+    achieved = pass_flops(wl) / (seg_avg[dom] / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved / peak_tf if peak_tf else None, "peak_kind": f"{peak_kind} bf16 burst",
+                "traffic": recorded_traffic(kname, wl.name),
+                "duration_note": "segment time: the pass kernel plus its small merge kernel"}
+
+    e2e = run_e2e(args, step, pinned, (Q, K, V), flush, dist, dev, world, wl)
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": statistics.fmean(step_ms), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(wl),
+        "segments_ms": {"pass1_lse": seg_avg[0], "pass2_token_weights": seg_avg[1], "rest": seg_avg[2]},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": step.kernel_launches() * args.steps,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                   "samples": clk["samples"], "window": "1 s soak of the same step, then the timed steps"},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, groups, dt = time_oracle(wl, host)
+        out["cpu_baseline"] = {"value": v / 1e6, "unit": UNIT, "cores": oracle_cores(), "kind": "oracle",
+                               "sample": f"{groups} KV groups of this layer through the fp64 oracle in {dt:.1f} s "
+                                         f"(one group = {wl.G} query heads x 1 KV head; N/Hkv tokens each)"}
+    if rank == 0:
+        print(json.dumps(out))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, step, pinned, dev_inputs, flush, dist, dev, world, wl):
+    """Pinned host Q, K, V in; the packed streams and widths a caller keeps, out."""
+    import torch
+    Q, K, V = dev_inputs
+    h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in ("Q", "K", "V"))
+    streams = (step.v_streams, step.k_streams)
+    land = {"bits_v": torch.empty(step.bits_v.numel(), dtype=torch.uint8, pin_memory=True),
+            "bits_k": torch.empty(step.bits_k.numel(), dtype=torch.uint8, pin_memory=True),
+            "counts": [torch.empty(8, dtype=torch.int64, pin_memory=True) for _ in streams],
+            "streams": [[tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                               for t in (s.codes[i], s.scales[i], s.ids[i], s.goff[i])) for i in range(4)]
+                        for s in streams]}
+    times, d2h = [], 0
+    barrier(dist, dev)
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        Q.copy_(pinned["Q"], non_blocking=True)
+        K.copy_(pinned["K"], non_blocking=True)
+        V.copy_(pinned["V"], non_blocking=True)
+        step.replay()
+        nbytes = 0
+        for j, s in enumerate(streams):
+            land["counts"][j].copy_(s.counts, non_blocking=True)
+            nbytes += 64
+        land["bits_v"].copy_(step.bits_v, non_blocking=True)
+        land["bits_k"].copy_(step.bits_k, non_blocking=True)
+        nbytes += step.bits_v.numel() + step.bits_k.numel()
+        torch.cuda.synchronize()
+        for j, s in enumerate(streams):
+            c = land["counts"][j].tolist()
+            for i, wd in enumerate((2, 4, 8, 16)):
+                nu, ng = c[i], c[4 + i]
+                lc, ls, li, lg = land["streams"][j][i]
+                lc[:ng * 8 * wd].copy_(s.codes[i][:ng * 8 * wd], non_blocking=True)
+                li[:nu].copy_(s.ids[i][:nu], non_blocking=True)
+                lg[:nu].copy_(s.goff[i][:nu], non_blocking=True)
+                nbytes += ng * 8 * wd + nu * 12
+                if wd != 16:
+                    ls[:ng].copy_(s.scales[i][:ng], non_blocking=True)
+                    nbytes += ng * 2
+        torch.cuda.synchronize()
+        times.append(time.perf_counter() - t0)
+        d2h = nbytes
+    barrier(dist, dev)
+    total = reduce_max(dist, sum(times), dev)
+    return {"value": world * args.steps * wl.N / total / 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "path": "pinned host Q,K,V -> device, graph replay of the C-ABI calls, packed streams + widths -> host"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

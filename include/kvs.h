@@ -75,6 +75,8 @@ int kvs_get_device_error(void* stream);
 #define KVS_MODE_KVZIP       4u  /* s_plus[Hkv, N] = max over heads and rows of a_{r,t}  [KVzap §2.1, KVzip] */
 #define KVS_MODE_KVZIP_PLUS  8u  /* s_plus[Hkv, N] = max_heads max_r a^h_{r,t} |h_r| / |W_O^h v_t|
                                                                                      [KVzap §2.1, KVzip+] */
+#define KVS_MODE_LSE_GIVEN  16u  /* lse is an INPUT (from an earlier call): pass 1 is skipped and pass 2
+                                    reuses it.  Lets a caller time or schedule the two passes apart. */
 
 /* Bytes of workspace kvs_score_attention needs for these sizes and mode. */
 size_t kvs_score_workspace_size(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d,
@@ -84,7 +86,8 @@ size_t kvs_score_workspace_size(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, i
  * attention matrix.  Pass 1 computes every window row's log-sum-exp; pass 2
  * recomputes the probabilities a = exp(s - lse) and reduces them per key.
  *   mode    : KVS_MODE_LSE is implied; add KVS_MODE_RDKV_WT and at most one of
- *             KVS_MODE_KVZIP / KVS_MODE_KVZIP_PLUS.
+ *             KVS_MODE_KVZIP / KVS_MODE_KVZIP_PLUS; with KVS_MODE_LSE_GIVEN the
+ *             lse buffer is read instead of written.
  *   Q, K    : bf16, required.  V, h, W_O: bf16, required for KVZIP_PLUS only
  *             (D = hidden size, ignored otherwise).
  *   lse     : float [Hq, W], natural log, required.

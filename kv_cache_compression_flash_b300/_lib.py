@@ -24,6 +24,7 @@ MODE_LSE = 1
 MODE_RDKV_WT = 2
 MODE_KVZIP = 4
 MODE_KVZIP_PLUS = 8
+MODE_LSE_GIVEN = 16
 
 WIDTHS_ALL = (1 << 2) | (1 << 4) | (1 << 8) | (1 << 16)
 WIDTHS_KEEP_OR_EVICT = 1 << 16
@@ -143,6 +144,8 @@ def score_attention(Q, K, *, q_pos0=None, mode=MODE_LSE | MODE_RDKV_WT, V=None, 
     dev = Q.device
     out = {} if out is None else out
     lse = out.get("lse")
+    if lse is None and mode & MODE_LSE_GIVEN:
+        raise KvsError("MODE_LSE_GIVEN needs out['lse'] as input")
     if lse is None:
         lse = out["lse"] = torch.empty(Hq, W, dtype=torch.float32, device=dev)
     w_t = s_plus = None

@@ -104,8 +104,28 @@ __device__ __forceinline__ bool cand_better(const FixCand& a, const FixCand& b) 
   return a.u < b.u;
 }
 
+// first candidate in item order over the block (result valid in every thread)
+__device__ __forceinline__ FixCand block_best(FixCand best, FixCand* s_cand) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    FixCand o_c;
+    o_c.theta = __shfl_xor_sync(0xFFFFFFFFu, best.theta, o);
+    o_c.u = __shfl_xor_sync(0xFFFFFFFFu, best.u, o);
+    o_c.cost = __shfl_xor_sync(0xFFFFFFFFu, best.cost, o);
+    o_c.pad_ = 0;
+    if (o_c.theta != 0ull && (best.theta == 0ull || cand_better(o_c, best))) best = o_c;
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) s_cand[threadIdx.x >> 5] = best;
+  __syncthreads();
+  FixCand bb = s_cand[0];
+  for (int i = 1; i < (kAllocThreads >> 5); ++i)
+    if (s_cand[i].theta != 0ull && (bb.theta == 0ull || cand_better(s_cand[i], bb))) bb = s_cand[i];
+  return bb;
+}
+
 __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocParams p) {
-  __shared__ unsigned long long s_hist[256];
+  __shared__ unsigned s_hist[256];  // per-block cost per bin (< 2^32: units per block x 16)
   __shared__ unsigned long long s_red[kAllocThreads / 32];
   __shared__ unsigned long long s_sel_above;
   __shared__ int s_sel;
@@ -162,30 +182,38 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
     const int shift = 56 - 8 * pass;
     s_hist[tid] = 0;  // kAllocThreads == 256 bins
     __syncthreads();
-    for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) {
-      const double key = static_cast<double>(p.w[u]) * static_cast<double>(p.sigma[u]);
-      if (key <= 0.0) continue;
+    // Early passes see the exponent bits, which nearly all thetas share: the
+    // lanes of a warp that fall in one bin are merged first (match_any), so a
+    // bin takes one atomic per warp and step instead of one per item.
+    for (long long base = u_begin; base < u_end; base += kAllocThreads) {
+      const long long u = base + tid;
+      double key = 0.0;
+      if (u < u_end) key = static_cast<double>(p.w[u]) * static_cast<double>(p.sigma[u]);
       for (int k = 0; k < p.K; ++k) {
         const unsigned long long v = static_cast<unsigned long long>(__double_as_longlong(p.c[k] * key));
-        if ((v & pmask) == prefix) atomicAdd(&s_hist[(v >> shift) & 255ull], static_cast<unsigned long long>(p.cost[k]));
+        const unsigned bin =
+            (key > 0.0 && (v & pmask) == prefix) ? static_cast<unsigned>((v >> shift) & 255ull) : 256u;
+        const unsigned grp = __match_any_sync(0xFFFFFFFFu, bin);
+        if (bin != 256u && (tid & 31) == __ffs(grp) - 1)
+          atomicAdd(&s_hist[bin], static_cast<unsigned>(__popc(grp) * p.cost[k]));
       }
     }
     __syncthreads();
-    if (s_hist[tid]) atomicAdd(&H->hist[pass][tid], s_hist[tid]);
+    if (s_hist[tid]) atomicAdd(&H->hist[pass][tid], static_cast<unsigned long long>(s_hist[tid]));
     if (!grid_barrier(&H->sync, nb)) return;
-    if (tid == 0) {
-      unsigned long long a = above;
-      int sel = 0;
-      for (int dgt = 255; dgt >= 0; --dgt) {
-        const unsigned long long h = ld_vol(&H->hist[pass][dgt]);
-        if (a + h > p.B) {
-          sel = dgt;
-          break;
-        }
-        a += h;
+    {
+      // thread i looks at digit 255 - i; an inclusive scan gives the cost of
+      // every item at or above that digit; the first thread whose total
+      // exceeds the budget owns the digit of lambda*
+      const unsigned long long h = ld_vol(&H->hist[pass][255 - tid]);
+      unsigned long long block_total;
+      const unsigned long long incl = block_exscan(h, s_red, &block_total) + h;
+      const bool over = above + incl > p.B;
+      const int first = __syncthreads_count(!over);  // over is monotone in tid
+      if (tid == first) {
+        s_sel = 255 - tid;
+        s_sel_above = above + incl - h;
       }
-      s_sel = sel;
-      s_sel_above = a;
     }
     __syncthreads();
     prefix |= static_cast<unsigned long long>(s_sel) << shift;
@@ -207,13 +235,11 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
   if (tid == 0) p.tie_block[b] = blk_tie;
   if (!grid_barrier(&H->sync, nb)) return;
   unsigned long long carry = above;
-  if (tid == 0) {
+  {
     unsigned long long e = 0;
-    for (int i = 0; i < b; ++i) e += ld_vol(&p.tie_block[i]);
-    s_sel_above = e;
+    for (int i = tid; i < b; i += kAllocThreads) e += ld_vol(&p.tie_block[i]);
+    carry += block_sum(e, s_red);
   }
-  __syncthreads();
-  carry += s_sel_above;
   for (long long base = u_begin; base < u_end; base += kAllocThreads) {
     const long long u = base + tid;
     int lvl = 0;
@@ -256,33 +282,21 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
       FixCand c = {static_cast<unsigned long long>(__double_as_longlong(th)), u, p.cost[lvl], 0};
       if (best.theta == 0ull || cand_better(c, best)) best = c;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      FixCand o_c;
-      o_c.theta = __shfl_xor_sync(0xFFFFFFFFu, best.theta, o);
-      o_c.u = __shfl_xor_sync(0xFFFFFFFFu, best.u, o);
-      o_c.cost = __shfl_xor_sync(0xFFFFFFFFu, best.cost, o);
-      o_c.pad_ = 0;
-      if (o_c.theta != 0ull && (best.theta == 0ull || cand_better(o_c, best))) best = o_c;
-    }
-    if ((tid & 31) == 0) s_cand[tid >> 5] = best;
-    __syncthreads();
-    if (tid == 0) {
-      FixCand bb = s_cand[0];
-      for (int i = 1; i < (kAllocThreads >> 5); ++i)
-        if (s_cand[i].theta != 0ull && (bb.theta == 0ull || cand_better(s_cand[i], bb))) bb = s_cand[i];
-      p.cand[it * nb + b] = bb;
-    }
+    best = block_best(best, s_cand);
+    if (tid == 0) p.cand[it * nb + b] = best;
     if (!grid_barrier(&H->sync, nb)) return;
-    if (tid == 0) {
+    {
       FixCand bb = {0ull, 0ll, 0, 0};
-      for (int i = 0; i < nb; ++i) {
+      for (int i = tid; i < nb; i += kAllocThreads) {
         const volatile FixCand* vc = &p.cand[it * nb + i];
         FixCand c2 = {vc->theta, vc->u, vc->cost, 0};
         if (c2.theta != 0ull && (bb.theta == 0ull || cand_better(c2, bb))) bb = c2;
       }
-      s_best = bb;
-      s_flag = bb.theta != 0ull;
+      bb = block_best(bb, s_cand);
+      if (tid == 0) {
+        s_best = bb;
+        s_flag = bb.theta != 0ull;
+      }
     }
     __syncthreads();
     if (!s_flag) break;

@@ -74,7 +74,7 @@ struct ScorePlan {
   int kt_chunk, n_split1;
   int qt_chunk, n_split2;
   int gram_slice_len;
-  bool want_wt, want_max, want_plus;
+  bool want_wt, want_max, want_plus, lse_given;
 };
 
 int validate_shape(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t q_pos0) {
@@ -92,7 +92,7 @@ int plan_score(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t
                uint32_t mode, ScorePlan* pl) {
   int st = validate_shape(Hq, Hkv, W, N, d, q_pos0);
   if (st) return st;
-  if ((mode & ~(KVS_MODE_LSE | KVS_MODE_RDKV_WT | KVS_MODE_KVZIP | KVS_MODE_KVZIP_PLUS)) != 0)
+  if ((mode & ~(KVS_MODE_LSE | KVS_MODE_RDKV_WT | KVS_MODE_KVZIP | KVS_MODE_KVZIP_PLUS | KVS_MODE_LSE_GIVEN)) != 0)
     return KVS_ERR_INVALID_ARG;
   if ((mode & KVS_MODE_KVZIP) && (mode & KVS_MODE_KVZIP_PLUS)) return KVS_ERR_INVALID_ARG;
   if ((mode & KVS_MODE_KVZIP_PLUS) && (D <= 0 || D % 8 != 0)) return KVS_ERR_INVALID_ARG;
@@ -115,6 +115,7 @@ int plan_score(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t
   pl->want_wt = (mode & KVS_MODE_RDKV_WT) != 0;
   pl->want_plus = (mode & KVS_MODE_KVZIP_PLUS) != 0;
   pl->want_max = (mode & (KVS_MODE_KVZIP | KVS_MODE_KVZIP_PLUS)) != 0;
+  pl->lse_given = (mode & KVS_MODE_LSE_GIVEN) != 0;
   const long long target = static_cast<long long>(sm_count()) * 2 * 4;
   long long w1 = 0;
   for (int pb = 0; pb < g.n_pb; ++pb) w1 += pb_nkt(g, pb);
@@ -145,7 +146,7 @@ struct ScoreWs {
 size_t carve_score(const ScorePlan& pl, void* base, size_t cap, ScoreWs* w) {
   WsCarver c{static_cast<char*>(base), 0, cap};
   const ScoreGeom& g = pl.geo;
-  w->part1 = c.take<float2>(static_cast<size_t>(g.n_rt) * pl.n_split1 * 128);
+  w->part1 = pl.lse_given ? nullptr : c.take<float2>(static_cast<size_t>(g.n_rt) * pl.n_split1 * 128);
   w->b_plain = (pl.want_wt || (pl.want_max && !pl.want_plus)) ? c.take<float>(static_cast<size_t>(g.n_rt) * 128)
                                                               : nullptr;
   w->b_scaled = pl.want_plus ? c.take<float>(static_cast<size_t>(g.n_rt) * 128) : nullptr;
@@ -223,10 +224,14 @@ int score_dh(const ScorePlan& pl, const uint16_t* Q, const uint16_t* K, const ui
     vnorm_kernel<DH><<<dim3(static_cast<unsigned>(cdiv(g.N, 64)), g.Hq), 256, vsmem, st>>>(
         V, w.gram, kGramSlices, g.Hq, g.G, g.N, w.vn);
   }
-  rc = launch_lse<DH>(pl, mq, mk, w.part1, st);
-  if (rc) return rc;
-  lse_finalize_kernel<<<g.n_rt, 128, 0, st>>>(g, pl.kt_chunk, pl.n_split1, w.part1, w.hn, lse, w.b_plain,
-                                               w.b_scaled);
+  if (pl.lse_given) {
+    if (w.b_plain || w.b_scaled) lse_offsets_kernel<<<g.n_rt, 128, 0, st>>>(g, lse, w.hn, w.b_plain, w.b_scaled);
+  } else {
+    rc = launch_lse<DH>(pl, mq, mk, w.part1, st);
+    if (rc) return rc;
+    lse_finalize_kernel<<<g.n_rt, 128, 0, st>>>(g, pl.kt_chunk, pl.n_split1, w.part1, w.hn, lse, w.b_plain,
+                                                 w.b_scaled);
+  }
   if (pl.want_wt) {
     rc = launch_col<DH, false>(pl, mq, mk, w.b_plain, nullptr, w_t, w.part_sum, st);
     if (rc) return rc;
@@ -241,6 +246,7 @@ int score_dh(const ScorePlan& pl, const uint16_t* Q, const uint16_t* K, const ui
 
 // ---- allocation ---------------------------------------------------------------
 int alloc_blocks_max() { return sm_count() * 8; }
+constexpr long long kAllocUnitsPerBlock = 2048;
 
 size_t alloc_ws_bytes(int nb) {
   WsCarver c{nullptr, 0, 0};
@@ -416,7 +422,8 @@ int kvs_score_plan_info(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d
   info[2] = pl.qt_chunk;
   info[3] = pl.n_split2;
   const int per_col = 1 + (pl.n_split2 > 1 ? 1 : 0);
-  info[4] = (pl.want_plus ? 3 : 0) + 2 + (pl.want_wt ? per_col : 0) + (pl.want_max ? per_col : 0);
+  const int head = pl.lse_given ? ((pl.want_wt || pl.want_max) ? 1 : 0) : 2;
+  info[4] = (pl.want_plus ? 3 : 0) + head + (pl.want_wt ? per_col : 0) + (pl.want_max ? per_col : 0);
   return KVS_OK;
 }
 
@@ -475,7 +482,7 @@ int kvs_channel_weights(const uint16_t* Q, const uint16_t* K, int64_t Hq, int64_
     colsumsq_kernel<128><<<gk, kNormThreads, 0, st>>>(K, static_cast<int>(N), nullptr, kp, nullptr);
   }
   const int n = static_cast<int>(Hkv * d);
-  channel_weight_finalize_kernel<<<static_cast<int>(cdiv(n, 256)), 256, 0, st>>>(
+  channel_weight_finalize_kernel<<<static_cast<int>(cdiv(n, 8)), 256, 0, st>>>(
       qp, static_cast<int>(nq), kp, static_cast<int>(nk), static_cast<int>(Hkv), static_cast<int>(d),
       static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))), w_c);
   KVS_CUDA_TRY(cudaGetLastError());
@@ -519,7 +526,7 @@ int kvs_unit_rms(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis,
     else
       colsumsq_kernel<128><<<grid, kNormThreads, 0, st>>>(X, static_cast<int>(N), keep_bits, part, cnt);
     const int n = static_cast<int>(Hkv * d);
-    masked_rms_finalize_kernel<<<static_cast<int>(cdiv(n, 256)), 256, 0, st>>>(
+    masked_rms_finalize_kernel<<<static_cast<int>(cdiv(n, 8)), 256, 0, st>>>(
         part, cnt, static_cast<int>(nk), static_cast<int>(Hkv), static_cast<int>(d), sigma);
   }
   KVS_CUDA_TRY(cudaGetLastError());
@@ -559,7 +566,9 @@ int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t bud
   int occ = 0;
   KVS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, allocate_kernel, kAllocThreads, 0));
   const int nb_cap = std::min(std::max(occ, 1) * sm_count(), alloc_blocks_max());
-  const int nb = static_cast<int>(std::max<long long>(1, std::min<long long>(nb_cap, cdiv(U, kAllocThreads))));
+  // a few thousand units per block: fewer blocks make every grid barrier cheaper
+  const int nb = static_cast<int>(std::max<long long>(1, std::min<long long>(nb_cap, cdiv(U, kAllocUnitsPerBlock))));
+  if (cdiv(U, nb) * 16 >= (1ll << 32)) return KVS_ERR_UNSUPPORTED;  // per-block histogram counts are 32-bit
   WsCarver c{static_cast<char*>(workspace), 0, workspace_bytes};
   p.hdr = c.take<AllocHeader>(1);
   p.tie_block = c.take<unsigned long long>(nb);

@@ -11,7 +11,7 @@
 namespace kvs {
 
 constexpr int kNormThreads = 256;
-constexpr int kColChunkRows = 256;
+constexpr int kColChunkRows = 64;
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&f)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -41,14 +41,23 @@ __global__ void __launch_bounds__(kNormThreads) colsumsq_kernel(const uint16_t* 
   for (int k = 0; k < 8; ++k) acc[k] = 0.f;
   int n = 0;
   const size_t gbase = static_cast<size_t>(g) * rows;
-  for (int r = r_begin + rsub; r < r_end; r += RPI) {
-    if (keep && keep[gbase + r] == 0) continue;
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(X + (gbase + r) * DH + cseg));
-    float f[8];
-    bf16x8_to_f32(u, f);
+  for (int base = r_begin + rsub; base < r_end; base += 4 * RPI) {
+    uint4 u[4];
+    bool ok[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] = fmaf(f[k], f[k], acc[k]);
-    ++n;
+    for (int j = 0; j < 4; ++j) {  // four independent loads in flight
+      const int r = base + j * RPI;
+      ok[j] = r < r_end && (keep == nullptr || keep[gbase + r] != 0);
+      u[j] = ok[j] ? __ldg(reinterpret_cast<const uint4*>(X + (gbase + r) * DH + cseg)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float f[8];
+      bf16x8_to_f32(u[j], f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] = fmaf(f[k], f[k], acc[k]);
+      n += ok[j] ? 1 : 0;
+    }
   }
 #pragma unroll
   for (int k = 0; k < 8; ++k) red[rsub][cseg + k] = acc[k];
@@ -66,33 +75,42 @@ __global__ void __launch_bounds__(kNormThreads) colsumsq_kernel(const uint16_t* 
   }
 }
 
-// w_c[g][c] = sqrt(sum_q) * sqrt(sum_k) * inv_sqrt_d, chunk partials summed in order
+// sum of the chunk partials of column (g, c): one warp, lane-strided, then a
+// fixed xor tree (deterministic)
+__device__ __forceinline__ float warp_sum_partials(const float* __restrict__ part, const int nchunk, const int g,
+                                                   const int c, const int d) {
+  float s = 0.f;
+  for (int i = threadIdx.x & 31; i < nchunk; i += 32) s += part[(static_cast<size_t>(g) * nchunk + i) * d + c];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+  return s;
+}
+
+// w_c[g][c] = sqrt(sum_q) * sqrt(sum_k) * inv_sqrt_d; one warp per output
 __global__ void channel_weight_finalize_kernel(const float* __restrict__ qpart, const int nq,
                                                const float* __restrict__ kpart, const int nk, const int Hkv,
                                                const int d, const float inv_sqrt_d, float* __restrict__ w_c) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  const int idx = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (idx >= Hkv * d) return;
   const int g = idx / d, c = idx % d;
-  float sq = 0.f, sk = 0.f;
-  for (int i = 0; i < nq; ++i) sq += qpart[(static_cast<size_t>(g) * nq + i) * d + c];
-  for (int i = 0; i < nk; ++i) sk += kpart[(static_cast<size_t>(g) * nk + i) * d + c];
-  w_c[idx] = sqrtf(sq) * sqrtf(sk) * inv_sqrt_d;
+  const float sq = warp_sum_partials(qpart, nq, g, c, d);
+  const float sk = warp_sum_partials(kpart, nk, g, c, d);
+  if ((threadIdx.x & 31) == 0) w_c[idx] = sqrtf(sq) * sqrtf(sk) * inv_sqrt_d;
 }
 
-// sigma[g][c] = sqrt(sum / kept), 0 when no token is kept
+// sigma[g][c] = sqrt(sum / kept), 0 when no token is kept; one warp per output
 __global__ void masked_rms_finalize_kernel(const float* __restrict__ part, const int* __restrict__ cnt,
                                            const int nchunk, const int Hkv, const int d,
                                            float* __restrict__ sigma) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  const int idx = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (idx >= Hkv * d) return;
   const int g = idx / d, c = idx % d;
-  float s = 0.f;
+  const float s = warp_sum_partials(part, nchunk, g, c, d);
   int n = 0;
-  for (int i = 0; i < nchunk; ++i) {
-    s += part[(static_cast<size_t>(g) * nchunk + i) * d + c];
-    n += cnt[g * nchunk + i];
-  }
-  sigma[idx] = n > 0 ? sqrtf(s / static_cast<float>(n)) : 0.f;
+  for (int i = threadIdx.x & 31; i < nchunk; i += 32) n += cnt[g * nchunk + i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, o);
+  if ((threadIdx.x & 31) == 0) sigma[idx] = n > 0 ? sqrtf(s / static_cast<float>(n)) : 0.f;
 }
 
 // sigma[row] = sqrt(mean_c X[row][c]^2); DH/8 threads per row

@@ -274,6 +274,20 @@ __global__ void lse_finalize_kernel(const ScoreGeom geo, const int kt_chunk, con
   if (b_scaled) b_scaled[static_cast<size_t>(rt) * 128 + row] = valid ? l2 - lg2_approx(hn[r]) : INFINITY;
 }
 
+// Pass-2 offsets from a given lse (natural log, [Hq, W]), same layout as above.
+__global__ void lse_offsets_kernel(const ScoreGeom geo, const float* __restrict__ lse, const float* __restrict__ hn,
+                                   float* __restrict__ b_plain, float* __restrict__ b_scaled) {
+  const int rt = blockIdx.x, row = threadIdx.x;
+  const int pb = rt % geo.n_pb;
+  const int gh = rt / geo.n_pb;
+  const int g = gh / geo.n_hc, hc = gh % geo.n_hc;
+  const int hl = row / geo.P, r = pb * geo.P + row % geo.P;
+  const bool valid = r < geo.W;
+  const float l2 = valid ? lse[static_cast<size_t>(g * geo.G + hc * geo.Gt + hl) * geo.W + r] * kLog2e : 0.f;
+  if (b_plain) b_plain[static_cast<size_t>(rt) * 128 + row] = valid ? l2 : INFINITY;
+  if (b_scaled) b_scaled[static_cast<size_t>(rt) * 128 + row] = valid ? l2 - lg2_approx(hn[r]) : INFINITY;
+}
+
 // ---------------------------------------------------------------------------
 // pass 2: per-key reductions over queries (K-stationary)
 // ---------------------------------------------------------------------------

@@ -5,7 +5,7 @@ tokens, then packing (and optionally dequantisation), each step a call into
 libkvs.so.   [RDKV §2.2 pipeline; §2.3 TriZone streams]
 
 Buffers are allocated once per shape so a step allocates nothing and can be
-replayed inside a CUDA graph.
+replayed from CUDA graphs.
 """
 from __future__ import annotations
 
@@ -17,7 +17,14 @@ from . import _lib as K_
 
 
 class RdkvLayerStep:
-    """Preallocated outputs and workspaces for one pool shape."""
+    """Preallocated outputs and workspaces for one pool shape.
+
+    run() = pass1() + pass2() + rest(): pass 1 computes the row LSE, pass 2
+    the token weights from it, rest() everything after scoring.
+    """
+
+    PASS2_MODE = K_.MODE_RDKV_WT | K_.MODE_LSE_GIVEN
+    SEGMENTS = ("pass1", "pass2", "rest")
 
     def __init__(self, Hq, Hkv, N, W, d, avg_bits, device="cuda", width_mask=K_.WIDTHS_ALL, dequant=True):
         self.shape = (Hq, Hkv, N, W, d)
@@ -38,11 +45,13 @@ class RdkvLayerStep:
         self.k_streams = K_.Streams(Hkv, N, d, 1, self.B_k, dev)
         self.v_hat = torch.empty(Hkv, N, d, **f32) if dequant else None
         self.k_hat = torch.empty(Hkv, N, d, **f32) if dequant else None
-        self.ws = {k: K_.Workspace() for k in ("score", "cw", "rms0", "rms1", "av", "ak", "pv", "pk", "dv", "dk")}
-        # size every workspace now so run() allocates nothing
+        names = ("score", "score2", "cw", "rms0", "rms1", "av", "ak", "pv", "pk", "dv", "dk")
+        self.ws = {k: K_.Workspace() for k in names}
+        # size every workspace now so a step allocates nothing
         L = K_.lib()
         sizes = {
-            "score": L.kvs_score_workspace_size(Hq, Hkv, W, N, d, 0, N - W, K_.MODE_LSE | K_.MODE_RDKV_WT),
+            "score": L.kvs_score_workspace_size(Hq, Hkv, W, N, d, 0, N - W, K_.MODE_LSE),
+            "score2": L.kvs_score_workspace_size(Hq, Hkv, W, N, d, 0, N - W, self.PASS2_MODE),
             "cw": L.kvs_channel_weights_workspace_size(Hq, Hkv, W, N, d),
             "rms0": 256, "rms1": L.kvs_unit_rms_workspace_size(Hkv, N, d, 1),
             "av": L.kvs_allocate_workspace_size(self.U_v), "ak": L.kvs_allocate_workspace_size(self.U_k),
@@ -51,11 +60,13 @@ class RdkvLayerStep:
         }
         for k, n in sizes.items():
             self.ws[k].get(n, dev)
+        self.graphs = None
 
-    # number of kernels one run() launches (memset nodes excluded)
     def kernel_launches(self) -> int:
+        """Kernels one step launches (memset nodes excluded)."""
         Hq, Hkv, N, W, d = self.shape
-        n = K_.score_plan_info(Hq, Hkv, W, N, d, mode=K_.MODE_LSE | K_.MODE_RDKV_WT)[4]
+        n = K_.score_plan_info(Hq, Hkv, W, N, d, mode=K_.MODE_LSE)[4]
+        n += K_.score_plan_info(Hq, Hkv, W, N, d, mode=self.PASS2_MODE)[4]
         n += 3          # channel weights: 2 column passes + finalize
         n += 1          # sigma_t
         n += 1 + 2      # V allocation, sigma_c (pass + finalize)
@@ -65,11 +76,17 @@ class RdkvLayerStep:
             n += 4 + 4  # V dequant (count, scan, rank, dequant), K dequant (kept, plan, zero, dequant)
         return n
 
-    def run(self, Q, K, V, stream=None):
+    def pass1(self, Q, K, V, stream=None):
         Hq, Hkv, N, W, d = self.shape
-        ws = self.ws
-        K_.score_attention(Q, K, q_pos0=N - W, mode=K_.MODE_LSE | K_.MODE_RDKV_WT, out=self.out, ws=ws["score"],
+        K_.score_attention(Q, K, q_pos0=N - W, mode=K_.MODE_LSE, out=self.out, ws=self.ws["score"], stream=stream)
+
+    def pass2(self, Q, K, V, stream=None):
+        Hq, Hkv, N, W, d = self.shape
+        K_.score_attention(Q, K, q_pos0=N - W, mode=self.PASS2_MODE, out=self.out, ws=self.ws["score2"],
                            stream=stream)
+
+    def rest(self, Q, K, V, stream=None):
+        ws = self.ws
         K_.channel_weights(Q, K, out=self.w_c, ws=ws["cw"], stream=stream)
         K_.unit_rms(V, 0, out=self.sig_t, ws=ws["rms0"], stream=stream)
         K_.allocate_bits(self.out["w_t"], self.sig_t, self.B_v, self.width_mask, out=self.bits_v, ws=ws["av"],
@@ -82,4 +99,38 @@ class RdkvLayerStep:
         if self.dequant:
             K_.dequantize(self.v_streams, self.bits_v, None, out=self.v_hat, ws=ws["dv"], stream=stream)
             K_.dequantize(self.k_streams, self.bits_k, self.bits_v, out=self.k_hat, ws=ws["dk"], stream=stream)
+
+    def run(self, Q, K, V, stream=None):
+        self.pass1(Q, K, V, stream)
+        self.pass2(Q, K, V, stream)
+        self.rest(Q, K, V, stream)
+        return self
+
+    # ---- CUDA graphs: one per segment, so a replay launches no Python -------
+    def capture(self, Q, K, V):
+        """Records pass1 / pass2 / rest as three CUDA graphs over these buffers."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                self.run(Q, K, V)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graphs = {}
+        for name in self.SEGMENTS:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="relaxed"):
+                getattr(self, name)(Q, K, V)
+            self.graphs[name] = g
+        torch.cuda.synchronize()
+        return self
+
+    def replay(self, events=None):
+        """Replays the captured step; `events` (4 CUDA events) bracket the segments."""
+        if events is not None:
+            events[0].record()
+        for i, name in enumerate(self.SEGMENTS):
+            self.graphs[name].replay()
+            if events is not None:
+                events[i + 1].record()
         return self
