@@ -151,6 +151,28 @@ int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t bud
                       uint32_t width_mask, uint8_t* bits,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* kvs_allocate_bits for callers that must not allocate device memory.  The
+ * papers have no counterpart: this entry point exists for host code that
+ * cannot call cudaMalloc (or any allocating library), e.g. an inference
+ * engine that reserves all device memory for its own pool at start-up, or a
+ * plug-in that runs where only the engine may allocate.  Instead of a caller
+ * workspace it uses one fixed scratch array of KVS_STATIC_ALLOC_SCRATCH_BYTES
+ * that lives inside the library; every GPU that loads libkvs.so holds those
+ * bytes until the process exits.  Inputs and outputs are as for
+ * kvs_allocate_bits, and so are the results (bit for bit).
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture.
+ *  - All calls share the one array and it keeps the previous call's
+ *    contents; each call clears the part that must start at zero.  Calls
+ *    whose kernels overlap on the GPU (different streams, or several host
+ *    threads) race on the array: serialise them.
+ *  - Returns KVS_ERR_WORKSPACE when this GPU would need more scratch than the
+ *    array holds (more than about 300 SMs); other errors as kvs_allocate_bits. */
+#define KVS_STATIC_ALLOC_SCRATCH_BYTES (1u << 20)
+int kvs_allocate_bits_static(const float* w, const float* sigma, int64_t U, int64_t budget_bits,
+                             uint32_t width_mask, uint8_t* bits, void* stream);
+
 /* ---- quantise / pack / dequantise --------------------------------------- */
 /* Width-grouped streams, one per width 2, 4, 8, 16 (index 0..3)   [RDKV §2.3, TriZone].
  * A unit is a token row (axis 0, V cache) or a channel over the kept tokens

@@ -45,6 +45,7 @@ SIGNATURES = {
     "kvs_allocate_workspace_size": (c_size_t, [c_int64]),
     "kvs_allocate_bits": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_uint32, c_void_p, c_void_p, c_size_t,
                                   c_void_p]),
+    "kvs_allocate_bits_static": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_uint32, c_void_p, c_void_p]),
     "kvs_pack_capacity": (c_int, [c_int64] * 3 + [c_int, c_int64, POINTER(c_int64), POINTER(c_int64)]),
     "kvs_pack_workspace_size": (c_size_t, [c_int64] * 3 + [c_int]),
     "kvs_quantize_pack": (c_int, [c_void_p] + [c_int64] * 3 + [c_int, c_void_p, c_void_p, c_void_p, c_void_p,

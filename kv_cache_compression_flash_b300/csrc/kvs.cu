@@ -621,3 +621,44 @@ int kvs_dequantize(const kvs_stream_set* streams, int64_t Hkv, int64_t N, int64_
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// kvs_allocate_bits_static: the allocator with library-owned scratch, for
+// callers that cannot allocate device memory themselves.
+// ---------------------------------------------------------------------------
+// Host code must not pass this name to a kernel: on the host it only stands
+// in for the symbol; the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_static_alloc_scratch[KVS_STATIC_ALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxStaticDevices = 64;
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_addr[kMaxStaticDevices] = {};
+
+// device address of the scratch array on the current device (looked up once per device)
+int static_scratch_address(void** out) {
+  int dev = 0;
+  KVS_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxStaticDevices) return KVS_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+  if (g_static_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    KVS_CUDA_TRY(cudaGetSymbolAddress(&p, g_static_alloc_scratch));
+    g_static_scratch_addr[dev] = p;
+  }
+  *out = g_static_scratch_addr[dev];
+  return KVS_OK;
+}
+}  // namespace
+
+extern "C" int kvs_allocate_bits_static(const float* w, const float* sigma, int64_t U, int64_t budget_bits,
+                                        uint32_t width_mask, uint8_t* bits, void* stream) {
+  if (U < 0 || budget_bits < 0) return KVS_ERR_INVALID_ARG;
+  if (kvs_allocate_workspace_size(U) > KVS_STATIC_ALLOC_SCRATCH_BYTES) return KVS_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const int rc = static_scratch_address(&scratch);
+  if (rc) return rc;
+  // the allocator zeroes its own header on the stream before its kernel runs
+  return kvs_allocate_bits(w, sigma, U, budget_bits, width_mask, bits, scratch, KVS_STATIC_ALLOC_SCRATCH_BYTES,
+                           stream);
+}
