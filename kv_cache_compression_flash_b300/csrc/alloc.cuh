@@ -12,10 +12,11 @@
 // keeps taking later items that still fit and whose previous step was taken.
 //
 // B300 design: one cooperative launch, all blocks resident, grid barriers with
-// bounded waits.  lambda* is found exactly by an 8-pass radix select on the
-// fp64 bit patterns of theta (positive doubles order like their bit patterns),
-// each pass a cost-weighted 256-bin histogram; every block then decides the
-// digit redundantly so one barrier per pass suffices.  Ties at lambda* are
+// bounded waits.  Each block computes its units' thetas once (fp64) into
+// shared memory.  lambda* is found exactly by a 6-pass radix select (11-bit
+// digits) on the fp64 bit patterns of theta (positive doubles order like their
+// bit patterns), each pass a cost-weighted 2048-bin histogram; every block then
+// decides the digit redundantly so one barrier per pass suffices.  Ties at lambda* are
 // resolved in unit order by a grid-wide scan; the fix scan is an arg-max
 // (theta, then lowest unit) over each unit's next upgrade, repeated while the
 // leftover budget buys something (at most max_step/min_step rounds).
@@ -28,13 +29,20 @@ namespace kvs {
 constexpr int kAllocThreads = 256;
 constexpr int kMaxFixRounds = 16;
 
+constexpr int kRadixBits = 11;                 // digit width of the radix select
+constexpr int kRadixBins = 1 << kRadixBits;    // 2048
+constexpr int kRadixPasses = 6;                // 11+11+11+11+11+9 = 64 bits
+constexpr int kBinsPerThread = kRadixBins / kAllocThreads;
+
+__host__ __device__ constexpr int radix_shift(int pass) { return pass < 5 ? 53 - 11 * pass : 0; }
+__host__ __device__ constexpr int radix_width(int pass) { return pass < 5 ? 11 : 9; }
+
 struct AllocHeader {
   GridSync sync;
   unsigned long long total;  // cost of every positive upgrade item
   int bad;                   // a weight or sigma was negative or not finite
   int pad_;
-  unsigned long long hist[8][256];
-  unsigned long long first_cut;  // B-side cost before the first item that did not fit
+  unsigned long long first_cut;  // cost taken before the first item that did not fit
 };
 
 struct FixCand {
@@ -49,6 +57,7 @@ struct AllocParams {
   const float* sigma;
   uint8_t* bits;
   long long U;
+  long long per;    // units per block
   unsigned long long B;
   int K;            // upgrade steps = allowed widths - 1
   int min_cost;     // smallest step
@@ -56,6 +65,7 @@ struct AllocParams {
   int cost[4];      // step sizes b_{k+1} - b_k
   int width[5];     // allowed widths, ascending, width[0] = 0
   AllocHeader* hdr;
+  unsigned long long* hist;       // [kRadixPasses][kRadixBins] cost-weighted counts
   unsigned long long* tie_block;  // [gridDim.x]
   FixCand* cand;                  // [kMaxFixRounds][gridDim.x]
 };
@@ -124,8 +134,25 @@ __device__ __forceinline__ FixCand block_best(FixCand best, FixCand* s_cand) {
   return bb;
 }
 
+// theta bit pattern of item (u, k): from the block's shared-memory cache when
+// CACHE, else recomputed (fp64 is slow on this part, so the cache is the fast
+// path).  0 when the unit's key is not positive.
+template <bool CACHE>
+struct ThetaSource {
+  const AllocParams& p;
+  const unsigned long long* cache;  // [K][per]
+  long long u_begin;
+  __device__ __forceinline__ unsigned long long operator()(long long u, int k) const {
+    if (CACHE) return cache[static_cast<long long>(k) * p.per + (u - u_begin)];
+    const double key = static_cast<double>(p.w[u]) * static_cast<double>(p.sigma[u]);
+    return key > 0.0 ? static_cast<unsigned long long>(__double_as_longlong(p.c[k] * key)) : 0ull;
+  }
+};
+
+template <bool CACHE>
 __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocParams p) {
-  __shared__ unsigned s_hist[256];  // per-block cost per bin (< 2^32: units per block x 16)
+  extern __shared__ unsigned long long s_theta[];  // [K][per] when CACHE
+  __shared__ unsigned s_hist[kRadixBins];          // per-block cost per bin (< 2^32: units per block x 16)
   __shared__ unsigned long long s_red[kAllocThreads / 32];
   __shared__ unsigned long long s_sel_above;
   __shared__ int s_sel;
@@ -135,16 +162,20 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
   __shared__ int s_flag;
 
   const int nb = gridDim.x, b = blockIdx.x, tid = threadIdx.x;
-  const long long per = (p.U + nb - 1) / nb;
-  const long long u_begin = static_cast<long long>(b) * per;
-  const long long u_end = min(p.U, u_begin + per);
+  const long long u_begin = static_cast<long long>(b) * p.per;
+  const long long u_end = min(p.U, u_begin + p.per);
   AllocHeader* H = p.hdr;
+  const ThetaSource<CACHE> theta{p, s_theta, u_begin};
 
   if (tid < 17) s_lvl_of_width[tid] = -1;
   __syncthreads();
   if (tid <= p.K) s_lvl_of_width[p.width[tid]] = tid;
+  // the first pass's global histogram starts at zero (later ones are cleared
+  // one pass ahead, see below)
+  if (b == 0)
+    for (int i = tid; i < kRadixBins; i += kAllocThreads) p.hist[i] = 0ull;
 
-  // ---- phase 0: validate, total cost of positive items -------------------
+  // ---- phase 0: validate, cache thetas, total cost of positive items ------
   unsigned long long my_total = 0;
   int my_bad = 0;
   const int full_cost = p.width[p.K];
@@ -153,6 +184,10 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
     if (!(isfinite(wf) && isfinite(sf) && wf >= 0.f && sf >= 0.f)) my_bad = 1;
     const double key = static_cast<double>(wf) * static_cast<double>(sf);
     if (key > 0.0) my_total += static_cast<unsigned long long>(full_cost);
+    if (CACHE)
+      for (int k = 0; k < p.K; ++k)
+        s_theta[static_cast<long long>(k) * p.per + (u - u_begin)] =
+            key > 0.0 ? static_cast<unsigned long long>(__double_as_longlong(p.c[k] * key)) : 0ull;
   }
   const unsigned long long blk_total = block_sum(my_total, s_red);
   const int blk_bad = __syncthreads_or(my_bad);
@@ -169,55 +204,71 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
     return;
   }
   if (total <= p.B) {  // every upgrade fits
-    for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) {
-      const double key = static_cast<double>(p.w[u]) * static_cast<double>(p.sigma[u]);
-      p.bits[u] = key > 0.0 ? static_cast<uint8_t>(full_cost) : 0;
-    }
+    for (long long u = u_begin + tid; u < u_end; u += kAllocThreads)
+      p.bits[u] = theta(u, 0) != 0ull ? static_cast<uint8_t>(full_cost) : 0;
     return;
   }
 
   // ---- phase 1: radix select of lambda* on theta bit patterns ------------
   unsigned long long prefix = 0, pmask = 0, above = 0;
-  for (int pass = 0; pass < 8; ++pass) {
-    const int shift = 56 - 8 * pass;
-    s_hist[tid] = 0;  // kAllocThreads == 256 bins
+  for (int pass = 0; pass < kRadixPasses; ++pass) {
+    const int shift = radix_shift(pass);
+    const unsigned long long dmask = (1ull << radix_width(pass)) - 1ull;
+    for (int i = tid; i < kRadixBins; i += kAllocThreads) s_hist[i] = 0;
+    // the next pass's global histogram is idle until the barrier below
+    if (b == nb - 1 && pass + 1 < kRadixPasses)
+      for (int i = tid; i < kRadixBins; i += kAllocThreads) p.hist[(pass + 1) * kRadixBins + i] = 0ull;
     __syncthreads();
     // Early passes see the exponent bits, which nearly all thetas share: the
     // lanes of a warp that fall in one bin are merged first (match_any), so a
     // bin takes one atomic per warp and step instead of one per item.
     for (long long base = u_begin; base < u_end; base += kAllocThreads) {
       const long long u = base + tid;
-      double key = 0.0;
-      if (u < u_end) key = static_cast<double>(p.w[u]) * static_cast<double>(p.sigma[u]);
       for (int k = 0; k < p.K; ++k) {
-        const unsigned long long v = static_cast<unsigned long long>(__double_as_longlong(p.c[k] * key));
-        const unsigned bin =
-            (key > 0.0 && (v & pmask) == prefix) ? static_cast<unsigned>((v >> shift) & 255ull) : 256u;
+        const unsigned long long v = u < u_end ? theta(u, k) : 0ull;
+        const unsigned bin = (v != 0ull && (v & pmask) == prefix) ? static_cast<unsigned>((v >> shift) & dmask)
+                                                                   : static_cast<unsigned>(kRadixBins);
         const unsigned grp = __match_any_sync(0xFFFFFFFFu, bin);
-        if (bin != 256u && (tid & 31) == __ffs(grp) - 1)
+        if (bin != static_cast<unsigned>(kRadixBins) && (tid & 31) == __ffs(grp) - 1)
           atomicAdd(&s_hist[bin], static_cast<unsigned>(__popc(grp) * p.cost[k]));
       }
     }
     __syncthreads();
-    if (s_hist[tid]) atomicAdd(&H->hist[pass][tid], static_cast<unsigned long long>(s_hist[tid]));
+    for (int i = tid; i < kRadixBins; i += kAllocThreads)
+      if (s_hist[i]) atomicAdd(&p.hist[pass * kRadixBins + i], static_cast<unsigned long long>(s_hist[i]));
     if (!grid_barrier(&H->sync, nb)) return;
     {
-      // thread i looks at digit 255 - i; an inclusive scan gives the cost of
-      // every item at or above that digit; the first thread whose total
-      // exceeds the budget owns the digit of lambda*
-      const unsigned long long h = ld_vol(&H->hist[pass][255 - tid]);
+      // thread t owns the kBinsPerThread digits just below 2047 - t*kBinsPerThread
+      // (descending); a scan over threads gives the cost of all higher digits, and
+      // the first thread whose range pushes the running cost past B holds lambda*
+      unsigned long long h[kBinsPerThread], mine = 0;
+      const unsigned long long* hp = p.hist + pass * kRadixBins;
+#pragma unroll
+      for (int j = 0; j < kBinsPerThread; ++j) {
+        h[j] = ld_vol(&hp[kRadixBins - 1 - (tid * kBinsPerThread + j)]);
+        mine += h[j];
+      }
       unsigned long long block_total;
-      const unsigned long long incl = block_exscan(h, s_red, &block_total) + h;
-      const bool over = above + incl > p.B;
+      const unsigned long long ex = block_exscan(mine, s_red, &block_total);
+      const bool over = above + ex + mine > p.B;
       const int first = __syncthreads_count(!over);  // over is monotone in tid
       if (tid == first) {
-        s_sel = 255 - tid;
-        s_sel_above = above + incl - h;
+        unsigned long long a = above + ex;
+        int sel = 0;
+        for (int j = 0; j < kBinsPerThread; ++j) {
+          if (a + h[j] > p.B) {
+            sel = kRadixBins - 1 - (tid * kBinsPerThread + j);
+            break;
+          }
+          a += h[j];
+        }
+        s_sel = sel;
+        s_sel_above = a;
       }
     }
     __syncthreads();
     prefix |= static_cast<unsigned long long>(s_sel) << shift;
-    pmask |= 255ull << shift;
+    pmask |= dmask << shift;
     above = s_sel_above;
     __syncthreads();
   }
@@ -225,12 +276,9 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
 
   // ---- phase 2: prefix levels; ties at lambda* resolved in unit order -----
   unsigned long long my_tie = 0;
-  for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) {
-    const double key = static_cast<double>(p.w[u]) * static_cast<double>(p.sigma[u]);
-    if (key <= 0.0) continue;
+  for (long long u = u_begin + tid; u < u_end; u += kAllocThreads)
     for (int k = 0; k < p.K; ++k)
-      if (static_cast<unsigned long long>(__double_as_longlong(p.c[k] * key)) == lam) my_tie += p.cost[k];
-  }
+      if (theta(u, k) == lam) my_tie += p.cost[k];
   const unsigned long long blk_tie = block_sum(my_tie, s_red);
   if (tid == 0) p.tie_block[b] = blk_tie;
   if (!grid_barrier(&H->sync, nb)) return;
@@ -245,13 +293,10 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
     int lvl = 0;
     unsigned long long tie = 0;
     if (u < u_end) {
-      const double key = static_cast<double>(p.w[u]) * static_cast<double>(p.sigma[u]);
-      if (key > 0.0) {
-        for (int k = 0; k < p.K; ++k) {
-          const unsigned long long v = static_cast<unsigned long long>(__double_as_longlong(p.c[k] * key));
-          if (v > lam) ++lvl;
-          else if (v == lam) tie = p.cost[k];
-        }
+      for (int k = 0; k < p.K; ++k) {
+        const unsigned long long v = theta(u, k);
+        if (v > lam) ++lvl;
+        else if (v == lam) tie = p.cost[k];
       }
     }
     unsigned long long chunk_total;
@@ -276,10 +321,9 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
     for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) {
       const int lvl = s_lvl_of_width[p.bits[u]];
       if (lvl < 0 || lvl >= p.K || p.cost[lvl] > R) continue;
-      const double key = static_cast<double>(p.w[u]) * static_cast<double>(p.sigma[u]);
-      const double th = p.c[lvl] * key;
-      if (!(th > 0.0)) continue;
-      FixCand c = {static_cast<unsigned long long>(__double_as_longlong(th)), u, p.cost[lvl], 0};
+      const unsigned long long th = theta(u, lvl);
+      if (th == 0ull) continue;
+      FixCand c = {th, u, p.cost[lvl], 0};
       if (best.theta == 0ull || cand_better(c, best)) best = c;
     }
     best = block_best(best, s_cand);

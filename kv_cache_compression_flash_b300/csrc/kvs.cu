@@ -251,6 +251,7 @@ constexpr long long kAllocUnitsPerBlock = 2048;
 size_t alloc_ws_bytes(int nb) {
   WsCarver c{nullptr, 0, 0};
   c.take<AllocHeader>(1);
+  c.take<unsigned long long>(static_cast<size_t>(kRadixPasses) * kRadixBins);
   c.take<unsigned long long>(nb);
   c.take<FixCand>(static_cast<size_t>(kMaxFixRounds) * nb);
   return c.used;
@@ -317,23 +318,27 @@ template <int DH>
 int pack_dh(const uint16_t* X, int64_t Hkv, int64_t N, int axis, const uint8_t* bits, const uint8_t* keep,
             const kvs_stream_set* s, const PackWs& w, cudaStream_t st, bool dequant, float* out) {
   const int sms = sm_count();
-  if (axis == 0) {
+  if (axis == 0 && dequant) {  // decode straight from the stream entries
+    const long long rows = Hkv * N;
+    const StreamPtrs sp = to_ptrs(s, true);
+    const int zb = static_cast<int>(std::min<long long>(cdiv(rows * (DH / 4), 256), static_cast<long long>(sms) * 16));
+    zero_dropped_rows_kernel<DH><<<zb, 256, 0, st>>>(bits, rows, out);
+    const int blocks = static_cast<int>(std::min<long long>(cdiv(rows * (DH / 64), 16), static_cast<long long>(sms) * 16));
+    dequant_entries_rows_kernel<DH><<<blocks, 256, 0, st>>>(sp, out);
+  } else if (axis == 0) {
     const long long U = Hkv * N;
     const int nchunk = static_cast<int>(cdiv(U, kPlanChunk));
-    const StreamPtrs sp = to_ptrs(s, !dequant);
+    const StreamPtrs sp = to_ptrs(s, true);
     plan_count_kernel<<<nchunk, kPlanThreads, 0, st>>>(bits, U, w.chunk);
     plan_scan_kernel<<<1, 1024, 0, st>>>(w.chunk, nchunk, DH / 64, sp);
-    plan_rank_kernel<<<nchunk, kPlanThreads, 0, st>>>(bits, U, w.chunk, DH / 64, w.rank, sp, dequant ? 0 : 1);
+    plan_rank_kernel<<<nchunk, kPlanThreads, 0, st>>>(bits, U, w.chunk, DH / 64, w.rank, sp, 1);
     const long long ngroups = U * (DH / 64);
     const int blocks = static_cast<int>(std::min<long long>(cdiv(ngroups, 16), static_cast<long long>(sms) * 16));
-    if (dequant)
-      dequant_rows_kernel<DH><<<blocks, 256, 0, st>>>(sp, bits, w.rank, U, out);
-    else
-      pack_rows_kernel<DH><<<blocks, 256, 0, st>>>(X, bits, w.rank, U, sp);
+    pack_rows_kernel<DH><<<blocks, 256, 0, st>>>(X, bits, w.rank, U, sp);
   } else {
     const StreamPtrs sp = to_ptrs(s, !dequant);
     kept_index_kernel<<<static_cast<int>(Hkv), 1024, 0, st>>>(keep, static_cast<int>(N), w.kept, w.n_kept);
-    plan_channels_kernel<<<1, kPlanThreads, 0, st>>>(bits, static_cast<int>(Hkv * DH), DH, w.n_kept, w.rank, sp,
+    plan_channels_kernel<<<1, kPlanChannelThreads, 0, st>>>(bits, static_cast<int>(Hkv * DH), DH, w.n_kept, w.rank, sp,
                                                      dequant ? 0 : 1);
     const dim3 grid(static_cast<unsigned>(cdiv(N, 64)), static_cast<unsigned>(Hkv));
     if (dequant) {
@@ -355,7 +360,7 @@ int pack_common(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis, 
   int rc = pack_shape_ok(Hkv, N, d, axis);
   if (rc) return rc;
   if (!bits || !streams_ok(s) || (axis == 1 && !keep) || (dequant ? !out : !X)) return KVS_ERR_INVALID_ARG;
-  if (!dequant && !s->counts) return KVS_ERR_INVALID_ARG;
+  if ((!dequant || axis == 0) && !s->counts) return KVS_ERR_INVALID_ARG;
   if (X && !aligned16(X)) return KVS_ERR_INVALID_ARG;
   if (out && !aligned16(out)) return KVS_ERR_INVALID_ARG;
   PackWs w;
@@ -563,15 +568,26 @@ int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t bud
     p.min_cost = std::min(p.min_cost, p.cost[k]);
     p.c[k] = (std::ldexp(1.0, -b0) - std::ldexp(1.0, -b1)) / static_cast<double>(b1 - b0);
   }
-  int occ = 0;
-  KVS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, allocate_kernel, kAllocThreads, 0));
-  const int nb_cap = std::min(std::max(occ, 1) * sm_count(), alloc_blocks_max());
-  // a few thousand units per block: fewer blocks make every grid barrier cheaper
-  const int nb = static_cast<int>(std::max<long long>(1, std::min<long long>(nb_cap, cdiv(U, kAllocUnitsPerBlock))));
-  if (cdiv(U, nb) * 16 >= (1ll << 32)) return KVS_ERR_UNSUPPORTED;  // per-block histogram counts are 32-bit
+  // Preferred: a few thousand units per block with their thetas cached in
+  // shared memory; needs every block co-resident.  Otherwise fall back to
+  // recomputing thetas from w and sigma in every pass.
+  const int sms = sm_count();
+  const size_t cache_smem = static_cast<size_t>(kAllocUnitsPerBlock) * p.K * sizeof(unsigned long long);
+  KVS_CUDA_TRY(allow_smem(allocate_kernel<true>, cache_smem));
+  int occ_c = 0, occ_u = 0;
+  KVS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_c, allocate_kernel<true>, kAllocThreads, cache_smem));
+  KVS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_u, allocate_kernel<false>, kAllocThreads, 0));
+  long long nb = std::max<long long>(1, cdiv(U, kAllocUnitsPerBlock));
+  const bool cached = nb <= static_cast<long long>(occ_c) * sms && nb <= alloc_blocks_max();
+  if (!cached) nb = std::max<long long>(1, std::min<long long>(cdiv(U, kAllocUnitsPerBlock),
+                                                              std::min<long long>(static_cast<long long>(std::max(occ_u, 1)) * sms,
+                                                                                  alloc_blocks_max())));
+  p.per = cdiv(U, nb);
+  if (p.per * 16 >= (1ll << 32)) return KVS_ERR_UNSUPPORTED;  // per-block histogram counts are 32-bit
   WsCarver c{static_cast<char*>(workspace), 0, workspace_bytes};
   p.hdr = c.take<AllocHeader>(1);
-  p.tie_block = c.take<unsigned long long>(nb);
+  p.hist = c.take<unsigned long long>(static_cast<size_t>(kRadixPasses) * kRadixBins);
+  p.tie_block = c.take<unsigned long long>(static_cast<size_t>(nb));
   p.cand = c.take<FixCand>(static_cast<size_t>(kMaxFixRounds) * nb);
   if (!c.ok() || !workspace) return KVS_ERR_WORKSPACE;
   p.w = w;
@@ -581,8 +597,14 @@ int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t bud
   p.B = static_cast<unsigned long long>(budget_bits);
   KVS_CUDA_TRY(cudaMemsetAsync(p.hdr, 0, sizeof(AllocHeader), st));
   void* args[] = {&p};
-  KVS_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(allocate_kernel), dim3(nb),
-                                           dim3(kAllocThreads), args, 0, st));
+  if (cached) {
+    const size_t smem = static_cast<size_t>(p.per) * p.K * sizeof(unsigned long long);
+    KVS_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(allocate_kernel<true>),
+                                             dim3(static_cast<unsigned>(nb)), dim3(kAllocThreads), args, smem, st));
+  } else {
+    KVS_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(allocate_kernel<false>),
+                                             dim3(static_cast<unsigned>(nb)), dim3(kAllocThreads), args, 0, st));
+  }
   return KVS_OK;
 }
 

@@ -261,27 +261,38 @@ __global__ void __launch_bounds__(256) pack_rows_kernel(const uint16_t* __restri
   }
 }
 
+// Token units decoded from the streams themselves: entry j of width slot s is
+// unit ids[s][j] with groups goff[s][j] ..; counts[] (written by the packer)
+// says how many entries each slot holds.  One half-warp per group.
 template <int DH>
-__global__ void __launch_bounds__(256) dequant_rows_kernel(const StreamPtrs sp, const uint8_t* __restrict__ bits,
-                                                           const int* __restrict__ rank, const long long U,
-                                                           float* __restrict__ out) {
+__global__ void __launch_bounds__(256) dequant_entries_rows_kernel(const StreamPtrs sp, float* __restrict__ out) {
   constexpr int GPU = DH / 64;
-  const int l16 = threadIdx.x & 15;
-  const long long n_groups = U * GPU;
-  const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x / 16);
-  for (long long gidx = static_cast<long long>(blockIdx.x) * (blockDim.x / 16) + (threadIdx.x >> 4);
-       gidx < n_groups; gidx += stride) {
-    const long long u = gidx / GPU;
-    const int gi = static_cast<int>(gidx % GPU);
-    const int w = bits[u];
-    const int s = width_slot(w);
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
-    if (s >= 0) {
-      const int r = rank[u];
-      const long long grp = static_cast<long long>(r) * GPU + gi;
-      if (r >= 0 && r < sp.cap_units[s] && grp < sp.cap_groups[s])
-        dequant_lane4(sp.codes[s] + grp * (8 * w), w, l16, sp.scales[s] + grp, y);
+  __shared__ long long s_off[5];
+  if (threadIdx.x == 0) {
+    long long run = 0;
+    for (int s = 0; s < 4; ++s) {
+      s_off[s] = run;
+      run += min(static_cast<long long>(sp.counts[s]), sp.cap_units[s]) * GPU;
     }
+    s_off[4] = run;
+  }
+  __syncthreads();
+  const int l16 = threadIdx.x & 15;
+  const long long total = s_off[4];
+  const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x / 16);
+  for (long long gidx = static_cast<long long>(blockIdx.x) * (blockDim.x / 16) + (threadIdx.x >> 4); gidx < total;
+       gidx += stride) {
+    int s = 0;
+    while (s < 3 && gidx >= s_off[s + 1]) ++s;
+    const long long local = gidx - s_off[s];
+    const long long jj = local / GPU;
+    const int gi = static_cast<int>(local % GPU);
+    const long long u = sp.ids[s][jj];
+    const long long grp = sp.goff[s][jj] + gi;
+    if (grp >= sp.cap_groups[s]) continue;
+    const int w = s == 3 ? 16 : (2 << s);
+    float y[4];
+    dequant_lane4(sp.codes[s] + grp * (8 * w), w, l16, sp.scales[s] + grp, y);
     *reinterpret_cast<float4*>(out + u * DH + gi * 64 + l16 * 4) = make_float4(y[0], y[1], y[2], y[3]);
   }
 }
@@ -289,7 +300,8 @@ __global__ void __launch_bounds__(256) dequant_rows_kernel(const StreamPtrs sp, 
 // ---------------------------------------------------------------------------
 // channel units (axis 1, K cache) over the tokens each head keeps
 // ---------------------------------------------------------------------------
-// kept[g][j] = j-th kept token of head g (ascending); n_kept[g]
+// kept[g][j] = j-th kept token of head g (ascending); n_kept[g].  One block
+// per head, 4 consecutive tokens per thread per step.
 __global__ void __launch_bounds__(1024) kept_index_kernel(const uint8_t* __restrict__ keep_bits, const int N,
                                                           int* __restrict__ kept, int* __restrict__ n_kept) {
   __shared__ int s_w[32];
@@ -297,16 +309,27 @@ __global__ void __launch_bounds__(1024) kept_index_kernel(const uint8_t* __restr
   const int g = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) s_carry = 0;
   __syncthreads();
-  for (int base = 0; base < N; base += 1024) {
-    const int t = base + threadIdx.x;
-    const int k = (t < N && keep_bits[static_cast<size_t>(g) * N + t] != 0) ? 1 : 0;
-    const unsigned bal = __ballot_sync(0xFFFFFFFFu, k);
-    const int in_warp = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) s_w[warp] = __popc(bal);
+  const uint8_t* kb = keep_bits + static_cast<size_t>(g) * N;
+  for (int base = 0; base < N; base += 4096) {
+    const int t0 = base + threadIdx.x * 4;
+    int k[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) k[e] = (t0 + e < N && kb[t0 + e] != 0) ? 1 : 0;
+    const int mine = k[0] + k[1] + k[2] + k[3];
+    int x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_w[warp] = x;
     __syncthreads();
     int before = s_carry;
     for (int i = 0; i < warp; ++i) before += s_w[i];
-    if (k) kept[static_cast<size_t>(g) * N + before + in_warp] = t;
+    int pos = before + x - mine;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (k[e]) kept[static_cast<size_t>(g) * N + pos++] = t0 + e;
     __syncthreads();
     if (threadIdx.x == 0) {
       int tot = 0;
@@ -320,17 +343,18 @@ __global__ void __launch_bounds__(1024) kept_index_kernel(const uint8_t* __restr
 
 // single block plan over channel units u = g*DH + c: rank, ids, group offsets
 // (a unit of head g has ceil(n_kept[g]/64) groups), counts and capacity check
-__global__ void __launch_bounds__(kPlanThreads) plan_channels_kernel(const uint8_t* __restrict__ bits,
+constexpr int kPlanChannelThreads = 1024;
+__global__ void __launch_bounds__(kPlanChannelThreads) plan_channels_kernel(const uint8_t* __restrict__ bits,
                                                                      const int U, const int DH,
                                                                      const int* __restrict__ n_kept,
                                                                      int* __restrict__ rank, const StreamPtrs sp,
                                                                      const int write_streams) {
-  __shared__ long long s_u[kPlanThreads / 32][4], s_g[kPlanThreads / 32][4];
+  __shared__ long long s_u[kPlanChannelThreads / 32][4], s_g[kPlanChannelThreads / 32][4];
   __shared__ long long s_cu[4], s_cg[4];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x < 4) s_cu[threadIdx.x] = s_cg[threadIdx.x] = 0;
   __syncthreads();
-  for (int base = 0; base < U; base += kPlanThreads) {
+  for (int base = 0; base < U; base += kPlanChannelThreads) {
     const int u = base + threadIdx.x;
     const int s = u < U ? width_slot(bits[u]) : -1;
     const long long ng = u < U ? (n_kept[u / DH] + 63) / 64 : 0;
@@ -371,7 +395,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_channels_kernel(const uint8
     }
     __syncthreads();
     if (threadIdx.x < 4) {
-      for (int i = 0; i < kPlanThreads / 32; ++i) {
+      for (int i = 0; i < kPlanChannelThreads / 32; ++i) {
         s_cu[threadIdx.x] += s_u[i][threadIdx.x];
         s_cg[threadIdx.x] += s_g[i][threadIdx.x];
       }
@@ -388,6 +412,30 @@ __global__ void __launch_bounds__(kPlanThreads) plan_channels_kernel(const uint8
   }
 }
 
+// Width and first stream group of every channel of head g, staged once per CTA
+// (so the per-channel loops below issue no dependent global loads).  base = -1
+// for channels that are not stored.
+template <int DH>
+__device__ __forceinline__ void stage_channel_meta(const StreamPtrs& sp, const uint8_t* __restrict__ bits,
+                                                   const int* __restrict__ rank, const int g, const int j,
+                                                   int* s_w, long long* s_base) {
+  for (int c = threadIdx.x; c < DH; c += blockDim.x) {
+    const int u = g * DH + c;
+    const int w = bits[u];
+    const int s = width_slot(w);
+    long long base = -1;
+    if (s >= 0) {
+      const int r = rank[u];
+      if (r >= 0 && r < sp.cap_units[s]) {
+        const long long grp = sp.goff[s][r] + j;
+        if (grp < sp.cap_groups[s]) base = grp;
+      }
+    }
+    s_w[c] = w;
+    s_base[c] = base;
+  }
+}
+
 // grid (ceil(N/64), Hkv), 256 threads: token group j of head g for every channel
 template <int DH>
 __global__ void __launch_bounds__(256) pack_channels_kernel(const uint16_t* __restrict__ X, const int N,
@@ -395,12 +443,17 @@ __global__ void __launch_bounds__(256) pack_channels_kernel(const uint16_t* __re
                                                             const int* __restrict__ rank,
                                                             const int* __restrict__ kept,
                                                             const int* __restrict__ n_kept, const StreamPtrs sp) {
-  constexpr int LD = DH + 8;
-  __shared__ __align__(16) uint16_t tile[64][LD];
+  // odd word stride: the column reads below (lane i takes rows 4i..4i+3)
+  // spread over the banks instead of piling onto two
+  constexpr int LDW = DH / 2 + 1;  // 32-bit words per row
+  __shared__ uint32_t tile[64][LDW];
+  __shared__ int s_w[DH];
+  __shared__ long long s_base[DH];
   const int j = blockIdx.x, g = blockIdx.y;
   const int n = n_kept[g];
   if (j * 64 >= n) return;
   const int rows = min(64, n - j * 64);
+  stage_channel_meta<DH>(sp, bits, rank, g, j, s_w, s_base);
   for (int e = threadIdx.x; e < 64 * (DH / 8); e += 256) {
     const int i = e / (DH / 8), c8 = (e % (DH / 8)) * 8;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -408,24 +461,24 @@ __global__ void __launch_bounds__(256) pack_channels_kernel(const uint16_t* __re
       const int t = kept[static_cast<size_t>(g) * N + j * 64 + i];
       v = __ldg(reinterpret_cast<const uint4*>(X + (static_cast<size_t>(g) * N + t) * DH + c8));
     }
-    *reinterpret_cast<uint4*>(&tile[i][c8]) = v;
+    uint32_t* row = &tile[i][c8 / 2];
+    row[0] = v.x;
+    row[1] = v.y;
+    row[2] = v.z;
+    row[3] = v.w;
   }
   __syncthreads();
   const int l16 = threadIdx.x & 15, hw = threadIdx.x >> 4;
   for (int c = hw; c < DH; c += 16) {
-    const int u = g * DH + c;
-    const int w = bits[u];
+    const long long grp = s_base[c];
+    if (grp < 0) continue;
+    const int w = s_w[c];
     const int s = width_slot(w);
-    if (s < 0) continue;
-    const int r = rank[u];
-    if (r < 0 || r >= sp.cap_units[s]) continue;
-    const long long grp = sp.goff[s][r] + j;
-    if (grp >= sp.cap_groups[s]) continue;
     float x[4];
     uint32_t rw[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      rw[e] = tile[4 * l16 + e][c];
+      rw[e] = (tile[4 * l16 + e][c >> 1] >> ((c & 1) * 16)) & 0xFFFFu;
       x[e] = __uint_as_float(rw[e] << 16);
     }
     const uint2 raw = make_uint2(rw[0] | (rw[1] << 16), rw[2] | (rw[3] << 16));
@@ -450,23 +503,24 @@ __global__ void __launch_bounds__(256) dequant_channels_kernel(const StreamPtrs 
                                                                const int* __restrict__ kept,
                                                                const int* __restrict__ n_kept,
                                                                float* __restrict__ out) {
-  __shared__ __align__(16) float tile[64][DH + 4];
+  constexpr int LD = DH + 1;  // odd stride: conflict-light column writes
+  __shared__ float tile[64][LD];
+  __shared__ int s_w[DH];
+  __shared__ long long s_base[DH];
   const int j = blockIdx.x, g = blockIdx.y;
   const int n = n_kept[g];
   if (j * 64 >= n) return;
   const int rows = min(64, n - j * 64);
+  stage_channel_meta<DH>(sp, bits, rank, g, j, s_w, s_base);
+  __syncthreads();
   const int l16 = threadIdx.x & 15, hw = threadIdx.x >> 4;
   for (int c = hw; c < DH; c += 16) {
-    const int u = g * DH + c;
-    const int w = bits[u];
-    const int s = width_slot(w);
     float y[4] = {0.f, 0.f, 0.f, 0.f};
-    if (s >= 0) {
-      const int r = rank[u];
-      if (r >= 0 && r < sp.cap_units[s]) {
-        const long long grp = sp.goff[s][r] + j;
-        if (grp < sp.cap_groups[s]) dequant_lane4(sp.codes[s] + grp * (8 * w), w, l16, sp.scales[s] + grp, y);
-      }
+    const long long grp = s_base[c];
+    if (grp >= 0) {
+      const int w = s_w[c];
+      const int s = width_slot(w);
+      dequant_lane4(sp.codes[s] + grp * (8 * w), w, l16, sp.scales[s] + grp, y);
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) tile[4 * l16 + e][c] = y[e];
@@ -476,7 +530,7 @@ __global__ void __launch_bounds__(256) dequant_channels_kernel(const StreamPtrs 
     const int i = e / (DH / 4), c4 = (e % (DH / 4)) * 4;
     const int t = kept[static_cast<size_t>(g) * N + j * 64 + i];
     *reinterpret_cast<float4*>(out + (static_cast<size_t>(g) * N + t) * DH + c4) =
-        *reinterpret_cast<const float4*>(&tile[i][c4]);
+        make_float4(tile[i][c4], tile[i][c4 + 1], tile[i][c4 + 2], tile[i][c4 + 3]);
   }
 }
 

@@ -73,7 +73,7 @@ class RdkvLayerStep:
         n += 1          # K allocation
         n += 4 + 3      # V pack (count, scan, rank, pack), K pack (kept, plan, pack)
         if self.dequant:
-            n += 4 + 4  # V dequant (count, scan, rank, dequant), K dequant (kept, plan, zero, dequant)
+            n += 2 + 4  # V dequant (zero, decode entries), K dequant (kept, plan, zero, dequant)
         return n
 
     def pass1(self, Q, K, V, stream=None):
