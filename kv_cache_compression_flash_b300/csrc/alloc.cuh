@@ -191,13 +191,17 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
   }
   const unsigned long long blk_total = block_sum(my_total, s_red);
   const int blk_bad = __syncthreads_or(my_bad);
-  if (tid == 0) {
-    if (blk_total) atomicAdd(&H->total, blk_total);
-    if (blk_bad) atomicOr(&H->bad, 1);
+  unsigned long long total = blk_total;
+  int bad = blk_bad;
+  if (nb > 1) {
+    if (tid == 0) {
+      if (blk_total) atomicAdd(&H->total, blk_total);
+      if (blk_bad) atomicOr(&H->bad, 1);
+    }
+    if (!grid_barrier(&H->sync, nb)) return;
+    total = ld_vol(&H->total);
+    bad = *reinterpret_cast<volatile int*>(&H->bad);
   }
-  if (!grid_barrier(&H->sync, nb)) return;
-  const unsigned long long total = ld_vol(&H->total);
-  const int bad = *reinterpret_cast<volatile int*>(&H->bad);
   if (bad) {
     if (b == 0 && tid == 0) record_error(KVS_ERR_RANGE);
     for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) p.bits[u] = 0;
@@ -234,9 +238,12 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
       }
     }
     __syncthreads();
-    for (int i = tid; i < kRadixBins; i += kAllocThreads)
-      if (s_hist[i]) atomicAdd(&p.hist[pass * kRadixBins + i], static_cast<unsigned long long>(s_hist[i]));
-    if (!grid_barrier(&H->sync, nb)) return;
+    const bool single = nb == 1;  // one block: its histogram is the whole histogram
+    if (!single) {
+      for (int i = tid; i < kRadixBins; i += kAllocThreads)
+        if (s_hist[i]) atomicAdd(&p.hist[pass * kRadixBins + i], static_cast<unsigned long long>(s_hist[i]));
+      if (!grid_barrier(&H->sync, nb)) return;
+    }
     {
       // thread t owns the kBinsPerThread digits just below 2047 - t*kBinsPerThread
       // (descending); a scan over threads gives the cost of all higher digits, and
@@ -245,7 +252,8 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
       const unsigned long long* hp = p.hist + pass * kRadixBins;
 #pragma unroll
       for (int j = 0; j < kBinsPerThread; ++j) {
-        h[j] = ld_vol(&hp[kRadixBins - 1 - (tid * kBinsPerThread + j)]);
+        const int bin = kRadixBins - 1 - (tid * kBinsPerThread + j);
+        h[j] = single ? static_cast<unsigned long long>(s_hist[bin]) : ld_vol(&hp[bin]);
         mine += h[j];
       }
       unsigned long long block_total;
@@ -279,11 +287,11 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
   for (long long u = u_begin + tid; u < u_end; u += kAllocThreads)
     for (int k = 0; k < p.K; ++k)
       if (theta(u, k) == lam) my_tie += p.cost[k];
-  const unsigned long long blk_tie = block_sum(my_tie, s_red);
-  if (tid == 0) p.tie_block[b] = blk_tie;
-  if (!grid_barrier(&H->sync, nb)) return;
   unsigned long long carry = above;
-  {
+  if (nb > 1) {
+    const unsigned long long blk_tie = block_sum(my_tie, s_red);
+    if (tid == 0) p.tie_block[b] = blk_tie;
+    if (!grid_barrier(&H->sync, nb)) return;
     unsigned long long e = 0;
     for (int i = tid; i < b; i += kAllocThreads) e += ld_vol(&p.tie_block[i]);
     carry += block_sum(e, s_red);
@@ -311,7 +319,11 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
     }
     carry += chunk_total;
   }
-  if (!grid_barrier(&H->sync, nb)) return;
+  if (nb > 1) {
+    if (!grid_barrier(&H->sync, nb)) return;
+  } else {
+    __syncthreads();
+  }
 
   // ---- phase 3: budget-fix rounds ------------------------------------------
   long long R = static_cast<long long>(p.B) - static_cast<long long>(ld_vol(&H->first_cut));
@@ -327,9 +339,14 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
       if (best.theta == 0ull || cand_better(c, best)) best = c;
     }
     best = block_best(best, s_cand);
-    if (tid == 0) p.cand[it * nb + b] = best;
-    if (!grid_barrier(&H->sync, nb)) return;
-    {
+    if (nb == 1) {  // the block's best is the global best
+      if (tid == 0) {
+        s_best = best;
+        s_flag = best.theta != 0ull;
+      }
+    } else {
+      if (tid == 0) p.cand[it * nb + b] = best;
+      if (!grid_barrier(&H->sync, nb)) return;
       FixCand bb = {0ull, 0ll, 0, 0};
       for (int i = tid; i < nb; i += kAllocThreads) {
         const volatile FixCand* vc = &p.cand[it * nb + i];

@@ -61,6 +61,8 @@ class RdkvLayerStep:
         for k, n in sizes.items():
             self.ws[k].get(n, dev)
         self.graphs = None
+        self.side_stream = torch.cuda.Stream(device=dev)
+        self.v_done = torch.cuda.Event()
 
     def kernel_launches(self) -> int:
         """Kernels one step launches (memset nodes excluded)."""
@@ -86,19 +88,32 @@ class RdkvLayerStep:
                            stream=stream)
 
     def rest(self, Q, K, V, stream=None):
+        """Everything after scoring, as two dependent chains on two streams:
+        V: sigma_t -> V allocation -> V pack (-> dequant);
+        K: w_c (from the start), then after the V widths: sigma_c -> K
+        allocation -> K pack (-> dequant)."""
         ws = self.ws
-        K_.channel_weights(Q, K, out=self.w_c, ws=ws["cw"], stream=stream)
-        K_.unit_rms(V, 0, out=self.sig_t, ws=ws["rms0"], stream=stream)
+        main = stream if stream is not None else torch.cuda.current_stream()
+        side = self.side_stream
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            K_.channel_weights(Q, K, out=self.w_c, ws=ws["cw"], stream=side)
+        K_.unit_rms(V, 0, out=self.sig_t, ws=ws["rms0"], stream=main)
         K_.allocate_bits(self.out["w_t"], self.sig_t, self.B_v, self.width_mask, out=self.bits_v, ws=ws["av"],
-                         stream=stream)
-        K_.unit_rms(K, 1, keep_bits=self.bits_v, out=self.sig_c, ws=ws["rms1"], stream=stream)
-        K_.allocate_bits(self.w_c, self.sig_c, self.B_k, self.width_mask, out=self.bits_k, ws=ws["ak"],
-                         stream=stream)
-        K_.quantize_pack(V, 0, self.bits_v, None, self.v_streams, ws=ws["pv"], stream=stream)
-        K_.quantize_pack(K, 1, self.bits_k, self.bits_v, self.k_streams, ws=ws["pk"], stream=stream)
+                         stream=main)
+        self.v_done.record(main)
+        with torch.cuda.stream(side):
+            side.wait_event(self.v_done)
+            K_.unit_rms(K, 1, keep_bits=self.bits_v, out=self.sig_c, ws=ws["rms1"], stream=side)
+            K_.allocate_bits(self.w_c, self.sig_c, self.B_k, self.width_mask, out=self.bits_k, ws=ws["ak"],
+                             stream=side)
+            K_.quantize_pack(K, 1, self.bits_k, self.bits_v, self.k_streams, ws=ws["pk"], stream=side)
+            if self.dequant:
+                K_.dequantize(self.k_streams, self.bits_k, self.bits_v, out=self.k_hat, ws=ws["dk"], stream=side)
+        K_.quantize_pack(V, 0, self.bits_v, None, self.v_streams, ws=ws["pv"], stream=main)
         if self.dequant:
-            K_.dequantize(self.v_streams, self.bits_v, None, out=self.v_hat, ws=ws["dv"], stream=stream)
-            K_.dequantize(self.k_streams, self.bits_k, self.bits_v, out=self.k_hat, ws=ws["dk"], stream=stream)
+            K_.dequantize(self.v_streams, self.bits_v, None, out=self.v_hat, ws=ws["dv"], stream=main)
+        main.wait_stream(side)
 
     def run(self, Q, K, V, stream=None):
         self.pass1(Q, K, V, stream)
