@@ -226,6 +226,22 @@ int kvs_dequantize(const kvs_stream_set* streams, int64_t Hkv, int64_t N, int64_
                    const uint8_t* bits, const uint8_t* keep_bits, float* out,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- threshold pruning with a sliding window ------------------------------ */
+/* KVzap's adaptive eviction   [KVzap §2.3: tokens whose score falls below a
+ * fixed threshold tau are dropped; the last w tokens are always kept]:
+ *   bits[g*N + t] = keep_width  if score[g*N + t] >= tau or t >= N - window
+ *                   0           otherwise (evicted)
+ *   score      : float [Hkv, N], e.g. s_plus from kvs_score_attention; compare
+ *                in the score's own domain (pass exp(tau) to threshold log-scores)
+ *   window     : 0 <= window; window >= N keeps everything
+ *   keep_width : the width kept tokens get, one of 2, 4, 8, 16
+ *   bits       : uint8 [Hkv, N], usable as the widths (and keep mask) of
+ *                kvs_quantize_pack.
+ * A non-finite score records KVS_ERR_RANGE in the error word; that token is
+ * evicted unless the window keeps it. */
+int kvs_threshold_keep(const float* score, int64_t Hkv, int64_t N, float tau, int64_t window,
+                       uint32_t keep_width, uint8_t* bits, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -52,6 +52,8 @@ SIGNATURES = {
                                                                c_size_t, c_void_p]),
     "kvs_dequantize": (c_int, [c_void_p] + [c_int64] * 3 + [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
                                                             c_void_p]),
+    "kvs_threshold_keep": (c_int, [c_void_p, c_int64, c_int64, ctypes.c_float, c_int64, c_uint32, c_void_p,
+                                   c_void_p]),
 }
 
 
@@ -278,3 +280,14 @@ def dequantize(streams: Streams, bits, keep_bits, *, out=None, ws=None, stream=N
     _check(L.kvs_dequantize(ctypes.byref(streams.c), Hkv, N, d, axis, _ptr(bits), _ptr(keep_bits), _ptr(y),
                             _ptr(buf), buf.numel(), _stream(stream)), "kvs_dequantize")
     return y
+
+
+def threshold_keep(score, tau, window=128, keep_width=16, *, out=None, stream=None):
+    """uint8 widths [Hkv, N]: keep_width where score >= tau or in the last `window` positions, else 0."""
+    if score.dtype != torch.float32 or not score.is_cuda or not score.is_contiguous() or score.dim() != 2:
+        raise KvsError("score must be a contiguous float32 CUDA tensor [Hkv, N]")
+    Hkv, N = score.shape
+    bits = out if out is not None else torch.empty(Hkv, N, dtype=torch.uint8, device=score.device)
+    _check(lib().kvs_threshold_keep(_ptr(score), Hkv, N, float(tau), int(window), int(keep_width), _ptr(bits),
+                                    _stream(stream)), "kvs_threshold_keep")
+    return bits

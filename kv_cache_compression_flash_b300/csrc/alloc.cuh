@@ -64,11 +64,65 @@ struct AllocParams {
   double c[4];      // chord slopes, descending
   int cost[4];      // step sizes b_{k+1} - b_k
   int width[5];     // allowed widths, ascending, width[0] = 0
+  int dyadic;       // every c_k = n_k 2^-e_k exactly (n_k < 2^16): thetas from integer arithmetic
+  unsigned n[4];
+  int e[4];
   AllocHeader* hdr;
   unsigned long long* hist;       // [kRadixPasses][kRadixBins] cost-weighted counts
   unsigned long long* tie_block;  // [gridDim.x]
   FixCand* cand;                  // [kMaxFixRounds][gridDim.x]
 };
+
+// key = (double)w * (double)sigma is exact: its significand is the product of
+// the two 24-bit significands.  KeyParts holds that product M (< 2^48) and the
+// exponent E of its lowest bit; M == 0 when the key is 0.
+struct KeyParts {
+  unsigned long long M;
+  int E;
+};
+
+__device__ __forceinline__ KeyParts key_parts(float w, float s) {
+  const uint32_t wb = __float_as_uint(w), sb = __float_as_uint(s);
+  uint32_t ew = (wb >> 23) & 0xFFu, es = (sb >> 23) & 0xFFu;
+  uint32_t mw = wb & 0x7FFFFFu, ms = sb & 0x7FFFFFu;
+  if (ew) mw |= 0x800000u; else ew = 1u;  // subnormal: no implicit bit, exponent of 1
+  if (es) ms |= 0x800000u; else es = 1u;
+  KeyParts kp;
+  kp.M = static_cast<unsigned long long>(mw) * ms;
+  kp.E = static_cast<int>(ew + es) - 300;
+  return kp;
+}
+
+// Bit pattern of theta = fl64(c_k * key) for finite w, sigma >= 0 (0 when the
+// key is 0).  With dyadic slopes c_k = n_k 2^-e_k the product n_k M (< 2^64)
+// is formed exactly in integers and rounded once to 53 bits, half to even:
+// the same double the fp64 multiply gives, without the fp64 pipe (slow on this
+// part).
+__device__ __forceinline__ unsigned long long theta_from_parts(const AllocParams& p, const KeyParts& kp, int k) {
+  if (kp.M == 0ull) return 0ull;
+  const unsigned long long P = kp.M * p.n[k];
+  const int lz = __clzll(static_cast<long long>(P));
+  const unsigned long long Pn = P << lz;  // leading one at bit 63
+  unsigned long long mant = Pn >> 11;     // 53 bits
+  const unsigned rest = static_cast<unsigned>(Pn & 0x7FFull);
+  int ex = 63 - lz + kp.E - p.e[k];       // value = 1.f * 2^ex
+  if (rest > 0x400u || (rest == 0x400u && (mant & 1ull))) {
+    ++mant;
+    if (mant == (1ull << 53)) {
+      mant >>= 1;
+      ++ex;
+    }
+  }
+  return (static_cast<unsigned long long>(ex + 1023) << 52) | (mant & ((1ull << 52) - 1ull));
+}
+
+__device__ __forceinline__ unsigned long long theta_bits(const AllocParams& p, float w, float s, int k) {
+  if (!p.dyadic) {
+    const double key = static_cast<double>(w) * static_cast<double>(s);
+    return key > 0.0 ? static_cast<unsigned long long>(__double_as_longlong(p.c[k] * key)) : 0ull;
+  }
+  return theta_from_parts(p, key_parts(w, s), k);
+}
 
 __device__ __forceinline__ unsigned long long ld_vol(const unsigned long long* p) {
   return *reinterpret_cast<const volatile unsigned long long*>(p);
@@ -144,8 +198,7 @@ struct ThetaSource {
   long long u_begin;
   __device__ __forceinline__ unsigned long long operator()(long long u, int k) const {
     if (CACHE) return cache[static_cast<long long>(k) * p.per + (u - u_begin)];
-    const double key = static_cast<double>(p.w[u]) * static_cast<double>(p.sigma[u]);
-    return key > 0.0 ? static_cast<unsigned long long>(__double_as_longlong(p.c[k] * key)) : 0ull;
+    return theta_bits(p, p.w[u], p.sigma[u], k);
   }
 };
 
@@ -186,8 +239,7 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
     if (key > 0.0) my_total += static_cast<unsigned long long>(full_cost);
     if (CACHE)
       for (int k = 0; k < p.K; ++k)
-        s_theta[static_cast<long long>(k) * p.per + (u - u_begin)] =
-            key > 0.0 ? static_cast<unsigned long long>(__double_as_longlong(p.c[k] * key)) : 0ull;
+        s_theta[static_cast<long long>(k) * p.per + (u - u_begin)] = key > 0.0 ? theta_bits(p, wf, sf, k) : 0ull;
   }
   const unsigned long long blk_total = block_sum(my_total, s_red);
   const int blk_bad = __syncthreads_or(my_bad);

@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "alloc.cuh"
+#include "alloc_cluster.cuh"
 #include "common.cuh"
 #include "norms.cuh"
 #include "pack.cuh"
@@ -146,7 +147,7 @@ struct ScoreWs {
 size_t carve_score(const ScorePlan& pl, void* base, size_t cap, ScoreWs* w) {
   WsCarver c{static_cast<char*>(base), 0, cap};
   const ScoreGeom& g = pl.geo;
-  w->part1 = pl.lse_given ? nullptr : c.take<float2>(static_cast<size_t>(g.n_rt) * pl.n_split1 * 128);
+  w->part1 = pl.lse_given ? nullptr : c.take<float2>(static_cast<size_t>(g.n_rt) * pl.n_split1 * 256);
   w->b_plain = (pl.want_wt || (pl.want_max && !pl.want_plus)) ? c.take<float>(static_cast<size_t>(g.n_rt) * 128)
                                                               : nullptr;
   w->b_scaled = pl.want_plus ? c.take<float>(static_cast<size_t>(g.n_rt) * 128) : nullptr;
@@ -257,6 +258,85 @@ size_t alloc_ws_bytes(int nb) {
   return c.used;
 }
 
+// The one-cluster allocator, one instantiation per cluster size.
+using ClusterAllocFn = void (*)(AllocParams, int);
+ClusterAllocFn cluster_alloc_fn(int cl) {
+  switch (cl) {
+    case 1: return allocate_cluster_kernel<1>;
+    case 2: return allocate_cluster_kernel<2>;
+    case 4: return allocate_cluster_kernel<4>;
+    case 8: return allocate_cluster_kernel<8>;
+    case 16: return allocate_cluster_kernel<16>;
+    default: return nullptr;
+  }
+}
+
+cudaLaunchConfig_t cluster_cfg(int cl, size_t smem, cudaStream_t st, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cl));
+  cfg.blockDim = dim3(kCAThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Cluster size, units per CTA, candidate capacity and shared memory of the
+// one-cluster allocator, or *CL = 0 when the pool does not fit one cluster
+// (or no cluster of the needed size can be scheduled).
+int plan_cluster_alloc(long long U, int K, int* CL, long long* per, int* cand_cap, size_t* smem) {
+  *CL = 0;
+  // once per process: the shared-memory cap and which cluster sizes can be
+  // scheduled with that much shared memory per CTA
+  static size_t cap = 0;
+  static bool sched[kCAMaxCluster + 1] = {};
+  static std::once_flag once;
+  static cudaError_t init_err = cudaSuccess;
+  std::call_once(once, [] {
+    int dev = 0, max_smem = 0;
+    init_err = cudaGetDevice(&dev);
+    if (init_err == cudaSuccess)
+      init_err = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cap = max_smem > 4096 ? static_cast<size_t>(max_smem - 4096) : 0;  // room for the static part
+    for (int cl = 1; init_err == cudaSuccess && cl <= kCAMaxCluster; cl *= 2) {
+      ClusterAllocFn fn = cluster_alloc_fn(cl);
+      init_err = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (init_err == cudaSuccess)
+        init_err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(cap));
+      if (init_err != cudaSuccess) break;
+      cudaLaunchAttribute attr[1];
+      const cudaLaunchConfig_t cfg = cluster_cfg(cl, cap, nullptr, attr);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
+      sched[cl] = n > 0;
+    }
+  });
+  if (init_err != cudaSuccess) return KVS_ERR_CUDA;
+  const long long items = U * K;
+  int cl = 1;
+  while (cl < kCAMaxCluster && static_cast<long long>(cl) * 8192 < items) cl *= 2;
+  for (; cl <= kCAMaxCluster; cl *= 2) {
+    const long long pr = cdiv(U, cl);
+    const size_t base = ca_smem_bytes(pr, K, cl, 0);
+    if (base + 256 * sizeof(CACand) > cap || !sched[cl]) continue;
+    const int cc = static_cast<int>(std::min<size_t>(4096, (cap - base) / sizeof(CACand)));
+    *CL = cl;
+    *per = pr;
+    *cand_cap = cc;
+    *smem = ca_smem_bytes(pr, K, cl, cc);
+    return KVS_OK;
+  }
+  return KVS_OK;
+}
+
 // ---- packing --------------------------------------------------------------------
 StreamPtrs to_ptrs(const kvs_stream_set* s, bool with_counts) {
   StreamPtrs p;
@@ -285,24 +365,21 @@ bool streams_ok(const kvs_stream_set* s) {
 }
 
 struct PackWs {
-  int* chunk;
-  int* rank;
   int* kept;
   int* n_kept;
+  long long* chan_base;
 };
 
 size_t carve_pack(int64_t Hkv, int64_t N, int64_t d, int axis, void* base, size_t cap, PackWs* w) {
   WsCarver c{static_cast<char*>(base), 0, cap};
-  if (axis == 0) {
-    const long long U = Hkv * N;
-    w->chunk = c.take<int>(static_cast<size_t>(cdiv(U, kPlanChunk)) * 4);
-    w->rank = c.take<int>(static_cast<size_t>(U));
-    w->kept = w->n_kept = nullptr;
-  } else {
-    w->chunk = nullptr;
-    w->rank = c.take<int>(static_cast<size_t>(Hkv * d));
+  w->kept = w->n_kept = nullptr;
+  w->chan_base = nullptr;
+  if (axis == 1) {
     w->kept = c.take<int>(static_cast<size_t>(Hkv * N));
     w->n_kept = c.take<int>(static_cast<size_t>(Hkv));
+    w->chan_base = c.take<long long>(static_cast<size_t>(Hkv * d));
+  } else {
+    c.take<int>(1);  // no scratch; keep a non-zero size for callers that pass one
   }
   return c.used;
 }
@@ -311,6 +388,54 @@ int pack_shape_ok(int64_t Hkv, int64_t N, int64_t d, int axis) {
   if (Hkv <= 0 || N <= 0 || d <= 0 || (axis != 0 && axis != 1)) return KVS_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return KVS_ERR_UNSUPPORTED;
   if (Hkv * N >= (1ll << 31)) return KVS_ERR_UNSUPPORTED;
+  // channel plan: per-width unit counts in 16 bits, group counts in 32 bits
+  if (axis == 1 && (Hkv * d >= (1ll << 16) || Hkv * d * cdiv(N, 64) >= (1ll << 32))) return KVS_ERR_UNSUPPORTED;
+  return KVS_OK;
+}
+
+template <class F>
+cudaError_t set_cluster_attrs(F fn) {
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
+template <class F, class... A>
+cudaError_t launch_cluster(F fn, dim3 grid, int cl, int threads, size_t smem, cudaStream_t st, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, args...);
+}
+
+// the axis-0 plan on one cluster of CL CTAs
+int launch_rows_plan(const uint8_t* bits, long long U, int gpu, const StreamPtrs& sp, cudaStream_t st) {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] { err = set_cluster_attrs(rows_plan_kernel<16>); });
+  if (err != cudaSuccess) return KVS_ERR_CUDA;
+  int cl = 1;
+  while (cl < 16 && static_cast<long long>(cl) * 2048 < U) cl *= 2;
+  const long long per = cdiv(U, cl);
+  cudaError_t e;
+  switch (cl) {
+    case 1: e = launch_cluster(rows_plan_kernel<1>, dim3(1), 1, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
+    case 2: e = launch_cluster(rows_plan_kernel<2>, dim3(2), 2, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
+    case 4: e = launch_cluster(rows_plan_kernel<4>, dim3(4), 4, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
+    case 8: e = launch_cluster(rows_plan_kernel<8>, dim3(8), 8, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
+    default: e = launch_cluster(rows_plan_kernel<16>, dim3(16), 16, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
+  }
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return KVS_ERR_CUDA;
+  }
   return KVS_OK;
 }
 
@@ -318,37 +443,38 @@ template <int DH>
 int pack_dh(const uint16_t* X, int64_t Hkv, int64_t N, int axis, const uint8_t* bits, const uint8_t* keep,
             const kvs_stream_set* s, const PackWs& w, cudaStream_t st, bool dequant, float* out) {
   const int sms = sm_count();
-  if (axis == 0 && dequant) {  // decode straight from the stream entries
-    const long long rows = Hkv * N;
-    const StreamPtrs sp = to_ptrs(s, true);
-    const int zb = static_cast<int>(std::min<long long>(cdiv(rows * (DH / 4), 256), static_cast<long long>(sms) * 16));
-    zero_dropped_rows_kernel<DH><<<zb, 256, 0, st>>>(bits, rows, out);
-    const int blocks = static_cast<int>(std::min<long long>(cdiv(rows * (DH / 64), 16), static_cast<long long>(sms) * 16));
-    dequant_entries_rows_kernel<DH><<<blocks, 256, 0, st>>>(sp, out);
-  } else if (axis == 0) {
+  if (axis == 0) {
     const long long U = Hkv * N;
-    const int nchunk = static_cast<int>(cdiv(U, kPlanChunk));
     const StreamPtrs sp = to_ptrs(s, true);
-    plan_count_kernel<<<nchunk, kPlanThreads, 0, st>>>(bits, U, w.chunk);
-    plan_scan_kernel<<<1, 1024, 0, st>>>(w.chunk, nchunk, DH / 64, sp);
-    plan_rank_kernel<<<nchunk, kPlanThreads, 0, st>>>(bits, U, w.chunk, DH / 64, w.rank, sp, 1);
     const long long ngroups = U * (DH / 64);
-    const int blocks = static_cast<int>(std::min<long long>(cdiv(ngroups, 16), static_cast<long long>(sms) * 16));
-    pack_rows_kernel<DH><<<blocks, 256, 0, st>>>(X, bits, w.rank, U, sp);
+    const int blocks = static_cast<int>(std::min<long long>(cdiv(ngroups, 16), static_cast<long long>(sms) * 8));
+    if (dequant) {  // decode straight from the stream entries
+      dequant_rows_kernel<DH><<<blocks, 256, 0, st>>>(sp, bits, U, out);
+    } else {
+      const int rc = launch_rows_plan(bits, U, DH / 64, sp, st);
+      if (rc) return rc;
+      pack_rows_kernel<DH><<<blocks, 256, 0, st>>>(X, sp);
+    }
   } else {
     const StreamPtrs sp = to_ptrs(s, !dequant);
-    kept_index_kernel<<<static_cast<int>(Hkv), 1024, 0, st>>>(keep, static_cast<int>(N), w.kept, w.n_kept);
-    plan_channels_kernel<<<1, kPlanChannelThreads, 0, st>>>(bits, static_cast<int>(Hkv * DH), DH, w.n_kept, w.rank, sp,
-                                                     dequant ? 0 : 1);
-    const dim3 grid(static_cast<unsigned>(cdiv(N, 64)), static_cast<unsigned>(Hkv));
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+      err = set_cluster_attrs(channels_plan_kernel<64>);
+      if (err == cudaSuccess) err = set_cluster_attrs(channels_plan_kernel<128>);
+    });
+    if (err != cudaSuccess) return KVS_ERR_CUDA;
+    const int cl = static_cast<int>(std::min<int64_t>(Hkv, 16));
+    KVS_CUDA_TRY(launch_cluster(channels_plan_kernel<DH>, dim3(static_cast<unsigned>(cl)), cl, kPlanThreads, 0, st,
+                                keep, static_cast<int>(N), static_cast<int>(Hkv), bits, w.kept, w.n_kept, w.chan_base,
+                                sp, dequant ? 0 : 1));
     if (dequant) {
-      const long long rows = Hkv * N;
-      const int zb = static_cast<int>(std::min<long long>(cdiv(rows * (DH / 4), 256), static_cast<long long>(sms) * 16));
-      zero_dropped_rows_kernel<DH><<<zb, 256, 0, st>>>(keep, rows, out);
-      dequant_channels_kernel<DH><<<grid, 256, 0, st>>>(sp, static_cast<int>(N), bits, w.rank, w.kept, w.n_kept,
+      const dim3 grid(static_cast<unsigned>(cdiv(N, 64) + 1), static_cast<unsigned>(Hkv));
+      dequant_channels_kernel<DH><<<grid, 256, 0, st>>>(sp, static_cast<int>(N), bits, w.chan_base, w.kept, w.n_kept,
                                                         out);
     } else {
-      pack_channels_kernel<DH><<<grid, 256, 0, st>>>(X, static_cast<int>(N), bits, w.rank, w.kept, w.n_kept, sp);
+      const dim3 grid(static_cast<unsigned>(cdiv(N, 64)), static_cast<unsigned>(Hkv));
+      pack_channels_kernel<DH><<<grid, 256, 0, st>>>(X, static_cast<int>(N), bits, w.chan_base, w.kept, w.n_kept, sp);
     }
   }
   return KVS_OK;
@@ -374,6 +500,35 @@ int pack_common(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis, 
   return KVS_OK;
 }
 
+// cluster size for column reductions over `rows` rows per group
+int colsq_cluster(long long rows) {
+  int cl = 1;
+  while (cl < 16 && static_cast<long long>(cl) * 256 < rows) cl *= 2;
+  return cl;
+}
+
+int launch_colsq(const uint16_t* A, long long rows_a, const uint8_t* keep, const uint16_t* B, long long rows_b,
+                 int64_t groups, int64_t d, int mode, float scale, float* out, cudaStream_t st) {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = set_cluster_attrs(colsq_cluster_kernel<64>);
+    if (err == cudaSuccess) err = set_cluster_attrs(colsq_cluster_kernel<128>);
+  });
+  if (err != cudaSuccess) return KVS_ERR_CUDA;
+  const int cl = colsq_cluster(std::max(rows_a, rows_b));
+  const dim3 grid(static_cast<unsigned>(cl), static_cast<unsigned>(groups));
+  const cudaError_t e =
+      d == 64 ? launch_cluster(colsq_cluster_kernel<64>, grid, cl, kColThreads, 0, st, A, static_cast<int>(rows_a), keep,
+                               B, static_cast<int>(rows_b), mode, scale, out)
+              : launch_cluster(colsq_cluster_kernel<128>, grid, cl, kColThreads, 0, st, A, static_cast<int>(rows_a),
+                               keep, B, static_cast<int>(rows_b), mode, scale, out);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return KVS_ERR_CUDA;
+  }
+  return KVS_OK;
+}
 }  // namespace
 
 // =============================================================================
@@ -457,54 +612,34 @@ int kvs_score_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
 }
 
 size_t kvs_channel_weights_workspace_size(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d) {
-  if (Hq <= 0 || Hkv <= 0 || W <= 0 || N <= 0 || Hq % Hkv) return 0;
-  WsCarver c{nullptr, 0, 0};
-  const long long nq = cdiv((Hq / Hkv) * W, kColChunkRows), nk = cdiv(N, kColChunkRows);
-  c.take<float>(static_cast<size_t>(Hkv * nq * d));
-  c.take<float>(static_cast<size_t>(Hkv * nk * d));
-  return c.used;
+  (void)Hq, (void)Hkv, (void)W, (void)N, (void)d;
+  return 0;  // one cluster per group reduces in shared memory
 }
+
 
 int kvs_channel_weights(const uint16_t* Q, const uint16_t* K, int64_t Hq, int64_t Hkv, int64_t W, int64_t N,
                         int64_t d, float* w_c, void* workspace, size_t workspace_bytes, void* stream) {
+  (void)workspace, (void)workspace_bytes;
   if (Hq <= 0 || Hkv <= 0 || W <= 0 || N <= 0 || d <= 0 || Hq % Hkv) return KVS_ERR_INVALID_ARG;
   if (!Q || !K || !w_c || !aligned16(Q) || !aligned16(K)) return KVS_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return KVS_ERR_UNSUPPORTED;
   if (Hkv * N >= (1ll << 31) || Hq * W >= (1ll << 31)) return KVS_ERR_UNSUPPORTED;
-  const long long rq = (Hq / Hkv) * W;
-  const long long nq = cdiv(rq, kColChunkRows), nk = cdiv(N, kColChunkRows);
-  WsCarver c{static_cast<char*>(workspace), 0, workspace_bytes};
-  float* qp = c.take<float>(static_cast<size_t>(Hkv * nq * d));
-  float* kp = c.take<float>(static_cast<size_t>(Hkv * nk * d));
-  if (!c.ok() || !workspace) return KVS_ERR_WORKSPACE;
-  cudaStream_t st = as_stream(stream);
-  const dim3 gq(static_cast<unsigned>(nq), static_cast<unsigned>(Hkv)), gk(static_cast<unsigned>(nk), static_cast<unsigned>(Hkv));
-  if (d == 64) {
-    colsumsq_kernel<64><<<gq, kNormThreads, 0, st>>>(Q, static_cast<int>(rq), nullptr, qp, nullptr);
-    colsumsq_kernel<64><<<gk, kNormThreads, 0, st>>>(K, static_cast<int>(N), nullptr, kp, nullptr);
-  } else {
-    colsumsq_kernel<128><<<gq, kNormThreads, 0, st>>>(Q, static_cast<int>(rq), nullptr, qp, nullptr);
-    colsumsq_kernel<128><<<gk, kNormThreads, 0, st>>>(K, static_cast<int>(N), nullptr, kp, nullptr);
-  }
-  const int n = static_cast<int>(Hkv * d);
-  channel_weight_finalize_kernel<<<static_cast<int>(cdiv(n, 8)), 256, 0, st>>>(
-      qp, static_cast<int>(nq), kp, static_cast<int>(nk), static_cast<int>(Hkv), static_cast<int>(d),
-      static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))), w_c);
+  const long long rq = (Hq / Hkv) * W;  // the group's query rows are contiguous in Q
+  const int rc = launch_colsq(Q, rq, nullptr, K, N, Hkv, d, kColChannelWeight,
+                              static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))), w_c, as_stream(stream));
+  if (rc) return rc;
   KVS_CUDA_TRY(cudaGetLastError());
   return KVS_OK;
 }
 
 size_t kvs_unit_rms_workspace_size(int64_t Hkv, int64_t N, int64_t d, int axis) {
-  if (axis == 0) return 0;
-  WsCarver c{nullptr, 0, 0};
-  const long long nk = cdiv(N, kColChunkRows);
-  c.take<float>(static_cast<size_t>(Hkv * nk * d));
-  c.take<int>(static_cast<size_t>(Hkv * nk));
-  return c.used;
+  (void)Hkv, (void)N, (void)d, (void)axis;
+  return 0;
 }
 
 int kvs_unit_rms(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis, const uint8_t* keep_bits,
                  float* sigma, void* workspace, size_t workspace_bytes, void* stream) {
+  (void)workspace, (void)workspace_bytes;
   if (Hkv <= 0 || N <= 0 || d <= 0 || (axis != 0 && axis != 1)) return KVS_ERR_INVALID_ARG;
   if (!X || !sigma || !aligned16(X)) return KVS_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return KVS_ERR_UNSUPPORTED;
@@ -513,26 +648,15 @@ int kvs_unit_rms(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis,
   const int sms = sm_count();
   if (axis == 0) {
     const long long rows = Hkv * N;
-    const int rpb = kNormThreads / (static_cast<int>(d) / 8);
-    const int blocks = static_cast<int>(std::min<long long>(cdiv(rows, rpb), static_cast<long long>(sms) * 16));
+    const int rpb = kNormThreads / (static_cast<int>(d) / 8) * 4;
+    const int blocks = static_cast<int>(std::min<long long>(cdiv(rows, rpb), static_cast<long long>(sms) * 8));
     if (d == 64)
       row_rms_kernel<64><<<blocks, kNormThreads, 0, st>>>(X, static_cast<int>(rows), sigma);
     else
       row_rms_kernel<128><<<blocks, kNormThreads, 0, st>>>(X, static_cast<int>(rows), sigma);
   } else {
-    const long long nk = cdiv(N, kColChunkRows);
-    WsCarver c{static_cast<char*>(workspace), 0, workspace_bytes};
-    float* part = c.take<float>(static_cast<size_t>(Hkv * nk * d));
-    int* cnt = c.take<int>(static_cast<size_t>(Hkv * nk));
-    if (!c.ok() || !workspace) return KVS_ERR_WORKSPACE;
-    const dim3 grid(static_cast<unsigned>(nk), static_cast<unsigned>(Hkv));
-    if (d == 64)
-      colsumsq_kernel<64><<<grid, kNormThreads, 0, st>>>(X, static_cast<int>(N), keep_bits, part, cnt);
-    else
-      colsumsq_kernel<128><<<grid, kNormThreads, 0, st>>>(X, static_cast<int>(N), keep_bits, part, cnt);
-    const int n = static_cast<int>(Hkv * d);
-    masked_rms_finalize_kernel<<<static_cast<int>(cdiv(n, 8)), 256, 0, st>>>(
-        part, cnt, static_cast<int>(nk), static_cast<int>(Hkv), static_cast<int>(d), sigma);
+    const int rc = launch_colsq(X, N, keep_bits, nullptr, 0, Hkv, d, kColMaskedRms, 1.f, sigma, st);
+    if (rc) return rc;
   }
   KVS_CUDA_TRY(cudaGetLastError());
   return KVS_OK;
@@ -550,6 +674,7 @@ int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t bud
   if (U == 0) return KVS_OK;
   if (!w || !sigma || !bits) return KVS_ERR_INVALID_ARG;
   cudaStream_t st = as_stream(stream);
+  int rc = KVS_OK;
   AllocParams p;
   std::memset(&p, 0, sizeof(p));
   int nw = 1;
@@ -568,9 +693,50 @@ int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t bud
     p.min_cost = std::min(p.min_cost, p.cost[k]);
     p.c[k] = (std::ldexp(1.0, -b0) - std::ldexp(1.0, -b1)) / static_cast<double>(b1 - b0);
   }
-  // Preferred: a few thousand units per block with their thetas cached in
-  // shared memory; needs every block co-resident.  Otherwise fall back to
-  // recomputing thetas from w and sigma in every pass.
+  // c_k = (2^(b1-b0) - 1) / ((b1-b0) 2^b1): dyadic unless b1-b0 keeps an odd factor
+  p.dyadic = 1;
+  for (int k = 0; k < p.K; ++k) {
+    const int b0 = p.width[k], b1 = p.width[k + 1], d = b1 - b0;
+    unsigned long long num = (1ull << d) - 1ull, den = static_cast<unsigned long long>(d);
+    int e = b1;
+    for (unsigned long long q = 3; q <= den; q += 2)
+      while (den % q == 0 && num % q == 0) {
+        den /= q;
+        num /= q;
+      }
+    while ((den & 1ull) == 0ull) {
+      den >>= 1;
+      ++e;
+    }
+    if (den != 1ull || num >= (1ull << 16)) {
+      p.dyadic = 0;
+      break;
+    }
+    p.n[k] = static_cast<unsigned>(num);
+    p.e[k] = e;
+  }
+  p.w = w;
+  p.sigma = sigma;
+  p.bits = bits;
+  p.U = U;
+  p.B = static_cast<unsigned long long>(budget_bits);
+  // Preferred: one thread-block cluster holds every item's threshold in
+  // shared memory and needs no workspace.
+  int CL = 0, cand_cap = 0;
+  long long per = 0;
+  size_t ca_smem = 0;
+  rc = plan_cluster_alloc(U, p.K, &CL, &per, &cand_cap, &ca_smem);
+  if (rc) return rc;
+  if (CL > 0) {
+    p.per = per;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = cluster_cfg(CL, ca_smem, st, attr);
+    KVS_CUDA_TRY(cudaLaunchKernelEx(&cfg, cluster_alloc_fn(CL), p, cand_cap));
+    return KVS_OK;
+  }
+  // Otherwise a cooperative grid: a few thousand units per block with their
+  // thetas cached in shared memory (every block co-resident), or, failing
+  // that, thetas recomputed from w and sigma in every pass.
   const int sms = sm_count();
   const size_t cache_smem = static_cast<size_t>(kAllocUnitsPerBlock) * p.K * sizeof(unsigned long long);
   KVS_CUDA_TRY(allow_smem(allocate_kernel<true>, cache_smem));
@@ -590,11 +756,6 @@ int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t bud
   p.tie_block = c.take<unsigned long long>(static_cast<size_t>(nb));
   p.cand = c.take<FixCand>(static_cast<size_t>(kMaxFixRounds) * nb);
   if (!c.ok() || !workspace) return KVS_ERR_WORKSPACE;
-  p.w = w;
-  p.sigma = sigma;
-  p.bits = bits;
-  p.U = U;
-  p.B = static_cast<unsigned long long>(budget_bits);
   KVS_CUDA_TRY(cudaMemsetAsync(p.hdr, 0, sizeof(AllocHeader), st));
   void* args[] = {&p};
   if (cached) {
@@ -640,6 +801,21 @@ int kvs_dequantize(const kvs_stream_set* streams, int64_t Hkv, int64_t N, int64_
                    const uint8_t* keep_bits, float* out, void* workspace, size_t workspace_bytes, void* stream) {
   return pack_common(nullptr, Hkv, N, d, axis, bits, keep_bits, streams, workspace, workspace_bytes, stream, true,
                      out);
+}
+
+int kvs_threshold_keep(const float* score, int64_t Hkv, int64_t N, float tau, int64_t window,
+                       uint32_t keep_width, uint8_t* bits, void* stream) {
+  if (Hkv <= 0 || N <= 0 || window < 0 || !score || !bits) return KVS_ERR_INVALID_ARG;
+  if (keep_width != 2 && keep_width != 4 && keep_width != 8 && keep_width != 16) return KVS_ERR_INVALID_ARG;
+  if (Hkv * N >= (1ll << 31)) return KVS_ERR_UNSUPPORTED;
+  if (N % 4 == 0 && (!aligned16(score) || (reinterpret_cast<uintptr_t>(bits) & 3u))) return KVS_ERR_INVALID_ARG;
+  const long long total = Hkv * N;
+  const int blocks = static_cast<int>(std::min<long long>(cdiv(total, 1024), static_cast<long long>(sm_count()) * 8));
+  threshold_keep_kernel<<<blocks, 256, 0, as_stream(stream)>>>(score, total, static_cast<int>(N), tau,
+                                                               static_cast<int>(std::min<int64_t>(window, N)),
+                                                               static_cast<uint8_t>(keep_width), bits);
+  KVS_CUDA_TRY(cudaGetLastError());
+  return KVS_OK;
 }
 
 }  // extern "C"

@@ -6,6 +6,8 @@
 // reductions (so results are deterministic).
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace kvs {
@@ -113,26 +115,201 @@ __global__ void masked_rms_finalize_kernel(const float* __restrict__ part, const
   if ((threadIdx.x & 31) == 0) sigma[idx] = n > 0 ? sqrtf(s / static_cast<float>(n)) : 0.f;
 }
 
-// sigma[row] = sqrt(mean_c X[row][c]^2); DH/8 threads per row
+// sigma[row] = sqrt(mean_c X[row][c]^2); DH/8 threads per row, four rows per
+// thread in flight
 template <int DH>
 __global__ void __launch_bounds__(kNormThreads) row_rms_kernel(const uint16_t* __restrict__ X, const int rows,
                                                                float* __restrict__ sigma) {
   constexpr int TPR = DH / 8;
   constexpr int RPB = kNormThreads / TPR;
   const int sub = threadIdx.x % TPR;
-  for (int base = blockIdx.x * RPB; base < rows; base += gridDim.x * RPB) {
-    const int r = base + static_cast<int>(threadIdx.x / TPR);
-    float acc = 0.f;
-    if (r < rows) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(X + static_cast<size_t>(r) * DH + sub * 8));
-      float f[8];
-      bf16x8_to_f32(u, f);
+  for (int base = blockIdx.x * RPB * 4; base < rows; base += gridDim.x * RPB * 4) {
+    uint4 u[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc = fmaf(f[k], f[k], acc);
+    for (int j = 0; j < 4; ++j) {
+      const int r = base + j * RPB + static_cast<int>(threadIdx.x / TPR);
+      u[j] = r < rows ? __ldg(reinterpret_cast<const uint4*>(X + static_cast<size_t>(r) * DH + sub * 8))
+                      : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-    if (sub == 0 && r < rows) sigma[r] = sqrtf(acc / static_cast<float>(DH));
+    for (int j = 0; j < 4; ++j) {
+      const int r = base + j * RPB + static_cast<int>(threadIdx.x / TPR);
+      float f[8];
+      bf16x8_to_f32(u[j], f);
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc = fmaf(f[k], f[k], acc);
+#pragma unroll
+      for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+      if (sub == 0 && r < rows) sigma[r] = sqrtf(acc / static_cast<float>(DH));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Column sums of squares on one thread-block cluster per group: CTA r of the
+// cluster reduces rows [r*R, r*R + R) of group g (and of a second tensor B
+// when given), the cluster's CTA 0 adds the CTAs' partials in rank order
+// through distributed shared memory and writes the result, so no workspace
+// and no second launch is needed (and the sum order is fixed).
+//   mode kColChannelWeight: out[g][c] = sqrt(sum_A) sqrt(sum_B) * scale  (w_c)
+//   mode kColMaskedRms:     out[g][c] = sqrt(sum_A over kept rows / kept), 0 if none
+// grid (CL, groups), cluster (CL, 1, 1), kColThreads threads.
+// ---------------------------------------------------------------------------
+constexpr int kColThreads = 512;
+constexpr int kColChannelWeight = 0;
+constexpr int kColMaskedRms = 1;
+
+template <int DH>
+__device__ __forceinline__ void colsq_rows(const uint16_t* __restrict__ X, const uint8_t* __restrict__ keep,
+                                           const int r_begin, const int r_end, float (&acc)[8], int* n_kept) {
+  constexpr int TPR = DH / 8;                // threads per row, 8 channels each
+  constexpr int RPI = kColThreads / TPR;     // rows per step
+  const int rsub = threadIdx.x / TPR, cseg = (threadIdx.x % TPR) * 8;
+  int n = 0;
+  for (int base = r_begin + rsub; base < r_end; base += 4 * RPI) {
+    uint4 u[4];
+    bool ok[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // four independent 16-byte loads in flight
+      const int r = base + j * RPI;
+      ok[j] = r < r_end && (keep == nullptr || keep[r] != 0);
+      u[j] = ok[j] ? __ldg(reinterpret_cast<const uint4*>(X + static_cast<size_t>(r) * DH + cseg))
+                   : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float f[8];
+      bf16x8_to_f32(u[j], f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] = fmaf(f[k], f[k], acc[k]);
+      n += ok[j] ? 1 : 0;
+    }
+  }
+  *n_kept = n;
+}
+
+// per-CTA column partials: red[c] = sum over the CTA's rows (fixed order)
+template <int DH>
+__device__ __forceinline__ void colsq_block_reduce(const float (&acc)[8], float* red_rows /*[RPI][DH]*/,
+                                                   float* out /*[DH]*/) {
+  constexpr int TPR = DH / 8;
+  constexpr int RPI = kColThreads / TPR;
+  const int rsub = threadIdx.x / TPR, cseg = (threadIdx.x % TPR) * 8;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) red_rows[rsub * DH + cseg + k] = acc[k];
+  __syncthreads();
+  for (int c = threadIdx.x; c < DH; c += kColThreads) {
+    float s = 0.f;
+    for (int i = 0; i < RPI; ++i) s += red_rows[i * DH + c];
+    out[c] = s;
+  }
+}
+
+template <int DH>
+__global__ void __launch_bounds__(kColThreads, 1) colsq_cluster_kernel(
+    const uint16_t* __restrict__ A, const int rows_a, const uint8_t* __restrict__ keep_a,
+    const uint16_t* __restrict__ B, const int rows_b, const int mode, const float scale, float* __restrict__ out) {
+  namespace cgn = cooperative_groups;
+  cgn::cluster_group cluster = cgn::this_cluster();
+  constexpr int TPR = DH / 8;
+  constexpr int RPI = kColThreads / TPR;
+  __shared__ float red_rows[RPI * DH];
+  __shared__ float part_a[DH], part_b[DH];
+  __shared__ int red_n[kColThreads / 32];
+  __shared__ int s_n;
+  const int CL = static_cast<int>(cluster.num_blocks());
+  const int r = static_cast<int>(cluster.block_rank());
+  const int g = blockIdx.y;
+  float acc[8];
+  int n = 0;
+  {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+    const int per = (rows_a + CL - 1) / CL;
+    const int r0 = min(rows_a, r * per), r1 = min(rows_a, r0 + per);
+    colsq_rows<DH>(A + static_cast<size_t>(g) * rows_a * DH, keep_a ? keep_a + static_cast<size_t>(g) * rows_a : nullptr,
+                   r0, r1, acc, &n);
+    colsq_block_reduce<DH>(acc, red_rows, part_a);
+  }
+  if (threadIdx.x % TPR != 0) n = 0;  // one count per row slot
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, o);
+  if ((threadIdx.x & 31) == 0) red_n[threadIdx.x >> 5] = n;
+  if (B != nullptr) {
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+    const int per = (rows_b + CL - 1) / CL;
+    const int r0 = min(rows_b, r * per), r1 = min(rows_b, r0 + per);
+    int nb;
+    colsq_rows<DH>(B + static_cast<size_t>(g) * rows_b * DH, nullptr, r0, r1, acc, &nb);
+    colsq_block_reduce<DH>(acc, red_rows, part_b);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int i = 0; i < kColThreads / 32; ++i) t += red_n[i];
+    s_n = t;
+  }
+  cluster.sync();  // every CTA's partials are complete
+  if (r == 0) {
+    for (int c = threadIdx.x; c < DH; c += kColThreads) {
+      float sa = 0.f, sb = 0.f;
+      int nn = 0;
+      for (int q = 0; q < CL; ++q) {
+        sa += cluster.map_shared_rank(part_a, q)[c];
+        if (B != nullptr) sb += cluster.map_shared_rank(part_b, q)[c];
+        nn += *cluster.map_shared_rank(&s_n, q);
+      }
+      float v;
+      if (mode == kColChannelWeight)
+        v = sqrtf(sa) * sqrtf(sb) * scale;
+      else
+        v = nn > 0 ? sqrtf(sa / static_cast<float>(nn)) : 0.f;
+      out[static_cast<size_t>(g) * DH + c] = v;
+    }
+  }
+  cluster.sync();  // keep every CTA's shared memory until CTA 0 has read it
+}
+
+// ---------------------------------------------------------------------------
+// threshold pruning with a sliding window   [KVzap §2.3]
+// bits[g][t] = keep_width if score >= tau or t >= N - window, else 0; four
+// scores per thread (16-byte loads when the row allows)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) threshold_keep_kernel(const float* __restrict__ score, const long long total,
+                                                             const int N, const float tau, const int window,
+                                                             const uint8_t keep_width, uint8_t* __restrict__ bits) {
+  const bool vec = (N % 4) == 0;
+  for (long long i4 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 4; i4 < total;
+       i4 += static_cast<long long>(gridDim.x) * blockDim.x * 4) {
+    float v[4];
+    if (vec) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(score + i4));
+      v[0] = f.x, v[1] = f.y, v[2] = f.z, v[3] = f.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = i4 + e < total ? score[i4 + e] : 0.f;
+    }
+    uint32_t out = 0;
+    bool bad = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const long long i = i4 + e;
+      const int t = static_cast<int>(i % N);
+      if (!isfinite(v[e])) bad = true;
+      const bool keep = t >= N - window || (isfinite(v[e]) && v[e] >= tau);
+      out |= static_cast<uint32_t>(keep ? keep_width : 0) << (8 * e);
+    }
+    if (bad && i4 < total) record_error(KVS_ERR_RANGE);
+    if (vec) {
+      *reinterpret_cast<uint32_t*>(bits + i4) = out;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (i4 + e < total) bits[i4 + e] = static_cast<uint8_t>(out >> (8 * e));
+    }
   }
 }
 

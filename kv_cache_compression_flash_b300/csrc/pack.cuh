@@ -12,18 +12,20 @@
 // issues one aligned store of w/2 bytes and a half-warp writes its block in one
 // coalesced transaction.
 //
-// Stream order (ascending unit id within a width) comes from a three-kernel
-// plan: per-chunk counts, one exclusive scan over the chunks, per-unit ranks.
+// Stream order (ascending unit id within a width) comes from a plan computed
+// on one thread-block cluster (exclusive scans of the per-width unit and
+// group counts, exchanged through distributed shared memory); the pack and
+// dequantise kernels then run over the whole GPU.
 #pragma once
 
+#include <cooperative_groups.h>
 #include <cuda_fp16.h>
 
 #include "common.cuh"
 
 namespace kvs {
 
-constexpr int kPlanThreads = 256;
-constexpr int kPlanChunk = kPlanThreads * 4;
+constexpr int kPlanThreads = 512;
 
 struct StreamPtrs {
   uint8_t* codes[4];
@@ -41,6 +43,21 @@ __device__ __forceinline__ int width_slot(uint32_t w) {
 
 __device__ __forceinline__ unsigned half_mask() { return 0xFFFFu << (threadIdx.x & 16); }
 
+// round-half-even(x / s) for bf16 x and fp16 s > 0 with |x / s| <= 128, from
+// one reciprocal r ~ 1/s: floor(x r) is within one of the nearest integer
+// (|x r - x/s| <= 2^-16), and the choice between n0 = floor(x r) and n0 + 1
+// is the sign of x - (n0 + 1/2) s.  One FMA gives that sign exactly: the
+// product (n0 + 1/2) s has at most 20 significant bits, and a single rounding
+// never changes the sign of a difference nor makes a nonzero one zero.  A zero
+// difference is a tie, which goes to the even neighbour.
+__device__ __forceinline__ int round_div_even(const float x, const float s, const float r) {
+  const float n0 = floorf(x * r);
+  const float e = fmaf(-(n0 + 0.5f), s, x);
+  int n = static_cast<int>(n0);
+  if (e > 0.f || (e == 0.f && (n & 1))) ++n;
+  return n;
+}
+
 // Quantise this lane's 4 elements of a 64-element group (the half-warp holds
 // the group).  Returns the 4w code bits; *scale_bits gets the fp16 scale.
 __device__ __forceinline__ uint32_t quantize_lane4(const float (&x)[4], const int w, uint16_t* scale_bits,
@@ -56,10 +73,11 @@ __device__ __forceinline__ uint32_t quantize_lane4(const float (&x)[4], const in
   *scale_bits = __half_as_ushort(sh);
   uint32_t packed = 0;
   const uint32_t cmask = (1u << w) - 1u;
+  if (s > 0.f && !isinf(s)) {
+    const float r = __frcp_rn(s);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float q = s > 0.f ? rintf(__fdiv_rn(x[e], s)) : 0.f;
-    packed |= (static_cast<uint32_t>(static_cast<int>(q)) & cmask) << (w * e);
+    for (int e = 0; e < 4; ++e)
+      packed |= (static_cast<uint32_t>(round_div_even(x[e], s, r)) & cmask) << (w * e);
   }
   return packed;
 }
@@ -111,177 +129,262 @@ __device__ __forceinline__ void lane_bf16x4(const uint16_t* src, float (&x)[4], 
 }
 
 // ---------------------------------------------------------------------------
-// plan for token units (axis 0): rank of each unit within its width
+// plan for token units (axis 0): ids and group offsets of every stored unit
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kPlanThreads) plan_count_kernel(const uint8_t* __restrict__ bits,
-                                                                  const long long U,
-                                                                  int* __restrict__ chunk_counts) {
-  __shared__ int s_c[kPlanThreads / 32][4];
-  const long long base = static_cast<long long>(blockIdx.x) * kPlanChunk + threadIdx.x * 4;
-  int c[4] = {0, 0, 0, 0};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const long long u = base + e;
-    if (u < U) {
-      const int s = width_slot(bits[u]);
-      if (s >= 0) ++c[s];
-    }
-  }
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) c[s] += __shfl_xor_sync(0xFFFFFFFFu, c[s], o);
-  }
-  if ((threadIdx.x & 31) == 0)
-    for (int s = 0; s < 4; ++s) s_c[threadIdx.x >> 5][s] = c[s];
-  __syncthreads();
-  if (threadIdx.x < 4) {
-    int t = 0;
-    for (int i = 0; i < kPlanThreads / 32; ++i) t += s_c[i][threadIdx.x];
-    chunk_counts[blockIdx.x * 4 + threadIdx.x] = t;
-  }
+// Packs the four per-width counters of a thread into two u64 (32 bits each).
+__device__ __forceinline__ void plan_pack2(const unsigned (&c)[4], unsigned long long* lo, unsigned long long* hi) {
+  *lo = static_cast<unsigned long long>(c[0]) | (static_cast<unsigned long long>(c[1]) << 32);
+  *hi = static_cast<unsigned long long>(c[2]) | (static_cast<unsigned long long>(c[3]) << 32);
 }
 
-// single block: chunk counts -> exclusive offsets (in place); totals -> counts
-__global__ void __launch_bounds__(1024) plan_scan_kernel(int* __restrict__ chunk_counts, const int nchunk,
-                                                         const int groups_per_unit, const StreamPtrs sp) {
-  __shared__ long long s_tot[4];
-  if (threadIdx.x < 4) {
-    const int s = threadIdx.x;
-    long long run = 0;
-    for (int i = 0; i < nchunk; ++i) {
-      const int v = chunk_counts[i * 4 + s];
-      chunk_counts[i * 4 + s] = static_cast<int>(run);
-      run += v;
-    }
-    s_tot[s] = run;
+// exclusive scan over the block in thread order (kPlanThreads threads);
+// sbuf holds kPlanThreads/32 + 1 entries; *total = block sum.  Sums must stay
+// below 2^32 per 32-bit field.
+__device__ __forceinline__ unsigned long long plan_block_exscan(unsigned long long v, unsigned long long* sbuf,
+                                                                unsigned long long* total) {
+  constexpr int NW = kPlanThreads / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
   }
   __syncthreads();
-  if (threadIdx.x < 4) {
-    const int s = threadIdx.x;
-    const long long units = s_tot[s], groups = units * groups_per_unit;
+  if (lane == 31) sbuf[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long t = lane < NW ? sbuf[lane] : 0ull;
+    unsigned long long z = t;
+#pragma unroll
+    for (int o = 1; o < NW; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, z, o);
+      if (lane >= o) z += y;
+    }
+    if (lane < NW) sbuf[lane] = z - t;
+    if (lane == NW - 1) sbuf[NW] = z;
+  }
+  __syncthreads();
+  *total = sbuf[NW];
+  return sbuf[warp] + x - v;
+}
+
+// 16 width bytes starting at unit u (zero past `end`): one 16-byte load
+// when aligned and in range, else byte loads
+__device__ __forceinline__ uint4 load_bits16(const uint8_t* __restrict__ bits, const long long u, const long long end) {
+  if (u + 16 <= end && (reinterpret_cast<uintptr_t>(bits + u) & 15u) == 0)
+    return __ldg(reinterpret_cast<const uint4*>(bits + u));
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    if (u + e < end) w[e >> 2] |= static_cast<uint32_t>(bits[u + e]) << (8 * (e & 3));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ int bits16_at(const uint4& v, int e) {
+  const uint32_t w = e < 4 ? v.x : e < 8 ? v.y : e < 12 ? v.z : v.w;
+  return static_cast<int>((w >> (8 * (e & 3))) & 0xFFu);
+}
+
+// One cluster of CL CTAs; CTA r plans units [r*per, r*per + per) in steps of
+// kPlanThreads * 16 units, thread t taking 16 contiguous ones per step.
+// Writes ids[s][k] = unit and group_offsets[s][k] = k * groups_per_unit for
+// the k-th stored unit of width slot s, and counts.  Each step's ids are
+// staged in shared memory by width and then written out contiguously.
+template <int CL>
+__global__ void __launch_bounds__(kPlanThreads, 1) rows_plan_kernel(const uint8_t* __restrict__ bits,
+                                                                    const long long U, const long long per,
+                                                                    const int groups_per_unit, const StreamPtrs sp) {
+  namespace cgp = cooperative_groups;
+  cgp::cluster_group cluster = cgp::this_cluster();
+  const int rank = CL > 1 ? static_cast<int>(cluster.block_rank()) : 0;
+  constexpr int kStep = kPlanThreads * 16;
+  __shared__ unsigned long long sbuf[kPlanThreads / 32 + 1];
+  __shared__ unsigned long long s_tot[2];
+  __shared__ unsigned long long s_all[CL][2];
+  __shared__ int32_t stage[kStep];
+  __shared__ int s_seg[5];
+  const long long begin = static_cast<long long>(rank) * per;
+  const long long end = min(U, begin + per);
+  auto count16 = [&](const uint4& v, unsigned (&c)[4]) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int sl = width_slot(bits16_at(v, e));
+      if (sl >= 0) ++c[sl];
+    }
+  };
+  // totals of this CTA's range, then every CTA's, for the running prefix
+  unsigned long long tlo = 0, thi = 0;
+  for (long long b = begin; b < end; b += kStep) {
+    unsigned c[4] = {0u, 0u, 0u, 0u};
+    count16(load_bits16(bits, b + threadIdx.x * 16, end), c);
+    tlo += static_cast<unsigned long long>(c[0]) | (static_cast<unsigned long long>(c[1]) << 32);
+    thi += static_cast<unsigned long long>(c[2]) | (static_cast<unsigned long long>(c[3]) << 32);
+  }
+  {
+    unsigned long long a, bb;
+    (void)plan_block_exscan(tlo, sbuf, &a);
+    (void)plan_block_exscan(thi, sbuf, &bb);
+    if (threadIdx.x == 0) {
+      s_tot[0] = a;
+      s_tot[1] = bb;
+    }
+  }
+  if (CL > 1) cluster.sync();
+  else __syncthreads();
+  if (threadIdx.x < CL) {
+    const unsigned long long* rt = CL > 1 ? cluster.map_shared_rank(s_tot, static_cast<int>(threadIdx.x)) : s_tot;
+    s_all[threadIdx.x][0] = rt[0];
+    s_all[threadIdx.x][1] = rt[1];
+  }
+  __syncthreads();
+  unsigned long long plo = 0, phi = 0, glo = 0, ghi = 0;
+  for (int q = 0; q < CL; ++q) {
+    if (q < rank) {
+      plo += s_all[q][0];
+      phi += s_all[q][1];
+    }
+    glo += s_all[q][0];
+    ghi += s_all[q][1];
+  }
+  for (long long b = begin; b < end; b += kStep) {
+    const long long u0 = b + threadIdx.x * 16;
+    const uint4 v = load_bits16(bits, u0, end);
+    unsigned c[4] = {0u, 0u, 0u, 0u};
+    count16(v, c);
+    unsigned long long slo, shi;
+    const unsigned long long elo = plan_block_exscan(
+        static_cast<unsigned long long>(c[0]) | (static_cast<unsigned long long>(c[1]) << 32), sbuf, &slo);
+    const unsigned long long ehi = plan_block_exscan(
+        static_cast<unsigned long long>(c[2]) | (static_cast<unsigned long long>(c[3]) << 32), sbuf, &shi);
+    const int st[4] = {static_cast<int>(slo & 0xFFFFFFFFull), static_cast<int>(slo >> 32),
+                       static_cast<int>(shi & 0xFFFFFFFFull), static_cast<int>(shi >> 32)};
+    const int seg[5] = {0, st[0], st[0] + st[1], st[0] + st[1] + st[2], st[0] + st[1] + st[2] + st[3]};
+    int lr[4] = {seg[0] + static_cast<int>(elo & 0xFFFFFFFFull), seg[1] + static_cast<int>(elo >> 32),
+                 seg[2] + static_cast<int>(ehi & 0xFFFFFFFFull), seg[3] + static_cast<int>(ehi >> 32)};
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int sl = width_slot(bits16_at(v, e));
+      if (sl >= 0 && u0 + e < end) stage[lr[sl]++] = static_cast<int32_t>(u0 + e);
+    }
+    if (threadIdx.x < 5) s_seg[threadIdx.x] = seg[threadIdx.x];
+    __syncthreads();
+    const long long base[4] = {static_cast<long long>(plo & 0xFFFFFFFFull), static_cast<long long>(plo >> 32),
+                               static_cast<long long>(phi & 0xFFFFFFFFull), static_cast<long long>(phi >> 32)};
+    for (int j = threadIdx.x; j < s_seg[4]; j += kPlanThreads) {
+      int sl = 0;
+      while (sl < 3 && j >= s_seg[sl + 1]) ++sl;
+      const long long k = base[sl] + (j - s_seg[sl]);
+      if (k < sp.cap_units[sl]) {
+        sp.ids[sl][k] = stage[j];
+        sp.goff[sl][k] = k * groups_per_unit;
+      }
+    }
+    __syncthreads();  // the stage is reused by the next step
+    plo += slo;
+    phi += shi;
+  }
+  if (rank == CL - 1 && threadIdx.x < 4) {
+    const int sl = threadIdx.x;
+    const unsigned long long tot = sl == 0   ? (glo & 0xFFFFFFFFull)
+                                   : sl == 1 ? (glo >> 32)
+                                   : sl == 2 ? (ghi & 0xFFFFFFFFull)
+                                             : (ghi >> 32);
+    const long long units = static_cast<long long>(tot), groups = units * groups_per_unit;
     if (sp.counts) {
-      sp.counts[s] = units;
-      sp.counts[4 + s] = groups;
+      sp.counts[sl] = units;
+      sp.counts[4 + sl] = groups;
     }
-    if (units > sp.cap_units[s] || groups > sp.cap_groups[s]) record_error(KVS_ERR_RANGE);
+    if (units > sp.cap_units[sl] || groups > sp.cap_groups[sl]) record_error(KVS_ERR_RANGE);
   }
+  if (CL > 1) cluster.sync();  // keep shared memory alive until every CTA has read the totals
 }
 
-// per-unit ranks; with `sp` non-null also writes ids and group offsets
-__global__ void __launch_bounds__(kPlanThreads) plan_rank_kernel(const uint8_t* __restrict__ bits,
-                                                                 const long long U,
-                                                                 const int* __restrict__ chunk_off,
-                                                                 const int groups_per_unit, int* __restrict__ rank,
-                                                                 const StreamPtrs sp, const int write_streams) {
-  __shared__ int s_w[kPlanThreads / 32][4];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const long long base = static_cast<long long>(blockIdx.x) * kPlanChunk + threadIdx.x * 4;
-  int slot[4];
-  int c[4] = {0, 0, 0, 0};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const long long u = base + e;
-    slot[e] = u < U ? width_slot(bits[u]) : -1;
-    if (slot[e] >= 0) ++c[slot[e]];
-  }
-  int ex[4];
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    int x = c[s];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-      if (lane >= o) x += y;
-    }
-    ex[s] = x - c[s];
-    if (lane == 31) s_w[warp][s] = x;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    int before = chunk_off[blockIdx.x * 4 + s];
-    for (int i = 0; i < warp; ++i) before += s_w[i][s];
-    ex[s] += before;
-  }
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const long long u = base + e;
-    if (u >= U) break;
-    const int s = slot[e];
-    int r = -1;
-    if (s >= 0) {
-      r = ex[s]++;
-      if (write_streams && r < sp.cap_units[s]) {
-        sp.ids[s][r] = static_cast<int32_t>(u);
-        sp.goff[s][r] = static_cast<int64_t>(r) * groups_per_unit;
-      }
-    }
-    rank[u] = r;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// token units (axis 0, V cache): one half-warp per 64-element group
-// ---------------------------------------------------------------------------
-template <int DH>
-__global__ void __launch_bounds__(256) pack_rows_kernel(const uint16_t* __restrict__ X,
-                                                        const uint8_t* __restrict__ bits,
-                                                        const int* __restrict__ rank, const long long U,
-                                                        const StreamPtrs sp) {
-  constexpr int GPU = DH / 64;
-  const int l16 = threadIdx.x & 15;
-  const long long n_groups = U * GPU;
-  const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x / 16);
-  for (long long gidx = static_cast<long long>(blockIdx.x) * (blockDim.x / 16) + (threadIdx.x >> 4);
-       gidx < n_groups; gidx += stride) {
-    const long long u = gidx / GPU;
-    const int gi = static_cast<int>(gidx % GPU);
-    const int w = bits[u];
-    const int s = width_slot(w);
-    if (s < 0) continue;
-    const int r = rank[u];
-    if (r < 0 || r >= sp.cap_units[s]) continue;
-    const long long grp = static_cast<long long>(r) * GPU + gi;
-    if (grp >= sp.cap_groups[s]) continue;
-    float x[4];
-    uint2 raw;
-    lane_bf16x4(X + u * DH + gi * 64 + l16 * 4, x, &raw);
-    uint32_t packed = 0;
-    if (w != 16) {
-      uint16_t sb;
-      bool ovf;
-      packed = quantize_lane4(x, w, &sb, &ovf);
-      if (l16 == 0) {
-        sp.scales[s][grp] = sb;
-        if (ovf) record_error(KVS_ERR_RANGE);
-      }
-    }
-    store_lane_codes(sp.codes[s] + grp * (8 * w), w, l16, packed, raw);
-  }
-}
-
-// Token units decoded from the streams themselves: entry j of width slot s is
-// unit ids[s][j] with groups goff[s][j] ..; counts[] (written by the packer)
-// says how many entries each slot holds.  One half-warp per group.
-template <int DH>
-__global__ void __launch_bounds__(256) dequant_entries_rows_kernel(const StreamPtrs sp, float* __restrict__ out) {
-  constexpr int GPU = DH / 64;
-  __shared__ long long s_off[5];
+// entry offsets (in groups) of the four widths from the device counts
+__device__ __forceinline__ void entry_offsets(const StreamPtrs& sp, const int gpu, long long* s_off) {
   if (threadIdx.x == 0) {
     long long run = 0;
     for (int s = 0; s < 4; ++s) {
       s_off[s] = run;
-      run += min(static_cast<long long>(sp.counts[s]), sp.cap_units[s]) * GPU;
+      run += min(static_cast<long long>(sp.counts[s]), sp.cap_units[s]) * gpu;
     }
     s_off[4] = run;
   }
   __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// token units (axis 0, V cache): one half-warp per 64-element group, over the
+// stream entries the plan wrote (so every store is sequential in its stream)
+// ---------------------------------------------------------------------------
+template <int DH>
+__global__ void __launch_bounds__(256) pack_rows_kernel(const uint16_t* __restrict__ X, const StreamPtrs sp) {
+  constexpr int GPU = DH / 64;
+  constexpr int kUnroll = 4;  // groups per half-warp per step, their loads in flight together
+  __shared__ long long s_off[5];
+  entry_offsets(sp, GPU, s_off);
   const int l16 = threadIdx.x & 15;
   const long long total = s_off[4];
   const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x / 16);
+  for (long long g0 = static_cast<long long>(blockIdx.x) * (blockDim.x / 16) + (threadIdx.x >> 4); g0 < total;
+       g0 += stride * kUnroll) {
+    int sl[kUnroll];
+    long long grp[kUnroll], u[kUnroll];
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const long long gidx = g0 + j * stride;
+      int s = 0;
+      while (s < 3 && gidx >= s_off[s + 1]) ++s;
+      sl[j] = gidx < total ? s : -1;
+      grp[j] = gidx - s_off[s];  // == entry * GPU + gi
+      if (sl[j] >= 0 && grp[j] >= sp.cap_groups[s]) sl[j] = -1;
+      u[j] = sl[j] >= 0 ? static_cast<long long>(sp.ids[s][grp[j] / GPU]) : 0;
+    }
+    float x[kUnroll][4];
+    uint2 raw[kUnroll];
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      if (sl[j] >= 0) {
+        lane_bf16x4(X + u[j] * DH + static_cast<int>(grp[j] % GPU) * 64 + l16 * 4, x[j], &raw[j]);
+      } else {
+        x[j][0] = x[j][1] = x[j][2] = x[j][3] = 0.f;
+        raw[j] = make_uint2(0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int s = sl[j];
+      if (s < 0) continue;  // uniform over the half-warp
+      const int w = s == 3 ? 16 : (2 << s);
+      uint32_t packed = 0;
+      if (w != 16) {
+        uint16_t sb;
+        bool ovf;
+        packed = quantize_lane4(x[j], w, &sb, &ovf);
+        if (l16 == 0) {
+          sp.scales[s][grp[j]] = sb;
+          if (ovf) record_error(KVS_ERR_RANGE);
+        }
+      }
+      store_lane_codes(sp.codes[s] + grp[j] * (8 * w), w, l16, packed, raw[j]);
+    }
+  }
+}
+
+// Token units decoded from the stream entries (entry j of width slot s is
+// unit ids[s][j] with groups goff[s][j] ..), and rows of evicted units
+// (bits == 0) zeroed, in one launch.  One half-warp per group.
+template <int DH>
+__global__ void __launch_bounds__(256) dequant_rows_kernel(const StreamPtrs sp, const uint8_t* __restrict__ bits,
+                                                           const long long U, float* __restrict__ out) {
+  constexpr int GPU = DH / 64;
+  __shared__ long long s_off[5];
+  entry_offsets(sp, GPU, s_off);
+  const int l16 = threadIdx.x & 15;
+  const long long total = s_off[4];
+  const long long hw_stride = static_cast<long long>(gridDim.x) * (blockDim.x / 16);
   for (long long gidx = static_cast<long long>(blockIdx.x) * (blockDim.x / 16) + (threadIdx.x >> 4); gidx < total;
-       gidx += stride) {
+       gidx += hw_stride) {
     int s = 0;
     while (s < 3 && gidx >= s_off[s + 1]) ++s;
     const long long local = gidx - s_off[s];
@@ -295,152 +398,123 @@ __global__ void __launch_bounds__(256) dequant_entries_rows_kernel(const StreamP
     dequant_lane4(sp.codes[s] + grp * (8 * w), w, l16, sp.scales[s] + grp, y);
     *reinterpret_cast<float4*>(out + u * DH + gi * 64 + l16 * 4) = make_float4(y[0], y[1], y[2], y[3]);
   }
+  // evicted rows
+  constexpr int TPR = DH / 4;
+  const long long zt = U * TPR;
+  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < zt;
+       e += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = e / TPR;
+    if (bits[r] == 0)
+      *reinterpret_cast<float4*>(out + r * DH + (e % TPR) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 }
 
 // ---------------------------------------------------------------------------
 // channel units (axis 1, K cache) over the tokens each head keeps
 // ---------------------------------------------------------------------------
-// kept[g][j] = j-th kept token of head g (ascending); n_kept[g].  One block
-// per head, 4 consecutive tokens per thread per step.
-__global__ void __launch_bounds__(1024) kept_index_kernel(const uint8_t* __restrict__ keep_bits, const int N,
-                                                          int* __restrict__ kept, int* __restrict__ n_kept) {
-  __shared__ int s_w[32];
-  __shared__ int s_carry;
-  const int g = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) s_carry = 0;
-  __syncthreads();
-  const uint8_t* kb = keep_bits + static_cast<size_t>(g) * N;
-  for (int base = 0; base < N; base += 4096) {
-    const int t0 = base + threadIdx.x * 4;
-    int k[4];
+// One cluster of CL CTAs; CTA r handles heads r, r + CL, ...:
+//   kept[g][0 .. n_kept) = the kept tokens of head g, ascending;
+//   kept[g][n_kept .. N) = its dropped tokens (descending from the end); n_kept[g].
+// Then CTA 0 plans the channel units u = g*DH + c in unit order:
+//   chan_base[u] = first stream group of unit u (-1: not stored), and, with
+//   write_streams, ids / group offsets / counts (a unit of head g has
+//   ceil(n_kept[g] / 64) groups).
+template <int DH>
+__global__ void __launch_bounds__(kPlanThreads, 1) channels_plan_kernel(
+    const uint8_t* __restrict__ keep, const int N, const int Hkv, const uint8_t* __restrict__ bits,
+    int* __restrict__ kept, int* __restrict__ n_kept, long long* __restrict__ chan_base, const StreamPtrs sp,
+    const int write_streams) {
+  namespace cgp = cooperative_groups;
+  cgp::cluster_group cluster = cgp::this_cluster();
+  const int CL = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  __shared__ unsigned long long sbuf[kPlanThreads / 32 + 1];
+  constexpr int kStep = kPlanThreads * 16;
+  for (int g = rank; g < Hkv; g += CL) {
+    const uint8_t* kb = keep + static_cast<size_t>(g) * N;
+    int* kg = kept + static_cast<size_t>(g) * N;
+    unsigned long long carry = 0;  // kept tokens before this step
+    for (int b = 0; b < N; b += kStep) {
+      const int t0 = b + threadIdx.x * 16;
+      const uint4 v = load_bits16(kb, t0, N);
+      unsigned mask = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) k[e] = (t0 + e < N && kb[t0 + e] != 0) ? 1 : 0;
-    const int mine = k[0] + k[1] + k[2] + k[3];
-    int x = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-      if (lane >= o) x += y;
+      for (int e = 0; e < 16; ++e)
+        if (bits16_at(v, e) != 0) mask |= 1u << e;
+      unsigned long long step_tot;
+      const unsigned long long ex = plan_block_exscan(__popc(mask), sbuf, &step_tot);
+      int pk = static_cast<int>(carry + ex);       // next kept slot
+      int pd = N - 1 - (t0 - pk);                  // next dropped slot, from the end
+      const int valid = max(0, min(16, N - t0));
+      for (int e = 0; e < valid; ++e) {
+        if (mask & (1u << e))
+          kg[pk++] = t0 + e;
+        else
+          kg[pd--] = t0 + e;
+      }
+      carry += step_tot;
     }
-    if (lane == 31) s_w[warp] = x;
-    __syncthreads();
-    int before = s_carry;
-    for (int i = 0; i < warp; ++i) before += s_w[i];
-    int pos = before + x - mine;
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (k[e]) kept[static_cast<size_t>(g) * N + pos++] = t0 + e;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int tot = 0;
-      for (int i = 0; i < 32; ++i) tot += s_w[i];
-      s_carry += tot;
-    }
-    __syncthreads();
+    if (threadIdx.x == 0) n_kept[g] = static_cast<int>(carry);
   }
-  if (threadIdx.x == 0) n_kept[g] = s_carry;
-}
-
-// single block plan over channel units u = g*DH + c: rank, ids, group offsets
-// (a unit of head g has ceil(n_kept[g]/64) groups), counts and capacity check
-constexpr int kPlanChannelThreads = 1024;
-__global__ void __launch_bounds__(kPlanChannelThreads) plan_channels_kernel(const uint8_t* __restrict__ bits,
-                                                                     const int U, const int DH,
-                                                                     const int* __restrict__ n_kept,
-                                                                     int* __restrict__ rank, const StreamPtrs sp,
-                                                                     const int write_streams) {
-  __shared__ long long s_u[kPlanChannelThreads / 32][4], s_g[kPlanChannelThreads / 32][4];
-  __shared__ long long s_cu[4], s_cg[4];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x < 4) s_cu[threadIdx.x] = s_cg[threadIdx.x] = 0;
-  __syncthreads();
-  for (int base = 0; base < U; base += kPlanChannelThreads) {
-    const int u = base + threadIdx.x;
-    const int s = u < U ? width_slot(bits[u]) : -1;
-    const long long ng = u < U ? (n_kept[u / DH] + 63) / 64 : 0;
-    long long exu[4], exg[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      long long xu = (s == q) ? 1 : 0, xg = (s == q) ? ng : 0;
-      const long long cu0 = xu, cg0 = xg;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const long long yu = __shfl_up_sync(0xFFFFFFFFu, xu, o), yg = __shfl_up_sync(0xFFFFFFFFu, xg, o);
-        if (lane >= o) {
-          xu += yu;
-          xg += yg;
-        }
-      }
-      exu[q] = xu - cu0;
-      exg[q] = xg - cg0;
-      if (lane == 31) {
-        s_u[warp][q] = xu;
-        s_g[warp][q] = xg;
-      }
+  cluster.sync();  // every head's kept count is written (cluster scope orders global memory)
+  if (rank != 0) return;
+  // channel plan: thread t takes units [t*m, t*m + m); per-width unit counts
+  // (16-bit fields) and group counts (32-bit fields) scanned over the block
+  const int U = Hkv * DH;
+  const int m = (U + kPlanThreads - 1) / kPlanThreads;
+  const int u0 = threadIdx.x * m, u1 = min(U, u0 + m);
+  unsigned long long cu = 0, cg01 = 0, cg23 = 0;
+  for (int u = u0; u < u1; ++u) {
+    const int sl = width_slot(bits[u]);
+    if (sl < 0) continue;
+    const unsigned long long ng = static_cast<unsigned long long>((__ldcg(n_kept + u / DH) + 63) / 64);
+    cu += 1ull << (16 * sl);
+    if (sl < 2) cg01 += ng << (32 * sl);
+    else cg23 += ng << (32 * (sl - 2));
+  }
+  unsigned long long tu, t01, t23;
+  const unsigned long long eu = plan_block_exscan(cu, sbuf, &tu);
+  const unsigned long long e01 = plan_block_exscan(cg01, sbuf, &t01);
+  const unsigned long long e23 = plan_block_exscan(cg23, sbuf, &t23);
+  long long ru[4], rg[4];
+  for (int sl = 0; sl < 4; ++sl) {
+    ru[sl] = static_cast<long long>((eu >> (16 * sl)) & 0xFFFFull);
+    rg[sl] = static_cast<long long>(sl < 2 ? (e01 >> (32 * sl)) & 0xFFFFFFFFull : (e23 >> (32 * (sl - 2))) & 0xFFFFFFFFull);
+  }
+  for (int u = u0; u < u1; ++u) {
+    const int sl = width_slot(bits[u]);
+    if (sl < 0) {
+      chan_base[u] = -1;
+      continue;
     }
-    __syncthreads();
-    if (s >= 0) {
-      long long ru = s_cu[s] + exu[s], rg = s_cg[s] + exg[s];
-      for (int i = 0; i < warp; ++i) {
-        ru += s_u[i][s];
-        rg += s_g[i][s];
-      }
-      rank[u] = static_cast<int>(ru);
-      if (write_streams && ru < sp.cap_units[s]) {
-        sp.ids[s][ru] = u;
-        sp.goff[s][ru] = rg;
-      }
-    } else if (u < U) {
-      rank[u] = -1;
+    const long long ng = (__ldcg(n_kept + u / DH) + 63) / 64;
+    const bool fits = ru[sl] < sp.cap_units[sl] && rg[sl] + ng <= sp.cap_groups[sl];
+    chan_base[u] = fits ? rg[sl] : -1;
+    if (write_streams && fits) {
+      sp.ids[sl][ru[sl]] = u;
+      sp.goff[sl][ru[sl]] = rg[sl];
     }
-    __syncthreads();
-    if (threadIdx.x < 4) {
-      for (int i = 0; i < kPlanChannelThreads / 32; ++i) {
-        s_cu[threadIdx.x] += s_u[i][threadIdx.x];
-        s_cg[threadIdx.x] += s_g[i][threadIdx.x];
-      }
-    }
-    __syncthreads();
+    ++ru[sl];
+    rg[sl] += ng;
   }
   if (threadIdx.x < 4 && write_streams) {
-    const int s = threadIdx.x;
+    const int sl = threadIdx.x;
+    const long long units = static_cast<long long>((tu >> (16 * sl)) & 0xFFFFull);
+    const long long groups =
+        static_cast<long long>(sl < 2 ? (t01 >> (32 * sl)) & 0xFFFFFFFFull : (t23 >> (32 * (sl - 2))) & 0xFFFFFFFFull);
     if (sp.counts) {
-      sp.counts[s] = s_cu[s];
-      sp.counts[4 + s] = s_cg[s];
+      sp.counts[sl] = units;
+      sp.counts[4 + sl] = groups;
     }
-    if (s_cu[s] > sp.cap_units[s] || s_cg[s] > sp.cap_groups[s]) record_error(KVS_ERR_RANGE);
+    if (units > sp.cap_units[sl] || groups > sp.cap_groups[sl]) record_error(KVS_ERR_RANGE);
   }
 }
 
-// Width and first stream group of every channel of head g, staged once per CTA
-// (so the per-channel loops below issue no dependent global loads).  base = -1
-// for channels that are not stored.
-template <int DH>
-__device__ __forceinline__ void stage_channel_meta(const StreamPtrs& sp, const uint8_t* __restrict__ bits,
-                                                   const int* __restrict__ rank, const int g, const int j,
-                                                   int* s_w, long long* s_base) {
-  for (int c = threadIdx.x; c < DH; c += blockDim.x) {
-    const int u = g * DH + c;
-    const int w = bits[u];
-    const int s = width_slot(w);
-    long long base = -1;
-    if (s >= 0) {
-      const int r = rank[u];
-      if (r >= 0 && r < sp.cap_units[s]) {
-        const long long grp = sp.goff[s][r] + j;
-        if (grp < sp.cap_groups[s]) base = grp;
-      }
-    }
-    s_w[c] = w;
-    s_base[c] = base;
-  }
-}
-
-// grid (ceil(N/64), Hkv), 256 threads: token group j of head g for every channel
+// grid (ceil(N/64), Hkv), 256 threads: kept-token group j of head g for every channel
 template <int DH>
 __global__ void __launch_bounds__(256) pack_channels_kernel(const uint16_t* __restrict__ X, const int N,
                                                             const uint8_t* __restrict__ bits,
-                                                            const int* __restrict__ rank,
+                                                            const long long* __restrict__ chan_base,
                                                             const int* __restrict__ kept,
                                                             const int* __restrict__ n_kept, const StreamPtrs sp) {
   // odd word stride: the column reads below (lane i takes rows 4i..4i+3)
@@ -453,7 +527,11 @@ __global__ void __launch_bounds__(256) pack_channels_kernel(const uint16_t* __re
   const int n = n_kept[g];
   if (j * 64 >= n) return;
   const int rows = min(64, n - j * 64);
-  stage_channel_meta<DH>(sp, bits, rank, g, j, s_w, s_base);
+  for (int c = threadIdx.x; c < DH; c += blockDim.x) {
+    const long long b = chan_base[g * DH + c];
+    s_w[c] = bits[g * DH + c];
+    s_base[c] = b >= 0 ? b + j : -1;
+  }
   for (int e = threadIdx.x; e < 64 * (DH / 8); e += 256) {
     const int i = e / (DH / 8), c8 = (e % (DH / 8)) * 8;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -496,10 +574,13 @@ __global__ void __launch_bounds__(256) pack_channels_kernel(const uint16_t* __re
   }
 }
 
+// grid (ceil(N/64) + 1, Hkv), 256 threads.  CTA (j, g) with j below the head's
+// kept-group count decodes kept-token group j of every channel; the CTAs
+// after those zero the head's dropped tokens, 64 per CTA.
 template <int DH>
 __global__ void __launch_bounds__(256) dequant_channels_kernel(const StreamPtrs sp, const int N,
                                                                const uint8_t* __restrict__ bits,
-                                                               const int* __restrict__ rank,
+                                                               const long long* __restrict__ chan_base,
                                                                const int* __restrict__ kept,
                                                                const int* __restrict__ n_kept,
                                                                float* __restrict__ out) {
@@ -509,9 +590,25 @@ __global__ void __launch_bounds__(256) dequant_channels_kernel(const StreamPtrs 
   __shared__ long long s_base[DH];
   const int j = blockIdx.x, g = blockIdx.y;
   const int n = n_kept[g];
-  if (j * 64 >= n) return;
+  const int ngk = (n + 63) / 64;
+  if (j >= ngk) {  // zero dropped tokens kept[g][n + 64 jz ..]
+    const int jz = j - ngk;
+    const int d0 = n + jz * 64;
+    if (d0 >= N) return;
+    const int cnt = min(64, N - d0);
+    for (int e = threadIdx.x; e < cnt * (DH / 4); e += 256) {
+      const int i = e / (DH / 4), c4 = (e % (DH / 4)) * 4;
+      const int t = kept[static_cast<size_t>(g) * N + d0 + i];
+      *reinterpret_cast<float4*>(out + (static_cast<size_t>(g) * N + t) * DH + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
   const int rows = min(64, n - j * 64);
-  stage_channel_meta<DH>(sp, bits, rank, g, j, s_w, s_base);
+  for (int c = threadIdx.x; c < DH; c += blockDim.x) {
+    const long long b = chan_base[g * DH + c];
+    s_w[c] = bits[g * DH + c];
+    s_base[c] = b >= 0 ? b + j : -1;
+  }
   __syncthreads();
   const int l16 = threadIdx.x & 15, hw = threadIdx.x >> 4;
   for (int c = hw; c < DH; c += 16) {
@@ -531,20 +628,6 @@ __global__ void __launch_bounds__(256) dequant_channels_kernel(const StreamPtrs 
     const int t = kept[static_cast<size_t>(g) * N + j * 64 + i];
     *reinterpret_cast<float4*>(out + (static_cast<size_t>(g) * N + t) * DH + c4) =
         make_float4(tile[i][c4], tile[i][c4 + 1], tile[i][c4 + 2], tile[i][c4 + 3]);
-  }
-}
-
-// zero the rows of tokens that are not kept (bits == 0)
-template <int DH>
-__global__ void __launch_bounds__(256) zero_dropped_rows_kernel(const uint8_t* __restrict__ keep_bits,
-                                                                const long long rows, float* __restrict__ out) {
-  constexpr int TPR = DH / 4;
-  const long long total = rows * TPR;
-  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
-       e += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long r = e / TPR;
-    if (keep_bits[r] == 0)
-      *reinterpret_cast<float4*>(out + r * DH + (e % TPR) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 

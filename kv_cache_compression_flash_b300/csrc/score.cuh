@@ -11,9 +11,12 @@
 // Both passes are flash-style: 128x128 logit tiles S = Q K^T are produced by
 // tcgen05.mma into tensor memory (fp32) from 128-byte-swizzled bf16 tiles that
 // TMA streams into shared memory; the N x N matrix never exists in HBM.
-// Roles per CTA: warps 0-3 reduce the tiles (one TMEM lane, i.e. one tile row,
-// per thread), warp 4 issues TMA, warp 5 issues the MMAs.  Two TMEM buffers
-// let the MMA of tile i+1 run while tile i is being reduced.
+// Roles per CTA: warps 0-7 reduce the tiles, warp 8 issues TMA, warp 9 issues
+// the MMAs.  Reducer warp w reads TMEM lanes 32(w%4)..+31 (one tile row per
+// thread) and the column half w/4 of the tile, in two 32-column chunks whose
+// loads overlap the previous chunk's arithmetic (packed fp32x2 FMA/ADD, ex2 on
+// the special-function unit).  Two TMEM buffers let the MMA of tile i+1 run
+// while tile i is being reduced.
 //
 // GQA packing: a 128-row query tile holds P = 128/Gt consecutive window rows
 // of Gt heads of one KV group (row j = head (j / P), position pmin + j % P), so
@@ -31,7 +34,8 @@
 
 namespace kvs {
 
-constexpr int kScoreThreads = 192;
+constexpr int kScoreThreads = 320;   // 8 reducer warps, 1 TMA warp, 1 MMA warp
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 
@@ -101,8 +105,44 @@ struct LseSmem {
   int abort_flag;
 };
 
-// partial[(rt * n_split + split) * 128 + row] = (running max m, sum l), log2 domain:
-// the rows' 2^(x - m) summed over the split's key tiles, x = s * log2(e)/sqrt(d).
+// partial[((rt * n_split + split) * 2 + half) * 128 + row] = (running max m,
+// sum l), log2 domain: the row's 2^(x - m) summed over the split's key tiles
+// and the column half, x = s * log2(e)/sqrt(d).
+
+// one 32-column chunk of a pass-1 row: mask (diagonal tiles), running max and
+// rescaled sum
+__device__ __forceinline__ void lse_chunk(uint32_t (&r)[32], const int t0, const int pos, const bool diag,
+                                          const float c, float& m, float& l) {
+  float* v = reinterpret_cast<float*>(r);
+  if (diag) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (t0 + j > pos) v[j] = -INFINITY;
+  }
+  float x[11];
+#pragma unroll
+  for (int k = 0; k < 10; ++k) x[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+  x[10] = fmaxf(v[30], v[31]);
+  const float y0 = fmax3(x[0], x[1], x[2]), y1 = fmax3(x[3], x[4], x[5]), y2 = fmax3(x[6], x[7], x[8]);
+  const float z = fmax3(fmax3(y0, y1, y2), x[9], x[10]);
+  const float m_new = fmaxf(m, z * c);
+  if (m_new == -INFINITY) return;  // every element so far masked
+  const unsigned long long c2 = f2_pack(c, c), nm2 = f2_pack(-m_new, -m_new);
+  unsigned long long acc0 = 0ull, acc1 = 0ull;  // two packed pairs of partial sums
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    float e0, e1, e2, e3;
+    f2_unpack(f2_fma(f2_pack(v[j], v[j + 1]), c2, nm2), &e0, &e1);
+    f2_unpack(f2_fma(f2_pack(v[j + 2], v[j + 3]), c2, nm2), &e2, &e3);
+    acc0 = f2_add(acc0, f2_pack(ex2_approx(e0), ex2_approx(e1)));
+    acc1 = f2_add(acc1, f2_pack(ex2_approx(e2), ex2_approx(e3)));
+  }
+  float s0, s1, s2, s3;
+  f2_unpack(f2_add(acc0, acc1), &s0, &s1);
+  (void)s2, (void)s3;
+  l = l * ex2_approx(m - m_new) + (s0 + s1);
+  m = m_new;
+}
 template <int DH, int NS>
 __global__ void __launch_bounds__(kScoreThreads, 2)
     lse_pass_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
@@ -130,7 +170,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.s_full[b], 1);
-      mbar_init(&S.s_empty[b], 4);
+      mbar_init(&S.s_empty[b], 8);
     }
     mbar_init(&S.drain, 1);
     S.abort_flag = 0;
@@ -146,7 +186,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   const uint32_t tmem = S.tmem_base;
   volatile int* abort_flag = &S.abort_flag;
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     if (lane == 0) {  // TMA producer
       prefetch_tensormap(&mapQ);
       prefetch_tensormap(&mapK);
@@ -172,7 +212,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
         for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(&S.k_full[i % NS], (i / NS) & 1, &never);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {  // MMA issuer
       if (mbar_wait(&S.q_full, 0, abort_flag)) {
         for (int i = 0; i < niter; ++i) {
@@ -191,51 +231,31 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
         mbar_wait(&S.drain, 0, &never);
       }
     }
-  } else {  // warps 0-3: one tile row per thread
-    const int row = warp * 32 + lane;
+  } else {  // warps 0-7: one tile row per thread, column half warp / 4
+    const int q4 = warp & 3, hh = warp >> 2;
+    const int row = q4 * 32 + lane;
     const int pos = pmin + row % geo.P;
     const float c = geo.c_log2;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + hh * 64;
     float m = -INFINITY, l = 0.f;
+    uint32_t va[32], vb[32];
     for (int i = 0; i < niter; ++i) {
       const int b = i & 1;
       if (!mbar_wait(&S.s_full[b], (i >> 1) & 1, abort_flag)) break;
       tc_fence_after();
-      const int t0 = (kt0 + i) * 128;
-      const bool diag = t0 + 127 > pmin;
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        float v[32];
-        tmem_load32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * 128 + ch * 32, v);
-        if (diag) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (t0 + ch * 32 + j > pos) v[j] = -INFINITY;
-        }
-        float cm0 = fmaxf(v[0], v[1]), cm1 = fmaxf(v[2], v[3]);
-#pragma unroll
-        for (int j = 4; j < 32; j += 4) {
-          cm0 = fmaxf(cm0, fmaxf(v[j], v[j + 1]));
-          cm1 = fmaxf(cm1, fmaxf(v[j + 2], v[j + 3]));
-        }
-        const float m_new = fmaxf(m, fmaxf(cm0, cm1) * c);
-        if (m_new != -INFINITY) {
-          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            a0 += ex2_approx(fmaf(v[j], c, -m_new));
-            a1 += ex2_approx(fmaf(v[j + 1], c, -m_new));
-            a2 += ex2_approx(fmaf(v[j + 2], c, -m_new));
-            a3 += ex2_approx(fmaf(v[j + 3], c, -m_new));
-          }
-          l = l * ex2_approx(m - m_new) + ((a0 + a1) + (a2 + a3));
-          m = m_new;
-        }
-      }
-      tc_fence_before();
+      const int t0 = (kt0 + i) * 128 + hh * 64;
+      const bool diag = t0 + 63 > pmin;
+      tmem_issue32(lane_base + b * 128, va);
+      tmem_wait32(va);
+      tmem_issue32(lane_base + b * 128 + 32, vb);
+      lse_chunk(va, t0, pos, diag, c, m, l);
+      tmem_wait32(vb);
+      tc_fence_before();  // this warp is done with the TMEM buffer
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.s_empty[b]);
+      lse_chunk(vb, t0 + 32, pos, diag, c, m, l);
     }
-    partial[(static_cast<size_t>(rt) * n_split + split) * 128 + row] = make_float2(m, l);
+    partial[((static_cast<size_t>(rt) * n_split + split) * 2 + hh) * 128 + row] = make_float2(m, l);
   }
   tc_fence_before();
   __syncthreads();
@@ -258,11 +278,11 @@ __global__ void lse_finalize_kernel(const ScoreGeom geo, const int kt_chunk, con
   const int gh = rt / geo.n_pb;
   const int g = gh / geo.n_hc, hc = gh % geo.n_hc;
   const int ns = ceil_div_i(pb_nkt(geo, pb), kt_chunk);
-  const float2* p = partial + static_cast<size_t>(rt) * n_split * 128 + row;
+  const float2* p = partial + static_cast<size_t>(rt) * n_split * 256 + row;
   float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, p[s * 128].x);
+  for (int s = 0; s < 2 * ns; ++s) M = fmaxf(M, p[s * 128].x);
   float L = 0.f;
-  for (int s = 0; s < ns; ++s) {
+  for (int s = 0; s < 2 * ns; ++s) {
     const float2 v = p[s * 128];
     if (v.x != -INFINITY) L += v.y * ex2_approx(v.x - M);
   }
@@ -296,6 +316,7 @@ struct ColSmem {
   uint8_t k[TileCfg<DH>::kTileBytes];
   uint8_t q[NS][TileCfg<DH>::kTileBytes];
   float bv[NS][128];
+  float comb[128];
   uint64_t k_full, q_full[NS], q_empty[NS], s_full[2], s_empty[2], drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -331,11 +352,11 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
     mbar_init(&S.k_full, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&S.q_full[s], 1);
-      mbar_init(&S.q_empty[s], 1 + 4);
+      mbar_init(&S.q_empty[s], 1 + 8);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.s_full[b], 1);
-      mbar_init(&S.s_empty[b], 4);
+      mbar_init(&S.s_empty[b], 8);
     }
     mbar_init(&S.drain, 1);
     S.abort_flag = 0;
@@ -351,7 +372,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   const uint32_t tmem = S.tmem_base;
   volatile int* abort_flag = &S.abort_flag;
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     if (lane == 0) {  // TMA producer
       prefetch_tensormap(&mapQ);
       prefetch_tensormap(&mapK);
@@ -380,7 +401,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
         for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(&S.q_full[i % NS], (i / NS) & 1, &never);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {  // MMA issuer: S^T tile = K_tile (M = 128 keys) x Q_tile^T (N = 128 rows)
       if (mbar_wait(&S.k_full, 0, abort_flag)) {
         for (int i = 0; i < niter; ++i) {
@@ -399,10 +420,12 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
         mbar_wait(&S.drain, 0, &never);
       }
     }
-  } else {  // warps 0-3: one key per thread
-    const int krow = warp * 32 + lane;
+  } else {  // warps 0-7: one key per thread (TMEM lane), query-column half warp / 4
+    const int q4 = warp & 3, hh = warp >> 2;
+    const int krow = q4 * 32 + lane;
     const int t = t0 + krow;
     const float c = geo.c_log2;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + hh * 64;
     float acc = 0.f;
     float best = 0.f;
     float mx[GT];
@@ -420,6 +443,47 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
         mx[h] = -INFINITY;
       }
     };
+    // one 32-column chunk: x = s c - b_col, masked where the query precedes the key
+    auto chunk = [&](uint32_t (&r)[32], const float* bcol, const int col0, const int pmin, const bool diag) {
+      float* v = reinterpret_cast<float*>(r);
+      const unsigned long long c2 = f2_pack(c, c);
+      const float4* b4 = reinterpret_cast<const float4*>(bcol);
+#pragma unroll
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 bb = b4[j4];
+        f2_unpack(f2_fma(f2_pack(v[4 * j4], v[4 * j4 + 1]), c2, f2_pack(-bb.x, -bb.y)), &v[4 * j4], &v[4 * j4 + 1]);
+        f2_unpack(f2_fma(f2_pack(v[4 * j4 + 2], v[4 * j4 + 3]), c2, f2_pack(-bb.z, -bb.w)), &v[4 * j4 + 2],
+                  &v[4 * j4 + 3]);
+      }
+      if (diag) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (pmin + ((col0 + j) % P) < t) v[j] = -INFINITY;
+      }
+      if (MAXMODE) {
+        float x[11];
+#pragma unroll
+        for (int k = 0; k < 10; ++k) x[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+        x[10] = fmaxf(v[30], v[31]);
+        const float z = fmax3(fmax3(fmax3(x[0], x[1], x[2]), fmax3(x[3], x[4], x[5]), fmax3(x[6], x[7], x[8])),
+                              x[9], x[10]);
+        const int hl = col0 / P;  // P >= 32: the chunk lies in one head
+#pragma unroll
+        for (int h = 0; h < GT; ++h)
+          if (h == hl) mx[h] = fmaxf(mx[h], z);
+      } else {
+        unsigned long long a0 = 0ull, a1 = 0ull;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          a0 = f2_add(a0, f2_pack(ex2_approx(v[j]), ex2_approx(v[j + 1])));
+          a1 = f2_add(a1, f2_pack(ex2_approx(v[j + 2]), ex2_approx(v[j + 3])));
+        }
+        float s0, s1;
+        f2_unpack(f2_add(a0, a1), &s0, &s1);
+        acc += s0 + s1;
+      }
+    };
+    uint32_t va[32], vb[32];
     for (int i = 0; i < niter; ++i) {
       const int s = i % NS, b = i & 1;
       const int q = q0 + i;
@@ -434,62 +498,32 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
       tc_fence_after();
       const int pmin = geo.q_pos0 + pb * P;
       const bool diag = pmin < t0 + 127;
-      const float4* bvs = reinterpret_cast<const float4*>(S.bv[s]);
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        float v[32];
-        tmem_load32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * 128 + ch * 32, v);
-#pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 bb = bvs[ch * 8 + j4];
-          v[4 * j4 + 0] = fmaf(v[4 * j4 + 0], c, -bb.x);
-          v[4 * j4 + 1] = fmaf(v[4 * j4 + 1], c, -bb.y);
-          v[4 * j4 + 2] = fmaf(v[4 * j4 + 2], c, -bb.z);
-          v[4 * j4 + 3] = fmaf(v[4 * j4 + 3], c, -bb.w);
-        }
-        if (diag) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (pmin + ((ch * 32 + j) % P) < t) v[j] = -INFINITY;
-        }
-        if (MAXMODE) {
-          float m0 = fmaxf(v[0], v[1]), m1 = fmaxf(v[2], v[3]);
-#pragma unroll
-          for (int j = 4; j < 32; j += 4) {
-            m0 = fmaxf(m0, fmaxf(v[j], v[j + 1]));
-            m1 = fmaxf(m1, fmaxf(v[j + 2], v[j + 3]));
-          }
-          const int hl = (ch * 32) / P;  // P >= 32: the chunk lies in one head
-#pragma unroll
-          for (int h = 0; h < GT; ++h)
-            if (h == hl) mx[h] = fmaxf(mx[h], fmaxf(m0, m1));
-        } else {
-          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            a0 += ex2_approx(v[j]);
-            a1 += ex2_approx(v[j + 1]);
-            a2 += ex2_approx(v[j + 2]);
-            a3 += ex2_approx(v[j + 3]);
-          }
-          acc += (a0 + a1) + (a2 + a3);
-        }
-      }
-      tc_fence_before();
+      tmem_issue32(lane_base + b * 128, va);
+      tmem_wait32(va);
+      tmem_issue32(lane_base + b * 128 + 32, vb);
+      chunk(va, S.bv[s] + hh * 64, hh * 64, pmin, diag);
+      tmem_wait32(vb);
+      tc_fence_before();  // this warp is done with the TMEM buffer
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&S.s_empty[b]);
-        mbar_arrive(&S.q_empty[s]);
-      }
+      if (lane == 0) mbar_arrive(&S.s_empty[b]);
+      chunk(vb, S.bv[s] + hh * 64 + 32, hh * 64 + 32, pmin, diag);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.q_empty[s]);  // done reading bv[s]
     }
     if (MAXMODE && cur_hc >= 0) flush(cur_hc);
-    const float res = MAXMODE ? best : acc;
-    if (t < geo.N) {
-      const size_t o = static_cast<size_t>(g) * geo.N + t;
-      if (n_split == 1)
-        out_direct[o] = res;
-      else
-        out_partial[static_cast<size_t>(split) * geo.Hkv * geo.N + o] = res;
+    // combine the two column halves in a fixed order: half 1 hands its value to half 0
+    float* comb = reinterpret_cast<float*>(S.comb);
+    if (hh == 1) comb[krow] = MAXMODE ? best : acc;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (hh == 0) {
+      const float res = MAXMODE ? fmaxf(best, comb[krow]) : acc + comb[krow];
+      if (t < geo.N) {
+        const size_t o = static_cast<size_t>(g) * geo.N + t;
+        if (n_split == 1)
+          out_direct[o] = res;
+        else
+          out_partial[static_cast<size_t>(split) * geo.Hkv * geo.N + o] = res;
+      }
     }
   }
   tc_fence_before();

@@ -69,13 +69,13 @@ class RdkvLayerStep:
         Hq, Hkv, N, W, d = self.shape
         n = K_.score_plan_info(Hq, Hkv, W, N, d, mode=K_.MODE_LSE)[4]
         n += K_.score_plan_info(Hq, Hkv, W, N, d, mode=self.PASS2_MODE)[4]
-        n += 3          # channel weights: 2 column passes + finalize
+        n += 1          # channel weights (one cluster per KV head)
         n += 1          # sigma_t
-        n += 1 + 2      # V allocation, sigma_c (pass + finalize)
+        n += 1 + 1      # V allocation, sigma_c
         n += 1          # K allocation
-        n += 4 + 3      # V pack (count, scan, rank, pack), K pack (kept, plan, pack)
+        n += 2 + 2      # V pack (plan, pack), K pack (plan, pack)
         if self.dequant:
-            n += 2 + 4  # V dequant (zero, decode entries), K dequant (kept, plan, zero, dequant)
+            n += 1 + 2  # V dequant (decode + zero), K dequant (plan, decode + zero)
         return n
 
     def pass1(self, Q, K, V, stream=None):

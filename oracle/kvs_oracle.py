@@ -13,7 +13,8 @@ Sources (web summaries of the papers; sections as printed there):
               §2.2 reverse water-filling over {0,2,4,8,16}, stages 1-3;
               §2.3 TriZone streams grouped by width.
   [KVzap]     "KVzap - Poda del KV Cache Rapida, Adaptativa y Fiel"
-              (gist.science 2601.07891): §2.1 the KVzip and KVzip+ scores.
+              (gist.science 2601.07891): §2.1 the KVzip and KVzip+ scores;
+              §2.3 threshold pruning with a sliding window.
   [KVSculpt]  "KVSculpt: KV Cache Compression as Distillation"
               (gist.science 2603.27819): §2 loss, the log-sum-exp term.
 
@@ -389,3 +390,25 @@ def rdkv_compress(Q, K, V, q_pos0, avg_bits, widths=WIDTHS):
             "bits_v": bits_v, "bits_k": bits_k, "keep": keep,
             "v_streams": quantize_pack(V, 0, bits_v),
             "k_streams": quantize_pack(K, 1, bits_k, keep)}
+
+
+# ----------------------------------------------------------------------------
+# O6. threshold pruning with a sliding window
+# ----------------------------------------------------------------------------
+def threshold_keep(score, tau, window, keep_width=16):
+    """KVzap's adaptive eviction [KVzap §2.3]: a token whose score is below the
+    fixed threshold tau is dropped, except that the last `window` positions
+    are always kept.
+
+    score [Hkv, N] is read as float32 and compared with float32(tau) (the
+    comparison the library makes); a NaN score is not >= tau, so it is dropped
+    unless the window keeps it.  Returns uint8 widths: keep_width or 0.
+    Pins: hand-worked fixture; window >= N keeps all; tau = -inf keeps all
+    finite scores; tau = +inf keeps exactly the window.
+    """
+    score = np.asarray(score, dtype=np.float32)
+    Hkv, N = score.shape
+    with np.errstate(invalid="ignore"):
+        keep = score >= np.float32(tau)
+    keep[:, max(0, N - int(window)):] = True
+    return np.where(keep, keep_width, 0).astype(np.uint8)

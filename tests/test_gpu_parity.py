@@ -154,6 +154,22 @@ def test_allocation_power_of_two_ties():
         assert (gpu_alloc(w, s, B) == O.allocate_bits(w, s, B)).all(), B
 
 
+@pytest.mark.parametrize("U", [5000, 50000, 400000])
+def test_allocation_many_equal_keys(U):
+    """Thousands of items share one threshold (more than a cluster CTA lists
+    for its exact low-half pass), and pools past one cluster's shared memory
+    (400 000 units) take the grid path."""
+    rng = np.random.default_rng(U)
+    w = np.ones(U, np.float32)
+    w[rng.random(U) < 0.3] = 4.0                      # theta(u,0) of these == theta(v,1) of the ones
+    w[rng.random(U) < 0.01] = 0.0
+    s = np.ones(U, np.float32)
+    for avg in (0.5, 2.0, 3.3, 7.9):
+        B = int(math.floor(avg * U))
+        assert (gpu_alloc(w, s, B) == O.allocate_bits(w, s, B)).all(), avg
+    assert L.device_error() == 0
+
+
 def test_allocation_rejects_bad_weights():
     w = np.ones(100, np.float32)
     w[7] = np.nan
@@ -246,3 +262,19 @@ def test_pipeline_vs_oracle(name):
     sc = L.unit_rms(K, 1, keep_bits=bv)
     np.testing.assert_allclose(sc.cpu().numpy(), ref["sigma_c"], rtol=TOL)
     assert L.device_error() == 0
+
+
+@pytest.mark.parametrize("Hkv,N", [(1, 1), (2, 7), (8, 8192), (3, 1001)])
+def test_threshold_keep_bit_exact(Hkv, N):
+    """KVzap threshold + sliding window   [KVzap §2.3], against the oracle."""
+    rng = np.random.default_rng(N)
+    s = (rng.random((Hkv, N)) ** 3).astype(np.float32)
+    s[:, ::5] = np.float32(0.125)                      # ties at tau
+    for tau, window, kw in ((0.125, 128, 16), (0.5, 0, 8), (0.0, 3, 2), (2.0, N + 5, 4)):
+        got = L.threshold_keep(torch.from_numpy(s).to(DEV), tau, window, kw).cpu().numpy()
+        assert np.array_equal(got, O.threshold_keep(s, tau, window, kw)), (tau, window, kw)
+    assert L.device_error() == 0
+    s[0, 0] = np.nan
+    got = L.threshold_keep(torch.from_numpy(s).to(DEV), 0.1, 0, 16).cpu().numpy()
+    assert np.array_equal(got, O.threshold_keep(s, 0.1, 0, 16))
+    assert L.device_error() == 3

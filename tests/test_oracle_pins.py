@@ -340,3 +340,27 @@ def test_zero_group_and_overflow():
     Y[0, 0, 0] = 2.0 ** 100                                                   # bf16-exact, beyond fp16 range
     with pytest.raises(OverflowError):
         O.quantize_pack(Y, 0, np.array([8], np.uint8))
+
+
+# ----------------------------------------------------------------------------
+# threshold pruning with a sliding window   [KVzap §2.3]
+# ----------------------------------------------------------------------------
+def test_threshold_hand_examples(root):
+    import json
+    cases = json.load(open(os.path.join(root, "tests", "golden", "threshold_hand_examples.json")))["cases"]
+    for c in cases:
+        got = O.threshold_keep(np.array(c["score"], np.float32), c["tau"], c["window"], c["keep_width"])
+        assert got.tolist() == c["bits"], c["why"]
+
+
+def test_threshold_special_cases():
+    rng = np.random.default_rng(3)
+    s = rng.random((3, 50)).astype(np.float32)
+    assert (O.threshold_keep(s, 2.0, 50) == 16).all()                    # the window covers every token
+    assert (O.threshold_keep(s, -np.inf, 0) == 16).all()                 # every finite score passes
+    b = O.threshold_keep(s, np.inf, 7)
+    assert (b[:, -7:] == 16).all() and (b[:, :-7] == 0).all()            # only the window
+    s[0, 3] = np.nan
+    assert O.threshold_keep(s, 0.0, 0)[0, 3] == 0                        # NaN never passes
+    kept = [int((O.threshold_keep(s, t, 5) > 0).sum()) for t in (0.1, 0.3, 0.6, 0.9)]
+    assert kept == sorted(kept, reverse=True)                            # monotone in tau

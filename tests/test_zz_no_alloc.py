@@ -43,10 +43,17 @@ def _static(w, s, budget, mask):
     return bits
 
 
+# Pools that fit one thread-block cluster's shared memory need no scratch at
+# all; these sizes are past that, so both calls run the grid allocator on the
+# library's scratch array.
+SCRATCH_SIZES = {L.WIDTHS_ALL: (400000, 250000), L.WIDTHS_KEEP_OR_EVICT: (1000000, 700000)}
+
+
 @pytest.mark.parametrize("mask", [L.WIDTHS_ALL, L.WIDTHS_KEEP_OR_EVICT])
 def test_static_scratch_matches_workspace_allocator_twice(mask):
     # the first call is the larger one, so stale scratch would be visible in the second
-    for U, seed, avg in ((70000, 1, 3.0), (3000, 2, 2.5)):
+    big, small = SCRATCH_SIZES[mask]
+    for U, seed, avg in ((big, 1, 3.0), (small, 2, 2.5)):
         w, s = _weights(U, seed)
         budget = int(math.floor(avg * U))
         expect = L.allocate_bits(w, s, budget, mask)
