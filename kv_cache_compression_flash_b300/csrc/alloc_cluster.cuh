@@ -209,8 +209,8 @@ __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const A
       wv[j] = i < n_mine ? p.w[u_begin + i] : 0.f;
       sv[j] = i < n_mine ? p.sigma[u_begin + i] : 0.f;
     }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
+#pragma unroll 1
+    for (int j = 0; j < 8; ++j) {  // not unrolled: keeps the executed code small
       const int i = i0 + j * kCAThreads + tid;
       if (i >= n_mine) break;
       const bool ok = isfinite(wv[j]) && isfinite(sv[j]) && wv[j] >= 0.f && sv[j] >= 0.f;
@@ -312,13 +312,12 @@ __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const A
   };
 
   uint32_t P = 0, M = 0;  // selected top bits so far
-  {
-    const unsigned d0 = cluster_pass(each_top(0u, 0u), 21, 11);
-    P = d0 << 21;
-    M = 0x7FFu << 21;
-    const unsigned d1 = cluster_pass(each_top(P, M), 10, 11);
-    P |= d1 << 10;
-    M |= 0x7FFu << 10;
+#pragma unroll 1
+  for (int ps = 0; ps < 2; ++ps) {  // bits 31..21, then 20..10
+    const int sh = ps == 0 ? 21 : 10;
+    const unsigned d = cluster_pass(each_top(P, M), sh, 11);
+    P |= d << sh;
+    M |= 0x7FFu << sh;
   }
 
   // the items sharing the top 22 bits, gathered into every CTA when they fit

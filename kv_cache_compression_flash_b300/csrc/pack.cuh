@@ -58,6 +58,15 @@ __device__ __forceinline__ int round_div_even(const float x, const float s, cons
   return n;
 }
 
+// round-half-even(x / s): x * (1/s) is within 2^-16 of x / s, so its rint is
+// the answer unless it sits near a half-integer; there the exact test decides
+__device__ __forceinline__ int q_round(const float x, const float s, const float r) {
+  const float t = x * r;
+  const float q = rintf(t);
+  if (fabsf(t - q) < 0.49993896484375f) return static_cast<int>(q);  // 1/2 - 2^-14
+  return round_div_even(x, s, r);
+}
+
 // Quantise this lane's 4 elements of a 64-element group (the half-warp holds
 // the group).  Returns the 4w code bits; *scale_bits gets the fp16 scale.
 __device__ __forceinline__ uint32_t quantize_lane4(const float (&x)[4], const int w, uint16_t* scale_bits,
@@ -76,8 +85,7 @@ __device__ __forceinline__ uint32_t quantize_lane4(const float (&x)[4], const in
   if (s > 0.f && !isinf(s)) {
     const float r = __frcp_rn(s);
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      packed |= (static_cast<uint32_t>(round_div_even(x[e], s, r)) & cmask) << (w * e);
+    for (int e = 0; e < 4; ++e) packed |= (static_cast<uint32_t>(q_round(x[e], s, r)) & cmask) << (w * e);
   }
   return packed;
 }
@@ -127,6 +135,9 @@ __device__ __forceinline__ void lane_bf16x4(const uint16_t* src, float (&x)[4], 
   x[2] = __uint_as_float(r.y << 16);
   x[3] = __uint_as_float(r.y & 0xFFFF0000u);
 }
+
+__device__ __forceinline__ float bf16_lo(uint32_t p) { return __uint_as_float(p << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t p) { return __uint_as_float(p & 0xFFFF0000u); }
 
 // ---------------------------------------------------------------------------
 // plan for token units (axis 0): ids and group offsets of every stored unit
@@ -314,66 +325,49 @@ __device__ __forceinline__ void entry_offsets(const StreamPtrs& sp, const int gp
 }
 
 // ---------------------------------------------------------------------------
-// token units (axis 0, V cache): one half-warp per 64-element group, over the
-// stream entries the plan wrote (so every store is sequential in its stream)
+// token units (axis 0, V cache): one lane per 64-element group, over the
+// stream entries the plan wrote (consecutive lanes write consecutive blocks)
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ int entry_slot(const long long* s_off, const long long gidx) {
+  int s = 0;
+  while (s < 3 && gidx >= s_off[s + 1]) ++s;
+  return s;
+}
+
 template <int DH>
 __global__ void __launch_bounds__(256) pack_rows_kernel(const uint16_t* __restrict__ X, const StreamPtrs sp) {
   constexpr int GPU = DH / 64;
-  constexpr int kUnroll = 4;  // groups per half-warp per step, their loads in flight together
   __shared__ long long s_off[5];
   entry_offsets(sp, GPU, s_off);
   const int l16 = threadIdx.x & 15;
-  const long long total = s_off[4];
-  const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x / 16);
-  for (long long g0 = static_cast<long long>(blockIdx.x) * (blockDim.x / 16) + (threadIdx.x >> 4); g0 < total;
-       g0 += stride * kUnroll) {
-    int sl[kUnroll];
-    long long grp[kUnroll], u[kUnroll];
-#pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      const long long gidx = g0 + j * stride;
-      int s = 0;
-      while (s < 3 && gidx >= s_off[s + 1]) ++s;
-      sl[j] = gidx < total ? s : -1;
-      grp[j] = gidx - s_off[s];  // == entry * GPU + gi
-      if (sl[j] >= 0 && grp[j] >= sp.cap_groups[s]) sl[j] = -1;
-      u[j] = sl[j] >= 0 ? static_cast<long long>(sp.ids[s][grp[j] / GPU]) : 0;
-    }
-    float x[kUnroll][4];
-    uint2 raw[kUnroll];
-#pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      if (sl[j] >= 0) {
-        lane_bf16x4(X + u[j] * DH + static_cast<int>(grp[j] % GPU) * 64 + l16 * 4, x[j], &raw[j]);
-      } else {
-        x[j][0] = x[j][1] = x[j][2] = x[j][3] = 0.f;
-        raw[j] = make_uint2(0u, 0u);
+  const int total = static_cast<int>(s_off[4]);  // groups < 2^31 (units < 2^31, two groups each)
+  const int stride = gridDim.x * (blockDim.x / 16);
+  for (int gidx = blockIdx.x * (blockDim.x / 16) + (threadIdx.x >> 4); gidx < total; gidx += stride) {
+    const int s = entry_slot(s_off, gidx);
+    const int grp = gidx - static_cast<int>(s_off[s]);  // == entry * GPU + gi
+    if (grp >= sp.cap_groups[s]) continue;
+    const long long u = sp.ids[s][grp / GPU];
+    float x[4];
+    uint2 raw;
+    lane_bf16x4(X + u * DH + (grp % GPU) * 64 + l16 * 4, x, &raw);
+    const int w = s == 3 ? 16 : (2 << s);
+    uint32_t packed = 0;
+    if (w != 16) {
+      uint16_t sb;
+      bool ovf;
+      packed = quantize_lane4(x, w, &sb, &ovf);
+      if (l16 == 0) {
+        sp.scales[s][grp] = sb;
+        if (ovf) record_error(KVS_ERR_RANGE);
       }
     }
-#pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      const int s = sl[j];
-      if (s < 0) continue;  // uniform over the half-warp
-      const int w = s == 3 ? 16 : (2 << s);
-      uint32_t packed = 0;
-      if (w != 16) {
-        uint16_t sb;
-        bool ovf;
-        packed = quantize_lane4(x[j], w, &sb, &ovf);
-        if (l16 == 0) {
-          sp.scales[s][grp[j]] = sb;
-          if (ovf) record_error(KVS_ERR_RANGE);
-        }
-      }
-      store_lane_codes(sp.codes[s] + grp[j] * (8 * w), w, l16, packed, raw[j]);
-    }
+    store_lane_codes(sp.codes[s] + static_cast<long long>(grp) * (8 * w), w, l16, packed, raw);
   }
 }
 
 // Token units decoded from the stream entries (entry j of width slot s is
-// unit ids[s][j] with groups goff[s][j] ..), and rows of evicted units
-// (bits == 0) zeroed, in one launch.  One half-warp per group.
+// unit ids[s][j] with groups goff[s][j] ..), one half-warp per group; rows of
+// evicted units (bits == 0) are zeroed in the same launch, one warp per row.
 template <int DH>
 __global__ void __launch_bounds__(256) dequant_rows_kernel(const StreamPtrs sp, const uint8_t* __restrict__ bits,
                                                            const long long U, float* __restrict__ out) {
@@ -381,15 +375,12 @@ __global__ void __launch_bounds__(256) dequant_rows_kernel(const StreamPtrs sp, 
   __shared__ long long s_off[5];
   entry_offsets(sp, GPU, s_off);
   const int l16 = threadIdx.x & 15;
-  const long long total = s_off[4];
-  const long long hw_stride = static_cast<long long>(gridDim.x) * (blockDim.x / 16);
-  for (long long gidx = static_cast<long long>(blockIdx.x) * (blockDim.x / 16) + (threadIdx.x >> 4); gidx < total;
-       gidx += hw_stride) {
-    int s = 0;
-    while (s < 3 && gidx >= s_off[s + 1]) ++s;
-    const long long local = gidx - s_off[s];
-    const long long jj = local / GPU;
-    const int gi = static_cast<int>(local % GPU);
+  const int total = static_cast<int>(s_off[4]);
+  const int stride = gridDim.x * (blockDim.x / 16);
+  for (int gidx = blockIdx.x * (blockDim.x / 16) + (threadIdx.x >> 4); gidx < total; gidx += stride) {
+    const int s = entry_slot(s_off, gidx);
+    const int local = gidx - static_cast<int>(s_off[s]);
+    const int jj = local / GPU, gi = local % GPU;
     const long long u = sp.ids[s][jj];
     const long long grp = sp.goff[s][jj] + gi;
     if (grp >= sp.cap_groups[s]) continue;
@@ -398,14 +389,19 @@ __global__ void __launch_bounds__(256) dequant_rows_kernel(const StreamPtrs sp, 
     dequant_lane4(sp.codes[s] + grp * (8 * w), w, l16, sp.scales[s] + grp, y);
     *reinterpret_cast<float4*>(out + u * DH + gi * 64 + l16 * 4) = make_float4(y[0], y[1], y[2], y[3]);
   }
-  // evicted rows
-  constexpr int TPR = DH / 4;
-  const long long zt = U * TPR;
-  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < zt;
-       e += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long r = e / TPR;
-    if (bits[r] == 0)
-      *reinterpret_cast<float4*>(out + r * DH + (e % TPR) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+  // evicted rows: a warp takes 32 rows, then zeroes the ones with width 0
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+  for (long long r0 = (static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5)) * 32; r0 < U;
+       r0 += nwarps * 32) {
+    const bool zero = r0 + lane < U && bits[r0 + lane] == 0;
+    unsigned m = __ballot_sync(0xFFFFFFFFu, zero);
+    while (m) {
+      const int i = __ffs(m) - 1;
+      m &= m - 1;
+      float4* o4 = reinterpret_cast<float4*>(out + (r0 + i) * DH);
+      for (int c4 = lane; c4 < DH / 4; c4 += 32) o4[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 }
 
@@ -510,7 +506,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) channels_plan_kernel(
   }
 }
 
-// grid (ceil(N/64), Hkv), 256 threads: kept-token group j of head g for every channel
+// grid (ceil(N/64), Hkv), 256 threads: kept-token group j of head g for every
+// channel; one half-warp per channel (lane i: tokens 4i..4i+3)
 template <int DH>
 __global__ void __launch_bounds__(256) pack_channels_kernel(const uint16_t* __restrict__ X, const int N,
                                                             const uint8_t* __restrict__ bits,
@@ -575,8 +572,9 @@ __global__ void __launch_bounds__(256) pack_channels_kernel(const uint16_t* __re
 }
 
 // grid (ceil(N/64) + 1, Hkv), 256 threads.  CTA (j, g) with j below the head's
-// kept-group count decodes kept-token group j of every channel; the CTAs
-// after those zero the head's dropped tokens, 64 per CTA.
+// kept-group count decodes kept-token group j of every channel (one
+// half-warp per channel) through a shared-memory tile and writes the tokens'
+// rows; the CTAs after those zero the head's dropped tokens, 64 per CTA.
 template <int DH>
 __global__ void __launch_bounds__(256) dequant_channels_kernel(const StreamPtrs sp, const int N,
                                                                const uint8_t* __restrict__ bits,
@@ -592,8 +590,7 @@ __global__ void __launch_bounds__(256) dequant_channels_kernel(const StreamPtrs 
   const int n = n_kept[g];
   const int ngk = (n + 63) / 64;
   if (j >= ngk) {  // zero dropped tokens kept[g][n + 64 jz ..]
-    const int jz = j - ngk;
-    const int d0 = n + jz * 64;
+    const int d0 = n + (j - ngk) * 64;
     if (d0 >= N) return;
     const int cnt = min(64, N - d0);
     for (int e = threadIdx.x; e < cnt * (DH / 4); e += 256) {
