@@ -204,6 +204,8 @@ struct ThetaSource {
 
 template <bool CACHE>
 __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocParams p) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
   extern __shared__ unsigned long long s_theta[];  // [K][per] when CACHE
   __shared__ unsigned s_hist[kRadixBins];          // per-block cost per bin (< 2^32: units per block x 16)
   __shared__ unsigned long long s_red[kAllocThreads / 32];

@@ -155,6 +155,8 @@ __device__ __forceinline__ unsigned ca_block_select(const uint32_t* loc, int S, 
 
 template <int CL>
 __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const AllocParams p, const int cand_cap) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = CL > 1 ? static_cast<int>(cluster.block_rank()) : 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

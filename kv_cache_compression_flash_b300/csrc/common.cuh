@@ -309,8 +309,44 @@ __device__ __forceinline__ bool grid_barrier(GridSync* gs, unsigned int nblocks)
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: every kernel of the library is launched so
+// that it may start while the kernel before it on the stream drains.  A
+// kernel calls pdl_wait() before it touches memory the previous kernel may
+// still be writing (or reading), and pdl_trigger() to let the next kernel
+// launch; both are no-ops when the launch did not ask for this.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // small host helpers
 // ---------------------------------------------------------------------------
+// Launches `kern` with programmatic stream serialization (and, with cluster
+// > 0, as clusters of that many CTAs along x).
+template <typename... Params, typename... Args>
+inline cudaError_t launch_k(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Params>(args)...);
+}
 struct WsCarver {
   char* base;
   size_t used;

@@ -117,16 +117,20 @@ int plan_score(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t
   pl->want_plus = (mode & KVS_MODE_KVZIP_PLUS) != 0;
   pl->want_max = (mode & (KVS_MODE_KVZIP | KVS_MODE_KVZIP_PLUS)) != 0;
   pl->lse_given = (mode & KVS_MODE_LSE_GIVEN) != 0;
-  const long long target = static_cast<long long>(sm_count()) * 2 * 4;
+  // Split long loops so the grid holds about three waves of pass-1 CTAs (two
+  // per SM) and one wave of pass-2 CTAs; measured on the bench workload, more
+  // splits cost more in pipeline fill and merging than they gain in balance.
+  const long long slots = static_cast<long long>(sm_count()) * 2;
+  const long long target = static_cast<long long>(sm_count()) * 8, target2 = slots;
   long long w1 = 0;
-  for (int pb = 0; pb < g.n_pb; ++pb) w1 += pb_nkt(g, pb);
+  for (int pb = 1; pb < g.n_pb + 1; pb += 2) w1 += pb_nkt(g, std::min(pb, g.n_pb - 1));  // per pair of row tiles
   w1 *= static_cast<long long>(g.Hkv) * g.n_hc;
   pl->kt_chunk = static_cast<int>(std::max<long long>(4, cdiv(w1, target)));
   pl->n_split1 = static_cast<int>(cdiv(pb_nkt(g, g.n_pb - 1), pl->kt_chunk));
   long long w2 = 0;
   for (int kt = 0; kt < g.n_kt; ++kt) w2 += kt_nvis(g, kt);
   w2 *= static_cast<long long>(g.Hkv) * g.n_hc;
-  pl->qt_chunk = static_cast<int>(std::max<long long>(4, cdiv(w2, target)));
+  pl->qt_chunk = static_cast<int>(std::max<long long>(4, cdiv(w2, target2)));
   pl->n_split2 = static_cast<int>(cdiv(static_cast<long long>(kt_nvis(g, 0)) * g.n_hc, pl->qt_chunk));
   if (pl->n_split2 < 1) pl->n_split2 = 1;
   pl->gram_slice_len = static_cast<int>(cdiv(cdiv(std::max<int64_t>(D, 1), kGramSlices), 32) * 32);
@@ -166,6 +170,7 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 }
 
 constexpr int kStages = 2;
+constexpr int kStages1 = 3;  // pass-1 K ring
 // Each scoring CTA holds 256 TMEM columns; 512 exist per SM.  Asking for at
 // least this much shared memory keeps residency at two CTAs per SM.
 constexpr size_t kScoreMinSmem = 80 * 1024;
@@ -173,11 +178,14 @@ constexpr size_t kScoreMinSmem = 80 * 1024;
 template <int DH>
 int launch_lse(const ScorePlan& pl, const CUtensorMap& mq, const CUtensorMap& mk, float2* part,
                cudaStream_t st) {
-  auto kern = lse_pass_kernel<DH, kStages>;
-  const size_t smem = std::max(sizeof(LseSmem<DH, kStages>) + 1024, kScoreMinSmem);
+  auto kern = lse_pass_kernel<DH, kStages1>;
+  // at least half the shared memory: one CTA per SM (it holds all 512 TMEM columns)
+  const size_t smem = std::max(sizeof(LseSmem<DH, kStages1>) + 1024, static_cast<size_t>(116 * 1024));
   KVS_CUDA_TRY(allow_smem(kern, smem));
-  dim3 grid(pl.n_split1, pl.geo.n_rt);
-  kern<<<grid, kScoreThreads, smem, st>>>(mq, mk, pl.geo, pl.kt_chunk, pl.n_split1, part);
+  const int n_pairs = pl.geo.Hkv * pl.geo.n_hc * ((pl.geo.n_pb + 1) / 2);
+  const int n_items = n_pairs * pl.n_split1;
+  const int grid = std::min(n_items, sm_count());  // persistent: one CTA per SM
+  KVS_CUDA_TRY(launch_k(kern, dim3(grid), dim3(kScoreThreads1), smem, st, 0, mq, mk, pl.geo, pl.kt_chunk, pl.n_split1, n_items, part));
   return KVS_OK;
 }
 
@@ -188,11 +196,11 @@ int launch_col_gt(const ScorePlan& pl, const CUtensorMap& mq, const CUtensorMap&
   const size_t smem = std::max(sizeof(ColSmem<DH, kStages>) + 1024, kScoreMinSmem);
   KVS_CUDA_TRY(allow_smem(kern, smem));
   dim3 grid(pl.n_split2, pl.geo.n_kt * pl.geo.Hkv);
-  kern<<<grid, kScoreThreads, smem, st>>>(mq, mk, pl.geo, pl.qt_chunk, pl.n_split2, bvals, vn, out, part);
+  KVS_CUDA_TRY(launch_k(kern, dim3(grid), dim3(kScoreThreads), smem, st, 0, mq, mk, pl.geo, pl.qt_chunk, pl.n_split2, bvals, vn, out, part));
   if (pl.n_split2 > 1) {
     const int total = pl.geo.Hkv * pl.geo.N;
-    colreduce_finalize_kernel<MAXM><<<static_cast<int>(cdiv(total, 256)), 256, 0, st>>>(
-        pl.geo, pl.qt_chunk, pl.n_split2, part, out);
+    KVS_CUDA_TRY(launch_k(colreduce_finalize_kernel<MAXM>, dim3(static_cast<unsigned>(cdiv(total, 256))), dim3(256),
+                          0, st, 0, pl.geo, pl.qt_chunk, pl.n_split2, part, out));
   }
   return KVS_OK;
 }
@@ -218,20 +226,22 @@ int score_dh(const ScorePlan& pl, const uint16_t* Q, const uint16_t* K, const ui
   rc = make_map_3d(&mk, K, DH, g.N, g.Hkv, 64, 128, 1);
   if (rc) return rc;
   if (pl.want_plus) {
-    row_norm_kernel<<<static_cast<int>(cdiv(g.W, 8)), 256, 0, st>>>(h, g.W, pl.D, w.hn);
-    gram_kernel<DH><<<dim3(kGramSlices, g.Hq, DH / 64), 256, 0, st>>>(WO, pl.D, g.Hq, pl.gram_slice_len, w.gram);
+    KVS_CUDA_TRY(launch_k(row_norm_kernel, dim3(static_cast<unsigned>(cdiv(g.W, 8))), dim3(256), 0, st, 0, h, g.W,
+                          pl.D, w.hn));
+    KVS_CUDA_TRY(launch_k(gram_kernel<DH>, dim3(kGramSlices, g.Hq, DH / 64), dim3(256), 0, st, 0, WO, pl.D, g.Hq,
+                          pl.gram_slice_len, w.gram));
     const size_t vsmem = (static_cast<size_t>(DH) * DH + static_cast<size_t>(DH) * 64) * sizeof(float);
     KVS_CUDA_TRY(allow_smem(vnorm_kernel<DH>, vsmem));
-    vnorm_kernel<DH><<<dim3(static_cast<unsigned>(cdiv(g.N, 64)), g.Hq), 256, vsmem, st>>>(
-        V, w.gram, kGramSlices, g.Hq, g.G, g.N, w.vn);
+    KVS_CUDA_TRY(launch_k(vnorm_kernel<DH>, dim3(static_cast<unsigned>(cdiv(g.N, 64)), g.Hq), dim3(256), vsmem, st, 0,
+                          V, w.gram, kGramSlices, g.Hq, g.G, g.N, w.vn));
   }
   if (pl.lse_given) {
-    if (w.b_plain || w.b_scaled) lse_offsets_kernel<<<g.n_rt, 128, 0, st>>>(g, lse, w.hn, w.b_plain, w.b_scaled);
+    if (w.b_plain || w.b_scaled) KVS_CUDA_TRY(launch_k(lse_offsets_kernel, dim3(g.n_rt), dim3(128), 0, st, 0, g, lse, w.hn, w.b_plain, w.b_scaled));
   } else {
     rc = launch_lse<DH>(pl, mq, mk, w.part1, st);
     if (rc) return rc;
-    lse_finalize_kernel<<<g.n_rt, 128, 0, st>>>(g, pl.kt_chunk, pl.n_split1, w.part1, w.hn, lse, w.b_plain,
-                                                 w.b_scaled);
+    KVS_CUDA_TRY(launch_k(lse_finalize_kernel, dim3(g.n_rt), dim3(128), 0, st, 0, g, pl.kt_chunk, pl.n_split1, w.part1, w.hn, lse, w.b_plain,
+                                                 w.b_scaled));
   }
   if (pl.want_wt) {
     rc = launch_col<DH, false>(pl, mq, mk, w.b_plain, nullptr, w_t, w.part_sum, st);
@@ -400,19 +410,7 @@ cudaError_t set_cluster_attrs(F fn) {
 
 template <class F, class... A>
 cudaError_t launch_cluster(F fn, dim3 grid, int cl, int threads, size_t smem, cudaStream_t st, A... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(static_cast<unsigned>(threads));
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fn, args...);
+  return launch_k(fn, grid, dim3(static_cast<unsigned>(threads)), smem, st, cl, args...);
 }
 
 // the axis-0 plan on one cluster of CL CTAs
@@ -449,11 +447,11 @@ int pack_dh(const uint16_t* X, int64_t Hkv, int64_t N, int axis, const uint8_t* 
     const long long ngroups = U * (DH / 64);
     const int blocks = static_cast<int>(std::min<long long>(cdiv(ngroups, 16), static_cast<long long>(sms) * 8));
     if (dequant) {  // decode straight from the stream entries
-      dequant_rows_kernel<DH><<<blocks, 256, 0, st>>>(sp, bits, U, out);
+      KVS_CUDA_TRY(launch_k(dequant_rows_kernel<DH>, dim3(blocks), dim3(256), 0, st, 0, sp, bits, U, out));
     } else {
       const int rc = launch_rows_plan(bits, U, DH / 64, sp, st);
       if (rc) return rc;
-      pack_rows_kernel<DH><<<blocks, 256, 0, st>>>(X, sp);
+      KVS_CUDA_TRY(launch_k(pack_rows_kernel<DH>, dim3(blocks), dim3(256), 0, st, 0, X, sp));
     }
   } else {
     const StreamPtrs sp = to_ptrs(s, !dequant);
@@ -470,11 +468,11 @@ int pack_dh(const uint16_t* X, int64_t Hkv, int64_t N, int axis, const uint8_t* 
                                 sp, dequant ? 0 : 1));
     if (dequant) {
       const dim3 grid(static_cast<unsigned>(cdiv(N, 64) + 1), static_cast<unsigned>(Hkv));
-      dequant_channels_kernel<DH><<<grid, 256, 0, st>>>(sp, static_cast<int>(N), bits, w.chan_base, w.kept, w.n_kept,
-                                                        out);
+      KVS_CUDA_TRY(launch_k(dequant_channels_kernel<DH>, dim3(grid), dim3(256), 0, st, 0, sp, static_cast<int>(N), bits, w.chan_base, w.kept, w.n_kept,
+                                                        out));
     } else {
       const dim3 grid(static_cast<unsigned>(cdiv(N, 64)), static_cast<unsigned>(Hkv));
-      pack_channels_kernel<DH><<<grid, 256, 0, st>>>(X, static_cast<int>(N), bits, w.chan_base, w.kept, w.n_kept, sp);
+      KVS_CUDA_TRY(launch_k(pack_channels_kernel<DH>, dim3(grid), dim3(256), 0, st, 0, X, static_cast<int>(N), bits, w.chan_base, w.kept, w.n_kept, sp));
     }
   }
   return KVS_OK;
@@ -651,9 +649,9 @@ int kvs_unit_rms(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis,
     const int rpb = kNormThreads / (static_cast<int>(d) / 8) * 4;
     const int blocks = static_cast<int>(std::min<long long>(cdiv(rows, rpb), static_cast<long long>(sms) * 8));
     if (d == 64)
-      row_rms_kernel<64><<<blocks, kNormThreads, 0, st>>>(X, static_cast<int>(rows), sigma);
+      KVS_CUDA_TRY(launch_k(row_rms_kernel<64>, dim3(blocks), dim3(kNormThreads), 0, st, 0, X, static_cast<int>(rows), sigma));
     else
-      row_rms_kernel<128><<<blocks, kNormThreads, 0, st>>>(X, static_cast<int>(rows), sigma);
+      KVS_CUDA_TRY(launch_k(row_rms_kernel<128>, dim3(blocks), dim3(kNormThreads), 0, st, 0, X, static_cast<int>(rows), sigma));
   } else {
     const int rc = launch_colsq(X, N, keep_bits, nullptr, 0, Hkv, d, kColMaskedRms, 1.f, sigma, st);
     if (rc) return rc;
@@ -729,9 +727,8 @@ int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t bud
   if (rc) return rc;
   if (CL > 0) {
     p.per = per;
-    cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = cluster_cfg(CL, ca_smem, st, attr);
-    KVS_CUDA_TRY(cudaLaunchKernelEx(&cfg, cluster_alloc_fn(CL), p, cand_cap));
+    KVS_CUDA_TRY(launch_k(cluster_alloc_fn(CL), dim3(static_cast<unsigned>(CL)), dim3(kCAThreads), ca_smem, st, CL, p,
+                          cand_cap));
     return KVS_OK;
   }
   // Otherwise a cooperative grid: a few thousand units per block with their
@@ -811,9 +808,9 @@ int kvs_threshold_keep(const float* score, int64_t Hkv, int64_t N, float tau, in
   if (N % 4 == 0 && (!aligned16(score) || (reinterpret_cast<uintptr_t>(bits) & 3u))) return KVS_ERR_INVALID_ARG;
   const long long total = Hkv * N;
   const int blocks = static_cast<int>(std::min<long long>(cdiv(total, 1024), static_cast<long long>(sm_count()) * 8));
-  threshold_keep_kernel<<<blocks, 256, 0, as_stream(stream)>>>(score, total, static_cast<int>(N), tau,
+  KVS_CUDA_TRY(launch_k(threshold_keep_kernel, dim3(blocks), dim3(256), 0, as_stream(stream), 0, score, total, static_cast<int>(N), tau,
                                                                static_cast<int>(std::min<int64_t>(window, N)),
-                                                               static_cast<uint8_t>(keep_width), bits);
+                                                               static_cast<uint8_t>(keep_width), bits));
   KVS_CUDA_TRY(cudaGetLastError());
   return KVS_OK;
 }

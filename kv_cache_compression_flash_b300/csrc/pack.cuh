@@ -206,6 +206,8 @@ template <int CL>
 __global__ void __launch_bounds__(kPlanThreads, 1) rows_plan_kernel(const uint8_t* __restrict__ bits,
                                                                     const long long U, const long long per,
                                                                     const int groups_per_unit, const StreamPtrs sp) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
   namespace cgp = cooperative_groups;
   cgp::cluster_group cluster = cgp::this_cluster();
   const int rank = CL > 1 ? static_cast<int>(cluster.block_rank()) : 0;
@@ -336,6 +338,8 @@ __device__ __forceinline__ int entry_slot(const long long* s_off, const long lon
 
 template <int DH>
 __global__ void __launch_bounds__(256) pack_rows_kernel(const uint16_t* __restrict__ X, const StreamPtrs sp) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
   constexpr int GPU = DH / 64;
   __shared__ long long s_off[5];
   entry_offsets(sp, GPU, s_off);
@@ -371,6 +375,8 @@ __global__ void __launch_bounds__(256) pack_rows_kernel(const uint16_t* __restri
 template <int DH>
 __global__ void __launch_bounds__(256) dequant_rows_kernel(const StreamPtrs sp, const uint8_t* __restrict__ bits,
                                                            const long long U, float* __restrict__ out) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
   constexpr int GPU = DH / 64;
   __shared__ long long s_off[5];
   entry_offsets(sp, GPU, s_off);
@@ -420,6 +426,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) channels_plan_kernel(
     const uint8_t* __restrict__ keep, const int N, const int Hkv, const uint8_t* __restrict__ bits,
     int* __restrict__ kept, int* __restrict__ n_kept, long long* __restrict__ chan_base, const StreamPtrs sp,
     const int write_streams) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
   namespace cgp = cooperative_groups;
   cgp::cluster_group cluster = cgp::this_cluster();
   const int CL = static_cast<int>(cluster.num_blocks());
@@ -514,6 +522,8 @@ __global__ void __launch_bounds__(256) pack_channels_kernel(const uint16_t* __re
                                                             const long long* __restrict__ chan_base,
                                                             const int* __restrict__ kept,
                                                             const int* __restrict__ n_kept, const StreamPtrs sp) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
   // odd word stride: the column reads below (lane i takes rows 4i..4i+3)
   // spread over the banks instead of piling onto two
   constexpr int LDW = DH / 2 + 1;  // 32-bit words per row
@@ -582,6 +592,8 @@ __global__ void __launch_bounds__(256) dequant_channels_kernel(const StreamPtrs 
                                                                const int* __restrict__ kept,
                                                                const int* __restrict__ n_kept,
                                                                float* __restrict__ out) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
   constexpr int LD = DH + 1;  // odd stride: conflict-light column writes
   __shared__ float tile[64][LD];
   __shared__ int s_w[DH];

@@ -11,12 +11,15 @@
 // Both passes are flash-style: 128x128 logit tiles S = Q K^T are produced by
 // tcgen05.mma into tensor memory (fp32) from 128-byte-swizzled bf16 tiles that
 // TMA streams into shared memory; the N x N matrix never exists in HBM.
-// Roles per CTA: warps 0-7 reduce the tiles, warp 8 issues TMA, warp 9 issues
-// the MMAs.  Reducer warp w reads TMEM lanes 32(w%4)..+31 (one tile row per
-// thread) and the column half w/4 of the tile, in two 32-column chunks whose
-// loads overlap the previous chunk's arithmetic (packed fp32x2 FMA/ADD, ex2 on
-// the special-function unit).  Two TMEM buffers let the MMA of tile i+1 run
-// while tile i is being reduced.
+// Reducer warp w reads TMEM lanes 32(w%4)..+31 (one tile row per thread), all
+// 128 columns of a tile in four 32-column chunks whose loads overlap the
+// previous chunk's arithmetic (packed fp32x2 FMA/ADD, ex2 on the
+// special-function unit).  The reducer warps form two groups that take
+// alternate tiles (ping-pong), so one group's TMEM loads and barrier waits
+// overlap the other's arithmetic, and two TMEM buffers let the MMA of the next
+// tile run meanwhile.  Pass 1 (one CTA per SM): 16 reducer warps, TMA warp
+// 16, MMA warp 17.  Pass 2 (two CTAs per SM): 8 reducer warps, TMA warp 8,
+// MMA warp 9.
 //
 // GQA packing: a 128-row query tile holds P = 128/Gt consecutive window rows
 // of Gt heads of one KV group (row j = head (j / P), position pmin + j % P), so
@@ -34,8 +37,10 @@
 
 namespace kvs {
 
-constexpr int kScoreThreads = 320;   // 8 reducer warps, 1 TMA warp, 1 MMA warp
+constexpr int kScoreThreads = 320;   // pass 2: 8 reducer warps, 1 TMA warp, 1 MMA warp
 constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kScoreThreads1 = 576;  // pass 1: 16 reducer warps (two row tiles), 1 TMA warp, 1 MMA warp
+constexpr int kTmaWarp1 = 16, kMmaWarp1 = 17;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 
@@ -98,16 +103,16 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // ---------------------------------------------------------------------------
 template <int DH, int NS>
 struct LseSmem {
-  uint8_t q[TileCfg<DH>::kTileBytes];
+  uint8_t q[2][2][TileCfg<DH>::kTileBytes];  // [item parity][row tile]
   uint8_t k[NS][TileCfg<DH>::kTileBytes];
-  uint64_t q_full, k_full[NS], k_empty[NS], s_full[2], s_empty[2], drain;
+  uint64_t q_full[2], q_empty[2], k_full[NS], k_empty[NS], s_full[2], s_empty[2], drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-// partial[((rt * n_split + split) * 2 + half) * 128 + row] = (running max m,
+// partial[((rt * n_split + split) * 2 + group) * 128 + row] = (running max m,
 // sum l), log2 domain: the row's 2^(x - m) summed over the split's key tiles
-// and the column half, x = s * log2(e)/sqrt(d).
+// that reducer group `group` took (even or odd ones), x = s * log2(e)/sqrt(d).
 
 // one 32-column chunk of a pass-1 row: mask (diagonal tiles), running max and
 // rescaled sum
@@ -137,93 +142,142 @@ __device__ __forceinline__ void lse_chunk(uint32_t (&r)[32], const int t0, const
     acc0 = f2_add(acc0, f2_pack(ex2_approx(e0), ex2_approx(e1)));
     acc1 = f2_add(acc1, f2_pack(ex2_approx(e2), ex2_approx(e3)));
   }
-  float s0, s1, s2, s3;
+  float s0, s1;
   f2_unpack(f2_add(acc0, acc1), &s0, &s1);
-  (void)s2, (void)s3;
   l = l * ex2_approx(m - m_new) + (s0 + s1);
   m = m_new;
 }
+
+// Persistent CTAs (one per SM) walk work items it = blockIdx.x, + gridDim.x, ...;
+// item (pair, split) = TWO row tiles (position blocks 2pp, 2pp+1 of a head
+// chunk) over key tiles [split * kt_chunk, ..).  Every K tile TMA brings in
+// feeds two MMAs (M = 256 in effect), halving the L2 -> shared-memory traffic
+// per flop; the pipeline (TMA ring, two double-buffered TMEM accumulator
+// pairs, the next item's row tiles) runs on across items.  Reducer warps 0-7
+// take the even K tiles and warps 8-15 the odd ones (ping-pong: one group's
+// TMEM loads overlap the other's arithmetic); within a group, warps 0-3 and
+// 4-7 take row tiles 0 and 1, one tile row (all 128 columns) per thread.
+// Warp 16 issues TMA, warp 17 the MMAs.
+struct LseItem {
+  int pb0, g, hc, gh, kt0, kt1;
+  bool two;
+};
+
+__device__ __forceinline__ bool lse_item(const ScoreGeom& geo, const int kt_chunk, const int n_split, const int it,
+                                         LseItem* x) {
+  const int n_pp = (geo.n_pb + 1) / 2;
+  const int jy = it / n_split, split = it % n_split;
+  const int pp = n_pp - 1 - (jy % n_pp);  // longest rows first
+  x->gh = jy / n_pp;
+  x->g = x->gh / geo.n_hc;
+  x->hc = x->gh % geo.n_hc;
+  x->pb0 = 2 * pp;
+  x->two = 2 * pp + 1 < geo.n_pb;
+  x->kt0 = split * kt_chunk;
+  x->kt1 = min(pb_nkt(geo, x->two ? x->pb0 + 1 : x->pb0), x->kt0 + kt_chunk);
+  return x->kt0 < x->kt1;
+}
+
 template <int DH, int NS>
-__global__ void __launch_bounds__(kScoreThreads, 2)
+__global__ void __launch_bounds__(kScoreThreads1, 1)
     lse_pass_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
-                    const ScoreGeom geo, const int kt_chunk, const int n_split, float2* __restrict__ partial) {
+                    const ScoreGeom geo, const int kt_chunk, const int n_split, const int n_items,
+                    float2* __restrict__ partial) {
   extern __shared__ uint8_t smem_raw[];
   LseSmem<DH, NS>& S = *reinterpret_cast<LseSmem<DH, NS>*>(align1024(smem_raw));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x;
-  const int jy = blockIdx.y;
-  const int pb = geo.n_pb - 1 - (jy % geo.n_pb);  // longest rows launch first
-  const int gh = jy / geo.n_pb;
-  const int g = gh / geo.n_hc, hc = gh % geo.n_hc;
-  const int rt = gh * geo.n_pb + pb;
-  const int pmin = geo.q_pos0 + pb * geo.P;
-  const int kt0 = split * kt_chunk;
-  const int kt1 = min(pb_nkt(geo, pb), kt0 + kt_chunk);
-  if (kt0 >= kt1 || timeout_recorded()) return;  // uniform over the CTA, before any barrier
-  const int niter = kt1 - kt0;
+  if (timeout_recorded()) return;  // uniform over the CTA, before any barrier
 
   if (threadIdx.x == 0) {
-    mbar_init(&S.q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.q_full[b], 1);
+      mbar_init(&S.q_empty[b], 1);
+      mbar_init(&S.s_full[b], 1);
+      mbar_init(&S.s_empty[b], 8);  // the 8 warps of the group that owns buffer b
+    }
     for (int s = 0; s < NS; ++s) {
       mbar_init(&S.k_full[s], 1);
       mbar_init(&S.k_empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&S.s_full[b], 1);
-      mbar_init(&S.s_empty[b], 8);
     }
     mbar_init(&S.drain, 1);
     S.abort_flag = 0;
     mbar_fence_init();
   }
   if (warp == 0) {
-    tmem_alloc(&S.tmem_base, 256);
+    tmem_alloc(&S.tmem_base, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // Q, K and the offsets may come from the previous kernel on the stream
+  pdl_trigger();
   const uint32_t tmem = S.tmem_base;
   volatile int* abort_flag = &S.abort_flag;
 
-  if (warp == kTmaWarp) {
+  if (warp == kTmaWarp1) {
     if (lane == 0) {  // TMA producer
       prefetch_tensormap(&mapQ);
       prefetch_tensormap(&mapK);
       constexpr uint32_t kBytes = TileCfg<DH>::kTileBytes;
-      mbar_arrive_expect_tx(&S.q_full, kBytes);
+      int n_it = 0, kc = 0, issued = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        LseItem x;
+        if (!lse_item(geo, kt_chunk, n_split, it, &x)) continue;
+        const int qb = n_it & 1;
+        if (!mbar_wait(&S.q_empty[qb], ((n_it >> 1) & 1) ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(&S.q_full[qb], 2 * kBytes);
 #pragma unroll
-      for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
-        tma_load_3d(S.q + p * 16384, &mapQ, &S.q_full, p * 64, pb * geo.P, g * geo.G + hc * geo.Gt);
-      int issued = 0;
-      for (int i = 0; i < niter; ++i) {
-        const int s = i % NS;
-        const uint32_t ph = (i / NS) & 1;
-        if (!mbar_wait(&S.k_empty[s], ph ^ 1u, abort_flag)) break;
-        mbar_arrive_expect_tx(&S.k_full[s], kBytes);
+        for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
-          tma_load_3d(S.k[s] + p * 16384, &mapK, &S.k_full[s], p * 64, (kt0 + i) * 128, g);
-        issued = i + 1;
+          for (int p = 0; p < TileCfg<DH>::kPanels; ++p)  // a missing second tile reads as zeros
+            tma_load_3d(S.q[qb][t] + p * 16384, &mapQ, &S.q_full[qb], p * 64, (x.pb0 + t) * geo.P,
+                        x.g * geo.G + x.hc * geo.Gt);
+        ++n_it;
+        for (int kt = x.kt0; kt < x.kt1; ++kt, ++kc) {
+          const int s = kc % NS;
+          if (!mbar_wait(&S.k_empty[s], ((kc / NS) & 1) ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&S.k_full[s], kBytes);
+#pragma unroll
+          for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
+            tma_load_3d(S.k[s] + p * 16384, &mapK, &S.k_full[s], p * 64, kt * 128, x.g);
+          issued = kc + 1;
+        }
       }
       if (*abort_flag) {  // let our copies land before the CTA goes away
         volatile int never = 0;
-        mbar_wait(&S.q_full, 0, &never);
+        for (int i = max(0, n_it - 2); i < n_it; ++i) mbar_wait(&S.q_full[i & 1], (i >> 1) & 1, &never);
         for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(&S.k_full[i % NS], (i / NS) & 1, &never);
       }
     }
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) {  // MMA issuer
-      if (mbar_wait(&S.q_full, 0, abort_flag)) {
-        for (int i = 0; i < niter; ++i) {
-          const int s = i % NS, b = i & 1;
-          if (!mbar_wait(&S.k_full[s], (i / NS) & 1, abort_flag)) break;
-          if (!mbar_wait(&S.s_empty[b], ((i >> 1) & 1) ^ 1u, abort_flag)) break;
+  } else if (warp == kMmaWarp1) {
+    if (lane == 0) {  // MMA issuer: two row tiles against each K tile
+      int n_it = 0, kc = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        LseItem x;
+        if (!lse_item(geo, kt_chunk, n_split, it, &x)) continue;
+        const int qb = n_it & 1;
+        if (!mbar_wait(&S.q_full[qb], (n_it >> 1) & 1, abort_flag)) break;
+        ++n_it;
+        for (int kt = x.kt0; kt < x.kt1; ++kt, ++kc) {
+          const int s = kc % NS, b = kc & 1;
+          if (!mbar_wait(&S.k_full[s], (kc / NS) & 1, abort_flag) ||
+              !mbar_wait(&S.s_empty[b], ((kc >> 1) & 1) ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          issue_tile_mma<DH>(tmem + b * 128, smem_u32(S.q), smem_u32(S.k[s]));
+          issue_tile_mma<DH>(tmem + (2 * b) * 128, smem_u32(S.q[qb][0]), smem_u32(S.k[s]));
+          if (x.two) issue_tile_mma<DH>(tmem + (2 * b + 1) * 128, smem_u32(S.q[qb][1]), smem_u32(S.k[s]));
           umma_commit(&S.k_empty[s]);
           umma_commit(&S.s_full[b]);
         }
+        if (ok) umma_commit(&S.q_empty[qb]);  // the item's row tiles are free once its MMAs finish
       }
       if (*abort_flag) {
         volatile int never = 0;
@@ -231,37 +285,67 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
         mbar_wait(&S.drain, 0, &never);
       }
     }
-  } else {  // warps 0-7: one tile row per thread, column half warp / 4
-    const int q4 = warp & 3, hh = warp >> 2;
+  } else {  // warps 0-15: group warp / 8 takes the tiles of its parity (ping-pong), row tile (warp / 4) % 2
+    const int grp = warp >> 3, t = (warp >> 2) & 1, q4 = warp & 3;
     const int row = q4 * 32 + lane;
-    const int pos = pmin + row % geo.P;
     const float c = geo.c_log2;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + hh * 64;
-    float m = -INFINITY, l = 0.f;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + t * 128;
     uint32_t va[32], vb[32];
-    for (int i = 0; i < niter; ++i) {
-      const int b = i & 1;
-      if (!mbar_wait(&S.s_full[b], (i >> 1) & 1, abort_flag)) break;
-      tc_fence_after();
-      const int t0 = (kt0 + i) * 128 + hh * 64;
-      const bool diag = t0 + 63 > pmin;
-      tmem_issue32(lane_base + b * 128, va);
-      tmem_wait32(va);
-      tmem_issue32(lane_base + b * 128 + 32, vb);
-      lse_chunk(va, t0, pos, diag, c, m, l);
-      tmem_wait32(vb);
-      tc_fence_before();  // this warp is done with the TMEM buffer
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.s_empty[b]);
-      lse_chunk(vb, t0 + 32, pos, diag, c, m, l);
+    int kc = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      LseItem x;
+      if (!lse_item(geo, kt_chunk, n_split, it, &x)) continue;
+      const int pmin = geo.q_pos0 + (x.pb0 + t) * geo.P;
+      const int pos = pmin + row % geo.P;
+      const bool active = t == 0 || x.two;
+      float m = -INFINITY, l = 0.f;
+      for (int kt = x.kt0; kt < x.kt1; ++kt, ++kc) {
+        if ((kc & 1) != grp) continue;  // the other group's tile
+        const int b = kc & 1;
+        if (!mbar_wait(&S.s_full[b], (kc >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (active) {
+          const int t0 = kt * 128;
+          const bool diag = t0 + 127 > pmin;
+          const uint32_t base = lane_base + b * 256;
+          // four 32-column chunks; each chunk's load overlaps the previous chunk's arithmetic
+          tmem_issue32(base, va);
+          tmem_wait32(va);
+          tmem_issue32(base + 32, vb);
+          lse_chunk(va, t0, pos, diag, c, m, l);
+          tmem_wait32(vb);
+          tmem_issue32(base + 64, va);
+          lse_chunk(vb, t0 + 32, pos, diag, c, m, l);
+          tmem_wait32(va);
+          tmem_issue32(base + 96, vb);
+          lse_chunk(va, t0 + 64, pos, diag, c, m, l);
+          tmem_wait32(vb);
+          tc_fence_before();  // this warp is done with the TMEM buffer
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.s_empty[b]);
+          lse_chunk(vb, t0 + 96, pos, diag, c, m, l);
+        } else {  // no second row tile: only release the buffer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.s_empty[b]);
+        }
+      }
+      if (ok && active) {
+        const int rt = x.gh * geo.n_pb + x.pb0 + t;
+        const int split = it % n_split;
+        partial[((static_cast<size_t>(rt) * n_split + split) * 2 + grp) * 128 + row] = make_float2(m, l);
+      }
     }
-    partial[((static_cast<size_t>(rt) * n_split + split) * 2 + hh) * 128 + row] = make_float2(m, l);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -273,6 +357,8 @@ __global__ void lse_finalize_kernel(const ScoreGeom geo, const int kt_chunk, con
                                     const float2* __restrict__ partial, const float* __restrict__ hn,
                                     float* __restrict__ lse, float* __restrict__ b_plain,
                                     float* __restrict__ b_scaled) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
   const int rt = blockIdx.x, row = threadIdx.x;
   const int pb = rt % geo.n_pb;
   const int gh = rt / geo.n_pb;
@@ -297,6 +383,8 @@ __global__ void lse_finalize_kernel(const ScoreGeom geo, const int kt_chunk, con
 // Pass-2 offsets from a given lse (natural log, [Hq, W]), same layout as above.
 __global__ void lse_offsets_kernel(const ScoreGeom geo, const float* __restrict__ lse, const float* __restrict__ hn,
                                    float* __restrict__ b_plain, float* __restrict__ b_scaled) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
   const int rt = blockIdx.x, row = threadIdx.x;
   const int pb = rt % geo.n_pb;
   const int gh = rt / geo.n_pb;
@@ -352,11 +440,11 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
     mbar_init(&S.k_full, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&S.q_full[s], 1);
-      mbar_init(&S.q_empty[s], 1 + 8);
+      mbar_init(&S.q_empty[s], 1 + 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.s_full[b], 1);
-      mbar_init(&S.s_empty[b], 8);
+      mbar_init(&S.s_empty[b], 4);
     }
     mbar_init(&S.drain, 1);
     S.abort_flag = 0;
@@ -369,6 +457,8 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // Q, K and the offsets may come from the previous kernel on the stream
+  pdl_trigger();
   const uint32_t tmem = S.tmem_base;
   volatile int* abort_flag = &S.abort_flag;
 
@@ -420,12 +510,12 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
         mbar_wait(&S.drain, 0, &never);
       }
     }
-  } else {  // warps 0-7: one key per thread (TMEM lane), query-column half warp / 4
+  } else {  // warps 0-7: one key per thread (TMEM lane); group warp / 4 takes the query tiles of its parity
     const int q4 = warp & 3, hh = warp >> 2;
     const int krow = q4 * 32 + lane;
     const int t = t0 + krow;
     const float c = geo.c_log2;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + hh * 64;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
     float acc = 0.f;
     float best = 0.f;
     float mx[GT];
@@ -492,26 +582,34 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
         if (cur_hc >= 0) flush(cur_hc);
         cur_hc = hc;
       }
+      if ((i & 1) != hh) continue;  // the other group's tile (it also releases the stage)
       if (!mbar_wait(&S.s_full[b], (i >> 1) & 1, abort_flag)) break;
       // the staged offsets bv[s] arrived with the query tile
       if (!mbar_wait(&S.q_full[s], (i / NS) & 1, abort_flag)) break;
       tc_fence_after();
       const int pmin = geo.q_pos0 + pb * P;
       const bool diag = pmin < t0 + 127;
-      tmem_issue32(lane_base + b * 128, va);
+      const uint32_t base = lane_base + b * 128;
+      tmem_issue32(base, va);
       tmem_wait32(va);
-      tmem_issue32(lane_base + b * 128 + 32, vb);
-      chunk(va, S.bv[s] + hh * 64, hh * 64, pmin, diag);
+      tmem_issue32(base + 32, vb);
+      chunk(va, S.bv[s], 0, pmin, diag);
+      tmem_wait32(vb);
+      tmem_issue32(base + 64, va);
+      chunk(vb, S.bv[s] + 32, 32, pmin, diag);
+      tmem_wait32(va);
+      tmem_issue32(base + 96, vb);
+      chunk(va, S.bv[s] + 64, 64, pmin, diag);
       tmem_wait32(vb);
       tc_fence_before();  // this warp is done with the TMEM buffer
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.s_empty[b]);
-      chunk(vb, S.bv[s] + hh * 64 + 32, hh * 64 + 32, pmin, diag);
+      chunk(vb, S.bv[s] + 96, 96, pmin, diag);
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.q_empty[s]);  // done reading bv[s]
     }
     if (MAXMODE && cur_hc >= 0) flush(cur_hc);
-    // combine the two column halves in a fixed order: half 1 hands its value to half 0
+    // combine the two groups in a fixed order: group 1 hands its value to group 0
     float* comb = reinterpret_cast<float*>(S.comb);
     if (hh == 1) comb[krow] = MAXMODE ? best : acc;
     asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -538,6 +636,8 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
 template <bool MAXMODE>
 __global__ void colreduce_finalize_kernel(const ScoreGeom geo, const int qt_chunk, const int n_split,
                                           const float* __restrict__ part, float* __restrict__ out) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   const int total = geo.Hkv * geo.N;
   if (idx >= total) return;
@@ -557,6 +657,8 @@ __global__ void colreduce_finalize_kernel(const ScoreGeom geo, const int qt_chun
 // out[r] = |X[r, :]|_2, one warp per row, 16-byte loads, fixed-order reduction
 __global__ void row_norm_kernel(const uint16_t* __restrict__ X, const int rows, const int cols,
                                 float* __restrict__ out) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
   const int warps = blockDim.x >> 5;
   const int r = blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -585,6 +687,8 @@ __global__ void row_norm_kernel(const uint16_t* __restrict__ X, const int rows, 
 template <int DH>
 __global__ void __launch_bounds__(256) gram_kernel(const uint16_t* __restrict__ WO, const int D, const int Hq,
                                                    const int slice_len, float* __restrict__ gram) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
   constexpr int CPT = DH / 16;
   __shared__ float T[32][DH + 4];
   const int s = blockIdx.x, h = blockIdx.y, c1b = blockIdx.z * 64;
@@ -634,6 +738,8 @@ __global__ void __launch_bounds__(256) vnorm_kernel(const uint16_t* __restrict__
                                                     const float* __restrict__ gram, const int n_slices,
                                                     const int Hq, const int G, const int N,
                                                     float* __restrict__ vn) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
   constexpr int CPT = DH / 16;
   extern __shared__ uint8_t smem_raw[];
   float* Gs = reinterpret_cast<float*>(smem_raw);  // [DH][DH]
