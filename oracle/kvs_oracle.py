@@ -412,3 +412,57 @@ def threshold_keep(score, tau, window, keep_width=16):
         keep = score >= np.float32(tau)
     keep[:, max(0, N - int(window)):] = True
     return np.where(keep, keep_width, 0).astype(np.uint8)
+
+
+# ----------------------------------------------------------------------------
+# O7. decode attention over the TriZone streams
+# ----------------------------------------------------------------------------
+def trizone_decode(q, K_hat, V_hat, keep, k_new=None, v_new=None):
+    """One decode step of attention over a compressed cache.   [RDKV §2.3, TriZone]
+
+    The page's decode kernel computes the logits and the output over three
+    zones at once, with dequantisation inside the products:
+      zone A + B: the old cache, dequantised (K_hat, V_hat from dequantize();
+                  zone B is the width-16 part of V), over the kept tokens only;
+      zone C:     k_new, v_new [Hkv, Nc, d], tokens generated since compression,
+                  all visible.
+    An evicted token (keep false) takes no part in the softmax.  Since fusing
+    the dequantisation into the products changes no value, the plain definition
+    is attention over the dequantised cache:
+      s_t = q_h . k_t / sqrt(d),   lse_h = ln sum_t exp(s_t),
+      out_h = sum_t exp(s_t - lse_h) v_t,
+    with query head h reading KV head h // G.  No visible token: out = 0 and
+    lse = -inf.
+    q [Hq, d]; K_hat, V_hat [Hkv, N, d]; keep [Hkv, N].  Returns (out [Hq, d],
+    lse [Hq]) in float64.
+    Pins: hand-worked fixture; one visible token gives its V row; equal logits
+    give the mean of V; evicted tokens have no effect however large their key;
+    the two-part log-sum-exp merge; permutation invariance.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    K_hat = np.asarray(K_hat, dtype=np.float64)
+    V_hat = np.asarray(V_hat, dtype=np.float64)
+    keep = np.asarray(keep).astype(bool)
+    Hq, d = q.shape
+    Hkv = K_hat.shape[0]
+    G = Hq // Hkv
+    out = np.zeros((Hq, d))
+    lse = np.full(Hq, -np.inf)
+    for hd in range(Hq):
+        g = hd // G
+        keys = [K_hat[g, keep[g]]]
+        vals = [V_hat[g, keep[g]]]
+        if k_new is not None:
+            keys.append(np.asarray(k_new, dtype=np.float64)[g])
+            vals.append(np.asarray(v_new, dtype=np.float64)[g])
+        Kv = np.concatenate(keys, axis=0)
+        Vv = np.concatenate(vals, axis=0)
+        if Kv.shape[0] == 0:
+            continue
+        s = Kv @ q[hd] / math.sqrt(d)
+        m = s.max()
+        e = np.exp(s - m)
+        z = e.sum()
+        lse[hd] = m + math.log(z)
+        out[hd] = (e @ Vv) / z
+    return out, lse

@@ -364,3 +364,96 @@ def test_threshold_special_cases():
     assert O.threshold_keep(s, 0.0, 0)[0, 3] == 0                        # NaN never passes
     kept = [int((O.threshold_keep(s, t, 5) > 0).sum()) for t in (0.1, 0.3, 0.6, 0.9)]
     assert kept == sorted(kept, reverse=True)                            # monotone in tau
+
+
+# ----------------------------------------------------------------------------
+# decode attention over the TriZone streams   [RDKV §2.3]
+# ----------------------------------------------------------------------------
+def _lse_value(s):
+    return {"ln2": math.log(2), "ln3": math.log(3), "ln4": math.log(4), "-inf": -math.inf}[s]
+
+
+def test_trizone_hand_examples():
+    ex = json.load(open(os.path.join(GOLD, "trizone_hand_examples.json")))["examples"]
+    for e in ex:
+        kn = None if e["k_new"] is None else np.array(e["k_new"], float)
+        vn = None if e["v_new"] is None else np.array(e["v_new"], float)
+        out, lse = O.trizone_decode(np.array(e["q"], float), np.array(e["K_hat"], float),
+                                    np.array(e["V_hat"], float), np.array(e["keep"], bool), kn, vn)
+        np.testing.assert_allclose(out, np.array(e["out"], float), rtol=0, atol=1e-13, err_msg=e["name"])
+        want = np.array([_lse_value(s) for s in e["lse"]])
+        np.testing.assert_array_equal(np.isinf(lse), np.isinf(want))
+        fin = np.isfinite(want)
+        np.testing.assert_allclose(lse[fin], want[fin], rtol=0, atol=1e-13, err_msg=e["name"])
+
+
+def _trizone_case(rng, Hq=4, Hkv=2, N=37, d=8, Nc=3):
+    q = rng.standard_normal((Hq, d))
+    K = rng.standard_normal((Hkv, N, d))
+    V = rng.standard_normal((Hkv, N, d))
+    keep = rng.random((Hkv, N)) > 0.4
+    kn = rng.standard_normal((Hkv, Nc, d))
+    vn = rng.standard_normal((Hkv, Nc, d))
+    return q, K, V, keep, kn, vn
+
+
+def test_trizone_single_visible_token_and_equal_logits():
+    rng = np.random.default_rng(21)
+    q, K, V, keep, kn, vn = _trizone_case(rng)
+    keep1 = np.zeros_like(keep)
+    keep1[:, 5] = True
+    out, lse = O.trizone_decode(q, K, V, keep1)
+    for hd in range(4):
+        g = hd // 2
+        np.testing.assert_array_equal(out[hd], V[g, 5])                    # softmax of one logit is 1
+        assert abs(lse[hd] - K[g, 5] @ q[hd] / math.sqrt(8)) < 1e-13
+    out, lse = O.trizone_decode(np.zeros_like(q), K, V, keep, kn, vn)       # every logit 0: the mean
+    for hd in range(4):
+        g = hd // 2
+        rows = np.concatenate([V[g, keep[g]], vn[g]])
+        np.testing.assert_allclose(out[hd], rows.mean(axis=0), rtol=0, atol=1e-13)
+        assert abs(lse[hd] - math.log(rows.shape[0])) < 1e-13
+
+
+def test_trizone_evicted_tokens_have_no_effect():
+    rng = np.random.default_rng(22)
+    q, K, V, keep, kn, vn = _trizone_case(rng)
+    base = O.trizone_decode(q, K, V, keep, kn, vn)
+    K2, V2 = K.copy(), V.copy()
+    K2[~keep] = 1e3 * np.sign(q[0]).reshape(1, -1)                         # would dominate if visible
+    V2[~keep] = 7e5
+    got = O.trizone_decode(q, K2, V2, keep, kn, vn)
+    np.testing.assert_array_equal(got[0], base[0])
+    np.testing.assert_array_equal(got[1], base[1])
+
+
+def test_trizone_two_part_merge_and_permutation():
+    """Attention over A u B equals the log-sum-exp merge of attention over A and
+    over B (the split a decode kernel relies on), and a permutation of the old
+    tokens changes nothing."""
+    rng = np.random.default_rng(23)
+    q, K, V, keep, kn, vn = _trizone_case(rng, N=60, Nc=5)
+    out, lse = O.trizone_decode(q, K, V, keep, kn, vn)
+    oa, la = O.trizone_decode(q, K, V, keep)                               # old tokens only
+    ob, lb = O.trizone_decode(q, K, V, np.zeros_like(keep), kn, vn)        # new tokens only
+    m = np.maximum(la, lb)
+    wa, wb = np.exp(la - m), np.exp(lb - m)
+    np.testing.assert_allclose(lse, m + np.log(wa + wb), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out, (wa[:, None] * oa + wb[:, None] * ob) / (wa + wb)[:, None], rtol=0, atol=1e-12)
+    perm = rng.permutation(60)
+    op, lp = O.trizone_decode(q, K[:, perm], V[:, perm], keep[:, perm], kn, vn)
+    np.testing.assert_allclose(op, out, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lp, lse, rtol=0, atol=1e-12)
+
+
+def test_trizone_gqa_head_mapping():
+    """Query head h reads KV head h // G: with constant V rows per KV head the
+    output of head h is that constant."""
+    rng = np.random.default_rng(24)
+    q, K, V, keep, kn, vn = _trizone_case(rng, Hq=6, Hkv=3)
+    for g in range(3):
+        V[g] = g + 1.0
+        vn[g] = g + 1.0
+    out, _ = O.trizone_decode(q, K, V, keep, kn, vn)
+    for hd in range(6):
+        np.testing.assert_allclose(out[hd], hd // 2 + 1.0, rtol=1e-14)
