@@ -299,6 +299,8 @@ def quantize_pack(X, axis, bits, keep=None):
             ng = -(-n // GROUP)
             offs.append(ng_total)
             ng_total += ng
+            if ng == 0:                                # a channel over no kept token: no groups
+                continue
             xp = np.zeros(ng * GROUP)
             xp[:n] = x
             xg = xp.reshape(ng, GROUP)

@@ -94,3 +94,35 @@ def test_alloc_and_pack_argument_errors(lib):
     assert lib.kvs_quantize_pack(p, 8, 64, 96, 0, p, None, ctypes.byref(s), p, 1 << 20, None) == 2
     assert lib.kvs_unit_rms(p, 8, 64, 128, 3, None, p, p, 1 << 20, None) == 1
     assert lib.kvs_channel_weights(p, p, 8, 3, 16, 64, 128, p, p, 1 << 20, None) == 1
+
+
+def test_trizone_sizes_and_argument_errors(lib):
+    # header 8 heads x 16 int64 (1 KiB) + one uint32 per token, each part 256-aligned
+    assert lib.kvs_trizone_index_size(8, 8192) == 1024 + 8 * 8192 * 4
+    # 32 heads x (32 old chunks + 1 zone C chunk) records: max and sum (4224 B each, padded
+    # to 4352) and 128 output floats
+    assert lib.kvs_trizone_workspace_size(32, 8, 8192, 128, 100) == 2 * 4352 + 32 * 33 * 128 * 4
+    assert lib.kvs_trizone_workspace_size(0, 8, 8192, 128, 0) == 0
+    p = ctypes.c_void_p(1 << 20)
+    s = L.StreamSetC()
+    dec = lib.kvs_trizone_decode
+    args = [p, 32, 8, 8192, 128, ctypes.byref(s), ctypes.byref(s), p, None, None, None, 0, p, p, p, 1 << 30, None]
+    bad = list(args)
+    bad[0] = None                                                       # no queries
+    assert dec(*bad) == 1
+    bad = list(args)
+    bad[2] = 5                                                          # Hq not a multiple of Hkv
+    assert dec(*bad) == 1
+    bad = list(args)
+    bad[4] = 64                                                         # only d = 128
+    assert dec(*bad) == 2
+    bad = list(args)
+    bad[1], bad[2] = 24, 8                                              # G = 3
+    assert dec(*bad) == 2
+    bad = list(args)
+    bad[11] = 10                                                        # zone C rows without buffers
+    assert dec(*bad) == 1
+    bad = list(args)
+    bad[15] = 16                                                        # workspace too small
+    assert dec(*bad) == 6
+    assert lib.kvs_trizone_index(ctypes.byref(s), ctypes.byref(s), p, 8, 8192, 128, p, 1 << 30, None) == 1  # no counts

@@ -457,3 +457,16 @@ def test_trizone_gqa_head_mapping():
     out, _ = O.trizone_decode(q, K, V, keep, kn, vn)
     for hd in range(6):
         np.testing.assert_allclose(out[hd], hd // 2 + 1.0, rtol=1e-14)
+
+
+def test_channels_over_no_kept_token_have_no_groups():
+    """Axis 1 with every token evicted: each channel unit holds zero elements,
+    so it is listed with no groups and dequantises to zeros."""
+    X = np.ones((2, 5, 64))
+    keep = np.zeros((2, 5), bool)
+    bits = np.array([2, 4, 8, 16] * 32, np.uint8)
+    st = O.quantize_pack(X, 1, bits, keep)
+    for wd in (2, 4, 8, 16):
+        assert st[wd]["n_groups"] == 0 and st[wd]["codes"].size == 0
+        assert st[wd]["ids"].size == 32 and (st[wd]["group_offsets"] == 0).all()
+    assert not O.dequantize(st, X.shape, 1, bits, keep).any()
