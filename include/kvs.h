@@ -242,6 +242,52 @@ int kvs_dequantize(const kvs_stream_set* streams, int64_t Hkv, int64_t N, int64_
 int kvs_threshold_keep(const float* score, int64_t Hkv, int64_t N, float tau, int64_t window,
                        uint32_t keep_width, uint8_t* bits, void* stream);
 
+/* ---- TriZone decode attention ------------------------------------------- */
+/* One decode step of attention over a compressed pool, with dequantisation
+ * inside both products   [RDKV §2.3, TriZone: zone A = the packed K channels
+ * and V rows at widths 2/4/8, zone B = the width-16 streams read as raw bf16,
+ * zone C = bf16 K/V rows of tokens generated after compression].  For query
+ * head hd (KV head g = hd / G):
+ *     s_t = q_hd . k_t / sqrt(d) over the kept old tokens t (bits_V > 0; an
+ *           evicted token takes no part) and the n_new new tokens,
+ *     lse[hd] = ln sum_t exp(s_t),   out[hd] = sum_t exp(s_t - lse[hd]) v_t,
+ * where k_t, v_t of an old token are the dequantised values kvs_dequantize
+ * returns (a K channel of width 0 contributes zero).  No visible token:
+ * out = 0, lse = -inf.
+ * Supported: d = 128; G in {1, 2} or a multiple of 4.
+ *
+ * kvs_trizone_index builds, once per compressed pool (after kvs_quantize_pack
+ * of both caches), the per-KV-head lookup the decode kernel reads:
+ *     k_streams : K streams (axis 1) and v_streams : V streams (axis 0), as
+ *                 written by kvs_quantize_pack, counts included (HOST pointers
+ *                 to structs of device pointers)
+ *     bits_v    : uint8 [Hkv, N], the V widths the V streams were packed with
+ *     index     : device, kvs_trizone_index_size(Hkv, N) bytes, 256-aligned;
+ *                 opaque to the caller, valid while the streams are unchanged.
+ * Streams that do not match bits_v record KVS_ERR_RANGE; the decode then skips
+ * what it cannot locate and stays inside the stream capacities.
+ *
+ * kvs_trizone_decode:
+ *     q        : bf16 [Hq, d], the decode step's queries, 16-byte aligned
+ *     k_new, v_new : bf16 [Hkv, nc_cap, d], zone C rows (row j of KV head g at
+ *                (g*nc_cap + j)*d); may be NULL when nc_cap = 0
+ *     n_new    : DEVICE int32 scalar, the valid zone C rows (0 <= n_new <=
+ *                nc_cap; outside that range records KVS_ERR_RANGE and is
+ *                clamped).  Read on the device, so a captured CUDA graph
+ *                replays across decode steps while zone C grows.
+ *     out      : float [Hq, d];  lse : float [Hq] (natural log)
+ *     workspace: kvs_trizone_workspace_size(Hq, Hkv, N, d, nc_cap) bytes,
+ *                256-aligned.
+ * Stream codes must be 16-byte aligned. */
+size_t kvs_trizone_index_size(int64_t Hkv, int64_t N);
+int kvs_trizone_index(const kvs_stream_set* k_streams, const kvs_stream_set* v_streams, const uint8_t* bits_v,
+                      int64_t Hkv, int64_t N, int64_t d, void* index, size_t index_bytes, void* stream);
+size_t kvs_trizone_workspace_size(int64_t Hq, int64_t Hkv, int64_t N, int64_t d, int64_t nc_cap);
+int kvs_trizone_decode(const uint16_t* q, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
+                       const kvs_stream_set* k_streams, const kvs_stream_set* v_streams, const void* index,
+                       const uint16_t* k_new, const uint16_t* v_new, const int32_t* n_new, int64_t nc_cap,
+                       float* out, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

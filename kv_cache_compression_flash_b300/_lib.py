@@ -54,6 +54,12 @@ SIGNATURES = {
                                                             c_void_p]),
     "kvs_threshold_keep": (c_int, [c_void_p, c_int64, c_int64, ctypes.c_float, c_int64, c_uint32, c_void_p,
                                    c_void_p]),
+    "kvs_trizone_index_size": (c_size_t, [c_int64, c_int64]),
+    "kvs_trizone_index": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_void_p, c_size_t,
+                                  c_void_p]),
+    "kvs_trizone_workspace_size": (c_size_t, [c_int64] * 5),
+    "kvs_trizone_decode": (c_int, [c_void_p] + [c_int64] * 4 + [c_void_p] * 6 + [c_int64] + [c_void_p] * 3
+                           + [c_size_t, c_void_p]),
 }
 
 
@@ -291,3 +297,39 @@ def threshold_keep(score, tau, window=128, keep_width=16, *, out=None, stream=No
     _check(lib().kvs_threshold_keep(_ptr(score), Hkv, N, float(tau), int(window), int(keep_width), _ptr(bits),
                                     _stream(stream)), "kvs_threshold_keep")
     return bits
+
+
+def trizone_index(k_streams: Streams, v_streams: Streams, bits_v, *, out=None, stream=None):
+    """The decode lookup of one compressed pool (uint8 device buffer, opaque)."""
+    Hkv, N, d = v_streams.shape
+    L = lib()
+    n = L.kvs_trizone_index_size(Hkv, N)
+    idx = out if out is not None else torch.empty(n, dtype=torch.uint8, device=v_streams.counts.device)
+    _check(L.kvs_trizone_index(ctypes.byref(k_streams.c), ctypes.byref(v_streams.c), _ptr(bits_v), Hkv, N, d,
+                               _ptr(idx), idx.numel(), _stream(stream)), "kvs_trizone_index")
+    return idx
+
+
+def trizone_decode(q, k_streams: Streams, v_streams: Streams, index, k_new=None, v_new=None, n_new=None, *,
+                   out=None, lse=None, ws=None, stream=None):
+    """One decode step over the compressed pool plus zone C rows: (out [Hq, d] fp32, lse [Hq] fp32).
+
+    k_new, v_new: bf16 [Hkv, nc_cap, d] or None; n_new: device int32 [1] (valid rows)."""
+    _bf16(q, "q")
+    Hq, d = q.shape
+    Hkv, N, _ = v_streams.shape
+    nc_cap = 0
+    if k_new is not None:
+        _bf16(k_new, "k_new")
+        _bf16(v_new, "v_new")
+        nc_cap = k_new.shape[1]
+        if n_new is None or n_new.dtype != torch.int32 or not n_new.is_cuda:
+            raise KvsError("n_new must be an int32 CUDA tensor when zone C rows are given")
+    L = lib()
+    o = out if out is not None else torch.empty(Hq, d, dtype=torch.float32, device=q.device)
+    ls = lse if lse is not None else torch.empty(Hq, dtype=torch.float32, device=q.device)
+    buf = _ws(ws, "trizone", L.kvs_trizone_workspace_size(Hq, Hkv, N, d, nc_cap), q.device)
+    _check(L.kvs_trizone_decode(_ptr(q), Hq, Hkv, N, d, ctypes.byref(k_streams.c), ctypes.byref(v_streams.c),
+                                _ptr(index), _ptr(k_new), _ptr(v_new), _ptr(n_new), nc_cap, _ptr(o), _ptr(ls),
+                                _ptr(buf), buf.numel(), _stream(stream)), "kvs_trizone_decode")
+    return o, ls

@@ -13,6 +13,7 @@
 #include "norms.cuh"
 #include "pack.cuh"
 #include "score.cuh"
+#include "decode.cuh"
 
 using namespace kvs;
 
@@ -31,229 +32,7 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
-// ---- TMA tensor maps ---------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// 3-D bf16 map over [dim2][dim1][dim0] (dim0 contiguous), 128-byte swizzle,
-// out-of-range elements read as zero.
-int make_map_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2, uint32_t box0,
-                uint32_t box1, uint32_t box2) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return KVS_ERR_CUDA;
-  const cuuint64_t gdim[3] = {dim0, dim1, dim2};
-  const cuuint64_t gstride[2] = {dim0 * 2, dim0 * dim1 * 2};
-  const cuuint32_t box[3] = {box0, box1, box2};
-  const cuuint32_t estride[3] = {1, 1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box,
-                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? KVS_OK : KVS_ERR_CUDA;
-}
-
-// ---- scoring plan -------------------------------------------------------------
-constexpr int kGramSlices = 8;
-
-struct ScorePlan {
-  ScoreGeom geo;
-  int d, D;
-  int kt_chunk, n_split1;
-  int qt_chunk, n_split2;
-  int gram_slice_len;
-  bool want_wt, want_max, want_plus, lse_given;
-};
-
-int validate_shape(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t q_pos0) {
-  if (Hq <= 0 || Hkv <= 0 || W <= 0 || N <= 0 || d <= 0 || q_pos0 < 0) return KVS_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0 || q_pos0 + W > N) return KVS_ERR_INVALID_ARG;
-  const int64_t G = Hq / Hkv;
-  if (d != 64 && d != 128) return KVS_ERR_UNSUPPORTED;
-  if (!(G <= 4 || G % 4 == 0)) return KVS_ERR_UNSUPPORTED;
-  if (N >= (1ll << 31) || Hkv * N >= (1ll << 31) || Hq * W >= (1ll << 31) || Hq >= (1 << 16))
-    return KVS_ERR_UNSUPPORTED;
-  return KVS_OK;
-}
-
-int plan_score(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t D, int64_t q_pos0,
-               uint32_t mode, ScorePlan* pl) {
-  int st = validate_shape(Hq, Hkv, W, N, d, q_pos0);
-  if (st) return st;
-  if ((mode & ~(KVS_MODE_LSE | KVS_MODE_RDKV_WT | KVS_MODE_KVZIP | KVS_MODE_KVZIP_PLUS | KVS_MODE_LSE_GIVEN)) != 0)
-    return KVS_ERR_INVALID_ARG;
-  if ((mode & KVS_MODE_KVZIP) && (mode & KVS_MODE_KVZIP_PLUS)) return KVS_ERR_INVALID_ARG;
-  if ((mode & KVS_MODE_KVZIP_PLUS) && (D <= 0 || D % 8 != 0)) return KVS_ERR_INVALID_ARG;
-  ScoreGeom& g = pl->geo;
-  g.Hq = static_cast<int>(Hq);
-  g.Hkv = static_cast<int>(Hkv);
-  g.G = static_cast<int>(Hq / Hkv);
-  g.Gt = g.G <= 4 ? g.G : 4;
-  g.P = 128 / g.Gt;
-  g.W = static_cast<int>(W);
-  g.N = static_cast<int>(N);
-  g.q_pos0 = static_cast<int>(q_pos0);
-  g.n_hc = g.G / g.Gt;
-  g.n_pb = static_cast<int>(cdiv(W, g.P));
-  g.n_rt = g.Hkv * g.n_hc * g.n_pb;
-  g.n_kt = static_cast<int>(cdiv(N, 128));
-  g.c_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
-  pl->d = static_cast<int>(d);
-  pl->D = static_cast<int>(D);
-  pl->want_wt = (mode & KVS_MODE_RDKV_WT) != 0;
-  pl->want_plus = (mode & KVS_MODE_KVZIP_PLUS) != 0;
-  pl->want_max = (mode & (KVS_MODE_KVZIP | KVS_MODE_KVZIP_PLUS)) != 0;
-  pl->lse_given = (mode & KVS_MODE_LSE_GIVEN) != 0;
-  // Split long loops so the grid holds about three waves of pass-1 CTAs (two
-  // per SM) and one wave of pass-2 CTAs; measured on the bench workload, more
-  // splits cost more in pipeline fill and merging than they gain in balance.
-  const long long slots = static_cast<long long>(sm_count()) * 2;
-  const long long target = static_cast<long long>(sm_count()) * 8, target2 = slots;
-  long long w1 = 0;
-  for (int pb = 1; pb < g.n_pb + 1; pb += 2) w1 += pb_nkt(g, std::min(pb, g.n_pb - 1));  // per pair of row tiles
-  w1 *= static_cast<long long>(g.Hkv) * g.n_hc;
-  pl->kt_chunk = static_cast<int>(std::max<long long>(4, cdiv(w1, target)));
-  pl->n_split1 = static_cast<int>(cdiv(pb_nkt(g, g.n_pb - 1), pl->kt_chunk));
-  long long w2 = 0;
-  for (int kt = 0; kt < g.n_kt; ++kt) w2 += kt_nvis(g, kt);
-  w2 *= static_cast<long long>(g.Hkv) * g.n_hc;
-  pl->qt_chunk = static_cast<int>(std::max<long long>(4, cdiv(w2, target2)));
-  pl->n_split2 = static_cast<int>(cdiv(static_cast<long long>(kt_nvis(g, 0)) * g.n_hc, pl->qt_chunk));
-  if (pl->n_split2 < 1) pl->n_split2 = 1;
-  pl->gram_slice_len = static_cast<int>(cdiv(cdiv(std::max<int64_t>(D, 1), kGramSlices), 32) * 32);
-  return KVS_OK;
-}
-
-struct ScoreWs {
-  float2* part1;
-  float* b_plain;
-  float* b_scaled;
-  float* part_sum;
-  float* part_max;
-  float* hn;
-  float* gram;
-  float* vn;
-};
-
-size_t carve_score(const ScorePlan& pl, void* base, size_t cap, ScoreWs* w) {
-  WsCarver c{static_cast<char*>(base), 0, cap};
-  const ScoreGeom& g = pl.geo;
-  w->part1 = pl.lse_given ? nullptr : c.take<float2>(static_cast<size_t>(g.n_rt) * pl.n_split1 * 256);
-  w->b_plain = (pl.want_wt || (pl.want_max && !pl.want_plus)) ? c.take<float>(static_cast<size_t>(g.n_rt) * 128)
-                                                              : nullptr;
-  w->b_scaled = pl.want_plus ? c.take<float>(static_cast<size_t>(g.n_rt) * 128) : nullptr;
-  const size_t kn = static_cast<size_t>(g.Hkv) * g.N;
-  w->part_sum = (pl.want_wt && pl.n_split2 > 1) ? c.take<float>(kn * pl.n_split2) : nullptr;
-  w->part_max = (pl.want_max && pl.n_split2 > 1) ? c.take<float>(kn * pl.n_split2) : nullptr;
-  w->hn = pl.want_plus ? c.take<float>(g.W) : nullptr;
-  w->gram = pl.want_plus ? c.take<float>(static_cast<size_t>(kGramSlices) * g.Hq * pl.d * pl.d) : nullptr;
-  w->vn = pl.want_plus ? c.take<float>(static_cast<size_t>(g.Hq) * g.N) : nullptr;
-  return c.used;
-}
-
-template <class K>
-cudaError_t allow_smem(K kernel, size_t bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-}
-
-constexpr int kStages = 2;
-constexpr int kStages1 = 3;  // pass-1 K ring
-// Each scoring CTA holds 256 TMEM columns; 512 exist per SM.  Asking for at
-// least this much shared memory keeps residency at two CTAs per SM.
-constexpr size_t kScoreMinSmem = 80 * 1024;
-
-template <int DH>
-int launch_lse(const ScorePlan& pl, const CUtensorMap& mq, const CUtensorMap& mk, float2* part,
-               cudaStream_t st) {
-  auto kern = lse_pass_kernel<DH, kStages1>;
-  // at least half the shared memory: one CTA per SM (it holds all 512 TMEM columns)
-  const size_t smem = std::max(sizeof(LseSmem<DH, kStages1>) + 1024, static_cast<size_t>(116 * 1024));
-  KVS_CUDA_TRY(allow_smem(kern, smem));
-  const int n_pairs = pl.geo.Hkv * pl.geo.n_hc * ((pl.geo.n_pb + 1) / 2);
-  const int n_items = n_pairs * pl.n_split1;
-  const int grid = std::min(n_items, sm_count());  // persistent: one CTA per SM
-  KVS_CUDA_TRY(launch_k(kern, dim3(grid), dim3(kScoreThreads1), smem, st, 0, mq, mk, pl.geo, pl.kt_chunk, pl.n_split1, n_items, part));
-  return KVS_OK;
-}
-
-template <int DH, int GT, bool MAXM>
-int launch_col_gt(const ScorePlan& pl, const CUtensorMap& mq, const CUtensorMap& mk, const float* bvals,
-                  const float* vn, float* out, float* part, cudaStream_t st) {
-  auto kern = colreduce_pass_kernel<DH, kStages, GT, MAXM>;
-  const size_t smem = std::max(sizeof(ColSmem<DH, kStages>) + 1024, kScoreMinSmem);
-  KVS_CUDA_TRY(allow_smem(kern, smem));
-  dim3 grid(pl.n_split2, pl.geo.n_kt * pl.geo.Hkv);
-  KVS_CUDA_TRY(launch_k(kern, dim3(grid), dim3(kScoreThreads), smem, st, 0, mq, mk, pl.geo, pl.qt_chunk, pl.n_split2, bvals, vn, out, part));
-  if (pl.n_split2 > 1) {
-    const int total = pl.geo.Hkv * pl.geo.N;
-    KVS_CUDA_TRY(launch_k(colreduce_finalize_kernel<MAXM>, dim3(static_cast<unsigned>(cdiv(total, 256))), dim3(256),
-                          0, st, 0, pl.geo, pl.qt_chunk, pl.n_split2, part, out));
-  }
-  return KVS_OK;
-}
-
-template <int DH, bool MAXM>
-int launch_col(const ScorePlan& pl, const CUtensorMap& mq, const CUtensorMap& mk, const float* bvals,
-               const float* vn, float* out, float* part, cudaStream_t st) {
-  switch (pl.geo.Gt) {
-    case 1: return launch_col_gt<DH, 1, MAXM>(pl, mq, mk, bvals, vn, out, part, st);
-    case 2: return launch_col_gt<DH, 2, MAXM>(pl, mq, mk, bvals, vn, out, part, st);
-    case 4: return launch_col_gt<DH, 4, MAXM>(pl, mq, mk, bvals, vn, out, part, st);
-    default: return KVS_ERR_UNSUPPORTED;
-  }
-}
-
-template <int DH>
-int score_dh(const ScorePlan& pl, const uint16_t* Q, const uint16_t* K, const uint16_t* V, const uint16_t* h,
-             const uint16_t* WO, float* lse, float* w_t, float* s_plus, const ScoreWs& w, cudaStream_t st) {
-  const ScoreGeom& g = pl.geo;
-  CUtensorMap mq, mk;
-  int rc = make_map_3d(&mq, Q, DH, g.W, g.Hq, 64, g.P, g.Gt);
-  if (rc) return rc;
-  rc = make_map_3d(&mk, K, DH, g.N, g.Hkv, 64, 128, 1);
-  if (rc) return rc;
-  if (pl.want_plus) {
-    KVS_CUDA_TRY(launch_k(row_norm_kernel, dim3(static_cast<unsigned>(cdiv(g.W, 8))), dim3(256), 0, st, 0, h, g.W,
-                          pl.D, w.hn));
-    KVS_CUDA_TRY(launch_k(gram_kernel<DH>, dim3(kGramSlices, g.Hq, DH / 64), dim3(256), 0, st, 0, WO, pl.D, g.Hq,
-                          pl.gram_slice_len, w.gram));
-    const size_t vsmem = (static_cast<size_t>(DH) * DH + static_cast<size_t>(DH) * 64) * sizeof(float);
-    KVS_CUDA_TRY(allow_smem(vnorm_kernel<DH>, vsmem));
-    KVS_CUDA_TRY(launch_k(vnorm_kernel<DH>, dim3(static_cast<unsigned>(cdiv(g.N, 64)), g.Hq), dim3(256), vsmem, st, 0,
-                          V, w.gram, kGramSlices, g.Hq, g.G, g.N, w.vn));
-  }
-  if (pl.lse_given) {
-    if (w.b_plain || w.b_scaled) KVS_CUDA_TRY(launch_k(lse_offsets_kernel, dim3(g.n_rt), dim3(128), 0, st, 0, g, lse, w.hn, w.b_plain, w.b_scaled));
-  } else {
-    rc = launch_lse<DH>(pl, mq, mk, w.part1, st);
-    if (rc) return rc;
-    KVS_CUDA_TRY(launch_k(lse_finalize_kernel, dim3(g.n_rt), dim3(128), 0, st, 0, g, pl.kt_chunk, pl.n_split1, w.part1, w.hn, lse, w.b_plain,
-                                                 w.b_scaled));
-  }
-  if (pl.want_wt) {
-    rc = launch_col<DH, false>(pl, mq, mk, w.b_plain, nullptr, w_t, w.part_sum, st);
-    if (rc) return rc;
-  }
-  if (pl.want_max) {
-    rc = launch_col<DH, true>(pl, mq, mk, pl.want_plus ? w.b_scaled : w.b_plain, pl.want_plus ? w.vn : nullptr,
-                              s_plus, w.part_max, st);
-    if (rc) return rc;
-  }
-  return KVS_OK;
-}
+#include "score_host.cuh"
 
 // ---- allocation ---------------------------------------------------------------
 int alloc_blocks_max() { return sm_count() * 8; }
@@ -811,6 +590,90 @@ int kvs_threshold_keep(const float* score, int64_t Hkv, int64_t N, float tau, in
   KVS_CUDA_TRY(launch_k(threshold_keep_kernel, dim3(blocks), dim3(256), 0, as_stream(stream), 0, score, total, static_cast<int>(N), tau,
                                                                static_cast<int>(std::min<int64_t>(window, N)),
                                                                static_cast<uint8_t>(keep_width), bits));
+  KVS_CUDA_TRY(cudaGetLastError());
+  return KVS_OK;
+}
+
+// ---- TriZone decode attention ------------------------------------------------
+size_t kvs_trizone_index_size(int64_t Hkv, int64_t N) {
+  if (Hkv <= 0 || N <= 0) return 0;
+  return static_cast<size_t>(cdiv(Hkv * kTzHdr * 8, 256) * 256 + cdiv(Hkv * N * 4, 256) * 256);
+}
+
+int kvs_trizone_index(const kvs_stream_set* k_streams, const kvs_stream_set* v_streams, const uint8_t* bits_v,
+                      int64_t Hkv, int64_t N, int64_t d, void* index, size_t index_bytes, void* stream) {
+  if (Hkv <= 0 || N <= 0 || d <= 0 || !bits_v || !index) return KVS_ERR_INVALID_ARG;
+  if (!streams_ok(k_streams) || !streams_ok(v_streams) || !k_streams->counts || !v_streams->counts)
+    return KVS_ERR_INVALID_ARG;
+  if (d != kTzD || Hkv * N >= (1ll << 31) || Hkv * d >= (1ll << 31)) return KVS_ERR_UNSUPPORTED;
+  for (int i = 0; i < 4; ++i)
+    if (v_streams->cap_groups[i] > static_cast<int64_t>(kTzLocMask) + 1) return KVS_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(index) & 255u) || index_bytes < kvs_trizone_index_size(Hkv, N))
+    return KVS_ERR_WORKSPACE;
+  long long* hdr = static_cast<long long*>(index);
+  uint32_t* vloc = reinterpret_cast<uint32_t*>(static_cast<char*>(index) + cdiv(Hkv * kTzHdr * 8, 256) * 256);
+  KVS_CUDA_TRY(launch_k(trizone_index_kernel, dim3(static_cast<unsigned>(Hkv)), dim3(1024), 0, as_stream(stream), 0,
+                        to_ptrs(k_streams, true), to_ptrs(v_streams, true), bits_v, static_cast<int>(N),
+                        static_cast<int>(d), hdr, vloc));
+  KVS_CUDA_TRY(cudaGetLastError());
+  return KVS_OK;
+}
+
+size_t kvs_trizone_workspace_size(int64_t Hq, int64_t Hkv, int64_t N, int64_t d, int64_t nc_cap) {
+  if (Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || nc_cap < 0) return 0;
+  const long long slots = cdiv(N, kTzChunk) + cdiv(nc_cap, kTzChunk);
+  return static_cast<size_t>(2 * cdiv(Hq * slots * 4, 256) * 256 + cdiv(Hq * slots * d * 4, 256) * 256);
+}
+
+int kvs_trizone_decode(const uint16_t* q, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
+                       const kvs_stream_set* k_streams, const kvs_stream_set* v_streams, const void* index,
+                       const uint16_t* k_new, const uint16_t* v_new, const int32_t* n_new, int64_t nc_cap,
+                       float* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || nc_cap < 0 || !q || !index || !out || !lse)
+    return KVS_ERR_INVALID_ARG;
+  if (Hq % Hkv) return KVS_ERR_INVALID_ARG;
+  if (nc_cap > 0 && (!k_new || !v_new || !n_new)) return KVS_ERR_INVALID_ARG;
+  if (!streams_ok(k_streams) || !streams_ok(v_streams)) return KVS_ERR_INVALID_ARG;
+  const long long G = Hq / Hkv;
+  if (d != kTzD || !(G == 1 || G == 2 || G % 4 == 0) || Hkv * N >= (1ll << 31) || nc_cap >= (1ll << 30))
+    return KVS_ERR_UNSUPPORTED;
+  for (int i = 0; i < 4; ++i)
+    if (!aligned16(k_streams->codes[i]) || !aligned16(v_streams->codes[i])) return KVS_ERR_INVALID_ARG;
+  if (!aligned16(q) || (nc_cap > 0 && (!aligned16(k_new) || !aligned16(v_new)))) return KVS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(index) & 255u)) return KVS_ERR_WORKSPACE;
+  const size_t need = kvs_trizone_workspace_size(Hq, Hkv, N, d, nc_cap);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return KVS_ERR_WORKSPACE;
+  const int HG = G >= 4 ? 4 : static_cast<int>(G);
+  const long long Z = G / HG;
+  // flash-decoding split: about two CTAs per SM over the (KV head, head slice) pairs
+  const long long per_pair = std::max<long long>(1, 2LL * sm_count() / (Hkv * Z));
+  const int n_split = static_cast<int>(std::min<long long>(cdiv(N, kTzChunk), per_pair));
+  const int n_csplit = static_cast<int>(std::min<long long>(cdiv(nc_cap, kTzChunk), per_pair));
+  const int slots = n_split + n_csplit;
+  const long long rec_cap = Hq * (cdiv(N, kTzChunk) + cdiv(nc_cap, kTzChunk));   // layout of the workspace size
+  float* pm = static_cast<float*>(workspace);
+  float* pl = reinterpret_cast<float*>(static_cast<char*>(workspace) + cdiv(rec_cap * 4, 256) * 256);
+  float* po = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * cdiv(rec_cap * 4, 256) * 256);
+  const long long* hdr = static_cast<const long long*>(index);
+  const uint32_t* vloc =
+      reinterpret_cast<const uint32_t*>(static_cast<const char*>(index) + cdiv(Hkv * kTzHdr * 8, 256) * 256);
+  const dim3 grid(static_cast<unsigned>(slots), static_cast<unsigned>(Hkv), static_cast<unsigned>(Z));
+  const float qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  const StreamPtrs ks = to_ptrs(k_streams, false), vs = to_ptrs(v_streams, false);
+  cudaStream_t st = as_stream(stream);
+  const int g_ = static_cast<int>(G), n_ = static_cast<int>(N), ncap = static_cast<int>(nc_cap);
+  if (HG == 4)
+    KVS_CUDA_TRY(launch_k(trizone_decode_kernel<4>, grid, dim3(kTzThreads), 0, st, 0, q, g_, n_, ks, vs, hdr, vloc,
+                          k_new, v_new, n_new, ncap, n_split, qscale, pm, pl, po));
+  else if (HG == 2)
+    KVS_CUDA_TRY(launch_k(trizone_decode_kernel<2>, grid, dim3(kTzThreads), 0, st, 0, q, g_, n_, ks, vs, hdr, vloc,
+                          k_new, v_new, n_new, ncap, n_split, qscale, pm, pl, po));
+  else
+    KVS_CUDA_TRY(launch_k(trizone_decode_kernel<1>, grid, dim3(kTzThreads), 0, st, 0, q, g_, n_, ks, vs, hdr, vloc,
+                          k_new, v_new, n_new, ncap, n_split, qscale, pm, pl, po));
+  KVS_CUDA_TRY(launch_k(trizone_combine_kernel, dim3(static_cast<unsigned>(Hq)), dim3(kTzD), 0, st, 0, slots, pm, pl,
+                        po, out, lse));
   KVS_CUDA_TRY(cudaGetLastError());
   return KVS_OK;
 }

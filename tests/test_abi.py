@@ -99,9 +99,9 @@ def test_alloc_and_pack_argument_errors(lib):
 def test_trizone_sizes_and_argument_errors(lib):
     # header 8 heads x 16 int64 (1 KiB) + one uint32 per token, each part 256-aligned
     assert lib.kvs_trizone_index_size(8, 8192) == 1024 + 8 * 8192 * 4
-    # 32 heads x (32 old chunks + 1 zone C chunk) records: max and sum (4224 B each, padded
-    # to 4352) and 128 output floats
-    assert lib.kvs_trizone_workspace_size(32, 8, 8192, 128, 100) == 2 * 4352 + 32 * 33 * 128 * 4
+    # 32 heads x (64 old chunks of 128 tokens + 1 zone C chunk) records: max and sum
+    # (8320 B each, padded to 8448) and 128 output floats
+    assert lib.kvs_trizone_workspace_size(32, 8, 8192, 128, 100) == 2 * 8448 + 32 * 65 * 128 * 4
     assert lib.kvs_trizone_workspace_size(0, 8, 8192, 128, 0) == 0
     p = ctypes.c_void_p(1 << 20)
     s = L.StreamSetC()
