@@ -150,10 +150,14 @@ def measured_peaks():
     return 1800.0, 6400.0, "fallback"
 
 
+# the sources that define the scoring passes: their kernels and their launch plan
+PASS_SOURCES = ("common.cuh", "score.cuh", "score_host.cuh")
+
+
 def csrc_hash() -> str:
     h = hashlib.sha256()
     cdir = os.path.join(ROOT, "kv_cache_compression_flash_b300", "csrc")
-    for f in sorted(os.listdir(cdir)):
+    for f in PASS_SOURCES:
         h.update(open(os.path.join(cdir, f), "rb").read())
     return h.hexdigest()[:16]
 
