@@ -597,7 +597,7 @@ int kvs_threshold_keep(const float* score, int64_t Hkv, int64_t N, float tau, in
 // ---- TriZone decode attention ------------------------------------------------
 size_t kvs_trizone_index_size(int64_t Hkv, int64_t N) {
   if (Hkv <= 0 || N <= 0) return 0;
-  return static_cast<size_t>(cdiv(Hkv * kTzHdr * 8, 256) * 256 + cdiv(Hkv * N * 4, 256) * 256);
+  return static_cast<size_t>(tz_layout(Hkv, N).total);
 }
 
 int kvs_trizone_index(const kvs_stream_set* k_streams, const kvs_stream_set* v_streams, const uint8_t* bits_v,
@@ -606,23 +606,25 @@ int kvs_trizone_index(const kvs_stream_set* k_streams, const kvs_stream_set* v_s
   if (!streams_ok(k_streams) || !streams_ok(v_streams) || !k_streams->counts || !v_streams->counts)
     return KVS_ERR_INVALID_ARG;
   if (d != kTzD || Hkv * N >= (1ll << 31) || Hkv * d >= (1ll << 31)) return KVS_ERR_UNSUPPORTED;
-  for (int i = 0; i < 4; ++i)
-    if (v_streams->cap_groups[i] > static_cast<int64_t>(kTzLocMask) + 1) return KVS_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(index) & 255u) || index_bytes < kvs_trizone_index_size(Hkv, N))
     return KVS_ERR_WORKSPACE;
-  long long* hdr = static_cast<long long*>(index);
-  uint32_t* vloc = reinterpret_cast<uint32_t*>(static_cast<char*>(index) + cdiv(Hkv * kTzHdr * 8, 256) * 256);
+  const TzLayout lay = tz_layout(Hkv, N);
+  char* base = static_cast<char*>(index);
   KVS_CUDA_TRY(launch_k(trizone_index_kernel, dim3(static_cast<unsigned>(Hkv)), dim3(1024), 0, as_stream(stream), 0,
                         to_ptrs(k_streams, true), to_ptrs(v_streams, true), bits_v, static_cast<int>(N),
-                        static_cast<int>(d), hdr, vloc));
+                        static_cast<int>(d), reinterpret_cast<long long*>(base),
+                        reinterpret_cast<int*>(base + lay.vstart), reinterpret_cast<uint8_t*>(base + lay.vslot)));
   KVS_CUDA_TRY(cudaGetLastError());
   return KVS_OK;
 }
 
+// partial records the decode may write: one per (query head, CTA column)
+static long long tz_slot_cap(int64_t N, int64_t nc_cap) { return cdiv(N, 64) + cdiv(nc_cap, kTzChunkC); }
+
 size_t kvs_trizone_workspace_size(int64_t Hq, int64_t Hkv, int64_t N, int64_t d, int64_t nc_cap) {
   if (Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || nc_cap < 0) return 0;
-  const long long slots = cdiv(N, kTzChunk) + cdiv(nc_cap, kTzChunk);
-  return static_cast<size_t>(2 * cdiv(Hq * slots * 4, 256) * 256 + cdiv(Hq * slots * d * 4, 256) * 256);
+  const long long rec = Hq * tz_slot_cap(N, nc_cap);
+  return static_cast<size_t>(2 * cdiv(rec * 4, 256) * 256 + cdiv(rec * d * 4, 256) * 256);
 }
 
 int kvs_trizone_decode(const uint16_t* q, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
@@ -638,7 +640,9 @@ int kvs_trizone_decode(const uint16_t* q, int64_t Hq, int64_t Hkv, int64_t N, in
   if (d != kTzD || !(G == 1 || G == 2 || G % 4 == 0) || Hkv * N >= (1ll << 31) || nc_cap >= (1ll << 30))
     return KVS_ERR_UNSUPPORTED;
   for (int i = 0; i < 4; ++i)
-    if (!aligned16(k_streams->codes[i]) || !aligned16(v_streams->codes[i])) return KVS_ERR_INVALID_ARG;
+    if (!aligned16(k_streams->codes[i]) || !aligned16(v_streams->codes[i]) ||
+        (reinterpret_cast<uintptr_t>(v_streams->scales[i]) & 3u))
+      return KVS_ERR_INVALID_ARG;
   if (!aligned16(q) || (nc_cap > 0 && (!aligned16(k_new) || !aligned16(v_new)))) return KVS_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(index) & 255u)) return KVS_ERR_WORKSPACE;
   const size_t need = kvs_trizone_workspace_size(Hq, Hkv, N, d, nc_cap);
@@ -647,31 +651,33 @@ int kvs_trizone_decode(const uint16_t* q, int64_t Hq, int64_t Hkv, int64_t N, in
   const int HG = G >= 4 ? 4 : static_cast<int>(G);
   const long long Z = G / HG;
   // flash-decoding split: about two CTAs per SM over the (KV head, head slice) pairs
-  const long long per_pair = std::max<long long>(1, 2LL * sm_count() / (Hkv * Z));
-  const int n_split = static_cast<int>(std::min<long long>(cdiv(N, kTzChunk), per_pair));
-  const int n_csplit = static_cast<int>(std::min<long long>(cdiv(nc_cap, kTzChunk), per_pair));
+  const long long per_pair = std::min<long long>(512, std::max<long long>(1, 2LL * sm_count() / (Hkv * Z)));
+  const int n_split = static_cast<int>(std::min<long long>(cdiv(N, 64), per_pair));
+  const int n_csplit = static_cast<int>(std::min<long long>(cdiv(nc_cap, kTzChunkC), per_pair));
   const int slots = n_split + n_csplit;
-  const long long rec_cap = Hq * (cdiv(N, kTzChunk) + cdiv(nc_cap, kTzChunk));   // layout of the workspace size
+  const long long rec_cap = Hq * tz_slot_cap(N, nc_cap);   // the layout of the workspace size
   float* pm = static_cast<float*>(workspace);
   float* pl = reinterpret_cast<float*>(static_cast<char*>(workspace) + cdiv(rec_cap * 4, 256) * 256);
   float* po = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * cdiv(rec_cap * 4, 256) * 256);
-  const long long* hdr = static_cast<const long long*>(index);
-  const uint32_t* vloc =
-      reinterpret_cast<const uint32_t*>(static_cast<const char*>(index) + cdiv(Hkv * kTzHdr * 8, 256) * 256);
+  const TzLayout lay = tz_layout(Hkv, N);
+  const char* ib = static_cast<const char*>(index);
+  const long long* hdr = reinterpret_cast<const long long*>(ib);
+  const int* vstart = reinterpret_cast<const int*>(ib + lay.vstart);
+  const uint8_t* vslot = reinterpret_cast<const uint8_t*>(ib + lay.vslot);
   const dim3 grid(static_cast<unsigned>(slots), static_cast<unsigned>(Hkv), static_cast<unsigned>(Z));
   const float qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   const StreamPtrs ks = to_ptrs(k_streams, false), vs = to_ptrs(v_streams, false);
   cudaStream_t st = as_stream(stream);
   const int g_ = static_cast<int>(G), n_ = static_cast<int>(N), ncap = static_cast<int>(nc_cap);
   if (HG == 4)
-    KVS_CUDA_TRY(launch_k(trizone_decode_kernel<4>, grid, dim3(kTzThreads), 0, st, 0, q, g_, n_, ks, vs, hdr, vloc,
-                          k_new, v_new, n_new, ncap, n_split, qscale, pm, pl, po));
+    KVS_CUDA_TRY(launch_k(trizone_decode_kernel<4>, grid, dim3(kTzThreads), 0, st, 0, q, g_, n_, ks, vs, hdr, vstart,
+                          vslot, k_new, v_new, n_new, ncap, n_split, qscale, pm, pl, po));
   else if (HG == 2)
-    KVS_CUDA_TRY(launch_k(trizone_decode_kernel<2>, grid, dim3(kTzThreads), 0, st, 0, q, g_, n_, ks, vs, hdr, vloc,
-                          k_new, v_new, n_new, ncap, n_split, qscale, pm, pl, po));
+    KVS_CUDA_TRY(launch_k(trizone_decode_kernel<2>, grid, dim3(kTzThreads), 0, st, 0, q, g_, n_, ks, vs, hdr, vstart,
+                          vslot, k_new, v_new, n_new, ncap, n_split, qscale, pm, pl, po));
   else
-    KVS_CUDA_TRY(launch_k(trizone_decode_kernel<1>, grid, dim3(kTzThreads), 0, st, 0, q, g_, n_, ks, vs, hdr, vloc,
-                          k_new, v_new, n_new, ncap, n_split, qscale, pm, pl, po));
+    KVS_CUDA_TRY(launch_k(trizone_decode_kernel<1>, grid, dim3(kTzThreads), 0, st, 0, q, g_, n_, ks, vs, hdr, vstart,
+                          vslot, k_new, v_new, n_new, ncap, n_split, qscale, pm, pl, po));
   KVS_CUDA_TRY(launch_k(trizone_combine_kernel, dim3(static_cast<unsigned>(Hq)), dim3(kTzD), 0, st, 0, slots, pm, pl,
                         po, out, lse));
   KVS_CUDA_TRY(cudaGetLastError());

@@ -97,11 +97,12 @@ def test_alloc_and_pack_argument_errors(lib):
 
 
 def test_trizone_sizes_and_argument_errors(lib):
-    # header 8 heads x 16 int64 (1 KiB) + one uint32 per token, each part 256-aligned
-    assert lib.kvs_trizone_index_size(8, 8192) == 1024 + 8 * 8192 * 4
-    # 32 heads x (64 old chunks of 128 tokens + 1 zone C chunk) records: max and sum
-    # (8320 B each, padded to 8448) and 128 output floats
-    assert lib.kvs_trizone_workspace_size(32, 8, 8192, 128, 100) == 2 * 8448 + 32 * 65 * 128 * 4
+    # header 8 heads x 16 int64 (1 KiB); per 64-token group the first V entry of
+    # each width (8 x 129 x 4 int32, padded to 16640 B); one width byte per token
+    assert lib.kvs_trizone_index_size(8, 8192) == 1024 + 16640 + 8 * 8192
+    # 32 heads x (128 groups of 64 tokens + 1 zone C step of 128) records: max and
+    # sum (16512 B each, padded to 16640) and 128 output floats
+    assert lib.kvs_trizone_workspace_size(32, 8, 8192, 128, 100) == 2 * 16640 + 32 * 129 * 128 * 4
     assert lib.kvs_trizone_workspace_size(0, 8, 8192, 128, 0) == 0
     p = ctypes.c_void_p(1 << 20)
     s = L.StreamSetC()
