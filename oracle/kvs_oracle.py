@@ -468,3 +468,71 @@ def trizone_decode(q, K_hat, V_hat, keep, k_new=None, v_new=None):
         lse[hd] = m + math.log(z)
         out[hd] = (e @ Vv) / z
     return out, lse
+
+
+# ----------------------------------------------------------------------------
+# O8. KV-CoRE: covariance (Gram) accumulation, spectrum, NER, low-rank error
+# ----------------------------------------------------------------------------
+def gram(X, keep=None):
+    """G[g] = sum_t x_t x_t^T over the tokens t of KV head g (the kept ones when
+    keep is given), in float64.   [KV-CoRE §2: the covariance updated token by
+    token, from which the singular values and right singular vectors follow]
+    X [Hkv, N, d]; keep [Hkv, N] or None.  Returns [Hkv, d, d].
+    Pins: a sum over two token blocks equals the sum over all; the trace is the
+    squared Frobenius norm; orthogonal columns give a diagonal of their squared
+    norms; the eigenvalues are the squared singular values of X (SVD).
+    """
+    X = np.asarray(X, dtype=np.float64)
+    Hkv, N, d = X.shape
+    G = np.zeros((Hkv, d, d))
+    for g in range(Hkv):
+        rows = X[g] if keep is None else X[g, np.asarray(keep, bool)[g]]
+        for x in rows:                                  # token by token, as the page describes
+            G[g] += np.outer(x, x)
+    return G
+
+
+def spectrum(G):
+    """Singular values of X from its Gram matrix: sigma_i = sqrt(max(lambda_i, 0))
+    for the eigenvalues lambda_i of G, in descending order.   [KV-CoRE §2]
+    The eigenvalues come from LAPACK's symmetric solver (a library primitive)."""
+    G = np.asarray(G, dtype=np.float64)
+    lam = np.linalg.eigvalsh(G)[..., ::-1]
+    return np.sqrt(np.maximum(lam, 0.0))
+
+
+def numerical_rank(sigma, rtol):
+    """Number of singular values above rtol * sigma_max (0 for an all-zero spectrum)."""
+    sigma = np.asarray(sigma, dtype=np.float64)
+    if sigma.size == 0 or sigma.max() <= 0:
+        return 0
+    return int((sigma > rtol * sigma.max()).sum())
+
+
+def ner(sigma, rtol=1e-3):
+    """Normalised effective rank   [KV-CoRE §2, NER].
+
+    The page defines NER as the effective rank, computed from the distribution
+    of the singular values, divided by the actual rank r, so 1/r <= NER <= 1;
+    it prints no formula.  Reading taken: the entropy effective rank over the
+    r singular values above rtol * sigma_max,
+        p_i = sigma_i / sum_{j<=r} sigma_j,   erank = exp(-sum_i p_i ln p_i),
+        NER = erank / r.
+    An all-zero spectrum gives 0.  Pins: equal singular values give 1; one
+    dominant value gives 1/r in the limit; the bounds hold on random spectra.
+    """
+    sigma = np.sort(np.asarray(sigma, dtype=np.float64))[::-1]
+    r = numerical_rank(sigma, rtol)
+    if r == 0:
+        return 0.0
+    s = sigma[:r]
+    p = s / s.sum()
+    H = -float(np.sum(p * np.log(p)))
+    return math.exp(H) / r
+
+
+def lowrank_error(sigma, r):
+    """Squared Frobenius error of the best rank-r approximation of X:
+    sum_{i>r} sigma_i^2.   [KV-CoRE §2, Eckart-Young-Mirsky]"""
+    sigma = np.sort(np.asarray(sigma, dtype=np.float64))[::-1]
+    return float(np.sum(sigma[r:] ** 2))

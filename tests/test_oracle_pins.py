@@ -470,3 +470,56 @@ def test_channels_over_no_kept_token_have_no_groups():
         assert st[wd]["n_groups"] == 0 and st[wd]["codes"].size == 0
         assert st[wd]["ids"].size == 32 and (st[wd]["group_offsets"] == 0).all()
     assert not O.dequantize(st, X.shape, 1, bits, keep).any()
+
+
+# ----------------------------------------------------------------------------
+# KV-CoRE: Gram accumulation, spectrum, NER, Eckart-Young error   [KV-CoRE §2]
+# ----------------------------------------------------------------------------
+def test_gram_blocks_trace_and_svd():
+    rng = np.random.default_rng(31)
+    X = rng.standard_normal((2, 40, 6)) * np.array([3, 1, 0.5, 0.1, 2, 1])
+    keep = rng.random((2, 40)) > 0.3
+    G = O.gram(X)
+    np.testing.assert_allclose(O.gram(X[:, :17]) + O.gram(X[:, 17:]), G, rtol=1e-12, atol=1e-12)  # token blocks
+    for g in range(2):
+        assert abs(np.trace(G[g]) - (X[g] ** 2).sum()) < 1e-9                      # trace = |X|_F^2
+        sv = np.linalg.svd(X[g], compute_uv=False)                                  # a different decomposition
+        np.testing.assert_allclose(O.spectrum(G)[g], sv, rtol=1e-9, atol=1e-9)
+        Gk = O.gram(X, keep)[g]
+        np.testing.assert_allclose(Gk, X[g, keep[g]].T @ X[g, keep[g]], rtol=1e-12, atol=1e-12)
+
+
+def test_gram_orthogonal_columns():
+    """X = U diag(s) with orthonormal columns U: G = diag(s^2), sigma = s sorted."""
+    rng = np.random.default_rng(32)
+    U, _ = np.linalg.qr(rng.standard_normal((50, 5)))
+    s = np.array([4.0, 0.5, 2.0, 1.0, 3.0])
+    G = O.gram((U * s)[None])[0]
+    np.testing.assert_allclose(G, np.diag(s ** 2), atol=1e-12)
+    np.testing.assert_allclose(O.spectrum(G), np.sort(s)[::-1], rtol=1e-12)
+
+
+def test_ner_closed_forms_and_bounds():
+    assert O.ner([3.0] * 7) == pytest.approx(1.0, abs=1e-15)                       # equal values: erank = r
+    # sigma = (2, 1, 1): p = (1/2, 1/4, 1/4), H = (1/2)ln2 + (1/2)ln4 = (3/2)ln2,
+    # erank = 2^(3/2), NER = 2^(3/2) / 3 (worked by hand)
+    assert O.ner([2.0, 1.0, 1.0]) == pytest.approx(2 ** 1.5 / 3, rel=1e-14)
+    eps = 2e-3                                                                      # just above rtol = 1e-3
+    assert 1 / 5 <= O.ner([1.0] + [eps] * 4) < 1 / 5 * 1.2                         # one dominant value -> 1/r
+    assert O.ner([1.0, 1e-6, 1e-6]) == 1.0                                          # below rtol: rank 1
+    assert O.ner([0.0, 0.0]) == 0.0
+    rng = np.random.default_rng(33)
+    for _ in range(50):
+        s = rng.random(16) ** 4
+        r = O.numerical_rank(s, 1e-3)
+        assert 1 / r - 1e-12 <= O.ner(s) <= 1 + 1e-12
+
+
+def test_lowrank_error_is_eckart_young():
+    rng = np.random.default_rng(34)
+    X = rng.standard_normal((30, 8)) @ np.diag([5, 4, 3, 2, 1, 0.5, 0.2, 0.1])
+    sig = O.spectrum(O.gram(X[None]))[0]
+    U, S, Vt = np.linalg.svd(X, full_matrices=False)
+    for r in (0, 1, 3, 8):
+        Xr = (U[:, :r] * S[:r]) @ Vt[:r]
+        assert O.lowrank_error(sig, r) == pytest.approx(((X - Xr) ** 2).sum(), rel=1e-9, abs=1e-9)
