@@ -784,44 +784,57 @@ __global__ void __launch_bounds__(kTzThreads, 2) trizone_decode_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// combine: one CTA of 128 threads per query head; merges the partials in
-// order, skipping the empty ones (max = -inf)
+// combine: one CTA of 1024 threads per query head; thread (r, c) adds the
+// partials r, r + 8, ... of channel c, then the 8 sums are added in order.
+// Empty partials (max = -inf) get weight 0; their outputs are written as 0.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kTzD) trizone_combine_kernel(int slots, const float* __restrict__ pm,
-                                                               const float* __restrict__ pl,
-                                                               const float* __restrict__ po, float* __restrict__ out,
-                                                               float* __restrict__ lse) {
+constexpr int kTzCombineThreads = 8 * kTzD;
+
+__global__ void __launch_bounds__(kTzCombineThreads) trizone_combine_kernel(int slots, const float* __restrict__ pm,
+                                                                            const float* __restrict__ pl,
+                                                                            const float* __restrict__ po,
+                                                                            float* __restrict__ out,
+                                                                            float* __restrict__ lse) {
   pdl_wait();
-  __shared__ float s_f[1024], s_red[8];
-  const int hd = blockIdx.x, c = threadIdx.x, lane = c & 31, warp = c >> 5;
+  __shared__ float s_f[1024], s_o[8][kTzD], s_red[32], s_M;
+  const int hd = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long r0 = static_cast<long long>(hd) * slots;
   const int n = slots < 1024 ? slots : 1024;        // the host keeps slots <= 1024
-  float M = -INFINITY;
-  for (int x = c; x < n; x += kTzD) M = fmaxf(M, pm[r0 + x]);
+  float m = tid < n ? pm[r0 + tid] : -INFINITY;
+  float M = m;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   if (lane == 0) s_red[warp] = M;
   __syncthreads();
-  M = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
-  float L = 0.f;
-  for (int x = c; x < n; x += kTzD) {
-    const float m = pm[r0 + x];
-    const float f = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
-    s_f[x] = f;
-    L = fmaf(pl[r0 + x], f, L);
+  if (tid == 0) {
+    float x = s_red[0];
+    for (int w = 1; w < 32; ++w) x = fmaxf(x, s_red[w]);
+    s_M = x;
   }
+  __syncthreads();
+  M = s_M;
+  const float f = (tid < n && M != -INFINITY && m != -INFINITY) ? exp2f(m - M) : 0.f;
+  if (tid < n) s_f[tid] = f;
+  float L = tid < n ? pl[r0 + tid] * f : 0.f;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   __syncthreads();
-  if (lane == 0) s_red[4 + warp] = L;
+  if (lane == 0) s_red[warp] = L;
   __syncthreads();
-  L = (s_red[4] + s_red[5]) + (s_red[6] + s_red[7]);
-  // every partial's output is written (zeros when empty), so the loads need no test
+  const int c = tid & (kTzD - 1), r = tid >> 7;
   float O = 0.f;
-#pragma unroll 8
-  for (int x = 0; x < n; ++x) O = fmaf(po[(r0 + x) * kTzD + c], s_f[x], O);
-  out[static_cast<long long>(hd) * kTzD + c] = L > 0.f ? O / L : 0.f;
-  if (c == 0) lse[hd] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+  for (int x = r; x < n; x += 8) O = fmaf(po[(r0 + x) * kTzD + c], s_f[x], O);
+  s_o[r][c] = O;
+  __syncthreads();
+  if (tid < kTzD) {
+    float Ls = 0.f;
+    for (int w = 0; w < 32; ++w) Ls += s_red[w];
+    float Os = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) Os += s_o[k][tid];
+    out[static_cast<long long>(hd) * kTzD + tid] = Ls > 0.f ? Os / Ls : 0.f;
+    if (tid == 0) lse[hd] = Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+  }
 }
 
 }  // namespace kvs

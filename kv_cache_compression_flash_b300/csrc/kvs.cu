@@ -678,8 +678,8 @@ int kvs_trizone_decode(const uint16_t* q, int64_t Hq, int64_t Hkv, int64_t N, in
   else
     KVS_CUDA_TRY(launch_k(trizone_decode_kernel<1>, grid, dim3(kTzThreads), 0, st, 0, q, g_, n_, ks, vs, hdr, vstart,
                           vslot, k_new, v_new, n_new, ncap, n_split, qscale, pm, pl, po));
-  KVS_CUDA_TRY(launch_k(trizone_combine_kernel, dim3(static_cast<unsigned>(Hq)), dim3(kTzD), 0, st, 0, slots, pm, pl,
-                        po, out, lse));
+  KVS_CUDA_TRY(launch_k(trizone_combine_kernel, dim3(static_cast<unsigned>(Hq)), dim3(kTzCombineThreads), 0, st, 0,
+                        slots, pm, pl, po, out, lse));
   KVS_CUDA_TRY(cudaGetLastError());
   return KVS_OK;
 }
