@@ -288,6 +288,39 @@ int kvs_trizone_decode(const uint16_t* q, int64_t Hq, int64_t Hkv, int64_t N, in
                        const uint16_t* k_new, const uint16_t* v_new, const int32_t* n_new, int64_t nc_cap,
                        float* out, float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- KV-CoRE: Gram accumulation, spectrum and NER ------------------------ */
+/* The covariance of a cache, updated over its tokens, and the singular values
+ * it yields   [KV-CoRE §2: incremental covariance -> singular values and right
+ * singular vectors; Eckart-Young-Mirsky; NER].
+ *
+ * kvs_gram:  G[g] (+)= sum_t x_t x_t^T over the tokens t of KV head g
+ *     X        : bf16 [Hkv, N, d], d = 128, 16-byte aligned (a whole cache, or
+ *                one block of new tokens when accumulating)
+ *     keep_bits: uint8 [Hkv, N] or NULL; a token with keep_bits[t] == 0 is left
+ *                out (pass bits_V to take the RDKV kept set)
+ *     accumulate: 0 writes G, nonzero adds to it (token-block by token-block
+ *                accumulation; the sum over blocks equals the sum over all)
+ *     G        : float [Hkv, d, d], 16-byte aligned.  bf16 products are exact
+ *                in fp32; the sums are fp32 (tensor cores), adding the token
+ *                ranges' partial sums in a fixed order (deterministic).
+ *     workspace: kvs_gram_workspace_size(Hkv, N, d) bytes, 16-byte aligned.
+ *
+ * kvs_spectrum: per KV head, from G[g] (symmetrised):
+ *     sigma[g, i] = sqrt(max(lambda_i, 0)) in descending order (fp32 cyclic
+ *                   Jacobi, run until the off-diagonal norm is below
+ *                   1e-5 |G|_F or stops shrinking, at most 24 sweeps),
+ *     rank[g]     = #{i : sigma_i > rtol * sigma_max}, 0 <= rtol < 1,
+ *     ner[g]      = exp(-sum_{i<rank} p_i ln p_i) / rank with
+ *                   p_i = sigma_i / sum_{j<rank} sigma_j   (the normalised
+ *                   effective rank, 1/rank <= ner <= 1; 0 for G = 0).
+ * The page gives no NER formula: this is the entropy effective rank over the
+ * numerical rank. */
+size_t kvs_gram_workspace_size(int64_t Hkv, int64_t N, int64_t d);
+int kvs_gram(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, const uint8_t* keep_bits, int accumulate,
+             float* G, void* workspace, size_t workspace_bytes, void* stream);
+int kvs_spectrum(const float* G, int64_t Hkv, int64_t d, float rtol, float* sigma, float* ner, int32_t* rank,
+                 void* stream);
+
 #ifdef __cplusplus
 }
 #endif

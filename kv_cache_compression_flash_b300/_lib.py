@@ -60,6 +60,9 @@ SIGNATURES = {
     "kvs_trizone_workspace_size": (c_size_t, [c_int64] * 5),
     "kvs_trizone_decode": (c_int, [c_void_p] + [c_int64] * 4 + [c_void_p] * 6 + [c_int64] + [c_void_p] * 3
                            + [c_size_t, c_void_p]),
+    "kvs_gram_workspace_size": (c_size_t, [c_int64] * 3),
+    "kvs_gram": (c_int, [c_void_p] + [c_int64] * 3 + [c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "kvs_spectrum": (c_int, [c_void_p, c_int64, c_int64, ctypes.c_float, c_void_p, c_void_p, c_void_p, c_void_p]),
 }
 
 
@@ -333,3 +336,28 @@ def trizone_decode(q, k_streams: Streams, v_streams: Streams, index, k_new=None,
                                 _ptr(index), _ptr(k_new), _ptr(v_new), _ptr(n_new), nc_cap, _ptr(o), _ptr(ls),
                                 _ptr(buf), buf.numel(), _stream(stream)), "kvs_trizone_decode")
     return o, ls
+
+
+def gram(X, keep_bits=None, *, out=None, accumulate=False, ws=None, stream=None):
+    """G [Hkv, d, d] float32: sum over tokens of x x^T per KV head (added to `out` when accumulate)."""
+    _bf16(X, "X")
+    Hkv, N, d = X.shape
+    L = lib()
+    G = out if out is not None else torch.zeros(Hkv, d, d, dtype=torch.float32, device=X.device)
+    buf = _ws(ws, "gram", L.kvs_gram_workspace_size(Hkv, N, d), X.device)
+    _check(L.kvs_gram(_ptr(X), Hkv, N, d, _ptr(keep_bits), 1 if accumulate else 0, _ptr(G), _ptr(buf), buf.numel(),
+                      _stream(stream)), "kvs_gram")
+    return G
+
+
+def spectrum(G, rtol=1e-3, *, stream=None):
+    """(sigma [Hkv, d] descending, ner [Hkv], rank [Hkv] int32) of the Gram matrices G [Hkv, d, d]."""
+    if G.dtype != torch.float32 or not G.is_cuda or not G.is_contiguous() or G.dim() != 3:
+        raise KvsError("G must be a contiguous float32 CUDA tensor [Hkv, d, d]")
+    Hkv, d, _ = G.shape
+    sigma = torch.empty(Hkv, d, dtype=torch.float32, device=G.device)
+    ner = torch.empty(Hkv, dtype=torch.float32, device=G.device)
+    rank = torch.empty(Hkv, dtype=torch.int32, device=G.device)
+    _check(lib().kvs_spectrum(_ptr(G), Hkv, d, float(rtol), _ptr(sigma), _ptr(ner), _ptr(rank), _stream(stream)),
+           "kvs_spectrum")
+    return sigma, ner, rank

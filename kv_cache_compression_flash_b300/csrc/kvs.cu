@@ -14,6 +14,7 @@
 #include "pack.cuh"
 #include "score.cuh"
 #include "decode.cuh"
+#include "core.cuh"
 
 using namespace kvs;
 
@@ -680,6 +681,49 @@ int kvs_trizone_decode(const uint16_t* q, int64_t Hq, int64_t Hkv, int64_t N, in
                           vslot, k_new, v_new, n_new, ncap, n_split, qscale, pm, pl, po));
   KVS_CUDA_TRY(launch_k(trizone_combine_kernel, dim3(static_cast<unsigned>(Hq)), dim3(kTzCombineThreads), 0, st, 0,
                         slots, pm, pl, po, out, lse));
+  KVS_CUDA_TRY(cudaGetLastError());
+  return KVS_OK;
+}
+
+// ---- KV-CoRE: Gram accumulation and spectrum --------------------------------
+static int gram_split(int64_t Hkv, int64_t N) {
+  return static_cast<int>(std::max<long long>(1, std::min<long long>(cdiv(N, kGramTile), 2LL * sm_count() / Hkv)));
+}
+
+size_t kvs_gram_workspace_size(int64_t Hkv, int64_t N, int64_t d) {
+  if (Hkv <= 0 || N <= 0 || d != kGramD) return 0;
+  return static_cast<size_t>(gram_split(Hkv, N)) * Hkv * kGramD * kGramD * 4;
+}
+
+int kvs_gram(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, const uint8_t* keep_bits, int accumulate,
+             float* G, void* workspace, size_t workspace_bytes, void* stream) {
+  if (Hkv <= 0 || N <= 0 || d <= 0 || !X || !G) return KVS_ERR_INVALID_ARG;
+  if (d != kGramD || Hkv * N >= (1ll << 31)) return KVS_ERR_UNSUPPORTED;
+  if (!aligned16(X) || !aligned16(G)) return KVS_ERR_INVALID_ARG;
+  const size_t need = kvs_gram_workspace_size(Hkv, N, d);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return KVS_ERR_WORKSPACE;
+  const int ns = gram_split(Hkv, N);
+  const int per = static_cast<int>(cdiv(cdiv(N, kGramTile), ns) * kGramTile);
+  cudaStream_t st = as_stream(stream);
+  KVS_CUDA_TRY(allow_smem(gram_partial_kernel, kGramSmem));
+  float* part = static_cast<float*>(workspace);
+  KVS_CUDA_TRY(launch_k(gram_partial_kernel, dim3(static_cast<unsigned>(ns), static_cast<unsigned>(Hkv)),
+                        dim3(kGramThreads), kGramSmem, st, 0, X, static_cast<int>(N), keep_bits, per, part));
+  const long long per_split = Hkv * kGramD * kGramD;
+  KVS_CUDA_TRY(launch_k(gram_reduce_kernel, dim3(static_cast<unsigned>(cdiv(per_split, 256))), dim3(256), 0, st, 0,
+                        static_cast<const float*>(part), ns, per_split, accumulate ? 1 : 0, G));
+  KVS_CUDA_TRY(cudaGetLastError());
+  return KVS_OK;
+}
+
+int kvs_spectrum(const float* G, int64_t Hkv, int64_t d, float rtol, float* sigma, float* ner, int32_t* rank,
+                 void* stream) {
+  if (Hkv <= 0 || d <= 0 || !G || !sigma || !ner || !rank || !(rtol >= 0.f) || !(rtol < 1.f))
+    return KVS_ERR_INVALID_ARG;
+  if (d != kGramD) return KVS_ERR_UNSUPPORTED;
+  KVS_CUDA_TRY(allow_smem(spectrum_kernel, kSpecSmem));
+  KVS_CUDA_TRY(launch_k(spectrum_kernel, dim3(static_cast<unsigned>(Hkv)), dim3(kSpecThreads), kSpecSmem,
+                        as_stream(stream), 0, G, rtol, sigma, ner, rank));
   KVS_CUDA_TRY(cudaGetLastError());
   return KVS_OK;
 }

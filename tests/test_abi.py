@@ -127,3 +127,14 @@ def test_trizone_sizes_and_argument_errors(lib):
     bad[15] = 16                                                        # workspace too small
     assert dec(*bad) == 6
     assert lib.kvs_trizone_index(ctypes.byref(s), ctypes.byref(s), p, 8, 8192, 128, p, 1 << 30, None) == 1  # no counts
+
+
+def test_core_sizes_and_argument_errors(lib):
+    assert lib.kvs_gram_workspace_size(8, 8192, 64) == 0                # d = 128 only
+    assert lib.kvs_gram_workspace_size(8, 100, 128) == 1 * 8 * 128 * 128 * 4   # one 128-token range per head
+    p = ctypes.c_void_p(1 << 20)
+    assert lib.kvs_gram(None, 8, 100, 128, None, 0, p, p, 1 << 30, None) == 1
+    assert lib.kvs_gram(p, 8, 100, 64, None, 0, p, p, 1 << 30, None) == 2
+    assert lib.kvs_gram(p, 8, 100, 128, None, 0, p, p, 16, None) == 6
+    assert lib.kvs_spectrum(p, 8, 128, ctypes.c_float(1.5), p, p, p, None) == 1  # rtol outside [0, 1)
+    assert lib.kvs_spectrum(p, 8, 64, ctypes.c_float(1e-3), p, p, p, None) == 2
