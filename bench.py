@@ -46,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--soak-s", type=float, default=1.0, help="untimed replays before timing (clock samples)")
     ap.add_argument("--trizone", action="store_true",
                     help="time one TriZone decode step over the workload's compressed pool instead")
+    ap.add_argument("--core", action="store_true",
+                    help="time the KV-CoRE Gram accumulation and spectrum of the workload's K cache instead")
     return ap.parse_args(argv)
 
 
@@ -488,12 +490,63 @@ def run_trizone(args):
     return 0
 
 
+def run_core(args):
+    """KV-CoRE over the workload's K cache: kvs_gram (all tokens of every KV
+    head) and kvs_spectrum, each timed with events, L2 flushed before each."""
+    import torch
+    from kv_cache_compression_flash_b300 import _lib as L
+    from kv_cache_compression_flash_b300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    dev = torch.device("cuda", 0)
+    K = synth.make_layer(wl)["K"].to(dev)
+    G = torch.empty(wl.Hkv, wl.d, wl.d, dtype=torch.float32, device=dev)
+    ws = L.Workspace()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        L.gram(K, out=G, ws=ws)
+        L.spectrum(G)
+    torch.cuda.synchronize()
+    tg, ts = [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record()
+        L.gram(K, out=G, ws=ws)
+        e1.record()
+        sigma, ner, rank = L.spectrum(G)
+        e2.record()
+        torch.cuda.synchronize()
+        tg.append(e0.elapsed_time(e1) * 1e3)
+        ts.append(e1.elapsed_time(e2) * 1e3)
+    if L.device_error() != 0:
+        raise SystemExit("device error")
+    gram_us = statistics.median(tg)
+    byts = K.numel() * 2
+    flops = 2.0 * wl.Hkv * wl.N * wl.d * wl.d
+    peak_tf, peak_gbs, peak_kind = measured_peaks()
+    print(json.dumps({
+        "metric": "KV-CoRE Gram accumulation over the K cache (all KV heads)", "value": gram_us, "unit": "us",
+        "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",
+        "data": "synthetic", "config": {"workload": wl.name, "Hkv": wl.Hkv, "N": wl.N, "d": wl.d,
+                                        "l2": "flushed before each step (untimed)"},
+        "roofline": {"bound": "hbm", "achieved": byts / (gram_us * 1e-6) / 1e9, "peak": peak_gbs, "unit": "GB/s",
+                     "frac": byts / (gram_us * 1e-6) / 1e9 / peak_gbs if peak_gbs else None,
+                     "peak_kind": f"{peak_kind} copy", "algorithmic_bytes": byts,
+                     "tensor_tflops": flops / (gram_us * 1e-6) / 1e12},
+        "spectrum_us": statistics.median(ts), "ner": [round(float(x), 4) for x in ner.cpu()],
+        "rank": [int(x) for x in rank.cpu()], "gpu_launches": 3 * args.steps,
+    }))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
     if args.trizone:
         return run_trizone(args)
+    if args.core:
+        return run_core(args)
     return run_ours(args)
 
 
