@@ -536,3 +536,32 @@ def lowrank_error(sigma, r):
     sum_{i>r} sigma_i^2.   [KV-CoRE §2, Eckart-Young-Mirsky]"""
     sigma = np.sort(np.asarray(sigma, dtype=np.float64))[::-1]
     return float(np.sum(sigma[r:] ** 2))
+
+
+# ----------------------------------------------------------------------------
+# O9. block LSE (the compression zone's attention mass)
+# ----------------------------------------------------------------------------
+def block_lse(Q, K, q_pos0, n_block):
+    """lse[hd, r] = ln sum_{t < n_block, t <= p_r} exp(q_r . k_t / sqrt(d)),
+    p_r = q_pos0 + r.   [KVSculpt §2: the LSE term matches the attention mass
+    of the compressed block, the leading zone of the cache]
+    Q [Hq, W, d]; K [Hkv, N, d] with 1 <= n_block <= N.  Returns [Hq, W].
+    Pins: one key gives its logit; equal keys give logit + ln(count); the
+    block LSE and a brute-force sum over the rest of the visible keys add up
+    to the full row LSE.
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    Hq, W, d = Q.shape
+    Hkv = K.shape[0]
+    G = Hq // Hkv
+    out = np.empty((Hq, W))
+    t = np.arange(n_block)
+    for hd in range(Hq):
+        Kb = K[hd // G, :n_block]
+        for r in range(W):
+            s = Kb @ Q[hd, r] / math.sqrt(d)
+            s = s[t <= q_pos0 + r]
+            m = s.max()
+            out[hd, r] = m + math.log(np.exp(s - m).sum())
+    return out

@@ -523,3 +523,40 @@ def test_lowrank_error_is_eckart_young():
     for r in (0, 1, 3, 8):
         Xr = (U[:, :r] * S[:r]) @ Vt[:r]
         assert O.lowrank_error(sig, r) == pytest.approx(((X - Xr) ** 2).sum(), rel=1e-9, abs=1e-9)
+
+
+# ----------------------------------------------------------------------------
+# block LSE   [KVSculpt §2]
+# ----------------------------------------------------------------------------
+def test_block_lse_closed_forms():
+    rng = np.random.default_rng(41)
+    Q = rng.standard_normal((4, 6, 8))
+    K = rng.standard_normal((2, 20, 8))
+    got = O.block_lse(Q, K, 14, 1)                                   # one key: its logit
+    for hd in range(4):
+        np.testing.assert_allclose(got[hd], Q[hd] @ K[hd // 2, 0] / math.sqrt(8), rtol=1e-13)
+    Kc = np.repeat(K[:, :1], 20, axis=1)                              # equal keys: logit + ln(count)
+    for q0, nb in ((14, 9), (3, 12), (0, 20)):
+        got = O.block_lse(Q, Kc, q0, nb)
+        for hd in range(4):
+            cnt = np.minimum(nb, q0 + np.arange(6) + 1)
+            np.testing.assert_allclose(got[hd], Q[hd] @ Kc[hd // 2, 0] / math.sqrt(8) + np.log(cnt), rtol=1e-13)
+
+
+def test_block_lse_plus_rest_is_row_lse():
+    """exp(block LSE) + the brute-force sum over the visible keys after the block
+    = exp(row LSE over the whole prefix)."""
+    rng = np.random.default_rng(42)
+    Q = rng.standard_normal((2, 5, 4))
+    K = rng.standard_normal((1, 11, 4))
+    q0, nb = 6, 7
+    blk = O.block_lse(Q, K, q0, nb)
+    for hd in range(2):
+        for r in range(5):
+            rest = 0.0
+            for t in range(nb, q0 + r + 1):                              # pure-Python sum
+                rest += math.exp(sum(Q[hd, r, i] * K[0, t, i] for i in range(4)) / 2.0)
+            full = 0.0
+            for t in range(0, q0 + r + 1):
+                full += math.exp(sum(Q[hd, r, i] * K[0, t, i] for i in range(4)) / 2.0)
+            assert math.exp(blk[hd, r]) + rest == pytest.approx(full, rel=1e-12)
