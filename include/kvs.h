@@ -109,6 +109,22 @@ int kvs_score_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
 int kvs_score_plan_info(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t D,
                         int64_t q_pos0, uint32_t mode, int64_t* info);
 
+/* ---- block LSE ------------------------------------------------------------ */
+/* The row log-sum-exp over a leading block of keys   [KVSculpt §2: the LSE
+ * term of the loss matches the attention mass of the compressed block, the
+ * zone [0, N - m) of a cache whose last m tokens are retained]:
+ *     lse[hd, r] = ln sum_{t < n_block, t <= q_pos0 + r} exp(s_{r,t})
+ * with the keys K[g, 0 .. n_block) of the [Hkv, N, d] cache (each head's rows
+ * stay at their place: no copy of the block is needed).  Queries at or after
+ * n_block see the whole block.  1 <= n_block <= N; other arguments, layouts
+ * and errors as kvs_score_attention with KVS_MODE_LSE (whose result this is
+ * for n_block = N). */
+size_t kvs_block_lse_workspace_size(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t q_pos0,
+                                    int64_t n_block);
+int kvs_block_lse(const uint16_t* Q, const uint16_t* K, int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d,
+                  int64_t q_pos0, int64_t n_block, float* lse, void* workspace, size_t workspace_bytes,
+                  void* stream);
+
 /* Channel distortion weights  w_c[g, c] = |Q_{:,c}| |K_{:,c}| / sqrt(d)   [RDKV §2.1, w_c]
  * The query column stacks the G heads' W window rows of group g; the key
  * column spans all N tokens of KV head g.  w_c: float [Hkv, d]. */

@@ -60,6 +60,8 @@ SIGNATURES = {
     "kvs_trizone_workspace_size": (c_size_t, [c_int64] * 5),
     "kvs_trizone_decode": (c_int, [c_void_p] + [c_int64] * 4 + [c_void_p] * 6 + [c_int64] + [c_void_p] * 3
                            + [c_size_t, c_void_p]),
+    "kvs_block_lse_workspace_size": (c_size_t, [c_int64] * 7),
+    "kvs_block_lse": (c_int, [c_void_p, c_void_p] + [c_int64] * 7 + [c_void_p, c_void_p, c_size_t, c_void_p]),
     "kvs_gram_workspace_size": (c_size_t, [c_int64] * 3),
     "kvs_gram": (c_int, [c_void_p] + [c_int64] * 3 + [c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
     "kvs_spectrum": (c_int, [c_void_p, c_int64, c_int64, ctypes.c_float, c_void_p, c_void_p, c_void_p, c_void_p]),
@@ -361,3 +363,20 @@ def spectrum(G, rtol=1e-3, *, stream=None):
     _check(lib().kvs_spectrum(_ptr(G), Hkv, d, float(rtol), _ptr(sigma), _ptr(ner), _ptr(rank), _stream(stream)),
            "kvs_spectrum")
     return sigma, ner, rank
+
+
+def block_lse(Q, K, n_block, *, q_pos0=None, out=None, ws=None, stream=None):
+    """Row LSE over keys [0, n_block) of each KV head: float [Hq, W]."""
+    _bf16(Q, "Q")
+    _bf16(K, "K")
+    Hq, W, d = Q.shape
+    Hkv, N, _ = K.shape
+    if q_pos0 is None:
+        q_pos0 = N - W
+    L = lib()
+    lse = out if out is not None else torch.empty(Hq, W, dtype=torch.float32, device=Q.device)
+    n = L.kvs_block_lse_workspace_size(Hq, Hkv, W, N, d, q_pos0, n_block)
+    buf = _ws(ws, "block_lse", n, Q.device)
+    _check(L.kvs_block_lse(_ptr(Q), _ptr(K), Hq, Hkv, W, N, d, q_pos0, n_block, _ptr(lse), _ptr(buf), buf.numel(),
+                           _stream(stream)), "kvs_block_lse")
+    return lse

@@ -389,6 +389,34 @@ int kvs_score_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
   return KVS_OK;
 }
 
+size_t kvs_block_lse_workspace_size(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t q_pos0,
+                                    int64_t n_block) {
+  ScorePlan pl;
+  if (n_block < 1 || plan_score(Hq, Hkv, W, N, d, 0, q_pos0, KVS_MODE_LSE, &pl, n_block) != KVS_OK) return 0;
+  ScoreWs w;
+  return carve_score(pl, nullptr, 0, &w);
+}
+
+int kvs_block_lse(const uint16_t* Q, const uint16_t* K, int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d,
+                  int64_t q_pos0, int64_t n_block, float* lse, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+  if (n_block < 1) return KVS_ERR_INVALID_ARG;
+  ScorePlan pl;
+  int rc = plan_score(Hq, Hkv, W, N, d, 0, q_pos0, KVS_MODE_LSE, &pl, n_block);
+  if (rc) return rc;
+  if (!Q || !K || !lse) return KVS_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K)) return KVS_ERR_INVALID_ARG;
+  ScoreWs w;
+  if (carve_score(pl, workspace, workspace_bytes, &w) > workspace_bytes || !workspace) return KVS_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KVS_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  rc = d == 64 ? score_dh<64>(pl, Q, K, nullptr, nullptr, nullptr, lse, nullptr, nullptr, w, st)
+               : score_dh<128>(pl, Q, K, nullptr, nullptr, nullptr, lse, nullptr, nullptr, w, st);
+  if (rc) return rc;
+  KVS_CUDA_TRY(cudaGetLastError());
+  return KVS_OK;
+}
+
 size_t kvs_channel_weights_workspace_size(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d) {
   (void)Hq, (void)Hkv, (void)W, (void)N, (void)d;
   return 0;  // one cluster per group reduces in shared memory

@@ -46,6 +46,7 @@ constexpr float kLog2e = 1.44269504088896340736f;
 
 struct ScoreGeom {
   int Hq, Hkv, G, Gt, P, W, N, q_pos0;
+  int pos_cap;  // N - 1: a query at a later position sees every key (a block of keys before the queries)
   int n_hc;   // G / Gt head chunks per group
   int n_pb;   // ceil(W / P) position blocks
   int n_rt;   // Hkv * n_hc * n_pb query-row tiles
@@ -59,7 +60,8 @@ __host__ __device__ inline int ceil_div_i(int a, int b) { return (a + b - 1) / b
 __host__ __device__ inline int pb_pmax(const ScoreGeom& g, int pb) {
   int r1 = (pb + 1) * g.P;
   if (r1 > g.W) r1 = g.W;
-  return g.q_pos0 + r1 - 1;
+  const int p = g.q_pos0 + r1 - 1;
+  return p < g.pos_cap ? p : g.pos_cap;
 }
 __host__ __device__ inline int pb_nkt(const ScoreGeom& g, int pb) { return pb_pmax(g, pb) / 128 + 1; }
 
@@ -296,8 +298,9 @@ __global__ void __launch_bounds__(kScoreThreads1, 1)
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       LseItem x;
       if (!lse_item(geo, kt_chunk, n_split, it, &x)) continue;
-      const int pmin = geo.q_pos0 + (x.pb0 + t) * geo.P;
-      const int pos = pmin + row % geo.P;
+      const int p0 = geo.q_pos0 + (x.pb0 + t) * geo.P;
+      const int pmin = min(p0, geo.pos_cap);
+      const int pos = min(p0 + row % geo.P, geo.pos_cap);
       const bool active = t == 0 || x.two;
       float m = -INFINITY, l = 0.f;
       for (int kt = x.kt0; kt < x.kt1; ++kt, ++kc) {

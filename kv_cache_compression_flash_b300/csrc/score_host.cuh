@@ -25,12 +25,13 @@ EncodeTiledFn encode_fn() {
 
 // 3-D bf16 map over [dim2][dim1][dim0] (dim0 contiguous), 128-byte swizzle,
 // out-of-range elements read as zero.
+// `rows2` is the row count between consecutive dim2 slices (dim1 when dense).
 int make_map_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2, uint32_t box0,
-                uint32_t box1, uint32_t box2) {
+                uint32_t box1, uint32_t box2, uint64_t rows2 = 0) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return KVS_ERR_CUDA;
   const cuuint64_t gdim[3] = {dim0, dim1, dim2};
-  const cuuint64_t gstride[2] = {dim0 * 2, dim0 * dim1 * 2};
+  const cuuint64_t gstride[2] = {dim0 * 2, dim0 * (rows2 ? rows2 : dim1) * 2};
   const cuuint32_t box[3] = {box0, box1, box2};
   const cuuint32_t estride[3] = {1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box,
@@ -49,6 +50,7 @@ struct ScorePlan {
   int qt_chunk, n_split2;
   int gram_slice_len;
   bool want_wt, want_max, want_plus, lse_given;
+  long long k_rows;  // rows of K per KV head in memory (N unless the keys are a leading block)
 };
 
 int validate_shape(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t q_pos0) {
@@ -62,10 +64,15 @@ int validate_shape(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int
   return KVS_OK;
 }
 
+// n_keys > 0: the keys are rows [0, n_keys) of each head of an N-row cache and
+// only the row LSE is computed (queries at or after n_keys see every key).
 int plan_score(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t D, int64_t q_pos0,
-               uint32_t mode, ScorePlan* pl) {
+               uint32_t mode, ScorePlan* pl, int64_t n_keys = 0) {
   int st = validate_shape(Hq, Hkv, W, N, d, q_pos0);
   if (st) return st;
+  if (n_keys < 0 || n_keys > N || (n_keys > 0 && mode != KVS_MODE_LSE)) return KVS_ERR_INVALID_ARG;
+  pl->k_rows = N;
+  if (n_keys > 0) N = n_keys;
   if ((mode & ~(KVS_MODE_LSE | KVS_MODE_RDKV_WT | KVS_MODE_KVZIP | KVS_MODE_KVZIP_PLUS | KVS_MODE_LSE_GIVEN)) != 0)
     return KVS_ERR_INVALID_ARG;
   if ((mode & KVS_MODE_KVZIP) && (mode & KVS_MODE_KVZIP_PLUS)) return KVS_ERR_INVALID_ARG;
@@ -79,6 +86,7 @@ int plan_score(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t
   g.W = static_cast<int>(W);
   g.N = static_cast<int>(N);
   g.q_pos0 = static_cast<int>(q_pos0);
+  g.pos_cap = static_cast<int>(N - 1);
   g.n_hc = g.G / g.Gt;
   g.n_pb = static_cast<int>(cdiv(W, g.P));
   g.n_rt = g.Hkv * g.n_hc * g.n_pb;
@@ -196,7 +204,7 @@ int score_dh(const ScorePlan& pl, const uint16_t* Q, const uint16_t* K, const ui
   CUtensorMap mq, mk;
   int rc = make_map_3d(&mq, Q, DH, g.W, g.Hq, 64, g.P, g.Gt);
   if (rc) return rc;
-  rc = make_map_3d(&mk, K, DH, g.N, g.Hkv, 64, 128, 1);
+  rc = make_map_3d(&mk, K, DH, g.N, g.Hkv, 64, 128, 1, static_cast<uint64_t>(pl.k_rows));
   if (rc) return rc;
   if (pl.want_plus) {
     KVS_CUDA_TRY(launch_k(row_norm_kernel, dim3(static_cast<unsigned>(cdiv(g.W, 8))), dim3(256), 0, st, 0, h, g.W,

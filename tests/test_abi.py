@@ -138,3 +138,13 @@ def test_core_sizes_and_argument_errors(lib):
     assert lib.kvs_gram(p, 8, 100, 128, None, 0, p, p, 16, None) == 6
     assert lib.kvs_spectrum(p, 8, 128, ctypes.c_float(1.5), p, p, p, None) == 1  # rtol outside [0, 1)
     assert lib.kvs_spectrum(p, 8, 64, ctypes.c_float(1e-3), p, p, p, None) == 2
+
+
+def test_block_lse_argument_errors(lib):
+    assert lib.kvs_block_lse_workspace_size(32, 8, 512, 8192, 128, 7680, 7680) > 0
+    assert lib.kvs_block_lse_workspace_size(32, 8, 512, 8192, 128, 7680, 0) == 0          # empty block
+    assert lib.kvs_block_lse_workspace_size(32, 8, 512, 8192, 128, 7680, 8193) == 0       # past the cache
+    p = ctypes.c_void_p(1 << 20)
+    assert lib.kvs_block_lse(p, p, 32, 8, 512, 8192, 128, 7680, 0, p, p, 1 << 30, None) == 1
+    assert lib.kvs_block_lse(p, p, 32, 8, 512, 8192, 96, 7680, 100, p, p, 1 << 30, None) == 2
+    assert lib.kvs_block_lse(p, p, 32, 8, 512, 8192, 128, 7681, 100, p, p, 1 << 30, None) == 1  # window past N
