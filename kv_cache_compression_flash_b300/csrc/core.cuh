@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float* __restric
 // ---------------------------------------------------------------------------
 // spectrum: one CTA of 256 threads per head, G in shared memory (row pitch 129)
 // ---------------------------------------------------------------------------
-constexpr int kSpecThreads = 256;
+constexpr int kSpecThreads = 1024;
 constexpr int kSpecPitch = kGramD + 1;
 constexpr int kSpecMaxSweeps = 24;
 constexpr size_t kSpecSmem = static_cast<size_t>(kGramD) * kSpecPitch * 4 + 64 * 4 * 4 + 32 * 4 + 64;
