@@ -37,6 +37,7 @@ namespace cg = cooperative_groups;
 constexpr int kCAThreads = 512;
 constexpr int kCAWarps = kCAThreads / 32;
 constexpr int kCAMaxCluster = 16;
+constexpr int kCATieList = 64;   // ties at lambda* settled from a list (more: block scans)
 
 struct CACand {
   unsigned long long theta;  // full bit pattern
@@ -197,6 +198,8 @@ __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const A
   __shared__ unsigned long long s_above;
   __shared__ unsigned s_fill;
   __shared__ unsigned long long s_pub_lam;
+  __shared__ unsigned s_ntie;
+  __shared__ int s_tie_i[kCATieList], s_tie_c[kCATieList];
 
   // ---- phase 0: validate, cache top halves, total cost of positive items ----
   // (loads batched 8 units per thread so their latencies overlap)
@@ -389,6 +392,38 @@ __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const A
       __syncthreads();
       above = s_above;
       pre = s_pub_lam;
+    } else if (n_cand <= 128) {
+      // one candidate per thread: lambda* is a theta whose cost strictly
+      // above stays within B while the cost at or above it does not (every
+      // candidate with that theta qualifies; the lowest index is taken)
+      const bool has = static_cast<unsigned long long>(tid) < n_cand;
+      const unsigned long long t = has ? cand[tid].theta : 0ull;
+      unsigned long long gt = 0, ge = 0;
+      if (has) {
+        for (unsigned long long m = 0; m < n_cand; ++m) {
+          const CACand cm = cand[m];
+          const unsigned c = static_cast<unsigned>(p.cost[cm.uk & 3]);
+          if (cm.theta > t) gt += c;
+          if (cm.theta >= t) ge += c;
+        }
+      }
+      const bool hit = has && above + gt <= p.B && above + ge > p.B;
+      if (tid == 0) s_sel = 0xFFFFFFFFu;
+      __syncthreads();
+      if (hit) atomicMin(&s_sel, static_cast<unsigned>(tid));
+      __syncthreads();
+      const unsigned src = s_sel;
+      if (src == 0xFFFFFFFFu) {                    // cannot happen; keeps the result defined
+        if (tid == 0) record_error(KVS_ERR_RANGE);
+      } else if (tid == static_cast<int>(src)) {
+        s_above = above + gt;
+        s_pub_lam = t;
+      }
+      __syncthreads();
+      if (src != 0xFFFFFFFFu) {
+        above = s_above;
+        pre = s_pub_lam;
+      }
     } else {
       // local passes over bits 41..0 of the full thetas (the top 22 are P)
       unsigned long long msk = static_cast<unsigned long long>(M) << 32;
@@ -465,12 +500,22 @@ __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const A
     }
     return l;
   };
-  // levels first; ties at lambda* (rare: one theta value) are settled below
+  // levels first; ties at lambda* (the theta of lambda* itself, and any equal
+  // ones: a handful) are listed and settled below
   unsigned long long my_tie = 0;
+  if (tid == 0) s_ntie = 0;
+  __syncthreads();
   for (int i = tid; i < n_mine; i += kCAThreads) {
     int tc;
     lvl[i] = static_cast<uint8_t>(unit_level(i, &tc));
     my_tie += static_cast<unsigned long long>(tc);
+    if (tc) {
+      const unsigned slot = atomicAdd(&s_ntie, 1u);
+      if (slot < kCATieList) {
+        s_tie_i[slot] = i;
+        s_tie_c[slot] = tc;
+      }
+    }
   }
   const int cta_has_tie = __syncthreads_or(my_tie != 0ull);
   const unsigned long long blk_tie = cta_has_tie ? ca_block_sum(my_tie, s_red) : 0ull;
@@ -485,7 +530,39 @@ __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const A
   }
   __syncthreads();
   unsigned long long my_used = 0;  // cumulative cost through the last tie taken here
-  if (cta_has_tie) {  // take ties in unit order while the running cost fits B
+  if (cta_has_tie && s_ntie <= kCATieList) {  // uniform: the list holds every tie of this CTA
+    // warp 0 orders the listed ties by unit and takes them while the running cost fits B
+    if (warp == 0) {
+      const int nt = static_cast<int>(s_ntie);
+      int ia = lane < nt ? s_tie_i[lane] : 0x7FFFFFFF, ib = lane + 32 < nt ? s_tie_i[lane + 32] : 0x7FFFFFFF;
+      const int ca = lane < nt ? s_tie_c[lane] : 0, cb = lane + 32 < nt ? s_tie_c[lane + 32] : 0;
+      // rank of each entry in unit order, then the cost of the entries before it
+      unsigned long long before_a = 0, before_b = 0;
+      for (int m = 0; m < nt; ++m) {
+        const int im = __shfl_sync(0xFFFFFFFFu, m < 32 ? ia : ib, m & 31);
+        const int cm = __shfl_sync(0xFFFFFFFFu, m < 32 ? ca : cb, m & 31);
+        if (im < ia) before_a += static_cast<unsigned long long>(cm);
+        if (im < ib) before_b += static_cast<unsigned long long>(cm);
+      }
+      unsigned long long mu = 0;
+      if (lane < nt) {
+        const unsigned long long cum = carry + before_a + static_cast<unsigned long long>(ca);
+        if (cum <= p.B) {
+          lvl[ia] = static_cast<uint8_t>(lvl[ia] + 1);
+          mu = cum;
+        }
+      }
+      if (lane + 32 < nt) {
+        const unsigned long long cum = carry + before_b + static_cast<unsigned long long>(cb);
+        if (cum <= p.B) {
+          lvl[ib] = static_cast<uint8_t>(lvl[ib] + 1);
+          mu = max(mu, cum);
+        }
+      }
+      my_used = mu;                                // folded over the block below
+    }
+    __syncthreads();
+  } else if (cta_has_tie) {  // many ties: take them in unit order, block scan by block scan
     for (int base = 0; base < n_mine; base += kCAThreads) {
       const int i = base + tid;
       int tc = 0;
