@@ -235,6 +235,12 @@ int pack_dh(const uint16_t* X, int64_t Hkv, int64_t N, int axis, const uint8_t* 
     }
   } else {
     const StreamPtrs sp = to_ptrs(s, !dequant);
+    if (dequant && N <= kDirectMaxN && Hkv * DH < 65536) {  // each CTA plans its own head
+      const dim3 grid(static_cast<unsigned>(cdiv(N, 64) + 1), static_cast<unsigned>(Hkv));
+      KVS_CUDA_TRY(launch_k(dequant_channels_direct_kernel<DH>, grid, dim3(256), 0, st, 0, sp, static_cast<int>(N),
+                            bits, keep, out));
+      return KVS_OK;
+    }
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {

@@ -640,4 +640,141 @@ __global__ void __launch_bounds__(256) dequant_channels_kernel(const StreamPtrs 
   }
 }
 
+// ---------------------------------------------------------------------------
+// dequantise the channel streams without a plan kernel (N <= kDirectMaxN)
+// ---------------------------------------------------------------------------
+// grid (ceil(N/64) + 1, Hkv), 256 threads.  Each CTA works out for its own
+// head what the plan kernel would give: the kept tokens in order (a block scan
+// of the head's keep bytes) and each channel's first stream group (the entry
+// of unit g*DH + c in its width stream is the number of earlier units of that
+// width; the group offset is read back from the stream).  CTA j < ngk decodes
+// kept-token group j; the CTAs after those zero the head's dropped tokens.
+constexpr int kDirectMaxN = 16384;
+
+__device__ __forceinline__ unsigned long long direct_exscan256(unsigned long long v, unsigned long long* sbuf,
+                                                               unsigned long long* total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) sbuf[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long t = lane < 8 ? sbuf[lane] : 0ull;
+    unsigned long long z = t;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, z, o);
+      if (lane >= o) z += y;
+    }
+    if (lane < 8) sbuf[lane] = z - t;
+    if (lane == 7) sbuf[8] = z;
+  }
+  __syncthreads();
+  *total = sbuf[8];
+  return sbuf[warp] + x - v;
+}
+
+template <int DH>
+__global__ void __launch_bounds__(256) dequant_channels_direct_kernel(const StreamPtrs sp, const int N,
+                                                                      const uint8_t* __restrict__ bits,
+                                                                      const uint8_t* __restrict__ keep,
+                                                                      float* __restrict__ out) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
+  constexpr int LD = DH + 1;
+  __shared__ float tile[64][LD];
+  __shared__ int s_w[DH];
+  __shared__ long long s_base[DH];
+  __shared__ int s_tok[64];
+  __shared__ unsigned long long sbuf[9];
+  const int j = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
+  // ---- the head's kept tokens: thread tid takes bytes [t0, t0 + per) ----
+  const int per = ((N + 255) / 256 + 15) / 16 * 16;
+  const int t0 = tid * per;
+  const uint8_t* kb = keep + static_cast<size_t>(g) * N;
+  int cnt = 0;
+  for (int e = 0; e < per; e += 16) {
+    if (t0 + e >= N) break;
+    const uint4 v = load_bits16(kb, t0 + e, N);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) cnt += (t0 + e + k < N && bits16_at(v, k) != 0) ? 1 : 0;
+  }
+  unsigned long long tot;
+  const int ex = static_cast<int>(direct_exscan256(static_cast<unsigned long long>(cnt), sbuf, &tot));
+  const int n = static_cast<int>(tot);
+  const int ngk = (n + 63) / 64;
+  const bool kept_cta = j < ngk;
+  // this CTA's 64 list entries: kept ranks [64j, 64j + 64), or dropped ranks after the kept groups
+  const int lo = kept_cta ? 64 * j : 64 * (j - ngk);
+  const int hi = lo + 64;
+  const int my_lo = kept_cta ? ex : t0 - ex;                       // first kept / dropped rank of my bytes
+  const int my_n = kept_cta ? cnt : max(0, min(per, N - t0)) - cnt;
+  if (my_lo < hi && my_lo + my_n > lo) {
+    int r = my_lo;
+    for (int e = 0; e < per && t0 + e < N; ++e) {
+      const bool kept = kb[t0 + e] != 0;
+      if (kept == kept_cta) {
+        if (r >= lo && r < hi) s_tok[r - lo] = t0 + e;
+        ++r;
+      }
+    }
+  }
+  const int rows = kept_cta ? min(64, n - lo) : max(0, min(64, (N - n) - lo));
+  if (!kept_cta) {
+    __syncthreads();
+    for (int e = tid; e < rows * (DH / 4); e += 256) {
+      const int i = e / (DH / 4), c4 = (e % (DH / 4)) * 4;
+      *reinterpret_cast<float4*>(out + (static_cast<size_t>(g) * N + s_tok[i]) * DH + c4) =
+          make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
+  // ---- each channel's entry in its width stream, then its first group ----
+  unsigned long long before = 0;                   // units of each width before this head, 16-bit fields
+  for (int u = tid; u < g * DH; u += 256) {
+    const int sl = width_slot(bits[u]);
+    if (sl >= 0) before += 1ull << (16 * sl);
+  }
+  unsigned long long base_all;
+  (void)direct_exscan256(before, sbuf, &base_all);
+  const int sl_me = tid < DH ? width_slot(bits[g * DH + tid]) : -1;
+  const unsigned long long mine = sl_me >= 0 ? 1ull << (16 * sl_me) : 0ull;
+  unsigned long long head_tot;
+  const unsigned long long exh = direct_exscan256(mine, sbuf, &head_tot);
+  if (tid < DH) {
+    long long b = -1;
+    if (sl_me >= 0) {
+      const long long entry = static_cast<long long>(((base_all + exh) >> (16 * sl_me)) & 0xFFFFull);
+      if (entry < sp.cap_units[sl_me]) b = sp.goff[sl_me][entry] + j;
+      if (b >= sp.cap_groups[sl_me]) b = -1;
+    }
+    s_w[tid] = sl_me >= 0 ? static_cast<int>(bits[g * DH + tid]) : 0;
+    s_base[tid] = b;
+  }
+  __syncthreads();
+  const int l16 = threadIdx.x & 15, hw = threadIdx.x >> 4;
+  for (int c = hw; c < DH; c += 16) {
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    const long long grp = s_base[c];
+    if (grp >= 0) {
+      const int w = s_w[c];
+      const int s = width_slot(w);
+      dequant_lane4(sp.codes[s] + grp * (8 * w), w, l16, sp.scales[s] + grp, y);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) tile[4 * l16 + e][c] = y[e];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < rows * (DH / 4); e += 256) {
+    const int i = e / (DH / 4), c4 = (e % (DH / 4)) * 4;
+    *reinterpret_cast<float4*>(out + (static_cast<size_t>(g) * N + s_tok[i]) * DH + c4) =
+        make_float4(tile[i][c4], tile[i][c4 + 1], tile[i][c4 + 2], tile[i][c4 + 3]);
+  }
+}
+
 }  // namespace kvs

@@ -75,7 +75,9 @@ class RdkvLayerStep:
         n += 1          # K allocation
         n += 2 + 2      # V pack (plan, pack), K pack (plan, pack)
         if self.dequant:
-            n += 1 + 2  # V dequant (decode + zero), K dequant (plan, decode + zero)
+            # V dequant (decode + zero); K dequant (decode + zero, planned inside the
+            # kernel up to 16 384 tokens, else a plan kernel first)
+            n += 1 + (1 if N <= 16384 and Hkv * d < 65536 else 2)
         return n
 
     def pass1(self, Q, K, V, stream=None):
