@@ -10,7 +10,9 @@
 //                        registers (8 x 8 bf16 blocks) and stored as X^T in the
 //                        K-major 128-byte-swizzle layout; both MMA operands are
 //                        that one tile, so tcgen05.mma (M = N = 128, K = 16,
-//                        bf16 products exact in fp32) accumulates X^T X in TMEM.
+//                        bf16 products exact in fp32) accumulates X^T X in TMEM
+//                        (even and odd tiles in two accumulators, added at the
+//                        end: half the sequential fp32 additions).
 //                        Two tile buffers: the next tile is transposed while
 //                        the tensor core consumes the previous one.
 //   gram_reduce_kernel   adds the per-range partials in range order
@@ -70,7 +72,7 @@ __global__ void __launch_bounds__(kGramThreads) gram_partial_kernel(const uint16
     mbar_fence_init();
   }
   if (warp == 0) {
-    tmem_alloc(&S.tmem_base, 128);
+    tmem_alloc(&S.tmem_base, 256);                 // two accumulators: even and odd tiles
     tmem_relinquish();
   }
   tc_fence_before();
@@ -135,7 +137,8 @@ __global__ void __launch_bounds__(kGramThreads) gram_partial_kernel(const uint16
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
-        umma_bf16(tmem, sdesc_kmajor_sw128(a + off), sdesc_kmajor_sw128(a + off), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        umma_bf16(tmem + 128u * b, sdesc_kmajor_sw128(a + off), sdesc_kmajor_sw128(a + off), idesc,
+                  (i > 1 || kk > 0) ? 1u : 0u);
       }
       umma_commit(&S.mma_done[b]);
     }
@@ -151,9 +154,14 @@ __global__ void __launch_bounds__(kGramThreads) gram_partial_kernel(const uint16
     const int rrow = 32 * warp + lane;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      float v[32];
+      float v[32], v2[32];
       if (have) {
         tmem_load32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * c, v);
+        if (ntiles > 1) {
+          tmem_load32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 128 + 32 * c, v2);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] += v2[k];
+        }
       } else {
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = 0.f;
@@ -168,7 +176,7 @@ __global__ void __launch_bounds__(kGramThreads) gram_partial_kernel(const uint16
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 256);
   }
 }
 

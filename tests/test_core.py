@@ -2,9 +2,10 @@
 [KV-CoRE §2].
 
 Tolerances.  bf16 products are exact in fp32 and the tensor cores add them in
-fp32, so an entry of G carries a relative error of a few 2^-24 per addition
-over the token count: the test allows 1e-5 * sum_t |x_t|^2 (the trace, which
-bounds every entry).  The spectrum comes from fp32 Jacobi on that G: an
+fp32: a CTA adds its token range into two accumulators (even and odd tiles)
+16 tokens per step, and the ranges are added in order, so an entry of G is
+within (range / 32 + ranges) * 2^-24 of the trace (which bounds every entry)
+in the worst case; the tests allow twice that, at least 1e-5.  The spectrum comes from fp32 Jacobi on that G: an
 eigenvalue moves by at most about 1e-6 * |G|_F, so sigma = sqrt(lambda) moves
 by at most 1e-6 relative for the large values and by sqrt(1e-6 |G|_F) for the
 smallest; the NER is compared within 1e-3 with the rank equal, on data whose
@@ -35,13 +36,20 @@ def structured(Hkv, N, seed, ranks=(64,), scale_hi=(1.0, 0.1), low=1e-5):
     return torch.stack(out).float().bfloat16()
 
 
+def gram_rtol(Hkv, N):
+    ranges = max(1, min(-(-N // 128), torch.cuda.get_device_properties(0).multi_processor_count // Hkv))
+    per = -(-N // ranges)
+    return max(1e-5, 2 * (per / 32 + ranges) * 2.0 ** -24)
+
+
 def check_gram(G, X, keep=None):
     x64 = X.double().numpy()
     ref = O.gram(x64, keep)
     got = G.cpu().numpy().astype(np.float64)
+    tol = gram_rtol(x64.shape[0], x64.shape[1])
     for g in range(x64.shape[0]):
         tr = np.trace(ref[g])
-        assert np.abs(got[g] - ref[g]).max() <= 1e-5 * tr, (g, np.abs(got[g] - ref[g]).max(), tr)
+        assert np.abs(got[g] - ref[g]).max() <= tol * tr, (g, np.abs(got[g] - ref[g]).max(), tr)
 
 
 @pytest.mark.parametrize("Hkv,N", [(2, 1000), (1, 1), (3, 129), (8, 4096)])
@@ -109,9 +117,10 @@ def test_gram_full_size_properties():
     assert L.device_error() == 0
     Gc = G.cpu().double()
     k64 = K.double()
+    tol = gram_rtol(wl.Hkv, wl.N)
     for g in range(wl.Hkv):
         fro2 = float((k64[g] ** 2).sum())
-        assert abs(float(torch.trace(Gc[g])) - fro2) <= 1e-5 * fro2
+        assert abs(float(torch.trace(Gc[g])) - fro2) <= tol * fro2
         assert float((Gc[g] - Gc[g].T).abs().max()) <= 1e-6 * fro2
         assert abs(float((sigma[g].double() ** 2).sum().cpu()) - fro2) <= 1e-4 * fro2   # sum sigma^2 = trace
         assert 0 < int(rank[g]) <= 128 and 1.0 / int(rank[g]) - 1e-6 <= float(ner[g]) <= 1.0 + 1e-6
