@@ -33,7 +33,10 @@ constexpr int kGramThreads = 256;
 constexpr int kGramD = 128;
 constexpr int kGramTile = 128;                   // tokens per tile (two 64-token K panels)
 constexpr int kGramTileBytes = 2 * 16384;        // X^T tile: 128 rows x 128 tokens bf16
-constexpr int kGramSmem = 2 * kGramTileBytes + 1024 + 64;
+// two tile buffers, alignment slack and the control block, padded so that at
+// most two CTAs share an SM: two CTAs take all 512 TMEM columns
+constexpr int kGramSmem = 80 * 1024;
+static_assert(2 * kGramTileBytes + 1024 + 64 <= kGramSmem, "gram shared memory");
 
 struct GramCtl {
   uint64_t mma_done[2];
