@@ -86,6 +86,12 @@ def reduce_max(dist, x: float, device=None) -> float:
     return float(t.item())
 
 
+def replica_value(world: int, steps: int, tokens_per_pool: int, slowest_s: float) -> float:
+    """Whole-job throughput in M tok/s: every rank compresses one pool per step
+    (weak scaling), and the job takes as long as its slowest rank."""
+    return world * steps * tokens_per_pool / slowest_s / 1e6
+
+
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
@@ -310,7 +316,7 @@ def run_ours(args):
     seg = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)] for i in range(args.steps)]
     step_ms = [sum(s) for s in seg]
     total_s = reduce_max(dist, sum(step_ms) / 1e3, dev)
-    value = world * args.steps * wl.N / total_s / 1e6
+    value = replica_value(world, args.steps, wl.N, total_s)
     seg_avg = [statistics.fmean(s[j] for s in seg) for j in range(3)]
 
     # ---- roofline of the dominant kernel (the slower scoring pass) -------------
@@ -447,7 +453,7 @@ def run_e2e(args, step, pinned, dev_inputs, flush, dist, dev, world, wl):
     elapsed = time.perf_counter() - t0
     barrier(dist, dev)
     total = reduce_max(dist, elapsed, dev)
-    return {"value": world * args.steps * wl.N / total / 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d,
+    return {"value": replica_value(world, args.steps, wl.N, total), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h[0],
             "path": "pinned host Q,K,V -> device, graph replay of the C-ABI calls, packed streams + widths -> "
                     "host; two pools in flight (copies of one step overlap the compute of the next)"}
