@@ -289,6 +289,8 @@ def run_ours(args):
 
     for _ in range(args.warmup):
         flush.zero_()
+        step.replay_step()
+        flush.zero_()
         step.replay()
     torch.cuda.synchronize()
     if L.device_error() != 0:
@@ -299,24 +301,38 @@ def run_ours(args):
     while time.perf_counter() - t_soak < args.soak_s:  # clocks under load before the timed region
         for _ in range(20):
             flush.zero_()
-            step.replay()
+            step.replay_step()
         torch.cuda.synchronize()
 
+    # the timed steps: the whole step replayed as one graph, events around it
+    step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
     barrier(dist, dev)
     torch.cuda.synchronize()
     for i in range(args.steps):
         flush.zero_()
-        step.replay(evs[i])
+        step_evs[i][0].record()
+        step.replay_step()
+        step_evs[i][1].record()
     torch.cuda.synchronize()
     barrier(dist, dev)
     clk = clocks.stop()
     if L.device_error() != 0:
         raise SystemExit("device error during the timed region")
-
-    seg = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)] for i in range(args.steps)]
-    step_ms = [sum(s) for s in seg]
+    step_ms = [a.elapsed_time(b) for a, b in step_evs]
     total_s = reduce_max(dist, sum(step_ms) / 1e3, dev)
     value = replica_value(world, args.steps, wl.N, total_s)
+
+    # the segments (pass 1, pass 2, the rest), each its own graph with events
+    # between them, for the per-segment times and the roofline of the pass kernel
+    n_seg = min(args.steps, 50)
+    for i in range(n_seg):
+        flush.zero_()
+        step.replay(evs[i])
+    torch.cuda.synchronize()
+    if L.device_error() != 0:
+        raise SystemExit("device error while timing the segments")
+    seg = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)] for i in range(n_seg)]
     seg_avg = [statistics.fmean(s[j] for s in seg) for j in range(3)]
 
     # ---- roofline of the dominant kernel (the slower scoring pass) -------------
@@ -405,7 +421,7 @@ def run_e2e(args, step, pinned, dev_inputs, flush, dist, dev, world, wl):
         if i >= 2:
             comp.wait_event(ev_out[s])         # step i-2's streams have left
         with torch.cuda.stream(comp):
-            st.replay()
+            st.replay_step()
             for j, sm in enumerate((st.v_streams, st.k_streams)):
                 land["counts"][j].copy_(sm.counts, non_blocking=True)
             land["bits_v"].copy_(st.bits_v, non_blocking=True)

@@ -139,7 +139,17 @@ class RdkvLayerStep:
             with torch.cuda.graph(g, capture_error_mode="relaxed"):
                 getattr(self, name)(Q, K, V)
             self.graphs[name] = g
+        # the whole step as one graph as well: no launch gap between segments
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            self.run(Q, K, V)
+        self.step_graph = g
         torch.cuda.synchronize()
+        return self
+
+    def replay_step(self):
+        """Replays the whole captured step as one graph."""
+        self.step_graph.replay()
         return self
 
     def replay(self, events=None):
