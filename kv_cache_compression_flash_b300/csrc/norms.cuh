@@ -77,23 +77,28 @@ __device__ __forceinline__ void colsq_rows(const uint16_t* __restrict__ X, const
   constexpr int RPI = kColThreads / TPR;     // rows per step
   const int rsub = threadIdx.x / TPR, cseg = (threadIdx.x % TPR) * 8;
   int n = 0;
-  for (int base = r_begin + rsub; base < r_end; base += 4 * RPI) {
-    uint4 u[4];
-    bool ok[4];
+  constexpr int kInFlight = 8;
+  for (int base = r_begin + rsub; base < r_end; base += kInFlight * RPI) {
+    uint4 u[kInFlight];
+    uint8_t kp[kInFlight];
+    // the rows' loads do not wait for their keep bytes: both go out together and
+    // a dropped row is left out afterwards
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {  // four independent 16-byte loads in flight
+    for (int j = 0; j < kInFlight; ++j) {
       const int r = base + j * RPI;
-      ok[j] = r < r_end && (keep == nullptr || keep[r] != 0);
-      u[j] = ok[j] ? __ldg(reinterpret_cast<const uint4*>(X + static_cast<size_t>(r) * DH + cseg))
-                   : make_uint4(0u, 0u, 0u, 0u);
+      const bool in = r < r_end;
+      u[j] = in ? __ldg(reinterpret_cast<const uint4*>(X + static_cast<size_t>(r) * DH + cseg))
+                : make_uint4(0u, 0u, 0u, 0u);
+      kp[j] = in ? (keep == nullptr ? 1 : __ldg(keep + r)) : 0;
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kInFlight; ++j) {
+      if (kp[j] == 0) continue;
       float f[8];
       bf16x8_to_f32(u[j], f);
 #pragma unroll
       for (int k = 0; k < 8; ++k) acc[k] = fmaf(f[k], f[k], acc[k]);
-      n += ok[j] ? 1 : 0;
+      ++n;
     }
   }
   *n_kept = n;
