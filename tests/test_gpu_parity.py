@@ -278,3 +278,20 @@ def test_threshold_keep_bit_exact(Hkv, N):
     got = L.threshold_keep(torch.from_numpy(s).to(DEV), 0.1, 0, 16).cpu().numpy()
     assert np.array_equal(got, O.threshold_keep(s, 0.1, 0, 16))
     assert L.device_error() == 3
+
+
+def test_one_graph_step_matches_the_eager_step():
+    """The bench's one-graph replay of the whole step gives the eager step's results."""
+    wl = synth.WORKLOADS["llama3_8b_layer_n8192_w512"]
+    t = synth.make_layer(wl)
+    Q, K, V = (t[k].to(DEV) for k in ("Q", "K", "V"))
+    a = RdkvLayerStep(wl.Hq, wl.Hkv, wl.N, wl.W, wl.d, 3, device=DEV)
+    a.run(Q, K, V)
+    b = RdkvLayerStep(wl.Hq, wl.Hkv, wl.N, wl.W, wl.d, 3, device=DEV)
+    b.capture(Q, K, V)
+    b.replay_step()
+    torch.cuda.synchronize()
+    assert L.device_error() == 0
+    assert torch.equal(a.sig_t, b.sig_t) and torch.equal(a.bits_v, b.bits_v) and torch.equal(a.bits_k, b.bits_k)
+    assert torch.equal(a.v_hat, b.v_hat) and torch.equal(a.k_hat, b.k_hat)
+    assert torch.equal(a.out["w_t"], b.out["w_t"])
