@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(1024) trizone_index_kernel(StreamPtrs ks, Stre
 // ---------------------------------------------------------------------------
 // one m16n8k16 bf16 MMA on rows 0-7 (rows 8-15 of A are zero; their outputs are dropped)
 __device__ __forceinline__ void tz_mma(float& d0, float& d1, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-  float x0, x1;
+  [[maybe_unused]] float x0, x1;  // rows 8-15 of the product: not needed
   asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%5}, {%7,%8}, {%0,%1,%9,%9};"
       : "+f"(d0), "+f"(d1), "=f"(x0), "=f"(x1)
       : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(0.f));
