@@ -565,3 +565,61 @@ def block_lse(Q, K, q_pos0, n_block):
             m = s.max()
             out[hd, r] = m + math.log(np.exp(s - m).sum())
     return out
+
+
+# ----------------------------------------------------------------------------
+# O10. KVSculpt targets and the ridge value solve
+# ----------------------------------------------------------------------------
+def block_attention(Q, K, V, q_pos0, n_block):
+    """Attention output and LSE of the window queries over the leading keys
+    [0, n_block) of each head: the targets (Y, lse) that KVSculpt's compressed
+    pairs must reproduce for the compression zone.   [KVSculpt §2, loss: MSE of
+    the output and the LSE term]
+    Y[hd, r] = sum_{t < n_block, t <= p_r} softmax_t(q_r . k_t / sqrt(d)) v_t.
+    Returns (Y [Hq, W, d], lse [Hq, W]).
+    Pins: one key gives its value row; equal keys give the mean of the visible
+    rows; the block and the rest of the prefix merge (by their LSE) into the
+    attention over the whole prefix.
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    Hq, W, d = Q.shape
+    G = Hq // K.shape[0]
+    Y = np.zeros((Hq, W, d))
+    lse = np.empty((Hq, W))
+    t = np.arange(n_block)
+    for hd in range(Hq):
+        Kb, Vb = K[hd // G, :n_block], V[hd // G, :n_block]
+        for r in range(W):
+            vis = t <= q_pos0 + r
+            s = Kb[vis] @ Q[hd, r] / math.sqrt(d)
+            m = s.max()
+            e = np.exp(s - m)
+            lse[hd, r] = m + math.log(e.sum())
+            Y[hd, r] = (e @ Vb[vis]) / e.sum()
+    return Y, lse
+
+
+def ridge_values(Qt, Kc, Y, lam):
+    """Closed-form values of KVSculpt's alternating solve for fixed keys
+    [KVSculpt §2: with the keys fixed, the values are a ridge least-squares
+    solution]:
+        A = softmax_rows(Qt Kc^T / sqrt(d))             [R, k]
+        V_c = argmin |A V - Y|_F^2 + lam |V|_F^2 = (A^T A + lam I)^-1 A^T Y.
+    Qt [R, d] training queries, Kc [k, d] compressed keys, Y [R, d] targets,
+    lam > 0.  Returns V_c [k, d].  The linear solve is LAPACK's (a library
+    primitive).
+    Pins: one key gives sum(Y) / (R + lam); noiseless targets Y = A V are
+    recovered as lam -> 0; the gradient of the objective vanishes at V_c.
+    """
+    Qt = np.asarray(Qt, dtype=np.float64)
+    Kc = np.asarray(Kc, dtype=np.float64)
+    Y = np.asarray(Y, dtype=np.float64)
+    d = Qt.shape[1]
+    S = Qt @ Kc.T / math.sqrt(d)
+    S = S - S.max(axis=1, keepdims=True)
+    A = np.exp(S)
+    A /= A.sum(axis=1, keepdims=True)
+    k = Kc.shape[0]
+    return np.linalg.solve(A.T @ A + lam * np.eye(k), A.T @ Y)

@@ -560,3 +560,55 @@ def test_block_lse_plus_rest_is_row_lse():
             for t in range(0, q0 + r + 1):
                 full += math.exp(sum(Q[hd, r, i] * K[0, t, i] for i in range(4)) / 2.0)
             assert math.exp(blk[hd, r]) + rest == pytest.approx(full, rel=1e-12)
+
+
+# ----------------------------------------------------------------------------
+# KVSculpt targets and ridge values   [KVSculpt §2]
+# ----------------------------------------------------------------------------
+def test_block_attention_closed_forms_and_merge():
+    rng = np.random.default_rng(51)
+    Q = rng.standard_normal((2, 4, 4))
+    K = rng.standard_normal((1, 9, 4))
+    V = rng.standard_normal((1, 9, 4))
+    Y, lse = O.block_attention(Q, K, V, 5, 1)                       # one key: its value row
+    np.testing.assert_allclose(Y, np.broadcast_to(V[0, 0], Y.shape), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse, O.block_lse(Q, K, 5, 1), rtol=1e-14)
+    Kc = np.repeat(K[:, :1], 9, axis=1)                              # equal keys: mean of the visible rows
+    Y, _ = O.block_attention(Q, Kc, V, 2, 7)
+    for r in range(4):
+        np.testing.assert_allclose(Y[0, r], V[0, :min(7, 3 + r)].mean(axis=0), rtol=1e-13)
+    # block [0, 5) merged with the rest of the prefix, by hand, = the whole prefix
+    Yb, lb = O.block_attention(Q, K, V, 5, 5)
+    Ya, la = O.block_attention(Q, K, V, 5, 9)
+    for hd in range(2):
+        for r in range(4):
+            num = math.exp(lb[hd, r]) * Yb[hd, r]
+            den = math.exp(lb[hd, r])
+            for t in range(5, 5 + r + 1):
+                w = math.exp(float(Q[hd, r] @ K[0, t]) / 2.0)
+                num = num + w * V[0, t]
+                den += w
+            np.testing.assert_allclose(Ya[hd, r], num / den, rtol=1e-12)
+            assert la[hd, r] == pytest.approx(math.log(den), rel=1e-12)
+
+
+def test_ridge_values_pins():
+    rng = np.random.default_rng(52)
+    Qt = rng.standard_normal((20, 8))
+    Y = rng.standard_normal((20, 8))
+    one = O.ridge_values(Qt, rng.standard_normal((1, 8)), Y, 0.5)    # one key: softmax is 1 everywhere
+    np.testing.assert_allclose(one[0], Y.sum(axis=0) / (20 + 0.5), rtol=1e-13)
+    Kc = rng.standard_normal((5, 8)) * 2
+    S = Qt @ Kc.T / math.sqrt(8)
+    A = np.exp(S - S.max(axis=1, keepdims=True))
+    A /= A.sum(axis=1, keepdims=True)
+    V_true = rng.standard_normal((5, 8))
+    np.testing.assert_allclose(O.ridge_values(Qt, Kc, A @ V_true, 1e-12), V_true, rtol=0, atol=1e-5)  # noiseless
+    lam = 0.3
+    Vc = O.ridge_values(Qt, Kc, Y, lam)
+    grad = A.T @ (A @ Vc - Y) + lam * Vc                              # optimality: the gradient vanishes
+    assert np.abs(grad).max() < 1e-12
+    for trial in range(5):                                           # and nearby points are no better
+        P = Vc + 1e-3 * rng.standard_normal(Vc.shape)
+        f = lambda X: ((A @ X - Y) ** 2).sum() + lam * (X ** 2).sum()
+        assert f(P) >= f(Vc)
