@@ -24,6 +24,7 @@ class RdkvLayerStep:
     """
 
     PASS2_MODE = K_.MODE_RDKV_WT | K_.MODE_LSE_GIVEN
+    BOTH_MODE = K_.MODE_LSE | K_.MODE_RDKV_WT      # both passes in one call (the merge writes pass 2's offsets)
     SEGMENTS = ("pass1", "pass2", "rest")
 
     def __init__(self, Hq, Hkv, N, W, d, avg_bits, device="cuda", width_mask=K_.WIDTHS_ALL, dequant=True):
@@ -45,13 +46,14 @@ class RdkvLayerStep:
         self.k_streams = K_.Streams(Hkv, N, d, 1, self.B_k, dev)
         self.v_hat = torch.empty(Hkv, N, d, **f32) if dequant else None
         self.k_hat = torch.empty(Hkv, N, d, **f32) if dequant else None
-        names = ("score", "score2", "cw", "rms0", "rms1", "av", "ak", "pv", "pk", "dv", "dk")
+        names = ("score", "score2", "score12", "cw", "rms0", "rms1", "av", "ak", "pv", "pk", "dv", "dk")
         self.ws = {k: K_.Workspace() for k in names}
         # size every workspace now so a step allocates nothing
         L = K_.lib()
         sizes = {
             "score": L.kvs_score_workspace_size(Hq, Hkv, W, N, d, 0, N - W, K_.MODE_LSE),
             "score2": L.kvs_score_workspace_size(Hq, Hkv, W, N, d, 0, N - W, self.PASS2_MODE),
+            "score12": L.kvs_score_workspace_size(Hq, Hkv, W, N, d, 0, N - W, self.BOTH_MODE),
             "cw": L.kvs_channel_weights_workspace_size(Hq, Hkv, W, N, d),
             "rms0": 256, "rms1": L.kvs_unit_rms_workspace_size(Hkv, N, d, 1),
             "av": L.kvs_allocate_workspace_size(self.U_v), "ak": L.kvs_allocate_workspace_size(self.U_k),
@@ -67,8 +69,7 @@ class RdkvLayerStep:
     def kernel_launches(self) -> int:
         """Kernels one step launches (memset nodes excluded)."""
         Hq, Hkv, N, W, d = self.shape
-        n = K_.score_plan_info(Hq, Hkv, W, N, d, mode=K_.MODE_LSE)[4]
-        n += K_.score_plan_info(Hq, Hkv, W, N, d, mode=self.PASS2_MODE)[4]
+        n = K_.score_plan_info(Hq, Hkv, W, N, d, mode=self.BOTH_MODE)[4]   # the step's one scoring call
         n += 1          # channel weights (one cluster per KV head)
         n += 1          # sigma_t
         n += 1 + 1      # V allocation, sigma_c
@@ -83,6 +84,12 @@ class RdkvLayerStep:
     def pass1(self, Q, K, V, stream=None):
         Hq, Hkv, N, W, d = self.shape
         K_.score_attention(Q, K, q_pos0=N - W, mode=K_.MODE_LSE, out=self.out, ws=self.ws["score"], stream=stream)
+
+    def score(self, Q, K, V, stream=None):
+        """Both passes in one call (the step); pass1/pass2 split them for timing."""
+        Hq, Hkv, N, W, d = self.shape
+        K_.score_attention(Q, K, q_pos0=N - W, mode=self.BOTH_MODE, out=self.out, ws=self.ws["score12"],
+                           stream=stream)
 
     def pass2(self, Q, K, V, stream=None):
         Hq, Hkv, N, W, d = self.shape
@@ -118,8 +125,7 @@ class RdkvLayerStep:
         main.wait_stream(side)
 
     def run(self, Q, K, V, stream=None):
-        self.pass1(Q, K, V, stream)
-        self.pass2(Q, K, V, stream)
+        self.score(Q, K, V, stream)
         self.rest(Q, K, V, stream)
         return self
 
