@@ -337,6 +337,48 @@ int kvs_gram(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, const uint8_t
 int kvs_spectrum(const float* G, int64_t Hkv, int64_t d, float rtol, float* sigma, float* ner, int32_t* rank,
                  void* stream);
 
+/* ---- KVSculpt: attention targets and closed-form values ------------------ */
+/* kvs_block_attention: the attention output and LSE of the window queries over
+ * the leading keys [0, n_block) of each KV head, the targets the compressed
+ * pairs of the compression zone are fitted to   [KVSculpt §2, the loss: the
+ * output term and the LSE term]:
+ *     Y[hd, r, :] = sum_t softmax_t(q_r . k_t / sqrt(d)) v_t,
+ *     lse[hd, r]  = ln sum_t exp(q_r . k_t / sqrt(d)),
+ * both over t < n_block with t <= q_pos0 + r (queries at or after n_block see
+ * the whole block).
+ *   Q      : bf16 [Hq, W, d];  K, V : bf16 [Hkv, N, d] (the cache itself; only
+ *            rows [0, n_block) of each head are read);
+ *   Y      : float [Hq, W, d], written;  lse : float [Hq, W] or NULL.
+ * Shapes and errors as kvs_block_lse (1 <= n_block <= N, d in {64, 128});
+ * every pointer 16-byte aligned.  No workspace.  fp32 accumulation of the
+ * bf16 products (one warp per query row, online softmax over chunks of 32
+ * keys).
+ *
+ * kvs_ridge_values: per KV head g, the values of k compressed pairs whose keys
+ * Kc[g] are fixed   [KVSculpt §2: with the keys fixed the values solve a
+ * ridge least-squares problem in closed form]:
+ *     A     = softmax_rows(Qt[g] Kc[g]^T / sqrt(d))            [R, k]
+ *     Vc[g] = (A^T A + lam I)^-1 A^T Y[g]                      [k, d]
+ *   Qt : bf16 [Hkv, R, d], the training queries of each head (Q [Hq, W, d]
+ *        is this layout with R = (Hq / Hkv) W);
+ *   Kc : bf16 [Hkv, k, d], 1 <= k <= 512;
+ *   Y  : float [Hkv, R, d], the targets (Y of kvs_block_attention is this
+ *        layout);
+ *   lam: > 0 and finite;
+ *   Vc : float [Hkv, k, d], written;
+ *   workspace: kvs_ridge_values_workspace_size(Hkv, R, k, d) bytes, 256-byte
+ *        aligned.
+ * fp32 throughout: A, then A^T A + lam I and A^T Y, then a Cholesky solve
+ * (one CTA per head).  A pivot that is not positive (lam too small for fp32
+ * against |A^T A|) records KVS_ERR_RANGE in the error word and sets that
+ * head's values to 0.  d in {64, 128}, else KVS_ERR_UNSUPPORTED; k > 512
+ * gives KVS_ERR_UNSUPPORTED. */
+int kvs_block_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t Hq, int64_t Hkv, int64_t W,
+                        int64_t N, int64_t d, int64_t q_pos0, int64_t n_block, float* Y, float* lse, void* stream);
+size_t kvs_ridge_values_workspace_size(int64_t Hkv, int64_t R, int64_t k, int64_t d);
+int kvs_ridge_values(const uint16_t* Qt, const uint16_t* Kc, const float* Y, int64_t Hkv, int64_t R, int64_t k,
+                     int64_t d, float lam, float* Vc, void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -65,6 +65,10 @@ SIGNATURES = {
     "kvs_gram_workspace_size": (c_size_t, [c_int64] * 3),
     "kvs_gram": (c_int, [c_void_p] + [c_int64] * 3 + [c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
     "kvs_spectrum": (c_int, [c_void_p, c_int64, c_int64, ctypes.c_float, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "kvs_block_attention": (c_int, [c_void_p] * 3 + [c_int64] * 7 + [c_void_p] * 3),
+    "kvs_ridge_values_workspace_size": (c_size_t, [c_int64] * 4),
+    "kvs_ridge_values": (c_int, [c_void_p] * 3 + [c_int64] * 4 + [ctypes.c_float, c_void_p, c_void_p, c_size_t,
+                                                                  c_void_p]),
 }
 
 
@@ -380,3 +384,39 @@ def block_lse(Q, K, n_block, *, q_pos0=None, out=None, ws=None, stream=None):
     _check(L.kvs_block_lse(_ptr(Q), _ptr(K), Hq, Hkv, W, N, d, q_pos0, n_block, _ptr(lse), _ptr(buf), buf.numel(),
                            _stream(stream)), "kvs_block_lse")
     return lse
+
+
+def block_attention(Q, K, V, n_block, *, q_pos0=None, want_lse=True, out=None, stream=None):
+    """(Y [Hq, W, d], lse [Hq, W] or None) float32: attention of the window
+    queries over keys [0, n_block) of each KV head (causal inside the block)."""
+    _bf16(Q, "Q"), _bf16(K, "K"), _bf16(V, "V")
+    Hq, W, d = Q.shape
+    Hkv, N, _ = K.shape
+    if tuple(V.shape) != tuple(K.shape):
+        raise KvsError("V must have K's shape")
+    if q_pos0 is None:
+        q_pos0 = N - W
+    Y = out if out is not None else torch.empty(Hq, W, d, dtype=torch.float32, device=Q.device)
+    lse = torch.empty(Hq, W, dtype=torch.float32, device=Q.device) if want_lse else None
+    _check(lib().kvs_block_attention(_ptr(Q), _ptr(K), _ptr(V), Hq, Hkv, W, N, d, q_pos0, n_block, _ptr(Y), _ptr(lse),
+                                     _stream(stream)), "kvs_block_attention")
+    return Y, lse
+
+
+def ridge_values(Qt, Kc, Y, lam, *, out=None, ws=None, stream=None):
+    """Vc [Hkv, k, d] float32 = (A^T A + lam I)^-1 A^T Y per KV head, with
+    A = softmax(Qt Kc^T / sqrt(d)); Qt bf16 [Hkv, R, d], Kc bf16 [Hkv, k, d],
+    Y float32 [Hkv, R, d]."""
+    _bf16(Qt, "Qt"), _bf16(Kc, "Kc")
+    if Y.dtype != torch.float32 or not Y.is_cuda or not Y.is_contiguous():
+        raise KvsError("Y must be a contiguous float32 CUDA tensor")
+    Hkv, R, d = Qt.shape
+    k = Kc.shape[1]
+    if tuple(Kc.shape) != (Hkv, k, d) or tuple(Y.shape) != (Hkv, R, d):
+        raise KvsError("Qt [Hkv, R, d], Kc [Hkv, k, d] and Y [Hkv, R, d] must agree")
+    L = lib()
+    Vc = out if out is not None else torch.empty(Hkv, k, d, dtype=torch.float32, device=Qt.device)
+    buf = _ws(ws, "ridge", L.kvs_ridge_values_workspace_size(Hkv, R, k, d), Qt.device)
+    _check(L.kvs_ridge_values(_ptr(Qt), _ptr(Kc), _ptr(Y), Hkv, R, k, d, float(lam), _ptr(Vc), _ptr(buf), buf.numel(),
+                              _stream(stream)), "kvs_ridge_values")
+    return Vc

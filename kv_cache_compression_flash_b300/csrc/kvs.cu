@@ -15,6 +15,7 @@
 #include "score.cuh"
 #include "decode.cuh"
 #include "core.cuh"
+#include "sculpt.cuh"
 
 using namespace kvs;
 
@@ -758,6 +759,83 @@ int kvs_spectrum(const float* G, int64_t Hkv, int64_t d, float rtol, float* sigm
   KVS_CUDA_TRY(allow_smem(spectrum_kernel, kSpecSmem));
   KVS_CUDA_TRY(launch_k(spectrum_kernel, dim3(static_cast<unsigned>(Hkv)), dim3(kSpecThreads), kSpecSmem,
                         as_stream(stream), 0, G, rtol, sigma, ner, rank));
+  KVS_CUDA_TRY(cudaGetLastError());
+  return KVS_OK;
+}
+
+// ---- KVSculpt: block attention targets, ridge values -----------------------
+int kvs_block_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t Hq, int64_t Hkv, int64_t W,
+                        int64_t N, int64_t d, int64_t q_pos0, int64_t n_block, float* Y, float* lse, void* stream) {
+  int rc = validate_shape(Hq, Hkv, W, N, d, q_pos0);
+  if (rc) return rc;
+  if (n_block < 1 || n_block > N) return KVS_ERR_INVALID_ARG;
+  if (!Q || !K || !V || !Y) return KVS_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Y)) return KVS_ERR_INVALID_ARG;
+  const long long rows = (Hq / Hkv) * W;  // one group's stacked query rows
+  const dim3 grid(static_cast<unsigned>(cdiv(rows, kSculptRowsPerCta)), static_cast<unsigned>(Hkv));
+  const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  cudaStream_t st = as_stream(stream);
+  const int G = static_cast<int>(Hq / Hkv);
+  if (d == 64)
+    KVS_CUDA_TRY(launch_k(block_attention_kernel<64>, grid, dim3(256), 0, st, 0, Q, K, V, G, static_cast<int>(W),
+                          static_cast<int>(N), static_cast<int>(q_pos0), static_cast<int>(n_block), scale, Y, lse));
+  else
+    KVS_CUDA_TRY(launch_k(block_attention_kernel<128>, grid, dim3(256), 0, st, 0, Q, K, V, G, static_cast<int>(W),
+                          static_cast<int>(N), static_cast<int>(q_pos0), static_cast<int>(n_block), scale, Y, lse));
+  KVS_CUDA_TRY(cudaGetLastError());
+  return KVS_OK;
+}
+
+namespace {
+int ridge_check(int64_t Hkv, int64_t R, int64_t k, int64_t d) {
+  if (Hkv <= 0 || R <= 0 || k <= 0 || d <= 0) return KVS_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return KVS_ERR_UNSUPPORTED;
+  if (k > kRidgeMaxK || Hkv >= 65536 || Hkv * R * k >= (1ll << 40) || R >= (1ll << 31)) return KVS_ERR_UNSUPPORTED;
+  return KVS_OK;
+}
+
+// A [Hkv, R, k], then M [Hkv, k, k] and B [Hkv, k, d], each 256-byte aligned
+size_t carve_ridge(int64_t Hkv, int64_t R, int64_t k, int64_t d, void* base, float** A, float** M, float** B) {
+  WsCarver c{static_cast<char*>(base), 0, 0};
+  *A = c.take<float>(static_cast<size_t>(Hkv * R * k));
+  *M = c.take<float>(static_cast<size_t>(Hkv * k * k));
+  *B = c.take<float>(static_cast<size_t>(Hkv * k * d));
+  return c.used;
+}
+}  // namespace
+
+size_t kvs_ridge_values_workspace_size(int64_t Hkv, int64_t R, int64_t k, int64_t d) {
+  if (ridge_check(Hkv, R, k, d) != KVS_OK) return 0;
+  float *A, *M, *B;
+  return carve_ridge(Hkv, R, k, d, nullptr, &A, &M, &B);
+}
+
+int kvs_ridge_values(const uint16_t* Qt, const uint16_t* Kc, const float* Y, int64_t Hkv, int64_t R, int64_t k,
+                     int64_t d, float lam, float* Vc, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = ridge_check(Hkv, R, k, d);
+  if (rc) return rc;
+  if (!(lam > 0.f) || !std::isfinite(lam)) return KVS_ERR_INVALID_ARG;
+  if (!Qt || !Kc || !Y || !Vc) return KVS_ERR_INVALID_ARG;
+  if (!aligned16(Qt) || !aligned16(Kc) || !aligned16(Y) || !aligned16(Vc)) return KVS_ERR_INVALID_ARG;
+  float *A, *M, *B;
+  const size_t need = carve_ridge(Hkv, R, k, d, workspace, &A, &M, &B);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return KVS_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  const dim3 gs(static_cast<unsigned>(cdiv(R, kSculptRowsPerCta)), static_cast<unsigned>(Hkv));
+  const int Ri = static_cast<int>(R), ki = static_cast<int>(k), di = static_cast<int>(d);
+  if (d == 64)
+    KVS_CUDA_TRY(launch_k(ridge_softmax_kernel<64>, gs, dim3(256), 0, st, 0, Qt, Kc, Ri, ki, scale, A));
+  else
+    KVS_CUDA_TRY(launch_k(ridge_softmax_kernel<128>, gs, dim3(256), 0, st, 0, Qt, Kc, Ri, ki, scale, A));
+  const unsigned kt = static_cast<unsigned>(cdiv(k, 32)), dt = static_cast<unsigned>(cdiv(d, 32));
+  KVS_CUDA_TRY(launch_k(ridge_atb_kernel, dim3(kt, kt, static_cast<unsigned>(Hkv)), dim3(256), 0, st, 0,
+                        static_cast<const float*>(A), static_cast<const float*>(A), Ri, ki, ki, lam, 1, M));
+  KVS_CUDA_TRY(launch_k(ridge_atb_kernel, dim3(dt, kt, static_cast<unsigned>(Hkv)), dim3(256), 0, st, 0,
+                        static_cast<const float*>(A), Y, Ri, ki, di, lam, 0, B));
+  KVS_CUDA_TRY(launch_k(ridge_solve_kernel, dim3(static_cast<unsigned>(Hkv)), dim3(kRidgeSolveThreads), 0, st, 0, M,
+                        B, ki, di, Vc));
   KVS_CUDA_TRY(cudaGetLastError());
   return KVS_OK;
 }

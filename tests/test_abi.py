@@ -148,3 +148,31 @@ def test_block_lse_argument_errors(lib):
     assert lib.kvs_block_lse(p, p, 32, 8, 512, 8192, 128, 7680, 0, p, p, 1 << 30, None) == 1
     assert lib.kvs_block_lse(p, p, 32, 8, 512, 8192, 96, 7680, 100, p, p, 1 << 30, None) == 2
     assert lib.kvs_block_lse(p, p, 32, 8, 512, 8192, 128, 7681, 100, p, p, 1 << 30, None) == 1  # window past N
+
+
+def test_sculpt_sizes_and_argument_errors(lib):
+    # A [Hkv, R, k], A^T A [Hkv, k, k], A^T Y [Hkv, k, d], fp32, each 256-byte aligned
+    assert lib.kvs_ridge_values_workspace_size(8, 2048, 256, 128) == 4 * 8 * (2048 * 256 + 256 * 256 + 256 * 128)
+    assert lib.kvs_ridge_values_workspace_size(1, 3, 5, 64) == 256 + 256 + 4 * 5 * 64
+    assert lib.kvs_ridge_values_workspace_size(8, 2048, 513, 128) == 0     # k above 512
+    assert lib.kvs_ridge_values_workspace_size(8, 2048, 256, 96) == 0      # d outside {64, 128}
+    assert lib.kvs_ridge_values_workspace_size(8, 0, 256, 128) == 0
+    p = ctypes.c_void_p(1 << 20)
+    lam = ctypes.c_float(0.1)
+    rv = lib.kvs_ridge_values
+    assert rv(None, p, p, 8, 2048, 256, 128, lam, p, p, 1 << 30, None) == 1
+    assert rv(p, p, p, 8, 2048, 256, 128, ctypes.c_float(0.0), p, p, 1 << 30, None) == 1       # lam must be > 0
+    assert rv(p, p, p, 8, 2048, 256, 128, ctypes.c_float(float("inf")), p, p, 1 << 30, None) == 1
+    assert rv(p, p, p, 8, 2048, 256, 128, ctypes.c_float(float("nan")), p, p, 1 << 30, None) == 1
+    assert rv(p, p, p, 8, 2048, 600, 128, lam, p, p, 1 << 30, None) == 2
+    assert rv(p, p, p, 8, 2048, 256, 96, lam, p, p, 1 << 30, None) == 2
+    assert rv(p, p, p, 8, 2048, 256, 128, lam, p, p, 1024, None) == 6                         # workspace too small
+    assert rv(p, p, p, 8, 2048, 256, 128, lam, p, ctypes.c_void_p((1 << 20) + 16), 1 << 30, None) == 6  # misaligned
+    assert rv(ctypes.c_void_p((1 << 20) + 2), p, p, 8, 2048, 256, 128, lam, p, p, 1 << 30, None) == 1
+    ba = lib.kvs_block_attention
+    assert ba(p, p, p, 32, 8, 512, 8192, 128, 7680, 0, p, None, None) == 1        # empty block
+    assert ba(p, p, p, 32, 8, 512, 8192, 128, 7680, 8193, p, None, None) == 1     # past the cache
+    assert ba(p, p, None, 32, 8, 512, 8192, 128, 7680, 100, p, None, None) == 1   # no V
+    assert ba(p, p, p, 32, 8, 512, 8192, 128, 7680, 100, None, None, None) == 1   # no Y
+    assert ba(p, p, p, 32, 8, 512, 8192, 96, 7680, 100, p, None, None) == 2
+    assert ba(p, p, p, 32, 8, 512, 8192, 128, 7681, 100, p, None, None) == 1      # window past N
