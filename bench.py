@@ -48,6 +48,8 @@ def parse_args(argv=None):
                     help="time one TriZone decode step over the workload's compressed pool instead")
     ap.add_argument("--core", action="store_true",
                     help="time the KV-CoRE Gram accumulation and spectrum of the workload's K cache instead")
+    ap.add_argument("--sculpt", action="store_true",
+                    help="time KVSculpt's zone targets (block attention) and ridge values instead")
     return ap.parse_args(argv)
 
 
@@ -158,6 +160,14 @@ def measured_peaks():
         d = json.load(open(p))
         return d.get("bf16_tflops"), d.get("hbm_gbs"), "measured"
     return 1800.0, 6400.0, "fallback"
+
+
+def fma_clock_mhz() -> float:
+    """The SM clock the fp32 FMA peak is taken at: the measured maximum."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p)).get("sm_max_mhz", 2032.0))
+    return 2032.0
 
 
 # the sources that define the scoring passes: their kernels and their launch plan
@@ -612,6 +622,80 @@ def run_core(args):
     return 0
 
 
+def run_sculpt(args):
+    """KVSculpt over the workload's compression zone (all but the window): the
+    targets Y and lse of the window queries over the zone (kvs_block_attention)
+    and the ridge values of 512 compressed pairs per KV head whose keys are
+    every (zone / 512)-th key of the zone (kvs_ridge_values), each timed with
+    events, L2 flushed before each step.  The block attention runs on the
+    tensor cores (bf16 products, fp32 sums), the ridge on the FMA pipes."""
+    import torch
+    from kv_cache_compression_flash_b300 import _lib as L
+    from kv_cache_compression_flash_b300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    dev = torch.device("cuda", 0)
+    t = synth.make_layer(wl)
+    Q, K, V = t["Q"].to(dev), t["K"].to(dev), t["V"].to(dev)
+    n_block = wl.N - wl.W
+    G = wl.Hq // wl.Hkv
+    R, k = G * wl.W, min(512, n_block)
+    stride = max(1, n_block // k)
+    Kc = K[:, :n_block:stride][:, :k].contiguous()
+    lam = 0.05 * R / k  # a twentieth of lambda_max(A^T A) when the attention is spread evenly
+    Y = torch.empty(wl.Hq, wl.W, wl.d, dtype=torch.float32, device=dev)
+    Vc = torch.empty(wl.Hkv, k, wl.d, dtype=torch.float32, device=dev)
+    ws = L.Workspace()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record()
+        _, lse = L.block_attention(Q, K, V, n_block, q_pos0=wl.q_pos0, out=Y)
+        if evs:
+            evs[1].record()
+        L.ridge_values(Q.view(wl.Hkv, R, wl.d), Kc, Y.view(wl.Hkv, R, wl.d), lam, out=Vc, ws=ws)
+        if evs:
+            evs[2].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ta, tr = [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        step(evs)
+        torch.cuda.synchronize()
+        ta.append(evs[0].elapsed_time(evs[1]) * 1e3)
+        tr.append(evs[1].elapsed_time(evs[2]) * 1e3)
+    if L.device_error() != 0:
+        raise SystemExit("device error")
+    attn_us, ridge_us = statistics.median(ta), statistics.median(tr)
+    # algorithmic flops: q.k and p.v per visible (row, key) pair; the ridge's
+    # logits, A^T A, A^T Y, Cholesky and the two triangular solves
+    n_vis = sum(min(n_block, wl.q_pos0 + r + 1) for r in range(wl.W))
+    attn_flops = 4.0 * wl.Hq * n_vis * wl.d
+    ridge_flops = wl.Hkv * (2.0 * R * k * wl.d + 2.0 * R * k * k + 2.0 * R * k * wl.d + k ** 3 / 3.0
+                            + 2.0 * k * k * wl.d)
+    peak_tf, _, peak_kind = measured_peaks()
+    print(json.dumps({
+        "metric": "KVSculpt zone targets + ridge values (all KV heads)", "value": attn_us + ridge_us, "unit": "us",
+        "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": wl.name, "Hq": wl.Hq, "Hkv": wl.Hkv, "W": wl.W, "N": wl.N,
+                                        "d": wl.d, "n_block": n_block, "R": R, "k": k,
+                                        "l2": "flushed before each step (untimed)"},
+        "block_attention_us": attn_us, "ridge_values_us": ridge_us,
+        "roofline": {"bound": "tensor", "achieved": attn_flops / (attn_us * 1e-6) / 1e12, "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": attn_flops / (attn_us * 1e-6) / 1e12 / peak_tf,
+                     "peak_kind": f"{peak_kind} bf16 dense", "kernel": "block_attention_kernel",
+                     "algorithmic_flops": attn_flops},
+        "ridge_tflops": ridge_flops / (ridge_us * 1e-6) / 1e12,
+        "ridge_fma_frac": ridge_flops / (ridge_us * 1e-6) / (148 * 128 * 2 * fma_clock_mhz() * 1e6),
+        "gpu_launches": 5 * args.steps,
+    }))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -620,6 +704,8 @@ def main(argv=None):
         return run_trizone(args)
     if args.core:
         return run_core(args)
+    if args.sculpt:
+        return run_sculpt(args)
     return run_ours(args)
 
 

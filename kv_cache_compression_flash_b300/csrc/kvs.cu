@@ -771,17 +771,22 @@ int kvs_block_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
   if (n_block < 1 || n_block > N) return KVS_ERR_INVALID_ARG;
   if (!Q || !K || !V || !Y) return KVS_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Y)) return KVS_ERR_INVALID_ARG;
-  const long long rows = (Hq / Hkv) * W;  // one group's stacked query rows
-  const dim3 grid(static_cast<unsigned>(cdiv(rows, kSculptRowsPerCta)), static_cast<unsigned>(Hkv));
-  const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
-  cudaStream_t st = as_stream(stream);
   const int G = static_cast<int>(Hq / Hkv);
-  if (d == 64)
-    KVS_CUDA_TRY(launch_k(block_attention_kernel<64>, grid, dim3(256), 0, st, 0, Q, K, V, G, static_cast<int>(W),
-                          static_cast<int>(N), static_cast<int>(q_pos0), static_cast<int>(n_block), scale, Y, lse));
-  else
-    KVS_CUDA_TRY(launch_k(block_attention_kernel<128>, grid, dim3(256), 0, st, 0, Q, K, V, G, static_cast<int>(W),
-                          static_cast<int>(N), static_cast<int>(q_pos0), static_cast<int>(n_block), scale, Y, lse));
+  const int Gt = (G == 1 || G == 2 || G == 4) ? G : (G % 4 == 0 ? 4 : 1);  // heads per CTA: 64 / Gt positions each
+  const dim3 grid(static_cast<unsigned>(cdiv(W, 64 / Gt)), static_cast<unsigned>(Hkv * (G / Gt)));
+  const float c_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  cudaStream_t st = as_stream(stream);
+  const int Wi = static_cast<int>(W), Ni = static_cast<int>(N), p0 = static_cast<int>(q_pos0),
+            nb = static_cast<int>(n_block);
+  if (d == 64) {
+    KVS_CUDA_TRY(allow_smem(block_attention_kernel<64>, BaCfg<64>::kSmem));
+    KVS_CUDA_TRY(launch_k(block_attention_kernel<64>, grid, dim3(kBaThreads), BaCfg<64>::kSmem, st, 0, Q, K, V, G,
+                          Gt, Wi, Ni, p0, nb, c_log2, Y, lse));
+  } else {
+    KVS_CUDA_TRY(allow_smem(block_attention_kernel<128>, BaCfg<128>::kSmem));
+    KVS_CUDA_TRY(launch_k(block_attention_kernel<128>, grid, dim3(kBaThreads), BaCfg<128>::kSmem, st, 0, Q, K, V, G,
+                          Gt, Wi, Ni, p0, nb, c_log2, Y, lse));
+  }
   KVS_CUDA_TRY(cudaGetLastError());
   return KVS_OK;
 }
@@ -834,8 +839,10 @@ int kvs_ridge_values(const uint16_t* Qt, const uint16_t* Kc, const float* Y, int
                         static_cast<const float*>(A), static_cast<const float*>(A), Ri, ki, ki, lam, 1, M));
   KVS_CUDA_TRY(launch_k(ridge_atb_kernel, dim3(dt, kt, static_cast<unsigned>(Hkv)), dim3(256), 0, st, 0,
                         static_cast<const float*>(A), Y, Ri, ki, di, lam, 0, B));
-  KVS_CUDA_TRY(launch_k(ridge_solve_kernel, dim3(static_cast<unsigned>(Hkv)), dim3(kRidgeSolveThreads), 0, st, 0, M,
-                        B, ki, di, Vc));
+  const size_t solve_smem = ridge_solve_smem(ki);
+  KVS_CUDA_TRY(allow_smem(ridge_solve_kernel, solve_smem));
+  KVS_CUDA_TRY(launch_k(ridge_solve_kernel, dim3(static_cast<unsigned>(Hkv)), dim3(kRidgeSolveThreads), solve_smem,
+                        st, 0, M, B, ki, di, Vc));
   KVS_CUDA_TRY(cudaGetLastError());
   return KVS_OK;
 }

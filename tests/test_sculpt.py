@@ -71,8 +71,9 @@ def test_block_attention_vs_oracle(Hq, Hkv, W, N, d, q_pos0, n_block):
     Yr, lser = O.block_attention(Q64, K64, V64, q_pos0, n_block)
     check_block_attention(Y.cpu().numpy(), lse.cpu().numpy(), Yr, lser, d,
                           logit_scale(Q64, K64[:, :n_block]), n_block, np.abs(V64[:, :n_block]).max())
-    if n_block == 1:
-        assert torch.equal(Y.cpu(), V[:, :1].float().repeat_interleave(Hq // Hkv, 0).expand(Hq, W, d))
+    if n_block == 1:  # one key: its weight is 1 and Y is its value row (to the rounding of 1 / l)
+        v0 = V[:, :1].float().repeat_interleave(Hq // Hkv, 0).expand(Hq, W, d).numpy()
+        assert np.abs(Y.cpu().numpy() - v0).max() <= 4 * U * np.abs(v0).max()
     # the block LSE kernel (tensor-core logits) agrees within its own tolerance
     lse_only = L.block_lse(Q.to(DEV), K.to(DEV), n_block, q_pos0=q_pos0).cpu().numpy()
     assert (np.abs(lse_only - lse.cpu().numpy()) <= 2e-3 * np.maximum(1.0, np.abs(lser))).all()
