@@ -827,18 +827,23 @@ int kvs_ridge_values(const uint16_t* Qt, const uint16_t* Kc, const float* Y, int
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return KVS_ERR_WORKSPACE;
   cudaStream_t st = as_stream(stream);
-  const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
-  const dim3 gs(static_cast<unsigned>(cdiv(R, kSculptRowsPerCta)), static_cast<unsigned>(Hkv));
+  const float c_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  const dim3 gs(static_cast<unsigned>(cdiv(R, 64)), static_cast<unsigned>(Hkv));
   const int Ri = static_cast<int>(R), ki = static_cast<int>(k), di = static_cast<int>(d);
-  if (d == 64)
-    KVS_CUDA_TRY(launch_k(ridge_softmax_kernel<64>, gs, dim3(256), 0, st, 0, Qt, Kc, Ri, ki, scale, A));
-  else
-    KVS_CUDA_TRY(launch_k(ridge_softmax_kernel<128>, gs, dim3(256), 0, st, 0, Qt, Kc, Ri, ki, scale, A));
-  const unsigned kt = static_cast<unsigned>(cdiv(k, 32)), dt = static_cast<unsigned>(cdiv(d, 32));
+  if (d == 64) {
+    KVS_CUDA_TRY(allow_smem(ridge_softmax_kernel<64>, RsCfg<64>::kSmem));
+    KVS_CUDA_TRY(launch_k(ridge_softmax_kernel<64>, gs, dim3(kBaThreads), RsCfg<64>::kSmem, st, 0, Qt, Kc, Ri, ki,
+                          c_log2, A));
+  } else {
+    KVS_CUDA_TRY(allow_smem(ridge_softmax_kernel<128>, RsCfg<128>::kSmem));
+    KVS_CUDA_TRY(launch_k(ridge_softmax_kernel<128>, gs, dim3(kBaThreads), RsCfg<128>::kSmem, st, 0, Qt, Kc, Ri, ki,
+                          c_log2, A));
+  }
+  const unsigned kt = static_cast<unsigned>(cdiv(k, kAtbTile)), dt = static_cast<unsigned>(cdiv(d, kAtbTile));
   KVS_CUDA_TRY(launch_k(ridge_atb_kernel, dim3(kt, kt, static_cast<unsigned>(Hkv)), dim3(256), 0, st, 0,
-                        static_cast<const float*>(A), static_cast<const float*>(A), Ri, ki, ki, lam, 1, M));
+                        static_cast<const float*>(A), static_cast<const float*>(A), Ri, ki, ki, lam, 1, 1, M));
   KVS_CUDA_TRY(launch_k(ridge_atb_kernel, dim3(dt, kt, static_cast<unsigned>(Hkv)), dim3(256), 0, st, 0,
-                        static_cast<const float*>(A), Y, Ri, ki, di, lam, 0, B));
+                        static_cast<const float*>(A), Y, Ri, ki, di, lam, 0, 0, B));
   const size_t solve_smem = ridge_solve_smem(ki);
   KVS_CUDA_TRY(allow_smem(ridge_solve_kernel, solve_smem));
   KVS_CUDA_TRY(launch_k(ridge_solve_kernel, dim3(static_cast<unsigned>(Hkv)), dim3(kRidgeSolveThreads), solve_smem,

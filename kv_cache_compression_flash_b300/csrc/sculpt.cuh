@@ -8,16 +8,17 @@
 //       CTA, keys in chunks of 64 staged by cp.async, an online softmax, and
 //       the P V product with P split into bf16 hi + lo so that the weights
 //       keep 16 significant bits.  Row r sees keys t < n_block, t <= q_pos0 + r.
-//   ridge_softmax_kernel<DH>    grid (ceil(R/8), Hkv), 256 threads: one warp
-//       per training query, lane l holds the logits of keys l, l+32, ...;
-//       A = softmax over all k compressed keys (no mask: every training query
-//       sees the whole compressed block).
-//   ridge_atb_kernel            C = P^T Q (+ lam I), 32 x 32 output tiles over
-//       32-row slices of P [R, m] and Q [R, n]: gives A^T A + lam I and A^T Y.
+//   ridge_softmax_kernel<DH>    A = softmax over all k compressed keys (no
+//       mask: every training query sees the whole compressed block), the
+//       logits on the tensor cores as in the block attention, in two sweeps
+//       over the keys (row max and sum, then the weights).
+//   ridge_atb_kernel            C = P^T Q (+ lam I), 64 x 64 output tiles with
+//       4 x 4 per thread over 16-row slices of P [R, m] and Q [R, n]: gives
+//       A^T A + lam I (lower triangle) and A^T Y.
 //   ridge_solve_kernel          one CTA per head: Cholesky of A^T A + lam I in
 //       place by panels of 32 columns, then the forward and backward
 //       substitutions for the d right-hand sides, also by blocks of 32 rows.
-// The ridge kernels are fp32 throughout, on the FMA pipes.
+// A^T A, A^T Y and the solve are fp32 on the FMA pipes.
 #pragma once
 
 #include "common.cuh"
@@ -27,40 +28,6 @@ namespace kvs {
 constexpr int kRidgeMaxK = 512;
 constexpr int kRidgeMaxD = 128;
 constexpr int kRidgeSolveThreads = 1024;
-constexpr int kSculptRowsPerCta = 8;
-
-__device__ __forceinline__ float sculpt_bf16(uint16_t v) { return __uint_as_float(static_cast<uint32_t>(v) << 16); }
-
-// q . k for one bf16 key row of DH channels, q pre-scaled in shared memory
-template <int DH>
-__device__ __forceinline__ float sculpt_dot(const uint16_t* __restrict__ krow, const float* q) {
-  const uint4* kr = reinterpret_cast<const uint4*>(krow);
-  float acc = 0.f;
-#pragma unroll 4
-  for (int c8 = 0; c8 < DH / 8; ++c8) {
-    const uint4 v = __ldg(kr + c8);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      acc = fmaf(__uint_as_float(w[e] << 16), q[8 * c8 + 2 * e], acc);
-      acc = fmaf(__uint_as_float(w[e] & 0xffff0000u), q[8 * c8 + 2 * e + 1], acc);
-    }
-  }
-  return acc;
-}
-
-__device__ __forceinline__ float warp_max_f(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-__device__ __forceinline__ float warp_sum_f(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
 // ---- block attention on the tensor cores (mma.sync m16n8k16, bf16 -> fp32) ----
 constexpr int kBaThreads = 128;  // 4 warps x 16 query rows
 constexpr int kBaKeys = 64;      // keys per chunk
@@ -287,86 +254,207 @@ __global__ void __launch_bounds__(kBaThreads) block_attention_kernel(
   }
 }
 
-// A[g][r][i] = softmax_i(Qt[g][r] . Kc[g][i] * scale), one warp per row r
+// A[g][r][i] = softmax_i(Qt[g][r] . Kc[g][i] / sqrt(d)) over the k compressed keys.
+// grid (ceil(R / 64), Hkv), 128 threads, 16 rows a warp; the logits come from
+// mma.sync as in the block attention, over chunks of 64 keys (cp.async,
+// double-buffered, rows past k clamped and masked), in two sweeps: the row max
+// and sum, then the normalised weights written to A.
 template <int DH>
-__global__ void __launch_bounds__(256) ridge_softmax_kernel(const uint16_t* __restrict__ Qt,
-                                                            const uint16_t* __restrict__ Kc, int R, int k,
-                                                            float scale, float* __restrict__ A) {
+struct RsCfg {
+  static constexpr int kLd = DH + 8;
+  static constexpr int kTileElems = kBaKeys * kLd;
+  static constexpr size_t kSmem = 2ull * kTileElems * 2 + 128;
+};
+
+template <int DH>
+__global__ void __launch_bounds__(kBaThreads) ridge_softmax_kernel(const uint16_t* __restrict__ Qt,
+                                                                   const uint16_t* __restrict__ Kc, int R, int k,
+                                                                   float c_log2, float* __restrict__ A) {
+  constexpr int kLd = RsCfg<DH>::kLd, kTile = RsCfg<DH>::kTileElems;
+  constexpr int KS = DH / 16;
+  constexpr int kChunks16 = DH / 8;
+  extern __shared__ uint8_t rs_raw[];
+  uint16_t* sm = reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(rs_raw) + 127) & ~uintptr_t(127));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = lane >> 2, qi = lane & 3;
+  const int g = blockIdx.y;
+  const int rw = blockIdx.x * 64 + warp * 16;  // the warp's first row
+  const int r_lo = min(rw + quad, R - 1), r_hi = min(rw + quad + 8, R - 1);
+  const bool st_lo = rw + quad < R, st_hi = rw + quad + 8 < R;
+  const int n_chunks = (k + kBaKeys - 1) / kBaKeys;
+  const uint16_t* Kg = Kc + static_cast<long long>(g) * k * DH;
+
   pdl_wait();
   pdl_trigger();
-  __shared__ float qs[kSculptRowsPerCta][DH];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = blockIdx.y;
-  const int r = blockIdx.x * kSculptRowsPerCta + warp;
-  if (r >= R) return;  // whole warps leave; no block barrier follows
-  const uint16_t* q = Qt + (static_cast<long long>(g) * R + r) * DH;
-  for (int c = lane; c < DH; c += 32) qs[warp][c] = sculpt_bf16(q[c]) * scale;
-  __syncwarp();
-  constexpr int kPer = kRidgeMaxK / 32;
-  float s[kPer];
-  float m = -INFINITY;
+  auto load_chunk = [&](int ch, int buf) {
+    const int t0 = ch * kBaKeys;
+    for (int e = tid; e < kBaKeys * kChunks16; e += kBaThreads) {
+      const int row = e / kChunks16, piece = e % kChunks16;
+      ba_cp16(smem_u32(sm + buf * kTile + row * kLd + piece * 8),
+              Kg + static_cast<long long>(min(t0 + row, k - 1)) * DH + piece * 8);
+    }
+    ba_commit();
+  };
+  load_chunk(0, 0);
+  uint32_t qf[KS][4];
+  {
+    const uint16_t* q_lo = Qt + (static_cast<long long>(g) * R + r_lo) * DH + 2 * qi;
+    const uint16_t* q_hi = Qt + (static_cast<long long>(g) * R + r_hi) * DH + 2 * qi;
 #pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int i = lane + 32 * u;
-    s[u] = -INFINITY;
-    if (i < k) {
-      s[u] = sculpt_dot<DH>(Kc + (static_cast<long long>(g) * k + i) * DH, qs[warp]);
-      m = fmaxf(m, s[u]);
+    for (int ks = 0; ks < KS; ++ks) {
+      qf[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(q_lo + 16 * ks));
+      qf[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(q_hi + 16 * ks));
+      qf[ks][2] = __ldg(reinterpret_cast<const uint32_t*>(q_lo + 16 * ks + 8));
+      qf[ks][3] = __ldg(reinterpret_cast<const uint32_t*>(q_hi + 16 * ks + 8));
     }
   }
-  m = warp_max_f(m);
-  float sum = 0.f;
+  const int mi = lane >> 3, mr = lane & 7;
+  const int k_row = (mi >> 1) * 8 + mr, k_col = (mi & 1) * 8;
+  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+  float* a_lo = A + (static_cast<long long>(g) * R + r_lo) * k;
+  float* a_hi = A + (static_cast<long long>(g) * R + r_hi) * k;
+  const int n_it = 2 * n_chunks;
+  for (int it = 0; it < n_it; ++it) {
+    const int buf = it & 1, ch = it % n_chunks;
+    if (it + 1 < n_it) {
+      load_chunk((it + 1) % n_chunks, buf ^ 1);
+      ba_wait<1>();
+    } else {
+      ba_wait<0>();
+    }
+    __syncthreads();
+    const uint32_t kbase = smem_u32(sm + buf * kTile);
+    float s[8][4];
 #pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    s[u] = lane + 32 * u < k ? expf(s[u] - m) : 0.f;
-    sum += s[u];
-  }
-  const float inv = 1.f / warp_sum_f(sum);  // the row maximum contributes 1
-  float* a = A + (static_cast<long long>(g) * R + r) * k;
+    for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
 #pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int i = lane + 32 * u;
-    if (i < k) a[i] = s[u] * inv;
+    for (int n2 = 0; n2 < 4; ++n2) {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        ba_ldsm4(kbase + ((16 * n2 + k_row) * kLd + 16 * ks + k_col) * 2, b0, b1, b2, b3);
+        ba_mma(s[2 * n2], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
+        ba_mma(s[2 * n2 + 1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
+      }
+    }
+    const int t0 = ch * kBaKeys;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int t = t0 + 8 * j + 2 * qi;
+      s[j][0] = t < k ? s[j][0] * c_log2 : -INFINITY;
+      s[j][1] = t + 1 < k ? s[j][1] * c_log2 : -INFINITY;
+      s[j][2] = t < k ? s[j][2] * c_log2 : -INFINITY;
+      s[j][3] = t + 1 < k ? s[j][3] * c_log2 : -INFINITY;
+    }
+    if (it < n_chunks) {  // sweep 1: the row max and sum
+      float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        mx_lo = fmaxf(mx_lo, fmaxf(s[j][0], s[j][1]));
+        mx_hi = fmaxf(mx_hi, fmaxf(s[j][2], s[j][3]));
+      }
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);  // finite: key 0 is in chunk 0
+      float ps_lo = 0.f, ps_hi = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        ps_lo += exp2f(s[j][0] - mn_lo) + exp2f(s[j][1] - mn_lo);
+        ps_hi += exp2f(s[j][2] - mn_hi) + exp2f(s[j][3] - mn_hi);
+      }
+      l_lo = l_lo * exp2f(m_lo - mn_lo) + ps_lo;
+      l_hi = l_hi * exp2f(m_hi - mn_hi) + ps_hi;
+      m_lo = mn_lo;
+      m_hi = mn_hi;
+      if (it == n_chunks - 1) {  // the full row sums, then their reciprocals
+        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+        l_lo = 1.f / l_lo;
+        l_hi = 1.f / l_hi;
+      }
+    } else {  // sweep 2: the weights
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int t = t0 + 8 * j + 2 * qi;
+        if (st_lo && t < k) a_lo[t] = exp2f(s[j][0] - m_lo) * l_lo;
+        if (st_lo && t + 1 < k) a_lo[t + 1] = exp2f(s[j][1] - m_lo) * l_lo;
+        if (st_hi && t < k) a_hi[t] = exp2f(s[j][2] - m_hi) * l_hi;
+        if (st_hi && t + 1 < k) a_hi[t + 1] = exp2f(s[j][3] - m_hi) * l_hi;
+      }
+    }
+    __syncthreads();  // every warp is done with this buffer before it is refilled
   }
 }
 
 // C[g][i][j] = sum_r P[g][r][i] Q[g][r][j]  (+ lam on the diagonal when add_diag)
-// grid (ceil(n/32), ceil(m/32), Hkv), 256 threads: thread (ty, tx) owns rows
-// ty, ty+8, ty+16, ty+24 of column tx of the 32 x 32 tile
+// grid (ceil(n/64), ceil(m/64), Hkv), 256 threads: a 64 x 64 output tile,
+// thread (ty, tx) = (tid / 16, tid % 16) owns rows 4 ty .. 4 ty + 3 and columns
+// 4 tx .. 4 tx + 3; slices of 16 rows of P and Q pass through shared memory,
+// the next slice's loads in flight while the current one is multiplied.  With
+// lower_only, tiles wholly above the diagonal are skipped: the solve reads only
+// the lower triangle of A^T A + lam I.
+constexpr int kAtbTile = 64, kAtbSlice = 16;
+
 __global__ void __launch_bounds__(256) ridge_atb_kernel(const float* __restrict__ P, const float* __restrict__ Q,
-                                                        int R, int m, int n, float lam, int add_diag,
+                                                        int R, int m, int n, float lam, int add_diag, int lower_only,
                                                         float* __restrict__ C) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float ps[32][33], qs[32][33];
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int i0 = blockIdx.y * kAtbTile, j0 = blockIdx.x * kAtbTile;
+  if (lower_only != 0 && j0 > i0 + kAtbTile - 1) return;  // the whole CTA, before any barrier
+  __shared__ __align__(16) float ps[kAtbSlice][kAtbTile];
+  __shared__ __align__(16) float qs[kAtbSlice][kAtbTile];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int g = blockIdx.z;
-  const int i0 = blockIdx.y * 32, j0 = blockIdx.x * 32;
   const float* Pg = P + static_cast<long long>(g) * R * m;
   const float* Qg = Q + static_cast<long long>(g) * R * n;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int r0 = 0; r0 < R; r0 += 32) {
-    __syncthreads();
-    for (int e = threadIdx.x; e < 32 * 32; e += 256) {
-      const int rr = e >> 5, cc = e & 31;
-      const int r = r0 + rr;
-      ps[rr][cc] = (r < R && i0 + cc < m) ? Pg[static_cast<long long>(r) * m + i0 + cc] : 0.f;
-      qs[rr][cc] = (r < R && j0 + cc < n) ? Qg[static_cast<long long>(r) * n + j0 + cc] : 0.f;
+  // this thread's four loads per slice: element e = tid + 256 u -> row e / 64, column e % 64
+  float pv[4], qv[4];
+  auto fetch = [&](int r0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = tid + 256 * u, rr = e >> 6, cc = e & 63, r = r0 + rr;
+      pv[u] = (r < R && i0 + cc < m) ? Pg[static_cast<long long>(r) * m + i0 + cc] : 0.f;
+      qv[u] = (r < R && j0 + cc < n) ? Qg[static_cast<long long>(r) * n + j0 + cc] : 0.f;
+    }
+  };
+  float acc[4][4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
+  fetch(0);
+  for (int r0 = 0; r0 < R; r0 += kAtbSlice) {
+    __syncthreads();  // the previous slice is consumed
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = tid + 256 * u;
+      ps[e >> 6][e & 63] = pv[u];
+      qs[e >> 6][e & 63] = qv[u];
     }
     __syncthreads();
-#pragma unroll 8
-    for (int rr = 0; rr < 32; ++rr) {
-      const float qv = qs[rr][tx];
+    if (r0 + kAtbSlice < R) fetch(r0 + kAtbSlice);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) acc[u] = fmaf(ps[rr][ty + 8 * u], qv, acc[u]);
+    for (int rr = 0; rr < kAtbSlice; ++rr) {
+      const float4 a = *reinterpret_cast<const float4*>(&ps[rr][4 * ty]);
+      const float4 b = *reinterpret_cast<const float4*>(&qs[rr][4 * tx]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
     }
   }
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int i = i0 + ty + 8 * u, j = j0 + tx;
-    if (i < m && j < n)
-      C[(static_cast<long long>(g) * m + i) * n + j] = acc[u] + ((add_diag != 0 && i == j) ? lam : 0.f);
-  }
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int i = i0 + 4 * ty + u, j = j0 + 4 * tx + v;
+      if (i < m && j < n)
+        C[(static_cast<long long>(g) * m + i) * n + j] = acc[u][v] + ((add_diag != 0 && i == j) ? lam : 0.f);
+    }
 }
 
 // In place: the lower triangle of M[g] (k x k) becomes its Cholesky factor L,
@@ -411,26 +499,32 @@ __global__ void __launch_bounds__(kRidgeSolveThreads) ridge_solve_kernel(float* 
       s_diag[r][c] = (r < nb && c <= r) ? Mg[static_cast<long long>(J + r) * k + J + c] : 0.f;
     }
     __syncthreads();
-    if (warp == 0) {  // lane r owns row r of the diagonal block
-      for (int c = 0; c < nb; ++c) {
-        const float p = s_diag[c][c];
-        if (!(p > 0.f)) {  // the same value in every lane
-          if (lane == 0) s_bad = 1;
-          break;
+    if (warp == 0) {  // lane r holds row r of the diagonal block in registers
+      float a[kCholNb];
+#pragma unroll
+      for (int c = 0; c < kCholNb; ++c) a[c] = s_diag[lane][c];
+      bool bad = false;
+#pragma unroll
+      for (int c = 0; c < kCholNb; ++c) {
+        if (c < nb) {  // the same in every lane
+          const float p = __shfl_sync(0xffffffffu, a[c], c);
+          bad |= !(p > 0.f);  // the same in every lane
+          const float piv = p > 0.f ? sqrtf(p) : 1.f;
+          a[c] = lane == c ? piv : (lane > c ? a[c] / piv : a[c]);
+          // rows below c take column c's rank-1 update: a[c2] -= L[lane][c] L[c2][c]
+#pragma unroll
+          for (int c2 = c + 1; c2 < kCholNb; ++c2) {
+            const float l = __shfl_sync(0xffffffffu, a[c], c2);
+            if (lane >= c2) a[c2] = fmaf(-a[c], l, a[c2]);
+          }
         }
-        const float piv = sqrtf(p);
-        __syncwarp();
-        if (lane == c) s_diag[c][c] = piv;
-        if (lane > c && lane < nb) s_diag[lane][c] /= piv;
-        __syncwarp();
-        if (lane > c && lane < nb) {
-          const float lrc = s_diag[lane][c];
-          for (int c2 = c + 1; c2 <= lane; ++c2) s_diag[lane][c2] = fmaf(-lrc, s_diag[c2][c], s_diag[lane][c2]);
-        }
-        __syncwarp();
       }
-      if (lane < nb)
-        for (int c = 0; c <= lane; ++c) Mg[static_cast<long long>(J + lane) * k + J + c] = s_diag[lane][c];
+      if (bad && lane == 0) s_bad = 1;
+#pragma unroll
+      for (int c = 0; c < kCholNb; ++c) {
+        s_diag[lane][c] = c <= lane ? a[c] : 0.f;
+        if (c <= lane && lane < nb) Mg[static_cast<long long>(J + lane) * k + J + c] = a[c];
+      }
     }
     __syncthreads();
     if (s_bad) break;  // the same value in every thread after the barrier
@@ -481,12 +575,22 @@ __global__ void __launch_bounds__(kRidgeSolveThreads) ridge_solve_kernel(float* 
       for (int r = warp; r < nb; r += kWarps) {  // row J + r minus its product with the solved rows
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         const int p0 = fwd ? 0 : J + nb, p1 = fwd ? J : k;
-        for (int p = p0; p < p1; ++p) {
-          const float l = fwd ? Mg[static_cast<long long>(J + r) * k + p] : Mg[static_cast<long long>(p) * k + J + r];
-          const float* xp = dst + static_cast<long long>(p) * d + lane;
+        for (int pb = p0; pb < p1; pb += 32) {  // 32 factor entries per load, one per lane, then broadcast
+          const int p = pb + lane;
+          const float lv = p < p1 ? (fwd ? Mg[static_cast<long long>(J + r) * k + p]
+                                         : Mg[static_cast<long long>(p) * k + J + r])
+                                  : 0.f;
+          const int qn = min(32, p1 - pb);
+#pragma unroll 8
+          for (int q = 0; q < 32; ++q) {
+            const float l = __shfl_sync(0xffffffffu, lv, q);
+            if (q < qn) {
+              const float* xp = dst + static_cast<long long>(pb + q) * d + lane;
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (u < nd) acc[u] = fmaf(l, xp[32 * u], acc[u]);
+              for (int u = 0; u < 4; ++u)
+                if (u < nd) acc[u] = fmaf(l, xp[32 * u], acc[u]);
+            }
+          }
         }
         float* out = dst + static_cast<long long>(J + r) * d + lane;
         const float* in = src + static_cast<long long>(J + r) * d + lane;
