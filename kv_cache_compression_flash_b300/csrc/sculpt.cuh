@@ -499,32 +499,26 @@ __global__ void __launch_bounds__(kRidgeSolveThreads) ridge_solve_kernel(float* 
       s_diag[r][c] = (r < nb && c <= r) ? Mg[static_cast<long long>(J + r) * k + J + c] : 0.f;
     }
     __syncthreads();
-    if (warp == 0) {  // lane r holds row r of the diagonal block in registers
-      float a[kCholNb];
-#pragma unroll
-      for (int c = 0; c < kCholNb; ++c) a[c] = s_diag[lane][c];
-      bool bad = false;
-#pragma unroll
-      for (int c = 0; c < kCholNb; ++c) {
-        if (c < nb) {  // the same in every lane
-          const float p = __shfl_sync(0xffffffffu, a[c], c);
-          bad |= !(p > 0.f);  // the same in every lane
-          const float piv = p > 0.f ? sqrtf(p) : 1.f;
-          a[c] = lane == c ? piv : (lane > c ? a[c] / piv : a[c]);
-          // rows below c take column c's rank-1 update: a[c2] -= L[lane][c] L[c2][c]
-#pragma unroll
-          for (int c2 = c + 1; c2 < kCholNb; ++c2) {
-            const float l = __shfl_sync(0xffffffffu, a[c], c2);
-            if (lane >= c2) a[c2] = fmaf(-a[c], l, a[c2]);
-          }
+    if (warp == 0) {  // lane r owns row r of the diagonal block
+      for (int c = 0; c < nb; ++c) {
+        const float p = s_diag[c][c];
+        if (!(p > 0.f)) {  // the same value in every lane
+          if (lane == 0) s_bad = 1;
+          break;
         }
+        const float piv = sqrtf(p);
+        __syncwarp();
+        if (lane == c) s_diag[c][c] = piv;
+        if (lane > c && lane < nb) s_diag[lane][c] /= piv;
+        __syncwarp();
+        if (lane > c && lane < nb) {
+          const float lrc = s_diag[lane][c];
+          for (int c2 = c + 1; c2 <= lane; ++c2) s_diag[lane][c2] = fmaf(-lrc, s_diag[c2][c], s_diag[lane][c2]);
+        }
+        __syncwarp();
       }
-      if (bad && lane == 0) s_bad = 1;
-#pragma unroll
-      for (int c = 0; c < kCholNb; ++c) {
-        s_diag[lane][c] = c <= lane ? a[c] : 0.f;
-        if (c <= lane && lane < nb) Mg[static_cast<long long>(J + lane) * k + J + c] = a[c];
-      }
+      if (lane < nb)
+        for (int c = 0; c <= lane; ++c) Mg[static_cast<long long>(J + lane) * k + J + c] = s_diag[lane][c];
     }
     __syncthreads();
     if (s_bad) break;  // the same value in every thread after the barrier
@@ -575,22 +569,12 @@ __global__ void __launch_bounds__(kRidgeSolveThreads) ridge_solve_kernel(float* 
       for (int r = warp; r < nb; r += kWarps) {  // row J + r minus its product with the solved rows
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         const int p0 = fwd ? 0 : J + nb, p1 = fwd ? J : k;
-        for (int pb = p0; pb < p1; pb += 32) {  // 32 factor entries per load, one per lane, then broadcast
-          const int p = pb + lane;
-          const float lv = p < p1 ? (fwd ? Mg[static_cast<long long>(J + r) * k + p]
-                                         : Mg[static_cast<long long>(p) * k + J + r])
-                                  : 0.f;
-          const int qn = min(32, p1 - pb);
-#pragma unroll 8
-          for (int q = 0; q < 32; ++q) {
-            const float l = __shfl_sync(0xffffffffu, lv, q);
-            if (q < qn) {
-              const float* xp = dst + static_cast<long long>(pb + q) * d + lane;
+        for (int p = p0; p < p1; ++p) {
+          const float l = fwd ? Mg[static_cast<long long>(J + r) * k + p] : Mg[static_cast<long long>(p) * k + J + r];
+          const float* xp = dst + static_cast<long long>(p) * d + lane;
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
-                if (u < nd) acc[u] = fmaf(l, xp[32 * u], acc[u]);
-            }
-          }
+          for (int u = 0; u < 4; ++u)
+            if (u < nd) acc[u] = fmaf(l, xp[32 * u], acc[u]);
         }
         float* out = dst + static_cast<long long>(J + r) * d + lane;
         const float* in = src + static_cast<long long>(J + r) * d + lane;
