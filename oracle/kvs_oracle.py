@@ -610,8 +610,11 @@ def ridge_values(Qt, Kc, Y, lam):
     Qt [R, d] training queries, Kc [k, d] compressed keys, Y [R, d] targets,
     lam > 0.  Returns V_c [k, d].  The linear solve is LAPACK's (a library
     primitive).
-    Pins: one key gives sum(Y) / (R + lam); noiseless targets Y = A V are
-    recovered as lam -> 0; the gradient of the objective vanishes at V_c.
+    Pins: one key gives sum(Y) / (R + lam); k equal keys give sum(Y) /
+    (R + lam k) in every row; two keys a e and 0 under copies of the unit query
+    e give the rank-one closed form with weights logistic(a / sqrt(d));
+    noiseless targets Y = A V are recovered as lam -> 0; the gradient of the
+    objective vanishes at V_c.
     """
     Qt = np.asarray(Qt, dtype=np.float64)
     Kc = np.asarray(Kc, dtype=np.float64)

@@ -612,3 +612,29 @@ def test_ridge_values_pins():
         P = Vc + 1e-3 * rng.standard_normal(Vc.shape)
         f = lambda X: ((A @ X - Y) ** 2).sum() + lam * (X ** 2).sum()
         assert f(P) >= f(Vc)
+
+
+def test_ridge_values_closed_forms():
+    """Two closed forms that fix the softmax and its 1/sqrt(d) scale without
+    restating them   [KVSculpt §2: ridge values for fixed keys].
+    Equal keys: every weight is 1/k, A^T A = (R / k^2) 1 1^T, and every value row
+    is sum(Y) / (R + lam k).  Two keys a e and 0 seen by R copies of the unit
+    query e: the weights are p = logistic(a / sqrt(d)) and 1 - p, so with
+    u = (p, 1 - p) the solution of the rank-one system is u sum(Y)^T / (R |u|^2 + lam)."""
+    rng = np.random.default_rng(53)
+    R, d, k, lam = 12, 16, 5, 0.7
+    Qt = rng.standard_normal((R, d))
+    Y = rng.standard_normal((R, d))
+    Kc = np.repeat(rng.standard_normal((1, d)), k, axis=0)
+    Vc = O.ridge_values(Qt, Kc, Y, lam)
+    np.testing.assert_allclose(Vc, np.broadcast_to(Y.sum(axis=0) / (R + lam * k), (k, d)), rtol=1e-12)
+
+    e = np.zeros(d)
+    e[3] = 1.0
+    a = 2.5
+    Qt = np.repeat(e[None, :], R, axis=0)
+    Kc = np.stack([a * e, np.zeros(d)])
+    p = 1.0 / (1.0 + math.exp(-a / math.sqrt(d)))
+    u = np.array([p, 1.0 - p])
+    expect = np.outer(u, Y.sum(axis=0)) / (R * (u @ u) + lam)
+    np.testing.assert_allclose(O.ridge_values(Qt, Kc, Y, lam), expect, rtol=1e-12)
