@@ -350,9 +350,10 @@ int kvs_spectrum(const float* G, int64_t Hkv, int64_t d, float rtol, float* sigm
  *            rows [0, n_block) of each head are read);
  *   Y      : float [Hq, W, d], written;  lse : float [Hq, W] or NULL.
  * Shapes and errors as kvs_block_lse (1 <= n_block <= N, d in {64, 128});
- * every pointer 16-byte aligned.  No workspace.  fp32 accumulation of the
- * bf16 products (one warp per query row, online softmax over chunks of 32
- * keys).
+ * every pointer 16-byte aligned.  No workspace.  Tensor cores: the logits are
+ * bf16 products summed in fp32; the weights enter the output product split
+ * into two bf16 parts (16 significant bits), so Y keeps fp32-level error; an
+ * online softmax over chunks of 64 keys.
  *
  * kvs_ridge_values: per KV head g, the values of k compressed pairs whose keys
  * Kc[g] are fixed   [KVSculpt §2: with the keys fixed the values solve a
@@ -368,7 +369,8 @@ int kvs_spectrum(const float* G, int64_t Hkv, int64_t d, float rtol, float* sigm
  *   Vc : float [Hkv, k, d], written;
  *   workspace: kvs_ridge_values_workspace_size(Hkv, R, k, d) bytes, 256-byte
  *        aligned.
- * fp32 throughout: A, then A^T A + lam I and A^T Y, then a Cholesky solve
+ * The logits as in kvs_block_attention (bf16 products, fp32 sums), then fp32:
+ * A, the lower triangle of A^T A + lam I, A^T Y, and a blocked Cholesky solve
  * (one CTA per head).  A pivot that is not positive (lam too small for fp32
  * against |A^T A|) records KVS_ERR_RANGE in the error word and sets that
  * head's values to 0.  d in {64, 128}, else KVS_ERR_UNSUPPORTED; k > 512
