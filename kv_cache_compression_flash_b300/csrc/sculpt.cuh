@@ -28,6 +28,7 @@ namespace kvs {
 constexpr int kRidgeMaxK = 512;
 constexpr int kRidgeMaxD = 128;
 constexpr int kRidgeSolveThreads = 1024;
+
 // ---- block attention on the tensor cores (mma.sync m16n8k16, bf16 -> fp32) ----
 constexpr int kBaThreads = 128;  // 4 warps x 16 query rows
 constexpr int kBaKeys = 64;      // keys per chunk
