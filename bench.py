@@ -31,18 +31,23 @@ sys.path.insert(0, ROOT)
 
 METRIC = "KV tokens scored+compressed/s per layer (M tok/s) and % of tensor/HBM roofline"
 UNIT = "M tok/s"
-DEFAULT_WORKLOAD = "llama3_8b_layer_n8192_w512"
+DEFAULT_WORKLOAD = "full_model_l32_b16_n16384"
+FULL_MODEL = "full_model_l32_b16_n16384"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
 
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 10 for the full-model batch, 200 for one pool)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=2, help="end-to-end steps of the full-model batch")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle time for the CPU baseline")
     ap.add_argument("--soak-s", type=float, default=1.0, help="untimed replays before timing (clock samples)")
     ap.add_argument("--trizone", action="store_true",
                     help="time one TriZone decode step over the workload's compressed pool instead")
@@ -154,6 +159,14 @@ def pass_flops(wl) -> float:
     return 2.0 * wl.d * pairs * wl.Hq
 
 
+def sustained_peak():
+    """The measured sustained bf16 rate (a seconds-long GEMM loop under the power cap), if recorded."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return json.load(open(p)).get("bf16_tflops_sustained")
+    return None
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -249,24 +262,25 @@ def run_reference(args):
         return 0
     from kv_cache_compression_flash_b300 import synth
     wl = synth.WORKLOADS[args.workload]
-    host = synth.make_layer(wl, layer=0)
+    pools = FULL_MODEL_ORACLE_POOLS if wl.name == FULL_MODEL else ((0, 0),)
+    hosts = [synth.make_layer(wl, l, q) for l, q in pools]
     for i in range(args.warmup):
-        oracle_group_step(wl, host, i % wl.Hkv)
+        oracle_group_step(wl, hosts[i % len(hosts)], (i // len(hosts)) % wl.Hkv)
     times = []
     for i in range(args.steps):
         t0 = time.perf_counter()
-        oracle_group_step(wl, host, i % wl.Hkv)
+        oracle_group_step(wl, hosts[i % len(hosts)], (i // len(hosts)) % wl.Hkv)
         times.append(time.perf_counter() - t0)
     total = sum(times)
     value = wl.N / wl.Hkv * args.steps / total / 1e6
     sample = (f"each step = the fp64 oracle's full RDKV pass (scores, weights, allocation, packing) over one "
-              f"KV group ({wl.G} query heads, 1 of {wl.Hkv} KV heads, N={wl.N}, W={wl.W}); "
-              f"counted as N/Hkv layer tokens")
+              f"KV group ({wl.G} query heads, 1 of {wl.Hkv} KV heads, N={wl.N}, W={wl.W}) of the (layer, sequence) "
+              f"pools {list(pools)} in turn; counted as N/Hkv layer tokens")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(wl),
+        "config": full_model_config(wl) if wl.name == FULL_MODEL else workload_config(wl),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_cores(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
@@ -696,10 +710,290 @@ def run_sculpt(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# the full-model batch: 32 layers x 16 sequences, every layer one pooled step
+# ---------------------------------------------------------------------------
+def full_model_inputs(wl, dev, layers):
+    """Every layer's Q, K, V for all its sequences, drawn on the device (seeded)."""
+    from kv_cache_compression_flash_b300 import synth
+    return [synth.make_pools(wl, l, range(wl.seqs), device=dev) for l in range(layers)]
+
+
+def oracle_pool_groups(wl, pools, seconds):
+    """The oracle's RDKV pass, one KV group at a time, over sampled (layer,
+    sequence) pools of the batch until `seconds`; (layer tokens/s, groups, s)."""
+    from kv_cache_compression_flash_b300 import synth
+    hosts = [synth.make_layer(wl, l, q) for l, q in pools]
+    groups, t0 = 0, time.perf_counter()
+    while True:
+        oracle_group_step(wl, hosts[groups % len(hosts)], (groups // len(hosts)) % wl.Hkv)
+        groups += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return wl.N * groups / wl.Hkv / dt, groups, dt
+
+
+FULL_MODEL_ORACLE_POOLS = ((0, 0), (15, 15), (31, 0))
+
+
+def full_model_config(wl):
+    return {"workload": wl.name, "layers": wl.layers, "seqs": wl.seqs, "Hq": wl.Hq, "Hkv": wl.Hkv, "N": wl.N,
+            "W": wl.W, "d": wl.d, "avg_bits": wl.avg_bits[0], "pools_per_step_per_gpu": wl.layers * wl.seqs,
+            "pools_per_launch": wl.seqs, "tokens_per_step": wl.layers * wl.seqs * wl.N,
+            "l2": "inputs (38.7 GB) far larger than L2; no flush", "parallelism": "replicas"}
+
+
+def run_full_model(args):
+    """One step = every layer of the batch through the whole RDKV path: per
+    layer one pooled step over its 16 sequences (pass 1, pass 2, w_c, sigma_t,
+    V allocation per pool, sigma_c, K allocation per pool, V and K pack and
+    dequantise).  All 32 layers' inputs (38.7 GB) are resident in HBM before
+    the timed region; they are far larger than L2, so no flush is needed.
+    Events on the launching stream bracket each layer's two scoring passes,
+    which gives the pass kernels' times inside the timed steps."""
+    import torch
+    from kv_cache_compression_flash_b300 import _lib as L
+    from kv_cache_compression_flash_b300 import synth
+    from kv_cache_compression_flash_b300.pipeline import RdkvLayerStep
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_group(world, "nccl")
+    L.lib()
+    wl = synth.WORKLOADS[FULL_MODEL]
+    layers, P = wl.layers, wl.seqs
+    t_gen = time.perf_counter()
+    inputs = full_model_inputs(wl, dev, layers)
+    torch.cuda.synchronize()
+    gen_s = time.perf_counter() - t_gen
+    avg = wl.avg_bits[0]
+    steps = [RdkvLayerStep(wl.Hq, wl.Hkv, wl.N, wl.W, wl.d, avg, device=dev, n_pools=P) for _ in range(2)]
+    main = torch.cuda.current_stream()
+
+    def one_step(evs=None):
+        for l in range(layers):
+            st, x = steps[l % 2], inputs[l]
+            if evs is not None:
+                evs[l][0].record(main)
+            st.pass1(x["Q"], x["K"], x["V"])
+            if evs is not None:
+                evs[l][1].record(main)
+            st.pass2(x["Q"], x["K"], x["V"])
+            if evs is not None:
+                evs[l][2].record(main)
+            st.rest(x["Q"], x["K"], x["V"])
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    if L.device_error() != 0:
+        raise SystemExit("device error during warm-up")
+    clocks = ClockSampler(local).start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak_s:
+        one_step()
+        torch.cuda.synchronize()
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    ev_pass = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(layers)]
+               for _ in range(args.steps)]
+    barrier(dist, dev)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        ev_step[i][0].record(main)
+        one_step(ev_pass[i])
+        ev_step[i][1].record(main)
+    torch.cuda.synchronize()
+    barrier(dist, dev)
+    clk = clocks.stop()
+    if L.device_error() != 0:
+        raise SystemExit("device error during the timed region")
+    step_ms = [a.elapsed_time(b) for a, b in ev_step]
+    total_s = reduce_max(dist, sum(step_ms) / 1e3, dev)
+    tokens_per_step = layers * P * wl.N                      # layer-tokens: every layer of every sequence
+    value = world * args.steps * tokens_per_step / total_s / 1e6
+    p1 = statistics.fmean(e[l][0].elapsed_time(e[l][1]) for e in ev_pass for l in range(layers))
+    p2 = statistics.fmean(e[l][1].elapsed_time(e[l][2]) for e in ev_pass for l in range(layers))
+    rest = statistics.fmean(step_ms) / layers - p1 - p2
+
+    peak_tf, _, peak_kind = measured_peaks()
+    peak_sus = sustained_peak()
+    dom_ms, kname = (p1, "lse_pass_kernel") if p1 >= p2 else (p2, "colreduce_pass_kernel")
+    flops = pass_flops(wl) * P                               # one launch covers the layer's 16 pools
+    achieved = flops / (dom_ms / 1e3) / 1e12
+    peak = peak_sus if peak_sus else peak_tf
+    roofline = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak if peak else None,
+                "peak_kind": f"{peak_kind} bf16 {'sustained' if peak_sus else 'burst'} (the pass runs inside a "
+                             f"seconds-long step)",
+                "frac_of_burst": achieved / peak_tf if peak_tf else None,
+                "flops_per_launch": flops, "launch_ms": dom_ms,
+                "traffic": recorded_traffic(kname, wl.name),
+                "duration_note": "CUDA events on the launching stream around each layer's pass (the pass kernel "
+                                 "plus its small merge kernel), averaged over every layer of the timed steps"}
+    launches = sum(st.kernel_launches() for st in steps[:1]) * layers + layers   # + pass 2's offsets kernel
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": statistics.fmean(step_ms), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, drawn on the device)",
+        "config": full_model_config(wl),
+        "segments_ms_per_layer": {"pass1_lse": p1, "pass2_token_weights": p2, "rest": rest},
+        "roofline": roofline,
+        "gpu_launches": launches * args.steps,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                   "samples": clk["samples"], "window": f"{args.soak_s:.0f} s soak of the same step, then the timed steps"},
+        "input_generation_s": gen_s,
+    }
+    if not args.no_e2e:
+        out["e2e"] = run_full_model_e2e(args, wl, inputs, steps, dist, dev, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, groups, dt = oracle_pool_groups(wl, FULL_MODEL_ORACLE_POOLS, args.cpu_seconds)
+        out["cpu_baseline"] = {
+            "value": v / 1e6, "unit": UNIT, "cores": oracle_cores(), "kind": "oracle",
+            "sample": f"{groups} KV groups of the (layer, sequence) pools {list(FULL_MODEL_ORACLE_POOLS)} through the "
+                      f"fp64 oracle in {dt:.1f} s (one group = {wl.G} query heads x 1 KV head, N/Hkv layer tokens "
+                      f"each); the whole batch's rate is extrapolated from these groups"}
+    if rank == 0:
+        print(json.dumps(out))
+        log_result(out)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_full_model_e2e(args, wl, dev_inputs, steps, dist, dev, world):
+    """The same step through the same calls with HOST buffers: every layer's
+    Q, K, V come from pinned host memory and its packed streams, widths and
+    counts go back to pinned host memory, every copy inside the timed region.
+    Two layers in flight: layer l's inputs cross the host link while layer
+    l-1 computes and layer l-2's streams come back."""
+    import torch
+    layers, P = wl.layers, wl.seqs
+    host = []
+    for l in range(layers):
+        try:
+            host.append({k: dev_inputs[l][k].cpu().pin_memory() for k in ("Q", "K", "V")})
+        except RuntimeError:            # not enough pinnable host memory: reuse the layers already there
+            break
+    n_host = len(host)
+    if n_host == 0:
+        return {"value": None, "unit": UNIT, "error": "no pinned host memory for the inputs"}
+    slots = [{k: torch.empty_like(dev_inputs[0][k]) for k in ("Q", "K", "V")} for _ in range(2)]
+    cp, comp, out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def landing(st):
+        return {"bits_v": torch.empty(st.bits_v.numel(), dtype=torch.uint8, pin_memory=True),
+                "bits_k": torch.empty(st.bits_k.numel(), dtype=torch.uint8, pin_memory=True),
+                "counts": [torch.empty(st.v_streams.counts.numel(), dtype=torch.int64, pin_memory=True)
+                           for _ in range(2)],
+                "streams": [[tuple(torch.empty(t.numel(), dtype=t.dtype, pin_memory=True)
+                                   for t in (s.codes[i], s.scales[i], s.ids[i], s.goff[i])) for i in range(4)]
+                            for s in (st.v_streams, st.k_streams)]}
+    lands = [landing(st) for st in steps]
+    h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in ("Q", "K", "V")) * layers
+    d2h = [0]
+
+    def issue(l):
+        s = l % 2
+        st, x, hx, land = steps[s], slots[s], host[l % n_host], lands[s]
+        if l >= 2:
+            cp.wait_event(ev_comp[s])          # layer l-2 no longer reads this slot
+        with torch.cuda.stream(cp):
+            for k in ("Q", "K", "V"):
+                x[k].copy_(hx[k], non_blocking=True)
+            ev_in[s].record(cp)
+        comp.wait_event(ev_in[s])
+        if l >= 2:
+            comp.wait_event(ev_out[s])         # layer l-2's streams have left
+        with torch.cuda.stream(comp):
+            st.run(x["Q"], x["K"], x["V"], stream=comp)
+            for j, sm in enumerate((st.v_streams, st.k_streams)):
+                land["counts"][j].copy_(sm.counts, non_blocking=True)
+            land["bits_v"].copy_(st.bits_v, non_blocking=True)
+            land["bits_k"].copy_(st.bits_k, non_blocking=True)
+            ev_comp[s].record(comp)
+
+    def drain(l):
+        s = l % 2
+        st, land = steps[s], lands[s]
+        ev_comp[s].synchronize()               # this layer's counts are on the host
+        nbytes = land["bits_v"].numel() + land["bits_k"].numel() + 2 * 8 * 8 * P
+        out.wait_event(ev_comp[s])
+        with torch.cuda.stream(out):
+            for j, sm in enumerate((st.v_streams, st.k_streams)):
+                c = land["counts"][j].view(P, 8).tolist()
+                for i, wd in enumerate((2, 4, 8, 16)):
+                    lc, ls, li, lg = land["streams"][j][i]
+                    cu, cg = sm.cap_units[i], sm.cap_groups[i]
+                    for q in range(P):
+                        nu, ng = c[q][i], c[q][4 + i]
+                        g0, u0 = q * cg, q * cu
+                        lc[g0 * 8 * wd:(g0 + ng) * 8 * wd].copy_(sm.codes[i][g0 * 8 * wd:(g0 + ng) * 8 * wd],
+                                                                 non_blocking=True)
+                        li[u0:u0 + nu].copy_(sm.ids[i][u0:u0 + nu], non_blocking=True)
+                        lg[u0:u0 + nu].copy_(sm.goff[i][u0:u0 + nu], non_blocking=True)
+                        nbytes += ng * 8 * wd + nu * 12
+                        if wd != 16:
+                            ls[g0:g0 + ng].copy_(sm.scales[i][g0:g0 + ng], non_blocking=True)
+                            nbytes += ng * 2
+            ev_out[s].record(out)
+        return nbytes
+
+    def run_steps(n):
+        total = 0
+        for i in range(n):
+            tot = 0
+            for l in range(layers):
+                issue(l)
+                if l:
+                    tot += drain(l - 1)
+            tot += drain(layers - 1)
+            total = tot
+        return total
+
+    run_steps(1)                               # warm
+    torch.cuda.synchronize()
+    barrier(dist, dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    d2h[0] = run_steps(args.e2e_steps)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    barrier(dist, dev)
+    total = reduce_max(dist, elapsed, dev)
+    tokens = layers * P * wl.N
+    return {"value": world * args.e2e_steps * tokens / total / 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h[0], "steps": args.e2e_steps,
+            "host_layers": n_host,
+            "path": "pinned host Q,K,V of every layer -> device, the C-ABI calls of the pooled step, packed "
+                    "streams + widths + counts -> pinned host; two layers in flight (copy in / compute / copy out "
+                    "on three streams)"}
+
+
+def log_result(line):
+    """Appends the line to the results log (bench_results.jsonl beside bench.py, one JSON line per run)."""
+    try:
+        with open(os.path.join(ROOT, "bench_results.jsonl"), "a") as f:
+            f.write(json.dumps(line) + "\n")
+    except OSError:
+        pass
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.steps is None:
+        args.steps = 10 if (args.workload == FULL_MODEL and not (args.trizone or args.core or args.sculpt)) else 200
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == FULL_MODEL and not (args.trizone or args.core or args.sculpt):
+        return run_full_model(args)
     if args.trizone:
         return run_trizone(args)
     if args.core:

@@ -35,7 +35,7 @@
  *    them skip the offending writes and return normally.
  *  - Device waits are bounded: a wait that exceeds about two seconds sets
  *    KVS_ERR_TIMEOUT in the error word and the kernel returns.
- *  - Supported: d in {64, 128}; 1 <= G and (G <= 4 or G % 4 == 0);
+ *  - Supported: d in {64, 128}; G in {1, 2} or a positive multiple of 4;
  *    0 <= q_pos0 and q_pos0 + W <= N; N, W >= 1; N < 2^31; Hkv*N < 2^31.
  */
 #ifndef KVS_H_
@@ -167,6 +167,25 @@ int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t bud
                       uint32_t width_mask, uint8_t* bits,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* kvs_allocate_bits over n_pools independent pools of U units each, in one
+ * call: pool q is units q*U .. q*U + U-1 of w, sigma and bits, solved on its
+ * own with the same budget_bits and width set (one pool = one (layer,
+ * sequence) of a batch   [RDKV §2.2: one allocation per cache]).  Results are
+ * bit for bit those of n_pools kvs_allocate_bits calls.  Pools that fit one
+ * thread-block cluster run side by side on the GPU; larger ones run one
+ * after the other on the stream, sharing the workspace
+ * (kvs_allocate_workspace_size(U) bytes).  n_pools < 65536. */
+int kvs_allocate_bits_pools(const float* w, const float* sigma, int64_t n_pools, int64_t U, int64_t budget_bits,
+                            uint32_t width_mask, uint8_t* bits, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* Host-only: how a pool of U units is allocated with this width mask.
+ * info: host int64[3] = {CTAs of the thread-block cluster that solves the
+ * pool without workspace (0: it does not fit one cluster), blocks of the
+ * cooperative grid that solves it otherwise (0 with a cluster), workspace
+ * bytes that grid uses}.  Queries the current device. */
+int kvs_allocate_plan_info(int64_t U, uint32_t width_mask, int64_t* info);
+
 /* kvs_allocate_bits for callers that must not allocate device memory.  The
  * papers have no counterpart: this entry point exists for host code that
  * cannot call cudaMalloc (or any allocating library), e.g. an inference
@@ -177,8 +196,9 @@ int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t bud
  * bytes until the process exits.  Inputs and outputs are as for
  * kvs_allocate_bits, and so are the results (bit for bit).
  *  - The first call on a device looks up the array's device address (once
- *    per device, with that device current); make that first call before any
- *    stream capture.
+ *    per device and context, with that device current); make that first call
+ *    before any stream capture.  After cudaDeviceReset the next call looks
+ *    the address up again in the new context.
  *  - All calls share the one array and it keeps the previous call's
  *    contents; each call clears the part that must start at zero.  Calls
  *    whose kernels overlap on the GPU (different streams, or several host
@@ -241,6 +261,27 @@ int kvs_quantize_pack(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int 
 int kvs_dequantize(const kvs_stream_set* streams, int64_t Hkv, int64_t N, int64_t d, int axis,
                    const uint8_t* bits, const uint8_t* keep_bits, float* out,
                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Pooled variants: n_pools independent caches of one shape, one (layer,
+ * sequence) each, packed (or unpacked) by one call   [RDKV §2.2-2.3, applied
+ * to every cache of a batch].  X [n_pools, Hkv, N, d]; bits [n_pools, U] (U =
+ * Hkv*N for axis 0, Hkv*d for axis 1); keep_bits [n_pools, Hkv*N]; out
+ * [n_pools, Hkv, N, d].  cap_units / cap_groups in `streams` are the capacities
+ * of ONE pool (kvs_pack_capacity), and every array holds n_pools of them back
+ * to back: pool q's codes start at byte q*cap_groups[i]*8*w, its scales at
+ * q*cap_groups[i], its unit ids and group offsets at q*cap_units[i] and its
+ * counts at counts[8*q].  Within a pool, unit ids and group offsets are local
+ * (as in a one-pool set), so pointers offset that way give a stream set that
+ * the one-pool calls accept.  Results are bit for bit those of n_pools
+ * one-pool calls.  n_pools < 65536 (axis 1: n_pools*Hkv < 65536).
+ * Workspace: kvs_pack_pools_workspace_size bytes. */
+size_t kvs_pack_pools_workspace_size(int64_t n_pools, int64_t Hkv, int64_t N, int64_t d, int axis);
+int kvs_quantize_pack_pools(const uint16_t* X, int64_t n_pools, int64_t Hkv, int64_t N, int64_t d, int axis,
+                            const uint8_t* bits, const uint8_t* keep_bits, const kvs_stream_set* streams,
+                            void* workspace, size_t workspace_bytes, void* stream);
+int kvs_dequantize_pools(const kvs_stream_set* streams, int64_t n_pools, int64_t Hkv, int64_t N, int64_t d, int axis,
+                         const uint8_t* bits, const uint8_t* keep_bits, float* out, void* workspace,
+                         size_t workspace_bytes, void* stream);
 
 /* ---- threshold pruning with a sliding window ------------------------------ */
 /* KVzap's adaptive eviction   [KVzap §2.3: tokens whose score falls below a

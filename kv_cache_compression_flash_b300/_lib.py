@@ -46,12 +46,20 @@ SIGNATURES = {
     "kvs_allocate_bits": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_uint32, c_void_p, c_void_p, c_size_t,
                                   c_void_p]),
     "kvs_allocate_bits_static": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_uint32, c_void_p, c_void_p]),
+    "kvs_allocate_bits_pools": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_uint32, c_void_p, c_void_p,
+                                        c_size_t, c_void_p]),
+    "kvs_allocate_plan_info": (c_int, [c_int64, c_uint32, POINTER(c_int64)]),
     "kvs_pack_capacity": (c_int, [c_int64] * 3 + [c_int, c_int64, POINTER(c_int64), POINTER(c_int64)]),
     "kvs_pack_workspace_size": (c_size_t, [c_int64] * 3 + [c_int]),
     "kvs_quantize_pack": (c_int, [c_void_p] + [c_int64] * 3 + [c_int, c_void_p, c_void_p, c_void_p, c_void_p,
                                                                c_size_t, c_void_p]),
     "kvs_dequantize": (c_int, [c_void_p] + [c_int64] * 3 + [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
                                                             c_void_p]),
+    "kvs_pack_pools_workspace_size": (c_size_t, [c_int64] * 4 + [c_int]),
+    "kvs_quantize_pack_pools": (c_int, [c_void_p] + [c_int64] * 4 + [c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                                     c_size_t, c_void_p]),
+    "kvs_dequantize_pools": (c_int, [c_void_p] + [c_int64] * 4 + [c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                                  c_size_t, c_void_p]),
     "kvs_threshold_keep": (c_int, [c_void_p, c_int64, c_int64, ctypes.c_float, c_int64, c_uint32, c_void_p,
                                    c_void_p]),
     "kvs_trizone_index_size": (c_size_t, [c_int64, c_int64]),
@@ -232,35 +240,84 @@ def allocate_bits(w, sigma, budget_bits, width_mask=WIDTHS_ALL, *, out=None, ws=
     return bits
 
 
-class Streams:
-    """Device buffers of one width-grouped stream set (see kvs_stream_set)."""
+def allocate_bits_pools(w, sigma, budget_bits, width_mask=WIDTHS_ALL, *, out=None, ws=None, stream=None):
+    """Widths of n_pools independent pools: w, sigma float32 [n_pools, U] (same budget per pool)."""
+    if w.dim() != 2 or w.shape != sigma.shape or w.dtype != torch.float32 or sigma.dtype != torch.float32:
+        raise KvsError("w and sigma must be float32 [n_pools, U] of equal shape")
+    if not (w.is_contiguous() and sigma.is_contiguous()):
+        raise KvsError("w and sigma must be contiguous")
+    P, U = w.shape
+    bits = out if out is not None else torch.empty(P, U, dtype=torch.uint8, device=w.device)
+    L = lib()
+    buf = _ws(ws, "alloc", L.kvs_allocate_workspace_size(U), w.device)
+    _check(L.kvs_allocate_bits_pools(_ptr(w), _ptr(sigma), P, U, int(budget_bits), width_mask, _ptr(bits), _ptr(buf),
+                                     buf.numel(), _stream(stream)), "kvs_allocate_bits_pools")
+    return bits
 
-    def __init__(self, Hkv, N, d, axis, budget_bits, device):
+
+def allocate_plan_info(U, width_mask=WIDTHS_ALL):
+    """(cluster CTAs or 0, grid blocks or 0, grid workspace bytes) of kvs_allocate_bits for U units."""
+    info = (c_int64 * 3)()
+    _check(lib().kvs_allocate_plan_info(U, width_mask, info), "kvs_allocate_plan_info")
+    return tuple(info)
+
+
+class Streams:
+    """Device buffers of a width-grouped stream set (see kvs_stream_set).
+
+    With n_pools > 1 the set holds that many pools of one shape back to back
+    (the layout kvs_quantize_pack_pools writes); pool(q) is a one-pool view."""
+
+    def __init__(self, Hkv, N, d, axis, budget_bits, device, n_pools=1):
         cu = (c_int64 * 4)()
         cg = (c_int64 * 4)()
         _check(lib().kvs_pack_capacity(Hkv, N, d, axis, int(budget_bits), cu, cg), "kvs_pack_capacity")
-        self.shape, self.axis = (Hkv, N, d), axis
+        self.shape, self.axis, self.n_pools = (Hkv, N, d), axis, n_pools
         self.cap_units, self.cap_groups = list(cu), list(cg)
+        P = n_pools
         self.codes, self.scales, self.ids, self.goff = [], [], [], []
         for i, wd in enumerate(STREAM_WIDTHS):
-            self.codes.append(torch.empty(max(1, cg[i] * 8 * wd), dtype=torch.uint8, device=device))
-            self.scales.append(torch.empty(max(1, cg[i]), dtype=torch.int16, device=device))
-            self.ids.append(torch.empty(max(1, cu[i]), dtype=torch.int32, device=device))
-            self.goff.append(torch.empty(max(1, cu[i]), dtype=torch.int64, device=device))
-        self.counts = torch.zeros(8, dtype=torch.int64, device=device)
+            self.codes.append(torch.empty(max(1, P * cg[i] * 8 * wd), dtype=torch.uint8, device=device))
+            self.scales.append(torch.empty(max(1, P * cg[i]), dtype=torch.int16, device=device))
+            self.ids.append(torch.empty(max(1, P * cu[i]), dtype=torch.int32, device=device))
+            self.goff.append(torch.empty(max(1, P * cu[i]), dtype=torch.int64, device=device))
+        self.counts = torch.zeros(8 * P, dtype=torch.int64, device=device)
+        self.c = self._struct(0)
+
+    def _struct(self, q):
         c = StreamSetC()
-        for i in range(4):
-            c.codes[i] = self.codes[i].data_ptr()
-            c.scales[i] = self.scales[i].data_ptr()
-            c.unit_ids[i] = self.ids[i].data_ptr()
-            c.group_offsets[i] = self.goff[i].data_ptr()
-            c.cap_units[i] = cu[i]
-            c.cap_groups[i] = cg[i]
-        c.counts = self.counts.data_ptr()
-        self.c = c
+        for i, wd in enumerate(STREAM_WIDTHS):
+            c.codes[i] = self.codes[i].data_ptr() + q * self.cap_groups[i] * 8 * wd
+            c.scales[i] = self.scales[i].data_ptr() + q * self.cap_groups[i] * 2
+            c.unit_ids[i] = self.ids[i].data_ptr() + q * self.cap_units[i] * 4
+            c.group_offsets[i] = self.goff[i].data_ptr() + q * self.cap_units[i] * 8
+            c.cap_units[i] = self.cap_units[i]
+            c.cap_groups[i] = self.cap_groups[i]
+        c.counts = self.counts.data_ptr() + q * 64
+        return c
+
+    def pool(self, q):
+        """A one-pool view of pool q (shares the memory)."""
+        if not 0 <= q < self.n_pools:
+            raise KvsError("pool index out of range")
+        v = object.__new__(Streams)
+        v.shape, v.axis, v.n_pools = self.shape, self.axis, 1
+        v.cap_units, v.cap_groups = self.cap_units, self.cap_groups
+        cu, cg = self.cap_units, self.cap_groups
+        v.codes = [self.codes[i][q * cg[i] * 8 * wd:(q + 1) * cg[i] * 8 * wd] if cg[i] else self.codes[i][:1]
+                   for i, wd in enumerate(STREAM_WIDTHS)]
+        v.scales = [self.scales[i][q * cg[i]:(q + 1) * cg[i]] if cg[i] else self.scales[i][:1] for i in range(4)]
+        v.ids = [self.ids[i][q * cu[i]:(q + 1) * cu[i]] if cu[i] else self.ids[i][:1] for i in range(4)]
+        v.goff = [self.goff[i][q * cu[i]:(q + 1) * cu[i]] if cu[i] else self.goff[i][:1] for i in range(4)]
+        v.counts = self.counts[8 * q:8 * q + 8]
+        v.c = self._struct(q)
+        v._parent = self
+        return v
 
     def host_view(self):
         """Copy the used part of every stream to host numpy arrays (width -> dict)."""
+        if self.n_pools != 1:
+            raise KvsError("host_view of a pooled set: take pool(q) first")
         counts = self.counts.cpu().tolist()
         out = {}
         for i, wd in enumerate(STREAM_WIDTHS):
@@ -294,6 +351,33 @@ def dequantize(streams: Streams, bits, keep_bits, *, out=None, ws=None, stream=N
     buf = _ws(ws, "deq%d" % axis, L.kvs_pack_workspace_size(Hkv, N, d, axis), dev)
     _check(L.kvs_dequantize(ctypes.byref(streams.c), Hkv, N, d, axis, _ptr(bits), _ptr(keep_bits), _ptr(y),
                             _ptr(buf), buf.numel(), _stream(stream)), "kvs_dequantize")
+    return y
+
+
+def quantize_pack_pools(X, axis, bits, keep_bits, streams: Streams, *, ws=None, stream=None):
+    """X bf16 [n_pools, Hkv, N, d]; bits uint8 [n_pools, U]; keep_bits uint8 [n_pools, Hkv*N] (axis 1)."""
+    _bf16(X, "X")
+    P, Hkv, N, d = X.shape
+    if streams.n_pools != P or tuple(streams.shape) != (Hkv, N, d) or streams.axis != axis:
+        raise KvsError("stream set does not match X")
+    L = lib()
+    buf = _ws(ws, "packp%d" % axis, L.kvs_pack_pools_workspace_size(P, Hkv, N, d, axis), X.device)
+    _check(L.kvs_quantize_pack_pools(_ptr(X), P, Hkv, N, d, axis, _ptr(bits), _ptr(keep_bits),
+                                     ctypes.byref(streams.c), _ptr(buf), buf.numel(), _stream(stream)),
+           "kvs_quantize_pack_pools")
+    return streams
+
+
+def dequantize_pools(streams: Streams, bits, keep_bits, *, out=None, ws=None, stream=None):
+    """float32 [n_pools, Hkv, N, d] from a pooled stream set."""
+    Hkv, N, d = streams.shape
+    P, axis = streams.n_pools, streams.axis
+    dev = streams.counts.device
+    y = out if out is not None else torch.empty(P, Hkv, N, d, dtype=torch.float32, device=dev)
+    L = lib()
+    buf = _ws(ws, "deqp%d" % axis, L.kvs_pack_pools_workspace_size(P, Hkv, N, d, axis), dev)
+    _check(L.kvs_dequantize_pools(ctypes.byref(streams.c), P, Hkv, N, d, axis, _ptr(bits), _ptr(keep_bits), _ptr(y),
+                                  _ptr(buf), buf.numel(), _stream(stream)), "kvs_dequantize_pools")
     return y
 
 

@@ -154,11 +154,17 @@ __device__ __forceinline__ unsigned ca_block_select(const uint32_t* loc, int S, 
   return *s_sel;
 }
 
+// grid (CL * pools): cluster q solves pool q, whose units are q*U .. q*U + U-1
+// of w, sigma and bits (every pool has the same size and budget).
 template <int CL>
 __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const AllocParams p, const int cand_cap) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
   cg::cluster_group cluster = cg::this_cluster();
+  const long long pool_base = static_cast<long long>(blockIdx.x / CL) * p.U;
+  const float* __restrict__ pw = p.w + pool_base;
+  const float* __restrict__ psig = p.sigma + pool_base;
+  uint8_t* __restrict__ pbits = p.bits + pool_base;
   const int rank = CL > 1 ? static_cast<int>(cluster.block_rank()) : 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.K;
@@ -211,8 +217,8 @@ __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const A
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int i = i0 + j * kCAThreads + tid;
-      wv[j] = i < n_mine ? p.w[u_begin + i] : 0.f;
-      sv[j] = i < n_mine ? p.sigma[u_begin + i] : 0.f;
+      wv[j] = i < n_mine ? pw[u_begin + i] : 0.f;
+      sv[j] = i < n_mine ? psig[u_begin + i] : 0.f;
     }
 #pragma unroll 1
     for (int j = 0; j < 8; ++j) {  // not unrolled: keeps the executed code small
@@ -249,7 +255,7 @@ __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const A
   if (bad || total <= p.B) {  // uniform over the cluster
     if (bad && rank == 0 && tid == 0) record_error(KVS_ERR_RANGE);
     for (int i = tid; i < n_mine; i += kCAThreads)
-      p.bits[u_begin + i] = (!bad && th[i] != 0u) ? static_cast<uint8_t>(full_cost) : 0;
+      pbits[u_begin + i] = (!bad && th[i] != 0u) ? static_cast<uint8_t>(full_cost) : 0;
     csync();
     return;
   }
@@ -353,7 +359,7 @@ __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const A
         if ((th[k * per + i] & M) == P) {
           const long long u = u_begin + i;
           const unsigned slot = atomicAdd(&s_fill, 1u);
-          cand[my_off + slot] = {theta_bits(p, p.w[u], p.sigma[u], k), u * 4 + k};
+          cand[my_off + slot] = {theta_bits(p, pw[u], psig[u], k), u * 4 + k};
         }
     __syncthreads();
     csync();  // every CTA's segment is written
@@ -462,7 +468,7 @@ __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const A
           for (int i = tid; i < n_mine; i += kCAThreads) {
             if (th[k * per + i] != top) continue;
             const long long u = u_begin + i;
-            const uint32_t v = static_cast<uint32_t>(theta_bits(p, p.w[u], p.sigma[u], k));
+            const uint32_t v = static_cast<uint32_t>(theta_bits(p, pw[u], psig[u], k));
             if ((v & msk) == pre) f(v, cost);
           }
         }
@@ -489,7 +495,7 @@ __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const A
       }
       if (t == lam_top && t != 0u) {
         const long long u = u_begin + i;
-        const unsigned long long f = theta_bits(p, p.w[u], p.sigma[u], k);
+        const unsigned long long f = theta_bits(p, pw[u], psig[u], k);
         if (f > lam) {
           ++l;
           continue;
@@ -579,7 +585,7 @@ __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const A
       carry += chunk_total;
     }
   }
-  for (int i = tid; i < n_mine; i += kCAThreads) p.bits[u_begin + i] = static_cast<uint8_t>(p.width[lvl[i]]);
+  for (int i = tid; i < n_mine; i += kCAThreads) pbits[u_begin + i] = static_cast<uint8_t>(p.width[lvl[i]]);
   // cost of the prefix = the largest cumulative cost of a tie taken, or `above`
   unsigned long long used = above;
   if (all_ties != 0ull) {  // uniform over the cluster
@@ -611,7 +617,7 @@ __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const A
       const uint32_t t = th[k * per + i];
       if (t == 0u || t < best_top) continue;
       const long long u = u_begin + i;
-      const CABest c = {theta_bits(p, p.w[u], p.sigma[u], k), u, p.cost[k], 0};
+      const CABest c = {theta_bits(p, pw[u], psig[u], k), u, p.cost[k], 0};
       if (t > best_top || ca_better(c, best)) {
         best = c;
         best_top = t;
@@ -645,7 +651,7 @@ __global__ void __launch_bounds__(kCAThreads, 1) allocate_cluster_kernel(const A
       const int i = static_cast<int>(g.u - u_begin);
       const int l = lvl[i] + 1;
       lvl[i] = static_cast<uint8_t>(l);
-      p.bits[g.u] = static_cast<uint8_t>(p.width[l]);
+      pbits[g.u] = static_cast<uint8_t>(p.width[l]);
     }
     R -= g.cost;
     __syncthreads();

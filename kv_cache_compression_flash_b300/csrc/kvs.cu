@@ -21,7 +21,7 @@ using namespace kvs;
 
 namespace {
 
-constexpr int kVersion = 100;
+constexpr int kVersion = 101;
 
 int sm_count() {
   int dev = 0, n = 0;
@@ -161,26 +161,29 @@ struct PackWs {
   long long* chan_base;
 };
 
-size_t carve_pack(int64_t Hkv, int64_t N, int64_t d, int axis, void* base, size_t cap, PackWs* w) {
+// HKV = heads of every pool together (n_pools * Hkv)
+size_t carve_pack(int64_t HKV, int64_t N, int64_t d, int axis, void* base, size_t cap, PackWs* w) {
   WsCarver c{static_cast<char*>(base), 0, cap};
   w->kept = w->n_kept = nullptr;
   w->chan_base = nullptr;
   if (axis == 1) {
-    w->kept = c.take<int>(static_cast<size_t>(Hkv * N));
-    w->n_kept = c.take<int>(static_cast<size_t>(Hkv));
-    w->chan_base = c.take<long long>(static_cast<size_t>(Hkv * d));
+    w->kept = c.take<int>(static_cast<size_t>(HKV * N));
+    w->n_kept = c.take<int>(static_cast<size_t>(HKV));
+    w->chan_base = c.take<long long>(static_cast<size_t>(HKV * d));
   } else {
     c.take<int>(1);  // no scratch; keep a non-zero size for callers that pass one
   }
   return c.used;
 }
 
-int pack_shape_ok(int64_t Hkv, int64_t N, int64_t d, int axis) {
-  if (Hkv <= 0 || N <= 0 || d <= 0 || (axis != 0 && axis != 1)) return KVS_ERR_INVALID_ARG;
+int pack_shape_ok(int64_t n_pools, int64_t Hkv, int64_t N, int64_t d, int axis) {
+  if (n_pools <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || (axis != 0 && axis != 1)) return KVS_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return KVS_ERR_UNSUPPORTED;
-  if (Hkv * N >= (1ll << 31)) return KVS_ERR_UNSUPPORTED;
-  // channel plan: per-width unit counts in 16 bits, group counts in 32 bits
-  if (axis == 1 && (Hkv * d >= (1ll << 16) || Hkv * d * cdiv(N, 64) >= (1ll << 32))) return KVS_ERR_UNSUPPORTED;
+  if (Hkv * N >= (1ll << 31) || n_pools * Hkv * N >= (1ll << 40) || n_pools > 65535) return KVS_ERR_UNSUPPORTED;
+  // channel plan: per-width unit counts in 16 bits, group counts in 32 bits;
+  // the channel kernels' grid rows run over every pool's heads
+  if (axis == 1 && (Hkv * d >= (1ll << 16) || Hkv * d * cdiv(N, 64) >= (1ll << 32) || n_pools * Hkv > 65535))
+    return KVS_ERR_UNSUPPORTED;
   return KVS_OK;
 }
 
@@ -194,8 +197,9 @@ cudaError_t launch_cluster(F fn, dim3 grid, int cl, int threads, size_t smem, cu
   return launch_k(fn, grid, dim3(static_cast<unsigned>(threads)), smem, st, cl, args...);
 }
 
-// the axis-0 plan on one cluster of CL CTAs
-int launch_rows_plan(const uint8_t* bits, long long U, int gpu, const StreamPtrs& sp, cudaStream_t st) {
+// the axis-0 plan: one cluster of CL CTAs per pool
+int launch_rows_plan(const uint8_t* bits, long long U, long long n_pools, int gpu, const StreamPtrs& sp,
+                     cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] { err = set_cluster_attrs(rows_plan_kernel<16>); });
@@ -203,13 +207,14 @@ int launch_rows_plan(const uint8_t* bits, long long U, int gpu, const StreamPtrs
   int cl = 1;
   while (cl < 16 && static_cast<long long>(cl) * 2048 < U) cl *= 2;
   const long long per = cdiv(U, cl);
+  const dim3 grid(static_cast<unsigned>(cl * n_pools));
   cudaError_t e;
   switch (cl) {
-    case 1: e = launch_cluster(rows_plan_kernel<1>, dim3(1), 1, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
-    case 2: e = launch_cluster(rows_plan_kernel<2>, dim3(2), 2, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
-    case 4: e = launch_cluster(rows_plan_kernel<4>, dim3(4), 4, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
-    case 8: e = launch_cluster(rows_plan_kernel<8>, dim3(8), 8, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
-    default: e = launch_cluster(rows_plan_kernel<16>, dim3(16), 16, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
+    case 1: e = launch_cluster(rows_plan_kernel<1>, grid, 1, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
+    case 2: e = launch_cluster(rows_plan_kernel<2>, grid, 2, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
+    case 4: e = launch_cluster(rows_plan_kernel<4>, grid, 4, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
+    case 8: e = launch_cluster(rows_plan_kernel<8>, grid, 8, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
+    default: e = launch_cluster(rows_plan_kernel<16>, grid, 16, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
   }
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
@@ -219,27 +224,32 @@ int launch_rows_plan(const uint8_t* bits, long long U, int gpu, const StreamPtrs
 }
 
 template <int DH>
-int pack_dh(const uint16_t* X, int64_t Hkv, int64_t N, int axis, const uint8_t* bits, const uint8_t* keep,
-            const kvs_stream_set* s, const PackWs& w, cudaStream_t st, bool dequant, float* out) {
+int pack_dh(const uint16_t* X, int64_t n_pools, int64_t Hkv, int64_t N, int axis, const uint8_t* bits,
+            const uint8_t* keep, const kvs_stream_set* s, const PackWs& w, cudaStream_t st, bool dequant, float* out) {
   const int sms = sm_count();
+  const int hkv = static_cast<int>(Hkv);
+  const unsigned gy = static_cast<unsigned>(n_pools * Hkv);  // channel kernels: every pool's heads
   if (axis == 0) {
     const long long U = Hkv * N;
     const StreamPtrs sp = to_ptrs(s, true);
     const long long ngroups = U * (DH / 64);
-    const int blocks = static_cast<int>(std::min<long long>(cdiv(ngroups, 16), static_cast<long long>(sms) * 8));
+    // about eight CTAs per SM over all the pools together
+    const long long per_pool = std::max<long long>(1, static_cast<long long>(sms) * 8 / n_pools);
+    const dim3 grid(static_cast<unsigned>(std::min<long long>(cdiv(ngroups, 16), per_pool)),
+                    static_cast<unsigned>(n_pools));
     if (dequant) {  // decode straight from the stream entries
-      KVS_CUDA_TRY(launch_k(dequant_rows_kernel<DH>, dim3(blocks), dim3(256), 0, st, 0, sp, bits, U, out));
+      KVS_CUDA_TRY(launch_k(dequant_rows_kernel<DH>, grid, dim3(256), 0, st, 0, sp, bits, U, out));
     } else {
-      const int rc = launch_rows_plan(bits, U, DH / 64, sp, st);
+      const int rc = launch_rows_plan(bits, U, n_pools, DH / 64, sp, st);
       if (rc) return rc;
-      KVS_CUDA_TRY(launch_k(pack_rows_kernel<DH>, dim3(blocks), dim3(256), 0, st, 0, X, sp));
+      KVS_CUDA_TRY(launch_k(pack_rows_kernel<DH>, grid, dim3(256), 0, st, 0, X, sp, U));
     }
   } else {
     const StreamPtrs sp = to_ptrs(s, !dequant);
     if (dequant && N <= kDirectMaxN && Hkv * DH < 65536) {  // each CTA plans its own head
-      const dim3 grid(static_cast<unsigned>(cdiv(N, 64) + 1), static_cast<unsigned>(Hkv));
+      const dim3 grid(static_cast<unsigned>(cdiv(N, 64) + 1), gy);
       KVS_CUDA_TRY(launch_k(dequant_channels_direct_kernel<DH>, grid, dim3(256), 0, st, 0, sp, static_cast<int>(N),
-                            bits, keep, out));
+                            bits, keep, out, hkv));
       return KVS_OK;
     }
     static std::once_flag once;
@@ -250,36 +260,38 @@ int pack_dh(const uint16_t* X, int64_t Hkv, int64_t N, int axis, const uint8_t* 
     });
     if (err != cudaSuccess) return KVS_ERR_CUDA;
     const int cl = static_cast<int>(std::min<int64_t>(Hkv, 16));
-    KVS_CUDA_TRY(launch_cluster(channels_plan_kernel<DH>, dim3(static_cast<unsigned>(cl)), cl, kPlanThreads, 0, st,
-                                keep, static_cast<int>(N), static_cast<int>(Hkv), bits, w.kept, w.n_kept, w.chan_base,
-                                sp, dequant ? 0 : 1));
+    KVS_CUDA_TRY(launch_cluster(channels_plan_kernel<DH>, dim3(static_cast<unsigned>(cl * n_pools)), cl, kPlanThreads,
+                                0, st, keep, static_cast<int>(N), hkv, bits, w.kept, w.n_kept, w.chan_base, sp,
+                                dequant ? 0 : 1));
     if (dequant) {
-      const dim3 grid(static_cast<unsigned>(cdiv(N, 64) + 1), static_cast<unsigned>(Hkv));
-      KVS_CUDA_TRY(launch_k(dequant_channels_kernel<DH>, dim3(grid), dim3(256), 0, st, 0, sp, static_cast<int>(N), bits, w.chan_base, w.kept, w.n_kept,
-                                                        out));
+      const dim3 grid(static_cast<unsigned>(cdiv(N, 64) + 1), gy);
+      KVS_CUDA_TRY(launch_k(dequant_channels_kernel<DH>, grid, dim3(256), 0, st, 0, sp, static_cast<int>(N), bits,
+                            w.chan_base, w.kept, w.n_kept, out, hkv));
     } else {
-      const dim3 grid(static_cast<unsigned>(cdiv(N, 64)), static_cast<unsigned>(Hkv));
-      KVS_CUDA_TRY(launch_k(pack_channels_kernel<DH>, dim3(grid), dim3(256), 0, st, 0, X, static_cast<int>(N), bits, w.chan_base, w.kept, w.n_kept, sp));
+      const dim3 grid(static_cast<unsigned>(cdiv(N, 64)), gy);
+      KVS_CUDA_TRY(launch_k(pack_channels_kernel<DH>, grid, dim3(256), 0, st, 0, X, static_cast<int>(N), bits,
+                            w.chan_base, w.kept, w.n_kept, sp, hkv));
     }
   }
   return KVS_OK;
 }
 
-int pack_common(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis, const uint8_t* bits,
+int pack_common(const uint16_t* X, int64_t n_pools, int64_t Hkv, int64_t N, int64_t d, int axis, const uint8_t* bits,
                 const uint8_t* keep, const kvs_stream_set* s, void* ws, size_t ws_bytes, void* stream,
                 bool dequant, float* out) {
-  int rc = pack_shape_ok(Hkv, N, d, axis);
+  int rc = pack_shape_ok(n_pools, Hkv, N, d, axis);
   if (rc) return rc;
   if (!bits || !streams_ok(s) || (axis == 1 && !keep) || (dequant ? !out : !X)) return KVS_ERR_INVALID_ARG;
   if ((!dequant || axis == 0) && !s->counts) return KVS_ERR_INVALID_ARG;
   if (X && !aligned16(X)) return KVS_ERR_INVALID_ARG;
   if (out && !aligned16(out)) return KVS_ERR_INVALID_ARG;
   PackWs w;
-  if (carve_pack(Hkv, N, d, axis, ws, ws_bytes, &w) > ws_bytes || (!ws && ws_bytes == 0)) return KVS_ERR_WORKSPACE;
+  if (carve_pack(n_pools * Hkv, N, d, axis, ws, ws_bytes, &w) > ws_bytes || (!ws && ws_bytes == 0))
+    return KVS_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KVS_ERR_WORKSPACE;
   cudaStream_t st = as_stream(stream);
-  rc = d == 64 ? pack_dh<64>(X, Hkv, N, axis, bits, keep, s, w, st, dequant, out)
-               : pack_dh<128>(X, Hkv, N, axis, bits, keep, s, w, st, dequant, out);
+  rc = d == 64 ? pack_dh<64>(X, n_pools, Hkv, N, axis, bits, keep, s, w, st, dequant, out)
+               : pack_dh<128>(X, n_pools, Hkv, N, axis, bits, keep, s, w, st, dequant, out);
   if (rc) return rc;
   KVS_CUDA_TRY(cudaGetLastError());
   return KVS_OK;
@@ -480,36 +492,30 @@ size_t kvs_allocate_workspace_size(int64_t U) {
   return alloc_ws_bytes(alloc_blocks_max());
 }
 
-int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t budget_bits, uint32_t width_mask,
-                      uint8_t* bits, void* workspace, size_t workspace_bytes, void* stream) {
-  if (U < 0 || budget_bits < 0) return KVS_ERR_INVALID_ARG;
-  if ((width_mask & ~KVS_WIDTHS_ALL & ~1u) != 0) return KVS_ERR_INVALID_ARG;
-  if (U == 0) return KVS_OK;
-  if (!w || !sigma || !bits) return KVS_ERR_INVALID_ARG;
-  cudaStream_t st = as_stream(stream);
-  int rc = KVS_OK;
-  AllocParams p;
-  std::memset(&p, 0, sizeof(p));
+}  // extern "C"
+
+namespace {
+// Width set, step costs and chord slopes of the allocation, from the mask.
+// Returns false when the mask allows no width but 0.
+bool alloc_widths(uint32_t width_mask, AllocParams* p) {
+  std::memset(p, 0, sizeof(*p));
   int nw = 1;
-  p.width[0] = 0;
+  p->width[0] = 0;
   for (int b : {2, 4, 8, 16})
-    if (width_mask & (1u << b)) p.width[nw++] = b;
-  p.K = nw - 1;
-  if (p.K == 0) {
-    KVS_CUDA_TRY(cudaMemsetAsync(bits, 0, static_cast<size_t>(U), st));
-    return KVS_OK;
-  }
-  p.min_cost = 1 << 30;
-  for (int k = 0; k < p.K; ++k) {
-    const int b0 = p.width[k], b1 = p.width[k + 1];
-    p.cost[k] = b1 - b0;
-    p.min_cost = std::min(p.min_cost, p.cost[k]);
-    p.c[k] = (std::ldexp(1.0, -b0) - std::ldexp(1.0, -b1)) / static_cast<double>(b1 - b0);
+    if (width_mask & (1u << b)) p->width[nw++] = b;
+  p->K = nw - 1;
+  if (p->K == 0) return false;
+  p->min_cost = 1 << 30;
+  for (int k = 0; k < p->K; ++k) {
+    const int b0 = p->width[k], b1 = p->width[k + 1];
+    p->cost[k] = b1 - b0;
+    p->min_cost = std::min(p->min_cost, p->cost[k]);
+    p->c[k] = (std::ldexp(1.0, -b0) - std::ldexp(1.0, -b1)) / static_cast<double>(b1 - b0);
   }
   // c_k = (2^(b1-b0) - 1) / ((b1-b0) 2^b1): dyadic unless b1-b0 keeps an odd factor
-  p.dyadic = 1;
-  for (int k = 0; k < p.K; ++k) {
-    const int b0 = p.width[k], b1 = p.width[k + 1], d = b1 - b0;
+  p->dyadic = 1;
+  for (int k = 0; k < p->K; ++k) {
+    const int b0 = p->width[k], b1 = p->width[k + 1], d = b1 - b0;
     unsigned long long num = (1ull << d) - 1ull, den = static_cast<unsigned long long>(d);
     int e = b1;
     for (unsigned long long q = 3; q <= den; q += 2)
@@ -522,68 +528,138 @@ int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t bud
       ++e;
     }
     if (den != 1ull || num >= (1ull << 16)) {
-      p.dyadic = 0;
+      p->dyadic = 0;
       break;
     }
-    p.n[k] = static_cast<unsigned>(num);
-    p.e[k] = e;
+    p->n[k] = static_cast<unsigned>(num);
+    p->e[k] = e;
+  }
+  return true;
+}
+
+// How a pool of U units is solved: on one cluster (*CL > 0, no workspace) or
+// on a cooperative grid of *nb blocks (cached: thetas kept in shared memory).
+struct AllocPlan {
+  int CL, cand_cap;
+  long long per;
+  size_t ca_smem;
+  long long nb;
+  bool cached;
+};
+
+int plan_alloc(long long U, int K, AllocPlan* ap) {
+  std::memset(ap, 0, sizeof(*ap));
+  int rc = plan_cluster_alloc(U, K, &ap->CL, &ap->per, &ap->cand_cap, &ap->ca_smem);
+  if (rc) return rc;
+  if (ap->CL > 0) return KVS_OK;
+  const int sms = sm_count();
+  const size_t cache_smem = static_cast<size_t>(kAllocUnitsPerBlock) * K * sizeof(unsigned long long);
+  KVS_CUDA_TRY(allow_smem(allocate_kernel<true>, cache_smem));
+  int occ_c = 0, occ_u = 0;
+  KVS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_c, allocate_kernel<true>, kAllocThreads, cache_smem));
+  KVS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_u, allocate_kernel<false>, kAllocThreads, 0));
+  long long nb = std::max<long long>(1, cdiv(U, kAllocUnitsPerBlock));
+  ap->cached = nb <= static_cast<long long>(occ_c) * sms && nb <= alloc_blocks_max();
+  if (!ap->cached)
+    nb = std::max<long long>(1, std::min<long long>(cdiv(U, kAllocUnitsPerBlock),
+                                                    std::min<long long>(static_cast<long long>(std::max(occ_u, 1)) * sms,
+                                                                        alloc_blocks_max())));
+  ap->nb = nb;
+  ap->per = cdiv(U, nb);
+  if (ap->per * 16 >= (1ll << 32)) return KVS_ERR_UNSUPPORTED;  // per-block histogram counts are 32-bit
+  return KVS_OK;
+}
+
+int allocate_pools(const float* w, const float* sigma, int64_t n_pools, int64_t U, int64_t budget_bits,
+                   uint32_t width_mask, uint8_t* bits, void* workspace, size_t workspace_bytes, void* stream) {
+  if (U < 0 || budget_bits < 0 || n_pools < 0) return KVS_ERR_INVALID_ARG;
+  if ((width_mask & ~KVS_WIDTHS_ALL & ~1u) != 0) return KVS_ERR_INVALID_ARG;
+  if (U == 0 || n_pools == 0) return KVS_OK;
+  if (!w || !sigma || !bits) return KVS_ERR_INVALID_ARG;
+  if (n_pools > 65535 || n_pools * U >= (1ll << 40)) return KVS_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  AllocParams p;
+  if (!alloc_widths(width_mask, &p)) {
+    KVS_CUDA_TRY(cudaMemsetAsync(bits, 0, static_cast<size_t>(n_pools * U), st));
+    return KVS_OK;
   }
   p.w = w;
   p.sigma = sigma;
   p.bits = bits;
   p.U = U;
   p.B = static_cast<unsigned long long>(budget_bits);
-  // Preferred: one thread-block cluster holds every item's threshold in
-  // shared memory and needs no workspace.
-  int CL = 0, cand_cap = 0;
-  long long per = 0;
-  size_t ca_smem = 0;
-  rc = plan_cluster_alloc(U, p.K, &CL, &per, &cand_cap, &ca_smem);
+  AllocPlan ap;
+  int rc = plan_alloc(U, p.K, &ap);
   if (rc) return rc;
-  if (CL > 0) {
-    p.per = per;
-    KVS_CUDA_TRY(launch_k(cluster_alloc_fn(CL), dim3(static_cast<unsigned>(CL)), dim3(kCAThreads), ca_smem, st, CL, p,
-                          cand_cap));
+  if (ap.CL > 0) {
+    // one thread-block cluster per pool holds every item's threshold in
+    // shared memory and needs no workspace
+    p.per = ap.per;
+    KVS_CUDA_TRY(launch_k(cluster_alloc_fn(ap.CL), dim3(static_cast<unsigned>(ap.CL * n_pools)), dim3(kCAThreads),
+                          ap.ca_smem, st, ap.CL, p, ap.cand_cap));
     return KVS_OK;
   }
-  // Otherwise a cooperative grid: a few thousand units per block with their
-  // thetas cached in shared memory (every block co-resident), or, failing
-  // that, thetas recomputed from w and sigma in every pass.
-  const int sms = sm_count();
-  const size_t cache_smem = static_cast<size_t>(kAllocUnitsPerBlock) * p.K * sizeof(unsigned long long);
-  KVS_CUDA_TRY(allow_smem(allocate_kernel<true>, cache_smem));
-  int occ_c = 0, occ_u = 0;
-  KVS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_c, allocate_kernel<true>, kAllocThreads, cache_smem));
-  KVS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_u, allocate_kernel<false>, kAllocThreads, 0));
-  long long nb = std::max<long long>(1, cdiv(U, kAllocUnitsPerBlock));
-  const bool cached = nb <= static_cast<long long>(occ_c) * sms && nb <= alloc_blocks_max();
-  if (!cached) nb = std::max<long long>(1, std::min<long long>(cdiv(U, kAllocUnitsPerBlock),
-                                                              std::min<long long>(static_cast<long long>(std::max(occ_u, 1)) * sms,
-                                                                                  alloc_blocks_max())));
-  p.per = cdiv(U, nb);
-  if (p.per * 16 >= (1ll << 32)) return KVS_ERR_UNSUPPORTED;  // per-block histogram counts are 32-bit
+  // a cooperative grid per pool, one pool after the other on the stream (they
+  // share the workspace): a few thousand units per block with their thetas
+  // cached in shared memory (every block co-resident), or, failing that,
+  // thetas recomputed from w and sigma in every pass
+  const long long nb = ap.nb;
+  p.per = ap.per;
   WsCarver c{static_cast<char*>(workspace), 0, workspace_bytes};
   p.hdr = c.take<AllocHeader>(1);
   p.hist = c.take<unsigned long long>(static_cast<size_t>(kRadixPasses) * kRadixBins);
   p.tie_block = c.take<unsigned long long>(static_cast<size_t>(nb));
   p.cand = c.take<FixCand>(static_cast<size_t>(kMaxFixRounds) * nb);
   if (!c.ok() || !workspace) return KVS_ERR_WORKSPACE;
-  KVS_CUDA_TRY(cudaMemsetAsync(p.hdr, 0, sizeof(AllocHeader), st));
-  void* args[] = {&p};
-  if (cached) {
-    const size_t smem = static_cast<size_t>(p.per) * p.K * sizeof(unsigned long long);
-    KVS_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(allocate_kernel<true>),
-                                             dim3(static_cast<unsigned>(nb)), dim3(kAllocThreads), args, smem, st));
-  } else {
-    KVS_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(allocate_kernel<false>),
-                                             dim3(static_cast<unsigned>(nb)), dim3(kAllocThreads), args, 0, st));
+  for (int64_t q = 0; q < n_pools; ++q) {
+    p.w = w + q * U;
+    p.sigma = sigma + q * U;
+    p.bits = bits + q * U;
+    KVS_CUDA_TRY(cudaMemsetAsync(p.hdr, 0, sizeof(AllocHeader), st));
+    void* args[] = {&p};
+    if (ap.cached) {
+      const size_t smem = static_cast<size_t>(p.per) * p.K * sizeof(unsigned long long);
+      KVS_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(allocate_kernel<true>),
+                                               dim3(static_cast<unsigned>(nb)), dim3(kAllocThreads), args, smem, st));
+    } else {
+      KVS_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(allocate_kernel<false>),
+                                               dim3(static_cast<unsigned>(nb)), dim3(kAllocThreads), args, 0, st));
+    }
   }
+  return KVS_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t budget_bits, uint32_t width_mask,
+                      uint8_t* bits, void* workspace, size_t workspace_bytes, void* stream) {
+  return allocate_pools(w, sigma, 1, U, budget_bits, width_mask, bits, workspace, workspace_bytes, stream);
+}
+
+int kvs_allocate_bits_pools(const float* w, const float* sigma, int64_t n_pools, int64_t U, int64_t budget_bits,
+                            uint32_t width_mask, uint8_t* bits, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  return allocate_pools(w, sigma, n_pools, U, budget_bits, width_mask, bits, workspace, workspace_bytes, stream);
+}
+
+int kvs_allocate_plan_info(int64_t U, uint32_t width_mask, int64_t* info) {
+  if (U < 0 || !info || (width_mask & ~KVS_WIDTHS_ALL & ~1u) != 0) return KVS_ERR_INVALID_ARG;
+  info[0] = info[1] = info[2] = 0;
+  AllocParams p;
+  if (U == 0 || !alloc_widths(width_mask, &p)) return KVS_OK;
+  AllocPlan ap;
+  const int rc = plan_alloc(U, p.K, &ap);
+  if (rc) return rc;
+  info[0] = ap.CL;
+  info[1] = ap.CL > 0 ? 0 : ap.nb;
+  info[2] = ap.CL > 0 ? 0 : static_cast<int64_t>(alloc_ws_bytes(static_cast<int>(ap.nb)));
   return KVS_OK;
 }
 
 int kvs_pack_capacity(int64_t Hkv, int64_t N, int64_t d, int axis, int64_t budget_bits, int64_t* cap_units,
                       int64_t* cap_groups) {
-  const int rc = pack_shape_ok(Hkv, N, d, axis);
+  const int rc = pack_shape_ok(1, Hkv, N, d, axis);
   if (rc) return rc;
   if (budget_bits < 0 || !cap_units || !cap_groups) return KVS_ERR_INVALID_ARG;
   const long long U = axis == 0 ? Hkv * N : Hkv * d;
@@ -597,22 +673,40 @@ int kvs_pack_capacity(int64_t Hkv, int64_t N, int64_t d, int axis, int64_t budge
 }
 
 size_t kvs_pack_workspace_size(int64_t Hkv, int64_t N, int64_t d, int axis) {
-  if (pack_shape_ok(Hkv, N, d, axis)) return 0;
+  return kvs_pack_pools_workspace_size(1, Hkv, N, d, axis);
+}
+
+size_t kvs_pack_pools_workspace_size(int64_t n_pools, int64_t Hkv, int64_t N, int64_t d, int axis) {
+  if (pack_shape_ok(n_pools, Hkv, N, d, axis)) return 0;
   PackWs w;
-  return carve_pack(Hkv, N, d, axis, nullptr, 0, &w);
+  return carve_pack(n_pools * Hkv, N, d, axis, nullptr, 0, &w);
 }
 
 int kvs_quantize_pack(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis, const uint8_t* bits,
                       const uint8_t* keep_bits, const kvs_stream_set* streams, void* workspace,
                       size_t workspace_bytes, void* stream) {
-  return pack_common(X, Hkv, N, d, axis, bits, keep_bits, streams, workspace, workspace_bytes, stream, false,
+  return pack_common(X, 1, Hkv, N, d, axis, bits, keep_bits, streams, workspace, workspace_bytes, stream, false,
                      nullptr);
 }
 
 int kvs_dequantize(const kvs_stream_set* streams, int64_t Hkv, int64_t N, int64_t d, int axis, const uint8_t* bits,
                    const uint8_t* keep_bits, float* out, void* workspace, size_t workspace_bytes, void* stream) {
-  return pack_common(nullptr, Hkv, N, d, axis, bits, keep_bits, streams, workspace, workspace_bytes, stream, true,
+  return pack_common(nullptr, 1, Hkv, N, d, axis, bits, keep_bits, streams, workspace, workspace_bytes, stream, true,
                      out);
+}
+
+int kvs_quantize_pack_pools(const uint16_t* X, int64_t n_pools, int64_t Hkv, int64_t N, int64_t d, int axis,
+                            const uint8_t* bits, const uint8_t* keep_bits, const kvs_stream_set* streams,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  return pack_common(X, n_pools, Hkv, N, d, axis, bits, keep_bits, streams, workspace, workspace_bytes, stream, false,
+                     nullptr);
+}
+
+int kvs_dequantize_pools(const kvs_stream_set* streams, int64_t n_pools, int64_t Hkv, int64_t N, int64_t d, int axis,
+                         const uint8_t* bits, const uint8_t* keep_bits, float* out, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return pack_common(nullptr, n_pools, Hkv, N, d, axis, bits, keep_bits, streams, workspace, workspace_bytes, stream,
+                     true, out);
 }
 
 int kvs_threshold_keep(const float* score, int64_t Hkv, int64_t N, float tau, int64_t window,
@@ -865,18 +959,44 @@ static __device__ __align__(256) unsigned char g_static_alloc_scratch[KVS_STATIC
 namespace {
 constexpr int kMaxStaticDevices = 64;
 std::mutex g_static_scratch_mu;
+// per device: the context the address was looked up in, and the address
+void* g_static_scratch_ctx[kMaxStaticDevices] = {};
 void* g_static_scratch_addr[kMaxStaticDevices] = {};
 
-// device address of the scratch array on the current device (looked up once per device)
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// Device address of the scratch array in the current device's context.  It
+// is looked up once per (device, context): a context made after
+// cudaDeviceReset holds the array at a new address, so a change of context
+// triggers a new lookup instead of reusing a dangling pointer.
 int static_scratch_address(void** out) {
   int dev = 0;
   KVS_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 0 || dev >= kMaxStaticDevices) return KVS_ERR_UNSUPPORTED;
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  if (!get_ctx) return KVS_ERR_CUDA;
+  CUcontext ctx = nullptr;  // null until the runtime has made a context current on this thread
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return KVS_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-  if (g_static_scratch_addr[dev] == nullptr) {
+  if (g_static_scratch_addr[dev] == nullptr || ctx == nullptr || g_static_scratch_ctx[dev] != static_cast<void*>(ctx)) {
     void* p = nullptr;
-    KVS_CUDA_TRY(cudaGetSymbolAddress(&p, g_static_alloc_scratch));
+    KVS_CUDA_TRY(cudaGetSymbolAddress(&p, g_static_alloc_scratch));  // makes the primary context current if needed
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return KVS_ERR_CUDA;
     g_static_scratch_addr[dev] = p;
+    g_static_scratch_ctx[dev] = static_cast<void*>(ctx);
   }
   *out = g_static_scratch_addr[dev];
   return KVS_OK;

@@ -27,6 +27,11 @@ namespace kvs {
 
 constexpr int kPlanThreads = 512;
 
+// A stream set may hold several pools (independent (layer, sequence) caches
+// of the same shape) back to back: pool q's arrays start at q * cap_units[s]
+// (ids, group offsets) and q * cap_groups[s] (codes in 8w-byte groups,
+// scales), its counts at counts[8 q].  Group offsets and unit ids stay local
+// to the pool, so each pool's streams read like a one-pool set.
 struct StreamPtrs {
   uint8_t* codes[4];
   uint16_t* scales[4];
@@ -202,12 +207,15 @@ __device__ __forceinline__ int bits16_at(const uint4& v, int e) {
 // Writes ids[s][k] = unit and group_offsets[s][k] = k * groups_per_unit for
 // the k-th stored unit of width slot s, and counts.  Each step's ids are
 // staged in shared memory by width and then written out contiguously.
+// grid (CL * pools): cluster q plans pool q (units q*U .. q*U + U-1 of bits).
 template <int CL>
 __global__ void __launch_bounds__(kPlanThreads, 1) rows_plan_kernel(const uint8_t* __restrict__ bits,
                                                                     const long long U, const long long per,
                                                                     const int groups_per_unit, const StreamPtrs sp) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
+  const long long pool = blockIdx.x / CL;
+  bits += pool * U;
   namespace cgp = cooperative_groups;
   cgp::cluster_group cluster = cgp::this_cluster();
   const int rank = CL > 1 ? static_cast<int>(cluster.block_rank()) : 0;
@@ -289,8 +297,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rows_plan_kernel(const uint8_
       while (sl < 3 && j >= s_seg[sl + 1]) ++sl;
       const long long k = base[sl] + (j - s_seg[sl]);
       if (k < sp.cap_units[sl]) {
-        sp.ids[sl][k] = stage[j];
-        sp.goff[sl][k] = k * groups_per_unit;
+        sp.ids[sl][pool * sp.cap_units[sl] + k] = stage[j];
+        sp.goff[sl][pool * sp.cap_units[sl] + k] = k * groups_per_unit;
       }
     }
     __syncthreads();  // the stage is reused by the next step
@@ -305,8 +313,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rows_plan_kernel(const uint8_
                                              : (ghi >> 32);
     const long long units = static_cast<long long>(tot), groups = units * groups_per_unit;
     if (sp.counts) {
-      sp.counts[sl] = units;
-      sp.counts[4 + sl] = groups;
+      sp.counts[8 * pool + sl] = units;
+      sp.counts[8 * pool + 4 + sl] = groups;
     }
     if (units > sp.cap_units[sl] || groups > sp.cap_groups[sl]) record_error(KVS_ERR_RANGE);
   }
@@ -314,12 +322,13 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rows_plan_kernel(const uint8_
 }
 
 // entry offsets (in groups) of the four widths from the device counts
-__device__ __forceinline__ void entry_offsets(const StreamPtrs& sp, const int gpu, long long* s_off) {
+__device__ __forceinline__ void entry_offsets(const StreamPtrs& sp, const int gpu, const long long pool,
+                                              long long* s_off) {
   if (threadIdx.x == 0) {
     long long run = 0;
     for (int s = 0; s < 4; ++s) {
       s_off[s] = run;
-      run += min(static_cast<long long>(sp.counts[s]), sp.cap_units[s]) * gpu;
+      run += min(static_cast<long long>(sp.counts[8 * pool + s]), sp.cap_units[s]) * gpu;
     }
     s_off[4] = run;
   }
@@ -336,13 +345,17 @@ __device__ __forceinline__ int entry_slot(const long long* s_off, const long lon
   return s;
 }
 
+// grid (blocks, pools): blockIdx.y is the pool (U units of X each)
 template <int DH>
-__global__ void __launch_bounds__(256) pack_rows_kernel(const uint16_t* __restrict__ X, const StreamPtrs sp) {
+__global__ void __launch_bounds__(256) pack_rows_kernel(const uint16_t* __restrict__ X, const StreamPtrs sp,
+                                                        const long long U) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
   constexpr int GPU = DH / 64;
   __shared__ long long s_off[5];
-  entry_offsets(sp, GPU, s_off);
+  const long long pool = blockIdx.y;
+  X += pool * U * DH;
+  entry_offsets(sp, GPU, pool, s_off);
   const int l16 = threadIdx.x & 15;
   const int total = static_cast<int>(s_off[4]);  // groups < 2^31 (units < 2^31, two groups each)
   const int stride = gridDim.x * (blockDim.x / 16);
@@ -350,7 +363,8 @@ __global__ void __launch_bounds__(256) pack_rows_kernel(const uint16_t* __restri
     const int s = entry_slot(s_off, gidx);
     const int grp = gidx - static_cast<int>(s_off[s]);  // == entry * GPU + gi
     if (grp >= sp.cap_groups[s]) continue;
-    const long long u = sp.ids[s][grp / GPU];
+    const long long u = sp.ids[s][pool * sp.cap_units[s] + grp / GPU];
+    const long long gb = pool * sp.cap_groups[s];
     float x[4];
     uint2 raw;
     lane_bf16x4(X + u * DH + (grp % GPU) * 64 + l16 * 4, x, &raw);
@@ -361,17 +375,18 @@ __global__ void __launch_bounds__(256) pack_rows_kernel(const uint16_t* __restri
       bool ovf;
       packed = quantize_lane4(x, w, &sb, &ovf);
       if (l16 == 0) {
-        sp.scales[s][grp] = sb;
+        sp.scales[s][gb + grp] = sb;
         if (ovf) record_error(KVS_ERR_RANGE);
       }
     }
-    store_lane_codes(sp.codes[s] + static_cast<long long>(grp) * (8 * w), w, l16, packed, raw);
+    store_lane_codes(sp.codes[s] + (gb + grp) * (8 * w), w, l16, packed, raw);
   }
 }
 
 // Token units decoded from the stream entries (entry j of width slot s is
 // unit ids[s][j] with groups goff[s][j] ..), one half-warp per group; rows of
 // evicted units (bits == 0) are zeroed in the same launch, one warp per row.
+// grid (blocks, pools): blockIdx.y is the pool (U units of bits and out each)
 template <int DH>
 __global__ void __launch_bounds__(256) dequant_rows_kernel(const StreamPtrs sp, const uint8_t* __restrict__ bits,
                                                            const long long U, float* __restrict__ out) {
@@ -379,7 +394,10 @@ __global__ void __launch_bounds__(256) dequant_rows_kernel(const StreamPtrs sp, 
   pdl_trigger();
   constexpr int GPU = DH / 64;
   __shared__ long long s_off[5];
-  entry_offsets(sp, GPU, s_off);
+  const long long pool = blockIdx.y;
+  bits += pool * U;
+  out += pool * U * DH;
+  entry_offsets(sp, GPU, pool, s_off);
   const int l16 = threadIdx.x & 15;
   const int total = static_cast<int>(s_off[4]);
   const int stride = gridDim.x * (blockDim.x / 16);
@@ -387,12 +405,13 @@ __global__ void __launch_bounds__(256) dequant_rows_kernel(const StreamPtrs sp, 
     const int s = entry_slot(s_off, gidx);
     const int local = gidx - static_cast<int>(s_off[s]);
     const int jj = local / GPU, gi = local % GPU;
-    const long long u = sp.ids[s][jj];
-    const long long grp = sp.goff[s][jj] + gi;
+    const long long u = sp.ids[s][pool * sp.cap_units[s] + jj];
+    const long long grp = sp.goff[s][pool * sp.cap_units[s] + jj] + gi;
     if (grp >= sp.cap_groups[s]) continue;
+    const long long gg = pool * sp.cap_groups[s] + grp;
     const int w = s == 3 ? 16 : (2 << s);
     float y[4];
-    dequant_lane4(sp.codes[s] + grp * (8 * w), w, l16, sp.scales[s] + grp, y);
+    dequant_lane4(sp.codes[s] + gg * (8 * w), w, l16, sp.scales[s] + gg, y);
     *reinterpret_cast<float4*>(out + u * DH + gi * 64 + l16 * 4) = make_float4(y[0], y[1], y[2], y[3]);
   }
   // evicted rows: a warp takes 32 rows, then zeroes the ones with width 0
@@ -432,6 +451,13 @@ __global__ void __launch_bounds__(kPlanThreads, 1) channels_plan_kernel(
   cgp::cluster_group cluster = cgp::this_cluster();
   const int CL = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
+  // cluster q plans pool q: its Hkv heads of keep / kept / n_kept and Hkv*DH units
+  const long long pool = blockIdx.x / CL;
+  keep += pool * Hkv * N;
+  kept += pool * Hkv * N;
+  n_kept += pool * Hkv;
+  bits += pool * Hkv * DH;
+  chan_base += pool * Hkv * DH;
   __shared__ unsigned long long sbuf[kPlanThreads / 32 + 1];
   constexpr int kStep = kPlanThreads * 16;
   for (int g = rank; g < Hkv; g += CL) {
@@ -495,8 +521,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) channels_plan_kernel(
     const bool fits = ru[sl] < sp.cap_units[sl] && rg[sl] + ng <= sp.cap_groups[sl];
     chan_base[u] = fits ? rg[sl] : -1;
     if (write_streams && fits) {
-      sp.ids[sl][ru[sl]] = u;
-      sp.goff[sl][ru[sl]] = rg[sl];
+      sp.ids[sl][pool * sp.cap_units[sl] + ru[sl]] = u;
+      sp.goff[sl][pool * sp.cap_units[sl] + ru[sl]] = rg[sl];
     }
     ++ru[sl];
     rg[sl] += ng;
@@ -507,8 +533,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) channels_plan_kernel(
     const long long groups =
         static_cast<long long>(sl < 2 ? (t01 >> (32 * sl)) & 0xFFFFFFFFull : (t23 >> (32 * (sl - 2))) & 0xFFFFFFFFull);
     if (sp.counts) {
-      sp.counts[sl] = units;
-      sp.counts[4 + sl] = groups;
+      sp.counts[8 * pool + sl] = units;
+      sp.counts[8 * pool + 4 + sl] = groups;
     }
     if (units > sp.cap_units[sl] || groups > sp.cap_groups[sl]) record_error(KVS_ERR_RANGE);
   }
@@ -516,12 +542,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1) channels_plan_kernel(
 
 // grid (ceil(N/64), Hkv), 256 threads: kept-token group j of head g for every
 // channel; one half-warp per channel (lane i: tokens 4i..4i+3)
+// (blockIdx.y runs over the heads of every pool: pool blockIdx.y / Hkv)
 template <int DH>
 __global__ void __launch_bounds__(256) pack_channels_kernel(const uint16_t* __restrict__ X, const int N,
                                                             const uint8_t* __restrict__ bits,
                                                             const long long* __restrict__ chan_base,
                                                             const int* __restrict__ kept,
-                                                            const int* __restrict__ n_kept, const StreamPtrs sp) {
+                                                            const int* __restrict__ n_kept, const StreamPtrs sp,
+                                                            const int Hkv) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
   // odd word stride: the column reads below (lane i takes rows 4i..4i+3)
@@ -559,6 +587,7 @@ __global__ void __launch_bounds__(256) pack_channels_kernel(const uint16_t* __re
     if (grp < 0) continue;
     const int w = s_w[c];
     const int s = width_slot(w);
+    const long long gg = static_cast<long long>(g / Hkv) * sp.cap_groups[s] + grp;
     float x[4];
     uint32_t rw[4];
 #pragma unroll
@@ -573,11 +602,11 @@ __global__ void __launch_bounds__(256) pack_channels_kernel(const uint16_t* __re
       bool ovf;
       packed = quantize_lane4(x, w, &sb, &ovf);
       if (l16 == 0) {
-        sp.scales[s][grp] = sb;
+        sp.scales[s][gg] = sb;
         if (ovf) record_error(KVS_ERR_RANGE);
       }
     }
-    store_lane_codes(sp.codes[s] + grp * (8 * w), w, l16, packed, raw);
+    store_lane_codes(sp.codes[s] + gg * (8 * w), w, l16, packed, raw);
   }
 }
 
@@ -585,13 +614,14 @@ __global__ void __launch_bounds__(256) pack_channels_kernel(const uint16_t* __re
 // kept-group count decodes kept-token group j of every channel (one
 // half-warp per channel) through a shared-memory tile and writes the tokens'
 // rows; the CTAs after those zero the head's dropped tokens, 64 per CTA.
+// (blockIdx.y runs over the heads of every pool: pool blockIdx.y / Hkv)
 template <int DH>
 __global__ void __launch_bounds__(256) dequant_channels_kernel(const StreamPtrs sp, const int N,
                                                                const uint8_t* __restrict__ bits,
                                                                const long long* __restrict__ chan_base,
                                                                const int* __restrict__ kept,
                                                                const int* __restrict__ n_kept,
-                                                               float* __restrict__ out) {
+                                                               float* __restrict__ out, const int Hkv) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
   constexpr int LD = DH + 1;  // odd stride: conflict-light column writes
@@ -626,7 +656,8 @@ __global__ void __launch_bounds__(256) dequant_channels_kernel(const StreamPtrs 
     if (grp >= 0) {
       const int w = s_w[c];
       const int s = width_slot(w);
-      dequant_lane4(sp.codes[s] + grp * (8 * w), w, l16, sp.scales[s] + grp, y);
+      const long long gg = static_cast<long long>(g / Hkv) * sp.cap_groups[s] + grp;
+      dequant_lane4(sp.codes[s] + gg * (8 * w), w, l16, sp.scales[s] + gg, y);
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) tile[4 * l16 + e][c] = y[e];
@@ -679,11 +710,12 @@ __device__ __forceinline__ unsigned long long direct_exscan256(unsigned long lon
   return sbuf[warp] + x - v;
 }
 
+// (blockIdx.y runs over the heads of every pool: pool blockIdx.y / Hkv)
 template <int DH>
 __global__ void __launch_bounds__(256) dequant_channels_direct_kernel(const StreamPtrs sp, const int N,
                                                                       const uint8_t* __restrict__ bits,
                                                                       const uint8_t* __restrict__ keep,
-                                                                      float* __restrict__ out) {
+                                                                      float* __restrict__ out, const int Hkv) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
   constexpr int LD = DH + 1;
@@ -736,8 +768,10 @@ __global__ void __launch_bounds__(256) dequant_channels_direct_kernel(const Stre
   }
   // ---- each channel's entry in its width stream, then its first group ----
   unsigned long long before = 0;                   // units of each width before this head, 16-bit fields
-  for (int u = tid; u < g * DH; u += 256) {
-    const int sl = width_slot(bits[u]);
+  const long long pool = g / Hkv;
+  const uint8_t* pbits = bits + pool * Hkv * DH;   // the pool's unit widths
+  for (int u = tid; u < (g % Hkv) * DH; u += 256) {
+    const int sl = width_slot(pbits[u]);
     if (sl >= 0) before += 1ull << (16 * sl);
   }
   unsigned long long base_all;
@@ -750,7 +784,7 @@ __global__ void __launch_bounds__(256) dequant_channels_direct_kernel(const Stre
     long long b = -1;
     if (sl_me >= 0) {
       const long long entry = static_cast<long long>(((base_all + exh) >> (16 * sl_me)) & 0xFFFFull);
-      if (entry < sp.cap_units[sl_me]) b = sp.goff[sl_me][entry] + j;
+      if (entry < sp.cap_units[sl_me]) b = sp.goff[sl_me][pool * sp.cap_units[sl_me] + entry] + j;
       if (b >= sp.cap_groups[sl_me]) b = -1;
     }
     s_w[tid] = sl_me >= 0 ? static_cast<int>(bits[g * DH + tid]) : 0;
@@ -764,7 +798,8 @@ __global__ void __launch_bounds__(256) dequant_channels_direct_kernel(const Stre
     if (grp >= 0) {
       const int w = s_w[c];
       const int s = width_slot(w);
-      dequant_lane4(sp.codes[s] + grp * (8 * w), w, l16, sp.scales[s] + grp, y);
+      const long long gg = pool * sp.cap_groups[s] + grp;
+      dequant_lane4(sp.codes[s] + gg * (8 * w), w, l16, sp.scales[s] + gg, y);
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) tile[4 * l16 + e][c] = y[e];

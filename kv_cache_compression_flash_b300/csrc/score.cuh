@@ -362,6 +362,7 @@ __global__ void lse_finalize_kernel(const ScoreGeom geo, const int kt_chunk, con
                                     float* __restrict__ b_scaled) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
+  if (timeout_recorded()) return;  // the partials were never written: leave the outputs untouched
   const int rt = blockIdx.x, row = threadIdx.x;
   const int pb = rt % geo.n_pb;
   const int gh = rt / geo.n_pb;
@@ -377,7 +378,7 @@ __global__ void lse_finalize_kernel(const ScoreGeom geo, const int kt_chunk, con
   }
   const float l2 = M + lg2_approx(L);
   const int hl = row / geo.P, r = pb * geo.P + row % geo.P;
-  const bool valid = r < geo.W;
+  const bool valid = r < geo.W && hl < geo.Gt;
   if (valid) lse[static_cast<size_t>(g * geo.G + hc * geo.Gt + hl) * geo.W + r] = l2 * kLn2;
   if (b_plain) b_plain[static_cast<size_t>(rt) * 128 + row] = valid ? l2 : INFINITY;
   if (b_scaled) b_scaled[static_cast<size_t>(rt) * 128 + row] = valid ? l2 - lg2_approx(hn[r]) : INFINITY;
@@ -393,7 +394,7 @@ __global__ void lse_offsets_kernel(const ScoreGeom geo, const float* __restrict_
   const int gh = rt / geo.n_pb;
   const int g = gh / geo.n_hc, hc = gh % geo.n_hc;
   const int hl = row / geo.P, r = pb * geo.P + row % geo.P;
-  const bool valid = r < geo.W;
+  const bool valid = r < geo.W && hl < geo.Gt;
   const float l2 = valid ? lse[static_cast<size_t>(g * geo.G + hc * geo.Gt + hl) * geo.W + r] * kLog2e : 0.f;
   if (b_plain) b_plain[static_cast<size_t>(rt) * 128 + row] = valid ? l2 : INFINITY;
   if (b_scaled) b_scaled[static_cast<size_t>(rt) * 128 + row] = valid ? l2 - lg2_approx(hn[r]) : INFINITY;
@@ -641,6 +642,7 @@ __global__ void colreduce_finalize_kernel(const ScoreGeom geo, const int qt_chun
                                           const float* __restrict__ part, float* __restrict__ out) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
+  if (timeout_recorded()) return;  // the partials were never written: leave the outputs untouched
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   const int total = geo.Hkv * geo.N;
   if (idx >= total) return;

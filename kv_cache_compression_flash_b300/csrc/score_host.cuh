@@ -58,7 +58,9 @@ int validate_shape(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int
   if (Hq % Hkv != 0 || q_pos0 + W > N) return KVS_ERR_INVALID_ARG;
   const int64_t G = Hq / Hkv;
   if (d != 64 && d != 128) return KVS_ERR_UNSUPPORTED;
-  if (!(G <= 4 || G % 4 == 0)) return KVS_ERR_UNSUPPORTED;
+  // a 128-row query tile packs Gt = min(G, 4) heads of P = 128 / Gt rows:
+  // exact only for G in {1, 2, 4} or a multiple of 4
+  if (!(G == 1 || G == 2 || G % 4 == 0)) return KVS_ERR_UNSUPPORTED;
   if (N >= (1ll << 31) || Hkv * N >= (1ll << 31) || Hq * W >= (1ll << 31) || Hq >= (1 << 16))
     return KVS_ERR_UNSUPPORTED;
   return KVS_OK;

@@ -1,8 +1,15 @@
-"""One pass of the RDKV hot path over one (layer, sequence) pool.
+"""One pass of the RDKV hot path over a batch of (layer, sequence) pools.
 
 Stage 1 weights, stage 2 V allocation, stage 3 K allocation over the kept
 tokens, then packing (and optionally dequantisation), each step a call into
 libkvs.so.   [RDKV §2.2 pipeline; §2.3 TriZone streams]
+
+A pool is one (layer, sequence) cache with all of its KV heads; the RD
+allocation is solved per pool.  n_pools pools of one shape are processed
+together: the scoring and norm calls see them as one cache of n_pools * Hkv
+KV heads (every quantity they compute is per KV head), the allocation and
+packing calls take the pool count and keep each pool's solution and streams
+separate.
 
 Buffers are allocated once per shape so a step allocates nothing and can be
 replayed from CUDA graphs.
@@ -17,18 +24,23 @@ from . import _lib as K_
 
 
 class RdkvLayerStep:
-    """Preallocated outputs and workspaces for one pool shape.
+    """Preallocated outputs and workspaces for n_pools pools of one shape.
 
-    run() = pass1() + pass2() + rest(): pass 1 computes the row LSE, pass 2
-    the token weights from it, rest() everything after scoring.
+    Inputs: Q [n_pools*Hq, W, d], K and V [n_pools*Hkv, N, d] (bf16,
+    contiguous; pool q's heads are rows q*Hq.. and q*Hkv..).
+    run() = score() + rest(): score() computes the row LSE (pass 1) and the
+    token weights (pass 2), rest() everything after scoring; pass1() and
+    pass2() split the scoring for timing.
     """
 
     PASS2_MODE = K_.MODE_RDKV_WT | K_.MODE_LSE_GIVEN
     BOTH_MODE = K_.MODE_LSE | K_.MODE_RDKV_WT      # both passes in one call (the merge writes pass 2's offsets)
     SEGMENTS = ("pass1", "pass2", "rest")
 
-    def __init__(self, Hq, Hkv, N, W, d, avg_bits, device="cuda", width_mask=K_.WIDTHS_ALL, dequant=True):
+    def __init__(self, Hq, Hkv, N, W, d, avg_bits, device="cuda", width_mask=K_.WIDTHS_ALL, dequant=True,
+                 n_pools=1):
         self.shape = (Hq, Hkv, N, W, d)
+        self.n_pools = P = n_pools
         self.dequant = dequant
         self.width_mask = width_mask
         dev = torch.device(device)
@@ -36,29 +48,30 @@ class RdkvLayerStep:
         self.B_v = int(math.floor(avg_bits * self.U_v))
         self.B_k = int(math.floor(avg_bits * self.U_k))
         f32 = dict(dtype=torch.float32, device=dev)
-        self.out = {"lse": torch.empty(Hq, W, **f32), "w_t": torch.empty(Hkv, N, **f32)}
-        self.w_c = torch.empty(Hkv, d, **f32)
-        self.sig_t = torch.empty(Hkv, N, **f32)
-        self.sig_c = torch.empty(Hkv, d, **f32)
-        self.bits_v = torch.empty(self.U_v, dtype=torch.uint8, device=dev)
-        self.bits_k = torch.empty(self.U_k, dtype=torch.uint8, device=dev)
-        self.v_streams = K_.Streams(Hkv, N, d, 0, self.B_v, dev)
-        self.k_streams = K_.Streams(Hkv, N, d, 1, self.B_k, dev)
-        self.v_hat = torch.empty(Hkv, N, d, **f32) if dequant else None
-        self.k_hat = torch.empty(Hkv, N, d, **f32) if dequant else None
+        self.out = {"lse": torch.empty(P * Hq, W, **f32), "w_t": torch.empty(P * Hkv, N, **f32)}
+        self.w_c = torch.empty(P * Hkv, d, **f32)
+        self.sig_t = torch.empty(P * Hkv, N, **f32)
+        self.sig_c = torch.empty(P * Hkv, d, **f32)
+        self.bits_v = torch.empty(P * self.U_v, dtype=torch.uint8, device=dev)
+        self.bits_k = torch.empty(P * self.U_k, dtype=torch.uint8, device=dev)
+        self.v_streams = K_.Streams(Hkv, N, d, 0, self.B_v, dev, n_pools=P)
+        self.k_streams = K_.Streams(Hkv, N, d, 1, self.B_k, dev, n_pools=P)
+        self.v_hat = torch.empty(P * Hkv, N, d, **f32) if dequant else None
+        self.k_hat = torch.empty(P * Hkv, N, d, **f32) if dequant else None
         names = ("score", "score2", "score12", "cw", "rms0", "rms1", "av", "ak", "pv", "pk", "dv", "dk")
         self.ws = {k: K_.Workspace() for k in names}
         # size every workspace now so a step allocates nothing
         L = K_.lib()
+        HQ, HKV = P * Hq, P * Hkv
         sizes = {
-            "score": L.kvs_score_workspace_size(Hq, Hkv, W, N, d, 0, N - W, K_.MODE_LSE),
-            "score2": L.kvs_score_workspace_size(Hq, Hkv, W, N, d, 0, N - W, self.PASS2_MODE),
-            "score12": L.kvs_score_workspace_size(Hq, Hkv, W, N, d, 0, N - W, self.BOTH_MODE),
-            "cw": L.kvs_channel_weights_workspace_size(Hq, Hkv, W, N, d),
-            "rms0": 256, "rms1": L.kvs_unit_rms_workspace_size(Hkv, N, d, 1),
+            "score": L.kvs_score_workspace_size(HQ, HKV, W, N, d, 0, N - W, K_.MODE_LSE),
+            "score2": L.kvs_score_workspace_size(HQ, HKV, W, N, d, 0, N - W, self.PASS2_MODE),
+            "score12": L.kvs_score_workspace_size(HQ, HKV, W, N, d, 0, N - W, self.BOTH_MODE),
+            "cw": L.kvs_channel_weights_workspace_size(HQ, HKV, W, N, d),
+            "rms0": 256, "rms1": L.kvs_unit_rms_workspace_size(HKV, N, d, 1),
             "av": L.kvs_allocate_workspace_size(self.U_v), "ak": L.kvs_allocate_workspace_size(self.U_k),
-            "pv": L.kvs_pack_workspace_size(Hkv, N, d, 0), "pk": L.kvs_pack_workspace_size(Hkv, N, d, 1),
-            "dv": L.kvs_pack_workspace_size(Hkv, N, d, 0), "dk": L.kvs_pack_workspace_size(Hkv, N, d, 1),
+            "pv": L.kvs_pack_pools_workspace_size(P, Hkv, N, d, 0), "pk": L.kvs_pack_pools_workspace_size(P, Hkv, N, d, 1),
+            "dv": L.kvs_pack_pools_workspace_size(P, Hkv, N, d, 0), "dk": L.kvs_pack_pools_workspace_size(P, Hkv, N, d, 1),
         }
         for k, n in sizes.items():
             self.ws[k].get(n, dev)
@@ -66,14 +79,21 @@ class RdkvLayerStep:
         self.side_stream = torch.cuda.Stream(device=dev)
         self.v_done = torch.cuda.Event()
 
+    # ---- views --------------------------------------------------------------
+    def pool_bits(self):
+        """(bits_v [n_pools, U_v], bits_k [n_pools, U_k])."""
+        return self.bits_v.view(self.n_pools, self.U_v), self.bits_k.view(self.n_pools, self.U_k)
+
     def kernel_launches(self) -> int:
         """Kernels one step launches (memset nodes excluded)."""
         Hq, Hkv, N, W, d = self.shape
-        n = K_.score_plan_info(Hq, Hkv, W, N, d, mode=self.BOTH_MODE)[4]   # the step's one scoring call
+        P = self.n_pools
+        n = K_.score_plan_info(P * Hq, P * Hkv, W, N, d, mode=self.BOTH_MODE)[4]   # the step's one scoring call
         n += 1          # channel weights (one cluster per KV head)
         n += 1          # sigma_t
-        n += 1 + 1      # V allocation, sigma_c
-        n += 1          # K allocation
+        for U in (self.U_v, self.U_k):   # allocations: one launch for every pool on clusters, else one per pool
+            n += 1 if K_.allocate_plan_info(U, self.width_mask)[0] > 0 else P
+        n += 1          # sigma_c
         n += 2 + 2      # V pack (plan, pack), K pack (plan, pack)
         if self.dequant:
             # V dequant (decode + zero); K dequant (decode + zero, planned inside the
@@ -81,18 +101,26 @@ class RdkvLayerStep:
             n += 1 + (1 if N <= 16384 and Hkv * d < 65536 else 2)
         return n
 
+    def _flat(self, Q, K, V):
+        Hq, Hkv, N, W, d = self.shape
+        P = self.n_pools
+        return (Q.view(P * Hq, W, d), K.view(P * Hkv, N, d), None if V is None else V.view(P * Hkv, N, d))
+
     def pass1(self, Q, K, V, stream=None):
         Hq, Hkv, N, W, d = self.shape
+        Q, K, V = self._flat(Q, K, V)
         K_.score_attention(Q, K, q_pos0=N - W, mode=K_.MODE_LSE, out=self.out, ws=self.ws["score"], stream=stream)
 
     def score(self, Q, K, V, stream=None):
         """Both passes in one call (the step); pass1/pass2 split them for timing."""
         Hq, Hkv, N, W, d = self.shape
+        Q, K, V = self._flat(Q, K, V)
         K_.score_attention(Q, K, q_pos0=N - W, mode=self.BOTH_MODE, out=self.out, ws=self.ws["score12"],
                            stream=stream)
 
     def pass2(self, Q, K, V, stream=None):
         Hq, Hkv, N, W, d = self.shape
+        Q, K, V = self._flat(Q, K, V)
         K_.score_attention(Q, K, q_pos0=N - W, mode=self.PASS2_MODE, out=self.out, ws=self.ws["score2"],
                            stream=stream)
 
@@ -101,6 +129,9 @@ class RdkvLayerStep:
         V: sigma_t -> V allocation -> V pack (-> dequant);
         K: w_c (from the start), then after the V widths: sigma_c -> K
         allocation -> K pack (-> dequant)."""
+        Hq, Hkv, N, W, d = self.shape
+        P = self.n_pools
+        Q, K, V = self._flat(Q, K, V)
         ws = self.ws
         main = stream if stream is not None else torch.cuda.current_stream()
         side = self.side_stream
@@ -108,20 +139,23 @@ class RdkvLayerStep:
         with torch.cuda.stream(side):
             K_.channel_weights(Q, K, out=self.w_c, ws=ws["cw"], stream=side)
         K_.unit_rms(V, 0, out=self.sig_t, ws=ws["rms0"], stream=main)
-        K_.allocate_bits(self.out["w_t"], self.sig_t, self.B_v, self.width_mask, out=self.bits_v, ws=ws["av"],
-                         stream=main)
+        bits_v, bits_k = self.pool_bits()
+        K_.allocate_bits_pools(self.out["w_t"].view(P, self.U_v), self.sig_t.view(P, self.U_v), self.B_v,
+                               self.width_mask, out=bits_v, ws=ws["av"], stream=main)
         self.v_done.record(main)
+        X4 = (P, Hkv, N, d)
         with torch.cuda.stream(side):
             side.wait_event(self.v_done)
             K_.unit_rms(K, 1, keep_bits=self.bits_v, out=self.sig_c, ws=ws["rms1"], stream=side)
-            K_.allocate_bits(self.w_c, self.sig_c, self.B_k, self.width_mask, out=self.bits_k, ws=ws["ak"],
-                             stream=side)
-            K_.quantize_pack(K, 1, self.bits_k, self.bits_v, self.k_streams, ws=ws["pk"], stream=side)
+            K_.allocate_bits_pools(self.w_c.view(P, self.U_k), self.sig_c.view(P, self.U_k), self.B_k,
+                                   self.width_mask, out=bits_k, ws=ws["ak"], stream=side)
+            K_.quantize_pack_pools(K.view(X4), 1, self.bits_k, self.bits_v, self.k_streams, ws=ws["pk"], stream=side)
             if self.dequant:
-                K_.dequantize(self.k_streams, self.bits_k, self.bits_v, out=self.k_hat, ws=ws["dk"], stream=side)
-        K_.quantize_pack(V, 0, self.bits_v, None, self.v_streams, ws=ws["pv"], stream=main)
+                K_.dequantize_pools(self.k_streams, self.bits_k, self.bits_v, out=self.k_hat.view(X4), ws=ws["dk"],
+                                    stream=side)
+        K_.quantize_pack_pools(V.view(X4), 0, self.bits_v, None, self.v_streams, ws=ws["pv"], stream=main)
         if self.dequant:
-            K_.dequantize(self.v_streams, self.bits_v, None, out=self.v_hat, ws=ws["dv"], stream=main)
+            K_.dequantize_pools(self.v_streams, self.bits_v, None, out=self.v_hat.view(X4), ws=ws["dv"], stream=main)
         main.wait_stream(side)
 
     def run(self, Q, K, V, stream=None):

@@ -158,6 +158,24 @@ def make_layer(wl: Workload, layer: int = 0, seq: int = 0, device="cpu") -> dict
     return out
 
 
+def make_pools(wl: Workload, layer: int, seqs, device="cpu") -> dict:
+    """Q [P*Hq, W, d], K and V [P*Hkv, N, d] (bf16) of the sequences `seqs` of one
+    layer, stacked pool after pool (pool i = sequence seqs[i], made by make_layer).
+    On a CUDA device the Gaussians come from that device's generator."""
+    seqs = list(seqs)
+    P = len(seqs)
+    dev = torch.device(device)
+    out = {"Q": torch.empty(P * wl.Hq, wl.W, wl.d, dtype=torch.bfloat16, device=dev),
+           "K": torch.empty(P * wl.Hkv, wl.N, wl.d, dtype=torch.bfloat16, device=dev),
+           "V": torch.empty(P * wl.Hkv, wl.N, wl.d, dtype=torch.bfloat16, device=dev)}
+    for i, sq in enumerate(seqs):
+        t = make_layer(wl, layer, sq, device=dev)
+        out["Q"][i * wl.Hq:(i + 1) * wl.Hq] = t["Q"]
+        out["K"][i * wl.Hkv:(i + 1) * wl.Hkv] = t["K"]
+        out["V"][i * wl.Hkv:(i + 1) * wl.Hkv] = t["V"]
+    return out
+
+
 def budget_bits(avg_bits: float, units: int) -> int:
     """Total budget B = floor(avg_bits * U) bits (widths counted per unit)."""
     return int(math.floor(avg_bits * units))

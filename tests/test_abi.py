@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.kvs_version() == 100
+    assert lib.kvs_version() == 101
     for code, name in L.STATUS.items():
         assert lib.kvs_status_string(code).decode() == name
 
@@ -50,7 +50,7 @@ def _score(lib, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(Q=None), 1), (dict(lse=None), 1), (dict(w_t=None), 1),
     (dict(Hq=7), 1), (dict(q_pos0=49), 1), (dict(q_pos0=-1), 1), (dict(N=0), 1), (dict(W=0), 1),
-    (dict(d=96), 2), (dict(Hq=12, Hkv=2), 2),
+    (dict(d=96), 2), (dict(Hq=12, Hkv=2), 2), (dict(Hq=6, Hkv=2), 2),    # G = 6, G = 3
     (dict(mode=L.MODE_LSE | L.MODE_KVZIP | L.MODE_KVZIP_PLUS, s_plus=1 << 20), 1),
     (dict(mode=L.MODE_LSE | L.MODE_KVZIP_PLUS, s_plus=1 << 20, D=64), 1),   # V, h, W_O missing
     (dict(mode=1 << 9), 1),
@@ -93,6 +93,20 @@ def test_alloc_and_pack_argument_errors(lib):
     assert lib.kvs_quantize_pack(p, 8, 64, 128, 2, p, None, ctypes.byref(s), p, 1 << 20, None) == 1  # bad axis
     assert lib.kvs_quantize_pack(p, 8, 64, 96, 0, p, None, ctypes.byref(s), p, 1 << 20, None) == 2
     assert lib.kvs_unit_rms(p, 8, 64, 128, 3, None, p, p, 1 << 20, None) == 1
+    # pooled allocation and packing
+    assert lib.kvs_allocate_bits_pools(p, p, -1, 10, 5, L.WIDTHS_ALL, p, p, 1 << 20, None) == 1
+    assert lib.kvs_allocate_bits_pools(p, p, 0, 10, 5, L.WIDTHS_ALL, p, p, 1 << 20, None) == 0   # no pools
+    assert lib.kvs_allocate_bits_pools(p, p, 1 << 16, 10, 5, L.WIDTHS_ALL, p, p, 1 << 20, None) == 2
+    assert lib.kvs_quantize_pack_pools(p, 0, 8, 64, 128, 0, p, None, ctypes.byref(s), p, 1 << 20, None) == 1
+    assert lib.kvs_quantize_pack_pools(p, 2, 8, 64, 96, 0, p, None, ctypes.byref(s), p, 1 << 20, None) == 2
+    assert lib.kvs_dequantize_pools(ctypes.byref(s), 3, 8, 64, 128, 2, p, None, p, p, 1 << 20, None) == 1
+    assert lib.kvs_pack_pools_workspace_size(4, 8, 8192, 128, 1) >= 4 * 8 * 8192 * 4     # kept-token index per head
+    assert lib.kvs_pack_pools_workspace_size(1, 8, 8192, 128, 1) == lib.kvs_pack_workspace_size(8, 8192, 128, 1)
+    assert lib.kvs_pack_pools_workspace_size(1 << 16, 1, 64, 128, 0) == 0
+    info = (ctypes.c_int64 * 3)()
+    assert lib.kvs_allocate_plan_info(-1, L.WIDTHS_ALL, info) == 1
+    assert lib.kvs_allocate_plan_info(10, 1 << 3, info) == 1
+    assert lib.kvs_allocate_plan_info(0, L.WIDTHS_ALL, info) == 0 and list(info) == [0, 0, 0]
     assert lib.kvs_channel_weights(p, p, 8, 3, 16, 64, 128, p, p, 1 << 20, None) == 1
 
 

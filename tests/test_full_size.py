@@ -154,6 +154,15 @@ def test_kvzip_plus_full_size():
     for g in (0, 7):
         wo_heads = np.stack([f64(t["W_O"][:, (g * G + i) * d:(g * G + i + 1) * d]) for i in range(G)])
         check_tail_keys(sp, t["Q"], t["K"], G, 0, g, 300, "s_plus", V=t["V"], h=t["h"], W_O_heads=wo_heads)
+    # every key of KV group 5 (their column maxima merged over pass 2's splits) against the oracle
+    assert L.score_plan_info(wl.Hq, wl.Hkv, wl.N, wl.N, d, D=wl.D, q_pos0=0,
+                             mode=L.MODE_LSE | L.MODE_KVZIP_PLUS)[3] > 1
+    g = 5
+    wo_heads = np.stack([f64(t["W_O"][:, (g * G + i) * d:(g * G + i + 1) * d]) for i in range(G)])
+    per = per_head_scores(f64(t["Q"][g * G:(g + 1) * G]), f64(t["K"][g]), 0, V=f64(t["V"][g]), h=f64(t["h"]),
+                          W_O_heads=wo_heads, workers=G)
+    assert_scores_close(sp[g], np.max([p["s_plus"] for p in per], axis=0), f"s_plus group {g}")
+    assert_lse_close(lse[g * G:(g + 1) * G], np.stack([p["lse"] for p in per]))
     # evict the bottom 80%: widths {0,16}, sigma = 1, B = 16 * keep -> exactly the top keys stay
     U = wl.Hkv * wl.N
     B = synth.kvzip_keep_budget(U, wl.evict_fraction)
@@ -242,34 +251,59 @@ def test_long_context_alloc_pack(long_layer, avg_bits):
 # ---------------------------------------------------------------------------
 # full model: 32 layers x 16 sequences, sampled (layer, sequence) pools
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("layer,seq", [(0, 0), (31, 15)])
-def test_full_model_sampled_pools(layer, seq):
+def test_full_model_pooled_layer():
+    """One layer of the full-model batch, its 16 sequences as 16 pools of one
+    pooled step (inputs drawn on the device): every KV head's weights sum to
+    G * W; sampled pools against the oracle on that pool alone, allocation
+    and packing fed the oracle's weights bit-exact inside the pooled calls."""
     wl = synth.WORKLOADS["full_model_l32_b16_n16384"]
-    t = synth.make_layer(wl, layer, seq)
-    Q, K, V = (t[k].to(DEV) for k in ("Q", "K", "V"))
+    layer, P = 31, wl.seqs
+    t = synth.make_pools(wl, layer, range(P), device=DEV)
     avg = wl.avg_bits[0]
-    step = RdkvLayerStep(wl.Hq, wl.Hkv, wl.N, wl.W, wl.d, avg, device=DEV)
-    step.run(Q, K, V)
+    step = RdkvLayerStep(wl.Hq, wl.Hkv, wl.N, wl.W, wl.d, avg, device=DEV, n_pools=P)
+    step.run(t["Q"], t["K"], t["V"])
     torch.cuda.synchronize()
     assert L.device_error() == 0
-    x = {k: f64(t[k]) for k in ("Q", "K", "V")}
-    ref = O.rdkv_compress(x["Q"], x["K"], x["V"], wl.q_pos0, avg)
-    assert_lse_close(step.out["lse"].cpu().numpy(), ref["scores"]["lse"])
-    assert_scores_close(step.out["w_t"].cpu().numpy(), ref["scores"]["w_t"], "w_t")
-    np.testing.assert_allclose(step.w_c.cpu().numpy(), ref["w_c"], rtol=TOL)
-    np.testing.assert_allclose(step.sig_t.cpu().numpy(), ref["sigma_t"], rtol=TOL)
-    bits_v = gpu_alloc(ref["scores"]["w_t"].astype(np.float32).ravel(), ref["sigma_t"].ravel(), step.B_v)
-    assert (bits_v == ref["bits_v"]).all()
-    bits_k = gpu_alloc(ref["w_c"].ravel(), ref["sigma_c"].ravel(), step.B_k)
-    assert (bits_k == ref["bits_k"]).all()
-    bv, bk = torch.from_numpy(bits_v).to(DEV), torch.from_numpy(bits_k).to(DEV)
-    sv = L.Streams(wl.Hkv, wl.N, wl.d, 0, step.B_v, DEV)
-    L.quantize_pack(V, 0, bv, None, sv)
-    sk = L.Streams(wl.Hkv, wl.N, wl.d, 1, step.B_k, DEV)
-    L.quantize_pack(K, 1, bk, bv, sk)
-
-    _cmp_streams(sv, ref["v_streams"])
-    _cmp_streams(sk, ref["k_streams"])
-    assert np.array_equal(L.dequantize(sv, bv, None).cpu().numpy(),
-                          O.dequantize(ref["v_streams"], (wl.Hkv, wl.N, wl.d), 0, bits_v))
+    wt = step.out["w_t"]
+    np.testing.assert_allclose(wt.double().sum(dim=1).cpu().numpy(), wl.G * wl.W, rtol=1e-4)
+    Hq, Hkv, N, d = wl.Hq, wl.Hkv, wl.N, wl.d
+    wv, sv = wt.view(P, -1).clone(), step.sig_t.view(P, -1).clone()
+    wk, sk = step.w_c.view(P, -1).clone(), step.sig_c.view(P, -1).clone()
+    refs = {}
+    for q in (0, P - 1):
+        x = [f64(t[k][q * h:(q + 1) * h]) for k, h in (("Q", Hq), ("K", Hkv), ("V", Hkv))]
+        ref = O.rdkv_compress(x[0], x[1], x[2], wl.q_pos0, avg)
+        refs[q] = ref
+        assert_lse_close(step.out["lse"][q * Hq:(q + 1) * Hq].cpu().numpy(), ref["scores"]["lse"])
+        assert_scores_close(wt[q * Hkv:(q + 1) * Hkv].cpu().numpy(), ref["scores"]["w_t"], f"w_t pool {q}")
+        np.testing.assert_allclose(step.w_c[q * Hkv:(q + 1) * Hkv].cpu().numpy(), ref["w_c"], rtol=TOL)
+        np.testing.assert_allclose(step.sig_t[q * Hkv:(q + 1) * Hkv].cpu().numpy(), ref["sigma_t"], rtol=TOL)
+        wv[q] = torch.from_numpy(ref["scores"]["w_t"].astype(np.float32).ravel())
+        sv[q] = torch.from_numpy(ref["sigma_t"].ravel())
+        wk[q] = torch.from_numpy(ref["w_c"].ravel())
+        sk[q] = torch.from_numpy(ref["sigma_c"].ravel())
+    bits_v = L.allocate_bits_pools(wv, sv, step.B_v)
+    bits_k = L.allocate_bits_pools(wk, sk, step.B_k)
+    X4 = (P, Hkv, N, d)
+    vs = L.Streams(Hkv, N, d, 0, step.B_v, DEV, n_pools=P)
+    L.quantize_pack_pools(t["V"].view(X4), 0, bits_v, None, vs)
+    ks = L.Streams(Hkv, N, d, 1, step.B_k, DEV, n_pools=P)
+    L.quantize_pack_pools(t["K"].view(X4), 1, bits_k, bits_v, ks)
+    vh = L.dequantize_pools(vs, bits_v, None)
+    torch.cuda.synchronize()
+    assert L.device_error() == 0
+    for q, ref in refs.items():
+        assert (bits_v[q].cpu().numpy() == ref["bits_v"]).all()
+        assert (bits_k[q].cpu().numpy() == ref["bits_k"]).all()
+        _cmp_streams(vs.pool(q), ref["v_streams"])
+        _cmp_streams(ks.pool(q), ref["k_streams"])
+        assert np.array_equal(vh[q].cpu().numpy(), O.dequantize(ref["v_streams"], (Hkv, N, d), 0, ref["bits_v"]))
+    # the pools the oracle did not see: the pooled calls equal one-pool calls
+    for q in (1, 7):
+        assert torch.equal(bits_v[q], L.allocate_bits(wv[q], sv[q], step.B_v))
+        one = L.Streams(Hkv, N, d, 0, step.B_v, DEV)
+        L.quantize_pack(t["V"][q * Hkv:(q + 1) * Hkv], 0, bits_v[q], None, one)
+        a, b = one.host_view(), vs.pool(q).host_view()
+        for wd in (2, 4, 8, 16):
+            assert np.array_equal(a[wd]["codes"], b[wd]["codes"]) and np.array_equal(a[wd]["ids"], b[wd]["ids"])
     assert L.device_error() == 0

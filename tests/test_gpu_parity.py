@@ -295,3 +295,100 @@ def test_one_graph_step_matches_the_eager_step():
     assert torch.equal(a.sig_t, b.sig_t) and torch.equal(a.bits_v, b.bits_v) and torch.equal(a.bits_k, b.bits_k)
     assert torch.equal(a.v_hat, b.v_hat) and torch.equal(a.k_hat, b.k_hat)
     assert torch.equal(a.out["w_t"], b.out["w_t"])
+
+
+def test_scores_kvzip_plus_split_merge():
+    """KVzip+ with pass 2 split over several CTAs per key tile: the column max of
+    a_{r,t} |h_r| is merged across the splits, and the 1 / |W_O^h v_t| factor
+    is applied after it   [KVzap §2.1, KVzip+]."""
+    Hq, Hkv, W, N, d, D = 8, 2, 700, 700, 128, 256
+    mode = L.MODE_LSE | L.MODE_KVZIP_PLUS
+    assert L.score_plan_info(Hq, Hkv, W, N, d, D=D, q_pos0=0, mode=mode)[3] > 1   # the merge runs
+    Q, K, V = rand_layer(Hq, Hkv, W, N, d, seed=4242, scale=1.4, sinks=3)
+    g = torch.Generator().manual_seed(4243)
+    h = (torch.randn(W, D, generator=g) * torch.exp(0.5 * torch.randn(W, 1, generator=g))).bfloat16()
+    WO = (torch.randn(D, Hq * d, generator=g) / math.sqrt(D)).bfloat16()
+    ref = O.attention_scores(f64(Q), f64(K), 0, V=f64(V), h=f64(h), W_O=f64(WO))
+    out = L.score_attention(Q.to(DEV), K.to(DEV), q_pos0=0, mode=mode, V=V.to(DEV), h=h.to(DEV), W_O=WO.to(DEV))
+    torch.cuda.synchronize()
+    assert L.device_error() == 0
+    assert_lse_close(out["lse"].cpu().numpy(), ref["lse"])
+    assert_scores_close(out["s_plus"].cpu().numpy(), ref["s_plus"], "s_plus")
+
+
+# ---------------------------------------------------------------------------
+# pooled calls: several (layer, sequence) pools of one shape in one call
+# ---------------------------------------------------------------------------
+def _pooled_inputs(P, Hq, Hkv, W, N, d, seed):
+    parts = [rand_layer(Hq, Hkv, W, N, d, seed=seed + 31 * q, scale=1.3, sinks=2) for q in range(P)]
+    return tuple(torch.cat([p[i] for p in parts]).contiguous() for i in range(3))
+
+
+@pytest.mark.parametrize("P,Hq,Hkv,W,N,d", [(3, 8, 2, 130, 700, 128), (2, 4, 4, 64, 300, 64),
+                                            (4, 32, 8, 96, 1000, 128)])
+def test_pooled_step_vs_oracle(P, Hq, Hkv, W, N, d):
+    """n_pools pools through one pooled step: every pool's scores match the
+    oracle on that pool alone; pooled allocation, packing and dequantisation
+    fed the oracle's weights and widths are bit-exact per pool."""
+    Q, K, V = _pooled_inputs(P, Hq, Hkv, W, N, d, seed=P * 1000 + N)
+    avg = 3
+    step = RdkvLayerStep(Hq, Hkv, N, W, d, avg, device=DEV, n_pools=P)
+    step.run(Q.to(DEV), K.to(DEV), V.to(DEV))
+    torch.cuda.synchronize()
+    assert L.device_error() == 0
+    q_pos0 = N - W
+    refs = []
+    for q in range(P):
+        x = [f64(t[q * h:(q + 1) * h]) for t, h in ((Q, Hq), (K, Hkv), (V, Hkv))]
+        ref = O.rdkv_compress(x[0], x[1], x[2], q_pos0, avg)
+        refs.append(ref)
+        assert_lse_close(step.out["lse"][q * Hq:(q + 1) * Hq].cpu().numpy(), ref["scores"]["lse"])
+        assert_scores_close(step.out["w_t"][q * Hkv:(q + 1) * Hkv].cpu().numpy(), ref["scores"]["w_t"], f"w_t {q}")
+        np.testing.assert_allclose(step.w_c[q * Hkv:(q + 1) * Hkv].cpu().numpy(), ref["w_c"], rtol=TOL)
+        np.testing.assert_allclose(step.sig_t[q * Hkv:(q + 1) * Hkv].cpu().numpy(), ref["sigma_t"], rtol=TOL)
+    # stage 2 and 3 on the oracle's weights, all pools in one call
+    wv = torch.from_numpy(np.stack([r["scores"]["w_t"].astype(np.float32).ravel() for r in refs])).to(DEV)
+    sv = torch.from_numpy(np.stack([r["sigma_t"].ravel() for r in refs])).to(DEV)
+    bits_v = L.allocate_bits_pools(wv, sv, step.B_v)
+    wk = torch.from_numpy(np.stack([r["w_c"].ravel() for r in refs])).to(DEV)
+    sk = torch.from_numpy(np.stack([r["sigma_c"].ravel() for r in refs])).to(DEV)
+    bits_k = L.allocate_bits_pools(wk, sk, step.B_k)
+    torch.cuda.synchronize()
+    for q, r in enumerate(refs):
+        assert (bits_v[q].cpu().numpy() == r["bits_v"]).all(), q
+        assert (bits_k[q].cpu().numpy() == r["bits_k"]).all(), q
+    Vd, Kd = V.to(DEV).view(P, Hkv, N, d), K.to(DEV).view(P, Hkv, N, d)
+    vs = L.Streams(Hkv, N, d, 0, step.B_v, DEV, n_pools=P)
+    L.quantize_pack_pools(Vd, 0, bits_v, None, vs)
+    ks = L.Streams(Hkv, N, d, 1, step.B_k, DEV, n_pools=P)
+    L.quantize_pack_pools(Kd, 1, bits_k, bits_v, ks)
+    vh = L.dequantize_pools(vs, bits_v, None)
+    kh = L.dequantize_pools(ks, bits_k, bits_v)
+    torch.cuda.synchronize()
+    assert L.device_error() == 0
+    for q, r in enumerate(refs):
+        _cmp_streams(vs.pool(q), r["v_streams"])
+        _cmp_streams(ks.pool(q), r["k_streams"])
+        assert np.array_equal(vh[q].cpu().numpy(), O.dequantize(r["v_streams"], (Hkv, N, d), 0, r["bits_v"]))
+        assert np.array_equal(kh[q].cpu().numpy(),
+                              O.dequantize(r["k_streams"], (Hkv, N, d), 1, r["bits_k"], r["keep"]))
+        # a pool's view reads back through the one-pool call too
+        assert np.array_equal(L.dequantize(vs.pool(q), bits_v[q], None).cpu().numpy(), vh[q].cpu().numpy())
+
+
+@pytest.mark.parametrize("U,P", [(1000, 5), (70000, 3), (400000, 2)])
+def test_pooled_allocation_matches_single_calls(U, P):
+    """allocate_bits_pools equals one allocate_bits call per pool, on the
+    cluster path and (400 000 units) on the cooperative-grid path."""
+    rng = np.random.default_rng(U + P)
+    w = (rng.random((P, U)) ** 3 * 10).astype(np.float32)
+    s = (rng.random((P, U)) + 0.05).astype(np.float32)
+    w[rng.random((P, U)) < 0.05] = 0
+    w[:, ::11] = w[:, 5:6]
+    wd, sd = torch.from_numpy(w).to(DEV), torch.from_numpy(s).to(DEV)
+    for avg in (0.7, 3.0):
+        B = int(math.floor(avg * U))
+        got = L.allocate_bits_pools(wd, sd, B)
+        for q in range(P):
+            assert torch.equal(got[q], L.allocate_bits(wd[q], sd[q], B)), (avg, q)
+    assert L.device_error() == 0

@@ -53,6 +53,10 @@ SCRATCH_SIZES = {L.WIDTHS_ALL: (400000, 250000), L.WIDTHS_KEEP_OR_EVICT: (100000
 def test_static_scratch_matches_workspace_allocator_twice(mask):
     # the first call is the larger one, so stale scratch would be visible in the second
     big, small = SCRATCH_SIZES[mask]
+    for U in (big, small):
+        cl, blocks, ws_bytes = L.allocate_plan_info(U, mask)
+        # the grid path, whose scratch lives in the library's array, and it fits there
+        assert cl == 0 and blocks > 0 and 0 < ws_bytes <= L.lib().kvs_allocate_workspace_size(U)
     for U, seed, avg in ((big, 1, 3.0), (small, 2, 2.5)):
         w, s = _weights(U, seed)
         budget = int(math.floor(avg * U))
