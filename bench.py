@@ -235,6 +235,35 @@ def oracle_group_step(wl, host, g):
     O.rdkv_compress(Q, Kx, Vx, wl.q_pos0, wl.avg_bits[0])
 
 
+KVZIP_ORACLE_ROWS = 1024
+
+
+def time_oracle_kvzip(wl, host, min_seconds=10.0):
+    """KVzip+: the oracle's score pass (materialised attention, the norms, the
+    column maxima) for one query head over the last KVZIP_ORACLE_ROWS query
+    rows against all keys, repeated until min_seconds; its time per visible
+    (row, key) pair is scaled to the whole layer (all heads, all N x N causal
+    pairs).  Returns (layer tokens/s, slices, seconds)."""
+    import numpy as np
+    import oracle as O
+    R, N, d = KVZIP_ORACLE_ROWS, wl.N, wl.d
+    f = lambda t: t.float().numpy().astype(np.float64)
+    Kg, Vg, h = f(host["K"][:1]), f(host["V"][:1]), f(host["h"][N - R:])
+    slices, t0 = 0, time.perf_counter()
+    while True:
+        hd = slices % wl.G
+        Qh = f(host["Q"][hd:hd + 1, N - R:])
+        O.attention_scores(Qh, Kg, N - R, V=Vg, h=h, W_O=f(host["W_O"][:, hd * d:(hd + 1) * d]))
+        slices += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    dt = time.perf_counter() - t0
+    pairs_slice = R * (N - R) + R * (R + 1) // 2
+    pairs_layer = wl.Hq * N * (N + 1) // 2
+    layer_s = dt / slices / pairs_slice * pairs_layer
+    return N / layer_s, slices, dt
+
+
 def time_oracle(wl, host, min_seconds=10.0):
     """Runs the oracle group by group until min_seconds; returns (layer tokens/s, groups, seconds)."""
     groups, t0 = 0, time.perf_counter()
@@ -248,9 +277,12 @@ def time_oracle(wl, host, min_seconds=10.0):
 
 
 def workload_config(wl):
-    return {"workload": wl.name, "Hq": wl.Hq, "Hkv": wl.Hkv, "N": wl.N, "W": wl.W, "d": wl.d,
-            "avg_bits": wl.avg_bits[0], "widths": list(wl.widths), "pools_per_step_per_gpu": 1,
-            "l2": "flushed between timed steps (256 MB write, untimed)", "parallelism": "replicas"}
+    c = {"workload": wl.name, "Hq": wl.Hq, "Hkv": wl.Hkv, "N": wl.N, "W": wl.W, "d": wl.d,
+         "avg_bits": wl.avg_bits[len(wl.avg_bits) // 2], "widths": list(wl.widths), "pools_per_step_per_gpu": 1,
+         "l2": "flushed between timed steps (256 MB write, untimed)", "parallelism": "replicas"}
+    if wl.mode == "kvzip_plus":
+        c.update({"mode": "kvzip_plus", "D": wl.D, "evict_fraction": wl.evict_fraction, "avg_bits": None})
+    return c
 
 
 # ---------------------------------------------------------------------------
@@ -262,6 +294,22 @@ def run_reference(args):
         return 0
     from kv_cache_compression_flash_b300 import synth
     wl = synth.WORKLOADS[args.workload]
+    if wl.mode == "kvzip_plus":
+        host = synth.make_layer(wl)
+        time_oracle_kvzip(wl, host, min_seconds=0.0)          # warm
+        v, n, dt = time_oracle_kvzip(wl, host, min_seconds=20.0)
+        sample = (f"{n} slices of the fp64 oracle's KVzip+ score pass in {dt:.1f} s (one slice = 1 query head x "
+                  f"the last {KVZIP_ORACLE_ROWS} query rows x all {wl.N} keys); time per visible pair scaled to "
+                  f"the whole layer")
+        value = v / 1e6
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": n, "warmup": 1, "ms_per_step": 1e3 * dt / n, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_config(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return 0
     pools = FULL_MODEL_ORACLE_POOLS if wl.name == FULL_MODEL else ((0, 0),)
     hosts = [synth.make_layer(wl, l, q) for l, q in pools]
     for i in range(args.warmup):
@@ -287,6 +335,15 @@ def run_reference(args):
     return 0
 
 
+def make_step(wl, host, dev, avg, h_dev=None):
+    """The workload's step: RDKV compression, or KVzap's eviction by KVzip+ score."""
+    from kv_cache_compression_flash_b300.pipeline import KvzipStep, RdkvLayerStep
+    if wl.mode == "kvzip_plus":
+        h = h_dev if h_dev is not None else host["h"].to(dev)
+        return KvzipStep(wl.Hq, wl.Hkv, wl.N, wl.W, wl.d, wl.evict_fraction, h, host["W_O"].to(dev), device=dev)
+    return RdkvLayerStep(wl.Hq, wl.Hkv, wl.N, wl.W, wl.d, avg, device=dev)
+
+
 def run_ours(args):
     import torch
 
@@ -304,9 +361,11 @@ def run_ours(args):
 
     wl = synth.WORKLOADS[args.workload]
     host = synth.make_layer(wl, layer=rank)                  # each rank: its own pool
-    pinned = {k: host[k].pin_memory() for k in ("Q", "K", "V")}
+    in_keys = ("Q", "K", "V", "h") if wl.mode == "kvzip_plus" else ("Q", "K", "V")
+    pinned = {k: host[k].pin_memory() for k in in_keys}
     Q, K, V = (pinned[k].to(dev) for k in ("Q", "K", "V"))
-    step = RdkvLayerStep(wl.Hq, wl.Hkv, wl.N, wl.W, wl.d, wl.avg_bits[0], device=dev)
+    avg = wl.avg_bits[len(wl.avg_bits) // 2]                 # the middle budget of a sweep
+    step = make_step(wl, host, dev, avg)
     step.capture(Q, K, V)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
@@ -369,33 +428,64 @@ def run_ours(args):
                 "traffic": recorded_traffic(kname, wl.name),
                 "duration_note": "segment time: the pass kernel plus its small merge kernel"}
 
-    e2e = run_e2e(args, step, pinned, (Q, K, V), flush, dist, dev, world, wl)
+    # a budget sweep: the post-scoring segment (allocation, packing, dequantisation)
+    # at every average budget of the workload, the scores computed once
+    sweep = {}
+    if len(wl.avg_bits) > 1:
+        for b in wl.avg_bits:
+            sb = step if b == avg else make_step(wl, host, dev, b)
+            if sb is not step:
+                sb.capture(Q, K, V)
+            ts = []
+            for i in range(min(args.steps, 20)):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                sb.graphs["rest"].replay()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            sweep[str(b)] = {"rest_ms": statistics.fmean(ts), "step_ms": seg_avg[0] + seg_avg[1] + statistics.fmean(ts),
+                             "M_tok_s": wl.N / ((seg_avg[0] + seg_avg[1] + statistics.fmean(ts)) / 1e3) / 1e6}
+        if L.device_error() != 0:
+            raise SystemExit("device error during the budget sweep")
+
+    e2e = run_e2e(args, step, pinned, (Q, K, V), flush, dist, dev, world, wl, avg)
 
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": statistics.fmean(step_ms), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(wl),
-        "segments_ms": {"pass1_lse": seg_avg[0], "pass2_token_weights": seg_avg[1], "rest": seg_avg[2]},
+        "segments_ms": {"pass1_lse": seg_avg[0], "pass2": seg_avg[1], "rest": seg_avg[2]},
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": step.kernel_launches() * args.steps,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                    "samples": clk["samples"], "window": "1 s soak of the same step, then the timed steps"},
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if sweep:
+        out["budget_sweep"] = sweep
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and wl.mode == "kvzip_plus":
+        v, n, dt = time_oracle_kvzip(wl, host)
+        out["cpu_baseline"] = {"value": v / 1e6, "unit": UNIT, "cores": oracle_cores(), "kind": "oracle",
+                               "sample": f"{n} slices of the fp64 oracle's KVzip+ score pass in {dt:.1f} s (one "
+                                         f"slice = 1 query head x the last {KVZIP_ORACLE_ROWS} query rows x all "
+                                         f"{wl.N} keys); time per visible pair scaled to the whole layer"}
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, groups, dt = time_oracle(wl, host)
         out["cpu_baseline"] = {"value": v / 1e6, "unit": UNIT, "cores": oracle_cores(), "kind": "oracle",
                                "sample": f"{groups} KV groups of this layer through the fp64 oracle in {dt:.1f} s "
                                          f"(one group = {wl.G} query heads x 1 KV head; N/Hkv tokens each)"}
     if rank == 0:
         print(json.dumps(out))
+        log_result(out)
     if dist is not None:
         dist.destroy_process_group()
     return 0
 
 
-def run_e2e(args, step, pinned, dev_inputs, flush, dist, dev, world, wl):
+def run_e2e(args, step, pinned, dev_inputs, flush, dist, dev, world, wl, avg):
     """Pinned host Q, K, V in; the packed streams and widths a caller keeps, out.
 
     Two pools in flight, as a serving loop would run them: while step i
@@ -405,10 +495,10 @@ def run_e2e(args, step, pinned, dev_inputs, flush, dist, dev, world, wl):
     the wall clock over all steps.  Inputs arrive by copy every step, so no L2
     flush is needed between steps."""
     import torch
-    from kv_cache_compression_flash_b300.pipeline import RdkvLayerStep
-    h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in ("Q", "K", "V"))
+    h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in pinned)
     # the second pool: its own inputs, outputs and captured graphs
-    step2 = RdkvLayerStep(wl.Hq, wl.Hkv, wl.N, wl.W, wl.d, wl.avg_bits[0], device=dev)
+    step2 = make_step(wl, {"W_O": step.W_O.cpu()} if hasattr(step, "W_O") else None, dev, avg,
+                      h_dev=torch.empty_like(step.h) if hasattr(step, "h") else None)
     inputs2 = tuple(torch.empty_like(x) for x in dev_inputs)
     for x, k in zip(inputs2, ("Q", "K", "V")):
         x.copy_(pinned[k])
@@ -440,6 +530,8 @@ def run_e2e(args, step, pinned, dev_inputs, flush, dist, dev, world, wl):
             Q.copy_(pinned["Q"], non_blocking=True)
             K.copy_(pinned["K"], non_blocking=True)
             V.copy_(pinned["V"], non_blocking=True)
+            if "h" in pinned:                  # KVzip+: the window's hidden states are an input too
+                st.h.copy_(pinned["h"], non_blocking=True)
             ev_in[s].record(cp)
         comp.wait_event(ev_in[s])
         if i >= 2:

@@ -68,6 +68,23 @@ int kvs_version(void);
  * else the first recorded code; KVS_ERR_CUDA if the read itself failed. */
 int kvs_get_device_error(void* stream);
 
+/* Test hook for failure handling; the papers have no counterpart.  Plants a
+ * fault in later launches so that a test can watch a bounded device wait run
+ * out, and shortens the wait limit so that it runs out quickly:
+ *   fault = KVS_DEBUG_WITHHOLD_LSE_ARRIVE: in each pass-1 CTA the MMA issuer
+ *           withholds the arrive that hands its first logit tile to the
+ *           reducers, whose wait then times out (KVS_ERR_TIMEOUT in the error
+ *           word; the CTA drains its copies and MMAs, frees its tensor memory
+ *           and returns; later kernels of the call skip their work);
+ *   fault = KVS_DEBUG_NONE: no fault;
+ *   wait_limit_ns = 0 restores the default limit (2 s); otherwise it is
+ *           clamped to [1 ms, 2 s].
+ * Synchronous (waits for the device); returns KVS_ERR_CUDA if the update fails.
+ * Reset with kvs_debug_inject(KVS_DEBUG_NONE, 0) before normal use. */
+#define KVS_DEBUG_NONE 0u
+#define KVS_DEBUG_WITHHOLD_LSE_ARRIVE 1u
+int kvs_debug_inject(uint32_t fault, uint64_t wait_limit_ns);
+
 /* ---- importance scoring ------------------------------------------------ */
 #define KVS_MODE_LSE         1u  /* lse[Hq, W]  = ln sum_{t<=p_r} exp(s_{r,t})         [KVSculpt §2, LSE term] */
 #define KVS_MODE_RDKV_WT     2u  /* w_t[Hkv, N] = sum over the group's heads and window rows of a_{r,t}
@@ -143,6 +160,14 @@ size_t kvs_unit_rms_workspace_size(int64_t Hkv, int64_t N, int64_t d, int axis);
 int kvs_unit_rms(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis,
                  const uint8_t* keep_bits, float* sigma,
                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Stage 3's two channel quantities from ONE read of the keys: w_c as
+ * kvs_channel_weights computes it (every token of K) and sigma_c as
+ * kvs_unit_rms(K, axis 1, keep_bits) computes it (the kept tokens)
+ * [RDKV §2.1 w_c; §2.2 stage 3 over the retained tokens].  keep_bits NULL
+ * keeps every token.  w_c, sigma_c: float [Hkv, d].  No workspace. */
+int kvs_channel_stats(const uint16_t* Q, const uint16_t* K, const uint8_t* keep_bits, int64_t Hq, int64_t Hkv,
+                      int64_t W, int64_t N, int64_t d, float* w_c, float* sigma_c, void* stream);
 
 /* ---- bit allocation ---------------------------------------------------- */
 /* Width set as a bit mask: bit b set <=> width b allowed.  Width 0 (evict) is

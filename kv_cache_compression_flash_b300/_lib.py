@@ -35,11 +35,13 @@ SIGNATURES = {
     "kvs_status_string": (c_char_p, [c_int]),
     "kvs_version": (c_int, []),
     "kvs_get_device_error": (c_int, [c_void_p]),
+    "kvs_debug_inject": (c_int, [c_uint32, ctypes.c_uint64]),
     "kvs_score_workspace_size": (c_size_t, [c_int64] * 7 + [c_uint32]),
     "kvs_score_attention": (c_int, [c_void_p] * 5 + [c_int64] * 7 + [c_uint32] + [c_void_p] * 4 + [c_size_t, c_void_p]),
     "kvs_score_plan_info": (c_int, [c_int64] * 7 + [c_uint32, POINTER(c_int64)]),
     "kvs_channel_weights_workspace_size": (c_size_t, [c_int64] * 5),
     "kvs_channel_weights": (c_int, [c_void_p, c_void_p] + [c_int64] * 5 + [c_void_p, c_void_p, c_size_t, c_void_p]),
+    "kvs_channel_stats": (c_int, [c_void_p] * 3 + [c_int64] * 5 + [c_void_p] * 3),
     "kvs_unit_rms_workspace_size": (c_size_t, [c_int64] * 3 + [c_int]),
     "kvs_unit_rms": (c_int, [c_void_p] + [c_int64] * 3 + [c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "kvs_allocate_workspace_size": (c_size_t, [c_int64]),
@@ -151,6 +153,15 @@ def _ws(ws, key, nbytes, device):
     return ws.get(nbytes, device)
 
 
+DEBUG_NONE = 0
+DEBUG_WITHHOLD_LSE_ARRIVE = 1
+
+
+def debug_inject(fault=DEBUG_NONE, wait_limit_ns=0):
+    """Test hook: plant a device fault in later launches and set the wait limit (0 = default)."""
+    _check(lib().kvs_debug_inject(fault, wait_limit_ns), "kvs_debug_inject")
+
+
 def device_error(stream=None) -> int:
     """Reads and clears the library's device error word (synchronises the stream)."""
     return lib().kvs_get_device_error(_stream(stream))
@@ -212,6 +223,18 @@ def channel_weights(Q, K, *, out=None, ws=None, stream=None):
     _check(L.kvs_channel_weights(_ptr(Q), _ptr(K), Hq, Hkv, W, N, d, _ptr(w_c), _ptr(buf), buf.numel(),
                                  _stream(stream)), "kvs_channel_weights")
     return w_c
+
+
+def channel_stats(Q, K, keep_bits=None, *, out_wc=None, out_sigma=None, stream=None):
+    """(w_c, sigma_c) float32 [Hkv, d] from one read of K: w_c over every token, sigma_c over the kept ones."""
+    _bf16(Q, "Q"), _bf16(K, "K")
+    Hq, W, d = Q.shape
+    Hkv, N, _ = K.shape
+    w_c = out_wc if out_wc is not None else torch.empty(Hkv, d, dtype=torch.float32, device=Q.device)
+    sc = out_sigma if out_sigma is not None else torch.empty(Hkv, d, dtype=torch.float32, device=Q.device)
+    _check(lib().kvs_channel_stats(_ptr(Q), _ptr(K), _ptr(keep_bits), Hq, Hkv, W, N, d, _ptr(w_c), _ptr(sc),
+                                   _stream(stream)), "kvs_channel_stats")
+    return w_c, sc
 
 
 def unit_rms(X, axis, keep_bits=None, *, out=None, ws=None, stream=None):

@@ -32,6 +32,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // every wait on another agent gives up after this long and records KVS_ERR_TIMEOUT
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// Test hooks (kvs_debug_inject): the wait limit in force, and a fault the
+// kernels plant on purpose so that a test can watch a bounded wait run out.
+// Read only where a wait has already spun, or once per launch.
+__device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+__device__ int g_debug_fault;
+
+__device__ __forceinline__ uint64_t wait_limit_ns() {
+  return *reinterpret_cast<volatile unsigned long long*>(&g_wait_limit_ns);
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -69,7 +79,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
-// when *abort_flag becomes nonzero or after kWaitLimitNs (then sets the flag
+// when *abort_flag becomes nonzero or after the wait limit (then sets the flag
 // and records KVS_ERR_TIMEOUT).  Returns false when it gave up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -82,7 +92,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
         *abort_flag = 1;
         return false;
       }
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > wait_limit_ns()) {
         *abort_flag = 1;
         record_error(KVS_ERR_TIMEOUT);
         return false;
@@ -294,7 +304,7 @@ __device__ __forceinline__ bool grid_barrier(GridSync* gs, unsigned int nblocks)
       const uint64_t t0 = global_timer_ns();
       while (*gen == g0) {
         __nanosleep(64);
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > wait_limit_ns()) {
           record_error(KVS_ERR_TIMEOUT);
           ok = 0;
           break;

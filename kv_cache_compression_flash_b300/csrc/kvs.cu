@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "alloc.cuh"
+#include "api.cuh"
 #include "alloc_cluster.cuh"
 #include "common.cuh"
 #include "norms.cuh"
@@ -159,19 +160,21 @@ struct PackWs {
   int* kept;
   int* n_kept;
   long long* chan_base;
+  uint32_t* row_counts;  // axis 0: per pool and chunk of kRowChunk units, the units of each stored width
 };
 
-// HKV = heads of every pool together (n_pools * Hkv)
-size_t carve_pack(int64_t HKV, int64_t N, int64_t d, int axis, void* base, size_t cap, PackWs* w) {
+size_t carve_pack(int64_t n_pools, int64_t Hkv, int64_t N, int64_t d, int axis, void* base, size_t cap, PackWs* w) {
   WsCarver c{static_cast<char*>(base), 0, cap};
+  const int64_t HKV = n_pools * Hkv;  // heads of every pool together
   w->kept = w->n_kept = nullptr;
   w->chan_base = nullptr;
+  w->row_counts = nullptr;
   if (axis == 1) {
     w->kept = c.take<int>(static_cast<size_t>(HKV * N));
     w->n_kept = c.take<int>(static_cast<size_t>(HKV));
     w->chan_base = c.take<long long>(static_cast<size_t>(HKV * d));
   } else {
-    c.take<int>(1);  // no scratch; keep a non-zero size for callers that pass one
+    w->row_counts = c.take<uint32_t>(static_cast<size_t>(n_pools * cdiv(Hkv * N, kRowChunk) * 4));
   }
   return c.used;
 }
@@ -197,66 +200,35 @@ cudaError_t launch_cluster(F fn, dim3 grid, int cl, int threads, size_t smem, cu
   return launch_k(fn, grid, dim3(static_cast<unsigned>(threads)), smem, st, cl, args...);
 }
 
-// the axis-0 plan: one cluster of CL CTAs per pool
-int launch_rows_plan(const uint8_t* bits, long long U, long long n_pools, int gpu, const StreamPtrs& sp,
-                     cudaStream_t st) {
-  static std::once_flag once;
-  static cudaError_t err = cudaSuccess;
-  std::call_once(once, [] { err = set_cluster_attrs(rows_plan_kernel<16>); });
-  if (err != cudaSuccess) return KVS_ERR_CUDA;
-  int cl = 1;
-  while (cl < 16 && static_cast<long long>(cl) * 2048 < U) cl *= 2;
-  const long long per = cdiv(U, cl);
-  const dim3 grid(static_cast<unsigned>(cl * n_pools));
-  cudaError_t e;
-  switch (cl) {
-    case 1: e = launch_cluster(rows_plan_kernel<1>, grid, 1, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
-    case 2: e = launch_cluster(rows_plan_kernel<2>, grid, 2, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
-    case 4: e = launch_cluster(rows_plan_kernel<4>, grid, 4, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
-    case 8: e = launch_cluster(rows_plan_kernel<8>, grid, 8, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
-    default: e = launch_cluster(rows_plan_kernel<16>, grid, 16, kPlanThreads, 0, st, bits, U, per, gpu, sp); break;
-  }
-  if (e != cudaSuccess) {
-    (void)cudaGetLastError();
-    return KVS_ERR_CUDA;
-  }
-  return KVS_OK;
-}
-
 template <int DH>
 int pack_dh(const uint16_t* X, int64_t n_pools, int64_t Hkv, int64_t N, int axis, const uint8_t* bits,
             const uint8_t* keep, const kvs_stream_set* s, const PackWs& w, cudaStream_t st, bool dequant, float* out) {
-  const int sms = sm_count();
   const int hkv = static_cast<int>(Hkv);
   const unsigned gy = static_cast<unsigned>(n_pools * Hkv);  // channel kernels: every pool's heads
   if (axis == 0) {
+    // per chunk of kRowChunk units, the count of each width; then one CTA per chunk, in unit order
     const long long U = Hkv * N;
-    const StreamPtrs sp = to_ptrs(s, true);
-    const long long ngroups = U * (DH / 64);
-    // about eight CTAs per SM over all the pools together
-    const long long per_pool = std::max<long long>(1, static_cast<long long>(sms) * 8 / n_pools);
-    const dim3 grid(static_cast<unsigned>(std::min<long long>(cdiv(ngroups, 16), per_pool)),
-                    static_cast<unsigned>(n_pools));
-    if (dequant) {  // decode straight from the stream entries
-      KVS_CUDA_TRY(launch_k(dequant_rows_kernel<DH>, grid, dim3(256), 0, st, 0, sp, bits, U, out));
-    } else {
-      const int rc = launch_rows_plan(bits, U, n_pools, DH / 64, sp, st);
-      if (rc) return rc;
-      KVS_CUDA_TRY(launch_k(pack_rows_kernel<DH>, grid, dim3(256), 0, st, 0, X, sp, U));
-    }
+    const StreamPtrs sp = to_ptrs(s, !dequant);
+    const int n_chunks = static_cast<int>(cdiv(U, kRowChunk));
+    const dim3 grid(static_cast<unsigned>(n_chunks), static_cast<unsigned>(n_pools));
+    KVS_CUDA_TRY(launch_k(rows_count_kernel, grid, dim3(kRowThreads), 0, st, 0, bits, U, n_chunks, w.row_counts));
+    if (dequant)
+      KVS_CUDA_TRY(launch_k(dequant_rows_kernel<DH>, grid, dim3(kRowThreads), 0, st, 0, sp, bits, U, n_chunks,
+                            static_cast<const uint32_t*>(w.row_counts), out));
+    else
+      KVS_CUDA_TRY(launch_k(pack_rows_kernel<DH>, grid, dim3(kRowThreads), 0, st, 0, X, bits, U, n_chunks,
+                            static_cast<const uint32_t*>(w.row_counts), sp));
   } else {
     const StreamPtrs sp = to_ptrs(s, !dequant);
-    if (dequant && N <= kDirectMaxN && Hkv * DH < 65536) {  // each CTA plans its own head
-      const dim3 grid(static_cast<unsigned>(cdiv(N, 64) + 1), gy);
-      KVS_CUDA_TRY(launch_k(dequant_channels_direct_kernel<DH>, grid, dim3(256), 0, st, 0, sp, static_cast<int>(N),
-                            bits, keep, out, hkv));
-      return KVS_OK;
-    }
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
       err = set_cluster_attrs(channels_plan_kernel<64>);
       if (err == cudaSuccess) err = set_cluster_attrs(channels_plan_kernel<128>);
+      if (err == cudaSuccess) err = allow_smem(pack_channels_kernel<64>, chan_pack_smem<64>());
+      if (err == cudaSuccess) err = allow_smem(pack_channels_kernel<128>, chan_pack_smem<128>());
+      if (err == cudaSuccess) err = allow_smem(dequant_channels_kernel<64>, chan_dequant_smem<64>());
+      if (err == cudaSuccess) err = allow_smem(dequant_channels_kernel<128>, chan_dequant_smem<128>());
     });
     if (err != cudaSuccess) return KVS_ERR_CUDA;
     const int cl = static_cast<int>(std::min<int64_t>(Hkv, 16));
@@ -264,13 +236,13 @@ int pack_dh(const uint16_t* X, int64_t n_pools, int64_t Hkv, int64_t N, int axis
                                 0, st, keep, static_cast<int>(N), hkv, bits, w.kept, w.n_kept, w.chan_base, sp,
                                 dequant ? 0 : 1));
     if (dequant) {
-      const dim3 grid(static_cast<unsigned>(cdiv(N, 64) + 1), gy);
-      KVS_CUDA_TRY(launch_k(dequant_channels_kernel<DH>, grid, dim3(256), 0, st, 0, sp, static_cast<int>(N), bits,
-                            w.chan_base, w.kept, w.n_kept, out, hkv));
+      const dim3 grid(static_cast<unsigned>(cdiv(N, 64 * kChanTGd) + 1), gy);
+      KVS_CUDA_TRY(launch_k(dequant_channels_kernel<DH>, grid, dim3(kChanThreads), chan_dequant_smem<DH>(), st, 0, sp,
+                            static_cast<int>(N), bits, w.chan_base, w.kept, w.n_kept, out, hkv));
     } else {
-      const dim3 grid(static_cast<unsigned>(cdiv(N, 64)), gy);
-      KVS_CUDA_TRY(launch_k(pack_channels_kernel<DH>, grid, dim3(256), 0, st, 0, X, static_cast<int>(N), bits,
-                            w.chan_base, w.kept, w.n_kept, sp, hkv));
+      const dim3 grid(static_cast<unsigned>(cdiv(cdiv(N, 64), kChanTG)), gy);
+      KVS_CUDA_TRY(launch_k(pack_channels_kernel<DH>, grid, dim3(kChanThreads), chan_pack_smem<DH>(), st, 0, X,
+                            static_cast<int>(N), bits, w.chan_base, w.kept, w.n_kept, sp, hkv));
     }
   }
   return KVS_OK;
@@ -282,12 +254,11 @@ int pack_common(const uint16_t* X, int64_t n_pools, int64_t Hkv, int64_t N, int6
   int rc = pack_shape_ok(n_pools, Hkv, N, d, axis);
   if (rc) return rc;
   if (!bits || !streams_ok(s) || (axis == 1 && !keep) || (dequant ? !out : !X)) return KVS_ERR_INVALID_ARG;
-  if ((!dequant || axis == 0) && !s->counts) return KVS_ERR_INVALID_ARG;
+  if (!dequant && !s->counts) return KVS_ERR_INVALID_ARG;
   if (X && !aligned16(X)) return KVS_ERR_INVALID_ARG;
   if (out && !aligned16(out)) return KVS_ERR_INVALID_ARG;
   PackWs w;
-  if (carve_pack(n_pools * Hkv, N, d, axis, ws, ws_bytes, &w) > ws_bytes || (!ws && ws_bytes == 0))
-    return KVS_ERR_WORKSPACE;
+  if (carve_pack(n_pools, Hkv, N, d, axis, ws, ws_bytes, &w) > ws_bytes || !ws) return KVS_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KVS_ERR_WORKSPACE;
   cudaStream_t st = as_stream(stream);
   rc = d == 64 ? pack_dh<64>(X, n_pools, Hkv, N, axis, bits, keep, s, w, st, dequant, out)
@@ -305,21 +276,31 @@ int colsq_cluster(long long rows) {
 }
 
 int launch_colsq(const uint16_t* A, long long rows_a, const uint8_t* keep, const uint16_t* B, long long rows_b,
-                 int64_t groups, int64_t d, int mode, float scale, float* out, cudaStream_t st) {
+                 int64_t groups, int64_t d, int mode, float scale, float* out, cudaStream_t st, float* out2 = nullptr) {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = set_cluster_attrs(colsq_cluster_kernel<64>);
-    if (err == cudaSuccess) err = set_cluster_attrs(colsq_cluster_kernel<128>);
+    err = set_cluster_attrs(colsq_cluster_kernel<64, false>);
+    if (err == cudaSuccess) err = set_cluster_attrs(colsq_cluster_kernel<128, false>);
+    if (err == cudaSuccess) err = set_cluster_attrs(colsq_cluster_kernel<64, true>);
+    if (err == cudaSuccess) err = set_cluster_attrs(colsq_cluster_kernel<128, true>);
   });
   if (err != cudaSuccess) return KVS_ERR_CUDA;
   const int cl = colsq_cluster(std::max(rows_a, rows_b));
   const dim3 grid(static_cast<unsigned>(cl), static_cast<unsigned>(groups));
-  const cudaError_t e =
-      d == 64 ? launch_cluster(colsq_cluster_kernel<64>, grid, cl, kColThreads, 0, st, A, static_cast<int>(rows_a), keep,
-                               B, static_cast<int>(rows_b), mode, scale, out)
-              : launch_cluster(colsq_cluster_kernel<128>, grid, cl, kColThreads, 0, st, A, static_cast<int>(rows_a),
-                               keep, B, static_cast<int>(rows_b), mode, scale, out);
+  const int ra = static_cast<int>(rows_a), rb = static_cast<int>(rows_b);
+  const bool stats = mode == kColChannelStats;
+  cudaError_t e;
+  if (d == 64)
+    e = stats ? launch_cluster(colsq_cluster_kernel<64, true>, grid, cl, kColThreads, 0, st, A, ra, keep, B, rb, mode,
+                               scale, out, out2)
+              : launch_cluster(colsq_cluster_kernel<64, false>, grid, cl, kColThreads, 0, st, A, ra, keep, B, rb, mode,
+                               scale, out, out2);
+  else
+    e = stats ? launch_cluster(colsq_cluster_kernel<128, true>, grid, cl, kColThreads, 0, st, A, ra, keep, B, rb, mode,
+                               scale, out, out2)
+              : launch_cluster(colsq_cluster_kernel<128, false>, grid, cl, kColThreads, 0, st, A, ra, keep, B, rb, mode,
+                               scale, out, out2);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return KVS_ERR_CUDA;
@@ -360,6 +341,18 @@ int kvs_get_device_error(void* stream) {
   return v;
 }
 
+int kvs_debug_inject(uint32_t fault, uint64_t wait_limit_ns) {
+  if (fault != KVS_DEBUG_NONE && fault != KVS_DEBUG_WITHHOLD_LSE_ARRIVE) return KVS_ERR_INVALID_ARG;
+  unsigned long long lim = wait_limit_ns == 0 ? kWaitLimitNs : wait_limit_ns;
+  lim = std::min<unsigned long long>(std::max<unsigned long long>(lim, 1000000ull), kWaitLimitNs);
+  const int f = static_cast<int>(fault);
+  KVS_CUDA_TRY(cudaDeviceSynchronize());
+  KVS_CUDA_TRY(cudaMemcpyToSymbol(kvs::g_debug_fault, &f, sizeof(int)));
+  KVS_CUDA_TRY(cudaMemcpyToSymbol(kvs::g_wait_limit_ns, &lim, sizeof(lim)));
+  KVS_CUDA_TRY(cudaDeviceSynchronize());
+  return KVS_OK;
+}
+
 size_t kvs_score_workspace_size(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t D,
                                 int64_t q_pos0, uint32_t mode) {
   ScorePlan pl;
@@ -388,6 +381,7 @@ int kvs_score_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
                         const uint16_t* W_O, int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t D,
                         int64_t q_pos0, uint32_t mode, float* lse, float* w_t, float* s_plus, void* workspace,
                         size_t workspace_bytes, void* stream) {
+  KVS_API_ENTRY();
   ScorePlan pl;
   int rc = plan_score(Hq, Hkv, W, N, d, D, q_pos0, mode, &pl);
   if (rc) return rc;
@@ -419,6 +413,7 @@ size_t kvs_block_lse_workspace_size(int64_t Hq, int64_t Hkv, int64_t W, int64_t 
 int kvs_block_lse(const uint16_t* Q, const uint16_t* K, int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d,
                   int64_t q_pos0, int64_t n_block, float* lse, void* workspace, size_t workspace_bytes,
                   void* stream) {
+  KVS_API_ENTRY();
   if (n_block < 1) return KVS_ERR_INVALID_ARG;
   ScorePlan pl;
   int rc = plan_score(Hq, Hkv, W, N, d, 0, q_pos0, KVS_MODE_LSE, &pl, n_block);
@@ -444,6 +439,7 @@ size_t kvs_channel_weights_workspace_size(int64_t Hq, int64_t Hkv, int64_t W, in
 
 int kvs_channel_weights(const uint16_t* Q, const uint16_t* K, int64_t Hq, int64_t Hkv, int64_t W, int64_t N,
                         int64_t d, float* w_c, void* workspace, size_t workspace_bytes, void* stream) {
+  KVS_API_ENTRY();
   (void)workspace, (void)workspace_bytes;
   if (Hq <= 0 || Hkv <= 0 || W <= 0 || N <= 0 || d <= 0 || Hq % Hkv) return KVS_ERR_INVALID_ARG;
   if (!Q || !K || !w_c || !aligned16(Q) || !aligned16(K)) return KVS_ERR_INVALID_ARG;
@@ -457,6 +453,22 @@ int kvs_channel_weights(const uint16_t* Q, const uint16_t* K, int64_t Hq, int64_
   return KVS_OK;
 }
 
+int kvs_channel_stats(const uint16_t* Q, const uint16_t* K, const uint8_t* keep_bits, int64_t Hq, int64_t Hkv,
+                      int64_t W, int64_t N, int64_t d, float* w_c, float* sigma_c, void* stream) {
+  KVS_API_ENTRY();
+  if (Hq <= 0 || Hkv <= 0 || W <= 0 || N <= 0 || d <= 0 || Hq % Hkv) return KVS_ERR_INVALID_ARG;
+  if (!Q || !K || !w_c || !sigma_c || !aligned16(Q) || !aligned16(K)) return KVS_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return KVS_ERR_UNSUPPORTED;
+  if (Hkv * N >= (1ll << 31) || Hq * W >= (1ll << 31)) return KVS_ERR_UNSUPPORTED;
+  const long long rq = (Hq / Hkv) * W;  // the group's query rows are contiguous in Q
+  const int rc = launch_colsq(K, N, keep_bits, Q, rq, Hkv, d, kColChannelStats,
+                              static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))), sigma_c, as_stream(stream),
+                              w_c);
+  if (rc) return rc;
+  KVS_CUDA_TRY(cudaGetLastError());
+  return KVS_OK;
+}
+
 size_t kvs_unit_rms_workspace_size(int64_t Hkv, int64_t N, int64_t d, int axis) {
   (void)Hkv, (void)N, (void)d, (void)axis;
   return 0;
@@ -464,6 +476,7 @@ size_t kvs_unit_rms_workspace_size(int64_t Hkv, int64_t N, int64_t d, int axis) 
 
 int kvs_unit_rms(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis, const uint8_t* keep_bits,
                  float* sigma, void* workspace, size_t workspace_bytes, void* stream) {
+  KVS_API_ENTRY();
   (void)workspace, (void)workspace_bytes;
   if (Hkv <= 0 || N <= 0 || d <= 0 || (axis != 0 && axis != 1)) return KVS_ERR_INVALID_ARG;
   if (!X || !sigma || !aligned16(X)) return KVS_ERR_INVALID_ARG;
@@ -634,12 +647,14 @@ extern "C" {
 
 int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t budget_bits, uint32_t width_mask,
                       uint8_t* bits, void* workspace, size_t workspace_bytes, void* stream) {
+  KVS_API_ENTRY();
   return allocate_pools(w, sigma, 1, U, budget_bits, width_mask, bits, workspace, workspace_bytes, stream);
 }
 
 int kvs_allocate_bits_pools(const float* w, const float* sigma, int64_t n_pools, int64_t U, int64_t budget_bits,
                             uint32_t width_mask, uint8_t* bits, void* workspace, size_t workspace_bytes,
                             void* stream) {
+  KVS_API_ENTRY();
   return allocate_pools(w, sigma, n_pools, U, budget_bits, width_mask, bits, workspace, workspace_bytes, stream);
 }
 
@@ -679,18 +694,20 @@ size_t kvs_pack_workspace_size(int64_t Hkv, int64_t N, int64_t d, int axis) {
 size_t kvs_pack_pools_workspace_size(int64_t n_pools, int64_t Hkv, int64_t N, int64_t d, int axis) {
   if (pack_shape_ok(n_pools, Hkv, N, d, axis)) return 0;
   PackWs w;
-  return carve_pack(n_pools * Hkv, N, d, axis, nullptr, 0, &w);
+  return carve_pack(n_pools, Hkv, N, d, axis, nullptr, 0, &w);
 }
 
 int kvs_quantize_pack(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, int axis, const uint8_t* bits,
                       const uint8_t* keep_bits, const kvs_stream_set* streams, void* workspace,
                       size_t workspace_bytes, void* stream) {
+  KVS_API_ENTRY();
   return pack_common(X, 1, Hkv, N, d, axis, bits, keep_bits, streams, workspace, workspace_bytes, stream, false,
                      nullptr);
 }
 
 int kvs_dequantize(const kvs_stream_set* streams, int64_t Hkv, int64_t N, int64_t d, int axis, const uint8_t* bits,
                    const uint8_t* keep_bits, float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  KVS_API_ENTRY();
   return pack_common(nullptr, 1, Hkv, N, d, axis, bits, keep_bits, streams, workspace, workspace_bytes, stream, true,
                      out);
 }
@@ -698,6 +715,7 @@ int kvs_dequantize(const kvs_stream_set* streams, int64_t Hkv, int64_t N, int64_
 int kvs_quantize_pack_pools(const uint16_t* X, int64_t n_pools, int64_t Hkv, int64_t N, int64_t d, int axis,
                             const uint8_t* bits, const uint8_t* keep_bits, const kvs_stream_set* streams,
                             void* workspace, size_t workspace_bytes, void* stream) {
+  KVS_API_ENTRY();
   return pack_common(X, n_pools, Hkv, N, d, axis, bits, keep_bits, streams, workspace, workspace_bytes, stream, false,
                      nullptr);
 }
@@ -705,12 +723,14 @@ int kvs_quantize_pack_pools(const uint16_t* X, int64_t n_pools, int64_t Hkv, int
 int kvs_dequantize_pools(const kvs_stream_set* streams, int64_t n_pools, int64_t Hkv, int64_t N, int64_t d, int axis,
                          const uint8_t* bits, const uint8_t* keep_bits, float* out, void* workspace,
                          size_t workspace_bytes, void* stream) {
+  KVS_API_ENTRY();
   return pack_common(nullptr, n_pools, Hkv, N, d, axis, bits, keep_bits, streams, workspace, workspace_bytes, stream,
                      true, out);
 }
 
 int kvs_threshold_keep(const float* score, int64_t Hkv, int64_t N, float tau, int64_t window,
                        uint32_t keep_width, uint8_t* bits, void* stream) {
+  KVS_API_ENTRY();
   if (Hkv <= 0 || N <= 0 || window < 0 || !score || !bits) return KVS_ERR_INVALID_ARG;
   if (keep_width != 2 && keep_width != 4 && keep_width != 8 && keep_width != 16) return KVS_ERR_INVALID_ARG;
   if (Hkv * N >= (1ll << 31)) return KVS_ERR_UNSUPPORTED;
@@ -732,6 +752,7 @@ size_t kvs_trizone_index_size(int64_t Hkv, int64_t N) {
 
 int kvs_trizone_index(const kvs_stream_set* k_streams, const kvs_stream_set* v_streams, const uint8_t* bits_v,
                       int64_t Hkv, int64_t N, int64_t d, void* index, size_t index_bytes, void* stream) {
+  KVS_API_ENTRY();
   if (Hkv <= 0 || N <= 0 || d <= 0 || !bits_v || !index) return KVS_ERR_INVALID_ARG;
   if (!streams_ok(k_streams) || !streams_ok(v_streams) || !k_streams->counts || !v_streams->counts)
     return KVS_ERR_INVALID_ARG;
@@ -761,6 +782,7 @@ int kvs_trizone_decode(const uint16_t* q, int64_t Hq, int64_t Hkv, int64_t N, in
                        const kvs_stream_set* k_streams, const kvs_stream_set* v_streams, const void* index,
                        const uint16_t* k_new, const uint16_t* v_new, const int32_t* n_new, int64_t nc_cap,
                        float* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  KVS_API_ENTRY();
   if (Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || nc_cap < 0 || !q || !index || !out || !lse)
     return KVS_ERR_INVALID_ARG;
   if (Hq % Hkv) return KVS_ERR_INVALID_ARG;
@@ -826,6 +848,7 @@ size_t kvs_gram_workspace_size(int64_t Hkv, int64_t N, int64_t d) {
 
 int kvs_gram(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, const uint8_t* keep_bits, int accumulate,
              float* G, void* workspace, size_t workspace_bytes, void* stream) {
+  KVS_API_ENTRY();
   if (Hkv <= 0 || N <= 0 || d <= 0 || !X || !G) return KVS_ERR_INVALID_ARG;
   if (d != kGramD || Hkv * N >= (1ll << 31)) return KVS_ERR_UNSUPPORTED;
   if (!aligned16(X) || !aligned16(G)) return KVS_ERR_INVALID_ARG;
@@ -847,6 +870,7 @@ int kvs_gram(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, const uint8_t
 
 int kvs_spectrum(const float* G, int64_t Hkv, int64_t d, float rtol, float* sigma, float* ner, int32_t* rank,
                  void* stream) {
+  KVS_API_ENTRY();
   if (Hkv <= 0 || d <= 0 || !G || !sigma || !ner || !rank || !(rtol >= 0.f) || !(rtol < 1.f))
     return KVS_ERR_INVALID_ARG;
   if (d != kGramD) return KVS_ERR_UNSUPPORTED;
@@ -860,6 +884,7 @@ int kvs_spectrum(const float* G, int64_t Hkv, int64_t d, float rtol, float* sigm
 // ---- KVSculpt: block attention targets, ridge values -----------------------
 int kvs_block_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int64_t Hq, int64_t Hkv, int64_t W,
                         int64_t N, int64_t d, int64_t q_pos0, int64_t n_block, float* Y, float* lse, void* stream) {
+  KVS_API_ENTRY();
   int rc = validate_shape(Hq, Hkv, W, N, d, q_pos0);
   if (rc) return rc;
   if (n_block < 1 || n_block > N) return KVS_ERR_INVALID_ARG;
@@ -911,6 +936,7 @@ size_t kvs_ridge_values_workspace_size(int64_t Hkv, int64_t R, int64_t k, int64_
 
 int kvs_ridge_values(const uint16_t* Qt, const uint16_t* Kc, const float* Y, int64_t Hkv, int64_t R, int64_t k,
                      int64_t d, float lam, float* Vc, void* workspace, size_t workspace_bytes, void* stream) {
+  KVS_API_ENTRY();
   int rc = ridge_check(Hkv, R, k, d);
   if (rc) return rc;
   if (!(lam > 0.f) || !std::isfinite(lam)) return KVS_ERR_INVALID_ARG;
@@ -1005,6 +1031,7 @@ int static_scratch_address(void** out) {
 
 extern "C" int kvs_allocate_bits_static(const float* w, const float* sigma, int64_t U, int64_t budget_bits,
                                         uint32_t width_mask, uint8_t* bits, void* stream) {
+  KVS_API_ENTRY();
   if (U < 0 || budget_bits < 0) return KVS_ERR_INVALID_ARG;
   if (kvs_allocate_workspace_size(U) > KVS_STATIC_ALLOC_SCRATCH_BYTES) return KVS_ERR_WORKSPACE;
   void* scratch = nullptr;

@@ -69,10 +69,14 @@ __global__ void __launch_bounds__(kNormThreads) row_rms_kernel(const uint16_t* _
 constexpr int kColThreads = 512;
 constexpr int kColChannelWeight = 0;
 constexpr int kColMaskedRms = 1;
+constexpr int kColChannelStats = 2;  // both from one read of the keys (A = K with keep, B = Q):
+                                     // out = the masked RMS of A, out2 = sqrt(sum_A all rows) sqrt(sum_B) * scale
 
-template <int DH>
+// acc: sums over the kept rows; with ALL, acc_all: sums over every row
+template <int DH, bool ALL = false>
 __device__ __forceinline__ void colsq_rows(const uint16_t* __restrict__ X, const uint8_t* __restrict__ keep,
-                                           const int r_begin, const int r_end, float (&acc)[8], int* n_kept) {
+                                           const int r_begin, const int r_end, float (&acc)[8], float (&acc_all)[8],
+                                           int* n_kept) {
   constexpr int TPR = DH / 8;                // threads per row, 8 channels each
   constexpr int RPI = kColThreads / TPR;     // rows per step
   const int rsub = threadIdx.x / TPR, cseg = (threadIdx.x % TPR) * 8;
@@ -93,9 +97,13 @@ __device__ __forceinline__ void colsq_rows(const uint16_t* __restrict__ X, const
     }
 #pragma unroll
     for (int j = 0; j < kInFlight; ++j) {
-      if (kp[j] == 0) continue;
       float f[8];
       bf16x8_to_f32(u[j], f);
+      if (ALL) {  // rows past the end loaded as zeros
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc_all[k] = fmaf(f[k], f[k], acc_all[k]);
+      }
+      if (kp[j] == 0) continue;
 #pragma unroll
       for (int k = 0; k < 8; ++k) acc[k] = fmaf(f[k], f[k], acc[k]);
       ++n;
@@ -121,10 +129,11 @@ __device__ __forceinline__ void colsq_block_reduce(const float (&acc)[8], float*
   }
 }
 
-template <int DH>
+template <int DH, bool STATS>
 __global__ void __launch_bounds__(kColThreads, 1) colsq_cluster_kernel(
     const uint16_t* __restrict__ A, const int rows_a, const uint8_t* __restrict__ keep_a,
-    const uint16_t* __restrict__ B, const int rows_b, const int mode, const float scale, float* __restrict__ out) {
+    const uint16_t* __restrict__ B, const int rows_b, const int mode, const float scale, float* __restrict__ out,
+    float* __restrict__ out2) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
   namespace cgn = cooperative_groups;
@@ -132,22 +141,26 @@ __global__ void __launch_bounds__(kColThreads, 1) colsq_cluster_kernel(
   constexpr int TPR = DH / 8;
   constexpr int RPI = kColThreads / TPR;
   __shared__ float red_rows[RPI * DH];
-  __shared__ float part_a[DH], part_b[DH];
+  __shared__ float part_a[DH], part_b[DH], part_all[STATS ? DH : 1];
   __shared__ int red_n[kColThreads / 32];
   __shared__ int s_n;
   const int CL = static_cast<int>(cluster.num_blocks());
   const int r = static_cast<int>(cluster.block_rank());
   const int g = blockIdx.y;
-  float acc[8];
+  float acc[8], acc_all[8];
   int n = 0;
   {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+    for (int k = 0; k < 8; ++k) acc[k] = acc_all[k] = 0.f;
     const int per = (rows_a + CL - 1) / CL;
     const int r0 = min(rows_a, r * per), r1 = min(rows_a, r0 + per);
-    colsq_rows<DH>(A + static_cast<size_t>(g) * rows_a * DH, keep_a ? keep_a + static_cast<size_t>(g) * rows_a : nullptr,
-                   r0, r1, acc, &n);
+    colsq_rows<DH, STATS>(A + static_cast<size_t>(g) * rows_a * DH,
+                          keep_a ? keep_a + static_cast<size_t>(g) * rows_a : nullptr, r0, r1, acc, acc_all, &n);
     colsq_block_reduce<DH>(acc, red_rows, part_a);
+    if (STATS) {
+      __syncthreads();
+      colsq_block_reduce<DH>(acc_all, red_rows, part_all);
+    }
   }
   if (threadIdx.x % TPR != 0) n = 0;  // one count per row slot
 #pragma unroll
@@ -160,7 +173,7 @@ __global__ void __launch_bounds__(kColThreads, 1) colsq_cluster_kernel(
     const int per = (rows_b + CL - 1) / CL;
     const int r0 = min(rows_b, r * per), r1 = min(rows_b, r0 + per);
     int nb;
-    colsq_rows<DH>(B + static_cast<size_t>(g) * rows_b * DH, nullptr, r0, r1, acc, &nb);
+    colsq_rows<DH>(B + static_cast<size_t>(g) * rows_b * DH, nullptr, r0, r1, acc, acc_all, &nb);
     colsq_block_reduce<DH>(acc, red_rows, part_b);
   }
   __syncthreads();
@@ -172,11 +185,12 @@ __global__ void __launch_bounds__(kColThreads, 1) colsq_cluster_kernel(
   cluster.sync();  // every CTA's partials are complete
   if (r == 0) {
     for (int c = threadIdx.x; c < DH; c += kColThreads) {
-      float sa = 0.f, sb = 0.f;
+      float sa = 0.f, sb = 0.f, sall = 0.f;
       int nn = 0;
       for (int q = 0; q < CL; ++q) {
         sa += cluster.map_shared_rank(part_a, q)[c];
         if (B != nullptr) sb += cluster.map_shared_rank(part_b, q)[c];
+        if (STATS) sall += cluster.map_shared_rank(part_all, q)[c];
         nn += *cluster.map_shared_rank(&s_n, q);
       }
       float v;
@@ -185,6 +199,7 @@ __global__ void __launch_bounds__(kColThreads, 1) colsq_cluster_kernel(
       else
         v = nn > 0 ? sqrtf(sa / static_cast<float>(nn)) : 0.f;
       out[static_cast<size_t>(g) * DH + c] = v;
+      if (STATS) out2[static_cast<size_t>(g) * DH + c] = sqrtf(sall) * sqrtf(sb) * scale;
     }
   }
   cluster.sync();  // keep every CTA's shared memory until CTA 0 has read it

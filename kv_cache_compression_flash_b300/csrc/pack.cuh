@@ -144,15 +144,6 @@ __device__ __forceinline__ void lane_bf16x4(const uint16_t* src, float (&x)[4], 
 __device__ __forceinline__ float bf16_lo(uint32_t p) { return __uint_as_float(p << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t p) { return __uint_as_float(p & 0xFFFF0000u); }
 
-// ---------------------------------------------------------------------------
-// plan for token units (axis 0): ids and group offsets of every stored unit
-// ---------------------------------------------------------------------------
-// Packs the four per-width counters of a thread into two u64 (32 bits each).
-__device__ __forceinline__ void plan_pack2(const unsigned (&c)[4], unsigned long long* lo, unsigned long long* hi) {
-  *lo = static_cast<unsigned long long>(c[0]) | (static_cast<unsigned long long>(c[1]) << 32);
-  *hi = static_cast<unsigned long long>(c[2]) | (static_cast<unsigned long long>(c[3]) << 32);
-}
-
 // exclusive scan over the block in thread order (kPlanThreads threads);
 // sbuf holds kPlanThreads/32 + 1 entries; *total = block sum.  Sums must stay
 // below 2^32 per 32-bit field.
@@ -202,231 +193,313 @@ __device__ __forceinline__ int bits16_at(const uint4& v, int e) {
   return static_cast<int>((w >> (8 * (e & 3))) & 0xFFu);
 }
 
-// One cluster of CL CTAs; CTA r plans units [r*per, r*per + per) in steps of
-// kPlanThreads * 16 units, thread t taking 16 contiguous ones per step.
-// Writes ids[s][k] = unit and group_offsets[s][k] = k * groups_per_unit for
-// the k-th stored unit of width slot s, and counts.  Each step's ids are
-// staged in shared memory by width and then written out contiguously.
-// grid (CL * pools): cluster q plans pool q (units q*U .. q*U + U-1 of bits).
-template <int CL>
-__global__ void __launch_bounds__(kPlanThreads, 1) rows_plan_kernel(const uint8_t* __restrict__ bits,
-                                                                    const long long U, const long long per,
-                                                                    const int groups_per_unit, const StreamPtrs sp) {
-  pdl_wait();  // inputs may come from the previous kernel on the stream
-  pdl_trigger();
-  const long long pool = blockIdx.x / CL;
-  bits += pool * U;
-  namespace cgp = cooperative_groups;
-  cgp::cluster_group cluster = cgp::this_cluster();
-  const int rank = CL > 1 ? static_cast<int>(cluster.block_rank()) : 0;
-  constexpr int kStep = kPlanThreads * 16;
-  __shared__ unsigned long long sbuf[kPlanThreads / 32 + 1];
-  __shared__ unsigned long long s_tot[2];
-  __shared__ unsigned long long s_all[CL][2];
-  __shared__ int32_t stage[kStep];
-  __shared__ int s_seg[5];
-  const long long begin = static_cast<long long>(rank) * per;
-  const long long end = min(U, begin + per);
-  auto count16 = [&](const uint4& v, unsigned (&c)[4]) {
+// exclusive scan over a block of NT threads in thread order; sbuf holds
+// NT/32 + 1 entries; *total = block sum.  Fields packed into the 64 bits
+// must not carry into each other.
+template <int NT>
+__device__ __forceinline__ unsigned long long block_exscan_u64(unsigned long long v, unsigned long long* sbuf,
+                                                               unsigned long long* total) {
+  constexpr int NW = NT / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned long long x = v;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int sl = width_slot(bits16_at(v, e));
-      if (sl >= 0) ++c[sl];
-    }
-  };
-  // totals of this CTA's range, then every CTA's, for the running prefix
-  unsigned long long tlo = 0, thi = 0;
-  for (long long b = begin; b < end; b += kStep) {
-    unsigned c[4] = {0u, 0u, 0u, 0u};
-    count16(load_bits16(bits, b + threadIdx.x * 16, end), c);
-    tlo += static_cast<unsigned long long>(c[0]) | (static_cast<unsigned long long>(c[1]) << 32);
-    thi += static_cast<unsigned long long>(c[2]) | (static_cast<unsigned long long>(c[3]) << 32);
-  }
-  {
-    unsigned long long a, bb;
-    (void)plan_block_exscan(tlo, sbuf, &a);
-    (void)plan_block_exscan(thi, sbuf, &bb);
-    if (threadIdx.x == 0) {
-      s_tot[0] = a;
-      s_tot[1] = bb;
-    }
-  }
-  if (CL > 1) cluster.sync();
-  else __syncthreads();
-  if (threadIdx.x < CL) {
-    const unsigned long long* rt = CL > 1 ? cluster.map_shared_rank(s_tot, static_cast<int>(threadIdx.x)) : s_tot;
-    s_all[threadIdx.x][0] = rt[0];
-    s_all[threadIdx.x][1] = rt[1];
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
   }
   __syncthreads();
-  unsigned long long plo = 0, phi = 0, glo = 0, ghi = 0;
-  for (int q = 0; q < CL; ++q) {
-    if (q < rank) {
-      plo += s_all[q][0];
-      phi += s_all[q][1];
-    }
-    glo += s_all[q][0];
-    ghi += s_all[q][1];
-  }
-  for (long long b = begin; b < end; b += kStep) {
-    const long long u0 = b + threadIdx.x * 16;
-    const uint4 v = load_bits16(bits, u0, end);
-    unsigned c[4] = {0u, 0u, 0u, 0u};
-    count16(v, c);
-    unsigned long long slo, shi;
-    const unsigned long long elo = plan_block_exscan(
-        static_cast<unsigned long long>(c[0]) | (static_cast<unsigned long long>(c[1]) << 32), sbuf, &slo);
-    const unsigned long long ehi = plan_block_exscan(
-        static_cast<unsigned long long>(c[2]) | (static_cast<unsigned long long>(c[3]) << 32), sbuf, &shi);
-    const int st[4] = {static_cast<int>(slo & 0xFFFFFFFFull), static_cast<int>(slo >> 32),
-                       static_cast<int>(shi & 0xFFFFFFFFull), static_cast<int>(shi >> 32)};
-    const int seg[5] = {0, st[0], st[0] + st[1], st[0] + st[1] + st[2], st[0] + st[1] + st[2] + st[3]};
-    int lr[4] = {seg[0] + static_cast<int>(elo & 0xFFFFFFFFull), seg[1] + static_cast<int>(elo >> 32),
-                 seg[2] + static_cast<int>(ehi & 0xFFFFFFFFull), seg[3] + static_cast<int>(ehi >> 32)};
+  if (lane == 31) sbuf[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long t = lane < NW ? sbuf[lane] : 0ull;
+    unsigned long long z = t;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int sl = width_slot(bits16_at(v, e));
-      if (sl >= 0 && u0 + e < end) stage[lr[sl]++] = static_cast<int32_t>(u0 + e);
+    for (int o = 1; o < NW; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, z, o);
+      if (lane >= o) z += y;
     }
-    if (threadIdx.x < 5) s_seg[threadIdx.x] = seg[threadIdx.x];
-    __syncthreads();
-    const long long base[4] = {static_cast<long long>(plo & 0xFFFFFFFFull), static_cast<long long>(plo >> 32),
-                               static_cast<long long>(phi & 0xFFFFFFFFull), static_cast<long long>(phi >> 32)};
-    for (int j = threadIdx.x; j < s_seg[4]; j += kPlanThreads) {
-      int sl = 0;
-      while (sl < 3 && j >= s_seg[sl + 1]) ++sl;
-      const long long k = base[sl] + (j - s_seg[sl]);
+    if (lane < NW) sbuf[lane] = z - t;
+    if (lane == NW - 1) sbuf[NW] = z;
+  }
+  __syncthreads();
+  *total = sbuf[NW];
+  return sbuf[warp] + x - v;
+}
+
+// ---------------------------------------------------------------------------
+// token units (axis 0, V cache), in unit order
+// ---------------------------------------------------------------------------
+// A pool's units are cut into chunks of kRowChunk.  rows_count_kernel counts
+// each chunk's units per stored width; the pack and dequantise kernels take
+// one chunk per CTA: the counts of the earlier chunks give the chunk's first
+// entry in every width stream, a block scan of its widths the entry of each
+// unit (the k-th stored unit of width w is entry k of stream w, so the
+// streams stay in ascending unit order).  Rows are then read or written in
+// unit order, 16 bytes a lane and eight lanes per 64-element group, with no
+// indirection between the loads.
+constexpr int kRowChunk = 1024;
+constexpr int kRowThreads = 256;
+static_assert(kRowChunk == 4 * kRowThreads, "four units per thread");
+
+// cnt[(pool * n_chunks + chunk) * 4 + slot] = units of the chunk stored in width slot `slot`
+__global__ void __launch_bounds__(kRowThreads) rows_count_kernel(const uint8_t* __restrict__ bits, const long long U,
+                                                                 const int n_chunks, uint32_t* __restrict__ cnt) {
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  pdl_trigger();
+  const long long pool = blockIdx.y;
+  const long long u0 = static_cast<long long>(blockIdx.x) * kRowChunk;
+  bits += pool * U;
+  unsigned long long c = 0;  // four 16-bit counters
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const long long u = u0 + threadIdx.x * 4 + e;
+    const int sl = u < U ? width_slot(bits[u]) : -1;
+    if (sl >= 0) c += 1ull << (16 * sl);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+  __shared__ unsigned long long s[kRowThreads / 32];
+  if ((threadIdx.x & 31) == 0) s[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x < 4) {
+    unsigned long long t = 0;
+#pragma unroll
+    for (int i = 0; i < kRowThreads / 32; ++i) t += s[i];
+    cnt[(pool * n_chunks + blockIdx.x) * 4 + threadIdx.x] = static_cast<uint32_t>((t >> (16 * threadIdx.x)) & 0xFFFFull);
+  }
+}
+
+// The chunk blockIdx.x of pool `pool`: s_w[i] = width of unit u0 + i, s_ent[i]
+// = its entry in its width stream (-1: width 0, or past the capacity).  With
+// write_streams, also the unit ids and group offsets of the chunk's entries
+// and, from the pool's last chunk, the counts.  Returns the chunk's units.
+__device__ __forceinline__ int rows_chunk_plan(const uint8_t* __restrict__ bits, const long long U, const int n_chunks,
+                                               const uint32_t* __restrict__ cnt, const long long pool, const int gpu,
+                                               const StreamPtrs& sp, const bool write_streams, int* s_ent,
+                                               uint8_t* s_w, long long* s_base, unsigned long long* sbuf) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int chunk = blockIdx.x;
+  const long long u0 = static_cast<long long>(chunk) * kRowChunk;
+  const int n = static_cast<int>(min(static_cast<long long>(kRowChunk), U - u0));
+  if (warp < 4) {  // the chunk's first entry per width: the earlier chunks' counts
+    long long a = 0;
+    const uint32_t* cp = cnt + pool * n_chunks * 4 + warp;
+    for (int c = lane; c < chunk; c += 32) a += cp[static_cast<long long>(c) * 4];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+    if (lane == 0) s_base[warp] = a;
+  }
+  uint32_t wv = 0;
+  unsigned long long c = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int i = tid * 4 + e;
+    const uint32_t b = i < n ? bits[u0 + i] : 0u;
+    wv |= b << (8 * e);
+    const int sl = width_slot(b);
+    if (sl >= 0) c += 1ull << (16 * sl);
+  }
+  unsigned long long tot;
+  unsigned long long ex = block_exscan_u64<kRowThreads>(c, sbuf, &tot);  // its barriers also publish s_base
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int i = tid * 4 + e;
+    const uint32_t b = (wv >> (8 * e)) & 0xFFu;
+    const int sl = width_slot(b);
+    int ent = -1;
+    if (sl >= 0 && i < n) {
+      const long long k = s_base[sl] + static_cast<long long>((ex >> (16 * sl)) & 0xFFFFull);
+      ex += 1ull << (16 * sl);
       if (k < sp.cap_units[sl]) {
-        sp.ids[sl][pool * sp.cap_units[sl] + k] = stage[j];
-        sp.goff[sl][pool * sp.cap_units[sl] + k] = k * groups_per_unit;
+        ent = static_cast<int>(k);
+        if (write_streams) {
+          sp.ids[sl][pool * sp.cap_units[sl] + k] = static_cast<int32_t>(u0 + i);
+          sp.goff[sl][pool * sp.cap_units[sl] + k] = k * gpu;
+        }
       }
     }
-    __syncthreads();  // the stage is reused by the next step
-    plo += slo;
-    phi += shi;
+    s_ent[i] = ent;
+    s_w[i] = static_cast<uint8_t>(b);
   }
-  if (rank == CL - 1 && threadIdx.x < 4) {
-    const int sl = threadIdx.x;
-    const unsigned long long tot = sl == 0   ? (glo & 0xFFFFFFFFull)
-                                   : sl == 1 ? (glo >> 32)
-                                   : sl == 2 ? (ghi & 0xFFFFFFFFull)
-                                             : (ghi >> 32);
-    const long long units = static_cast<long long>(tot), groups = units * groups_per_unit;
+  if (write_streams && chunk == n_chunks - 1 && tid < 4) {
+    const long long units = s_base[tid] + static_cast<long long>((tot >> (16 * tid)) & 0xFFFFull);
+    const long long groups = units * gpu;
     if (sp.counts) {
-      sp.counts[8 * pool + sl] = units;
-      sp.counts[8 * pool + 4 + sl] = groups;
+      sp.counts[8 * pool + tid] = units;
+      sp.counts[8 * pool + 4 + tid] = groups;
     }
-    if (units > sp.cap_units[sl] || groups > sp.cap_groups[sl]) record_error(KVS_ERR_RANGE);
-  }
-  if (CL > 1) cluster.sync();  // keep shared memory alive until every CTA has read the totals
-}
-
-// entry offsets (in groups) of the four widths from the device counts
-__device__ __forceinline__ void entry_offsets(const StreamPtrs& sp, const int gpu, const long long pool,
-                                              long long* s_off) {
-  if (threadIdx.x == 0) {
-    long long run = 0;
-    for (int s = 0; s < 4; ++s) {
-      s_off[s] = run;
-      run += min(static_cast<long long>(sp.counts[8 * pool + s]), sp.cap_units[s]) * gpu;
-    }
-    s_off[4] = run;
+    if (units > sp.cap_units[tid] || groups > sp.cap_groups[tid]) record_error(KVS_ERR_RANGE);
   }
   __syncthreads();
+  return n;
 }
 
-// ---------------------------------------------------------------------------
-// token units (axis 0, V cache): one lane per 64-element group, over the
-// stream entries the plan wrote (consecutive lanes write consecutive blocks)
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ int entry_slot(const long long* s_off, const long long gidx) {
-  int s = 0;
-  while (s < 3 && gidx >= s_off[s + 1]) ++s;
-  return s;
+// This lane's 8 elements of a 64-element group (eight lanes hold the group,
+// all 32 lanes of the warp take part).  Returns the 8w code bits, element e
+// at bits [w e, w e + w); *scale_bits gets the group's fp16 scale.
+__device__ __forceinline__ unsigned long long quantize_lane8(const float (&x)[8], const int w, uint16_t* scale_bits,
+                                                             bool* overflow) {
+  float a = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(x[e]));
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+  const float qmax = static_cast<float>((1 << (w - 1)) - 1);
+  const __half sh = __float2half_ru(__fdiv_rn(a, qmax));
+  const float s = __half2float(sh);
+  *overflow = isinf(s);
+  *scale_bits = __half_as_ushort(sh);
+  unsigned long long packed = 0ull;
+  const unsigned long long cmask = (1ull << w) - 1ull;
+  if (s > 0.f && !isinf(s)) {
+    const float r = __frcp_rn(s);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      packed |= (static_cast<unsigned long long>(static_cast<uint32_t>(q_round(x[e], s, r))) & cmask) << (w * e);
+  }
+  return packed;
 }
 
-// grid (blocks, pools): blockIdx.y is the pool (U units of X each)
+__device__ __forceinline__ void bf16x8(const uint4 u, float (&x)[8]) {
+  const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    x[2 * k] = __uint_as_float(v[k] << 16);
+    x[2 * k + 1] = __uint_as_float(v[k] & 0xFFFF0000u);
+  }
+}
+
+// the w bytes of this lane's codes (width 16: the raw 16 bytes), at the lane's place in the group's block
+__device__ __forceinline__ void store_lane8(uint8_t* group_base, const int w, const int l8, const unsigned long long packed,
+                                            const uint4 raw) {
+  switch (w) {
+    case 2: reinterpret_cast<uint16_t*>(group_base)[l8] = static_cast<uint16_t>(packed); break;
+    case 4: reinterpret_cast<uint32_t*>(group_base)[l8] = static_cast<uint32_t>(packed); break;
+    case 8: reinterpret_cast<unsigned long long*>(group_base)[l8] = packed; break;
+    default: {  // 8-byte aligned streams: two 8-byte stores
+      uint2* p = reinterpret_cast<uint2*>(group_base) + 2 * l8;
+      p[0] = make_uint2(raw.x, raw.y);
+      p[1] = make_uint2(raw.z, raw.w);
+    }
+  }
+}
+
+// grid (chunks, pools): pack the stored units of one chunk, in unit order
 template <int DH>
-__global__ void __launch_bounds__(256) pack_rows_kernel(const uint16_t* __restrict__ X, const StreamPtrs sp,
-                                                        const long long U) {
+__global__ void __launch_bounds__(kRowThreads) pack_rows_kernel(const uint16_t* __restrict__ X,
+                                                                const uint8_t* __restrict__ bits, const long long U,
+                                                                const int n_chunks, const uint32_t* __restrict__ cnt,
+                                                                const StreamPtrs sp) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
   constexpr int GPU = DH / 64;
-  __shared__ long long s_off[5];
+  constexpr int kWarps = kRowThreads / 32;
+  __shared__ int s_ent[kRowChunk];
+  __shared__ uint8_t s_w[kRowChunk];
+  __shared__ long long s_base[4];
+  __shared__ unsigned long long sbuf[kWarps + 1];
   const long long pool = blockIdx.y;
-  X += pool * U * DH;
-  entry_offsets(sp, GPU, pool, s_off);
-  const int l16 = threadIdx.x & 15;
-  const int total = static_cast<int>(s_off[4]);  // groups < 2^31 (units < 2^31, two groups each)
-  const int stride = gridDim.x * (blockDim.x / 16);
-  for (int gidx = blockIdx.x * (blockDim.x / 16) + (threadIdx.x >> 4); gidx < total; gidx += stride) {
-    const int s = entry_slot(s_off, gidx);
-    const int grp = gidx - static_cast<int>(s_off[s]);  // == entry * GPU + gi
-    if (grp >= sp.cap_groups[s]) continue;
-    const long long u = sp.ids[s][pool * sp.cap_units[s] + grp / GPU];
-    const long long gb = pool * sp.cap_groups[s];
-    float x[4];
-    uint2 raw;
-    lane_bf16x4(X + u * DH + (grp % GPU) * 64 + l16 * 4, x, &raw);
-    const int w = s == 3 ? 16 : (2 << s);
-    uint32_t packed = 0;
-    if (w != 16) {
-      uint16_t sb;
-      bool ovf;
-      packed = quantize_lane4(x, w, &sb, &ovf);
-      if (l16 == 0) {
-        sp.scales[s][gb + grp] = sb;
-        if (ovf) record_error(KVS_ERR_RANGE);
+  const int n = rows_chunk_plan(bits + pool * U, U, n_chunks, cnt, pool, GPU, sp, true, s_ent, s_w, s_base, sbuf);
+  const uint16_t* Xc = X + (pool * U + static_cast<long long>(blockIdx.x) * kRowChunk) * DH;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, sub = lane >> 3, l8 = lane & 7;
+  const int ng = n * GPU;
+  // a warp takes 4 consecutive groups per step, two steps' loads in flight
+  for (int gb = warp * 4; gb < ng; gb += 2 * kWarps * 4) {
+    uint4 raw[2];
+    int gl[2], s[2], w[2], ent[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      gl[k] = gb + k * kWarps * 4 + sub;
+      const int ui = gl[k] / GPU;
+      w[k] = gl[k] < ng ? s_w[ui] : 0;
+      ent[k] = gl[k] < ng ? s_ent[ui] : -1;
+      s[k] = width_slot(w[k]);
+      raw[k] = (s[k] >= 0 && ent[k] >= 0) ? __ldg(reinterpret_cast<const uint4*>(Xc + static_cast<long long>(gl[k]) * 64 + l8 * 8))
+                                          : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const bool act = s[k] >= 0 && ent[k] >= 0;
+      unsigned long long packed = 0ull;
+      uint16_t sb = 0;
+      bool ovf = false;
+      float x[8];
+      bf16x8(raw[k], x);
+      if (__any_sync(0xFFFFFFFFu, act && w[k] != 16)) {
+        // every lane takes part in the group maxima; inactive groups hold zeros
+        packed = quantize_lane8(x, (act && w[k] != 16) ? w[k] : 8, &sb, &ovf);
+      }
+      if (act) {
+        const long long grp = static_cast<long long>(ent[k]) * GPU + gl[k] % GPU;  // group in the pool's stream
+        const long long gg = pool * sp.cap_groups[s[k]] + grp;
+        if (w[k] != 16 && l8 == 0) {
+          sp.scales[s[k]][gg] = sb;
+          if (ovf) record_error(KVS_ERR_RANGE);
+        }
+        store_lane8(sp.codes[s[k]] + gg * (8 * w[k]), w[k], l8, packed, raw[k]);
       }
     }
-    store_lane_codes(sp.codes[s] + (gb + grp) * (8 * w), w, l16, packed, raw);
   }
 }
 
-// Token units decoded from the stream entries (entry j of width slot s is
-// unit ids[s][j] with groups goff[s][j] ..), one half-warp per group; rows of
-// evicted units (bits == 0) are zeroed in the same launch, one warp per row.
-// grid (blocks, pools): blockIdx.y is the pool (U units of bits and out each)
+// Decode this lane's 8 elements of a group.
+__device__ __forceinline__ void dequant_lane8(const uint8_t* group_base, const int w, const int l8,
+                                              const uint16_t* scale_ptr, float (&y)[8]) {
+  if (w == 16) {
+    const uint2* p = reinterpret_cast<const uint2*>(group_base) + 2 * l8;
+    const uint2 a = p[0], b = p[1];
+    bf16x8(make_uint4(a.x, a.y, b.x, b.y), y);
+    return;
+  }
+  unsigned long long packed;
+  if (w == 2)
+    packed = reinterpret_cast<const uint16_t*>(group_base)[l8];
+  else if (w == 4)
+    packed = reinterpret_cast<const uint32_t*>(group_base)[l8];
+  else
+    packed = reinterpret_cast<const unsigned long long*>(group_base)[l8];
+  const float s = __half2float(__ushort_as_half(*scale_ptr));
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int code = static_cast<int>((packed >> (w * e)) & ((1ull << w) - 1ull));
+    const int q = code >= (1 << (w - 1)) ? code - (1 << w) : code;
+    y[e] = static_cast<float>(q) * s;
+  }
+}
+
+// grid (chunks, pools): every row of one chunk, in unit order (width 0 -> zeros)
 template <int DH>
-__global__ void __launch_bounds__(256) dequant_rows_kernel(const StreamPtrs sp, const uint8_t* __restrict__ bits,
-                                                           const long long U, float* __restrict__ out) {
+__global__ void __launch_bounds__(kRowThreads) dequant_rows_kernel(const StreamPtrs sp, const uint8_t* __restrict__ bits,
+                                                                   const long long U, const int n_chunks,
+                                                                   const uint32_t* __restrict__ cnt,
+                                                                   float* __restrict__ out) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
   constexpr int GPU = DH / 64;
-  __shared__ long long s_off[5];
+  constexpr int kWarps = kRowThreads / 32;
+  __shared__ int s_ent[kRowChunk];
+  __shared__ uint8_t s_w[kRowChunk];
+  __shared__ long long s_base[4];
+  __shared__ unsigned long long sbuf[kWarps + 1];
   const long long pool = blockIdx.y;
-  bits += pool * U;
-  out += pool * U * DH;
-  entry_offsets(sp, GPU, pool, s_off);
-  const int l16 = threadIdx.x & 15;
-  const int total = static_cast<int>(s_off[4]);
-  const int stride = gridDim.x * (blockDim.x / 16);
-  for (int gidx = blockIdx.x * (blockDim.x / 16) + (threadIdx.x >> 4); gidx < total; gidx += stride) {
-    const int s = entry_slot(s_off, gidx);
-    const int local = gidx - static_cast<int>(s_off[s]);
-    const int jj = local / GPU, gi = local % GPU;
-    const long long u = sp.ids[s][pool * sp.cap_units[s] + jj];
-    const long long grp = sp.goff[s][pool * sp.cap_units[s] + jj] + gi;
-    if (grp >= sp.cap_groups[s]) continue;
-    const long long gg = pool * sp.cap_groups[s] + grp;
-    const int w = s == 3 ? 16 : (2 << s);
-    float y[4];
-    dequant_lane4(sp.codes[s] + gg * (8 * w), w, l16, sp.scales[s] + gg, y);
-    *reinterpret_cast<float4*>(out + u * DH + gi * 64 + l16 * 4) = make_float4(y[0], y[1], y[2], y[3]);
-  }
-  // evicted rows: a warp takes 32 rows, then zeroes the ones with width 0
-  const int lane = threadIdx.x & 31;
-  const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
-  for (long long r0 = (static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5)) * 32; r0 < U;
-       r0 += nwarps * 32) {
-    const bool zero = r0 + lane < U && bits[r0 + lane] == 0;
-    unsigned m = __ballot_sync(0xFFFFFFFFu, zero);
-    while (m) {
-      const int i = __ffs(m) - 1;
-      m &= m - 1;
-      float4* o4 = reinterpret_cast<float4*>(out + (r0 + i) * DH);
-      for (int c4 = lane; c4 < DH / 4; c4 += 32) o4[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int n = rows_chunk_plan(bits + pool * U, U, n_chunks, cnt, pool, GPU, sp, false, s_ent, s_w, s_base, sbuf);
+  float* oc = out + (pool * U + static_cast<long long>(blockIdx.x) * kRowChunk) * DH;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, sub = lane >> 3, l8 = lane & 7;
+  const int ng = n * GPU;
+  for (int gl = warp * 4 + sub; gl - sub < ng; gl += kWarps * 4) {
+    if (gl >= ng) continue;
+    const int ui = gl / GPU;
+    const int w = s_w[ui], ent = s_ent[ui], s = width_slot(w);
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = 0.f;
+    if (s >= 0 && ent >= 0) {
+      const long long gg = pool * sp.cap_groups[s] + static_cast<long long>(ent) * GPU + gl % GPU;
+      dequant_lane8(sp.codes[s] + gg * (8 * w), w, l8, sp.scales[s] + gg, y);
     }
+    float4* o = reinterpret_cast<float4*>(oc + static_cast<long long>(gl) * 64 + l8 * 8);
+    o[0] = make_float4(y[0], y[1], y[2], y[3]);
+    o[1] = make_float4(y[4], y[5], y[6], y[7]);
   }
 }
 
@@ -540,275 +613,172 @@ __global__ void __launch_bounds__(kPlanThreads, 1) channels_plan_kernel(
   }
 }
 
-// grid (ceil(N/64), Hkv), 256 threads: kept-token group j of head g for every
-// channel; one half-warp per channel (lane i: tokens 4i..4i+3)
-// (blockIdx.y runs over the heads of every pool: pool blockIdx.y / Hkv)
+// Channel kernels take kChanTG (pack) or kChanTGd (dequantise) consecutive
+// kept-token groups of one head per CTA, so each CTA moves tens of KB: the
+// kept rows are gathered into a shared-memory tile (16-byte loads, eight in
+// flight per thread) and the channels are read down its columns, eight lanes
+// per (channel, 64-token group) and eight tokens a lane.
+constexpr int kChanTG = 4;
+constexpr int kChanTGd = 2;
+constexpr int kChanThreads = 256;
+
 template <int DH>
-__global__ void __launch_bounds__(256) pack_channels_kernel(const uint16_t* __restrict__ X, const int N,
-                                                            const uint8_t* __restrict__ bits,
-                                                            const long long* __restrict__ chan_base,
-                                                            const int* __restrict__ kept,
-                                                            const int* __restrict__ n_kept, const StreamPtrs sp,
-                                                            const int Hkv) {
+__host__ __device__ constexpr size_t chan_pack_smem() { return static_cast<size_t>(64 * kChanTG) * (DH / 2 + 1) * 4; }
+template <int DH>
+__host__ __device__ constexpr size_t chan_dequant_smem() { return static_cast<size_t>(64 * kChanTGd) * (DH + 1) * 4; }
+
+// grid (ceil(ceil(N/64) / kChanTG), pools * Hkv): kept-token groups
+// [kChanTG jb, kChanTG jb + kChanTG) of head g for every channel
+template <int DH>
+__global__ void __launch_bounds__(kChanThreads) pack_channels_kernel(const uint16_t* __restrict__ X, const int N,
+                                                                     const uint8_t* __restrict__ bits,
+                                                                     const long long* __restrict__ chan_base,
+                                                                     const int* __restrict__ kept,
+                                                                     const int* __restrict__ n_kept, const StreamPtrs sp,
+                                                                     const int Hkv) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
-  // odd word stride: the column reads below (lane i takes rows 4i..4i+3)
-  // spread over the banks instead of piling onto two
-  constexpr int LDW = DH / 2 + 1;  // 32-bit words per row
-  __shared__ uint32_t tile[64][LDW];
+  constexpr int TOK = 64 * kChanTG;
+  constexpr int LDW = DH / 2 + 1;  // 32-bit words per tile row; odd, so column reads spread over the banks
+  extern __shared__ uint32_t ctile[];  // [TOK][LDW]: two bf16 channels a word
   __shared__ int s_w[DH];
   __shared__ long long s_base[DH];
-  const int j = blockIdx.x, g = blockIdx.y;
+  __shared__ int s_tok[TOK];
+  const int jb = blockIdx.x, g = blockIdx.y;
+  const long long pool = g / Hkv;
   const int n = n_kept[g];
-  if (j * 64 >= n) return;
-  const int rows = min(64, n - j * 64);
-  for (int c = threadIdx.x; c < DH; c += blockDim.x) {
-    const long long b = chan_base[g * DH + c];
-    s_w[c] = bits[g * DH + c];
-    s_base[c] = b >= 0 ? b + j : -1;
+  const int k0 = jb * TOK;
+  if (k0 >= n) return;
+  const int rows = min(TOK, n - k0);
+  for (int c = threadIdx.x; c < DH; c += kChanThreads) {
+    const long long b = chan_base[static_cast<long long>(g) * DH + c];
+    s_w[c] = bits[static_cast<long long>(g) * DH + c];
+    s_base[c] = b >= 0 ? b + jb * kChanTG : -1;
   }
-  for (int e = threadIdx.x; e < 64 * (DH / 8); e += 256) {
-    const int i = e / (DH / 8), c8 = (e % (DH / 8)) * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (i < rows) {
-      const int t = kept[static_cast<size_t>(g) * N + j * 64 + i];
-      v = __ldg(reinterpret_cast<const uint4*>(X + (static_cast<size_t>(g) * N + t) * DH + c8));
+  for (int i = threadIdx.x; i < TOK; i += kChanThreads)
+    s_tok[i] = i < rows ? kept[static_cast<long long>(g) * N + k0 + i] : -1;
+  __syncthreads();
+  // gather the kept rows; rows past the kept ones read as zeros (padding of a short last group)
+  constexpr int kLoads = TOK * (DH / 8) / kChanThreads;
+  constexpr int kBatch = 8;
+  const uint16_t* Xg = X + static_cast<long long>(g) * N * DH;
+#pragma unroll
+  for (int b0 = 0; b0 < kLoads; b0 += kBatch) {
+    uint4 v[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int e = (b0 + k) * kChanThreads + threadIdx.x;
+      const int i = e / (DH / 8), c8 = (e % (DH / 8)) * 8;
+      v[k] = i < rows ? __ldg(reinterpret_cast<const uint4*>(Xg + static_cast<long long>(s_tok[i]) * DH + c8))
+                      : make_uint4(0u, 0u, 0u, 0u);
     }
-    uint32_t* row = &tile[i][c8 / 2];
-    row[0] = v.x;
-    row[1] = v.y;
-    row[2] = v.z;
-    row[3] = v.w;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int e = (b0 + k) * kChanThreads + threadIdx.x;
+      const int i = e / (DH / 8), c8 = (e % (DH / 8)) * 8;
+      uint32_t* row = ctile + i * LDW + c8 / 2;
+      row[0] = v[k].x;
+      row[1] = v[k].y;
+      row[2] = v[k].z;
+      row[3] = v[k].w;
+    }
   }
   __syncthreads();
-  const int l16 = threadIdx.x & 15, hw = threadIdx.x >> 4;
-  for (int c = hw; c < DH; c += 16) {
-    const long long grp = s_base[c];
-    if (grp < 0) continue;
-    const int w = s_w[c];
-    const int s = width_slot(w);
-    const long long gg = static_cast<long long>(g / Hkv) * sp.cap_groups[s] + grp;
-    float x[4];
-    uint32_t rw[4];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, sub = lane >> 3, l8 = lane & 7;
+  // pairs (channel, group): p = jg * DH + c; a warp takes 4 consecutive channels of one group
+  for (int p0 = warp * 4; p0 < DH * kChanTG; p0 += (kChanThreads / 32) * 4) {
+    const int p = p0 + sub;
+    const int c = p % DH, jg = p / DH;
+    const int w = s_w[c], s = width_slot(w);
+    const bool act = s >= 0 && s_base[c] >= 0 && jg * 64 < rows;
+    float x[8];
+    uint32_t hw[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      rw[e] = (tile[4 * l16 + e][c >> 1] >> ((c & 1) * 16)) & 0xFFFFu;
-      x[e] = __uint_as_float(rw[e] << 16);
+    for (int e = 0; e < 8; ++e) {
+      const int r = jg * 64 + l8 * 8 + e;
+      hw[e] = (ctile[r * LDW + (c >> 1)] >> ((c & 1) * 16)) & 0xFFFFu;
+      x[e] = __uint_as_float(hw[e] << 16);
     }
-    const uint2 raw = make_uint2(rw[0] | (rw[1] << 16), rw[2] | (rw[3] << 16));
-    uint32_t packed = 0;
-    if (w != 16) {
-      uint16_t sb;
-      bool ovf;
-      packed = quantize_lane4(x, w, &sb, &ovf);
-      if (l16 == 0) {
+    unsigned long long packed = 0ull;
+    uint16_t sb = 0;
+    bool ovf = false;
+    if (__any_sync(0xFFFFFFFFu, act && w != 16)) packed = quantize_lane8(x, (act && w != 16) ? w : 8, &sb, &ovf);
+    if (act) {
+      const long long gg = pool * sp.cap_groups[s] + s_base[c] + jg;
+      if (w != 16 && l8 == 0) {
         sp.scales[s][gg] = sb;
         if (ovf) record_error(KVS_ERR_RANGE);
       }
+      const uint4 raw = make_uint4(hw[0] | (hw[1] << 16), hw[2] | (hw[3] << 16), hw[4] | (hw[5] << 16),
+                                   hw[6] | (hw[7] << 16));
+      store_lane8(sp.codes[s] + gg * (8 * w), w, l8, packed, raw);
     }
-    store_lane_codes(sp.codes[s] + gg * (8 * w), w, l16, packed, raw);
   }
 }
 
-// grid (ceil(N/64) + 1, Hkv), 256 threads.  CTA (j, g) with j below the head's
-// kept-group count decodes kept-token group j of every channel (one
-// half-warp per channel) through a shared-memory tile and writes the tokens'
-// rows; the CTAs after those zero the head's dropped tokens, 64 per CTA.
-// (blockIdx.y runs over the heads of every pool: pool blockIdx.y / Hkv)
+// grid (ceil(N / (64 kChanTGd)) + 1, pools * Hkv).  CTA jb below the head's
+// count of kept blocks decodes kept-token groups [kChanTGd jb, ..) of every
+// channel into a shared-memory tile and writes those tokens' rows; the CTAs
+// after those zero the head's dropped tokens, 64 kChanTGd per CTA.
 template <int DH>
-__global__ void __launch_bounds__(256) dequant_channels_kernel(const StreamPtrs sp, const int N,
-                                                               const uint8_t* __restrict__ bits,
-                                                               const long long* __restrict__ chan_base,
-                                                               const int* __restrict__ kept,
-                                                               const int* __restrict__ n_kept,
-                                                               float* __restrict__ out, const int Hkv) {
+__global__ void __launch_bounds__(kChanThreads) dequant_channels_kernel(const StreamPtrs sp, const int N,
+                                                                        const uint8_t* __restrict__ bits,
+                                                                        const long long* __restrict__ chan_base,
+                                                                        const int* __restrict__ kept,
+                                                                        const int* __restrict__ n_kept,
+                                                                        float* __restrict__ out, const int Hkv) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
-  constexpr int LD = DH + 1;  // odd stride: conflict-light column writes
-  __shared__ float tile[64][LD];
+  constexpr int TOK = 64 * kChanTGd;
+  constexpr int LD = DH + 1;  // odd: column writes spread over the banks
+  extern __shared__ float ftile[];  // [TOK][LD]
   __shared__ int s_w[DH];
   __shared__ long long s_base[DH];
-  const int j = blockIdx.x, g = blockIdx.y;
-  const int n = n_kept[g];
-  const int ngk = (n + 63) / 64;
-  if (j >= ngk) {  // zero dropped tokens kept[g][n + 64 jz ..]
-    const int d0 = n + (j - ngk) * 64;
-    if (d0 >= N) return;
-    const int cnt = min(64, N - d0);
-    for (int e = threadIdx.x; e < cnt * (DH / 4); e += 256) {
-      const int i = e / (DH / 4), c4 = (e % (DH / 4)) * 4;
-      const int t = kept[static_cast<size_t>(g) * N + d0 + i];
-      *reinterpret_cast<float4*>(out + (static_cast<size_t>(g) * N + t) * DH + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    return;
-  }
-  const int rows = min(64, n - j * 64);
-  for (int c = threadIdx.x; c < DH; c += blockDim.x) {
-    const long long b = chan_base[g * DH + c];
-    s_w[c] = bits[g * DH + c];
-    s_base[c] = b >= 0 ? b + j : -1;
-  }
-  __syncthreads();
-  const int l16 = threadIdx.x & 15, hw = threadIdx.x >> 4;
-  for (int c = hw; c < DH; c += 16) {
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
-    const long long grp = s_base[c];
-    if (grp >= 0) {
-      const int w = s_w[c];
-      const int s = width_slot(w);
-      const long long gg = static_cast<long long>(g / Hkv) * sp.cap_groups[s] + grp;
-      dequant_lane4(sp.codes[s] + gg * (8 * w), w, l16, sp.scales[s] + gg, y);
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) tile[4 * l16 + e][c] = y[e];
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < rows * (DH / 4); e += 256) {
-    const int i = e / (DH / 4), c4 = (e % (DH / 4)) * 4;
-    const int t = kept[static_cast<size_t>(g) * N + j * 64 + i];
-    *reinterpret_cast<float4*>(out + (static_cast<size_t>(g) * N + t) * DH + c4) =
-        make_float4(tile[i][c4], tile[i][c4 + 1], tile[i][c4 + 2], tile[i][c4 + 3]);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// dequantise the channel streams without a plan kernel (N <= kDirectMaxN)
-// ---------------------------------------------------------------------------
-// grid (ceil(N/64) + 1, Hkv), 256 threads.  Each CTA works out for its own
-// head what the plan kernel would give: the kept tokens in order (a block scan
-// of the head's keep bytes) and each channel's first stream group (the entry
-// of unit g*DH + c in its width stream is the number of earlier units of that
-// width; the group offset is read back from the stream).  CTA j < ngk decodes
-// kept-token group j; the CTAs after those zero the head's dropped tokens.
-constexpr int kDirectMaxN = 16384;
-
-__device__ __forceinline__ unsigned long long direct_exscan256(unsigned long long v, unsigned long long* sbuf,
-                                                               unsigned long long* total) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  unsigned long long x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-    if (lane >= o) x += y;
-  }
-  __syncthreads();
-  if (lane == 31) sbuf[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    const unsigned long long t = lane < 8 ? sbuf[lane] : 0ull;
-    unsigned long long z = t;
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, z, o);
-      if (lane >= o) z += y;
-    }
-    if (lane < 8) sbuf[lane] = z - t;
-    if (lane == 7) sbuf[8] = z;
-  }
-  __syncthreads();
-  *total = sbuf[8];
-  return sbuf[warp] + x - v;
-}
-
-// (blockIdx.y runs over the heads of every pool: pool blockIdx.y / Hkv)
-template <int DH>
-__global__ void __launch_bounds__(256) dequant_channels_direct_kernel(const StreamPtrs sp, const int N,
-                                                                      const uint8_t* __restrict__ bits,
-                                                                      const uint8_t* __restrict__ keep,
-                                                                      float* __restrict__ out, const int Hkv) {
-  pdl_wait();  // inputs may come from the previous kernel on the stream
-  pdl_trigger();
-  constexpr int LD = DH + 1;
-  __shared__ float tile[64][LD];
-  __shared__ int s_w[DH];
-  __shared__ long long s_base[DH];
-  __shared__ int s_tok[64];
-  __shared__ unsigned long long sbuf[9];
-  const int j = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
-  // ---- the head's kept tokens: thread tid takes bytes [t0, t0 + per) ----
-  const int per = ((N + 255) / 256 + 15) / 16 * 16;
-  const int t0 = tid * per;
-  const uint8_t* kb = keep + static_cast<size_t>(g) * N;
-  int cnt = 0;
-  for (int e = 0; e < per; e += 16) {
-    if (t0 + e >= N) break;
-    const uint4 v = load_bits16(kb, t0 + e, N);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) cnt += (t0 + e + k < N && bits16_at(v, k) != 0) ? 1 : 0;
-  }
-  unsigned long long tot;
-  const int ex = static_cast<int>(direct_exscan256(static_cast<unsigned long long>(cnt), sbuf, &tot));
-  const int n = static_cast<int>(tot);
-  const int ngk = (n + 63) / 64;
-  const bool kept_cta = j < ngk;
-  // this CTA's 64 list entries: kept ranks [64j, 64j + 64), or dropped ranks after the kept groups
-  const int lo = kept_cta ? 64 * j : 64 * (j - ngk);
-  const int hi = lo + 64;
-  const int my_lo = kept_cta ? ex : t0 - ex;                       // first kept / dropped rank of my bytes
-  const int my_n = kept_cta ? cnt : max(0, min(per, N - t0)) - cnt;
-  if (my_lo < hi && my_lo + my_n > lo) {
-    int r = my_lo;
-    for (int e = 0; e < per && t0 + e < N; ++e) {
-      const bool kept = kb[t0 + e] != 0;
-      if (kept == kept_cta) {
-        if (r >= lo && r < hi) s_tok[r - lo] = t0 + e;
-        ++r;
-      }
-    }
-  }
-  const int rows = kept_cta ? min(64, n - lo) : max(0, min(64, (N - n) - lo));
-  if (!kept_cta) {
-    __syncthreads();
-    for (int e = tid; e < rows * (DH / 4); e += 256) {
-      const int i = e / (DH / 4), c4 = (e % (DH / 4)) * 4;
-      *reinterpret_cast<float4*>(out + (static_cast<size_t>(g) * N + s_tok[i]) * DH + c4) =
-          make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    return;
-  }
-  // ---- each channel's entry in its width stream, then its first group ----
-  unsigned long long before = 0;                   // units of each width before this head, 16-bit fields
+  const int jb = blockIdx.x, g = blockIdx.y;
   const long long pool = g / Hkv;
-  const uint8_t* pbits = bits + pool * Hkv * DH;   // the pool's unit widths
-  for (int u = tid; u < (g % Hkv) * DH; u += 256) {
-    const int sl = width_slot(pbits[u]);
-    if (sl >= 0) before += 1ull << (16 * sl);
-  }
-  unsigned long long base_all;
-  (void)direct_exscan256(before, sbuf, &base_all);
-  const int sl_me = tid < DH ? width_slot(bits[g * DH + tid]) : -1;
-  const unsigned long long mine = sl_me >= 0 ? 1ull << (16 * sl_me) : 0ull;
-  unsigned long long head_tot;
-  const unsigned long long exh = direct_exscan256(mine, sbuf, &head_tot);
-  if (tid < DH) {
-    long long b = -1;
-    if (sl_me >= 0) {
-      const long long entry = static_cast<long long>(((base_all + exh) >> (16 * sl_me)) & 0xFFFFull);
-      if (entry < sp.cap_units[sl_me]) b = sp.goff[sl_me][pool * sp.cap_units[sl_me] + entry] + j;
-      if (b >= sp.cap_groups[sl_me]) b = -1;
+  const int n = n_kept[g];
+  const int nkb = (n + TOK - 1) / TOK;
+  const int* kg = kept + static_cast<long long>(g) * N;
+  float* og = out + static_cast<long long>(g) * N * DH;
+  if (jb >= nkb) {  // zero dropped tokens kept[g][n + TOK (jb - nkb) ..]
+    const int d0 = n + (jb - nkb) * TOK;
+    if (d0 >= N) return;
+    const int cnt = min(TOK, N - d0);
+    for (int e = threadIdx.x; e < cnt * (DH / 4); e += kChanThreads) {
+      const int i = e / (DH / 4), c4 = (e % (DH / 4)) * 4;
+      *reinterpret_cast<float4*>(og + static_cast<long long>(kg[d0 + i]) * DH + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    s_w[tid] = sl_me >= 0 ? static_cast<int>(bits[g * DH + tid]) : 0;
-    s_base[tid] = b;
+    return;
+  }
+  const int k0 = jb * TOK;
+  const int rows = min(TOK, n - k0);
+  for (int c = threadIdx.x; c < DH; c += kChanThreads) {
+    const long long b = chan_base[static_cast<long long>(g) * DH + c];
+    s_w[c] = bits[static_cast<long long>(g) * DH + c];
+    s_base[c] = b >= 0 ? b + jb * kChanTGd : -1;
   }
   __syncthreads();
-  const int l16 = threadIdx.x & 15, hw = threadIdx.x >> 4;
-  for (int c = hw; c < DH; c += 16) {
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
-    const long long grp = s_base[c];
-    if (grp >= 0) {
-      const int w = s_w[c];
-      const int s = width_slot(w);
-      const long long gg = pool * sp.cap_groups[s] + grp;
-      dequant_lane4(sp.codes[s] + gg * (8 * w), w, l16, sp.scales[s] + gg, y);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, sub = lane >> 3, l8 = lane & 7;
+  for (int p0 = warp * 4; p0 < DH * kChanTGd; p0 += (kChanThreads / 32) * 4) {
+    const int p = p0 + sub;
+    const int c = p % DH, jg = p / DH;
+    if (jg * 64 >= rows) continue;
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = 0.f;
+    const int w = s_w[c], s = width_slot(w);
+    if (s >= 0 && s_base[c] >= 0) {
+      const long long gg = pool * sp.cap_groups[s] + s_base[c] + jg;
+      dequant_lane8(sp.codes[s] + gg * (8 * w), w, l8, sp.scales[s] + gg, y);
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) tile[4 * l16 + e][c] = y[e];
+    for (int e = 0; e < 8; ++e) ftile[(jg * 64 + l8 * 8 + e) * LD + c] = y[e];
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < rows * (DH / 4); e += 256) {
+  for (int e = threadIdx.x; e < rows * (DH / 4); e += kChanThreads) {
     const int i = e / (DH / 4), c4 = (e % (DH / 4)) * 4;
-    *reinterpret_cast<float4*>(out + (static_cast<size_t>(g) * N + s_tok[i]) * DH + c4) =
-        make_float4(tile[i][c4], tile[i][c4 + 1], tile[i][c4 + 2], tile[i][c4 + 3]);
+    const float* t = ftile + i * LD + c4;
+    *reinterpret_cast<float4*>(og + static_cast<long long>(kg[k0 + i]) * DH + c4) = make_float4(t[0], t[1], t[2], t[3]);
   }
 }
 

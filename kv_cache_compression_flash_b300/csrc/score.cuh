@@ -17,9 +17,8 @@
 // special-function unit).  The reducer warps form two groups that take
 // alternate tiles (ping-pong), so one group's TMEM loads and barrier waits
 // overlap the other's arithmetic, and two TMEM buffers let the MMA of the next
-// tile run meanwhile.  Pass 1 (one CTA per SM): 16 reducer warps, TMA warp
-// 16, MMA warp 17.  Pass 2 (two CTAs per SM): 8 reducer warps, TMA warp 8,
-// MMA warp 9.
+// tile run meanwhile.  Both passes run one persistent CTA per SM: 16 reducer
+// warps, TMA warp 16, MMA warp 17.
 //
 // GQA packing: a 128-row query tile holds P = 128/Gt consecutive window rows
 // of Gt heads of one KV group (row j = head (j / P), position pmin + j % P), so
@@ -37,8 +36,6 @@
 
 namespace kvs {
 
-constexpr int kScoreThreads = 320;   // pass 2: 8 reducer warps, 1 TMA warp, 1 MMA warp
-constexpr int kTmaWarp = 8, kMmaWarp = 9;
 constexpr int kScoreThreads1 = 576;  // pass 1: 16 reducer warps (two row tiles), 1 TMA warp, 1 MMA warp
 constexpr int kTmaWarp1 = 16, kMmaWarp1 = 17;
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -260,6 +257,8 @@ __global__ void __launch_bounds__(kScoreThreads1, 1)
     if (lane == 0) {  // MMA issuer: two row tiles against each K tile
       int n_it = 0, kc = 0;
       bool ok = true;
+      // test hook: withhold the first tile's arrive, so the reducers' bounded wait runs out
+      const bool withhold = *reinterpret_cast<volatile int*>(&g_debug_fault) == KVS_DEBUG_WITHHOLD_LSE_ARRIVE;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         LseItem x;
         if (!lse_item(geo, kt_chunk, n_split, it, &x)) continue;
@@ -277,7 +276,7 @@ __global__ void __launch_bounds__(kScoreThreads1, 1)
           issue_tile_mma<DH>(tmem + (2 * b) * 128, smem_u32(S.q[qb][0]), smem_u32(S.k[s]));
           if (x.two) issue_tile_mma<DH>(tmem + (2 * b + 1) * 128, smem_u32(S.q[qb][1]), smem_u32(S.k[s]));
           umma_commit(&S.k_empty[s]);
-          umma_commit(&S.s_full[b]);
+          if (!(withhold && kc == 0)) umma_commit(&S.s_full[b]);
         }
         if (ok) umma_commit(&S.q_empty[qb]);  // the item's row tiles are free once its MMAs finish
       }
@@ -401,61 +400,97 @@ __global__ void lse_offsets_kernel(const ScoreGeom geo, const float* __restrict_
 }
 
 // ---------------------------------------------------------------------------
-// pass 2: per-key reductions over queries (K-stationary)
+// pass 2: per-key reductions over queries (K-stationary, persistent)
 // ---------------------------------------------------------------------------
+// Persistent CTAs (one per SM, all 512 TMEM columns) walk work items
+// it = blockIdx.x, + gridDim.x, ...; an item is a PAIR of key tiles (kt0,
+// kt0 + 1) of KV head g and a range of the query tiles that see key tile kt0
+// (head chunk major, position block minor).  Every query tile TMA brings in
+// feeds two MMAs, S^T_j = K_j Q^T for both key tiles (M = 256 keys in
+// effect), which halves the L2 -> shared-memory traffic per flop against one
+// key tile per CTA: one 128x128 tile per 128x128x128 MMA would ask the L2 for
+// more bytes per clock than it delivers.  Query tiles entirely before key tile
+// kt0 + 1 skip its MMA.
+// Reducer warp w: group hh = w / 8 takes the query tiles of its parity
+// (ping-pong over the two TMEM buffer pairs), key tile j = (w / 4) % 2, TMEM
+// lane quarter w % 4; each thread owns one key and reduces along its TMEM
+// row.  At the end of an item the two groups' values of a key are combined in
+// a fixed order (group 1 hands its value to group 0 through shared memory,
+// ordered by an mbarrier pair: no named barrier, so a wait that gives up can
+// never leave a warp stranded).  Warp 16 issues TMA, warp 17 the MMAs.
+constexpr int kScoreThreads2 = 576;
+constexpr int kTmaWarp2 = 16, kMmaWarp2 = 17;
+
 template <int DH, int NS>
 struct ColSmem {
-  uint8_t k[TileCfg<DH>::kTileBytes];
-  uint8_t q[NS][TileCfg<DH>::kTileBytes];
-  float bv[NS][128];
-  float comb[128];
-  uint64_t k_full, q_full[NS], q_empty[NS], s_full[2], s_empty[2], drain;
+  uint8_t k[2][TileCfg<DH>::kTileBytes];   // the item's two key tiles
+  uint8_t q[NS][TileCfg<DH>::kTileBytes];  // query-tile ring
+  float bv[NS][128];                       // the offsets that came with each query tile
+  float comb[2][128];                      // group 1 -> group 0 hand-off, per key tile
+  uint64_t k_full, k_empty, q_full[NS], q_empty[NS], s_full[2], s_empty[2], c_full, c_empty, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-// One CTA: 128 keys (kt) of KV head g, query tiles [q0, q1) of that key tile's
-// visible list (head chunk major, position block minor).
-//   MAXMODE = false: out = sum_j 2^(s_j c - b_j)               (w_t)
-//   MAXMODE = true : out = max_heads 2^(max_j (s_j c - b_j)) / vn[head][t]   (vn null: / 1)
+struct ColItem {
+  int g, kt0, q0, q1, nvis, pb_lo, pb_lo1, split;
+  bool two;
+};
+
+__host__ __device__ inline int col_pairs(const ScoreGeom& geo) { return (geo.n_kt + 1) / 2; }
+
+// item it = ((pair * Hkv) + g) * n_split + split: early pairs (the longest
+// query lists) first
+__device__ __forceinline__ bool col_item(const ScoreGeom& geo, const int qt_chunk, const int n_split, const int it,
+                                         ColItem* x) {
+  x->split = it % n_split;
+  const int r = it / n_split;
+  x->g = r % geo.Hkv;
+  x->kt0 = 2 * (r / geo.Hkv);
+  x->two = x->kt0 + 1 < geo.n_kt;
+  x->nvis = kt_nvis(geo, x->kt0);
+  x->pb_lo = geo.n_pb - x->nvis;
+  x->pb_lo1 = x->two ? geo.n_pb - kt_nvis(geo, x->kt0 + 1) : geo.n_pb;  // first block key tile kt0+1 sees
+  const int nq = x->nvis * geo.n_hc;
+  x->q0 = x->split * qt_chunk;
+  x->q1 = min(nq, x->q0 + qt_chunk);
+  return x->q0 < x->q1;
+}
+
+// MAXMODE = false: out = sum_j 2^(s_j c - b_j)                            (w_t)
+// MAXMODE = true : out = max_heads 2^(max_j (s_j c - b_j)) / vn[head][t]   (vn null: / 1)
 // Output goes to out_direct (n_split == 1) or out_partial[split][g*N + t].
 template <int DH, int NS, int GT, bool MAXMODE>
-__global__ void __launch_bounds__(kScoreThreads, 2)
+__global__ void __launch_bounds__(kScoreThreads2, 1)
     colreduce_pass_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
-                          const ScoreGeom geo, const int qt_chunk, const int n_split,
+                          const ScoreGeom geo, const int qt_chunk, const int n_split, const int n_items,
                           const float* __restrict__ bvals, const float* __restrict__ vn,
                           float* __restrict__ out_direct, float* __restrict__ out_partial) {
   constexpr int P = 128 / GT;
   extern __shared__ uint8_t smem_raw[];
   ColSmem<DH, NS>& S = *reinterpret_cast<ColSmem<DH, NS>*>(align1024(smem_raw));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x;
-  const int kt = blockIdx.y / geo.Hkv, g = blockIdx.y % geo.Hkv;
-  const int t0 = kt * 128;
-  const int nvis = kt_nvis(geo, kt);
-  const int pb_lo = geo.n_pb - nvis;
-  const int nq = nvis * geo.n_hc;
-  const int q0 = split * qt_chunk;
-  const int q1 = min(nq, q0 + qt_chunk);
-  if (q0 >= q1 || timeout_recorded()) return;
-  const int niter = q1 - q0;
+  if (timeout_recorded()) return;  // uniform over the CTA, before any barrier
 
   if (threadIdx.x == 0) {
     mbar_init(&S.k_full, 1);
+    mbar_init(&S.k_empty, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&S.q_full[s], 1);
-      mbar_init(&S.q_empty[s], 1 + 4);
+      mbar_init(&S.q_empty[s], 1 + 8);  // the MMAs, and the 8 warps that read the staged offsets
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.s_full[b], 1);
-      mbar_init(&S.s_empty[b], 4);
+      mbar_init(&S.s_empty[b], 8);      // the 8 warps of the group that owns buffer pair b
     }
+    mbar_init(&S.c_full, 8);
+    mbar_init(&S.c_empty, 8);
     mbar_init(&S.drain, 1);
     S.abort_flag = 0;
     mbar_fence_init();
   }
   if (warp == 0) {
-    tmem_alloc(&S.tmem_base, 256);
+    tmem_alloc(&S.tmem_base, 512);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -466,47 +501,71 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   const uint32_t tmem = S.tmem_base;
   volatile int* abort_flag = &S.abort_flag;
 
-  if (warp == kTmaWarp) {
+  if (warp == kTmaWarp2) {
     if (lane == 0) {  // TMA producer
       prefetch_tensormap(&mapQ);
       prefetch_tensormap(&mapK);
       constexpr uint32_t kBytes = TileCfg<DH>::kTileBytes;
-      mbar_arrive_expect_tx(&S.k_full, kBytes);
+      int n_it = 0, qc = 0, issued = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        ColItem x;
+        if (!col_item(geo, qt_chunk, n_split, it, &x)) continue;
+        // the key tiles: one buffer, free once the previous item's MMAs are done
+        if (!mbar_wait(&S.k_empty, (n_it & 1) ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(&S.k_full, 2 * kBytes);
 #pragma unroll
-      for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
-        tma_load_3d(S.k + p * 16384, &mapK, &S.k_full, p * 64, t0, g);
-      int issued = 0;
-      for (int i = 0; i < niter; ++i) {
-        const int s = i % NS;
-        if (!mbar_wait(&S.q_empty[s], ((i / NS) & 1) ^ 1u, abort_flag)) break;
-        const int q = q0 + i;
-        const int hc = q / nvis, pb = pb_lo + q % nvis;
-        const int rt = (g * geo.n_hc + hc) * geo.n_pb + pb;
-        mbar_arrive_expect_tx(&S.q_full[s], kBytes + 512u);
+        for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
-          tma_load_3d(S.q[s] + p * 16384, &mapQ, &S.q_full[s], p * 64, pb * P, g * geo.G + hc * GT);
-        bulk_load(S.bv[s], bvals + static_cast<size_t>(rt) * 128, 512u, &S.q_full[s]);
-        issued = i + 1;
+          for (int p = 0; p < TileCfg<DH>::kPanels; ++p)  // a tile past the last key reads as zeros
+            tma_load_3d(S.k[t] + p * 16384, &mapK, &S.k_full, p * 64, (x.kt0 + t) * 128, x.g);
+        ++n_it;
+        for (int q = x.q0; q < x.q1; ++q, ++qc) {
+          const int s = qc % NS;
+          if (!mbar_wait(&S.q_empty[s], ((qc / NS) & 1) ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int hc = q / x.nvis, pb = x.pb_lo + q % x.nvis;
+          const int rt = (x.g * geo.n_hc + hc) * geo.n_pb + pb;
+          mbar_arrive_expect_tx(&S.q_full[s], kBytes + 512u);
+#pragma unroll
+          for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
+            tma_load_3d(S.q[s] + p * 16384, &mapQ, &S.q_full[s], p * 64, pb * P, x.g * geo.G + hc * GT);
+          bulk_load(S.bv[s], bvals + static_cast<size_t>(rt) * 128, 512u, &S.q_full[s]);
+          issued = qc + 1;
+        }
       }
-      if (*abort_flag) {
+      if (*abort_flag) {  // let our copies land before the CTA goes away
         volatile int never = 0;
-        mbar_wait(&S.k_full, 0, &never);
+        if (n_it > 0) mbar_wait(&S.k_full, (n_it - 1) & 1, &never);
         for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(&S.q_full[i % NS], (i / NS) & 1, &never);
       }
     }
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) {  // MMA issuer: S^T tile = K_tile (M = 128 keys) x Q_tile^T (N = 128 rows)
-      if (mbar_wait(&S.k_full, 0, abort_flag)) {
-        for (int i = 0; i < niter; ++i) {
-          const int s = i % NS, b = i & 1;
-          if (!mbar_wait(&S.q_full[s], (i / NS) & 1, abort_flag)) break;
-          if (!mbar_wait(&S.s_empty[b], ((i >> 1) & 1) ^ 1u, abort_flag)) break;
+  } else if (warp == kMmaWarp2) {
+    if (lane == 0) {  // MMA issuer: S^T_j = K_j (M = 128 keys) x Q_tile^T (N = 128 rows), j = 0, 1
+      int n_it = 0, qc = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        ColItem x;
+        if (!col_item(geo, qt_chunk, n_split, it, &x)) continue;
+        if (!mbar_wait(&S.k_full, n_it & 1, abort_flag)) break;
+        ++n_it;
+        for (int q = x.q0; q < x.q1; ++q, ++qc) {
+          const int s = qc % NS, b = qc & 1;
+          if (!mbar_wait(&S.q_full[s], (qc / NS) & 1, abort_flag) ||
+              !mbar_wait(&S.s_empty[b], ((qc >> 1) & 1) ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          issue_tile_mma<DH>(tmem + b * 128, smem_u32(S.k), smem_u32(S.q[s]));
+          const int pb = x.pb_lo + q % x.nvis;
+          issue_tile_mma<DH>(tmem + (2 * b) * 128, smem_u32(S.k[0]), smem_u32(S.q[s]));
+          if (x.two && pb >= x.pb_lo1) issue_tile_mma<DH>(tmem + (2 * b + 1) * 128, smem_u32(S.k[1]), smem_u32(S.q[s]));
           umma_commit(&S.q_empty[s]);
           umma_commit(&S.s_full[b]);
         }
+        if (ok) umma_commit(&S.k_empty);  // the key tiles are free once the item's MMAs finish
       }
       if (*abort_flag) {
         volatile int never = 0;
@@ -514,125 +573,148 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
         mbar_wait(&S.drain, 0, &never);
       }
     }
-  } else {  // warps 0-7: one key per thread (TMEM lane); group warp / 4 takes the query tiles of its parity
-    const int q4 = warp & 3, hh = warp >> 2;
+  } else {  // warps 0-15: one key per thread (TMEM lane of key tile j); group hh takes the query tiles of its parity
+    const int hh = warp >> 3, j = (warp >> 2) & 1, q4 = warp & 3;
     const int krow = q4 * 32 + lane;
-    const int t = t0 + krow;
     const float c = geo.c_log2;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
-    float acc = 0.f;
-    float best = 0.f;
-    float mx[GT];
-#pragma unroll
-    for (int h = 0; h < GT; ++h) mx[h] = -INFINITY;
-    int cur_hc = -1;
-    auto flush = [&](int hc) {
-#pragma unroll
-      for (int h = 0; h < GT; ++h) {
-        if (mx[h] != -INFINITY && t < geo.N) {
-          float r = ex2_approx(mx[h]);
-          if (vn) r = r / vn[static_cast<size_t>(g * geo.G + hc * GT + h) * geo.N + t];
-          best = fmaxf(best, r);
-        }
-        mx[h] = -INFINITY;
-      }
-    };
-    // one 32-column chunk: x = s c - b_col, masked where the query precedes the key
-    auto chunk = [&](uint32_t (&r)[32], const float* bcol, const int col0, const int pmin, const bool diag) {
-      float* v = reinterpret_cast<float*>(r);
-      const unsigned long long c2 = f2_pack(c, c);
-      const float4* b4 = reinterpret_cast<const float4*>(bcol);
-#pragma unroll
-      for (int j4 = 0; j4 < 8; ++j4) {
-        const float4 bb = b4[j4];
-        f2_unpack(f2_fma(f2_pack(v[4 * j4], v[4 * j4 + 1]), c2, f2_pack(-bb.x, -bb.y)), &v[4 * j4], &v[4 * j4 + 1]);
-        f2_unpack(f2_fma(f2_pack(v[4 * j4 + 2], v[4 * j4 + 3]), c2, f2_pack(-bb.z, -bb.w)), &v[4 * j4 + 2],
-                  &v[4 * j4 + 3]);
-      }
-      if (diag) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (pmin + ((col0 + j) % P) < t) v[j] = -INFINITY;
-      }
-      if (MAXMODE) {
-        float x[11];
-#pragma unroll
-        for (int k = 0; k < 10; ++k) x[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
-        x[10] = fmaxf(v[30], v[31]);
-        const float z = fmax3(fmax3(fmax3(x[0], x[1], x[2]), fmax3(x[3], x[4], x[5]), fmax3(x[6], x[7], x[8])),
-                              x[9], x[10]);
-        const int hl = col0 / P;  // P >= 32: the chunk lies in one head
-#pragma unroll
-        for (int h = 0; h < GT; ++h)
-          if (h == hl) mx[h] = fmaxf(mx[h], z);
-      } else {
-        unsigned long long a0 = 0ull, a1 = 0ull;
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          a0 = f2_add(a0, f2_pack(ex2_approx(v[j]), ex2_approx(v[j + 1])));
-          a1 = f2_add(a1, f2_pack(ex2_approx(v[j + 2]), ex2_approx(v[j + 3])));
-        }
-        float s0, s1;
-        f2_unpack(f2_add(a0, a1), &s0, &s1);
-        acc += s0 + s1;
-      }
-    };
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + j * 128;
     uint32_t va[32], vb[32];
-    for (int i = 0; i < niter; ++i) {
-      const int s = i % NS, b = i & 1;
-      const int q = q0 + i;
-      const int hc = q / nvis, pb = pb_lo + q % nvis;
-      if (MAXMODE && hc != cur_hc) {
-        if (cur_hc >= 0) flush(cur_hc);
-        cur_hc = hc;
+    int qc = 0, n_it = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      ColItem x;
+      if (!col_item(geo, qt_chunk, n_split, it, &x)) continue;
+      const int t0 = (x.kt0 + j) * 128;
+      const int t = t0 + krow;
+      float acc = 0.f, best = 0.f;
+      float mx[GT];
+#pragma unroll
+      for (int h = 0; h < GT; ++h) mx[h] = -INFINITY;
+      int cur_hc = -1;
+      auto flush = [&](int hc) {
+#pragma unroll
+        for (int h = 0; h < GT; ++h) {
+          if (mx[h] != -INFINITY && t < geo.N) {
+            float r = ex2_approx(mx[h]);
+            if (vn) r = r / vn[static_cast<size_t>(x.g * geo.G + hc * GT + h) * geo.N + t];
+            best = fmaxf(best, r);
+          }
+          mx[h] = -INFINITY;
+        }
+      };
+      // one 32-column chunk: x = s c - b_col, masked where the query precedes the key
+      auto chunk = [&](uint32_t (&r)[32], const float* bcol, const int col0, const int pmin, const bool diag) {
+        float* v = reinterpret_cast<float*>(r);
+        const unsigned long long c2 = f2_pack(c, c);
+        const float4* b4 = reinterpret_cast<const float4*>(bcol);
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 bb = b4[j4];
+          f2_unpack(f2_fma(f2_pack(v[4 * j4], v[4 * j4 + 1]), c2, f2_pack(-bb.x, -bb.y)), &v[4 * j4],
+                    &v[4 * j4 + 1]);
+          f2_unpack(f2_fma(f2_pack(v[4 * j4 + 2], v[4 * j4 + 3]), c2, f2_pack(-bb.z, -bb.w)), &v[4 * j4 + 2],
+                    &v[4 * j4 + 3]);
+        }
+        if (diag) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (pmin + ((col0 + e) % P) < t) v[e] = -INFINITY;
+        }
+        if (MAXMODE) {
+          float y[11];
+#pragma unroll
+          for (int k = 0; k < 10; ++k) y[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+          y[10] = fmaxf(v[30], v[31]);
+          const float z = fmax3(fmax3(fmax3(y[0], y[1], y[2]), fmax3(y[3], y[4], y[5]), fmax3(y[6], y[7], y[8])),
+                                y[9], y[10]);
+          const int hl = col0 / P;  // P >= 32: the chunk lies in one head
+#pragma unroll
+          for (int h = 0; h < GT; ++h)
+            if (h == hl) mx[h] = fmaxf(mx[h], z);
+        } else {
+          unsigned long long a0 = 0ull, a1 = 0ull;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            a0 = f2_add(a0, f2_pack(ex2_approx(v[e]), ex2_approx(v[e + 1])));
+            a1 = f2_add(a1, f2_pack(ex2_approx(v[e + 2]), ex2_approx(v[e + 3])));
+          }
+          float s0, s1;
+          f2_unpack(f2_add(a0, a1), &s0, &s1);
+          acc += s0 + s1;
+        }
+      };
+      for (int q = x.q0; q < x.q1; ++q, ++qc) {
+        const int s = qc % NS, b = qc & 1;
+        const int hc = q / x.nvis, pb = x.pb_lo + q % x.nvis;
+        if (MAXMODE && hc != cur_hc) {
+          if (cur_hc >= 0) flush(cur_hc);
+          cur_hc = hc;
+        }
+        if ((qc & 1) != hh) continue;  // the other group's tile
+        if (!mbar_wait(&S.s_full[b], (qc >> 1) & 1, abort_flag) ||
+            !mbar_wait(&S.q_full[s], (qc / NS) & 1, abort_flag)) {  // the staged offsets arrived with the tile
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (j == 0 || (x.two && pb >= x.pb_lo1)) {
+          const int pmin = geo.q_pos0 + pb * P;
+          const bool diag = pmin < t0 + 127;
+          const uint32_t base = lane_base + b * 256;
+          tmem_issue32(base, va);
+          tmem_wait32(va);
+          tmem_issue32(base + 32, vb);
+          chunk(va, S.bv[s], 0, pmin, diag);
+          tmem_wait32(vb);
+          tmem_issue32(base + 64, va);
+          chunk(vb, S.bv[s] + 32, 32, pmin, diag);
+          tmem_wait32(va);
+          tmem_issue32(base + 96, vb);
+          chunk(va, S.bv[s] + 64, 64, pmin, diag);
+          tmem_wait32(vb);
+          tc_fence_before();  // this warp is done with the TMEM buffer
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.s_empty[b]);
+          chunk(vb, S.bv[s] + 96, 96, pmin, diag);
+        } else {  // key tile kt0+1 precedes every query of this tile: only release the buffer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.s_empty[b]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.q_empty[s]);  // done reading bv[s]
       }
-      if ((i & 1) != hh) continue;  // the other group's tile (it also releases the stage)
-      if (!mbar_wait(&S.s_full[b], (i >> 1) & 1, abort_flag)) break;
-      // the staged offsets bv[s] arrived with the query tile
-      if (!mbar_wait(&S.q_full[s], (i / NS) & 1, abort_flag)) break;
-      tc_fence_after();
-      const int pmin = geo.q_pos0 + pb * P;
-      const bool diag = pmin < t0 + 127;
-      const uint32_t base = lane_base + b * 128;
-      tmem_issue32(base, va);
-      tmem_wait32(va);
-      tmem_issue32(base + 32, vb);
-      chunk(va, S.bv[s], 0, pmin, diag);
-      tmem_wait32(vb);
-      tmem_issue32(base + 64, va);
-      chunk(vb, S.bv[s] + 32, 32, pmin, diag);
-      tmem_wait32(va);
-      tmem_issue32(base + 96, vb);
-      chunk(va, S.bv[s] + 64, 64, pmin, diag);
-      tmem_wait32(vb);
-      tc_fence_before();  // this warp is done with the TMEM buffer
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.s_empty[b]);
-      chunk(vb, S.bv[s] + 96, 96, pmin, diag);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.q_empty[s]);  // done reading bv[s]
-    }
-    if (MAXMODE && cur_hc >= 0) flush(cur_hc);
-    // combine the two groups in a fixed order: group 1 hands its value to group 0
-    float* comb = reinterpret_cast<float*>(S.comb);
-    if (hh == 1) comb[krow] = MAXMODE ? best : acc;
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    if (hh == 0) {
-      const float res = MAXMODE ? fmaxf(best, comb[krow]) : acc + comb[krow];
-      if (t < geo.N) {
-        const size_t o = static_cast<size_t>(g) * geo.N + t;
-        if (n_split == 1)
-          out_direct[o] = res;
-        else
-          out_partial[static_cast<size_t>(split) * geo.Hkv * geo.N + o] = res;
+      if (!ok) break;
+      if (MAXMODE && cur_hc >= 0) flush(cur_hc);
+      // the two groups' values of this key, combined in a fixed order
+      const float mine = MAXMODE ? best : acc;
+      if (hh == 1) {
+        if (!mbar_wait(&S.c_empty, (n_it & 1) ^ 1u, abort_flag)) break;
+        S.comb[j][krow] = mine;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.c_full);
+      } else {
+        if (!mbar_wait(&S.c_full, n_it & 1, abort_flag)) break;
+        const float other = S.comb[j][krow];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.c_empty);
+        const float res = MAXMODE ? fmaxf(mine, other) : mine + other;
+        if (t < geo.N) {
+          const size_t o = static_cast<size_t>(x.g) * geo.N + t;
+          if (n_split == 1)
+            out_direct[o] = res;
+          else
+            out_partial[static_cast<size_t>(x.split) * geo.Hkv * geo.N + o] = res;
+        }
       }
+      ++n_it;
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -647,7 +729,8 @@ __global__ void colreduce_finalize_kernel(const ScoreGeom geo, const int qt_chun
   const int total = geo.Hkv * geo.N;
   if (idx >= total) return;
   const int t = idx % geo.N;
-  const int ns = ceil_div_i(kt_nvis(geo, t / 128) * geo.n_hc, qt_chunk);
+  // a key's splits are those of its key-tile pair, whose query list is the first tile's
+  const int ns = ceil_div_i(kt_nvis(geo, (t / 128) & ~1) * geo.n_hc, qt_chunk);
   float r = 0.f;
   for (int s = 0; s < ns; ++s) {
     const float v = part[static_cast<size_t>(s) * total + idx];

@@ -100,18 +100,18 @@ int plan_score(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, int64_t d, int64_t
   pl->want_plus = (mode & KVS_MODE_KVZIP_PLUS) != 0;
   pl->want_max = (mode & (KVS_MODE_KVZIP | KVS_MODE_KVZIP_PLUS)) != 0;
   pl->lse_given = (mode & KVS_MODE_LSE_GIVEN) != 0;
-  // Split long loops so the grid holds about three waves of pass-1 CTAs (two
-  // per SM) and one wave of pass-2 CTAs; measured on the bench workload, more
-  // splits cost more in pipeline fill and merging than they gain in balance.
-  const long long slots = static_cast<long long>(sm_count()) * 2;
-  const long long target = static_cast<long long>(sm_count()) * 8, target2 = slots;
+  // Split long loops so that the persistent pass-1 CTAs see about eight work
+  // items each and the pass-2 CTAs (key-tile pairs) about four; measured on
+  // the 8 192-key layer, more splits cost more in pipeline fill and merging
+  // than they gain in balance.
+  const long long target = static_cast<long long>(sm_count()) * 8, target2 = static_cast<long long>(sm_count()) * 4;
   long long w1 = 0;
   for (int pb = 1; pb < g.n_pb + 1; pb += 2) w1 += pb_nkt(g, std::min(pb, g.n_pb - 1));  // per pair of row tiles
   w1 *= static_cast<long long>(g.Hkv) * g.n_hc;
   pl->kt_chunk = static_cast<int>(std::max<long long>(4, cdiv(w1, target)));
   pl->n_split1 = static_cast<int>(cdiv(pb_nkt(g, g.n_pb - 1), pl->kt_chunk));
-  long long w2 = 0;
-  for (int kt = 0; kt < g.n_kt; ++kt) w2 += kt_nvis(g, kt);
+  long long w2 = 0;  // query tiles over the key-tile pairs (a pair's list is its first tile's)
+  for (int kt = 0; kt < g.n_kt; kt += 2) w2 += kt_nvis(g, kt);
   w2 *= static_cast<long long>(g.Hkv) * g.n_hc;
   pl->qt_chunk = static_cast<int>(std::max<long long>(4, cdiv(w2, target2)));
   pl->n_split2 = static_cast<int>(cdiv(static_cast<long long>(kt_nvis(g, 0)) * g.n_hc, pl->qt_chunk));
@@ -152,11 +152,8 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
 }
 
-constexpr int kStages = 2;
+constexpr int kStages2 = 4;  // pass-2 query-tile ring
 constexpr int kStages1 = 3;  // pass-1 K ring
-// Each scoring CTA holds 256 TMEM columns; 512 exist per SM.  Asking for at
-// least this much shared memory keeps residency at two CTAs per SM.
-constexpr size_t kScoreMinSmem = 80 * 1024;
 
 template <int DH>
 int launch_lse(const ScorePlan& pl, const CUtensorMap& mq, const CUtensorMap& mk, float2* part,
@@ -175,11 +172,14 @@ int launch_lse(const ScorePlan& pl, const CUtensorMap& mq, const CUtensorMap& mk
 template <int DH, int GT, bool MAXM>
 int launch_col_gt(const ScorePlan& pl, const CUtensorMap& mq, const CUtensorMap& mk, const float* bvals,
                   const float* vn, float* out, float* part, cudaStream_t st) {
-  auto kern = colreduce_pass_kernel<DH, kStages, GT, MAXM>;
-  const size_t smem = std::max(sizeof(ColSmem<DH, kStages>) + 1024, kScoreMinSmem);
+  auto kern = colreduce_pass_kernel<DH, kStages2, GT, MAXM>;
+  // at least half the shared memory: one CTA per SM (it holds all 512 TMEM columns)
+  const size_t smem = std::max(sizeof(ColSmem<DH, kStages2>) + 1024, static_cast<size_t>(116 * 1024));
   KVS_CUDA_TRY(allow_smem(kern, smem));
-  dim3 grid(pl.n_split2, pl.geo.n_kt * pl.geo.Hkv);
-  KVS_CUDA_TRY(launch_k(kern, dim3(grid), dim3(kScoreThreads), smem, st, 0, mq, mk, pl.geo, pl.qt_chunk, pl.n_split2, bvals, vn, out, part));
+  const int n_items = col_pairs(pl.geo) * pl.geo.Hkv * pl.n_split2;
+  const int grid = std::min(n_items, sm_count());  // persistent: one CTA per SM
+  KVS_CUDA_TRY(launch_k(kern, dim3(grid), dim3(kScoreThreads2), smem, st, 0, mq, mk, pl.geo, pl.qt_chunk, pl.n_split2,
+                        n_items, bvals, vn, out, part));
   if (pl.n_split2 > 1) {
     const int total = pl.geo.Hkv * pl.geo.N;
     KVS_CUDA_TRY(launch_k(colreduce_finalize_kernel<MAXM>, dim3(static_cast<unsigned>(cdiv(total, 256))), dim3(256),

@@ -89,16 +89,13 @@ class RdkvLayerStep:
         Hq, Hkv, N, W, d = self.shape
         P = self.n_pools
         n = K_.score_plan_info(P * Hq, P * Hkv, W, N, d, mode=self.BOTH_MODE)[4]   # the step's one scoring call
-        n += 1          # channel weights (one cluster per KV head)
         n += 1          # sigma_t
         for U in (self.U_v, self.U_k):   # allocations: one launch for every pool on clusters, else one per pool
             n += 1 if K_.allocate_plan_info(U, self.width_mask)[0] > 0 else P
-        n += 1          # sigma_c
-        n += 2 + 2      # V pack (plan, pack), K pack (plan, pack)
+        n += 1          # w_c and sigma_c (one cluster per KV head)
+        n += 2 + 2      # V pack (chunk counts, pack), K pack (plan, pack)
         if self.dequant:
-            # V dequant (decode + zero); K dequant (decode + zero, planned inside the
-            # kernel up to 16 384 tokens, else a plan kernel first)
-            n += 1 + (1 if N <= 16384 and Hkv * d < 65536 else 2)
+            n += 2 + 2  # V dequant (chunk counts, decode), K dequant (plan, decode + zero)
         return n
 
     def _flat(self, Q, K, V):
@@ -127,7 +124,7 @@ class RdkvLayerStep:
     def rest(self, Q, K, V, stream=None):
         """Everything after scoring, as two dependent chains on two streams:
         V: sigma_t -> V allocation -> V pack (-> dequant);
-        K: w_c (from the start), then after the V widths: sigma_c -> K
+        K, after the V widths: w_c and sigma_c (one read of K) -> K
         allocation -> K pack (-> dequant)."""
         Hq, Hkv, N, W, d = self.shape
         P = self.n_pools
@@ -135,9 +132,6 @@ class RdkvLayerStep:
         ws = self.ws
         main = stream if stream is not None else torch.cuda.current_stream()
         side = self.side_stream
-        side.wait_stream(main)
-        with torch.cuda.stream(side):
-            K_.channel_weights(Q, K, out=self.w_c, ws=ws["cw"], stream=side)
         K_.unit_rms(V, 0, out=self.sig_t, ws=ws["rms0"], stream=main)
         bits_v, bits_k = self.pool_bits()
         K_.allocate_bits_pools(self.out["w_t"].view(P, self.U_v), self.sig_t.view(P, self.U_v), self.B_v,
@@ -146,7 +140,7 @@ class RdkvLayerStep:
         X4 = (P, Hkv, N, d)
         with torch.cuda.stream(side):
             side.wait_event(self.v_done)
-            K_.unit_rms(K, 1, keep_bits=self.bits_v, out=self.sig_c, ws=ws["rms1"], stream=side)
+            K_.channel_stats(Q, K, self.bits_v, out_wc=self.w_c, out_sigma=self.sig_c, stream=side)
             K_.allocate_bits_pools(self.w_c.view(P, self.U_k), self.sig_c.view(P, self.U_k), self.B_k,
                                    self.width_mask, out=bits_k, ws=ws["ak"], stream=side)
             K_.quantize_pack_pools(K.view(X4), 1, self.bits_k, self.bits_v, self.k_streams, ws=ws["pk"], stream=side)
@@ -201,3 +195,74 @@ class RdkvLayerStep:
             if events is not None:
                 events[i + 1].record()
         return self
+
+
+class KvzipStep(RdkvLayerStep):
+    """KVzap's eviction pass over one pool: KVzip+ scores, then the bottom
+    fraction of tokens evicted and the rest kept at 16 bits   [KVzap §2.1
+    score s+, §2.3 eviction by score].
+
+    Inputs as RdkvLayerStep plus h [W, D] and W_O [D, Hq*d] (given to the
+    constructor, they stay fixed).  Stage 2 is the allocation over widths
+    {0, 16} with sigma = 1 and budget 16 * (U - floor(evict * U)), which keeps
+    exactly the top-scoring tokens (ties to the lower unit); the K cache is
+    stored for the kept tokens at 16 bits per channel.
+    """
+
+    PASS2_MODE = K_.MODE_KVZIP_PLUS | K_.MODE_LSE_GIVEN
+    BOTH_MODE = K_.MODE_LSE | K_.MODE_KVZIP_PLUS
+
+    def __init__(self, Hq, Hkv, N, W, d, evict_fraction, h, W_O, device="cuda", dequant=True):
+        U = Hkv * N
+        keep = U - int(math.floor(evict_fraction * U))
+        super().__init__(Hq, Hkv, N, W, d, 16.0 * keep / U, device=device, width_mask=K_.WIDTHS_KEEP_OR_EVICT,
+                         dequant=dequant, n_pools=1)
+        dev = torch.device(device)
+        self.B_v = 16 * keep
+        self.B_k = 16 * self.U_k
+        self.h, self.W_O = h, W_O
+        self.D = h.shape[1]
+        self.out["s_plus"] = torch.empty(Hkv, N, dtype=torch.float32, device=dev)
+        self.ones = torch.ones(U, dtype=torch.float32, device=dev)
+        self.bits_k.fill_(16)                      # kept tokens: every K channel at 16 bits
+        self.v_streams = K_.Streams(Hkv, N, d, 0, self.B_v, dev)
+        self.k_streams = K_.Streams(Hkv, N, d, 1, self.B_k, dev)
+        L = K_.lib()
+        for k, mode in (("score", K_.MODE_LSE), ("score2", self.PASS2_MODE), ("score12", self.BOTH_MODE)):
+            self.ws[k].get(L.kvs_score_workspace_size(Hq, Hkv, W, N, d, self.D, N - W, mode), dev)
+
+    def kernel_launches(self) -> int:
+        Hq, Hkv, N, W, d = self.shape
+        n = K_.score_plan_info(Hq, Hkv, W, N, d, D=self.D, mode=self.BOTH_MODE)[4]
+        n += 1 if K_.allocate_plan_info(self.U_v, self.width_mask)[0] > 0 else 1
+        n += 2 + 2      # V pack (chunk counts, pack), K pack (plan, pack)
+        if self.dequant:
+            n += 2 + 2  # V dequant (chunk counts, decode), K dequant (plan, decode + zero)
+        return n
+
+    def _score(self, Q, K, V, mode, ws, stream):
+        Hq, Hkv, N, W, d = self.shape
+        K_.score_attention(Q, K, q_pos0=N - W, mode=mode, V=V, h=self.h, W_O=self.W_O, out=self.out, ws=ws,
+                           stream=stream)
+
+    def pass1(self, Q, K, V, stream=None):
+        self._score(Q, K, V, K_.MODE_LSE, self.ws["score"], stream)
+
+    def pass2(self, Q, K, V, stream=None):
+        self._score(Q, K, V, self.PASS2_MODE, self.ws["score2"], stream)
+
+    def score(self, Q, K, V, stream=None):
+        self._score(Q, K, V, self.BOTH_MODE, self.ws["score12"], stream)
+
+    def rest(self, Q, K, V, stream=None):
+        """Eviction by score (widths {0, 16}), then V rows and K channels of the
+        kept tokens packed raw (16 bits) and read back."""
+        ws = self.ws
+        main = stream if stream is not None else torch.cuda.current_stream()
+        K_.allocate_bits(self.out["s_plus"], self.ones, self.B_v, self.width_mask, out=self.bits_v, ws=ws["av"],
+                         stream=main)
+        K_.quantize_pack(V, 0, self.bits_v, None, self.v_streams, ws=ws["pv"], stream=main)
+        K_.quantize_pack(K, 1, self.bits_k, self.bits_v, self.k_streams, ws=ws["pk"], stream=main)
+        if self.dequant:
+            K_.dequantize(self.v_streams, self.bits_v, None, out=self.v_hat, ws=ws["dv"], stream=main)
+            K_.dequantize(self.k_streams, self.bits_k, self.bits_v, out=self.k_hat, ws=ws["dk"], stream=main)

@@ -154,9 +154,8 @@ def test_kvzip_plus_full_size():
     for g in (0, 7):
         wo_heads = np.stack([f64(t["W_O"][:, (g * G + i) * d:(g * G + i + 1) * d]) for i in range(G)])
         check_tail_keys(sp, t["Q"], t["K"], G, 0, g, 300, "s_plus", V=t["V"], h=t["h"], W_O_heads=wo_heads)
-    # every key of KV group 5 (their column maxima merged over pass 2's splits) against the oracle
-    assert L.score_plan_info(wl.Hq, wl.Hkv, wl.N, wl.N, d, D=wl.D, q_pos0=0,
-                             mode=L.MODE_LSE | L.MODE_KVZIP_PLUS)[3] > 1
+    # every key of KV group 5 against the oracle (the merge over pass 2's splits
+    # is covered at a size that splits, in test_gpu_parity.py)
     g = 5
     wo_heads = np.stack([f64(t["W_O"][:, (g * G + i) * d:(g * G + i + 1) * d]) for i in range(G)])
     per = per_head_scores(f64(t["Q"][g * G:(g + 1) * G]), f64(t["K"][g]), 0, V=f64(t["V"][g]), h=f64(t["h"]),

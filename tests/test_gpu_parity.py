@@ -117,6 +117,12 @@ def test_channel_weights_and_rms(shape):
     keep[0] = False
     sc = L.unit_rms(K.to(DEV), 1, keep_bits=keep.to(torch.uint8).reshape(-1).to(DEV))
     np.testing.assert_allclose(sc.cpu().numpy(), O.unit_rms(f64(K), 1, keep.numpy()), rtol=TOL, atol=0)
+    # both channel quantities from one read of K: the same sums in the same order
+    wc2, sc2 = L.channel_stats(Q.to(DEV), K.to(DEV), keep.to(torch.uint8).reshape(-1).to(DEV))
+    assert torch.equal(wc2, wc) and torch.equal(sc2, sc)
+    wc3, sc3 = L.channel_stats(Q.to(DEV), K.to(DEV), None)
+    assert torch.equal(wc3, wc)
+    np.testing.assert_allclose(sc3.cpu().numpy(), O.unit_rms(f64(K), 1), rtol=TOL)
 
 
 def gpu_alloc(w, s, B, mask=L.WIDTHS_ALL):
