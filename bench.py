@@ -46,6 +46,12 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--overlap", type=int, default=1,
+                    help="full-model batch: 1 runs each layer's post-scoring chain beside the next layer's passes")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="full-model batch: run only this many layers (a reduced case, e.g. for a profiler)")
+    ap.add_argument("--seqs", type=int, default=None,
+                    help="full-model batch: run only this many sequences per layer (a reduced case)")
     ap.add_argument("--e2e-steps", type=int, default=2, help="end-to-end steps of the full-model batch")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle time for the CPU baseline")
     ap.add_argument("--soak-s", type=float, default=1.0, help="untimed replays before timing (clock samples)")
@@ -833,7 +839,9 @@ def full_model_config(wl):
     return {"workload": wl.name, "layers": wl.layers, "seqs": wl.seqs, "Hq": wl.Hq, "Hkv": wl.Hkv, "N": wl.N,
             "W": wl.W, "d": wl.d, "avg_bits": wl.avg_bits[0], "pools_per_step_per_gpu": wl.layers * wl.seqs,
             "pools_per_launch": wl.seqs, "tokens_per_step": wl.layers * wl.seqs * wl.N,
-            "l2": "inputs (38.7 GB) far larger than L2; no flush", "parallelism": "replicas"}
+            "l2": "inputs ({:.1f} GB) far larger than L2; no flush".format(
+                wl.layers * wl.seqs * (wl.Hq * wl.W + 2 * wl.Hkv * wl.N) * wl.d * 2 / 1e9),
+            "parallelism": "replicas"}
 
 
 def run_full_model(args):
@@ -857,6 +865,9 @@ def run_full_model(args):
     dist = init_group(world, "nccl")
     L.lib()
     wl = synth.WORKLOADS[FULL_MODEL]
+    reduced = args.layers is not None or args.seqs is not None
+    if reduced:   # a smaller slice of the batch (profiling); the line says so in its config
+        wl = wl.small(layers=args.layers or wl.layers, seqs=args.seqs or wl.seqs)
     layers, P = wl.layers, wl.seqs
     t_gen = time.perf_counter()
     inputs = full_model_inputs(wl, dev, layers)
@@ -865,10 +876,19 @@ def run_full_model(args):
     avg = wl.avg_bits[0]
     steps = [RdkvLayerStep(wl.Hq, wl.Hkv, wl.N, wl.W, wl.d, avg, device=dev, n_pools=P) for _ in range(2)]
     main = torch.cuda.current_stream()
+    # With overlap, layer l's post-scoring chain runs on a second stream while
+    # layer l+1's scoring passes run on the first (the two step objects take
+    # the layers in turn; a layer's passes wait until the chain of the layer
+    # two back, which used the same buffers, is done).
+    rest_stream = torch.cuda.Stream(device=dev)
+    scored = [torch.cuda.Event() for _ in range(2)]
+    rested = [torch.cuda.Event() for _ in range(2)]
 
     def one_step(evs=None):
         for l in range(layers):
             st, x = steps[l % 2], inputs[l]
+            if args.overlap and l >= 2:
+                main.wait_event(rested[l % 2])
             if evs is not None:
                 evs[l][0].record(main)
             st.pass1(x["Q"], x["K"], x["V"])
@@ -877,7 +897,16 @@ def run_full_model(args):
             st.pass2(x["Q"], x["K"], x["V"])
             if evs is not None:
                 evs[l][2].record(main)
-            st.rest(x["Q"], x["K"], x["V"])
+            if args.overlap:
+                scored[l % 2].record(main)
+                rest_stream.wait_event(scored[l % 2])
+                with torch.cuda.stream(rest_stream):
+                    st.rest(x["Q"], x["K"], x["V"], stream=rest_stream)
+                rested[l % 2].record(rest_stream)
+            else:
+                st.rest(x["Q"], x["K"], x["V"])
+        if args.overlap:
+            main.wait_stream(rest_stream)
 
     for _ in range(args.warmup):
         one_step()
@@ -910,7 +939,7 @@ def run_full_model(args):
     value = world * args.steps * tokens_per_step / total_s / 1e6
     p1 = statistics.fmean(e[l][0].elapsed_time(e[l][1]) for e in ev_pass for l in range(layers))
     p2 = statistics.fmean(e[l][1].elapsed_time(e[l][2]) for e in ev_pass for l in range(layers))
-    rest = statistics.fmean(step_ms) / layers - p1 - p2
+    rest = statistics.fmean(step_ms) / layers - p1 - p2   # with overlap: the part of the chain not hidden
 
     peak_tf, _, peak_kind = measured_peaks()
     peak_sus = sustained_peak()
@@ -932,8 +961,9 @@ def run_full_model(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": statistics.fmean(step_ms), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, drawn on the device)",
-        "config": full_model_config(wl),
-        "segments_ms_per_layer": {"pass1_lse": p1, "pass2_token_weights": p2, "rest": rest},
+        "config": dict(full_model_config(wl), **({"reduced": True} if reduced else {})),
+        "segments_ms_per_layer": {"pass1_lse": p1, "pass2_token_weights": p2, "rest": rest,
+                                  "overlap": bool(args.overlap)},
         "roofline": roofline,
         "gpu_launches": launches * args.steps,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],

@@ -85,6 +85,12 @@ int kvs_get_device_error(void* stream);
 #define KVS_DEBUG_WITHHOLD_LSE_ARRIVE 1u
 int kvs_debug_inject(uint32_t fault, uint64_t wait_limit_ns);
 
+/* Test hook; the papers have no counterpart.  y[i] = the library's FMA-pipe
+ * 2^x[i] (Cody-Waite reduction and a degree-3 minimax polynomial, relative
+ * error below 1e-4; 0 for x < -125), the routine that takes part of the
+ * softmax exponentials off the special-function unit.  x, y: device float [n]. */
+int kvs_debug_exp2(const float* x, float* y, int64_t n, void* stream);
+
 /* ---- importance scoring ------------------------------------------------ */
 #define KVS_MODE_LSE         1u  /* lse[Hq, W]  = ln sum_{t<=p_r} exp(s_{r,t})         [KVSculpt §2, LSE term] */
 #define KVS_MODE_RDKV_WT     2u  /* w_t[Hkv, N] = sum over the group's heads and window rows of a_{r,t}

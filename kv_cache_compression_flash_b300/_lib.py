@@ -36,6 +36,7 @@ SIGNATURES = {
     "kvs_version": (c_int, []),
     "kvs_get_device_error": (c_int, [c_void_p]),
     "kvs_debug_inject": (c_int, [c_uint32, ctypes.c_uint64]),
+    "kvs_debug_exp2": (c_int, [c_void_p, c_void_p, c_int64, c_void_p]),
     "kvs_score_workspace_size": (c_size_t, [c_int64] * 7 + [c_uint32]),
     "kvs_score_attention": (c_int, [c_void_p] * 5 + [c_int64] * 7 + [c_uint32] + [c_void_p] * 4 + [c_size_t, c_void_p]),
     "kvs_score_plan_info": (c_int, [c_int64] * 7 + [c_uint32, POINTER(c_int64)]),
@@ -160,6 +161,15 @@ DEBUG_WITHHOLD_LSE_ARRIVE = 1
 def debug_inject(fault=DEBUG_NONE, wait_limit_ns=0):
     """Test hook: plant a device fault in later launches and set the wait limit (0 = default)."""
     _check(lib().kvs_debug_inject(fault, wait_limit_ns), "kvs_debug_inject")
+
+
+def debug_exp2(x, *, stream=None):
+    """The library's FMA-pipe 2^x of a float32 CUDA tensor (test hook)."""
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise KvsError("x must be a contiguous float32 CUDA tensor")
+    y = torch.empty_like(x)
+    _check(lib().kvs_debug_exp2(_ptr(x), _ptr(y), x.numel(), _stream(stream)), "kvs_debug_exp2")
+    return y
 
 
 def device_error(stream=None) -> int:

@@ -42,6 +42,32 @@ __device__ __forceinline__ uint64_t wait_limit_ns() {
   return *reinterpret_cast<volatile unsigned long long*>(&g_wait_limit_ns);
 }
 
+// ---------------------------------------------------------------------------
+// 2^x on the FMA pipe, to take part of the softmax exponentials off the
+// special-function unit.  Cody and Waite's range reduction (1980): x = n + f
+// with n = round(x) and |f| <= 1/2; 2^f by the degree-3 polynomial of relative
+// minimax error on [-1/2, 1/2] (coefficients from a Remez exchange,
+// kv_cache_compression_flash_b300/exp2_fit.py: max relative error 7.5e-5); 2^n
+// by adding n to the exponent field.  x below -125 (and -inf) gives 0: such
+// terms are under 2^-125, nothing next to the sums they join.
+// ---------------------------------------------------------------------------
+constexpr float kExp2C0 = 0x1.fff692p-1f;
+constexpr float kExp2C1 = 0x1.62f31ap-1f;
+constexpr float kExp2C2 = 0x1.f0de1ap-3f;
+constexpr float kExp2C3 = 0x1.c3f76p-5f;
+
+__device__ __forceinline__ float ex2_fma(float x) {
+  const float xc = fmaxf(x, -127.f);
+  const float t = xc + 12582912.f;       // 1.5 * 2^23: the nearest integer lands in the low mantissa bits
+  const float f = xc - (t - 12582912.f);  // exact, |f| <= 1/2
+  float p = fmaf(kExp2C3, f, kExp2C2);
+  p = fmaf(p, f, kExp2C1);
+  p = fmaf(p, f, kExp2C0);
+  // (bits(t) << 23) mod 2^32 = n << 23: the exponent bits of t shift out
+  const float r = __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+  return x >= -125.f ? r : 0.f;  // keeps the result a normal float
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -225,24 +225,21 @@ int pack_dh(const uint16_t* X, int64_t n_pools, int64_t Hkv, int64_t N, int axis
     std::call_once(once, [] {
       err = set_cluster_attrs(channels_plan_kernel<64>);
       if (err == cudaSuccess) err = set_cluster_attrs(channels_plan_kernel<128>);
-      if (err == cudaSuccess) err = allow_smem(pack_channels_kernel<64>, chan_pack_smem<64>());
-      if (err == cudaSuccess) err = allow_smem(pack_channels_kernel<128>, chan_pack_smem<128>());
-      if (err == cudaSuccess) err = allow_smem(dequant_channels_kernel<64>, chan_dequant_smem<64>());
-      if (err == cudaSuccess) err = allow_smem(dequant_channels_kernel<128>, chan_dequant_smem<128>());
     });
     if (err != cudaSuccess) return KVS_ERR_CUDA;
     const int cl = static_cast<int>(std::min<int64_t>(Hkv, 16));
     KVS_CUDA_TRY(launch_cluster(channels_plan_kernel<DH>, dim3(static_cast<unsigned>(cl * n_pools)), cl, kPlanThreads,
                                 0, st, keep, static_cast<int>(N), hkv, bits, w.kept, w.n_kept, w.chan_base, sp,
                                 dequant ? 0 : 1));
+    constexpr int TG = chan_groups_per_cta<DH>();
     if (dequant) {
-      const dim3 grid(static_cast<unsigned>(cdiv(N, 64 * kChanTGd) + 1), gy);
-      KVS_CUDA_TRY(launch_k(dequant_channels_kernel<DH>, grid, dim3(kChanThreads), chan_dequant_smem<DH>(), st, 0, sp,
-                            static_cast<int>(N), bits, w.chan_base, w.kept, w.n_kept, out, hkv));
+      const dim3 grid(static_cast<unsigned>(cdiv(N, 64 * TG) + 1), gy);
+      KVS_CUDA_TRY(launch_k(dequant_channels_kernel<DH>, grid, dim3(kChanThreads), 0, st, 0, sp, static_cast<int>(N),
+                            bits, w.chan_base, w.kept, w.n_kept, out, hkv));
     } else {
-      const dim3 grid(static_cast<unsigned>(cdiv(cdiv(N, 64), kChanTG)), gy);
-      KVS_CUDA_TRY(launch_k(pack_channels_kernel<DH>, grid, dim3(kChanThreads), chan_pack_smem<DH>(), st, 0, X,
-                            static_cast<int>(N), bits, w.chan_base, w.kept, w.n_kept, sp, hkv));
+      const dim3 grid(static_cast<unsigned>(cdiv(cdiv(N, 64), TG)), gy);
+      KVS_CUDA_TRY(launch_k(pack_channels_kernel<DH>, grid, dim3(kChanThreads), 0, st, 0, X, static_cast<int>(N), bits,
+                            w.chan_base, w.kept, w.n_kept, sp, hkv));
     }
   }
   return KVS_OK;
@@ -339,6 +336,23 @@ int kvs_get_device_error(void* stream) {
   KVS_CUDA_TRY(cudaMemcpyFromSymbol(&v, kvs::g_device_error, sizeof(int)));
   KVS_CUDA_TRY(cudaMemcpyToSymbol(kvs::g_device_error, &zero, sizeof(int)));
   return v;
+}
+
+namespace {
+__global__ void debug_exp2_kernel(const float* __restrict__ x, float* __restrict__ y, const long long n) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    y[i] = ex2_fma(x[i]);
+}
+}  // namespace
+
+int kvs_debug_exp2(const float* x, float* y, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!x || !y))) return KVS_ERR_INVALID_ARG;
+  if (n == 0) return KVS_OK;
+  const int blocks = static_cast<int>(std::min<long long>(cdiv(n, 256), 1024));
+  KVS_CUDA_TRY(launch_k(debug_exp2_kernel, dim3(blocks), dim3(256), 0, as_stream(stream), 0, x, y,
+                        static_cast<long long>(n)));
+  return KVS_OK;
 }
 
 int kvs_debug_inject(uint32_t fault, uint64_t wait_limit_ns) {

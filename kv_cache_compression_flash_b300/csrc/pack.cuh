@@ -72,6 +72,53 @@ __device__ __forceinline__ int q_round(const float x, const float s, const float
   return round_div_even(x, s, r);
 }
 
+// round-half-even(x r) on the FMA pipe: adding 1.5 * 2^23 rounds |x r| < 2^22
+// to the nearest integer (ties to even), which lands in the low mantissa bits.
+// *near_half flags a product within 2^-14 of a half-integer, where x r may
+// round differently from x / s: q_round settles those exactly.
+__device__ __forceinline__ int q_round_fast(const float x, const float r, bool* near_half) {
+  const float t = __fmul_rn(x, r);
+  const float y = __fadd_rn(t, 12582912.f);
+  *near_half = fabsf(__fsub_rn(t, __fsub_rn(y, 12582912.f))) >= 0.49993896484375f;  // 1/2 - 2^-14
+  return __float_as_int(y) - 0x4B400000;
+}
+
+// the w-bit two's-complement code in the low bits of c, as a float (exact:
+// the integer is added to 1.5 * 2^23 in the mantissa, no conversion unit)
+__device__ __forceinline__ float code_to_float(const uint32_t c, const int w) {
+  const int q = static_cast<int>(c << (32 - w)) >> (32 - w);
+  return __fsub_rn(__int_as_float(0x4B400000 + q), 12582912.f);
+}
+
+// max of two packed bf16 pairs
+__device__ __forceinline__ uint32_t bf16x2_max(const uint32_t a, const uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// codes of 8 consecutive elements of a group: the w-bit codes at bits [w e, w e + w)
+__device__ __forceinline__ unsigned long long quantize_octet(const float (&x)[8], const int w, const float s,
+                                                             const float r) {
+  const unsigned long long cmask = (1ull << w) - 1ull;
+  unsigned long long packed = 0ull;
+  bool near = false;
+  int q[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    bool nh;
+    q[e] = q_round_fast(x[e], r, &nh);
+    near |= nh;
+  }
+  if (near) {  // an element within 2^-14 of a half-integer: the exact test (rare)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) q[e] = q_round(x[e], s, r);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) packed |= (static_cast<unsigned long long>(static_cast<uint32_t>(q[e])) & cmask) << (w * e);
+  return packed;
+}
+
 // Quantise this lane's 4 elements of a 64-element group (the half-warp holds
 // the group).  Returns the 4w code bits; *scale_bits gets the fp16 scale.
 __device__ __forceinline__ uint32_t quantize_lane4(const float (&x)[4], const int w, uint16_t* scale_bits,
@@ -350,13 +397,7 @@ __device__ __forceinline__ unsigned long long quantize_lane8(const float (&x)[8]
   *overflow = isinf(s);
   *scale_bits = __half_as_ushort(sh);
   unsigned long long packed = 0ull;
-  const unsigned long long cmask = (1ull << w) - 1ull;
-  if (s > 0.f && !isinf(s)) {
-    const float r = __frcp_rn(s);
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-      packed |= (static_cast<unsigned long long>(static_cast<uint32_t>(q_round(x[e], s, r))) & cmask) << (w * e);
-  }
+  if (s > 0.f && !isinf(s)) packed = quantize_octet(x, w, s, __frcp_rn(s));
   return packed;
 }
 
@@ -460,11 +501,7 @@ __device__ __forceinline__ void dequant_lane8(const uint8_t* group_base, const i
     packed = reinterpret_cast<const unsigned long long*>(group_base)[l8];
   const float s = __half2float(__ushort_as_half(*scale_ptr));
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int code = static_cast<int>((packed >> (w * e)) & ((1ull << w) - 1ull));
-    const int q = code >= (1 << (w - 1)) ? code - (1 << w) : code;
-    y[e] = static_cast<float>(q) * s;
-  }
+  for (int e = 0; e < 8; ++e) y[e] = code_to_float(static_cast<uint32_t>(packed >> (w * e)), w) * s;
 }
 
 // grid (chunks, pools): every row of one chunk, in unit order (width 0 -> zeros)
@@ -613,22 +650,35 @@ __global__ void __launch_bounds__(kPlanThreads, 1) channels_plan_kernel(
   }
 }
 
-// Channel kernels take kChanTG (pack) or kChanTGd (dequantise) consecutive
-// kept-token groups of one head per CTA, so each CTA moves tens of KB: the
-// kept rows are gathered into a shared-memory tile (16-byte loads, eight in
-// flight per thread) and the channels are read down its columns, eight lanes
-// per (channel, 64-token group) and eight tokens a lane.
-constexpr int kChanTG = 4;
-constexpr int kChanTGd = 2;
+// Channel kernels: a CTA takes the kept tokens of TG = 512 / DH consecutive
+// 64-token groups of one head; warp w takes group w / (DH / 64) and 64
+// channels, two per lane (one 4-byte word of a row), so every row load and
+// every row store of a warp is one contiguous 128-byte (256-byte) segment and
+// needs no shared-memory transpose.  A lane holds its two channels' 64 values
+// of the group in registers (64 loads in flight), takes each channel's
+// absolute maximum with packed bf16 maxima, and writes the group's codes
+// eight elements (w bytes) at a time.
 constexpr int kChanThreads = 256;
 
 template <int DH>
-__host__ __device__ constexpr size_t chan_pack_smem() { return static_cast<size_t>(64 * kChanTG) * (DH / 2 + 1) * 4; }
-template <int DH>
-__host__ __device__ constexpr size_t chan_dequant_smem() { return static_cast<size_t>(64 * kChanTGd) * (DH + 1) * 4; }
+__host__ __device__ constexpr int chan_groups_per_cta() { return 8 / (DH / 64); }
 
-// grid (ceil(ceil(N/64) / kChanTG), pools * Hkv): kept-token groups
-// [kChanTG jb, kChanTG jb + kChanTG) of head g for every channel
+// w bytes of codes at byte offset o*w of a group's block (width 16: the raw 8 bf16 values)
+__device__ __forceinline__ void store_octet(uint8_t* group_base, const int w, const int o, const unsigned long long packed,
+                                            const uint4 raw) {
+  switch (w) {
+    case 2: reinterpret_cast<uint16_t*>(group_base)[o] = static_cast<uint16_t>(packed); break;
+    case 4: reinterpret_cast<uint32_t*>(group_base)[o] = static_cast<uint32_t>(packed); break;
+    case 8: reinterpret_cast<unsigned long long*>(group_base)[o] = packed; break;
+    default: {  // 8-byte aligned streams: two 8-byte stores
+      uint2* p = reinterpret_cast<uint2*>(group_base) + 2 * o;
+      p[0] = make_uint2(raw.x, raw.y);
+      p[1] = make_uint2(raw.z, raw.w);
+    }
+  }
+}
+
+// grid (ceil(ceil(N/64) / TG), pools * Hkv)
 template <int DH>
 __global__ void __launch_bounds__(kChanThreads) pack_channels_kernel(const uint16_t* __restrict__ X, const int N,
                                                                      const uint8_t* __restrict__ bits,
@@ -638,88 +688,95 @@ __global__ void __launch_bounds__(kChanThreads) pack_channels_kernel(const uint1
                                                                      const int Hkv) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
-  constexpr int TOK = 64 * kChanTG;
-  constexpr int LDW = DH / 2 + 1;  // 32-bit words per tile row; odd, so column reads spread over the banks
-  extern __shared__ uint32_t ctile[];  // [TOK][LDW]: two bf16 channels a word
-  __shared__ int s_w[DH];
-  __shared__ long long s_base[DH];
-  __shared__ int s_tok[TOK];
+  constexpr int CB = DH / 64;                       // warps per group: 64 channels each
+  constexpr int TG = chan_groups_per_cta<DH>();
+  __shared__ int s_tok[64 * TG];
   const int jb = blockIdx.x, g = blockIdx.y;
   const long long pool = g / Hkv;
   const int n = n_kept[g];
-  const int k0 = jb * TOK;
+  const int k0 = jb * 64 * TG;
   if (k0 >= n) return;
-  const int rows = min(TOK, n - k0);
-  for (int c = threadIdx.x; c < DH; c += kChanThreads) {
-    const long long b = chan_base[static_cast<long long>(g) * DH + c];
-    s_w[c] = bits[static_cast<long long>(g) * DH + c];
-    s_base[c] = b >= 0 ? b + jb * kChanTG : -1;
-  }
-  for (int i = threadIdx.x; i < TOK; i += kChanThreads)
-    s_tok[i] = i < rows ? kept[static_cast<long long>(g) * N + k0 + i] : -1;
+  const int rows = min(64 * TG, n - k0);
+  for (int i = threadIdx.x; i < 64 * TG; i += kChanThreads)
+    s_tok[i] = i < rows ? kept[static_cast<long long>(g) * N + k0 + i] : 0;
   __syncthreads();
-  // gather the kept rows; rows past the kept ones read as zeros (padding of a short last group)
-  constexpr int kLoads = TOK * (DH / 8) / kChanThreads;
-  constexpr int kBatch = 8;
-  const uint16_t* Xg = X + static_cast<long long>(g) * N * DH;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int jg = warp / CB, r0 = jg * 64;
+  if (r0 >= rows) return;
+  const int nr = min(64, rows - r0);
+  const int c0 = (warp % CB) * 64 + 2 * lane;
+  const uint16_t* Xg = X + static_cast<long long>(g) * N * DH + c0;
+  uint32_t v[64];  // channels c0 (low half) and c0 + 1 (high half) of the group's tokens; zeros past the kept ones
 #pragma unroll
-  for (int b0 = 0; b0 < kLoads; b0 += kBatch) {
-    uint4 v[kBatch];
+  for (int e = 0; e < 64; ++e)
+    v[e] = e < nr ? __ldg(reinterpret_cast<const uint32_t*>(Xg + static_cast<long long>(s_tok[r0 + e]) * DH)) : 0u;
+  uint32_t amax = 0u;  // packed bf16 absolute maxima (non-negative bf16 order like their bit patterns)
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int e = (b0 + k) * kChanThreads + threadIdx.x;
-      const int i = e / (DH / 8), c8 = (e % (DH / 8)) * 8;
-      v[k] = i < rows ? __ldg(reinterpret_cast<const uint4*>(Xg + static_cast<long long>(s_tok[i]) * DH + c8))
-                      : make_uint4(0u, 0u, 0u, 0u);
-    }
+  for (int e = 0; e < 64; ++e) amax = bf16x2_max(amax, v[e] & 0x7FFF7FFFu);
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int e = (b0 + k) * kChanThreads + threadIdx.x;
-      const int i = e / (DH / 8), c8 = (e % (DH / 8)) * 8;
-      uint32_t* row = ctile + i * LDW + c8 / 2;
-      row[0] = v[k].x;
-      row[1] = v[k].y;
-      row[2] = v[k].z;
-      row[3] = v[k].w;
-    }
-  }
-  __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, sub = lane >> 3, l8 = lane & 7;
-  // pairs (channel, group): p = jg * DH + c; a warp takes 4 consecutive channels of one group
-  for (int p0 = warp * 4; p0 < DH * kChanTG; p0 += (kChanThreads / 32) * 4) {
-    const int p = p0 + sub;
-    const int c = p % DH, jg = p / DH;
-    const int w = s_w[c], s = width_slot(w);
-    const bool act = s >= 0 && s_base[c] >= 0 && jg * 64 < rows;
-    float x[8];
-    uint32_t hw[8];
+  for (int h = 0; h < 2; ++h) {
+    const int c = c0 + h;
+    const long long u = static_cast<long long>(g) * DH + c;
+    const int w = bits[u], s = width_slot(w);
+    const long long b = chan_base[u];
+    if (s < 0 || b < 0) continue;
+    const long long gg = pool * sp.cap_groups[s] + b + jb * TG + jg;
+    uint8_t* blk = sp.codes[s] + gg * (8 * w);
+    const int sh = 16 * h;
+    if (w == 16) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int r = jg * 64 + l8 * 8 + e;
-      hw[e] = (ctile[r * LDW + (c >> 1)] >> ((c & 1) * 16)) & 0xFFFFu;
-      x[e] = __uint_as_float(hw[e] << 16);
-    }
-    unsigned long long packed = 0ull;
-    uint16_t sb = 0;
-    bool ovf = false;
-    if (__any_sync(0xFFFFFFFFu, act && w != 16)) packed = quantize_lane8(x, (act && w != 16) ? w : 8, &sb, &ovf);
-    if (act) {
-      const long long gg = pool * sp.cap_groups[s] + s_base[c] + jg;
-      if (w != 16 && l8 == 0) {
-        sp.scales[s][gg] = sb;
-        if (ovf) record_error(KVS_ERR_RANGE);
+      for (int o = 0; o < 8; ++o) {
+        uint32_t hw[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) hw[e] = (v[8 * o + e] >> sh) & 0xFFFFu;
+        store_octet(blk, 16, o, 0ull, make_uint4(hw[0] | (hw[1] << 16), hw[2] | (hw[3] << 16), hw[4] | (hw[5] << 16),
+                                                 hw[6] | (hw[7] << 16)));
       }
-      const uint4 raw = make_uint4(hw[0] | (hw[1] << 16), hw[2] | (hw[3] << 16), hw[4] | (hw[5] << 16),
-                                   hw[6] | (hw[7] << 16));
-      store_lane8(sp.codes[s] + gg * (8 * w), w, l8, packed, raw);
+      continue;
+    }
+    const float a = __uint_as_float(((amax >> sh) & 0xFFFFu) << 16);
+    const float qmax = static_cast<float>((1 << (w - 1)) - 1);
+    const __half shalf = __float2half_ru(__fdiv_rn(a, qmax));
+    const float sc = __half2float(shalf);
+    sp.scales[s][gg] = __half_as_ushort(shalf);
+    if (isinf(sc)) record_error(KVS_ERR_RANGE);
+    const bool live = sc > 0.f && !isinf(sc);
+    const float r = live ? __frcp_rn(sc) : 0.f;
+#pragma unroll
+    for (int o = 0; o < 8; ++o) {
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(((v[8 * o + e] >> sh) & 0xFFFFu) << 16);
+      const unsigned long long packed = live ? quantize_octet(x, w, sc, r) : 0ull;
+      store_octet(blk, w, o, packed, make_uint4(0u, 0u, 0u, 0u));
     }
   }
 }
 
-// grid (ceil(N / (64 kChanTGd)) + 1, pools * Hkv).  CTA jb below the head's
-// count of kept blocks decodes kept-token groups [kChanTGd jb, ..) of every
-// channel into a shared-memory tile and writes those tokens' rows; the CTAs
-// after those zero the head's dropped tokens, 64 kChanTGd per CTA.
+// 8 decoded values of one channel's octet o of a group
+__device__ __forceinline__ void dequant_octet(const uint8_t* group_base, const int w, const int o, const float s,
+                                              float (&y)[8]) {
+  if (w == 16) {
+    const uint2* p = reinterpret_cast<const uint2*>(group_base) + 2 * o;
+    const uint2 a = p[0], b = p[1];
+    bf16x8(make_uint4(a.x, a.y, b.x, b.y), y);
+    return;
+  }
+  unsigned long long packed;
+  if (w == 2)
+    packed = reinterpret_cast<const uint16_t*>(group_base)[o];
+  else if (w == 4)
+    packed = reinterpret_cast<const uint32_t*>(group_base)[o];
+  else
+    packed = reinterpret_cast<const unsigned long long*>(group_base)[o];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) y[e] = code_to_float(static_cast<uint32_t>(packed >> (w * e)), w) * s;
+}
+
+// grid (ceil(N / (64 TG)) + 1, pools * Hkv).  CTA jb below the head's count of
+// kept blocks decodes kept-token groups [TG jb, ..) of every channel and
+// writes those tokens' rows (a lane's two channels: one 8-byte store per
+// token); the CTAs after those zero the head's dropped tokens, 64 TG per CTA.
 template <int DH>
 __global__ void __launch_bounds__(kChanThreads) dequant_channels_kernel(const StreamPtrs sp, const int N,
                                                                         const uint8_t* __restrict__ bits,
@@ -729,11 +786,10 @@ __global__ void __launch_bounds__(kChanThreads) dequant_channels_kernel(const St
                                                                         float* __restrict__ out, const int Hkv) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
-  constexpr int TOK = 64 * kChanTGd;
-  constexpr int LD = DH + 1;  // odd: column writes spread over the banks
-  extern __shared__ float ftile[];  // [TOK][LD]
-  __shared__ int s_w[DH];
-  __shared__ long long s_base[DH];
+  constexpr int CB = DH / 64;
+  constexpr int TG = chan_groups_per_cta<DH>();
+  constexpr int TOK = 64 * TG;
+  __shared__ int s_tok[TOK];
   const int jb = blockIdx.x, g = blockIdx.y;
   const long long pool = g / Hkv;
   const int n = n_kept[g];
@@ -752,33 +808,43 @@ __global__ void __launch_bounds__(kChanThreads) dequant_channels_kernel(const St
   }
   const int k0 = jb * TOK;
   const int rows = min(TOK, n - k0);
-  for (int c = threadIdx.x; c < DH; c += kChanThreads) {
-    const long long b = chan_base[static_cast<long long>(g) * DH + c];
-    s_w[c] = bits[static_cast<long long>(g) * DH + c];
-    s_base[c] = b >= 0 ? b + jb * kChanTGd : -1;
-  }
+  for (int i = threadIdx.x; i < TOK; i += kChanThreads) s_tok[i] = i < rows ? kg[k0 + i] : 0;
   __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, sub = lane >> 3, l8 = lane & 7;
-  for (int p0 = warp * 4; p0 < DH * kChanTGd; p0 += (kChanThreads / 32) * 4) {
-    const int p = p0 + sub;
-    const int c = p % DH, jg = p / DH;
-    if (jg * 64 >= rows) continue;
-    float y[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int jg = warp / CB, r0 = jg * 64;
+  if (r0 >= rows) return;
+  const int nr = min(64, rows - r0);
+  const int c0 = (warp % CB) * 64 + 2 * lane;
+  const uint8_t* blk[2];
+  int wd[2];
+  float sc[2];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) y[e] = 0.f;
-    const int w = s_w[c], s = width_slot(w);
-    if (s >= 0 && s_base[c] >= 0) {
-      const long long gg = pool * sp.cap_groups[s] + s_base[c] + jg;
-      dequant_lane8(sp.codes[s] + gg * (8 * w), w, l8, sp.scales[s] + gg, y);
+  for (int h = 0; h < 2; ++h) {
+    const long long u = static_cast<long long>(g) * DH + c0 + h;
+    const int w = bits[u], s = width_slot(w);
+    const long long b = chan_base[u];
+    wd[h] = (s >= 0 && b >= 0) ? w : 0;
+    blk[h] = nullptr;
+    sc[h] = 0.f;
+    if (wd[h]) {
+      const long long gg = pool * sp.cap_groups[s] + b + jb * TG + jg;
+      blk[h] = sp.codes[s] + gg * (8 * w);
+      sc[h] = w == 16 ? 1.f : __half2float(__ushort_as_half(sp.scales[s][gg]));
     }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) ftile[(jg * 64 + l8 * 8 + e) * LD + c] = y[e];
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < rows * (DH / 4); e += kChanThreads) {
-    const int i = e / (DH / 4), c4 = (e % (DH / 4)) * 4;
-    const float* t = ftile + i * LD + c4;
-    *reinterpret_cast<float4*>(og + static_cast<long long>(kg[k0 + i]) * DH + c4) = make_float4(t[0], t[1], t[2], t[3]);
+  float* orow = og + c0;
+#pragma unroll 2
+  for (int o = 0; o < 8; ++o) {
+    float y0[8], y1[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y0[e] = y1[e] = 0.f;
+    if (wd[0]) dequant_octet(blk[0], wd[0], o, sc[0], y0);
+    if (wd[1]) dequant_octet(blk[1], wd[1], o, sc[1], y1);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int i = 8 * o + e;
+      if (i < nr) *reinterpret_cast<float2*>(orow + static_cast<long long>(s_tok[r0 + i]) * DH) = make_float2(y0[e], y1[e]);
+    }
   }
 }
 
