@@ -46,8 +46,9 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--overlap", type=int, default=1,
-                    help="full-model batch: 1 runs each layer's post-scoring chain beside the next layer's passes")
+    ap.add_argument("--overlap", type=int, default=0,
+                    help="full-model batch: 1 runs each layer's post-scoring chain beside the next layer's passes "
+                         "(measured no faster: the passes slow down by what the chain saves)")
     ap.add_argument("--layers", type=int, default=None,
                     help="full-model batch: run only this many layers (a reduced case, e.g. for a profiler)")
     ap.add_argument("--seqs", type=int, default=None,

@@ -269,6 +269,8 @@ typedef struct kvs_stream_set {
     int64_t*  counts;
 } kvs_stream_set;
 
+/* Every codes[i] pointer must be 16-byte aligned (KVS_ERR_INVALID_ARG otherwise). */
+
 /* Host-only: capacities that always suffice for an allocation of at most
  * budget_bits (a unit of width w costs w bits, so at most budget/w units of
  * that width exist).  cap_units, cap_groups: host int64[4]. */

@@ -225,6 +225,8 @@ int pack_dh(const uint16_t* X, int64_t n_pools, int64_t Hkv, int64_t N, int axis
     std::call_once(once, [] {
       err = set_cluster_attrs(channels_plan_kernel<64>);
       if (err == cudaSuccess) err = set_cluster_attrs(channels_plan_kernel<128>);
+      if (err == cudaSuccess) err = allow_smem(pack_channels_kernel<64>, chan_pack_smem<64>());
+      if (err == cudaSuccess) err = allow_smem(pack_channels_kernel<128>, chan_pack_smem<128>());
     });
     if (err != cudaSuccess) return KVS_ERR_CUDA;
     const int cl = static_cast<int>(std::min<int64_t>(Hkv, 16));
@@ -238,8 +240,8 @@ int pack_dh(const uint16_t* X, int64_t n_pools, int64_t Hkv, int64_t N, int axis
                             bits, w.chan_base, w.kept, w.n_kept, out, hkv));
     } else {
       const dim3 grid(static_cast<unsigned>(cdiv(cdiv(N, 64), TG)), gy);
-      KVS_CUDA_TRY(launch_k(pack_channels_kernel<DH>, grid, dim3(kChanThreads), 0, st, 0, X, static_cast<int>(N), bits,
-                            w.chan_base, w.kept, w.n_kept, sp, hkv));
+      KVS_CUDA_TRY(launch_k(pack_channels_kernel<DH>, grid, dim3(kChanThreads), chan_pack_smem<DH>(), st, 0, X,
+                            static_cast<int>(N), bits, w.chan_base, w.kept, w.n_kept, sp, hkv));
     }
   }
   return KVS_OK;
@@ -254,6 +256,8 @@ int pack_common(const uint16_t* X, int64_t n_pools, int64_t Hkv, int64_t N, int6
   if (!dequant && !s->counts) return KVS_ERR_INVALID_ARG;
   if (X && !aligned16(X)) return KVS_ERR_INVALID_ARG;
   if (out && !aligned16(out)) return KVS_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i)  // the code blocks are written and read 16 bytes at a time
+    if (!aligned16(s->codes[i])) return KVS_ERR_INVALID_ARG;
   PackWs w;
   if (carve_pack(n_pools, Hkv, N, d, axis, ws, ws_bytes, &w) > ws_bytes || !ws) return KVS_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KVS_ERR_WORKSPACE;

@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kNormThreads) row_rms_kernel(const uint16_t* _
 //   mode kColMaskedRms:     out[g][c] = sqrt(sum_A over kept rows / kept), 0 if none
 // grid (CL, groups), cluster (CL, 1, 1), kColThreads threads.
 // ---------------------------------------------------------------------------
-constexpr int kColThreads = 512;
+constexpr int kColThreads = 256;  // two CTAs per SM: more loads in flight than one larger CTA
 constexpr int kColChannelWeight = 0;
 constexpr int kColMaskedRms = 1;
 constexpr int kColChannelStats = 2;  // both from one read of the keys (A = K with keep, B = Q):
@@ -130,7 +130,7 @@ __device__ __forceinline__ void colsq_block_reduce(const float (&acc)[8], float*
 }
 
 template <int DH, bool STATS>
-__global__ void __launch_bounds__(kColThreads, 1) colsq_cluster_kernel(
+__global__ void __launch_bounds__(kColThreads, 2) colsq_cluster_kernel(
     const uint16_t* __restrict__ A, const int rows_a, const uint8_t* __restrict__ keep_a,
     const uint16_t* __restrict__ B, const int rows_b, const int mode, const float scale, float* __restrict__ out,
     float* __restrict__ out2) {

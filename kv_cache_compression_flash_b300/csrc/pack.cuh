@@ -72,17 +72,6 @@ __device__ __forceinline__ int q_round(const float x, const float s, const float
   return round_div_even(x, s, r);
 }
 
-// round-half-even(x r) on the FMA pipe: adding 1.5 * 2^23 rounds |x r| < 2^22
-// to the nearest integer (ties to even), which lands in the low mantissa bits.
-// *near_half flags a product within 2^-14 of a half-integer, where x r may
-// round differently from x / s: q_round settles those exactly.
-__device__ __forceinline__ int q_round_fast(const float x, const float r, bool* near_half) {
-  const float t = __fmul_rn(x, r);
-  const float y = __fadd_rn(t, 12582912.f);
-  *near_half = fabsf(__fsub_rn(t, __fsub_rn(y, 12582912.f))) >= 0.49993896484375f;  // 1/2 - 2^-14
-  return __float_as_int(y) - 0x4B400000;
-}
-
 // the w-bit two's-complement code in the low bits of c, as a float (exact:
 // the integer is added to 1.5 * 2^23 in the mantissa, no conversion unit)
 __device__ __forceinline__ float code_to_float(const uint32_t c, const int w) {
@@ -97,26 +86,90 @@ __device__ __forceinline__ uint32_t bf16x2_max(const uint32_t a, const uint32_t 
   return d;
 }
 
-// codes of 8 consecutive elements of a group: the w-bit codes at bits [w e, w e + w)
-__device__ __forceinline__ unsigned long long quantize_octet(const float (&x)[8], const int w, const float s,
-                                                             const float r) {
-  const unsigned long long cmask = (1ull << w) - 1ull;
-  unsigned long long packed = 0ull;
-  bool near = false;
-  int q[8];
+// Round-half-even of t = x r on the FMA pipe, two elements per instruction:
+// adding 1.5 * 2^23 rounds |t| < 2^22 to the nearest integer (ties to even),
+// which lands in the low mantissa bits, so the low w bits of y's pattern are
+// the w-bit two's-complement code.  d = t - (y - 1.5 * 2^23) is exact; an
+// element with |d| within 2^-14 of 1/2 may round differently from x / s, and
+// q_round settles those exactly (rare).
+constexpr float kRoundMagic = 12582912.f;                             // 1.5 * 2^23
+constexpr float kNearHalfSq = 0.49993896484375f * 0.49993896484375f;  // (1/2 - 2^-14)^2
+
+// the low w bits (w <= 8) of y[0..7]'s patterns packed at bits [w e, w e + w)
+__device__ __forceinline__ unsigned long long pack_codes8(const uint32_t (&yb)[8], const int w) {
+  const uint32_t cmask = (1u << w) - 1u;
+  uint32_t lo = 0u, hi = 0u;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    bool nh;
-    q[e] = q_round_fast(x[e], r, &nh);
-    near |= nh;
+    const int sh = w * e;
+    const uint32_t cb = yb[e] & cmask;
+    if (sh < 32)
+      lo |= cb << sh;
+    else
+      hi |= cb << (sh - 32);
   }
-  if (near) {  // an element within 2^-14 of a half-integer: the exact test (rare)
+  return static_cast<unsigned long long>(lo) | (static_cast<unsigned long long>(hi) << 32);
+}
+
+// codes of 8 consecutive elements of one group (one scale): x[e] as 4 packed pairs
+__device__ __forceinline__ unsigned long long quantize_octet(const float (&x)[8], const int w, const float s,
+                                                             const float r) {
+  const unsigned long long r2 = f2_pack(r, r), m2 = f2_pack(kRoundMagic, kRoundMagic),
+                           nm2 = f2_pack(-kRoundMagic, -kRoundMagic), neg1 = f2_pack(-1.f, -1.f);
+  uint32_t yb[8];
+  float dd[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) q[e] = q_round(x[e], s, r);
+  for (int k = 0; k < 4; ++k) {
+    const unsigned long long t = f2_mul(f2_pack(x[2 * k], x[2 * k + 1]), r2);
+    const unsigned long long y = f2_add(t, m2);
+    const unsigned long long d = f2_fma(f2_add(y, nm2), neg1, t);
+    float y0, y1;
+    f2_unpack(y, &y0, &y1);
+    yb[2 * k] = __float_as_uint(y0);
+    yb[2 * k + 1] = __float_as_uint(y1);
+    f2_unpack(f2_mul(d, d), &dd[2 * k], &dd[2 * k + 1]);
   }
+  if (fmax3(fmax3(dd[0], dd[1], dd[2]), fmax3(dd[3], dd[4], dd[5]), fmaxf(dd[6], dd[7])) >= kNearHalfSq) {
 #pragma unroll
-  for (int e = 0; e < 8; ++e) packed |= (static_cast<unsigned long long>(static_cast<uint32_t>(q[e])) & cmask) << (w * e);
-  return packed;
+    for (int e = 0; e < 8; ++e) yb[e] = static_cast<uint32_t>(q_round(x[e], s, r));  // the exact test
+  }
+  return pack_codes8(yb, w);
+}
+
+// The same for one octet of TWO channels at once (a lane's channel pair of a
+// K group): v[e] holds element e of channel 0 in its low bf16 half and of
+// channel 1 in its high half; each channel has its own width, scale and
+// reciprocal.  Results: *c0, *c1.
+__device__ __forceinline__ void quantize_octet_pair(const uint32_t (&v)[8], const int w0, const int w1, const float s0,
+                                                    const float s1, const float r0, const float r1,
+                                                    unsigned long long* c0, unsigned long long* c1) {
+  const unsigned long long r2 = f2_pack(r0, r1), m2 = f2_pack(kRoundMagic, kRoundMagic),
+                           nm2 = f2_pack(-kRoundMagic, -kRoundMagic), neg1 = f2_pack(-1.f, -1.f);
+  uint32_t ya[8], yb[8];
+  float da[8], db[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const unsigned long long t = f2_mul(f2_pack(__uint_as_float(v[e] << 16), __uint_as_float(v[e] & 0xFFFF0000u)), r2);
+    const unsigned long long y = f2_add(t, m2);
+    const unsigned long long d = f2_fma(f2_add(y, nm2), neg1, t);
+    float y0, y1;
+    f2_unpack(y, &y0, &y1);
+    ya[e] = __float_as_uint(y0);
+    yb[e] = __float_as_uint(y1);
+    f2_unpack(f2_mul(d, d), &da[e], &db[e]);
+  }
+  const float ma = fmax3(fmax3(da[0], da[1], da[2]), fmax3(da[3], da[4], da[5]), fmaxf(da[6], da[7]));
+  const float mb = fmax3(fmax3(db[0], db[1], db[2]), fmax3(db[3], db[4], db[5]), fmaxf(db[6], db[7]));
+  if (ma >= kNearHalfSq) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ya[e] = static_cast<uint32_t>(q_round(__uint_as_float(v[e] << 16), s0, r0));
+  }
+  if (mb >= kNearHalfSq) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) yb[e] = static_cast<uint32_t>(q_round(__uint_as_float(v[e] & 0xFFFF0000u), s1, r1));
+  }
+  *c0 = pack_codes8(ya, w0 <= 8 ? w0 : 8);
+  *c1 = pack_codes8(yb, w1 <= 8 ? w1 : 8);
 }
 
 // Quantise this lane's 4 elements of a 64-element group (the half-warp holds
@@ -678,7 +731,13 @@ __device__ __forceinline__ void store_octet(uint8_t* group_base, const int w, co
   }
 }
 
-// grid (ceil(ceil(N/64) / TG), pools * Hkv)
+// grid (ceil(ceil(N/64) / TG), pools * Hkv).  The codes of a warp's 64
+// channel blocks are staged in shared memory and then written block by block,
+// eight lanes per block (16 bytes a lane), so each store instruction writes
+// four contiguous blocks instead of 32 scattered pieces.
+template <int DH>
+__host__ __device__ constexpr size_t chan_pack_smem() { return static_cast<size_t>(kChanThreads / 32) * 64 * 128; }
+
 template <int DH>
 __global__ void __launch_bounds__(kChanThreads) pack_channels_kernel(const uint16_t* __restrict__ X, const int N,
                                                                      const uint8_t* __restrict__ bits,
@@ -690,7 +749,10 @@ __global__ void __launch_bounds__(kChanThreads) pack_channels_kernel(const uint1
   pdl_trigger();
   constexpr int CB = DH / 64;                       // warps per group: 64 channels each
   constexpr int TG = chan_groups_per_cta<DH>();
+  extern __shared__ __align__(16) uint8_t cstage[];  // per warp: 64 channel blocks of up to 128 bytes
   __shared__ int s_tok[64 * TG];
+  __shared__ uint8_t* s_dst[kChanThreads / 32][64];
+  __shared__ int s_wd[kChanThreads / 32][64];
   const int jb = blockIdx.x, g = blockIdx.y;
   const long long pool = g / Hkv;
   const int n = n_kept[g];
@@ -710,46 +772,63 @@ __global__ void __launch_bounds__(kChanThreads) pack_channels_kernel(const uint1
 #pragma unroll
   for (int e = 0; e < 64; ++e)
     v[e] = e < nr ? __ldg(reinterpret_cast<const uint32_t*>(Xg + static_cast<long long>(s_tok[r0 + e]) * DH)) : 0u;
-  uint32_t amax = 0u;  // packed bf16 absolute maxima (non-negative bf16 order like their bit patterns)
+  uint32_t amax = 0u;
 #pragma unroll
   for (int e = 0; e < 64; ++e) amax = bf16x2_max(amax, v[e] & 0x7FFF7FFFu);
+  uint8_t* stage = cstage + warp * (64 * 128);
+  // the two channels' widths, destinations and scales
+  int wd[2];
+  float sc[2], rc[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const int c = c0 + h;
-    const long long u = static_cast<long long>(g) * DH + c;
+    const int cl = 2 * lane + h;  // the channel's slot in the warp's stage
+    const long long u = static_cast<long long>(g) * DH + c0 + h;
     const int w = bits[u], s = width_slot(w);
     const long long b = chan_base[u];
-    if (s < 0 || b < 0) continue;
+    wd[h] = (s >= 0 && b >= 0) ? w : 0;
+    s_wd[warp][cl] = wd[h];
+    sc[h] = 0.f;
+    rc[h] = 0.f;
+    if (!wd[h]) continue;
     const long long gg = pool * sp.cap_groups[s] + b + jb * TG + jg;
-    uint8_t* blk = sp.codes[s] + gg * (8 * w);
-    const int sh = 16 * h;
-    if (w == 16) {
-#pragma unroll
-      for (int o = 0; o < 8; ++o) {
-        uint32_t hw[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) hw[e] = (v[8 * o + e] >> sh) & 0xFFFFu;
-        store_octet(blk, 16, o, 0ull, make_uint4(hw[0] | (hw[1] << 16), hw[2] | (hw[3] << 16), hw[4] | (hw[5] << 16),
-                                                 hw[6] | (hw[7] << 16)));
-      }
-      continue;
-    }
-    const float a = __uint_as_float(((amax >> sh) & 0xFFFFu) << 16);
+    s_dst[warp][cl] = sp.codes[s] + gg * (8 * w);
+    if (w == 16) continue;
+    const float a = __uint_as_float(((amax >> (16 * h)) & 0xFFFFu) << 16);
     const float qmax = static_cast<float>((1 << (w - 1)) - 1);
     const __half shalf = __float2half_ru(__fdiv_rn(a, qmax));
-    const float sc = __half2float(shalf);
+    sc[h] = __half2float(shalf);
     sp.scales[s][gg] = __half_as_ushort(shalf);
-    if (isinf(sc)) record_error(KVS_ERR_RANGE);
-    const bool live = sc > 0.f && !isinf(sc);
-    const float r = live ? __frcp_rn(sc) : 0.f;
+    if (isinf(sc[h])) record_error(KVS_ERR_RANGE);
+    if (sc[h] > 0.f && !isinf(sc[h])) rc[h] = __frcp_rn(sc[h]);
+  }
+  uint8_t* blk0 = stage + (2 * lane) * 128;
+  uint8_t* blk1 = blk0 + 128;
 #pragma unroll
-    for (int o = 0; o < 8; ++o) {
-      float x[8];
+  for (int o = 0; o < 8; ++o) {
+    uint32_t vo[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(((v[8 * o + e] >> sh) & 0xFFFFu) << 16);
-      const unsigned long long packed = live ? quantize_octet(x, w, sc, r) : 0ull;
-      store_octet(blk, w, o, packed, make_uint4(0u, 0u, 0u, 0u));
-    }
+    for (int e = 0; e < 8; ++e) vo[e] = v[8 * o + e];
+    unsigned long long q0 = 0ull, q1 = 0ull;
+    if (__any_sync(0xFFFFFFFFu, rc[0] != 0.f || rc[1] != 0.f))
+      quantize_octet_pair(vo, wd[0], wd[1], sc[0], sc[1], rc[0], rc[1], &q0, &q1);
+    if (rc[0] == 0.f) q0 = 0ull;  // an all-zero group (or width 16 / 0: not used)
+    if (rc[1] == 0.f) q1 = 0ull;
+    const uint4 raw0 = make_uint4((vo[0] & 0xFFFFu) | (vo[1] << 16), (vo[2] & 0xFFFFu) | (vo[3] << 16),
+                                  (vo[4] & 0xFFFFu) | (vo[5] << 16), (vo[6] & 0xFFFFu) | (vo[7] << 16));
+    const uint4 raw1 = make_uint4((vo[0] >> 16) | (vo[1] & 0xFFFF0000u), (vo[2] >> 16) | (vo[3] & 0xFFFF0000u),
+                                  (vo[4] >> 16) | (vo[5] & 0xFFFF0000u), (vo[6] >> 16) | (vo[7] & 0xFFFF0000u));
+    if (wd[0]) store_octet(blk0, wd[0], o, q0, raw0);
+    if (wd[1]) store_octet(blk1, wd[1], o, q1, raw1);
+  }
+  __syncwarp();
+  // the staged blocks, four channels per step, eight lanes per block
+  const int sub = lane >> 3, l8 = lane & 7;
+#pragma unroll 4
+  for (int c4 = 0; c4 < 64; c4 += 4) {
+    const int cl = c4 + sub;
+    const int w = s_wd[warp][cl];
+    if (2 * l8 < w)  // a block is 8w bytes: w/2 chunks of 16
+      *reinterpret_cast<uint4*>(s_dst[warp][cl] + 16 * l8) = *reinterpret_cast<const uint4*>(stage + cl * 128 + 16 * l8);
   }
 }
 
