@@ -112,7 +112,8 @@ size_t kvs_score_workspace_size(int64_t Hq, int64_t Hkv, int64_t W, int64_t N, i
  *             KVS_MODE_KVZIP / KVS_MODE_KVZIP_PLUS; with KVS_MODE_LSE_GIVEN the
  *             lse buffer is read instead of written.
  *   Q, K    : bf16, required.  V, h, W_O: bf16, required for KVZIP_PLUS only
- *             (D = hidden size, ignored otherwise).
+ *             (D = hidden size, ignored otherwise).  Every one of them
+ *             16-byte aligned.
  *   lse     : float [Hq, W], natural log, required.
  *   w_t     : float [Hkv, N], required with RDKV_WT, else may be NULL.
  *   s_plus  : float [Hkv, N], required with KVZIP or KVZIP_PLUS.  Keys no

@@ -54,7 +54,11 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// Rows t of head g are X + g * head_stride + t * ld (ld = 128 and head_stride
+// = N * 128 for a [heads, N, 128] cache; for the output projection W_O [D,
+// Hq * 128], head h's column slice has ld = Hq * 128 and head_stride = 128).
 __global__ void __launch_bounds__(kGramThreads) gram_partial_kernel(const uint16_t* __restrict__ X, int N,
+                                                                    const long long ld, const long long head_stride,
                                                                     const uint8_t* __restrict__ keep,
                                                                     int tokens_per_cta, float* __restrict__ part) {
   extern __shared__ uint8_t gsm_raw[];
@@ -86,7 +90,7 @@ __global__ void __launch_bounds__(kGramThreads) gram_partial_kernel(const uint16
   volatile int* abort_flag = &S.abort_flag;
   const uint32_t sbase = smem_u32(base);
   const int to = tid >> 4, co = tid & 15;          // this thread's 8 x 8 block: tokens 8*to.., channels 8*co..
-  const uint16_t* Xg = X + static_cast<long long>(g) * N * kGramD;
+  const uint16_t* Xg = X + static_cast<long long>(g) * head_stride;
   const uint8_t* kg = keep ? keep + static_cast<long long>(g) * N : nullptr;
 
   // this thread's 8 rows of tile i (16 bytes each); zeros past the range and for dropped tokens
@@ -96,7 +100,7 @@ __global__ void __launch_bounds__(kGramThreads) gram_partial_kernel(const uint16
     for (int r = 0; r < 8; ++r) {
       const long long t = t0 + r;
       const bool live = t < t_hi && (!kg || kg[t] != 0);
-      row[r] = live ? __ldg(reinterpret_cast<const uint4*>(Xg + t * kGramD + 8 * co)) : make_uint4(0u, 0u, 0u, 0u);
+      row[r] = live ? __ldg(reinterpret_cast<const uint4*>(Xg + t * ld + 8 * co)) : make_uint4(0u, 0u, 0u, 0u);
     }
   };
   uint4 nxt[8];

@@ -407,7 +407,7 @@ int kvs_score_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
   if (pl.want_wt && !w_t) return KVS_ERR_INVALID_ARG;
   if (pl.want_max && !s_plus) return KVS_ERR_INVALID_ARG;
   if (pl.want_plus && (!V || !h || !W_O)) return KVS_ERR_INVALID_ARG;
-  if (!aligned16(Q) || !aligned16(K) || (pl.want_plus && (!aligned16(V) || !aligned16(h))))
+  if (!aligned16(Q) || !aligned16(K) || (pl.want_plus && (!aligned16(V) || !aligned16(h) || !aligned16(W_O))))
     return KVS_ERR_INVALID_ARG;
   ScoreWs w;
   if (carve_score(pl, workspace, workspace_bytes, &w) > workspace_bytes || !workspace) return KVS_ERR_WORKSPACE;
@@ -878,7 +878,8 @@ int kvs_gram(const uint16_t* X, int64_t Hkv, int64_t N, int64_t d, const uint8_t
   KVS_CUDA_TRY(allow_smem(gram_partial_kernel, kGramSmem));
   float* part = static_cast<float*>(workspace);
   KVS_CUDA_TRY(launch_k(gram_partial_kernel, dim3(static_cast<unsigned>(ns), static_cast<unsigned>(Hkv)),
-                        dim3(kGramThreads), kGramSmem, st, 0, X, static_cast<int>(N), keep_bits, per, part));
+                        dim3(kGramThreads), kGramSmem, st, 0, X, static_cast<int>(N), static_cast<long long>(kGramD),
+                        static_cast<long long>(N) * kGramD, keep_bits, per, part));
   const long long per_split = Hkv * kGramD * kGramD;
   KVS_CUDA_TRY(launch_k(gram_reduce_kernel, dim3(static_cast<unsigned>(cdiv(per_split, 256))), dim3(256), 0, st, 0,
                         static_cast<const float*>(part), ns, per_split, accumulate ? 1 : 0, G));

@@ -32,6 +32,8 @@
 // a fixed order by small finalize kernels, so results are deterministic.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 namespace kvs {
@@ -158,14 +160,19 @@ __device__ __forceinline__ void lse_chunk(uint32_t (&r)[32], const int t0, const
 // 4-7 take row tiles 0 and 1, one tile row (all 128 columns) per thread.
 // Warp 16 issues TMA, warp 17 the MMAs.
 struct LseItem {
-  int pb0, g, hc, gh, kt0, kt1;
+  int pb0, g, hc, gh, kt0, kt1, split;
   bool two;
 };
 
+// it = split * (pairs * heads) + jy: the split index varies slowest, so the
+// persistent CTAs' strided item sequences do not line up with the short last
+// chunks
 __device__ __forceinline__ bool lse_item(const ScoreGeom& geo, const int kt_chunk, const int n_split, const int it,
                                          LseItem* x) {
   const int n_pp = (geo.n_pb + 1) / 2;
-  const int jy = it / n_split, split = it % n_split;
+  const int n_jy = n_pp * geo.Hkv * geo.n_hc;
+  const int jy = it % n_jy, split = it / n_jy;
+  x->split = split;
   const int pp = n_pp - 1 - (jy % n_pp);  // longest rows first
   x->gh = jy / n_pp;
   x->g = x->gh / geo.n_hc;
@@ -338,8 +345,7 @@ __global__ void __launch_bounds__(kScoreThreads1, 1)
       }
       if (ok && active) {
         const int rt = x.gh * geo.n_pb + x.pb0 + t;
-        const int split = it % n_split;
-        partial[((static_cast<size_t>(rt) * n_split + split) * 2 + grp) * 128 + row] = make_float2(m, l);
+        partial[((static_cast<size_t>(rt) * n_split + x.split) * 2 + grp) * 128 + row] = make_float2(m, l);
       }
     }
   }
@@ -439,12 +445,16 @@ struct ColItem {
 
 __host__ __device__ inline int col_pairs(const ScoreGeom& geo) { return (geo.n_kt + 1) / 2; }
 
-// item it = ((pair * Hkv) + g) * n_split + split: early pairs (the longest
-// query lists) first
+// item it = split * (pairs * Hkv) + pair * Hkv + g: early pairs (the longest
+// query lists) first within each split.  The split index varies slowest: the
+// persistent CTAs take items it, it + gridDim.x, ..., and with the split
+// fastest an even grid would hand every even CTA the long first chunks and
+// every odd CTA the short last ones.
 __device__ __forceinline__ bool col_item(const ScoreGeom& geo, const int qt_chunk, const int n_split, const int it,
                                          ColItem* x) {
-  x->split = it % n_split;
-  const int r = it / n_split;
+  const int per_split = col_pairs(geo) * geo.Hkv;
+  x->split = it / per_split;
+  const int r = it % per_split;
   x->g = r % geo.Hkv;
   x->kt0 = 2 * (r / geo.Hkv);
   x->two = x->kt0 + 1 < geo.n_kt;
@@ -883,6 +893,181 @@ __global__ void __launch_bounds__(256) vnorm_kernel(const uint16_t* __restrict__
       const int t = t0 + tq + x;
       if (t < N) vn[static_cast<size_t>(h) * N + t] = sqrtf(fmaxf(part[x], 0.f));
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// |W_O^h v_t| on the tensor cores (d = 128): vn^2 = v_t^T G_h v_t with
+// G_h = W_O^h^T W_O^h.  G_h (fp32, the sum of the Gram slices in slice order)
+// is split into two bf16 matrices, G = G_hi + G_lo (16 significant bits), and
+// P = V_tile G_h is two tcgen05 MMAs into TMEM (bf16 products exact, fp32
+// sums); the epilogue thread of token t then forms sum_c P[t, c] V[t, c],
+// reading its value row from global memory (L2-resident: TMA just brought the
+// tile in for the MMA).  Reading the row from the staged shared-memory tile
+// instead gave wrong sums, varying run to run, whenever both tile stages and
+// both accumulator buffers were in flight (with one of either, it was exact);
+// the global read is exact with the full pipeline.
+// grid (n_split, Hq), 192 threads: warps 0-3 the epilogue (one token row per
+// thread), warp 4 TMA (the value tiles of KV head h / G), warp 5 the MMAs.
+// ---------------------------------------------------------------------------
+constexpr int kVnThreads = 192;
+constexpr int kVnStages = 2;
+
+struct VnSmem {
+  uint8_t g_hi[2 * 16384];            // G_h high part, K-major 128-byte-swizzle panels (B operand)
+  uint8_t g_lo[2 * 16384];            // G_h low part
+  uint8_t v[kVnStages][2 * 16384];    // value tiles: 128 tokens x 128 channels (A operand)
+  uint64_t v_full[kVnStages], v_empty[kVnStages], acc_full[2], acc_empty[2], drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// byte offset of element (row r, column c) of a K-major 128-byte-swizzle tile of 128-column rows
+__device__ __forceinline__ uint32_t sw128_elem(int r, int c) {
+  return static_cast<uint32_t>((c >> 6) * 16384 + (r >> 3) * 1024 + (r & 7) * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) +
+                               (c & 7) * 2);
+}
+
+__global__ void __launch_bounds__(kVnThreads, 1)
+    vnorm_tc_kernel(const __grid_constant__ CUtensorMap mapV, const float* __restrict__ gram, const int n_slices,
+                    const int Hq, const int G, const int N, const int tiles_per_cta, float* __restrict__ vn,
+                    const uint16_t* __restrict__ V) {
+  extern __shared__ uint8_t smem_raw[];
+  VnSmem& S = *reinterpret_cast<VnSmem*>(align1024(smem_raw));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y, g = h / G;
+  const int n_tiles = (N + 127) / 128;
+  const int tile0 = blockIdx.x * tiles_per_cta;
+  const int tile1 = min(n_tiles, tile0 + tiles_per_cta);
+  if (tile0 >= tile1 || timeout_recorded()) return;  // uniform over the CTA, before any barrier
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kVnStages; ++s) {
+      mbar_init(&S.v_full[s], 1);
+      mbar_init(&S.v_empty[s], 1 + 4);  // the MMAs and the 4 epilogue warps (they read the tile too)
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.acc_full[b], 1);
+      mbar_init(&S.acc_empty[b], 4);
+    }
+    mbar_init(&S.drain, 1);
+    S.abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&S.tmem_base, 256);
+    tmem_relinquish();
+  }
+  pdl_wait();  // the Gram slices come from the previous kernel on the stream
+  // G_h = sum of the slices (fixed order), split into bf16 high and low parts
+  const float* gh = gram + static_cast<size_t>(h) * 128 * 128;
+  const size_t slice = static_cast<size_t>(Hq) * 128 * 128;
+  for (int e = threadIdx.x; e < 128 * 128; e += kVnThreads) {
+    float a = 0.f;
+    for (int s = 0; s < n_slices; ++s) a += gh[s * slice + e];
+    const int r = e >> 7, c = e & 127;  // B operand row n = r (G is symmetric), K index c
+    const __nv_bfloat16 hi = __float2bfloat16_rn(a);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(a - __bfloat162float(hi));
+    *reinterpret_cast<__nv_bfloat16*>(S.g_hi + sw128_elem(r, c)) = hi;
+    *reinterpret_cast<__nv_bfloat16*>(S.g_lo + sw128_elem(r, c)) = lo;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the stores above are visible to the tensor core
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_trigger();
+  const uint32_t tmem = S.tmem_base;
+  volatile int* abort_flag = &S.abort_flag;
+  const int nt = tile1 - tile0;
+
+  if (warp == 4) {
+    if (lane == 0) {  // TMA producer
+      prefetch_tensormap(&mapV);
+      int issued = 0;
+      for (int i = 0; i < nt; ++i) {
+        const int s = i % kVnStages;
+        if (!mbar_wait(&S.v_empty[s], ((i / kVnStages) & 1) ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(&S.v_full[s], 2 * 16384);
+#pragma unroll
+        for (int p = 0; p < 2; ++p) tma_load_3d(S.v[s] + p * 16384, &mapV, &S.v_full[s], p * 64, (tile0 + i) * 128, g);
+        issued = i + 1;
+      }
+      if (*abort_flag) {
+        volatile int never = 0;
+        for (int i = max(0, issued - kVnStages); i < issued; ++i)
+          mbar_wait(&S.v_full[i % kVnStages], (i / kVnStages) & 1, &never);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {  // MMA issuer: P = V_tile (M = 128 tokens) x G_h (N = 128 channels), hi then lo
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+      for (int i = 0; i < nt; ++i) {
+        const int s = i % kVnStages, b = i & 1;
+        if (!mbar_wait(&S.v_full[s], (i / kVnStages) & 1, abort_flag) ||
+            !mbar_wait(&S.acc_empty[b], ((i >> 1) & 1) ^ 1u, abort_flag))
+          break;
+        tc_fence_after();
+        const uint32_t a = smem_u32(S.v[s]);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t bm = smem_u32(part ? S.g_lo : S.g_hi);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
+            umma_bf16(tmem + b * 128, sdesc_kmajor_sw128(a + off), sdesc_kmajor_sw128(bm + off), idesc,
+                      (part > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(&S.v_empty[s]);
+        umma_commit(&S.acc_full[b]);
+      }
+      if (*abort_flag) {
+        volatile int never = 0;
+        umma_commit(&S.drain);
+        mbar_wait(&S.drain, 0, &never);
+      }
+    }
+  } else {  // warps 0-3: token row 32 warp + lane of each tile
+    const int row = warp * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint16_t* Vg = V + static_cast<long long>(g) * N * 128;
+    uint32_t pv[32];
+    for (int i = 0; i < nt; ++i) {
+      const int s = i % kVnStages, b = i & 1;
+      if (!mbar_wait(&S.acc_full[b], (i >> 1) & 1, abort_flag)) break;
+      tc_fence_after();
+      const int t = (tile0 + i) * 128 + row;
+      const uint16_t* vrow = Vg + static_cast<long long>(min(t, N - 1)) * 128;
+      float acc = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        tmem_issue32(lane_base + b * 128 + ch * 32, pv);
+        tmem_wait32(pv);
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8) {  // 8 channels of the value row per 16-byte load
+          const int c = ch * 32 + j8 * 8;
+          const uint4 q = __ldg(reinterpret_cast<const uint4*>(vrow + c));
+          const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            acc = fmaf(__uint_as_float(pv[j8 * 8 + 2 * k]), __uint_as_float(wv[k] << 16), acc);
+            acc = fmaf(__uint_as_float(pv[j8 * 8 + 2 * k + 1]), __uint_as_float(wv[k] & 0xFFFF0000u), acc);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&S.acc_empty[b]);
+        mbar_arrive(&S.v_empty[s]);
+      }
+      if (t < N) vn[static_cast<size_t>(h) * N + t] = sqrtf(fmaxf(acc, 0.f));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
   }
 }
 

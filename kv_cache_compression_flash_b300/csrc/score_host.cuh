@@ -211,12 +211,37 @@ int score_dh(const ScorePlan& pl, const uint16_t* Q, const uint16_t* K, const ui
   if (pl.want_plus) {
     KVS_CUDA_TRY(launch_k(row_norm_kernel, dim3(static_cast<unsigned>(cdiv(g.W, 8))), dim3(256), 0, st, 0, h, g.W,
                           pl.D, w.hn));
-    KVS_CUDA_TRY(launch_k(gram_kernel<DH>, dim3(kGramSlices, g.Hq, DH / 64), dim3(256), 0, st, 0, WO, pl.D, g.Hq,
-                          pl.gram_slice_len, w.gram));
+    if (DH == kGramD) {
+      // W_O^h^T W_O^h on the tensor cores: head h's 128 columns of W_O as a
+      // [D, 128] matrix with row stride Hq * 128; the slices' partial Grams
+      // are summed by the vnorm kernel in slice order
+      KVS_CUDA_TRY(allow_smem(gram_partial_kernel, kGramSmem));
+      const int per = static_cast<int>(cdiv(cdiv(pl.D, kGramTile), kGramSlices) * kGramTile);
+      KVS_CUDA_TRY(launch_k(gram_partial_kernel, dim3(kGramSlices, g.Hq), dim3(kGramThreads), kGramSmem, st, 0, WO, pl.D,
+                            static_cast<long long>(g.Hq) * DH, static_cast<long long>(DH),
+                            static_cast<const uint8_t*>(nullptr), per, w.gram));
+    } else {
+      KVS_CUDA_TRY(launch_k(gram_kernel<DH>, dim3(kGramSlices, g.Hq, DH / 64), dim3(256), 0, st, 0, WO, pl.D, g.Hq,
+                            pl.gram_slice_len, w.gram));
+    }
+    if (DH == kGramD) {  // the quadratic forms on the tensor cores
+      CUtensorMap mv;
+      rc = make_map_3d(&mv, V, DH, g.N, g.Hkv, 64, 128, 1);
+      if (rc) return rc;
+      const size_t vs = sizeof(VnSmem) + 1024;
+      KVS_CUDA_TRY(allow_smem(vnorm_tc_kernel, vs));
+      const int n_tiles = static_cast<int>(cdiv(g.N, 128));
+      const int per_head = static_cast<int>(std::max<long long>(1, sm_count() / g.Hq));  // CTAs per head: one wave
+      const int tiles_per_cta = static_cast<int>(cdiv(n_tiles, per_head));
+      const int n_split = static_cast<int>(cdiv(n_tiles, tiles_per_cta));
+      KVS_CUDA_TRY(launch_k(vnorm_tc_kernel, dim3(static_cast<unsigned>(n_split), g.Hq), dim3(kVnThreads), vs, st, 0, mv,
+                            static_cast<const float*>(w.gram), kGramSlices, g.Hq, g.G, g.N, tiles_per_cta, w.vn, V));
+    } else {
     const size_t vsmem = (static_cast<size_t>(DH) * DH + static_cast<size_t>(DH) * 64) * sizeof(float);
     KVS_CUDA_TRY(allow_smem(vnorm_kernel<DH>, vsmem));
     KVS_CUDA_TRY(launch_k(vnorm_kernel<DH>, dim3(static_cast<unsigned>(cdiv(g.N, 64)), g.Hq), dim3(256), vsmem, st, 0,
                           V, w.gram, kGramSlices, g.Hq, g.G, g.N, w.vn));
+    }
   }
   if (pl.lse_given) {
     if (w.b_plain || w.b_scaled) KVS_CUDA_TRY(launch_k(lse_offsets_kernel, dim3(g.n_rt), dim3(128), 0, st, 0, g, lse, w.hn, w.b_plain, w.b_scaled));
