@@ -46,8 +46,6 @@ __device__ __forceinline__ int width_slot(uint32_t w) {
   return w == 2 ? 0 : w == 4 ? 1 : w == 8 ? 2 : w == 16 ? 3 : -1;
 }
 
-__device__ __forceinline__ unsigned half_mask() { return 0xFFFFu << (threadIdx.x & 16); }
-
 // round-half-even(x / s) for bf16 x and fp16 s > 0 with |x / s| <= 128, from
 // one reciprocal r ~ 1/s: floor(x r) is within one of the nearest integer
 // (|x r - x/s| <= 2^-16), and the choice between n0 = floor(x r) and n0 + 1
@@ -91,155 +89,27 @@ __device__ __forceinline__ uint32_t bf16x2_max(const uint32_t a, const uint32_t 
 // which lands in the low mantissa bits, so the low w bits of y's pattern are
 // the w-bit two's-complement code.  d = t - (y - 1.5 * 2^23) is exact; an
 // element with |d| within 2^-14 of 1/2 may round differently from x / s, and
-// q_round settles those exactly (rare).
+// q_round settles those exactly.
+//
+// How far x / s can be from a half integer h: with x = m_x 2^(e_x - 7) (bf16)
+// and s = m_s 2^(e_s - 10) (fp16), x - h s is a multiple of 2^(e_s - 11)
+// whenever |x / s| >= 1/8, so x / s is either exactly h or at least 2^-12
+// away from it; x r is within 2^-16 of x / s, so only exact ties can round
+// the wrong way.  At width 2 (|x / s| <= 1) the only half integers are
+// +-1/2, whose even neighbour is 0: with r = 1/s rounded toward zero, |x r|
+// <= |x / s|, so a tie lands on or below 1/2 and rounds to 0, and every other
+// quotient rounds as x / s does.  Width 2 therefore needs no check at all;
+// there ties are common (s is the group maximum itself, so an element equal
+// to half of it is one), at widths 4 and 8 they are rare.
 constexpr float kRoundMagic = 12582912.f;                             // 1.5 * 2^23
 constexpr float kNearHalfSq = 0.49993896484375f * 0.49993896484375f;  // (1/2 - 2^-14)^2
+constexpr float kNoCheck = 4.f;                                       // above every d^2: never near
 
-// the low w bits (w <= 8) of y[0..7]'s patterns packed at bits [w e, w e + w)
-__device__ __forceinline__ unsigned long long pack_codes8(const uint32_t (&yb)[8], const int w) {
-  const uint32_t cmask = (1u << w) - 1u;
-  uint32_t lo = 0u, hi = 0u;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int sh = w * e;
-    const uint32_t cb = yb[e] & cmask;
-    if (sh < 32)
-      lo |= cb << sh;
-    else
-      hi |= cb << (sh - 32);
-  }
-  return static_cast<unsigned long long>(lo) | (static_cast<unsigned long long>(hi) << 32);
+// the reciprocal the quantisers use at width w (see above)
+__device__ __forceinline__ float quant_recip(const float s, const int w) {
+  return w == 2 ? __frcp_rz(s) : __frcp_rn(s);
 }
 
-// codes of 8 consecutive elements of one group (one scale): x[e] as 4 packed pairs
-__device__ __forceinline__ unsigned long long quantize_octet(const float (&x)[8], const int w, const float s,
-                                                             const float r) {
-  const unsigned long long r2 = f2_pack(r, r), m2 = f2_pack(kRoundMagic, kRoundMagic),
-                           nm2 = f2_pack(-kRoundMagic, -kRoundMagic), neg1 = f2_pack(-1.f, -1.f);
-  uint32_t yb[8];
-  float dd[8];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const unsigned long long t = f2_mul(f2_pack(x[2 * k], x[2 * k + 1]), r2);
-    const unsigned long long y = f2_add(t, m2);
-    const unsigned long long d = f2_fma(f2_add(y, nm2), neg1, t);
-    float y0, y1;
-    f2_unpack(y, &y0, &y1);
-    yb[2 * k] = __float_as_uint(y0);
-    yb[2 * k + 1] = __float_as_uint(y1);
-    f2_unpack(f2_mul(d, d), &dd[2 * k], &dd[2 * k + 1]);
-  }
-  if (fmax3(fmax3(dd[0], dd[1], dd[2]), fmax3(dd[3], dd[4], dd[5]), fmaxf(dd[6], dd[7])) >= kNearHalfSq) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) yb[e] = static_cast<uint32_t>(q_round(x[e], s, r));  // the exact test
-  }
-  return pack_codes8(yb, w);
-}
-
-// The same for one octet of TWO channels at once (a lane's channel pair of a
-// K group): v[e] holds element e of channel 0 in its low bf16 half and of
-// channel 1 in its high half; each channel has its own width, scale and
-// reciprocal.  Results: *c0, *c1.
-__device__ __forceinline__ void quantize_octet_pair(const uint32_t (&v)[8], const int w0, const int w1, const float s0,
-                                                    const float s1, const float r0, const float r1,
-                                                    unsigned long long* c0, unsigned long long* c1) {
-  const unsigned long long r2 = f2_pack(r0, r1), m2 = f2_pack(kRoundMagic, kRoundMagic),
-                           nm2 = f2_pack(-kRoundMagic, -kRoundMagic), neg1 = f2_pack(-1.f, -1.f);
-  uint32_t ya[8], yb[8];
-  float da[8], db[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const unsigned long long t = f2_mul(f2_pack(__uint_as_float(v[e] << 16), __uint_as_float(v[e] & 0xFFFF0000u)), r2);
-    const unsigned long long y = f2_add(t, m2);
-    const unsigned long long d = f2_fma(f2_add(y, nm2), neg1, t);
-    float y0, y1;
-    f2_unpack(y, &y0, &y1);
-    ya[e] = __float_as_uint(y0);
-    yb[e] = __float_as_uint(y1);
-    f2_unpack(f2_mul(d, d), &da[e], &db[e]);
-  }
-  const float ma = fmax3(fmax3(da[0], da[1], da[2]), fmax3(da[3], da[4], da[5]), fmaxf(da[6], da[7]));
-  const float mb = fmax3(fmax3(db[0], db[1], db[2]), fmax3(db[3], db[4], db[5]), fmaxf(db[6], db[7]));
-  if (ma >= kNearHalfSq) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) ya[e] = static_cast<uint32_t>(q_round(__uint_as_float(v[e] << 16), s0, r0));
-  }
-  if (mb >= kNearHalfSq) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) yb[e] = static_cast<uint32_t>(q_round(__uint_as_float(v[e] & 0xFFFF0000u), s1, r1));
-  }
-  *c0 = pack_codes8(ya, w0 <= 8 ? w0 : 8);
-  *c1 = pack_codes8(yb, w1 <= 8 ? w1 : 8);
-}
-
-// Quantise this lane's 4 elements of a 64-element group (the half-warp holds
-// the group).  Returns the 4w code bits; *scale_bits gets the fp16 scale.
-__device__ __forceinline__ uint32_t quantize_lane4(const float (&x)[4], const int w, uint16_t* scale_bits,
-                                                   bool* overflow) {
-  float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-  const unsigned m = half_mask();
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(m, a, o));
-  const float qmax = static_cast<float>((1 << (w - 1)) - 1);
-  const __half sh = __float2half_ru(__fdiv_rn(a, qmax));
-  const float s = __half2float(sh);
-  *overflow = isinf(s);
-  *scale_bits = __half_as_ushort(sh);
-  uint32_t packed = 0;
-  const uint32_t cmask = (1u << w) - 1u;
-  if (s > 0.f && !isinf(s)) {
-    const float r = __frcp_rn(s);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) packed |= (static_cast<uint32_t>(q_round(x[e], s, r)) & cmask) << (w * e);
-  }
-  return packed;
-}
-
-__device__ __forceinline__ void store_lane_codes(uint8_t* group_base, const int w, const int l16,
-                                                 const uint32_t packed, const uint2 raw) {
-  switch (w) {
-    case 2: group_base[l16] = static_cast<uint8_t>(packed); break;
-    case 4: reinterpret_cast<uint16_t*>(group_base)[l16] = static_cast<uint16_t>(packed); break;
-    case 8: reinterpret_cast<uint32_t*>(group_base)[l16] = packed; break;
-    default: reinterpret_cast<uint2*>(group_base)[l16] = raw; break;
-  }
-}
-
-// Decode this lane's 4 elements of a group.
-__device__ __forceinline__ void dequant_lane4(const uint8_t* group_base, const int w, const int l16,
-                                              const uint16_t* scale_ptr, float (&y)[4]) {
-  if (w == 16) {
-    const uint2 raw = reinterpret_cast<const uint2*>(group_base)[l16];
-    y[0] = __uint_as_float(raw.x << 16);
-    y[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-    y[2] = __uint_as_float(raw.y << 16);
-    y[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-    return;
-  }
-  uint32_t packed;
-  if (w == 2)
-    packed = group_base[l16];
-  else if (w == 4)
-    packed = reinterpret_cast<const uint16_t*>(group_base)[l16];
-  else
-    packed = reinterpret_cast<const uint32_t*>(group_base)[l16];
-  const float s = __half2float(__ushort_as_half(*scale_ptr));
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int code = static_cast<int>((packed >> (w * e)) & ((1u << w) - 1u));
-    const int q = code >= (1 << (w - 1)) ? code - (1 << w) : code;
-    y[e] = static_cast<float>(q) * s;
-  }
-}
-
-__device__ __forceinline__ void lane_bf16x4(const uint16_t* src, float (&x)[4], uint2* raw) {
-  const uint2 r = *reinterpret_cast<const uint2*>(src);
-  *raw = r;
-  x[0] = __uint_as_float(r.x << 16);
-  x[1] = __uint_as_float(r.x & 0xFFFF0000u);
-  x[2] = __uint_as_float(r.y << 16);
-  x[3] = __uint_as_float(r.y & 0xFFFF0000u);
-}
 
 __device__ __forceinline__ float bf16_lo(uint32_t p) { return __uint_as_float(p << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t p) { return __uint_as_float(p & 0xFFFF0000u); }
@@ -372,11 +242,15 @@ __global__ void __launch_bounds__(kRowThreads) rows_count_kernel(const uint8_t* 
 // The chunk blockIdx.x of pool `pool`: s_w[i] = width of unit u0 + i, s_ent[i]
 // = its entry in its width stream (-1: width 0, or past the capacity).  With
 // write_streams, also the unit ids and group offsets of the chunk's entries
-// and, from the pool's last chunk, the counts.  Returns the chunk's units.
+// and, from the pool's last chunk, the counts.  With s_list, the chunk's
+// stored units grouped by width slot, ascending within a slot (slot q's
+// units at s_list[lists[q] .. lists[q + 1])), and *slot_units = the units
+// per slot in four 16-bit fields.  Returns the chunk's units.
 __device__ __forceinline__ int rows_chunk_plan(const uint8_t* __restrict__ bits, const long long U, const int n_chunks,
                                                const uint32_t* __restrict__ cnt, const long long pool, const int gpu,
                                                const StreamPtrs& sp, const bool write_streams, int* s_ent,
-                                               uint8_t* s_w, long long* s_base, unsigned long long* sbuf) {
+                                               uint8_t* s_w, long long* s_base, unsigned long long* sbuf,
+                                               uint16_t* s_list = nullptr, unsigned long long* slot_units = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int chunk = blockIdx.x;
   const long long u0 = static_cast<long long>(chunk) * kRowChunk;
@@ -401,6 +275,8 @@ __device__ __forceinline__ int rows_chunk_plan(const uint8_t* __restrict__ bits,
   }
   unsigned long long tot;
   unsigned long long ex = block_exscan_u64<kRowThreads>(c, sbuf, &tot);  // its barriers also publish s_base
+  // start of each slot's list: the chunk totals of the slots below it (16-bit fields)
+  const unsigned long long list0 = (tot << 16) + (tot << 32) + (tot << 48);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int i = tid * 4 + e;
@@ -408,6 +284,7 @@ __device__ __forceinline__ int rows_chunk_plan(const uint8_t* __restrict__ bits,
     const int sl = width_slot(b);
     int ent = -1;
     if (sl >= 0 && i < n) {
+      if (s_list) s_list[((list0 + ex) >> (16 * sl)) & 0xFFFFull] = static_cast<uint16_t>(i);
       const long long k = s_base[sl] + static_cast<long long>((ex >> (16 * sl)) & 0xFFFFull);
       ex += 1ull << (16 * sl);
       if (k < sp.cap_units[sl]) {
@@ -430,28 +307,9 @@ __device__ __forceinline__ int rows_chunk_plan(const uint8_t* __restrict__ bits,
     }
     if (units > sp.cap_units[tid] || groups > sp.cap_groups[tid]) record_error(KVS_ERR_RANGE);
   }
+  if (slot_units) *slot_units = tot;
   __syncthreads();
   return n;
-}
-
-// This lane's 8 elements of a 64-element group (eight lanes hold the group,
-// all 32 lanes of the warp take part).  Returns the 8w code bits, element e
-// at bits [w e, w e + w); *scale_bits gets the group's fp16 scale.
-__device__ __forceinline__ unsigned long long quantize_lane8(const float (&x)[8], const int w, uint16_t* scale_bits,
-                                                             bool* overflow) {
-  float a = 0.f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(x[e]));
-#pragma unroll
-  for (int o = 4; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-  const float qmax = static_cast<float>((1 << (w - 1)) - 1);
-  const __half sh = __float2half_ru(__fdiv_rn(a, qmax));
-  const float s = __half2float(sh);
-  *overflow = isinf(s);
-  *scale_bits = __half_as_ushort(sh);
-  unsigned long long packed = 0ull;
-  if (s > 0.f && !isinf(s)) packed = quantize_octet(x, w, s, __frcp_rn(s));
-  return packed;
 }
 
 __device__ __forceinline__ void bf16x8(const uint4 u, float (&x)[8]) {
@@ -463,22 +321,204 @@ __device__ __forceinline__ void bf16x8(const uint4 u, float (&x)[8]) {
   }
 }
 
-// the w bytes of this lane's codes (width 16: the raw 16 bytes), at the lane's place in the group's block
-__device__ __forceinline__ void store_lane8(uint8_t* group_base, const int w, const int l8, const unsigned long long packed,
-                                            const uint4 raw) {
-  switch (w) {
-    case 2: reinterpret_cast<uint16_t*>(group_base)[l8] = static_cast<uint16_t>(packed); break;
-    case 4: reinterpret_cast<uint32_t*>(group_base)[l8] = static_cast<uint32_t>(packed); break;
-    case 8: reinterpret_cast<unsigned long long*>(group_base)[l8] = packed; break;
-    default: {  // 8-byte aligned streams: two 8-byte stores
-      uint2* p = reinterpret_cast<uint2*>(group_base) + 2 * l8;
-      p[0] = make_uint2(raw.x, raw.y);
-      p[1] = make_uint2(raw.z, raw.w);
+// Offset-binary rounding at width W (2, 4 or 8): adding M = 1.5 * 2^23 +
+// 2^(W-1) to t = x r in one FMA rounds t to the nearest integer q (ties to
+// even: M is even) and leaves c = q + 2^(W-1), which lies in [1, 2^W - 1], in
+// the low bits of the result's pattern, above the pattern of 1.5 * 2^23.  The
+// W-bit two's-complement code of q is c with its top bit flipped.  So the
+// codes of 8 elements at bits [W e, W e + W) are the sum of the patterns
+// shifted by W e (one shift-add each), minus the same sum over 1.5 * 2^23's
+// pattern, with every code's top bit flipped; each c fits its field, so the
+// fields never carry into each other.
+template <int W>
+struct OffsetCode {
+  static constexpr float kMagic = 12582912.f + static_cast<float>(1 << (W - 1));
+  static constexpr uint32_t kBase = 0x4B400000u;  // the pattern of 1.5 * 2^23
+  static constexpr int kPerWord = 32 / W;  // codes per 32-bit word
+  // sum of kBase << (W e) over the word's codes, mod 2^32
+  static constexpr uint32_t kBaseSum = [] {
+    uint32_t v = 0u;
+    for (int e = 0; e < kPerWord; ++e) v += kBase << (W * e);
+    return v;
+  }();
+  // every code's top bit
+  static constexpr uint32_t kTopBits = [] {
+    uint32_t v = 0u;
+    for (int e = 0; e < kPerWord; ++e) v |= (1u << (W - 1)) << (W * e);
+    return v;
+  }();
+};
+
+// The codes of NE elements of one group (scale s > 0, r = quant_recip(s, W))
+// at width W: element e at bits [W e, W e + W) of words[], NE W / 32 words.
+// At widths 4 and 8, elements whose x r lies within 2^-14 of a half integer
+// are settled by q_round.
+template <int W, int NE>
+__device__ __forceinline__ void quantize_w(const float (&x)[NE], const float s, const float r,
+                                           uint32_t (&words)[NE * W / 32]) {
+  using OC = OffsetCode<W>;
+  const unsigned long long r2 = f2_pack(r, r), m2 = f2_pack(OC::kMagic, OC::kMagic), neg1 = f2_pack(-1.f, -1.f);
+  uint32_t yb[NE];
+  float dd[NE];
+#pragma unroll
+  for (int k = 0; k < NE / 2; ++k) {
+    const unsigned long long xp = f2_pack(x[2 * k], x[2 * k + 1]);
+    const unsigned long long y = f2_fma(xp, r2, m2);  // M + round(x r)
+    float y0, y1;
+    f2_unpack(y, &y0, &y1);
+    yb[2 * k] = __float_as_uint(y0);
+    yb[2 * k + 1] = __float_as_uint(y1);
+    if constexpr (W != 2) {  // width 2 (r rounded toward zero) is exact as it stands
+      const unsigned long long nq = f2_fma(y, neg1, m2);  // -round(x r), exact
+      const unsigned long long d = f2_fma(xp, r2, nq);    // x r - round(x r)
+      f2_unpack(f2_mul(d, d), &dd[2 * k], &dd[2 * k + 1]);
+    }
+  }
+  if constexpr (W != 2) {
+    float m = dd[0];
+#pragma unroll
+    for (int e = 1; e + 1 < NE; e += 2) m = fmax3(m, dd[e], dd[e + 1]);
+    if (NE % 2 == 0) m = fmaxf(m, dd[NE - 1]);
+    if (m >= kNearHalfSq) {
+#pragma unroll
+      for (int e = 0; e < NE; ++e)
+        yb[e] = OC::kBase + (1u << (W - 1)) + static_cast<uint32_t>(q_round(x[e], s, r));  // the exact test
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < NE * W / 32; ++h) {
+    uint32_t acc = 0u;
+#pragma unroll
+    for (int f = 0; f < OC::kPerWord; ++f) acc += yb[h * OC::kPerWord + f] << (W * f);
+    words[h] = (acc - OC::kBaseSum) ^ OC::kTopBits;
+  }
+}
+
+// The offset code of quantize_w with the width w (2, 4 or 8) in
+// registers instead of the instruction stream, so lanes of one warp that hold
+// channels of different widths run the same instructions: the codes of 8
+// elements are a = sum over e < 4 and b = sum over e >= 4 of the patterns
+// times 2^(w (e mod 4)); the low word is a + b 2^(4w) (w <= 4) or a (w = 8),
+// the high word 0 or b, each minus the same sums over 1.5 * 2^23's pattern
+// and with the codes' top bits flipped.
+struct DynCode {
+  float magic;                 // 1.5 * 2^23 + 2^(w-1)
+  float near_sq;               // kNearHalfSq, or kNoCheck at width 2
+  uint32_t half;               // 2^(w-1)
+  uint32_t m1, m2, m3;         // 2^w, 2^2w, 2^3w
+  uint32_t mhi, hsel;          // 2^4w and 0 (w <= 4); 0 and 1 (w = 8)
+  uint32_t sub_lo, xor_lo, sub_hi, xor_hi;
+};
+
+__device__ __forceinline__ DynCode dyn_code(const int w) {
+  DynCode c;
+  c.half = 1u << (w - 1);
+  c.magic = 12582912.f + static_cast<float>(c.half);
+  c.near_sq = w == 2 ? kNoCheck : kNearHalfSq;
+  c.m1 = 1u << w;
+  c.m2 = c.m1 * c.m1;
+  c.m3 = c.m2 * c.m1;
+  const uint32_t sum4 = 1u + c.m1 + c.m2 + c.m3;  // 2^(w e) over e < 4
+  const uint32_t s4 = OffsetCode<2>::kBase * sum4, t4 = c.half * sum4;
+  if (w == 8) {
+    c.mhi = 0u, c.hsel = 1u, c.sub_lo = s4, c.xor_lo = t4, c.sub_hi = s4, c.xor_hi = t4;
+  } else {
+    const uint32_t m4 = c.m2 * c.m2;
+    c.mhi = m4, c.hsel = 0u, c.sub_lo = s4 + s4 * m4, c.xor_lo = t4 + t4 * m4, c.sub_hi = 0u, c.xor_hi = 0u;
+  }
+  return c;
+}
+
+// the 8w code bits of x[0..7] (scale s > 0, r = quant_recip(s, w)) at the width of c
+__device__ __forceinline__ unsigned long long quantize_octet_dyn(const float (&x)[8], const float s, const float r,
+                                                                 const DynCode& c) {
+  const unsigned long long r2 = f2_pack(r, r), m2 = f2_pack(c.magic, c.magic), neg1 = f2_pack(-1.f, -1.f);
+  uint32_t yb[8];
+  float dd[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const unsigned long long xp = f2_pack(x[2 * k], x[2 * k + 1]);
+    const unsigned long long y = f2_fma(xp, r2, m2);
+    const unsigned long long nq = f2_fma(y, neg1, m2);
+    const unsigned long long d = f2_fma(xp, r2, nq);
+    float y0, y1;
+    f2_unpack(y, &y0, &y1);
+    yb[2 * k] = __float_as_uint(y0);
+    yb[2 * k + 1] = __float_as_uint(y1);
+    f2_unpack(f2_mul(d, d), &dd[2 * k], &dd[2 * k + 1]);
+  }
+  if (fmax3(fmax3(dd[0], dd[1], dd[2]), fmax3(dd[3], dd[4], dd[5]), fmaxf(dd[6], dd[7])) >= c.near_sq) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      yb[e] = OffsetCode<2>::kBase + c.half + static_cast<uint32_t>(q_round(x[e], s, r));  // the exact test
+  }
+  const uint32_t a = yb[0] + yb[1] * c.m1 + yb[2] * c.m2 + yb[3] * c.m3;
+  const uint32_t b = yb[4] + yb[5] * c.m1 + yb[6] * c.m2 + yb[7] * c.m3;
+  const uint32_t lo = (a + b * c.mhi - c.sub_lo) ^ c.xor_lo;
+  const uint32_t hi = (b * c.hsel - c.sub_hi) ^ c.xor_hi;
+  return static_cast<unsigned long long>(lo) | (static_cast<unsigned long long>(hi) << 32);
+}
+
+// Pack this lane's 16 elements of the groups of kRowSteps warp steps at
+// width W (warp-uniform).  Lanes 4j .. 4j + 3 hold one group; ent[k] < 0: no
+// group.
+constexpr int kRowSteps = 2;
+
+template <int W, int GPU>
+__device__ __forceinline__ void pack_rows_steps(const StreamPtrs& sp, const long long pool, const int slot,
+                                                const int l4, const int gi, const uint4 (&raw)[kRowSteps][2],
+                                                const int (&ent)[kRowSteps]) {
+#pragma unroll
+  for (int k = 0; k < kRowSteps; ++k) {
+    const long long gg = pool * sp.cap_groups[slot] + static_cast<long long>(ent[k]) * GPU + gi;
+    if constexpr (W == 16) {
+      if (ent[k] >= 0) {
+        uint4* dst = reinterpret_cast<uint4*>(sp.codes[3] + gg * 128) + 2 * l4;
+        dst[0] = raw[k][0];
+        dst[1] = raw[k][1];
+      }
+    } else {
+      float x[16];
+      const uint32_t v[8] = {raw[k][0].x, raw[k][0].y, raw[k][0].z, raw[k][0].w,
+                             raw[k][1].x, raw[k][1].y, raw[k][1].z, raw[k][1].w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        x[2 * e] = bf16_lo(v[e]);
+        x[2 * e + 1] = bf16_hi(v[e]);
+      }
+      float a = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) a = fmaxf(a, fabsf(x[e]));
+#pragma unroll
+      for (int o = 2; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+      const __half sh = W == 2 ? __float2half_ru(a) : __float2half_ru(__fdiv_rn(a, static_cast<float>((1 << (W - 1)) - 1)));
+      const float sc = __half2float(sh);
+      uint32_t words[W / 2];
+#pragma unroll
+      for (int h = 0; h < W / 2; ++h) words[h] = 0u;
+      if (sc > 0.f && !isinf(sc)) quantize_w<W, 16>(x, sc, quant_recip(sc, W), words);
+      if (ent[k] >= 0) {
+        if (l4 == 0) {
+          sp.scales[slot][gg] = __half_as_ushort(sh);
+          if (isinf(sc)) record_error(KVS_ERR_RANGE);
+        }
+        uint8_t* dst = sp.codes[slot] + gg * (8 * W) + l4 * (2 * W);
+        if constexpr (W == 2)
+          *reinterpret_cast<uint32_t*>(dst) = words[0];
+        else if constexpr (W == 4)
+          *reinterpret_cast<uint2*>(dst) = make_uint2(words[0], words[1]);
+        else
+          *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+      }
     }
   }
 }
 
-// grid (chunks, pools): pack the stored units of one chunk, in unit order
+// grid (chunks, pools): pack the stored units of one chunk.  The plan groups
+// the chunk's units by width, so every warp works at one width (a template
+// parameter) on the units of one list: a warp takes 8 groups per step (4
+// lanes, 32 bytes a lane, per 64-element group), kRowSteps steps' loads in
+// flight.
 template <int DH>
 __global__ void __launch_bounds__(kRowThreads) pack_rows_kernel(const uint16_t* __restrict__ X,
                                                                 const uint8_t* __restrict__ bits, const long long U,
@@ -488,50 +528,53 @@ __global__ void __launch_bounds__(kRowThreads) pack_rows_kernel(const uint16_t* 
   pdl_trigger();
   constexpr int GPU = DH / 64;
   constexpr int kWarps = kRowThreads / 32;
+  constexpr int kStepUnits = 8 / GPU;            // units of one warp step
+  constexpr int kItemUnits = kRowSteps * kStepUnits;  // units of one work item
   __shared__ int s_ent[kRowChunk];
   __shared__ uint8_t s_w[kRowChunk];
+  __shared__ uint16_t s_list[kRowChunk];
   __shared__ long long s_base[4];
   __shared__ unsigned long long sbuf[kWarps + 1];
   const long long pool = blockIdx.y;
-  const int n = rows_chunk_plan(bits + pool * U, U, n_chunks, cnt, pool, GPU, sp, true, s_ent, s_w, s_base, sbuf);
+  unsigned long long per_slot;
+  rows_chunk_plan(bits + pool * U, U, n_chunks, cnt, pool, GPU, sp, true, s_ent, s_w, s_base, sbuf, s_list, &per_slot);
   const uint16_t* Xc = X + (pool * U + static_cast<long long>(blockIdx.x) * kRowChunk) * DH;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, sub = lane >> 3, l8 = lane & 7;
-  const int ng = n * GPU;
-  // a warp takes 4 consecutive groups per step, two steps' loads in flight
-  for (int gb = warp * 4; gb < ng; gb += 2 * kWarps * 4) {
-    uint4 raw[2];
-    int gl[2], s[2], w[2], ent[2];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, sub = lane >> 2, l4 = lane & 3;
+  // per slot: its units, first list entry and first work item
+  int n_sl[4], list0[4], item0[5];
+  list0[0] = 0;
+  item0[0] = 0;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      gl[k] = gb + k * kWarps * 4 + sub;
-      const int ui = gl[k] / GPU;
-      w[k] = gl[k] < ng ? s_w[ui] : 0;
-      ent[k] = gl[k] < ng ? s_ent[ui] : -1;
-      s[k] = width_slot(w[k]);
-      raw[k] = (s[k] >= 0 && ent[k] >= 0) ? __ldg(reinterpret_cast<const uint4*>(Xc + static_cast<long long>(gl[k]) * 64 + l8 * 8))
-                                          : make_uint4(0u, 0u, 0u, 0u);
+  for (int q = 0; q < 4; ++q) {
+    n_sl[q] = static_cast<int>((per_slot >> (16 * q)) & 0xFFFFull);
+    if (q < 3) list0[q + 1] = list0[q] + n_sl[q];
+    item0[q + 1] = item0[q] + (n_sl[q] + kItemUnits - 1) / kItemUnits;
+  }
+  for (int it = warp; it < item0[4]; it += kWarps) {
+    const int slot = (it >= item0[1]) + (it >= item0[2]) + (it >= item0[3]);
+    int ns = 0, l0 = 0, i0 = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (q == slot) ns = n_sl[q], l0 = list0[q], i0 = item0[q];
+    uint4 raw[kRowSteps][2];
+    int ent[kRowSteps];
+#pragma unroll
+    for (int k = 0; k < kRowSteps; ++k) {
+      const int j = (it - i0) * kItemUnits + k * kStepUnits + sub / GPU;  // place in the slot's list
+      const int ui = j < ns ? s_list[l0 + j] : -1;
+      ent[k] = ui >= 0 ? s_ent[ui] : -1;
+      raw[k][0] = raw[k][1] = make_uint4(0u, 0u, 0u, 0u);
+      if (ent[k] >= 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(Xc + static_cast<long long>(ui) * DH + (sub % GPU) * 64 + l4 * 16);
+        raw[k][0] = __ldg(src);
+        raw[k][1] = __ldg(src + 1);
+      }
     }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const bool act = s[k] >= 0 && ent[k] >= 0;
-      unsigned long long packed = 0ull;
-      uint16_t sb = 0;
-      bool ovf = false;
-      float x[8];
-      bf16x8(raw[k], x);
-      if (__any_sync(0xFFFFFFFFu, act && w[k] != 16)) {
-        // every lane takes part in the group maxima; inactive groups hold zeros
-        packed = quantize_lane8(x, (act && w[k] != 16) ? w[k] : 8, &sb, &ovf);
-      }
-      if (act) {
-        const long long grp = static_cast<long long>(ent[k]) * GPU + gl[k] % GPU;  // group in the pool's stream
-        const long long gg = pool * sp.cap_groups[s[k]] + grp;
-        if (w[k] != 16 && l8 == 0) {
-          sp.scales[s[k]][gg] = sb;
-          if (ovf) record_error(KVS_ERR_RANGE);
-        }
-        store_lane8(sp.codes[s[k]] + gg * (8 * w[k]), w[k], l8, packed, raw[k]);
-      }
+    switch (slot) {
+      case 0: pack_rows_steps<2, GPU>(sp, pool, 0, l4, sub % GPU, raw, ent); break;
+      case 1: pack_rows_steps<4, GPU>(sp, pool, 1, l4, sub % GPU, raw, ent); break;
+      case 2: pack_rows_steps<8, GPU>(sp, pool, 2, l4, sub % GPU, raw, ent); break;
+      default: pack_rows_steps<16, GPU>(sp, pool, 3, l4, sub % GPU, raw, ent); break;
     }
   }
 }
@@ -716,27 +759,20 @@ constexpr int kChanThreads = 256;
 template <int DH>
 __host__ __device__ constexpr int chan_groups_per_cta() { return 8 / (DH / 64); }
 
-// w bytes of codes at byte offset o*w of a group's block (width 16: the raw 8 bf16 values)
-__device__ __forceinline__ void store_octet(uint8_t* group_base, const int w, const int o, const unsigned long long packed,
-                                            const uint4 raw) {
-  switch (w) {
-    case 2: reinterpret_cast<uint16_t*>(group_base)[o] = static_cast<uint16_t>(packed); break;
-    case 4: reinterpret_cast<uint32_t*>(group_base)[o] = static_cast<uint32_t>(packed); break;
-    case 8: reinterpret_cast<unsigned long long*>(group_base)[o] = packed; break;
-    default: {  // 8-byte aligned streams: two 8-byte stores
-      uint2* p = reinterpret_cast<uint2*>(group_base) + 2 * o;
-      p[0] = make_uint2(raw.x, raw.y);
-      p[1] = make_uint2(raw.z, raw.w);
-    }
-  }
-}
-
 // grid (ceil(ceil(N/64) / TG), pools * Hkv).  The codes of a warp's 64
 // channel blocks are staged in shared memory and then written block by block,
 // eight lanes per block (16 bytes a lane), so each store instruction writes
-// four contiguous blocks instead of 32 scattered pieces.
+// four contiguous blocks instead of 32 scattered pieces.  In the stage, the
+// 16-byte chunk j of channel slot cl's 128-byte block sits at chunk
+// j ^ ((cl / 2) mod 8): the lanes' stores of one octet (channel slots 2 apart)
+// then spread over eight bank groups instead of one.
 template <int DH>
 __host__ __device__ constexpr size_t chan_pack_smem() { return static_cast<size_t>(kChanThreads / 32) * 64 * 128; }
+
+// byte b of channel slot cl's block in a warp's stage
+__device__ __forceinline__ int stage_off(const int cl, const int b) {
+  return cl * 128 + ((((b >> 4) ^ (cl >> 1)) & 7) << 4) + (b & 15);
+}
 
 template <int DH>
 __global__ void __launch_bounds__(kChanThreads) pack_channels_kernel(const uint16_t* __restrict__ X, const int N,
@@ -799,26 +835,42 @@ __global__ void __launch_bounds__(kChanThreads) pack_channels_kernel(const uint1
     sc[h] = __half2float(shalf);
     sp.scales[s][gg] = __half_as_ushort(shalf);
     if (isinf(sc[h])) record_error(KVS_ERR_RANGE);
-    if (sc[h] > 0.f && !isinf(sc[h])) rc[h] = __frcp_rn(sc[h]);
+    if (sc[h] > 0.f && !isinf(sc[h])) rc[h] = quant_recip(sc[h], w);
   }
-  uint8_t* blk0 = stage + (2 * lane) * 128;
-  uint8_t* blk1 = blk0 + 128;
+  // each channel of the pair in turn: widths 2 / 4 / 8 share one instruction
+  // stream (constants in registers), width 16 copies the raw values
 #pragma unroll
-  for (int o = 0; o < 8; ++o) {
-    uint32_t vo[8];
+  for (int h = 0; h < 2; ++h) {
+    const int cl = 2 * lane + h;
+    const int w = wd[h];
+    if (w == 16) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) vo[e] = v[8 * o + e];
-    unsigned long long q0 = 0ull, q1 = 0ull;
-    if (__any_sync(0xFFFFFFFFu, rc[0] != 0.f || rc[1] != 0.f))
-      quantize_octet_pair(vo, wd[0], wd[1], sc[0], sc[1], rc[0], rc[1], &q0, &q1);
-    if (rc[0] == 0.f) q0 = 0ull;  // an all-zero group (or width 16 / 0: not used)
-    if (rc[1] == 0.f) q1 = 0ull;
-    const uint4 raw0 = make_uint4((vo[0] & 0xFFFFu) | (vo[1] << 16), (vo[2] & 0xFFFFu) | (vo[3] << 16),
-                                  (vo[4] & 0xFFFFu) | (vo[5] << 16), (vo[6] & 0xFFFFu) | (vo[7] << 16));
-    const uint4 raw1 = make_uint4((vo[0] >> 16) | (vo[1] & 0xFFFF0000u), (vo[2] >> 16) | (vo[3] & 0xFFFF0000u),
-                                  (vo[4] >> 16) | (vo[5] & 0xFFFF0000u), (vo[6] >> 16) | (vo[7] & 0xFFFF0000u));
-    if (wd[0]) store_octet(blk0, wd[0], o, q0, raw0);
-    if (wd[1]) store_octet(blk1, wd[1], o, q1, raw1);
+      for (int o = 0; o < 8; ++o) {
+        uint32_t r4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // the channel's halves of two tokens
+          r4[k] = h ? __byte_perm(v[8 * o + 2 * k], v[8 * o + 2 * k + 1], 0x7632)
+                    : __byte_perm(v[8 * o + 2 * k], v[8 * o + 2 * k + 1], 0x5410);
+        *reinterpret_cast<uint4*>(stage + stage_off(cl, 16 * o)) = make_uint4(r4[0], r4[1], r4[2], r4[3]);
+      }
+    } else if (w != 0) {
+      const DynCode c = dyn_code(w);
+      const float scl = sc[h], rcp = rc[h];
+#pragma unroll
+      for (int o = 0; o < 8; ++o) {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = h ? bf16_hi(v[8 * o + e]) : bf16_lo(v[8 * o + e]);
+        const unsigned long long packed = rcp != 0.f ? quantize_octet_dyn(x, scl, rcp, c) : 0ull;
+        uint8_t* dst = stage + stage_off(cl, o * w);
+        if (w == 2)
+          *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
+        else if (w == 4)
+          *reinterpret_cast<uint32_t*>(dst) = static_cast<uint32_t>(packed);
+        else
+          *reinterpret_cast<unsigned long long*>(dst) = packed;
+      }
+    }
   }
   __syncwarp();
   // the staged blocks, four channels per step, eight lanes per block
@@ -828,7 +880,7 @@ __global__ void __launch_bounds__(kChanThreads) pack_channels_kernel(const uint1
     const int cl = c4 + sub;
     const int w = s_wd[warp][cl];
     if (2 * l8 < w)  // a block is 8w bytes: w/2 chunks of 16
-      *reinterpret_cast<uint4*>(s_dst[warp][cl] + 16 * l8) = *reinterpret_cast<const uint4*>(stage + cl * 128 + 16 * l8);
+      *reinterpret_cast<uint4*>(s_dst[warp][cl] + 16 * l8) = *reinterpret_cast<const uint4*>(stage + stage_off(cl, 16 * l8));
   }
 }
 

@@ -226,6 +226,62 @@ def test_pack_dequant_bit_exact(Hkv, N, d):
     assert L.device_error() == 0
 
 
+QMAX = {2: 1, 4: 7, 8: 127, 16: 7}
+
+
+def _tie_group(rng, w, n=64):
+    """64 bf16-exact values whose group maximum is qmax * s with s a power of two,
+    so that x / s lands exactly on half integers for about half of them (ties)."""
+    qm = QMAX[w]
+    s = 2.0 ** int(rng.integers(-6, 7))
+    sign = rng.choice([-1.0, 1.0], size=n)
+    tie = (rng.integers(0, qm, size=n) + 0.5) * s                    # (n + 1/2) s: 8 significant bits at most
+    grid = 2 ** int(np.floor(np.log2(255 / qm)))                      # qmax * grid < 256: 8 bits
+    other = np.floor(rng.random(n) * qm * grid) / grid * s           # on a fine grid below qmax s
+    g = np.where(rng.random(n) < 0.5, tie, other) * sign
+    g[rng.integers(0, n)] = qm * s * rng.choice([-1.0, 1.0])         # the group maximum
+    return g
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_pack_exact_ties_bit_exact(d):
+    """Elements exactly halfway between two codes, at every width and on both axes:
+    each must take the even code, as round-half-even of x / s does."""
+    Hkv, N = 2, 640
+    rng = np.random.default_rng(11 + d)
+    # V (rows): every row of width w is made of tie groups for that width
+    bits_v = rng.choice([2, 4, 8, 16], size=Hkv * N).astype(np.uint8)
+    X = np.zeros((Hkv, N, d))
+    for u in range(Hkv * N):
+        for g0 in range(0, d, 64):
+            X[u // N, u % N, g0:g0 + 64] = _tie_group(rng, int(bits_v[u]))
+    Xt = torch.from_numpy(X).float().bfloat16()
+    assert np.array_equal(f64(Xt), X)                                 # every value is bf16-exact
+    st = L.Streams(Hkv, N, d, 0, int(bits_v.astype(int).sum()), DEV)
+    bv = torch.from_numpy(bits_v).to(DEV)
+    L.quantize_pack(Xt.to(DEV), 0, bv, None, st)
+    ref_v = O.quantize_pack(X, 0, bits_v)
+    _cmp_streams(st, ref_v)
+    assert np.array_equal(L.dequantize(st, bv, None).cpu().numpy(), O.dequantize(ref_v, X.shape, 0, bits_v))
+    # K (channels over the kept tokens; every token kept): each channel's 64-token groups are tie groups
+    bits_k = rng.choice([2, 4, 8, 16], size=Hkv * d).astype(np.uint8)
+    Y = np.zeros((Hkv, N, d))
+    for h in range(Hkv):
+        for c in range(d):
+            for t0 in range(0, N, 64):
+                Y[h, t0:t0 + 64, c] = _tie_group(rng, int(bits_k[h * d + c]), min(64, N - t0))
+    Yt = torch.from_numpy(Y).float().bfloat16()
+    assert np.array_equal(f64(Yt), Y)
+    keep = np.ones((Hkv, N), dtype=bool)
+    sk = L.Streams(Hkv, N, d, 1, int(bits_k.astype(int).sum()), DEV)
+    bk = torch.from_numpy(bits_k).to(DEV)
+    L.quantize_pack(Yt.to(DEV), 1, bk, bv, sk)
+    ref_k = O.quantize_pack(Y, 1, bits_k, keep)
+    _cmp_streams(sk, ref_k)
+    assert np.array_equal(L.dequantize(sk, bk, bv).cpu().numpy(), O.dequantize(ref_k, Y.shape, 1, bits_k, keep))
+    assert L.device_error() == 0
+
+
 def test_pack_scale_overflow_is_reported():
     X = torch.zeros(1, 64, 64)
     X[0, 3, 5] = 2.0 ** 100
