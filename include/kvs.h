@@ -183,6 +183,9 @@ int kvs_channel_stats(const uint16_t* Q, const uint16_t* K, const uint8_t* keep_
 #define KVS_WIDTHS_KEEP_OR_EVICT  (1u << 16)
 
 size_t kvs_allocate_workspace_size(int64_t U);
+/* Workspace bytes that let kvs_allocate_bits_pools solve n_pools pools of U
+ * units side by side (never less than kvs_allocate_workspace_size(U)). */
+size_t kvs_allocate_pools_workspace_size(int64_t n_pools, int64_t U);
 
 /* min sum_u w_u sigma_u 2^-b_u  s.t.  sum_u b_u <= budget_bits, b_u in the
  * width set   [RDKV §2.1 objective; §2.2 reverse water-filling / Lagrangian
@@ -204,9 +207,12 @@ int kvs_allocate_bits(const float* w, const float* sigma, int64_t U, int64_t bud
  * own with the same budget_bits and width set (one pool = one (layer,
  * sequence) of a batch   [RDKV §2.2: one allocation per cache]).  Results are
  * bit for bit those of n_pools kvs_allocate_bits calls.  Pools that fit one
- * thread-block cluster run side by side on the GPU; larger ones run one
- * after the other on the stream, sharing the workspace
- * (kvs_allocate_workspace_size(U) bytes).  n_pools < 65536. */
+ * thread-block cluster run side by side on the GPU, one cluster each.  Larger
+ * ones run side by side too, as one cooperative grid with a row of blocks per
+ * pool, when the workspace holds kvs_allocate_pools_workspace_size(n_pools,
+ * U) bytes and the pools' blocks fit on the GPU at once; otherwise they run
+ * one after the other on the stream, sharing a workspace of
+ * kvs_allocate_workspace_size(U) bytes.  n_pools < 65536. */
 int kvs_allocate_bits_pools(const float* w, const float* sigma, int64_t n_pools, int64_t U, int64_t budget_bits,
                             uint32_t width_mask, uint8_t* bits, void* workspace, size_t workspace_bytes,
                             void* stream);

@@ -46,6 +46,7 @@ SIGNATURES = {
     "kvs_unit_rms_workspace_size": (c_size_t, [c_int64] * 3 + [c_int]),
     "kvs_unit_rms": (c_int, [c_void_p] + [c_int64] * 3 + [c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "kvs_allocate_workspace_size": (c_size_t, [c_int64]),
+    "kvs_allocate_pools_workspace_size": (c_size_t, [c_int64, c_int64]),
     "kvs_allocate_bits": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_uint32, c_void_p, c_void_p, c_size_t,
                                   c_void_p]),
     "kvs_allocate_bits_static": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_uint32, c_void_p, c_void_p]),
@@ -282,7 +283,7 @@ def allocate_bits_pools(w, sigma, budget_bits, width_mask=WIDTHS_ALL, *, out=Non
     P, U = w.shape
     bits = out if out is not None else torch.empty(P, U, dtype=torch.uint8, device=w.device)
     L = lib()
-    buf = _ws(ws, "alloc", L.kvs_allocate_workspace_size(U), w.device)
+    buf = _ws(ws, "alloc", L.kvs_allocate_pools_workspace_size(P, U), w.device)
     _check(L.kvs_allocate_bits_pools(_ptr(w), _ptr(sigma), P, U, int(budget_bits), width_mask, _ptr(bits), _ptr(buf),
                                      buf.numel(), _stream(stream)), "kvs_allocate_bits_pools")
     return bits

@@ -12,12 +12,13 @@
 // keeps taking later items that still fit and whose previous step was taken.
 //
 // B300 design: one cooperative launch, all blocks resident, grid barriers with
-// bounded waits.  Each block computes its units' thetas once (fp64) into
-// shared memory.  lambda* is found exactly by a 6-pass radix select (11-bit
-// digits) on the fp64 bit patterns of theta (positive doubles order like their
-// bit patterns), each pass a cost-weighted 2048-bin histogram; every block then
-// decides the digit redundantly so one barrier per pass suffices.  Ties at lambda* are
-// resolved in unit order by a grid-wide scan; the fix scan is an arg-max
+// bounded waits (several pools side by side: a block row per pool).  Each
+// block computes its units' thetas once (fp64) into shared memory.  lambda*
+// is found exactly by a 6-pass radix select (11-bit digits) on the fp64 bit
+// patterns of theta (positive doubles order like their bit patterns), each
+// pass a cost-weighted 2048-bin histogram; every block then decides the digit
+// redundantly so one barrier per pass suffices.  Ties at lambda* are resolved
+// in unit order by a grid-wide scan; the fix scan is an arg-max
 // (theta, then lowest unit) over each unit's next upgrade, repeated while the
 // leftover budget buys something (at most max_step/min_step rounds).
 #pragma once
@@ -194,18 +195,31 @@ __device__ __forceinline__ FixCand block_best(FixCand best, FixCand* s_cand) {
 template <bool CACHE>
 struct ThetaSource {
   const AllocParams& p;
+  const float* w;                   // the pool's weights and sigmas
+  const float* sigma;
   const unsigned long long* cache;  // [K][per]
   long long u_begin;
   __device__ __forceinline__ unsigned long long operator()(long long u, int k) const {
     if (CACHE) return cache[static_cast<long long>(k) * p.per + (u - u_begin)];
-    return theta_bits(p, p.w[u], p.sigma[u], k);
+    return theta_bits(p, w[u], sigma[u], k);
   }
 };
 
+// grid (blocks per pool, pools): block row q solves pool q (units q*U ..) on
+// its own slice of the workspace: header q, histograms q, and the per-block
+// tie and candidate arrays of row q; its grid barriers count that row only.
 template <bool CACHE>
 __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocParams p) {
   pdl_wait();  // inputs may come from the previous kernel on the stream
   pdl_trigger();
+  // the block row's pool (pointers only: the parameters stay in parameter space)
+  const long long q = blockIdx.y;
+  const float* const pw = p.w + q * p.U;
+  const float* const psig = p.sigma + q * p.U;
+  uint8_t* const pbits = p.bits + q * p.U;
+  unsigned long long* const phist = p.hist + q * kRadixPasses * kRadixBins;
+  unsigned long long* const ptie = p.tie_block + q * gridDim.x;
+  FixCand* const pcand = p.cand + q * kMaxFixRounds * gridDim.x;
   extern __shared__ unsigned long long s_theta[];  // [K][per] when CACHE
   __shared__ unsigned s_hist[kRadixBins];          // per-block cost per bin (< 2^32: units per block x 16)
   __shared__ unsigned long long s_red[kAllocThreads / 32];
@@ -219,8 +233,8 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
   const int nb = gridDim.x, b = blockIdx.x, tid = threadIdx.x;
   const long long u_begin = static_cast<long long>(b) * p.per;
   const long long u_end = min(p.U, u_begin + p.per);
-  AllocHeader* H = p.hdr;
-  const ThetaSource<CACHE> theta{p, s_theta, u_begin};
+  AllocHeader* H = p.hdr + q;
+  const ThetaSource<CACHE> theta{p, pw, psig, s_theta, u_begin};
 
   if (tid < 17) s_lvl_of_width[tid] = -1;
   __syncthreads();
@@ -228,14 +242,14 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
   // the first pass's global histogram starts at zero (later ones are cleared
   // one pass ahead, see below)
   if (b == 0)
-    for (int i = tid; i < kRadixBins; i += kAllocThreads) p.hist[i] = 0ull;
+    for (int i = tid; i < kRadixBins; i += kAllocThreads) phist[i] = 0ull;
 
   // ---- phase 0: validate, cache thetas, total cost of positive items ------
   unsigned long long my_total = 0;
   int my_bad = 0;
   const int full_cost = p.width[p.K];
   for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) {
-    const float wf = p.w[u], sf = p.sigma[u];
+    const float wf = pw[u], sf = psig[u];
     if (!(isfinite(wf) && isfinite(sf) && wf >= 0.f && sf >= 0.f)) my_bad = 1;
     const double key = static_cast<double>(wf) * static_cast<double>(sf);
     if (key > 0.0) my_total += static_cast<unsigned long long>(full_cost);
@@ -258,12 +272,12 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
   }
   if (bad) {
     if (b == 0 && tid == 0) record_error(KVS_ERR_RANGE);
-    for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) p.bits[u] = 0;
+    for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) pbits[u] = 0;
     return;
   }
   if (total <= p.B) {  // every upgrade fits
     for (long long u = u_begin + tid; u < u_end; u += kAllocThreads)
-      p.bits[u] = theta(u, 0) != 0ull ? static_cast<uint8_t>(full_cost) : 0;
+      pbits[u] = theta(u, 0) != 0ull ? static_cast<uint8_t>(full_cost) : 0;
     return;
   }
 
@@ -275,7 +289,7 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
     for (int i = tid; i < kRadixBins; i += kAllocThreads) s_hist[i] = 0;
     // the next pass's global histogram is idle until the barrier below
     if (b == nb - 1 && pass + 1 < kRadixPasses)
-      for (int i = tid; i < kRadixBins; i += kAllocThreads) p.hist[(pass + 1) * kRadixBins + i] = 0ull;
+      for (int i = tid; i < kRadixBins; i += kAllocThreads) phist[(pass + 1) * kRadixBins + i] = 0ull;
     __syncthreads();
     // Early passes see the exponent bits, which nearly all thetas share: the
     // lanes of a warp that fall in one bin are merged first (match_any), so a
@@ -295,7 +309,7 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
     const bool single = nb == 1;  // one block: its histogram is the whole histogram
     if (!single) {
       for (int i = tid; i < kRadixBins; i += kAllocThreads)
-        if (s_hist[i]) atomicAdd(&p.hist[pass * kRadixBins + i], static_cast<unsigned long long>(s_hist[i]));
+        if (s_hist[i]) atomicAdd(&phist[pass * kRadixBins + i], static_cast<unsigned long long>(s_hist[i]));
       if (!grid_barrier(&H->sync, nb)) return;
     }
     {
@@ -303,7 +317,7 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
       // (descending); a scan over threads gives the cost of all higher digits, and
       // the first thread whose range pushes the running cost past B holds lambda*
       unsigned long long h[kBinsPerThread], mine = 0;
-      const unsigned long long* hp = p.hist + pass * kRadixBins;
+      const unsigned long long* hp = phist + pass * kRadixBins;
 #pragma unroll
       for (int j = 0; j < kBinsPerThread; ++j) {
         const int bin = kRadixBins - 1 - (tid * kBinsPerThread + j);
@@ -344,10 +358,10 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
   unsigned long long carry = above;
   if (nb > 1) {
     const unsigned long long blk_tie = block_sum(my_tie, s_red);
-    if (tid == 0) p.tie_block[b] = blk_tie;
+    if (tid == 0) ptie[b] = blk_tie;
     if (!grid_barrier(&H->sync, nb)) return;
     unsigned long long e = 0;
-    for (int i = tid; i < b; i += kAllocThreads) e += ld_vol(&p.tie_block[i]);
+    for (int i = tid; i < b; i += kAllocThreads) e += ld_vol(&ptie[i]);
     carry += block_sum(e, s_red);
   }
   for (long long base = u_begin; base < u_end; base += kAllocThreads) {
@@ -369,7 +383,7 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
         if (cum <= p.B) ++lvl;
         else if (cum - tie <= p.B) H->first_cut = cum - tie;  // exactly one item: the first misfit
       }
-      p.bits[u] = static_cast<uint8_t>(p.width[lvl]);
+      pbits[u] = static_cast<uint8_t>(p.width[lvl]);
     }
     carry += chunk_total;
   }
@@ -385,7 +399,7 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
     if (R < p.min_cost) break;
     FixCand best = {0ull, 0ll, 0, 0};
     for (long long u = u_begin + tid; u < u_end; u += kAllocThreads) {
-      const int lvl = s_lvl_of_width[p.bits[u]];
+      const int lvl = s_lvl_of_width[pbits[u]];
       if (lvl < 0 || lvl >= p.K || p.cost[lvl] > R) continue;
       const unsigned long long th = theta(u, lvl);
       if (th == 0ull) continue;
@@ -399,11 +413,11 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
         s_flag = best.theta != 0ull;
       }
     } else {
-      if (tid == 0) p.cand[it * nb + b] = best;
+      if (tid == 0) pcand[it * nb + b] = best;
       if (!grid_barrier(&H->sync, nb)) return;
       FixCand bb = {0ull, 0ll, 0, 0};
       for (int i = tid; i < nb; i += kAllocThreads) {
-        const volatile FixCand* vc = &p.cand[it * nb + i];
+        const volatile FixCand* vc = &pcand[it * nb + i];
         FixCand c2 = {vc->theta, vc->u, vc->cost, 0};
         if (c2.theta != 0ull && (bb.theta == 0ull || cand_better(c2, bb))) bb = c2;
       }
@@ -417,8 +431,8 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(const AllocPara
     if (!s_flag) break;
     const long long ub = s_best.u;
     if (ub >= u_begin && ub < u_end && tid == static_cast<int>((ub - u_begin) % kAllocThreads)) {
-      const int lvl = s_lvl_of_width[p.bits[ub]];
-      p.bits[ub] = static_cast<uint8_t>(p.width[lvl + 1]);
+      const int lvl = s_lvl_of_width[pbits[ub]];
+      pbits[ub] = static_cast<uint8_t>(p.width[lvl + 1]);
     }
     R -= s_best.cost;
     __syncthreads();

@@ -41,12 +41,13 @@ inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 int alloc_blocks_max() { return sm_count() * 8; }
 constexpr long long kAllocUnitsPerBlock = 2048;
 
-size_t alloc_ws_bytes(int nb) {
+// workspace of the grid allocator for `pools` pools of nb blocks each
+size_t alloc_ws_bytes(long long nb, long long pools = 1) {
   WsCarver c{nullptr, 0, 0};
-  c.take<AllocHeader>(1);
-  c.take<unsigned long long>(static_cast<size_t>(kRadixPasses) * kRadixBins);
-  c.take<unsigned long long>(nb);
-  c.take<FixCand>(static_cast<size_t>(kMaxFixRounds) * nb);
+  c.take<AllocHeader>(static_cast<size_t>(pools));
+  c.take<unsigned long long>(static_cast<size_t>(pools) * kRadixPasses * kRadixBins);
+  c.take<unsigned long long>(static_cast<size_t>(pools * nb));
+  c.take<FixCand>(static_cast<size_t>(pools) * kMaxFixRounds * nb);
   return c.used;
 }
 
@@ -523,6 +524,14 @@ size_t kvs_allocate_workspace_size(int64_t U) {
   return alloc_ws_bytes(alloc_blocks_max());
 }
 
+size_t kvs_allocate_pools_workspace_size(int64_t n_pools, int64_t U) {
+  const size_t one = alloc_ws_bytes(alloc_blocks_max());
+  if (n_pools <= 1 || U <= 0) return one;
+  // the side-by-side grid: at most every block the GPU holds at once, over the pools
+  const long long nb = std::max<long long>(1, static_cast<long long>(alloc_blocks_max()) / n_pools);
+  return std::max(one, alloc_ws_bytes(nb, n_pools));
+}
+
 }  // extern "C"
 
 namespace {
@@ -601,6 +610,41 @@ int plan_alloc(long long U, int K, AllocPlan* ap) {
   return KVS_OK;
 }
 
+// Several pools too large for one cluster, solved at once: one cooperative
+// grid with a block row per pool.  Thetas stay cached in shared memory when
+// every pool's blocks fit on the GPU together with their caches, and are
+// recomputed from w and sigma in every pass otherwise.  nb = 0: the pools do
+// not fit side by side (they then run one after the other).
+struct MultiAllocPlan {
+  long long nb, per;
+  bool cached;
+};
+
+int plan_alloc_multi(long long U, int K, long long n_pools, MultiAllocPlan* mp) {
+  std::memset(mp, 0, sizeof(*mp));
+  const int sms = sm_count();
+  const size_t cache_smem = static_cast<size_t>(kAllocUnitsPerBlock) * K * sizeof(unsigned long long);
+  KVS_CUDA_TRY(allow_smem(allocate_kernel<true>, cache_smem));
+  int occ_c = 0, occ_u = 0;
+  KVS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_c, allocate_kernel<true>, kAllocThreads, cache_smem));
+  KVS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_u, allocate_kernel<false>, kAllocThreads, 0));
+  const long long nb_c = std::max<long long>(1, cdiv(U, kAllocUnitsPerBlock));
+  if (nb_c * n_pools <= static_cast<long long>(occ_c) * sms) {
+    mp->nb = nb_c;
+    mp->cached = true;
+  } else {
+    mp->nb = std::min<long long>(cdiv(U, kAllocThreads), static_cast<long long>(occ_u) * sms / n_pools);
+    mp->cached = false;
+  }
+  if (mp->nb < 1 || mp->nb > 65535) {
+    mp->nb = 0;
+    return KVS_OK;
+  }
+  mp->per = cdiv(U, mp->nb);
+  if (mp->per * 16 >= (1ll << 32)) mp->nb = 0;  // per-block histogram counts are 32-bit
+  return KVS_OK;
+}
+
 int allocate_pools(const float* w, const float* sigma, int64_t n_pools, int64_t U, int64_t budget_bits,
                    uint32_t width_mask, uint8_t* bits, void* workspace, size_t workspace_bytes, void* stream) {
   if (U < 0 || budget_bits < 0 || n_pools < 0) return KVS_ERR_INVALID_ARG;
@@ -629,6 +673,31 @@ int allocate_pools(const float* w, const float* sigma, int64_t n_pools, int64_t 
     KVS_CUDA_TRY(launch_k(cluster_alloc_fn(ap.CL), dim3(static_cast<unsigned>(ap.CL * n_pools)), dim3(kCAThreads),
                           ap.ca_smem, st, ap.CL, p, ap.cand_cap));
     return KVS_OK;
+  }
+  if (n_pools > 1 && workspace) {
+    MultiAllocPlan mp;
+    rc = plan_alloc_multi(U, p.K, n_pools, &mp);
+    if (rc) return rc;
+    if (mp.nb > 0 && alloc_ws_bytes(mp.nb, n_pools) <= workspace_bytes) {
+      p.per = mp.per;
+      WsCarver c{static_cast<char*>(workspace), 0, workspace_bytes};
+      p.hdr = c.take<AllocHeader>(static_cast<size_t>(n_pools));
+      p.hist = c.take<unsigned long long>(static_cast<size_t>(n_pools) * kRadixPasses * kRadixBins);
+      p.tie_block = c.take<unsigned long long>(static_cast<size_t>(n_pools * mp.nb));
+      p.cand = c.take<FixCand>(static_cast<size_t>(n_pools) * kMaxFixRounds * mp.nb);
+      KVS_CUDA_TRY(cudaMemsetAsync(p.hdr, 0, static_cast<size_t>(n_pools) * sizeof(AllocHeader), st));
+      void* args[] = {&p};
+      const dim3 grid(static_cast<unsigned>(mp.nb), static_cast<unsigned>(n_pools));
+      if (mp.cached) {
+        const size_t smem = static_cast<size_t>(p.per) * p.K * sizeof(unsigned long long);
+        KVS_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(allocate_kernel<true>), grid,
+                                                 dim3(kAllocThreads), args, smem, st));
+      } else {
+        KVS_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(allocate_kernel<false>), grid,
+                                                 dim3(kAllocThreads), args, 0, st));
+      }
+      return KVS_OK;
+    }
   }
   // a cooperative grid per pool, one pool after the other on the stream (they
   // share the workspace): a few thousand units per block with their thetas

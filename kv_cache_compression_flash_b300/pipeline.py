@@ -69,7 +69,7 @@ class RdkvLayerStep:
             "score12": L.kvs_score_workspace_size(HQ, HKV, W, N, d, 0, N - W, self.BOTH_MODE),
             "cw": L.kvs_channel_weights_workspace_size(HQ, HKV, W, N, d),
             "rms0": 256, "rms1": L.kvs_unit_rms_workspace_size(HKV, N, d, 1),
-            "av": L.kvs_allocate_workspace_size(self.U_v), "ak": L.kvs_allocate_workspace_size(self.U_k),
+            "av": L.kvs_allocate_pools_workspace_size(P, self.U_v), "ak": L.kvs_allocate_pools_workspace_size(P, self.U_k),
             "pv": L.kvs_pack_pools_workspace_size(P, Hkv, N, d, 0), "pk": L.kvs_pack_pools_workspace_size(P, Hkv, N, d, 1),
             "dv": L.kvs_pack_pools_workspace_size(P, Hkv, N, d, 0), "dk": L.kvs_pack_pools_workspace_size(P, Hkv, N, d, 1),
         }

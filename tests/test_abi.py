@@ -67,6 +67,8 @@ def test_workspace_sizes_and_plan(lib):
     info = L.score_plan_info(32, 8, 512, 8192, 128)
     assert info[0] >= 4 and info[1] >= 1 and info[2] >= 4 and info[3] >= 1 and info[4] >= 3
     assert lib.kvs_allocate_workspace_size(1000) > 0
+    assert lib.kvs_allocate_pools_workspace_size(16, 131072) >= lib.kvs_allocate_workspace_size(131072)
+    assert lib.kvs_allocate_pools_workspace_size(1, 1000) == lib.kvs_allocate_workspace_size(1000)
     assert lib.kvs_pack_workspace_size(8, 8192, 128, 0) > 0          # token units need no scratch
     assert lib.kvs_pack_workspace_size(8, 8192, 128, 1) >= 8 * 8192 * 4  # kept-token index per head
 

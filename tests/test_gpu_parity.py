@@ -438,10 +438,12 @@ def test_pooled_step_vs_oracle(P, Hq, Hkv, W, N, d):
         assert np.array_equal(L.dequantize(vs.pool(q), bits_v[q], None).cpu().numpy(), vh[q].cpu().numpy())
 
 
-@pytest.mark.parametrize("U,P", [(1000, 5), (70000, 3), (400000, 2)])
+@pytest.mark.parametrize("U,P", [(1000, 5), (70000, 3), (400000, 2), (131072, 4), (131072, 16)])
 def test_pooled_allocation_matches_single_calls(U, P):
-    """allocate_bits_pools equals one allocate_bits call per pool, on the
-    cluster path and (400 000 units) on the cooperative-grid path."""
+    """allocate_bits_pools equals one allocate_bits call per pool: on the
+    cluster path (1000, 70 000 units), and on the side-by-side cooperative grid
+    with the thetas cached (400 000 x 2, 131 072 x 4) and recomputed in every
+    pass (131 072 x 16: too many blocks for every pool's cache at once)."""
     rng = np.random.default_rng(U + P)
     w = (rng.random((P, U)) ** 3 * 10).astype(np.float32)
     s = (rng.random((P, U)) + 0.05).astype(np.float32)
@@ -453,4 +455,13 @@ def test_pooled_allocation_matches_single_calls(U, P):
         got = L.allocate_bits_pools(wd, sd, B)
         for q in range(P):
             assert torch.equal(got[q], L.allocate_bits(wd[q], sd[q], B)), (avg, q)
+    # with only one pool's workspace the pools run one after the other, with the same widths
+    lib = L.lib()
+    small = torch.empty(lib.kvs_allocate_workspace_size(U), dtype=torch.uint8, device=DEV)
+    seq = torch.empty(P, U, dtype=torch.uint8, device=DEV)
+    B = int(math.floor(2.5 * U))
+    rc = lib.kvs_allocate_bits_pools(L._ptr(wd), L._ptr(sd), P, U, B, L.WIDTHS_ALL, L._ptr(seq), L._ptr(small),
+                                     small.numel(), L._stream(None))
+    assert rc == 0
+    assert torch.equal(seq, L.allocate_bits_pools(wd, sd, B))
     assert L.device_error() == 0
