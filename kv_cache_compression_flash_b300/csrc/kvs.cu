@@ -270,10 +270,12 @@ int pack_common(const uint16_t* X, int64_t n_pools, int64_t Hkv, int64_t N, int6
   return KVS_OK;
 }
 
-// cluster size for column reductions over `rows` rows per group
+// cluster size for column reductions over `rows` rows per group: about
+// kColRowsPerCta rows a CTA, at most 16 CTAs
+constexpr long long kColRowsPerCta = 2048;
 int colsq_cluster(long long rows) {
   int cl = 1;
-  while (cl < 16 && static_cast<long long>(cl) * 256 < rows) cl *= 2;
+  while (cl < 16 && static_cast<long long>(cl) * kColRowsPerCta < rows) cl *= 2;
   return cl;
 }
 
@@ -286,6 +288,10 @@ int launch_colsq(const uint16_t* A, long long rows_a, const uint8_t* keep, const
     if (err == cudaSuccess) err = set_cluster_attrs(colsq_cluster_kernel<128, false>);
     if (err == cudaSuccess) err = set_cluster_attrs(colsq_cluster_kernel<64, true>);
     if (err == cudaSuccess) err = set_cluster_attrs(colsq_cluster_kernel<128, true>);
+    if (err == cudaSuccess) err = allow_smem(colsq_cluster_kernel<64, false>, col_ring_bytes<64>());
+    if (err == cudaSuccess) err = allow_smem(colsq_cluster_kernel<128, false>, col_ring_bytes<128>());
+    if (err == cudaSuccess) err = allow_smem(colsq_cluster_kernel<64, true>, col_ring_bytes<64>());
+    if (err == cudaSuccess) err = allow_smem(colsq_cluster_kernel<128, true>, col_ring_bytes<128>());
   });
   if (err != cudaSuccess) return KVS_ERR_CUDA;
   const int cl = colsq_cluster(std::max(rows_a, rows_b));
@@ -293,16 +299,17 @@ int launch_colsq(const uint16_t* A, long long rows_a, const uint8_t* keep, const
   const int ra = static_cast<int>(rows_a), rb = static_cast<int>(rows_b);
   const bool stats = mode == kColChannelStats;
   cudaError_t e;
+  const size_t sm64 = col_ring_bytes<64>(), sm128 = col_ring_bytes<128>();
   if (d == 64)
-    e = stats ? launch_cluster(colsq_cluster_kernel<64, true>, grid, cl, kColThreads, 0, st, A, ra, keep, B, rb, mode,
-                               scale, out, out2)
-              : launch_cluster(colsq_cluster_kernel<64, false>, grid, cl, kColThreads, 0, st, A, ra, keep, B, rb, mode,
-                               scale, out, out2);
+    e = stats ? launch_cluster(colsq_cluster_kernel<64, true>, grid, cl, kColThreads, sm64, st, A, ra, keep, B, rb,
+                               mode, scale, out, out2)
+              : launch_cluster(colsq_cluster_kernel<64, false>, grid, cl, kColThreads, sm64, st, A, ra, keep, B, rb,
+                               mode, scale, out, out2);
   else
-    e = stats ? launch_cluster(colsq_cluster_kernel<128, true>, grid, cl, kColThreads, 0, st, A, ra, keep, B, rb, mode,
-                               scale, out, out2)
-              : launch_cluster(colsq_cluster_kernel<128, false>, grid, cl, kColThreads, 0, st, A, ra, keep, B, rb, mode,
-                               scale, out, out2);
+    e = stats ? launch_cluster(colsq_cluster_kernel<128, true>, grid, cl, kColThreads, sm128, st, A, ra, keep, B, rb,
+                               mode, scale, out, out2)
+              : launch_cluster(colsq_cluster_kernel<128, false>, grid, cl, kColThreads, sm128, st, A, ra, keep, B, rb,
+                               mode, scale, out, out2);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return KVS_ERR_CUDA;
