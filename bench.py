@@ -62,6 +62,8 @@ def parse_args(argv=None):
                     help="time the KV-CoRE Gram accumulation and spectrum of the workload's K cache instead")
     ap.add_argument("--sculpt", action="store_true",
                     help="time KVSculpt's zone targets (block attention) and ridge values instead")
+    ap.add_argument("--chain", action="store_true",
+                    help="time the post-scoring chain of one full-model layer call by call instead")
     return ap.parse_args(argv)
 
 
@@ -735,6 +737,104 @@ def run_core(args):
     return 0
 
 
+def run_chain(args):
+    """The post-scoring chain of one layer of the full-model batch (its 16
+    sequences as pools, or --seqs of them), call by call: each call timed
+    with events, L2 flushed before each (untimed); its algorithmic bytes
+    over its time, against the measured HBM copy rate.  The whole chain as the
+    step runs it (two streams) is timed beside the calls."""
+    import torch
+    from kv_cache_compression_flash_b300 import _lib as L
+    from kv_cache_compression_flash_b300 import synth
+    from kv_cache_compression_flash_b300.pipeline import RdkvLayerStep
+    wl = synth.WORKLOADS[FULL_MODEL]
+    P = args.seqs or wl.seqs
+    dev = torch.device("cuda", 0)
+    x = synth.make_pools(wl, 0, range(P), device=dev)
+    Q, K, V = x["Q"], x["K"], x["V"]
+    st = RdkvLayerStep(wl.Hq, wl.Hkv, wl.N, wl.W, wl.d, wl.avg_bits[0], device=dev, n_pools=P)
+    st.run(Q, K, V)
+    torch.cuda.synchronize()
+    if L.device_error() != 0:
+        raise SystemExit("device error")
+    Hq, Hkv, N, W, d = st.shape
+    X4 = (P, Hkv, N, d)
+    bv, bk = st.pool_bits()
+    ws = st.ws
+    calls = [
+        ("sigma_t", lambda: L.unit_rms(V.view(P * Hkv, N, d), 0, out=st.sig_t, ws=ws["rms0"])),
+        ("alloc_v", lambda: L.allocate_bits_pools(st.out["w_t"].view(P, -1), st.sig_t.view(P, -1), st.B_v,
+                                                  out=bv, ws=ws["av"])),
+        ("channel_stats", lambda: L.channel_stats(Q.view(P * Hq, W, d), K.view(P * Hkv, N, d), st.bits_v,
+                                                  out_wc=st.w_c, out_sigma=st.sig_c)),
+        ("alloc_k", lambda: L.allocate_bits_pools(st.w_c.view(P, -1), st.sig_c.view(P, -1), st.B_k, out=bk,
+                                                  ws=ws["ak"])),
+        ("pack_v", lambda: L.quantize_pack_pools(V.view(X4), 0, st.bits_v, None, st.v_streams, ws=ws["pv"])),
+        ("pack_k", lambda: L.quantize_pack_pools(K.view(X4), 1, st.bits_k, st.bits_v, st.k_streams, ws=ws["pk"])),
+        ("dequant_v", lambda: L.dequantize_pools(st.v_streams, st.bits_v, None, out=st.v_hat.view(X4), ws=ws["dv"])),
+        ("dequant_k", lambda: L.dequantize_pools(st.k_streams, st.bits_k, st.bits_v, out=st.k_hat.view(X4),
+                                                 ws=ws["dk"])),
+        ("chain", lambda: st.rest(Q, K, V)),
+    ]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        for _, f in calls:
+            f()
+    torch.cuda.synchronize()
+    times = {n: [] for n, _ in calls}
+    for _ in range(args.steps):
+        for n, f in calls:
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            f()
+            e1.record()
+            torch.cuda.synchronize()
+            times[n].append(e0.elapsed_time(e1))
+    if L.device_error() != 0:
+        raise SystemExit("device error")
+    # algorithmic bytes: what each call must read and write once
+    U_v, U_k = P * Hkv * N, P * Hkv * d
+    cache = U_v * d * 2                                   # one bf16 cache (K or V) of the layer
+    kept = int((st.bits_v > 0).sum())                     # kept tokens (V rows stored, K columns' length)
+
+    def streams_bytes(s):
+        cnt = s.counts.view(P, 8).sum(0).tolist()         # units, groups per width slot
+        return sum(cnt[4 + i] * 8 * w + (2 * cnt[4 + i] if w < 16 else 0) + 12 * cnt[i]
+                   for i, w in enumerate((2, 4, 8, 16)))
+    sv, sk = streams_bytes(st.v_streams), streams_bytes(st.k_streams)
+    algo = {"sigma_t": cache + 4 * U_v, "alloc_v": 9 * U_v,
+            "channel_stats": cache + P * Hq * W * d * 2 + U_v + 8 * U_k, "alloc_k": 9 * U_k,
+            "pack_v": kept * d * 2 + sv + U_v, "pack_k": kept * d * 2 + sk + U_v + U_k,
+            "dequant_v": sv + U_v + U_v * d * 4, "dequant_k": sk + U_v + U_k + U_v * d * 4}
+    algo["chain"] = sum(algo.values())
+    _, peak_gbs, peak_kind = measured_peaks()
+    out_calls = {}
+    for n, _ in calls:
+        ms = statistics.median(times[n])
+        gbs = algo[n] / (ms * 1e-3) / 1e9
+        out_calls[n] = {"ms": ms, "algorithmic_bytes": algo[n], "GB/s": gbs,
+                        "frac": gbs / peak_gbs if peak_gbs else None}
+    print(json.dumps({
+        "metric": "post-scoring chain of one full-model layer, per call", "value": out_calls["chain"]["ms"],
+        "unit": "ms", "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "dtype": "bf16", "data": "synthetic (seeded, drawn on the device)",
+        "config": {"workload": wl.name, "layer": 0, "pools": P, "Hkv": Hkv, "N": N, "d": d, "avg_bits": wl.avg_bits[0],
+                   "kept_tokens": kept, "l2": "flushed before each call (untimed)"},
+        "peak": {"GB/s": peak_gbs, "kind": f"{peak_kind} copy"}, "calls": out_calls,
+        "gpu_launches": (st.kernel_launches() - scoring_launches(st)) * args.steps,
+    }))
+    return 0
+
+
+def scoring_launches(st):
+    """Launches of one step that belong to its scoring call (not in the chain)."""
+    from kv_cache_compression_flash_b300 import _lib as L
+    Hq, Hkv, N, W, d = st.shape
+    P = st.n_pools
+    return L.score_plan_info(P * Hq, P * Hkv, W, N, d, mode=st.BOTH_MODE)[4]
+
+
 def run_sculpt(args):
     """KVSculpt over the workload's compression zone (all but the window): the
     targets Y and lse of the window queries over the zone (kvs_block_attention)
@@ -1111,11 +1211,14 @@ def log_result(line):
 
 def main(argv=None):
     args = parse_args(argv)
+    side_leg = args.trizone or args.core or args.sculpt or args.chain
     if args.steps is None:
-        args.steps = 10 if (args.workload == FULL_MODEL and not (args.trizone or args.core or args.sculpt)) else 200
+        args.steps = 10 if (args.workload == FULL_MODEL and not side_leg) else 20 if args.chain else 200
     if args.impl == "reference":
         return run_reference(args)
-    if args.workload == FULL_MODEL and not (args.trizone or args.core or args.sculpt):
+    if args.chain:
+        return run_chain(args)
+    if args.workload == FULL_MODEL and not side_leg:
         return run_full_model(args)
     if args.trizone:
         return run_trizone(args)
