@@ -856,19 +856,24 @@ __global__ void __launch_bounds__(kChanThreads) pack_channels_kernel(const uint1
     } else if (w != 0) {
       const DynCode c = dyn_code(w);
       const float scl = sc[h], rcp = rc[h];
+      // the octets' codes (8w bits each) gather in a 64-bit word, stored as
+      // it fills: no branch on the width, one 8-byte store per 64 code bits
+      unsigned long long word = 0ull;
+      int fill = 0, k = 0;
 #pragma unroll
       for (int o = 0; o < 8; ++o) {
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = h ? bf16_hi(v[8 * o + e]) : bf16_lo(v[8 * o + e]);
         const unsigned long long packed = rcp != 0.f ? quantize_octet_dyn(x, scl, rcp, c) : 0ull;
-        uint8_t* dst = stage + stage_off(cl, o * w);
-        if (w == 2)
-          *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
-        else if (w == 4)
-          *reinterpret_cast<uint32_t*>(dst) = static_cast<uint32_t>(packed);
-        else
-          *reinterpret_cast<unsigned long long*>(dst) = packed;
+        word |= packed << fill;
+        fill += 8 * w;
+        if (fill == 64) {
+          *reinterpret_cast<unsigned long long*>(stage + stage_off(cl, 8 * k)) = word;
+          ++k;
+          word = 0ull;
+          fill = 0;
+        }
       }
     }
   }
