@@ -56,6 +56,9 @@ extern "C" {
 #define KVS_ERR_CUDA         4  /* a CUDA runtime call failed */
 #define KVS_ERR_TIMEOUT      5  /* a bounded device wait ran out */
 #define KVS_ERR_WORKSPACE    6  /* workspace too small or misaligned */
+#define KVS_ERR_BOUNDS       7  /* bounds-checked build only (libkvs_debug.so, compiled with
+                                   KVS_DEBUG): a data-dependent index fell outside its array;
+                                   the access was skipped */
 
 /* Human-readable name of a status code (static string). */
 const char* kvs_status_string(int status);
@@ -276,7 +279,9 @@ typedef struct kvs_stream_set {
     int64_t*  counts;
 } kvs_stream_set;
 
-/* Every codes[i] pointer must be 16-byte aligned (KVS_ERR_INVALID_ARG otherwise). */
+/* Every codes[i] pointer must be 16-byte aligned, and for token units (axis
+ * 0) every cap_groups[i] must be at least cap_units[i] * d / 64 (a stored
+ * token has d / 64 groups); KVS_ERR_INVALID_ARG otherwise. */
 
 /* Host-only: capacities that always suffice for an allocation of at most
  * budget_bits (a unit of width w costs w bits, so at most budget/w units of

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libkvs.so")
 
 KVS_OK = 0
 STATUS = {0: "KVS_OK", 1: "KVS_ERR_INVALID_ARG", 2: "KVS_ERR_UNSUPPORTED", 3: "KVS_ERR_RANGE",
-          4: "KVS_ERR_CUDA", 5: "KVS_ERR_TIMEOUT", 6: "KVS_ERR_WORKSPACE"}
+          4: "KVS_ERR_CUDA", 5: "KVS_ERR_TIMEOUT", 6: "KVS_ERR_WORKSPACE", 7: "KVS_ERR_BOUNDS"}
 
 MODE_LSE = 1
 MODE_RDKV_WT = 2

@@ -17,6 +17,20 @@ __device__ int g_device_error;
 
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_device_error, 0, code); }
 
+// Bounds check of a data-dependent index (a gathered token, a stream entry, a
+// computed head).  In the checked build (KVS_DEBUG defined) a false condition
+// records KVS_ERR_BOUNDS and the caller skips the access; otherwise the
+// condition is not evaluated.  Use: if (kvs_in_bounds(i < n)) a[i] = x;
+#ifdef KVS_DEBUG
+__device__ __forceinline__ bool kvs_in_bounds(const bool ok) {
+  if (!ok) record_error(KVS_ERR_BOUNDS);
+  return ok;
+}
+#define KVS_IN_BOUNDS(cond) ::kvs::kvs_in_bounds(cond)
+#else
+#define KVS_IN_BOUNDS(cond) true
+#endif
+
 // true once any kernel gave up on a wait: later CTAs skip their work so a
 // broken launch ends quickly instead of timing out wave after wave
 __device__ __forceinline__ bool timeout_recorded() {

@@ -257,8 +257,11 @@ int pack_common(const uint16_t* X, int64_t n_pools, int64_t Hkv, int64_t N, int6
   if (!dequant && !s->counts) return KVS_ERR_INVALID_ARG;
   if (X && !aligned16(X)) return KVS_ERR_INVALID_ARG;
   if (out && !aligned16(out)) return KVS_ERR_INVALID_ARG;
-  for (int i = 0; i < 4; ++i)  // the code blocks are written and read 16 bytes at a time
+  for (int i = 0; i < 4; ++i) {  // the code blocks are written and read 16 bytes at a time
     if (!aligned16(s->codes[i])) return KVS_ERR_INVALID_ARG;
+    // a stored token has d / 64 groups: entry k's groups must fit the group arrays
+    if (axis == 0 && s->cap_groups[i] < s->cap_units[i] * (d / 64)) return KVS_ERR_INVALID_ARG;
+  }
   PackWs w;
   if (carve_pack(n_pools, Hkv, N, d, axis, ws, ws_bytes, &w) > ws_bytes || !ws) return KVS_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KVS_ERR_WORKSPACE;
@@ -332,6 +335,7 @@ const char* kvs_status_string(int status) {
     case KVS_ERR_CUDA: return "KVS_ERR_CUDA";
     case KVS_ERR_TIMEOUT: return "KVS_ERR_TIMEOUT";
     case KVS_ERR_WORKSPACE: return "KVS_ERR_WORKSPACE";
+    case KVS_ERR_BOUNDS: return "KVS_ERR_BOUNDS";
     default: return "KVS_ERR_UNKNOWN";
   }
 }

@@ -471,8 +471,10 @@ __device__ __forceinline__ void pack_rows_steps(const StreamPtrs& sp, const long
 #pragma unroll
   for (int k = 0; k < kRowSteps; ++k) {
     const long long gg = pool * sp.cap_groups[slot] + static_cast<long long>(ent[k]) * GPU + gi;
+    // the group's stores (not its shuffles, which every lane joins) are skipped when out of bounds
+    const bool store = ent[k] >= 0 && KVS_IN_BOUNDS(static_cast<long long>(ent[k]) * GPU + gi < sp.cap_groups[slot]);
     if constexpr (W == 16) {
-      if (ent[k] >= 0) {
+      if (store) {
         uint4* dst = reinterpret_cast<uint4*>(sp.codes[3] + gg * 128) + 2 * l4;
         dst[0] = raw[k][0];
         dst[1] = raw[k][1];
@@ -497,7 +499,7 @@ __device__ __forceinline__ void pack_rows_steps(const StreamPtrs& sp, const long
 #pragma unroll
       for (int h = 0; h < W / 2; ++h) words[h] = 0u;
       if (sc > 0.f && !isinf(sc)) quantize_w<W, 16>(x, sc, quant_recip(sc, W), words);
-      if (ent[k] >= 0) {
+      if (store) {
         if (l4 == 0) {
           sp.scales[slot][gg] = __half_as_ushort(sh);
           if (isinf(sc)) record_error(KVS_ERR_RANGE);
@@ -626,7 +628,7 @@ __global__ void __launch_bounds__(kRowThreads) dequant_rows_kernel(const StreamP
     float y[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) y[e] = 0.f;
-    if (s >= 0 && ent >= 0) {
+    if (s >= 0 && ent >= 0 && KVS_IN_BOUNDS(static_cast<long long>(ent) * GPU + gl % GPU < sp.cap_groups[s])) {
       const long long gg = pool * sp.cap_groups[s] + static_cast<long long>(ent) * GPU + gl % GPU;
       dequant_lane8(sp.codes[s] + gg * (8 * w), w, l8, sp.scales[s] + gg, y);
     }
@@ -683,10 +685,13 @@ __global__ void __launch_bounds__(kPlanThreads, 1) channels_plan_kernel(
       int pd = N - 1 - (t0 - pk);                  // next dropped slot, from the end
       const int valid = max(0, min(16, N - t0));
       for (int e = 0; e < valid; ++e) {
-        if (mask & (1u << e))
-          kg[pk++] = t0 + e;
-        else
-          kg[pd--] = t0 + e;
+        if (mask & (1u << e)) {
+          if (KVS_IN_BOUNDS(pk >= 0 && pk < N)) kg[pk] = t0 + e;
+          ++pk;
+        } else {
+          if (KVS_IN_BOUNDS(pd >= 0 && pd < N)) kg[pd] = t0 + e;
+          --pd;
+        }
       }
       carry += step_tot;
     }
@@ -807,7 +812,9 @@ __global__ void __launch_bounds__(kChanThreads) pack_channels_kernel(const uint1
   uint32_t v[64];  // channels c0 (low half) and c0 + 1 (high half) of the group's tokens; zeros past the kept ones
 #pragma unroll
   for (int e = 0; e < 64; ++e)
-    v[e] = e < nr ? __ldg(reinterpret_cast<const uint32_t*>(Xg + static_cast<long long>(s_tok[r0 + e]) * DH)) : 0u;
+    v[e] = (e < nr && KVS_IN_BOUNDS(s_tok[r0 + e] >= 0 && s_tok[r0 + e] < N))
+               ? __ldg(reinterpret_cast<const uint32_t*>(Xg + static_cast<long long>(s_tok[r0 + e]) * DH))
+               : 0u;
   uint32_t amax = 0u;
 #pragma unroll
   for (int e = 0; e < 64; ++e) amax = bf16x2_max(amax, v[e] & 0x7FFF7FFFu);
@@ -821,7 +828,7 @@ __global__ void __launch_bounds__(kChanThreads) pack_channels_kernel(const uint1
     const long long u = static_cast<long long>(g) * DH + c0 + h;
     const int w = bits[u], s = width_slot(w);
     const long long b = chan_base[u];
-    wd[h] = (s >= 0 && b >= 0) ? w : 0;
+    wd[h] = (s >= 0 && b >= 0 && KVS_IN_BOUNDS(b + jb * TG + jg < sp.cap_groups[s])) ? w : 0;
     s_wd[warp][cl] = wd[h];
     sc[h] = 0.f;
     rc[h] = 0.f;
@@ -938,7 +945,9 @@ __global__ void __launch_bounds__(kChanThreads) dequant_channels_kernel(const St
     const int cnt = min(TOK, N - d0);
     for (int e = threadIdx.x; e < cnt * (DH / 4); e += kChanThreads) {
       const int i = e / (DH / 4), c4 = (e % (DH / 4)) * 4;
-      *reinterpret_cast<float4*>(og + static_cast<long long>(kg[d0 + i]) * DH + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int tok = kg[d0 + i];
+      if (KVS_IN_BOUNDS(tok >= 0 && tok < N))
+        *reinterpret_cast<float4*>(og + static_cast<long long>(tok) * DH + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     return;
   }
@@ -959,7 +968,7 @@ __global__ void __launch_bounds__(kChanThreads) dequant_channels_kernel(const St
     const long long u = static_cast<long long>(g) * DH + c0 + h;
     const int w = bits[u], s = width_slot(w);
     const long long b = chan_base[u];
-    wd[h] = (s >= 0 && b >= 0) ? w : 0;
+    wd[h] = (s >= 0 && b >= 0 && KVS_IN_BOUNDS(b + jb * TG + jg < sp.cap_groups[s])) ? w : 0;
     blk[h] = nullptr;
     sc[h] = 0.f;
     if (wd[h]) {
@@ -979,7 +988,8 @@ __global__ void __launch_bounds__(kChanThreads) dequant_channels_kernel(const St
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int i = 8 * o + e;
-      if (i < nr) *reinterpret_cast<float2*>(orow + static_cast<long long>(s_tok[r0 + i]) * DH) = make_float2(y0[e], y1[e]);
+      if (i < nr && KVS_IN_BOUNDS(s_tok[r0 + i] >= 0 && s_tok[r0 + i] < N))
+        *reinterpret_cast<float2*>(orow + static_cast<long long>(s_tok[r0 + i]) * DH) = make_float2(y0[e], y1[e]);
     }
   }
 }

@@ -112,6 +112,21 @@ def test_alloc_and_pack_argument_errors(lib):
     assert lib.kvs_channel_weights(p, p, 8, 3, 16, 64, 128, p, p, 1 << 20, None) == 1
 
 
+def test_pack_rejects_token_capacities_without_room_for_their_groups(lib):
+    # token units at d = 128 have two groups each: cap_groups < 2 cap_units is refused before any launch
+    p = ctypes.c_void_p(1 << 20)
+    s = L.StreamSetC()
+    for i in range(4):
+        s.codes[i] = s.scales[i] = s.unit_ids[i] = s.group_offsets[i] = 1 << 20
+        s.cap_units[i], s.cap_groups[i] = 100, 200
+    s.counts = 1 << 20
+    s.cap_groups[1] = 199
+    assert lib.kvs_quantize_pack(p, 8, 64, 128, 0, p, None, ctypes.byref(s), p, 1 << 20, None) == 1
+    assert lib.kvs_dequantize(ctypes.byref(s), 8, 64, 128, 0, p, None, p, p, 1 << 20, None) == 1
+    # channel units: a group count per unit depends on the kept tokens, so no such rule
+    assert lib.kvs_quantize_pack(p, 8, 64, 128, 1, p, None, ctypes.byref(s), p, 1 << 20, None) == 1  # no keep
+
+
 def test_trizone_sizes_and_argument_errors(lib):
     # header 8 heads x 16 int64 (1 KiB); per 64-token group the first V entry of
     # each width (8 x 129 x 4 int32, padded to 16640 B); one width byte per token
