@@ -989,21 +989,30 @@ int kvs_block_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
   if (n_block < 1 || n_block > N) return KVS_ERR_INVALID_ARG;
   if (!Q || !K || !V || !Y) return KVS_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Y)) return KVS_ERR_INVALID_ARG;
+  // tcgen05: one CTA per 128-row query tile of Gt heads x 128 / Gt positions
   const int G = static_cast<int>(Hq / Hkv);
-  const int Gt = (G == 1 || G == 2 || G == 4) ? G : (G % 4 == 0 ? 4 : 1);  // heads per CTA: 64 / Gt positions each
-  const dim3 grid(static_cast<unsigned>(cdiv(W, 64 / Gt)), static_cast<unsigned>(Hkv * (G / Gt)));
+  const int Gt = G >= 4 ? 4 : G;  // G is 1, 2 or a multiple of 4 (validate_shape)
+  const int Pp = 128 / Gt;
+  const int n_hc = G / Gt, n_pb = static_cast<int>(cdiv(W, Pp));
   const float c_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   cudaStream_t st = as_stream(stream);
-  const int Wi = static_cast<int>(W), Ni = static_cast<int>(N), p0 = static_cast<int>(q_pos0),
-            nb = static_cast<int>(n_block);
+  CUtensorMap mq, mk, mv;
+  rc = make_map_3d(&mq, Q, d, W, Hq, 64, Pp, Gt);
+  if (!rc) rc = make_map_3d(&mk, K, d, N, Hkv, 64, 128, 1);
+  if (!rc) rc = make_map_3d(&mv, V, d, N, Hkv, 64, 128, 1);
+  if (rc) return rc;
+  const dim3 grid(static_cast<unsigned>(Hkv * n_hc * n_pb));
+  const int Wi = static_cast<int>(W), p0 = static_cast<int>(q_pos0), nb = static_cast<int>(n_block);
   if (d == 64) {
-    KVS_CUDA_TRY(allow_smem(block_attention_kernel<64>, BaCfg<64>::kSmem));
-    KVS_CUDA_TRY(launch_k(block_attention_kernel<64>, grid, dim3(kBaThreads), BaCfg<64>::kSmem, st, 0, Q, K, V, G,
-                          Gt, Wi, Ni, p0, nb, c_log2, Y, lse));
+    const size_t smem = sizeof(BtSmem<64>) + 1024;
+    KVS_CUDA_TRY(allow_smem(block_attention_tc_kernel<64>, smem));
+    KVS_CUDA_TRY(launch_k(block_attention_tc_kernel<64>, grid, dim3(kBtThreads), smem, st, 0, mq, mk, mv, G, Gt, Wi,
+                          p0, nb, n_hc, n_pb, c_log2, Y, lse));
   } else {
-    KVS_CUDA_TRY(allow_smem(block_attention_kernel<128>, BaCfg<128>::kSmem));
-    KVS_CUDA_TRY(launch_k(block_attention_kernel<128>, grid, dim3(kBaThreads), BaCfg<128>::kSmem, st, 0, Q, K, V, G,
-                          Gt, Wi, Ni, p0, nb, c_log2, Y, lse));
+    const size_t smem = sizeof(BtSmem<128>) + 1024;
+    KVS_CUDA_TRY(allow_smem(block_attention_tc_kernel<128>, smem));
+    KVS_CUDA_TRY(launch_k(block_attention_tc_kernel<128>, grid, dim3(kBtThreads), smem, st, 0, mq, mk, mv, G, Gt,
+                          Wi, p0, nb, n_hc, n_pb, c_log2, Y, lse));
   }
   KVS_CUDA_TRY(cudaGetLastError());
   return KVS_OK;

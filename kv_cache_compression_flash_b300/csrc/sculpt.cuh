@@ -3,11 +3,9 @@
 // fitted to the block's attention output and LSE; with the keys fixed, the
 // values are a ridge least-squares solution].
 //
-//   block_attention_kernel<DH>  flash-style on the tensor cores (mma.sync
-//       m16n8k16 bf16, fp32 accumulation): 64 query rows of one KV group per
-//       CTA, keys in chunks of 64 staged by cp.async, an online softmax, and
-//       the P V product with P split into bf16 hi + lo so that the weights
-//       keep 16 significant bits.  Row r sees keys t < n_block, t <= q_pos0 + r.
+//   block_attention_tc_kernel<DH>  flash-style on tcgen05 (S and O in TMEM,
+//       P through shared memory into the second MMA; see below).  Row r sees
+//       keys t < n_block, t <= q_pos0 + r.
 //   ridge_softmax_kernel<DH>    A = softmax over all k compressed keys (no
 //       mask: every training query sees the whole compressed block), the
 //       logits on the tensor cores as in the block attention, in two sweeps
@@ -29,16 +27,9 @@ constexpr int kRidgeMaxK = 512;
 constexpr int kRidgeMaxD = 128;
 constexpr int kRidgeSolveThreads = 1024;
 
-// ---- block attention on the tensor cores (mma.sync m16n8k16, bf16 -> fp32) ----
-constexpr int kBaThreads = 128;  // 4 warps x 16 query rows
+// ---- mma.sync helpers (the ridge's softmax): m16n8k16, bf16 -> fp32 ----
+constexpr int kBaThreads = 128;  // 4 warps x 16 rows
 constexpr int kBaKeys = 64;      // keys per chunk
-
-template <int DH>
-struct BaCfg {
-  static constexpr int kLd = DH + 8;                          // smem row stride (elements): 16 B of padding
-  static constexpr int kTileElems = kBaKeys * kLd;            // one K or V chunk
-  static constexpr size_t kSmem = 4ull * kTileElems * 2 + 128;  // K and V, two buffers each, + alignment
-};
 
 __device__ __forceinline__ void ba_cp16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -79,187 +70,430 @@ __device__ __forceinline__ void ba_split(float x0, float x1, uint32_t& hi, uint3
   lo = ba_bf2(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
 }
 
-// Y[hd, r, :] and lse[hd, r] over the visible keys t < min(n_block, q_pos0 + r + 1).
-// grid (ceil(W / PP), Hkv * G / Gt), 128 threads; PP = 64 / Gt positions of Gt
-// heads of one KV group per CTA, so every key chunk serves all 64 rows.  Warp w
-// takes 16 rows: head w / (4 / Gt), positions p0 + (w % (4 / Gt)) * 16 + 0..15.
-// Per chunk of 64 keys (cp.async, double-buffered, rows past the block clamped
-// to its last key and masked): S = Q K^T by 64 MMAs (K through ldmatrix), the
-// online max and sum in the log2 domain (each row's values sit in the 4 lanes
-// of a quad), then O += P V with P split into bf16 hi + lo (two MMAs, 16
-// significant bits) and V through ldmatrix.trans.
+
+// ---- block attention on tcgen05 ---------------------------------------------
+// One CTA per 128-row query tile (Gt heads of one KV group x P = 128 / Gt
+// window positions, as in the scoring passes), looping over the block's keys
+// 128 at a time:
+//   S = Q K^T                 tcgen05.mma into TMEM (two buffers)
+//   P = 2^(S c - m)           eight softmax warps, two per TMEM lane quarter,
+//                             each taking 64 of a tile row's 128 keys; the pair
+//                             combines its half maxima through two spare TMEM
+//                             columns (both warps reach the same lanes; an
+//                             mbarrier per pair orders them): the row max m in the log2
+//                             domain is raised only when a row's tile max
+//                             exceeds it by kBtRescale, and then the row's O
+//                             and sum are scaled by 2^(m_old - m_new); P is
+//                             split into a high part (its upper 16 bits: bf16
+//                             by truncation) and the bf16 of the remainder (16
+//                             significant bits together), written as the A
+//                             operands
+//   O += P_hi V + P_lo V      two tcgen05.mma into TMEM, V transposed into the
+//                             K-major B operand by two warps (ldmatrix, then
+//                             stmatrix.trans) as it arrives from TMA
+// and at the end Y = O / l, lse = (m + log2 l) ln 2.  Warp 8 issues TMA, warp
+// 9 the MMAs, warps 10 and 11 transpose V; every wait is bounded.  One P and one transposed V buffer: the
+// softmax and the transposers of tile j wait for the O product of tile j - 1,
+// during which the tensor pipe runs S of tile j + 1.
+constexpr int kBtThreads = 384;
+constexpr int kBtSoftWarps = 8;
+constexpr int kBtTmaWarp = 8, kBtMmaWarp = 9, kBtXpWarp0 = 10;
+constexpr int kBtKStages = 2;
+constexpr float kBtRescale = 8.f;
+
 template <int DH>
-__global__ void __launch_bounds__(kBaThreads) block_attention_kernel(
-    const uint16_t* __restrict__ Q, const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, int G, int Gt,
-    int W, int N, int q_pos0, int n_block, float c_log2, float* __restrict__ Y, float* __restrict__ lse) {
-  constexpr int kLd = BaCfg<DH>::kLd, kTile = BaCfg<DH>::kTileElems;
-  constexpr int KS = DH / 16;  // k-steps of S
-  constexpr int NT = DH / 8;   // channel n-tiles of O
-  constexpr int kChunks16 = DH / 8;  // 16-byte pieces per key row
-  extern __shared__ uint8_t ba_raw[];
-  uint16_t* sm = reinterpret_cast<uint16_t*>((reinterpret_cast<uintptr_t>(ba_raw) + 127) & ~uintptr_t(127));
-  // sm: K buffer 0, K buffer 1, V buffer 0, V buffer 1
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quad = lane >> 2, qi = lane & 3;
-  const int wph = 4 / Gt, PP = 64 / Gt;
-  const int n_hc = G / Gt;
-  const int g = blockIdx.y / n_hc, hc = blockIdx.y % n_hc;
-  const int p0 = blockIdx.x * PP;
-  const int hd = g * G + hc * Gt + warp / wph;
-  const int pw = p0 + (warp % wph) * 16;  // the warp's first position (relative to the window)
-  const int r_lo = min(pw + quad, W - 1), r_hi = min(pw + quad + 8, W - 1);
-  const int nv_lo = min(n_block, q_pos0 + r_lo + 1), nv_hi = min(n_block, q_pos0 + r_hi + 1);
-  const int p_last = min(p0 + PP - 1, W - 1);
-  const int n_keys = min(n_block, q_pos0 + p_last + 1);  // keys any row of the CTA sees
-  const int n_chunks = (n_keys + kBaKeys - 1) / kBaKeys;
-  const uint16_t* Kg = K + static_cast<long long>(g) * N * DH;
-  const uint16_t* Vg = V + static_cast<long long>(g) * N * DH;
+struct BtSmem {
+  uint8_t q[TileCfg<DH>::kTileBytes];              // 128 rows x DH, K-major, DH / 64 panels
+  uint8_t k[kBtKStages][TileCfg<DH>::kTileBytes];  // 128 keys x DH
+  uint8_t v[TileCfg<DH>::kTileBytes];              // 128 keys x DH as TMA brings it (rows = keys)
+  uint8_t vt[2 * DH * 128];                        // DH rows x 128 keys, K-major, 2 panels of 64 keys
+  uint8_t p_hi[2 * 128 * 128];                     // 128 rows x 128 keys, K-major, 2 panels
+  uint8_t p_lo[2 * 128 * 128];
+  uint64_t q_full, k_full[kBtKStages], k_empty[kBtKStages], v_full, v_empty, vt_full, vt_empty, s_full[2],
+      s_empty[2], p_full, p_empty, o_full, drain, xch[4];
+  uint32_t tmem_base;
+  int abort_flag;
+};
 
-  pdl_wait();
-  pdl_trigger();
-  auto load_chunk = [&](int ch, int buf) {
-    const int t0 = ch * kBaKeys;
-    for (int e = tid; e < kBaKeys * kChunks16; e += kBaThreads) {
-      const int row = e / kChunks16, piece = e % kChunks16;
-      const long long src = static_cast<long long>(min(t0 + row, n_block - 1)) * DH + piece * 8;
-      const int dst = row * kLd + piece * 8;
-      ba_cp16(smem_u32(sm + buf * kTile + dst), Kg + src);
-      ba_cp16(smem_u32(sm + (2 + buf) * kTile + dst), Vg + src);
-    }
-    ba_commit();
-  };
-  load_chunk(0, 0);
+// byte offset of element (row r, column c) of a K-major 128-byte-swizzle
+// operand whose 64-column panels hold `rows` rows each
+__device__ __forceinline__ uint32_t bt_sw(int r, int c, int rows) {
+  return static_cast<uint32_t>((c >> 6) * rows * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
+}
 
-  // Q fragments, loaded once (rows past the window repeat the last row; not stored)
-  uint32_t qf[KS][4];
-  {
-    const uint16_t* q_lo = Q + (static_cast<long long>(hd) * W + r_lo) * DH + 2 * qi;
-    const uint16_t* q_hi = Q + (static_cast<long long>(hd) * W + r_hi) * DH + 2 * qi;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qf[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(q_lo + 16 * ks));
-      qf[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(q_hi + 16 * ks));
-      qf[ks][2] = __ldg(reinterpret_cast<const uint32_t*>(q_lo + 16 * ks + 8));
-      qf[ks][3] = __ldg(reinterpret_cast<const uint32_t*>(q_hi + 16 * ks + 8));
-    }
-  }
-  float o[NT][4];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;  // l: this lane's part of the row sum
+__device__ __forceinline__ void bt_stsm4_t(uint32_t addr, const uint32_t (&r)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
 
-  // ldmatrix row addresses: lane l feeds row l % 8 of matrix l / 8
-  const int mi = lane >> 3, mr = lane & 7;
-  const int k_row = (mi >> 1) * 8 + mr, k_col = (mi & 1) * 8;  // K: keys (+8 for matrices 2, 3), channels
-  const int v_row = (mi & 1) * 8 + mr, v_col = (mi >> 1) * 8;  // V: keys (+8 for matrices 1, 3), channels
+// 32 consecutive fp32 columns of this thread's TMEM lane, written back
+__device__ __forceinline__ void tmem_store32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
+      "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]),
+      "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]),
+      "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// one fp32 column of this thread's TMEM lane: store (waited), load (waited)
+__device__ __forceinline__ void tmem_store1(uint32_t taddr, float v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n\ttcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+               "f"(v)
+               : "memory");
+}
+__device__ __forceinline__ float tmem_load1(uint32_t taddr) {
+  float v;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\ttcgen05.wait::ld.sync.aligned;"
+               : "=f"(v)
+               : "r"(taddr)
+               : "memory");
+  return v;
+}
 
-  for (int ch = 0; ch < n_chunks; ++ch) {
-    const int buf = ch & 1;
-    if (ch + 1 < n_chunks) {
-      load_chunk(ch + 1, buf ^ 1);
-      ba_wait<1>();
-    } else {
-      ba_wait<0>();
-    }
-    __syncthreads();
-    const uint32_t kbase = smem_u32(sm + buf * kTile), vbase = smem_u32(sm + (2 + buf) * kTile);
-    float s[8][4];
+// O (+)= P V^T over the 128 keys of a tile: A = P (128 x 128 keys), B = Vt (DH rows x 128 keys)
+template <int DH>
+__device__ __forceinline__ void bt_issue_pv(uint32_t d_tmem, uint32_t a_base, uint32_t b_base, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, DH);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-    for (int n2 = 0; n2 < 4; ++n2) {
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t b0, b1, b2, b3;
-        ba_ldsm4(kbase + ((16 * n2 + k_row) * kLd + 16 * ks + k_col) * 2, b0, b1, b2, b3);
-        ba_mma(s[2 * n2], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
-        ba_mma(s[2 * n2 + 1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
-      }
-    }
-    // mask, scale to the log2 domain, chunk maxima
-    const int t0 = ch * kBaKeys;
-    float mx_lo = -INFINITY, mx_hi = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int t = t0 + 8 * j + 2 * qi;
-      s[j][0] = t < nv_lo ? s[j][0] * c_log2 : -INFINITY;
-      s[j][1] = t + 1 < nv_lo ? s[j][1] * c_log2 : -INFINITY;
-      s[j][2] = t < nv_hi ? s[j][2] * c_log2 : -INFINITY;
-      s[j][3] = t + 1 < nv_hi ? s[j][3] * c_log2 : -INFINITY;
-      mx_lo = fmaxf(mx_lo, fmaxf(s[j][0], s[j][1]));
-      mx_hi = fmaxf(mx_hi, fmaxf(s[j][2], s[j][3]));
-    }
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-    const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);  // finite: key 0 is in chunk 0
-    const float a_lo = exp2f(m_lo - mn_lo), a_hi = exp2f(m_hi - mn_hi);  // 0 on the first chunk
-    m_lo = mn_lo;
-    m_hi = mn_hi;
-    float ps_lo = 0.f, ps_hi = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      s[j][0] = exp2f(s[j][0] - mn_lo);
-      s[j][1] = exp2f(s[j][1] - mn_lo);
-      s[j][2] = exp2f(s[j][2] - mn_hi);
-      s[j][3] = exp2f(s[j][3] - mn_hi);
-      ps_lo += s[j][0] + s[j][1];
-      ps_hi += s[j][2] + s[j][3];
-    }
-    l_lo = l_lo * a_lo + ps_lo;
-    l_hi = l_hi * a_hi + ps_hi;
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      o[j][0] *= a_lo;
-      o[j][1] *= a_lo;
-      o[j][2] *= a_hi;
-      o[j][3] *= a_hi;
-    }
-    // O += P V: k-step kk covers keys 16 kk .. 16 kk + 15 of the chunk (n-tiles 2 kk, 2 kk + 1 of S)
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t h0, h1, h2, h3, w0, w1, w2, w3;
-      ba_split(s[2 * kk][0], s[2 * kk][1], h0, w0);
-      ba_split(s[2 * kk][2], s[2 * kk][3], h1, w1);
-      ba_split(s[2 * kk + 1][0], s[2 * kk + 1][1], h2, w2);
-      ba_split(s[2 * kk + 1][2], s[2 * kk + 1][3], h3, w3);
-#pragma unroll
-      for (int n2 = 0; n2 < NT / 2; ++n2) {
-        uint32_t b0, b1, b2, b3;
-        ba_ldsm4_t(vbase + ((16 * kk + v_row) * kLd + 16 * n2 + v_col) * 2, b0, b1, b2, b3);
-        ba_mma(o[2 * n2], h0, h1, h2, h3, b0, b1);
-        ba_mma(o[2 * n2], w0, w1, w2, w3, b0, b1);
-        ba_mma(o[2 * n2 + 1], h0, h1, h2, h3, b2, b3);
-        ba_mma(o[2 * n2 + 1], w0, w1, w2, w3, b2, b3);
-      }
-    }
-    __syncthreads();  // every warp is done with this buffer before it is refilled
-  }
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-  const float i_lo = 1.f / l_lo, i_hi = 1.f / l_hi;
-  const bool st_lo = pw + quad < W, st_hi = pw + quad + 8 < W;
-  float* y_lo = Y + (static_cast<long long>(hd) * W + r_lo) * DH + 2 * qi;
-  float* y_hi = Y + (static_cast<long long>(hd) * W + r_hi) * DH + 2 * qi;
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    if (st_lo) *reinterpret_cast<float2*>(y_lo + 8 * j) = make_float2(o[j][0] * i_lo, o[j][1] * i_lo);
-    if (st_hi) *reinterpret_cast<float2*>(y_hi + 8 * j) = make_float2(o[j][2] * i_hi, o[j][3] * i_hi);
-  }
-  if (lse != nullptr && qi == 0) {
-    if (st_lo) lse[static_cast<long long>(hd) * W + r_lo] = (m_lo + log2f(l_lo)) * 0.69314718055994530942f;
-    if (st_hi) lse[static_cast<long long>(hd) * W + r_hi] = (m_hi + log2f(l_hi)) * 0.69314718055994530942f;
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t ka = (kk >> 2) * (128u * 128u) + (kk & 3) * 32u;
+    const uint32_t kb = (kk >> 2) * (static_cast<uint32_t>(DH) * 128u) + (kk & 3) * 32u;
+    umma_bf16(d_tmem, sdesc_kmajor_sw128(a_base + ka), sdesc_kmajor_sw128(b_base + kb), idesc,
+              (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
+// grid: Hkv * n_hc * n_pb query tiles (tile rt: group rt / (n_hc n_pb), head chunk (rt / n_pb) % n_hc,
+// position block rt % n_pb); kBtThreads threads.
+template <int DH>
+__global__ void __launch_bounds__(kBtThreads, 1)
+    block_attention_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                              const __grid_constant__ CUtensorMap mapV, const int G, const int Gt, const int W,
+                              const int q_pos0, const int n_block, const int n_hc, const int n_pb,
+                              const float c_log2, float* __restrict__ Y, float* __restrict__ lse) {
+  extern __shared__ uint8_t smem_raw[];
+  BtSmem<DH>& S = *reinterpret_cast<BtSmem<DH>*>(align1024(smem_raw));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (timeout_recorded()) return;  // uniform over the CTA, before any barrier
+  const int P = 128 / Gt;
+  const int rt = blockIdx.x;
+  const int g = rt / (n_hc * n_pb), hc = (rt / n_pb) % n_hc, pb = rt % n_pb;
+  const int h0 = g * G + hc * Gt;  // the tile's first query head
+  const int p_last = min((pb + 1) * P, W) - 1;
+  const int n_keys = min(n_block, q_pos0 + p_last + 1);
+  const int n_kt = (n_keys + 127) / 128;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&S.q_full, 1);
+    for (int i = 0; i < kBtKStages; ++i) {
+      mbar_init(&S.k_full[i], 1);
+      mbar_init(&S.k_empty[i], 1);
+    }
+    mbar_init(&S.v_full, 1);
+    mbar_init(&S.v_empty, 2);   // the two transposer warps
+    mbar_init(&S.vt_full, 2);
+    mbar_init(&S.vt_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.s_full[b], 1);
+      mbar_init(&S.s_empty[b], kBtSoftWarps);
+    }
+    for (int q = 0; q < 4; ++q) mbar_init(&S.xch[q], 2);  // the two warps of a lane quarter
+    mbar_init(&S.p_full, kBtSoftWarps);
+    mbar_init(&S.p_empty, 1);
+    mbar_init(&S.o_full, 1);
+    mbar_init(&S.drain, 1);
+    S.abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&S.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();
+  pdl_trigger();
+  const uint32_t tmem = S.tmem_base;  // S buffers at columns 0 and 128, O at 256
+  volatile int* abort_flag = &S.abort_flag;
+  constexpr uint32_t kTile = TileCfg<DH>::kTileBytes;
+
+  if (warp == kBtTmaWarp) {
+    if (lane == 0) {  // TMA producer
+      prefetch_tensormap(&mapQ);
+      prefetch_tensormap(&mapK);
+      prefetch_tensormap(&mapV);
+      mbar_arrive_expect_tx(&S.q_full, kTile);
+#pragma unroll
+      for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
+        tma_load_3d(S.q + p * 16384, &mapQ, &S.q_full, p * 64, pb * P, h0);
+      int issued_k = 0, issued_v = 0;
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j % kBtKStages;
+        if (j >= kBtKStages && !mbar_wait(&S.k_empty[s], ((j / kBtKStages) - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&S.k_full[s], kTile);
+#pragma unroll
+        for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
+          tma_load_3d(S.k[s] + p * 16384, &mapK, &S.k_full[s], p * 64, j * 128, g);
+        issued_k = j + 1;
+        if (j >= 1 && !mbar_wait(&S.v_empty, (j - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&S.v_full, kTile);
+#pragma unroll
+        for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
+          tma_load_3d(S.v + p * 16384, &mapV, &S.v_full, p * 64, j * 128, g);
+        issued_v = j + 1;
+      }
+      if (*abort_flag) {  // let our copies land before the CTA goes away
+        volatile int never = 0;
+        mbar_wait(&S.q_full, 0, &never);
+        for (int i = max(0, issued_k - kBtKStages); i < issued_k; ++i)
+          mbar_wait(&S.k_full[i % kBtKStages], (i / kBtKStages) & 1, &never);
+        if (issued_v > 0) mbar_wait(&S.v_full, (issued_v - 1) & 1, &never);
+      }
+    }
+  } else if (warp == kBtMmaWarp) {
+    if (lane == 0) {  // MMA issuer
+      bool ok = mbar_wait(&S.q_full, 0, abort_flag);
+      auto mma_s = [&](int j) {
+        const int s = j % kBtKStages, b = j & 1;
+        if (!mbar_wait(&S.k_full[s], (j / kBtKStages) & 1, abort_flag)) return false;
+        if (j >= 2 && !mbar_wait(&S.s_empty[b], ((j >> 1) - 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        issue_tile_mma<DH>(tmem + b * 128, smem_u32(S.q), smem_u32(S.k[s]));
+        umma_commit(&S.k_empty[s]);
+        umma_commit(&S.s_full[b]);
+        return true;
+      };
+      if (ok) ok = mma_s(0);
+      for (int j = 0; j < n_kt && ok; ++j) {
+        if (j + 1 < n_kt && !(ok = mma_s(j + 1))) break;
+        if (!mbar_wait(&S.p_full, j & 1, abort_flag) || !mbar_wait(&S.vt_full, j & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        bt_issue_pv<DH>(tmem + 256, smem_u32(S.p_hi), smem_u32(S.vt), j > 0);
+        bt_issue_pv<DH>(tmem + 256, smem_u32(S.p_lo), smem_u32(S.vt), true);
+        umma_commit(&S.p_empty);
+        umma_commit(&S.vt_empty);
+      }
+      if (ok) umma_commit(&S.o_full);
+      if (*abort_flag) {
+        volatile int never = 0;
+        umma_commit(&S.drain);
+        mbar_wait(&S.drain, 0, &never);
+      }
+    }
+  } else if (warp >= kBtXpWarp0) {  // V transposers: rows = keys -> rows = channels
+    const int xw = warp - kBtXpWarp0, m = lane >> 3, i = lane & 7;
+    constexpr int kGroups = (DH / 8) * 4;  // (channel block, 4 key blocks) groups of four 8 x 8 blocks
+    for (int j = 0; j < n_kt; ++j) {
+      if (!mbar_wait(&S.v_full, j & 1, abort_flag)) break;
+      if (j >= 1 && !mbar_wait(&S.vt_empty, (j - 1) & 1, abort_flag)) break;
+      for (int gi = xw; gi < kGroups; gi += 2) {
+        const int cb = gi >> 2, kb = (gi & 3) * 4 + m;  // this lane's matrix: channel block cb, key block kb
+        const int t = kb * 8 + i;                        // ldmatrix row: key t, channels 8 cb .. 8 cb + 7
+        const uint32_t src = smem_u32(S.v) + (cb >> 3) * 16384 + t * 128 + ((((cb & 7)) ^ (t & 7)) << 4);
+        uint32_t r[4];
+        ba_ldsm4(src, r[0], r[1], r[2], r[3]);
+        const int c = cb * 8 + i;                        // stmatrix row: channel c, keys 8 kb .. 8 kb + 7
+        const uint32_t dst = smem_u32(S.vt) + bt_sw(c, kb * 8, DH);
+        bt_stsm4_t(dst, r);
+      }
+      __syncwarp();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
+      if (lane == 0) {
+        mbar_arrive(&S.vt_full);
+        mbar_arrive(&S.v_empty);
+      }
+    }
+  } else {  // warps 0-7: softmax; warp w takes TMEM lanes 32 (w % 4).. and keys 64 (w / 4) .. + 63 of every tile
+    const int q4 = warp & 3, half = warp >> 2;
+    const int row = q4 * 32 + lane;
+    const int hl = row / P, pos = pb * P + row % P;
+    const int posc = min(pos, W - 1);
+    const int vis = min(n_block, q_pos0 + posc + 1);  // keys this row sees
+    // the lowest visible count over the warp's rows: tiles below it need no mask
+    int vis_w = vis;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) vis_w = min(vis_w, __shfl_xor_sync(0xFFFFFFFFu, vis_w, o));
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+    const int c_lo = half * 64;                 // this warp's keys of a tile, and its columns of O
+    const int o_lo = half * (DH / 2);
+    const float c = c_log2;
+    const unsigned long long c2 = f2_pack(c, c);
+    float m = -INFINITY, l = 0.f;
+    uint32_t va[32], vb[32];
+    bool ok = true;
+    int nx = 0;  // exchanges done (the pair's mbarrier phase)
+    // this lane's value for the partner warp, through TMEM column 448 + 2 (exchange parity) + half
+    auto exchange = [&](float mine, float* other) {
+      tmem_store1(lane_base + 448 + 2 * (nx & 1) + half, mine);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.xch[q4]);
+      if (!mbar_wait(&S.xch[q4], nx & 1, abort_flag)) return false;
+      tc_fence_after();
+      *other = tmem_load1(lane_base + 448 + 2 * (nx & 1) + (half ^ 1));
+      ++nx;
+      return true;
+    };
+    for (int j = 0; j < n_kt && ok; ++j) {
+      const int b = j & 1, t0 = j * 128 + c_lo;
+      const bool full = t0 + 64 <= vis_w;  // every key of the warp's half tile is visible to all its rows
+      if (!mbar_wait(&S.s_full[b], (j >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sb = lane_base + b * 128 + c_lo;
+      // pass A: the half tile's row max, masked keys left out; then the whole row's, from the partner
+      tmem_issue32(sb, va);
+      tmem_issue32(sb + 32, vb);
+      tmem_wait32(va);
+      tmem_wait32(vb);
+      float z;
+      {
+        const float* x = reinterpret_cast<const float*>(va);
+        const float* y = reinterpret_cast<const float*>(vb);
+        if (full) {
+          float t[22];
+#pragma unroll
+          for (int k = 0; k < 10; ++k) t[k] = fmax3(x[3 * k], x[3 * k + 1], x[3 * k + 2]);
+          t[10] = fmaxf(x[30], x[31]);
+#pragma unroll
+          for (int k = 0; k < 10; ++k) t[11 + k] = fmax3(y[3 * k], y[3 * k + 1], y[3 * k + 2]);
+          t[21] = fmaxf(y[30], y[31]);
+          z = t[0];
+#pragma unroll
+          for (int k = 1; k < 21; k += 2) z = fmax3(z, t[k], t[k + 1]);
+          z = fmaxf(z, t[21]);
+        } else {
+          z = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if (t0 + e < vis) z = fmaxf(z, x[e]);
+            if (t0 + 32 + e < vis) z = fmaxf(z, y[e]);
+          }
+        }
+      }
+      float zo;
+      if (!exchange(z, &zo)) {
+        ok = false;
+        break;
+      }
+      z = fmaxf(z, zo) * c;
+      float alpha = 1.f;
+      const bool raise = m == -INFINITY || z > m + kBtRescale;
+      const float m_new = raise ? fmaxf(m, z) : m;
+      if (raise) alpha = ex2_approx(m - m_new);  // 0 on the first tile
+      // the O product of the previous tile is done: P and O are free
+      if (j >= 1 && !mbar_wait(&S.p_empty, (j - 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (j >= 1 && __any_sync(0xFFFFFFFFu, raise)) {  // scale this warp's rows and columns of O
+#pragma unroll
+        for (int ch = 0; ch < DH / 64; ++ch) {
+          float o[32];
+          tmem_load32(lane_base + 256 + o_lo + ch * 32, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_store32(lane_base + 256 + o_lo + ch * 32, o);
+        }
+        tmem_wait_st();
+      }
+      l *= alpha;
+      m = m_new;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.s_empty[b]);  // S is in registers: the buffer may refill
+      // pass B: P = 2^(s c - m), its half-row sum, and its two bf16 parts into the A operands
+      const unsigned long long nm2 = f2_pack(-m, -m);
+      unsigned long long acc2 = 0ull;
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        float* v = reinterpret_cast<float*>(ch == 0 ? va : vb);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float e0, e1;
+          f2_unpack(f2_fma(f2_pack(v[e], v[e + 1]), c2, nm2), &e0, &e1);
+          v[e] = ex2_approx(e0);
+          v[e + 1] = ex2_approx(e1);
+          if (!full) {
+            if (t0 + ch * 32 + e >= vis) v[e] = 0.f;
+            if (t0 + ch * 32 + e + 1 >= vis) v[e + 1] = 0.f;
+          }
+          acc2 = f2_add(acc2, f2_pack(v[e], v[e + 1]));
+        }
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys = 16 bytes of each operand
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int k2 = 0; k2 < 4; ++k2) {
+            const uint32_t b0 = __float_as_uint(v[q8 * 8 + 2 * k2]), b1 = __float_as_uint(v[q8 * 8 + 2 * k2 + 1]);
+            hi[k2] = __byte_perm(b0, b1, 0x7632);  // the upper halves: bf16 by truncation
+            float r0, r1;
+            f2_unpack(f2_add(f2_pack(v[q8 * 8 + 2 * k2], v[q8 * 8 + 2 * k2 + 1]),
+                             f2_pack(-__uint_as_float(b0 & 0xFFFF0000u), -__uint_as_float(b1 & 0xFFFF0000u))),
+                      &r0, &r1);
+            lo[k2] = ba_bf2(r0, r1);
+          }
+          const uint32_t off = bt_sw(row, c_lo + ch * 32 + q8 * 8, 128);
+          *reinterpret_cast<uint4*>(S.p_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(S.p_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      float s0, s1;
+      f2_unpack(acc2, &s0, &s1);
+      l += s0 + s1;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.p_full);
+    }
+    float lo_sum = 0.f;
+    if (ok && exchange(l, &lo_sum) && mbar_wait(&S.o_full, 0, abort_flag)) {
+      tc_fence_after();
+      const float lt = l + lo_sum;  // the whole row's sum (the same in both warps of the pair)
+      const bool store = pos < W && hl < Gt;
+      const long long hd = h0 + hl;
+      float* yr = Y + (hd * W + posc) * DH + o_lo;
+      const float inv = 1.f / lt;
+#pragma unroll
+      for (int ch = 0; ch < DH / 64; ++ch) {
+        float o[32];
+        tmem_load32(lane_base + 256 + o_lo + ch * 32, o);
+        if (store) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(yr + ch * 32 + e) = make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv,
+                                                                       o[e + 3] * inv);
+        }
+      }
+      if (store && lse && half == 0) lse[hd * W + posc] = (m + lg2_approx(lt)) * kLn2;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+
 // A[g][r][i] = softmax_i(Qt[g][r] . Kc[g][i] / sqrt(d)) over the k compressed keys.
-// grid (ceil(R / 64), Hkv), 128 threads, 16 rows a warp; the logits come from
-// mma.sync as in the block attention, over chunks of 64 keys (cp.async,
-// double-buffered, rows past k clamped and masked), in two sweeps: the row max
-// and sum, then the normalised weights written to A.
+// grid (ceil(R / 64), Hkv), 128 threads, 16 rows a warp; the logits from
+// mma.sync m16n8k16 over chunks of 64 keys (cp.async, double-buffered, rows
+// past k clamped and masked), in two sweeps: the row max and sum, then the
+// normalised weights written to A.
 template <int DH>
 struct RsCfg {
   static constexpr int kLd = DH + 8;
