@@ -88,28 +88,28 @@ __device__ __forceinline__ void ba_split(float x0, float x1, uint32_t& hi, uint3
 //                             by truncation) and the bf16 of the remainder (16
 //                             significant bits together), written as the A
 //                             operands
-//   O += P_hi V + P_lo V      two tcgen05.mma into TMEM, V transposed into the
-//                             K-major B operand by two warps (ldmatrix, then
-//                             stmatrix.trans) as it arrives from TMA
-// and at the end Y = O / l, lse = (m + log2 l) ln 2.  Warp 8 issues TMA, warp
-// 9 the MMAs, warps 10 and 11 transpose V; every wait is bounded.  One P and one transposed V buffer: the
-// softmax and the transposers of tile j wait for the O product of tile j - 1,
-// during which the tensor pipe runs S of tile j + 1.
-constexpr int kBtThreads = 384;
+//   O += P_hi V + P_lo V      two tcgen05.mma into TMEM, V straight from its TMA
+//                             tile as an MN-major B operand (channels
+//                             contiguous; the instruction's transpose bit)
+// and at the end Y = O / l, lse = (m + log2 l) ln 2.  Warp 8 issues TMA
+// (K and V each in a 2-stage ring), warp 9 the MMAs; every wait is bounded.
+// One P buffer: the softmax of tile j writes P after the O product of tile
+// j - 1, during which the tensor pipe runs S of tile j + 1.
+constexpr int kBtThreads = 320;
 constexpr int kBtSoftWarps = 8;
-constexpr int kBtTmaWarp = 8, kBtMmaWarp = 9, kBtXpWarp0 = 10;
+constexpr int kBtTmaWarp = 8, kBtMmaWarp = 9;
 constexpr int kBtKStages = 2;
+constexpr int kBtVStages = 2;
 constexpr float kBtRescale = 8.f;
 
 template <int DH>
 struct BtSmem {
   uint8_t q[TileCfg<DH>::kTileBytes];              // 128 rows x DH, K-major, DH / 64 panels
   uint8_t k[kBtKStages][TileCfg<DH>::kTileBytes];  // 128 keys x DH
-  uint8_t v[TileCfg<DH>::kTileBytes];              // 128 keys x DH as TMA brings it (rows = keys)
-  uint8_t vt[2 * DH * 128];                        // DH rows x 128 keys, K-major, 2 panels of 64 keys
+  uint8_t v[kBtVStages][TileCfg<DH>::kTileBytes];  // 128 keys x DH as TMA brings it: the MN-major B operand
   uint8_t p_hi[2 * 128 * 128];                     // 128 rows x 128 keys, K-major, 2 panels
   uint8_t p_lo[2 * 128 * 128];
-  uint64_t q_full, k_full[kBtKStages], k_empty[kBtKStages], v_full, v_empty, vt_full, vt_empty, s_full[2],
+  uint64_t q_full, k_full[kBtKStages], k_empty[kBtKStages], v_full[kBtVStages], v_empty[kBtVStages], s_full[2],
       s_empty[2], p_full, p_empty, o_full, drain, xch[4];
   uint32_t tmem_base;
   int abort_flag;
@@ -119,12 +119,6 @@ struct BtSmem {
 // operand whose 64-column panels hold `rows` rows each
 __device__ __forceinline__ uint32_t bt_sw(int r, int c, int rows) {
   return static_cast<uint32_t>((c >> 6) * rows * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
-}
-
-__device__ __forceinline__ void bt_stsm4_t(uint32_t addr, const uint32_t (&r)[4]) {
-  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]),
-               "r"(r[1]), "r"(r[2]), "r"(r[3])
-               : "memory");
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane, written back
@@ -155,15 +149,30 @@ __device__ __forceinline__ float tmem_load1(uint32_t taddr) {
   return v;
 }
 
-// O (+)= P V^T over the 128 keys of a tile: A = P (128 x 128 keys), B = Vt (DH rows x 128 keys)
+// Shared-memory descriptor of an MN-major operand with the 128-byte swizzle
+// (rows along K, each row 64 MN elements = 128 bytes): 8-row atoms every 1024
+// bytes along K (stride byte offset), 64-element blocks along MN every `lbo`
+// bytes (leading byte offset).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
+// O (+)= P V over the 128 keys of a tile: A = P (128 rows x 128 keys, K-major),
+// B = V as loaded (128 keys x DH, MN-major: the transpose bit of the instruction)
 template <int DH>
 __device__ __forceinline__ void bt_issue_pv(uint32_t d_tmem, uint32_t a_base, uint32_t b_base, bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, DH);
+  constexpr uint32_t idesc = idesc_bf16_f32(128, DH) | (1u << 16);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t ka = (kk >> 2) * (128u * 128u) + (kk & 3) * 32u;
-    const uint32_t kb = (kk >> 2) * (static_cast<uint32_t>(DH) * 128u) + (kk & 3) * 32u;
-    umma_bf16(d_tmem, sdesc_kmajor_sw128(a_base + ka), sdesc_kmajor_sw128(b_base + kb), idesc,
+    const uint32_t kb = kk * 2048u;  // 16 keys = two 8-row atoms
+    umma_bf16(d_tmem, sdesc_kmajor_sw128(a_base + ka), sdesc_mnmajor_sw128(b_base + kb, 16384u), idesc,
               (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -194,10 +203,10 @@ __global__ void __launch_bounds__(kBtThreads, 1)
       mbar_init(&S.k_full[i], 1);
       mbar_init(&S.k_empty[i], 1);
     }
-    mbar_init(&S.v_full, 1);
-    mbar_init(&S.v_empty, 2);   // the two transposer warps
-    mbar_init(&S.vt_full, 2);
-    mbar_init(&S.vt_empty, 1);
+    for (int i = 0; i < kBtVStages; ++i) {
+      mbar_init(&S.v_full[i], 1);
+      mbar_init(&S.v_empty[i], 1);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.s_full[b], 1);
       mbar_init(&S.s_empty[b], kBtSoftWarps);
@@ -241,11 +250,12 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
           tma_load_3d(S.k[s] + p * 16384, &mapK, &S.k_full[s], p * 64, j * 128, g);
         issued_k = j + 1;
-        if (j >= 1 && !mbar_wait(&S.v_empty, (j - 1) & 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&S.v_full, kTile);
+        const int sv = j % kBtVStages;
+        if (j >= kBtVStages && !mbar_wait(&S.v_empty[sv], ((j / kBtVStages) - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&S.v_full[sv], kTile);
 #pragma unroll
         for (int p = 0; p < TileCfg<DH>::kPanels; ++p)
-          tma_load_3d(S.v + p * 16384, &mapV, &S.v_full, p * 64, j * 128, g);
+          tma_load_3d(S.v[sv] + p * 16384, &mapV, &S.v_full[sv], p * 64, j * 128, g);
         issued_v = j + 1;
       }
       if (*abort_flag) {  // let our copies land before the CTA goes away
@@ -253,7 +263,8 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         mbar_wait(&S.q_full, 0, &never);
         for (int i = max(0, issued_k - kBtKStages); i < issued_k; ++i)
           mbar_wait(&S.k_full[i % kBtKStages], (i / kBtKStages) & 1, &never);
-        if (issued_v > 0) mbar_wait(&S.v_full, (issued_v - 1) & 1, &never);
+        for (int i = max(0, issued_v - kBtVStages); i < issued_v; ++i)
+          mbar_wait(&S.v_full[i % kBtVStages], (i / kBtVStages) & 1, &never);
       }
     }
   } else if (warp == kBtMmaWarp) {
@@ -272,44 +283,23 @@ __global__ void __launch_bounds__(kBtThreads, 1)
       if (ok) ok = mma_s(0);
       for (int j = 0; j < n_kt && ok; ++j) {
         if (j + 1 < n_kt && !(ok = mma_s(j + 1))) break;
-        if (!mbar_wait(&S.p_full, j & 1, abort_flag) || !mbar_wait(&S.vt_full, j & 1, abort_flag)) {
+        const int sv = j % kBtVStages;
+        if (!mbar_wait(&S.p_full, j & 1, abort_flag) ||
+            !mbar_wait(&S.v_full[sv], (j / kBtVStages) & 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        bt_issue_pv<DH>(tmem + 256, smem_u32(S.p_hi), smem_u32(S.vt), j > 0);
-        bt_issue_pv<DH>(tmem + 256, smem_u32(S.p_lo), smem_u32(S.vt), true);
+        bt_issue_pv<DH>(tmem + 256, smem_u32(S.p_hi), smem_u32(S.v[sv]), j > 0);
+        bt_issue_pv<DH>(tmem + 256, smem_u32(S.p_lo), smem_u32(S.v[sv]), true);
         umma_commit(&S.p_empty);
-        umma_commit(&S.vt_empty);
+        umma_commit(&S.v_empty[sv]);
       }
       if (ok) umma_commit(&S.o_full);
       if (*abort_flag) {
         volatile int never = 0;
         umma_commit(&S.drain);
         mbar_wait(&S.drain, 0, &never);
-      }
-    }
-  } else if (warp >= kBtXpWarp0) {  // V transposers: rows = keys -> rows = channels
-    const int xw = warp - kBtXpWarp0, m = lane >> 3, i = lane & 7;
-    constexpr int kGroups = (DH / 8) * 4;  // (channel block, 4 key blocks) groups of four 8 x 8 blocks
-    for (int j = 0; j < n_kt; ++j) {
-      if (!mbar_wait(&S.v_full, j & 1, abort_flag)) break;
-      if (j >= 1 && !mbar_wait(&S.vt_empty, (j - 1) & 1, abort_flag)) break;
-      for (int gi = xw; gi < kGroups; gi += 2) {
-        const int cb = gi >> 2, kb = (gi & 3) * 4 + m;  // this lane's matrix: channel block cb, key block kb
-        const int t = kb * 8 + i;                        // ldmatrix row: key t, channels 8 cb .. 8 cb + 7
-        const uint32_t src = smem_u32(S.v) + (cb >> 3) * 16384 + t * 128 + ((((cb & 7)) ^ (t & 7)) << 4);
-        uint32_t r[4];
-        ba_ldsm4(src, r[0], r[1], r[2], r[3]);
-        const int c = cb * 8 + i;                        // stmatrix row: channel c, keys 8 kb .. 8 kb + 7
-        const uint32_t dst = smem_u32(S.vt) + bt_sw(c, kb * 8, DH);
-        bt_stsm4_t(dst, r);
-      }
-      __syncwarp();
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
-      if (lane == 0) {
-        mbar_arrive(&S.vt_full);
-        mbar_arrive(&S.v_empty);
       }
     }
   } else {  // warps 0-7: softmax; warp w takes TMEM lanes 32 (w % 4).. and keys 64 (w / 4) .. + 63 of every tile
