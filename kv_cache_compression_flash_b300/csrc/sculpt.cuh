@@ -3,8 +3,8 @@
 // fitted to the block's attention output and LSE; with the keys fixed, the
 // values are a ridge least-squares solution].
 //
-//   block_attention_tc_kernel<DH>  flash-style on tcgen05 (S and O in TMEM,
-//       P through shared memory into the second MMA; see below).  Row r sees
+//   block_attention_tc_kernel<DH>  flash-style on tcgen05 (S, P and O in
+//       TMEM, P read there as the A operand of the second MMA; see below).  Row r sees
 //       keys t < n_block, t <= q_pos0 + r.
 //   ridge_softmax_kernel<DH>    A = softmax over all k compressed keys (no
 //       mask: every training query sees the whole compressed block), the
@@ -86,20 +86,22 @@ __device__ __forceinline__ void ba_split(float x0, float x1, uint32_t& hi, uint3
 //                             and sum are scaled by 2^(m_old - m_new); P is
 //                             split into a high part (its upper 16 bits: bf16
 //                             by truncation) and the bf16 of the remainder (16
-//                             significant bits together), written as the A
-//                             operands
-//   O += P_hi V + P_lo V      two tcgen05.mma into TMEM, V straight from its TMA
-//                             tile as an MN-major B operand (channels
-//                             contiguous; the instruction's transpose bit)
+//                             significant bits together), written as bf16
+//                             pairs into TMEM over the tile's own S columns
+//   O += P_hi V + P_lo V      two tcgen05.mma into TMEM, A = P read from TMEM,
+//                             V straight from its TMA tile as an MN-major B
+//                             operand (channels contiguous; the instruction's
+//                             transpose bit)
 // and at the end Y = O / l, lse = (m + log2 l) ln 2.  Warp 8 issues TMA
-// (K and V each in a 2-stage ring), warp 9 the MMAs; every wait is bounded.
-// One P buffer: the softmax of tile j writes P after the O product of tile
-// j - 1, during which the tensor pipe runs S of tile j + 1.
+// (K and V each in a 3-stage ring), warp 9 the MMAs; every wait is bounded.
+// Two S/P buffers: S of tile j + 2 goes into buffer j & 1 once the O product
+// of tile j has read its P; the softmax waits for the O product of tile j - 1
+// only when it has to scale O.
 constexpr int kBtThreads = 320;
 constexpr int kBtSoftWarps = 8;
 constexpr int kBtTmaWarp = 8, kBtMmaWarp = 9;
-constexpr int kBtKStages = 2;
-constexpr int kBtVStages = 2;
+constexpr int kBtKStages = 3;
+constexpr int kBtVStages = 3;
 constexpr float kBtRescale = 8.f;
 
 template <int DH>
@@ -107,10 +109,8 @@ struct BtSmem {
   uint8_t q[TileCfg<DH>::kTileBytes];              // 128 rows x DH, K-major, DH / 64 panels
   uint8_t k[kBtKStages][TileCfg<DH>::kTileBytes];  // 128 keys x DH
   uint8_t v[kBtVStages][TileCfg<DH>::kTileBytes];  // 128 keys x DH as TMA brings it: the MN-major B operand
-  uint8_t p_hi[2 * 128 * 128];                     // 128 rows x 128 keys, K-major, 2 panels
-  uint8_t p_lo[2 * 128 * 128];
   uint64_t q_full, k_full[kBtKStages], k_empty[kBtKStages], v_full[kBtVStages], v_empty[kBtVStages], s_full[2],
-      s_empty[2], p_full, p_empty, o_full, drain, xch[4];
+      s_free[2], p_full, o_done, o_full, drain, xch[4];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -163,18 +163,28 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t
   return d;
 }
 
-// O (+)= P V over the 128 keys of a tile: A = P (128 rows x 128 keys, K-major),
-// B = V as loaded (128 keys x DH, MN-major: the transpose bit of the instruction)
+// D[tmem] (+)= A[tmem] * B[smem]: the A operand read from tensor memory (one
+// row per lane, two 16-bit elements per 32-bit column)
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// O (+)= P V over the 128 keys of a tile: A = P in TMEM (64 columns of bf16
+// pairs, keys 2c and 2c + 1 in column c), B = V as loaded (128 keys x DH,
+// MN-major: the transpose bit of the instruction)
 template <int DH>
-__device__ __forceinline__ void bt_issue_pv(uint32_t d_tmem, uint32_t a_base, uint32_t b_base, bool accumulate) {
+__device__ __forceinline__ void bt_issue_pv(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, DH) | (1u << 16);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t ka = (kk >> 2) * (128u * 128u) + (kk & 3) * 32u;
-    const uint32_t kb = kk * 2048u;  // 16 keys = two 8-row atoms
-    umma_bf16(d_tmem, sdesc_kmajor_sw128(a_base + ka), sdesc_mnmajor_sw128(b_base + kb, 16384u), idesc,
-              (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < 8; ++kk)  // 16 keys a step: 8 columns of A, two 8-row atoms of B
+    umma_bf16_ts(d_tmem, a_tmem + kk * 8, sdesc_mnmajor_sw128(b_base + kk * 2048u, 16384u), idesc,
+                 (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // grid: Hkv * n_hc * n_pb query tiles (tile rt: group rt / (n_hc n_pb), head chunk (rt / n_pb) % n_hc,
@@ -209,11 +219,11 @@ __global__ void __launch_bounds__(kBtThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.s_full[b], 1);
-      mbar_init(&S.s_empty[b], kBtSoftWarps);
+      mbar_init(&S.s_free[b], 1);  // the O product that read P from the buffer is done
     }
     for (int q = 0; q < 4; ++q) mbar_init(&S.xch[q], 2);  // the two warps of a lane quarter
     mbar_init(&S.p_full, kBtSoftWarps);
-    mbar_init(&S.p_empty, 1);
+    mbar_init(&S.o_done, 1);
     mbar_init(&S.o_full, 1);
     mbar_init(&S.drain, 1);
     S.abort_flag = 0;
@@ -273,7 +283,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
       auto mma_s = [&](int j) {
         const int s = j % kBtKStages, b = j & 1;
         if (!mbar_wait(&S.k_full[s], (j / kBtKStages) & 1, abort_flag)) return false;
-        if (j >= 2 && !mbar_wait(&S.s_empty[b], ((j >> 1) - 1) & 1, abort_flag)) return false;
+        if (j >= 2 && !mbar_wait(&S.s_free[b], ((j >> 1) - 1) & 1, abort_flag)) return false;
         tc_fence_after();
         issue_tile_mma<DH>(tmem + b * 128, smem_u32(S.q), smem_u32(S.k[s]));
         umma_commit(&S.k_empty[s]);
@@ -290,10 +300,12 @@ __global__ void __launch_bounds__(kBtThreads, 1)
           break;
         }
         tc_fence_after();
-        bt_issue_pv<DH>(tmem + 256, smem_u32(S.p_hi), smem_u32(S.v[sv]), j > 0);
-        bt_issue_pv<DH>(tmem + 256, smem_u32(S.p_lo), smem_u32(S.v[sv]), true);
-        umma_commit(&S.p_empty);
+        const uint32_t pb_t = tmem + (j & 1) * 128;  // P of tile j sits over its S
+        bt_issue_pv<DH>(tmem + 256, pb_t, smem_u32(S.v[sv]), j > 0);
+        bt_issue_pv<DH>(tmem + 256, pb_t + 64, smem_u32(S.v[sv]), true);
         umma_commit(&S.v_empty[sv]);
+        umma_commit(&S.s_free[j & 1]);
+        umma_commit(&S.o_done);
       }
       if (ok) umma_commit(&S.o_full);
       if (*abort_flag) {
@@ -382,13 +394,17 @@ __global__ void __launch_bounds__(kBtThreads, 1)
       const bool raise = m == -INFINITY || z > m + kBtRescale;
       const float m_new = raise ? fmaxf(m, z) : m;
       if (raise) alpha = ex2_approx(m - m_new);  // 0 on the first tile
-      // the O product of the previous tile is done: P and O are free
-      if (j >= 1 && !mbar_wait(&S.p_empty, (j - 1) & 1, abort_flag)) {
-        ok = false;
-        break;
+      // to scale O, the O product of the previous tile must be done (that of
+      // tile j - 2 is: S of tile j was written after it)
+      const bool scale = j >= 1 && __any_sync(0xFFFFFFFFu, raise);
+      if (scale) {
+        if (!mbar_wait(&S.o_done, (j - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
       }
-      tc_fence_after();
-      if (j >= 1 && __any_sync(0xFFFFFFFFu, raise)) {  // scale this warp's rows and columns of O
+      if (scale) {  // scale this warp's rows and columns of O
 #pragma unroll
         for (int ch = 0; ch < DH / 64; ++ch) {
           float o[32];
@@ -401,12 +417,12 @@ __global__ void __launch_bounds__(kBtThreads, 1)
       }
       l *= alpha;
       m = m_new;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.s_empty[b]);  // S is in registers: the buffer may refill
-      // pass B: P = 2^(s c - m), its half-row sum, and its two bf16 parts into the A operands
+      // pass B: P = 2^(s c - m), its half-row sum, and its two bf16 parts into
+      // TMEM over this tile's S (both warps of the pair have read S: the
+      // exchange above came after their loads)
       const unsigned long long nm2 = f2_pack(-m, -m);
       unsigned long long acc2 = 0ull;
+      float phi[32], plo[32];  // bf16 pairs: keys c_lo + 2i, c_lo + 2i + 1 in entry i
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         float* v = reinterpret_cast<float*>(ch == 0 ? va : vb);
@@ -414,36 +430,29 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         for (int e = 0; e < 32; e += 2) {
           float e0, e1;
           f2_unpack(f2_fma(f2_pack(v[e], v[e + 1]), c2, nm2), &e0, &e1);
-          v[e] = ex2_approx(e0);
-          v[e + 1] = ex2_approx(e1);
+          float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
           if (!full) {
-            if (t0 + ch * 32 + e >= vis) v[e] = 0.f;
-            if (t0 + ch * 32 + e + 1 >= vis) v[e + 1] = 0.f;
+            if (t0 + ch * 32 + e >= vis) p0 = 0.f;
+            if (t0 + ch * 32 + e + 1 >= vis) p1 = 0.f;
           }
-          acc2 = f2_add(acc2, f2_pack(v[e], v[e + 1]));
-        }
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys = 16 bytes of each operand
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int k2 = 0; k2 < 4; ++k2) {
-            const uint32_t b0 = __float_as_uint(v[q8 * 8 + 2 * k2]), b1 = __float_as_uint(v[q8 * 8 + 2 * k2 + 1]);
-            hi[k2] = __byte_perm(b0, b1, 0x7632);  // the upper halves: bf16 by truncation
-            float r0, r1;
-            f2_unpack(f2_add(f2_pack(v[q8 * 8 + 2 * k2], v[q8 * 8 + 2 * k2 + 1]),
-                             f2_pack(-__uint_as_float(b0 & 0xFFFF0000u), -__uint_as_float(b1 & 0xFFFF0000u))),
-                      &r0, &r1);
-            lo[k2] = ba_bf2(r0, r1);
-          }
-          const uint32_t off = bt_sw(row, c_lo + ch * 32 + q8 * 8, 128);
-          *reinterpret_cast<uint4*>(S.p_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(S.p_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          acc2 = f2_add(acc2, f2_pack(p0, p1));
+          const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+          const uint32_t hi = __byte_perm(b0, b1, 0x7632);  // the upper halves: bf16 by truncation
+          float r0, r1;
+          f2_unpack(f2_add(f2_pack(p0, p1),
+                           f2_pack(-__uint_as_float(b0 & 0xFFFF0000u), -__uint_as_float(b1 & 0xFFFF0000u))),
+                    &r0, &r1);
+          phi[ch * 16 + e / 2] = __uint_as_float(hi);
+          plo[ch * 16 + e / 2] = __uint_as_float(ba_bf2(r0, r1));
         }
       }
+      const uint32_t pt = lane_base + b * 128 + half * 32;  // this warp's 32 columns of each part
+      tmem_store32(pt, phi);
+      tmem_store32(pt + 64, plo);
+      tmem_wait_st();
       float s0, s1;
       f2_unpack(acc2, &s0, &s1);
       l += s0 + s1;
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.p_full);
