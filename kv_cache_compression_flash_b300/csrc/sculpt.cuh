@@ -74,31 +74,33 @@ __device__ __forceinline__ void ba_split(float x0, float x1, uint32_t& hi, uint3
 // ---- block attention on tcgen05 ---------------------------------------------
 // One CTA per 128-row query tile (Gt heads of one KV group x P = 128 / Gt
 // window positions, as in the scoring passes), looping over the block's keys
-// 128 at a time:
-//   S = Q K^T                 tcgen05.mma into TMEM (two buffers)
-//   P = 2^(S c - m)           eight softmax warps, two per TMEM lane quarter,
-//                             each taking 64 of a tile row's 128 keys; the pair
-//                             combines its half maxima through two spare TMEM
-//                             columns (both warps reach the same lanes; an
-//                             mbarrier per pair orders them): the row max m in the log2
-//                             domain is raised only when a row's tile max
-//                             exceeds it by kBtRescale, and then the row's O
-//                             and sum are scaled by 2^(m_old - m_new); P is
-//                             split into a high part (its upper 16 bits: bf16
-//                             by truncation) and the bf16 of the remainder (16
+// 128 at a time.  The key tiles alternate between two softmax groups of four
+// warps (group g takes tiles j = g, g + 2, ...; warp w of a group reads TMEM
+// lanes 32 (w % 4) .., one query row a thread, all 128 keys of its tile); each
+// group keeps its own running max m, sum l and output accumulator O_g, so the
+// groups never wait on each other and one group's softmax overlaps the other
+// group's products on the tensor pipe:
+//   S = Q K^T                 tcgen05.mma into TMEM buffer j & 1
+//   P = 2^(S c - m_g)         the row max m_g in the log2 domain is raised
+//                             only when a row's tile max exceeds it by
+//                             kBtRescale, and then the row's O_g and l_g are
+//                             scaled by 2^(m_old - m_new); P is split into a
+//                             high part (its upper 16 bits: bf16 by
+//                             truncation) and the bf16 of the remainder (16
 //                             significant bits together), written as bf16
 //                             pairs into TMEM over the tile's own S columns
-//   O += P_hi V + P_lo V      two tcgen05.mma into TMEM, A = P read from TMEM,
+//   O_g += P_hi V + P_lo V    two tcgen05.mma into TMEM, A = P read from TMEM,
 //                             V straight from its TMA tile as an MN-major B
 //                             operand (channels contiguous; the instruction's
 //                             transpose bit)
-// and at the end Y = O / l, lse = (m + log2 l) ln 2.  Warp 8 issues TMA
-// (K and V each in a 3-stage ring), warp 9 the MMAs; every wait is bounded.
-// Two S/P buffers: S of tile j + 2 goes into buffer j & 1 once the O product
-// of tile j has read its P; the softmax waits for the O product of tile j - 1
-// only when it has to scale O.
+// and at the end the two groups' parts are merged, m = max(m_0, m_1),
+// O = sum_g 2^(m_g - m) O_g, l likewise, Y = O / l, lse = (m + log2 l) ln 2
+// (group g writes channels g DH / 2 .. of Y).  Warp 8 issues TMA (K and V
+// each in a 3-stage ring), warp 9 the MMAs: S of tile j + 2 goes into buffer
+// j & 1 once the O product of tile j has read its P.  Every wait is bounded.
+// TMEM: S/P buffers at columns 0 and 128, O_0 at 256, O_1 at 256 + DH.
 constexpr int kBtThreads = 320;
-constexpr int kBtSoftWarps = 8;
+constexpr int kBtSoftWarps = 8;  // two groups of four
 constexpr int kBtTmaWarp = 8, kBtMmaWarp = 9;
 constexpr int kBtKStages = 3;
 constexpr int kBtVStages = 3;
@@ -110,7 +112,7 @@ struct BtSmem {
   uint8_t k[kBtKStages][TileCfg<DH>::kTileBytes];  // 128 keys x DH
   uint8_t v[kBtVStages][TileCfg<DH>::kTileBytes];  // 128 keys x DH as TMA brings it: the MN-major B operand
   uint64_t q_full, k_full[kBtKStages], k_empty[kBtKStages], v_full[kBtVStages], v_empty[kBtVStages], s_full[2],
-      s_free[2], p_full, o_done, o_full, drain, xch[4];
+      p_full[2], pv_done[2], o_full, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -131,6 +133,19 @@ __device__ __forceinline__ void tmem_store32(uint32_t taddr, const float (&v)[32
       "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]),
       "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]),
       "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+// barrier `id` (not 0: __syncthreads) over the first `n` threads of the CTA
+__device__ __forceinline__ void named_barrier_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// 16 consecutive 32-bit columns of this thread's TMEM lane, written back
+__device__ __forceinline__ void tmem_store16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -219,11 +234,9 @@ __global__ void __launch_bounds__(kBtThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.s_full[b], 1);
-      mbar_init(&S.s_free[b], 1);  // the O product that read P from the buffer is done
+      mbar_init(&S.p_full[b], kBtSoftWarps / 2);  // the four warps of group b
+      mbar_init(&S.pv_done[b], 1);                // the O product that read P from buffer b is done
     }
-    for (int q = 0; q < 4; ++q) mbar_init(&S.xch[q], 2);  // the two warps of a lane quarter
-    mbar_init(&S.p_full, kBtSoftWarps);
-    mbar_init(&S.o_done, 1);
     mbar_init(&S.o_full, 1);
     mbar_init(&S.drain, 1);
     S.abort_flag = 0;
@@ -238,7 +251,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
   tc_fence_after();
   pdl_wait();
   pdl_trigger();
-  const uint32_t tmem = S.tmem_base;  // S buffers at columns 0 and 128, O at 256
+  const uint32_t tmem = S.tmem_base;  // S/P buffers at columns 0 and 128, O_0 at 256, O_1 at 256 + DH
   volatile int* abort_flag = &S.abort_flag;
   constexpr uint32_t kTile = TileCfg<DH>::kTileBytes;
 
@@ -280,32 +293,37 @@ __global__ void __launch_bounds__(kBtThreads, 1)
   } else if (warp == kBtMmaWarp) {
     if (lane == 0) {  // MMA issuer
       bool ok = mbar_wait(&S.q_full, 0, abort_flag);
-      auto mma_s = [&](int j) {
-        const int s = j % kBtKStages, b = j & 1;
+      auto mma_s = [&](int j) {  // S of tile j into buffer j & 1
+        const int s = j % kBtKStages;
         if (!mbar_wait(&S.k_full[s], (j / kBtKStages) & 1, abort_flag)) return false;
-        if (j >= 2 && !mbar_wait(&S.s_free[b], ((j >> 1) - 1) & 1, abort_flag)) return false;
         tc_fence_after();
-        issue_tile_mma<DH>(tmem + b * 128, smem_u32(S.q), smem_u32(S.k[s]));
+        issue_tile_mma<DH>(tmem + (j & 1) * 128, smem_u32(S.q), smem_u32(S.k[s]));
         umma_commit(&S.k_empty[s]);
-        umma_commit(&S.s_full[b]);
+        umma_commit(&S.s_full[j & 1]);
         return true;
       };
       if (ok) ok = mma_s(0);
+      if (ok && n_kt > 1) ok = mma_s(1);
       for (int j = 0; j < n_kt && ok; ++j) {
-        if (j + 1 < n_kt && !(ok = mma_s(j + 1))) break;
-        const int sv = j % kBtVStages;
-        if (!mbar_wait(&S.p_full, j & 1, abort_flag) ||
+        const int b = j & 1, sv = j % kBtVStages;
+        if (!mbar_wait(&S.p_full[b], (j >> 1) & 1, abort_flag) ||
             !mbar_wait(&S.v_full[sv], (j / kBtVStages) & 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t pb_t = tmem + (j & 1) * 128;  // P of tile j sits over its S
-        bt_issue_pv<DH>(tmem + 256, pb_t, smem_u32(S.v[sv]), j > 0);
-        bt_issue_pv<DH>(tmem + 256, pb_t + 64, smem_u32(S.v[sv]), true);
+        const uint32_t pt = tmem + b * 128, ot = tmem + 256 + b * DH;  // P of tile j sits over its S
+        bt_issue_pv<DH>(ot, pt, smem_u32(S.v[sv]), j >= 2);
+        bt_issue_pv<DH>(ot, pt + 64, smem_u32(S.v[sv]), true);
         umma_commit(&S.v_empty[sv]);
-        umma_commit(&S.s_free[j & 1]);
-        umma_commit(&S.o_done);
+        if (j + 2 < n_kt) {  // the buffer takes S of tile j + 2 once this product has read P
+          umma_commit(&S.pv_done[b]);
+          if (!mbar_wait(&S.pv_done[b], (j >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ok = mma_s(j + 2);
+        }
       }
       if (ok) umma_commit(&S.o_full);
       if (*abort_flag) {
@@ -314,8 +332,8 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         mbar_wait(&S.drain, 0, &never);
       }
     }
-  } else {  // warps 0-7: softmax; warp w takes TMEM lanes 32 (w % 4).. and keys 64 (w / 4) .. + 63 of every tile
-    const int q4 = warp & 3, half = warp >> 2;
+  } else {  // warps 0-7: softmax; group grp = warp / 4 takes tiles grp, grp + 2, ...; TMEM lanes 32 (warp % 4) ..
+    const int grp = warp >> 2, q4 = warp & 3;
     const int row = q4 * 32 + lane;
     const int hl = row / P, pos = pb * P + row % P;
     const int posc = min(pos, W - 1);
@@ -325,158 +343,169 @@ __global__ void __launch_bounds__(kBtThreads, 1)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) vis_w = min(vis_w, __shfl_xor_sync(0xFFFFFFFFu, vis_w, o));
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
-    const int c_lo = half * 64;                 // this warp's keys of a tile, and its columns of O
-    const int o_lo = half * (DH / 2);
+    const uint32_t sb = lane_base + grp * 128;       // this group's S/P buffer
+    const uint32_t ob = lane_base + 256 + grp * DH;  // and its O
     const float c = c_log2;
     const unsigned long long c2 = f2_pack(c, c);
     float m = -INFINITY, l = 0.f;
-    uint32_t va[32], vb[32];
     bool ok = true;
-    int nx = 0;  // exchanges done (the pair's mbarrier phase)
-    // this lane's value for the partner warp, through TMEM column 448 + 2 (exchange parity) + half
-    auto exchange = [&](float mine, float* other) {
-      tmem_store1(lane_base + 448 + 2 * (nx & 1) + half, mine);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.xch[q4]);
-      if (!mbar_wait(&S.xch[q4], nx & 1, abort_flag)) return false;
-      tc_fence_after();
-      *other = tmem_load1(lane_base + 448 + 2 * (nx & 1) + (half ^ 1));
-      ++nx;
-      return true;
-    };
-    for (int j = 0; j < n_kt && ok; ++j) {
-      const int b = j & 1, t0 = j * 128 + c_lo;
-      const bool full = t0 + 64 <= vis_w;  // every key of the warp's half tile is visible to all its rows
-      if (!mbar_wait(&S.s_full[b], (j >> 1) & 1, abort_flag)) {
+    for (int j = grp; j < n_kt; j += 2) {
+      const int t0 = j * 128;
+      const bool full = t0 + 128 <= vis_w;  // every key of the tile is visible to all the warp's rows
+      const int lim = vis - t0;             // keys of the tile this row sees (may be <= 0 or >= 128)
+      if (!mbar_wait(&S.s_full[grp], (j >> 1) & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t sb = lane_base + b * 128 + c_lo;
-      // pass A: the half tile's row max, masked keys left out; then the whole row's, from the partner
-      tmem_issue32(sb, va);
-      tmem_issue32(sb + 32, vb);
-      tmem_wait32(va);
-      tmem_wait32(vb);
+      // the tile's row max, masked keys left out: keys 0-63 first, then 64-127
+      // (kept in registers; 0-63 are read again for P)
+      auto mask = [&](uint32_t (&r)[32], int k0) {  // keys the row does not see: -inf (2^-inf = 0 in P)
+        if (!full) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (k0 + e >= lim) r[e] = 0xFF800000u;
+        }
+      };
+      auto chunk_max = [&](const uint32_t (&r)[32], int k0) {
+        const float* x = reinterpret_cast<const float*>(r);
+        float u[11];
+#pragma unroll
+        for (int k = 0; k < 10; ++k) u[k] = fmax3(x[3 * k], x[3 * k + 1], x[3 * k + 2]);
+        u[10] = fmaxf(x[30], x[31]);
+        return fmax3(fmax3(u[0], u[1], u[2]), fmax3(u[3], u[4], u[5]), fmax3(u[6], u[7], fmax3(u[8], u[9], u[10])));
+      };
       float z;
       {
-        const float* x = reinterpret_cast<const float*>(va);
-        const float* y = reinterpret_cast<const float*>(vb);
-        if (full) {
-          float t[22];
-#pragma unroll
-          for (int k = 0; k < 10; ++k) t[k] = fmax3(x[3 * k], x[3 * k + 1], x[3 * k + 2]);
-          t[10] = fmaxf(x[30], x[31]);
-#pragma unroll
-          for (int k = 0; k < 10; ++k) t[11 + k] = fmax3(y[3 * k], y[3 * k + 1], y[3 * k + 2]);
-          t[21] = fmaxf(y[30], y[31]);
-          z = t[0];
-#pragma unroll
-          for (int k = 1; k < 21; k += 2) z = fmax3(z, t[k], t[k + 1]);
-          z = fmaxf(z, t[21]);
-        } else {
-          z = -INFINITY;
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            if (t0 + e < vis) z = fmaxf(z, x[e]);
-            if (t0 + 32 + e < vis) z = fmaxf(z, y[e]);
-          }
-        }
+        uint32_t ra[32], rb[32];
+        tmem_issue32(sb, ra);
+        tmem_issue32(sb + 32, rb);
+        tmem_wait32(ra);
+        tmem_wait32(rb);
+        mask(ra, 0);
+        mask(rb, 32);
+        z = fmaxf(chunk_max(ra, 0), chunk_max(rb, 32));
       }
-      float zo;
-      if (!exchange(z, &zo)) {
-        ok = false;
-        break;
-      }
-      z = fmaxf(z, zo) * c;
+      uint32_t rc[32], rd[32];
+      tmem_issue32(sb + 64, rc);
+      tmem_issue32(sb + 96, rd);
+      tmem_wait32(rc);
+      tmem_wait32(rd);
+      mask(rc, 64);
+      mask(rd, 96);
+      z = fmax3(z, chunk_max(rc, 64), chunk_max(rd, 96));
+      z *= c;
+      // raised only past the margin (never by a tile with no visible key: z = -inf)
+      const bool raise = z > m + kBtRescale;
       float alpha = 1.f;
-      const bool raise = m == -INFINITY || z > m + kBtRescale;
-      const float m_new = raise ? fmaxf(m, z) : m;
-      if (raise) alpha = ex2_approx(m - m_new);  // 0 on the first tile
-      // to scale O, the O product of the previous tile must be done (that of
-      // tile j - 2 is: S of tile j was written after it)
-      const bool scale = j >= 1 && __any_sync(0xFFFFFFFFu, raise);
-      if (scale) {
-        if (!mbar_wait(&S.o_done, (j - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
-      if (scale) {  // scale this warp's rows and columns of O
-#pragma unroll
-        for (int ch = 0; ch < DH / 64; ++ch) {
-          float o[32];
-          tmem_load32(lane_base + 256 + o_lo + ch * 32, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_store32(lane_base + 256 + o_lo + ch * 32, o);
-        }
-        tmem_wait_st();
+      if (raise) {
+        alpha = ex2_approx(m - z);  // 0 on the row's first visible tile
+        m = z;
       }
       l *= alpha;
-      m = m_new;
-      // pass B: P = 2^(s c - m), its half-row sum, and its two bf16 parts into
-      // TMEM over this tile's S (both warps of the pair have read S: the
-      // exchange above came after their loads)
-      const unsigned long long nm2 = f2_pack(-m, -m);
+      // P = 2^(s c - m), its row sum, and its two bf16 parts into TMEM over
+      // this tile's S: keys 2i, 2i + 1 of the tile as a bf16 pair in column i
+      // (high part) and 64 + i (low part).  Keys 0-63 are read again first
+      // (their parts land on columns 0-31 and 64-95: S of keys 0-31, read,
+      // and of keys 64-95, in registers); keys 64-127 come from registers.
+      const float m_sub = m == -INFINITY ? 0.f : m;  // a row with no visible key yet: P = 0, not NaN
+      const unsigned long long nm2 = f2_pack(-m_sub, -m_sub);
       unsigned long long acc2 = 0ull;
-      float phi[32], plo[32];  // bf16 pairs: keys c_lo + 2i, c_lo + 2i + 1 in entry i
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        float* v = reinterpret_cast<float*>(ch == 0 ? va : vb);
+      auto chunk_p = [&](const uint32_t (&r)[32], int q) {
+        const float* x = reinterpret_cast<const float*>(r);
+        uint32_t hi[16], lo[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float e0, e1;
-          f2_unpack(f2_fma(f2_pack(v[e], v[e + 1]), c2, nm2), &e0, &e1);
-          float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
-          if (!full) {
-            if (t0 + ch * 32 + e >= vis) p0 = 0.f;
-            if (t0 + ch * 32 + e + 1 >= vis) p1 = 0.f;
-          }
+          f2_unpack(f2_fma(f2_pack(x[e], x[e + 1]), c2, nm2), &e0, &e1);
+          const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
           acc2 = f2_add(acc2, f2_pack(p0, p1));
           const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-          const uint32_t hi = __byte_perm(b0, b1, 0x7632);  // the upper halves: bf16 by truncation
+          hi[e / 2] = __byte_perm(b0, b1, 0x7632);  // the upper halves: bf16 by truncation
           float r0, r1;
           f2_unpack(f2_add(f2_pack(p0, p1),
                            f2_pack(-__uint_as_float(b0 & 0xFFFF0000u), -__uint_as_float(b1 & 0xFFFF0000u))),
                     &r0, &r1);
-          phi[ch * 16 + e / 2] = __uint_as_float(hi);
-          plo[ch * 16 + e / 2] = __uint_as_float(ba_bf2(r0, r1));
+          lo[e / 2] = ba_bf2(r0, r1);
+        }
+        tmem_store16(sb + q * 16, hi);
+        tmem_store16(sb + 64 + q * 16, lo);
+      };
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t ra[32];
+        tmem_load32(sb + q * 32, reinterpret_cast<float(&)[32]>(ra));
+        mask(ra, q * 32);
+        chunk_p(ra, q);
+      }
+      chunk_p(rc, 2);
+      chunk_p(rd, 3);
+      // scale this warp's rows of O_g (after P, with S out of the registers):
+      // its last product (tile j - 2) is done, for S of tile j was issued
+      // after it had read its P
+      if (j >= 2 && __any_sync(0xFFFFFFFFu, raise)) {
+#pragma unroll
+        for (int ch = 0; ch < DH / 32; ++ch) {
+          float o[32];
+          tmem_load32(ob + ch * 32, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_store32(ob + ch * 32, o);
         }
       }
-      const uint32_t pt = lane_base + b * 128 + half * 32;  // this warp's 32 columns of each part
-      tmem_store32(pt, phi);
-      tmem_store32(pt + 64, plo);
       tmem_wait_st();
       float s0, s1;
       f2_unpack(acc2, &s0, &s1);
       l += s0 + s1;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.p_full);
+      if (lane == 0) mbar_arrive(&S.p_full[grp]);
     }
-    float lo_sum = 0.f;
-    if (ok && exchange(l, &lo_sum) && mbar_wait(&S.o_full, 0, abort_flag)) {
+    // merge the two groups' parts: each thread leaves its row's m_g and l_g
+    // in columns 2 grp, 2 grp + 1 of buffer 0 (free: every product is done)
+    const bool good = ok && mbar_wait(&S.o_full, 0, abort_flag);
+    if (good) {
       tc_fence_after();
-      const float lt = l + lo_sum;  // the whole row's sum (the same in both warps of the pair)
+      tmem_store1(lane_base + 2 * grp, m);
+      tmem_store1(lane_base + 2 * grp + 1, l);
+    }
+    tc_fence_before();
+    named_barrier_sync(1, kBtSoftWarps * 32);  // every softmax warp reaches it once
+    tc_fence_after();
+    if (good && !*abort_flag) {
+      const float m_o = tmem_load1(lane_base + 2 * (grp ^ 1));
+      const float l_o = tmem_load1(lane_base + 2 * (grp ^ 1) + 1);
+      const float m0 = grp == 0 ? m : m_o, l0 = grp == 0 ? l : l_o;
+      const float m1 = grp == 0 ? m_o : m, l1 = grp == 0 ? l_o : l;
+      const bool two = n_kt > 1;  // O_1 holds a product
+      const float mt = two ? fmaxf(m0, m1) : m0;
+      const float a0 = ex2_approx(m0 - mt), a1 = two ? ex2_approx(m1 - mt) : 0.f;
+      const float lt = l0 * a0 + l1 * a1;
       const bool store = pos < W && hl < Gt;
       const long long hd = h0 + hl;
+      const int o_lo = grp * (DH / 2);  // this group's channels of Y
       float* yr = Y + (hd * W + posc) * DH + o_lo;
       const float inv = 1.f / lt;
+      const float w0 = a0 * inv, w1 = a1 * inv;
 #pragma unroll
       for (int ch = 0; ch < DH / 64; ++ch) {
-        float o[32];
+        float o[32], o1[32];
         tmem_load32(lane_base + 256 + o_lo + ch * 32, o);
+        if (two) {
+          tmem_load32(lane_base + 256 + DH + o_lo + ch * 32, o1);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = o[e] * w0 + o1[e] * w1;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= w0;
+        }
         if (store) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(yr + ch * 32 + e) = make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv,
-                                                                       o[e + 3] * inv);
+            *reinterpret_cast<float4*>(yr + ch * 32 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
         }
       }
-      if (store && lse && half == 0) lse[hd * W + posc] = (m + lg2_approx(lt)) * kLn2;
+      if (store && lse && grp == 0) lse[hd * W + posc] = (mt + lg2_approx(lt)) * kLn2;
     }
   }
   tc_fence_before();
