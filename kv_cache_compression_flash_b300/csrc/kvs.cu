@@ -1003,6 +1003,15 @@ int kvs_block_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
   if (rc) return rc;
   const dim3 grid(static_cast<unsigned>(Hkv * n_hc * n_pb));
   const int Wi = static_cast<int>(W), p0 = static_cast<int>(q_pos0), nb = static_cast<int>(n_block);
+  // the kernel's register split must fit the registers it is launched with
+  // (otherwise the softmax warpgroups would wait for registers forever)
+  auto split_fits = [](const void* kern) {
+    cudaFuncAttributes fa{};
+    return cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.numRegs * kBtThreads >= kBtRegPool;
+  };
+  if (!split_fits(reinterpret_cast<const void*>(d == 64 ? block_attention_tc_kernel<64>
+                                                        : block_attention_tc_kernel<128>)))
+    return KVS_ERR_UNSUPPORTED;
   if (d == 64) {
     const size_t smem = sizeof(BtSmem<64>) + 1024;
     KVS_CUDA_TRY(allow_smem(block_attention_tc_kernel<64>, smem));
@@ -1072,10 +1081,16 @@ int kvs_ridge_values(const uint16_t* Qt, const uint16_t* Kc, const float* Y, int
                         static_cast<const float*>(A), static_cast<const float*>(A), Ri, ki, ki, lam, 1, 1, M));
   KVS_CUDA_TRY(launch_k(ridge_atb_kernel, dim3(dt, kt, static_cast<unsigned>(Hkv)), dim3(256), 0, st, 0,
                         static_cast<const float*>(A), Y, Ri, ki, di, lam, 0, 0, B));
-  const size_t solve_smem = ridge_solve_smem(ki);
-  KVS_CUDA_TRY(allow_smem(ridge_solve_kernel, solve_smem));
-  KVS_CUDA_TRY(launch_k(ridge_solve_kernel, dim3(static_cast<unsigned>(Hkv)), dim3(kRidgeSolveThreads), solve_smem,
-                        st, 0, M, B, ki, di, Vc));
+  const dim3 gsolve(kRsCluster, static_cast<unsigned>(Hkv));  // a cluster of kRsCluster CTAs per head
+  if (d == 64) {
+    KVS_CUDA_TRY(allow_smem(ridge_solve_cluster_kernel<64>, kRsSmemBytes));
+    KVS_CUDA_TRY(launch_k(ridge_solve_cluster_kernel<64>, gsolve, dim3(kRsThreads), kRsSmemBytes, st, kRsCluster,
+                          static_cast<const float*>(M), static_cast<const float*>(B), ki, Vc));
+  } else {
+    KVS_CUDA_TRY(allow_smem(ridge_solve_cluster_kernel<128>, kRsSmemBytes));
+    KVS_CUDA_TRY(launch_k(ridge_solve_cluster_kernel<128>, gsolve, dim3(kRsThreads), kRsSmemBytes, st, kRsCluster,
+                          static_cast<const float*>(M), static_cast<const float*>(B), ki, Vc));
+  }
   KVS_CUDA_TRY(cudaGetLastError());
   return KVS_OK;
 }

@@ -13,11 +13,13 @@
 //   ridge_atb_kernel            C = P^T Q (+ lam I), 64 x 64 output tiles with
 //       4 x 4 per thread over 16-row slices of P [R, m] and Q [R, n]: gives
 //       A^T A + lam I (lower triangle) and A^T Y.
-//   ridge_solve_kernel          one CTA per head: Cholesky of A^T A + lam I in
-//       place by panels of 32 columns, then the forward and backward
-//       substitutions for the d right-hand sides, also by blocks of 32 rows.
+//   ridge_solve_cluster_kernel<DH>  a cluster of 8 CTAs per head: blocked
+//       Cholesky of A^T A + lam I and the forward and backward solves for
+//       the d right-hand sides, the matrix in the cluster's shared memory.
 // A^T A, A^T Y and the solve are fp32 on the FMA pipes.
 #pragma once
+
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 
@@ -25,7 +27,6 @@ namespace kvs {
 
 constexpr int kRidgeMaxK = 512;
 constexpr int kRidgeMaxD = 128;
-constexpr int kRidgeSolveThreads = 1024;
 
 // ---- mma.sync helpers (the ridge's softmax): m16n8k16, bf16 -> fp32 ----
 constexpr int kBaThreads = 128;  // 4 warps x 16 rows
@@ -97,9 +98,16 @@ __device__ __forceinline__ void ba_split(float x0, float x1, uint32_t& hi, uint3
 // O = sum_g 2^(m_g - m) O_g, l likewise, Y = O / l, lse = (m + log2 l) ln 2
 // (group g writes channels g DH / 2 .. of Y).  Warp 8 issues TMA (K and V
 // each in a 3-stage ring), warp 9 the MMAs: S of tile j + 2 goes into buffer
-// j & 1 once the O product of tile j has read its P.  Every wait is bounded.
+// j & 1 once the O product of tile j has read its P.  Warps 10 and 11 only
+// complete the third warpgroup, which hands its registers to the softmax
+// warpgroups (setmaxnreg), so the softmax runs without register spills.  Every
+// wait is bounded.
 // TMEM: S/P buffers at columns 0 and 128, O_0 at 256, O_1 at 256 + DH.
-constexpr int kBtThreads = 320;
+constexpr int kBtThreads = 384;  // three warpgroups: softmax groups 0 and 1, then TMA, MMA and two idle warps
+// registers a thread after the split: the softmax warpgroups take what the
+// third gives up (the sum stays within the launch's threads x registers)
+constexpr int kBtRegsSoft = 216, kBtRegsCtl = 56;
+constexpr int kBtRegPool = 2 * 128 * kBtRegsSoft + 128 * kBtRegsCtl;
 constexpr int kBtSoftWarps = 8;  // two groups of four
 constexpr int kBtTmaWarp = 8, kBtMmaWarp = 9;
 constexpr int kBtKStages = 3;
@@ -255,6 +263,8 @@ __global__ void __launch_bounds__(kBtThreads, 1)
   volatile int* abort_flag = &S.abort_flag;
   constexpr uint32_t kTile = TileCfg<DH>::kTileBytes;
 
+  if (warp >= kBtSoftWarps) {  // the third warpgroup gives registers up, then its TMA and MMA warps run
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBtRegsCtl));
   if (warp == kBtTmaWarp) {
     if (lane == 0) {  // TMA producer
       prefetch_tensormap(&mapQ);
@@ -332,7 +342,9 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         mbar_wait(&S.drain, 0, &never);
       }
     }
+  }
   } else {  // warps 0-7: softmax; group grp = warp / 4 takes tiles grp, grp + 2, ...; TMEM lanes 32 (warp % 4) ..
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBtRegsSoft));
     const int grp = warp >> 2, q4 = warp & 3;
     const int row = q4 * 32 + lane;
     const int hl = row / P, pos = pb * P + row % P;
@@ -720,153 +732,335 @@ __global__ void __launch_bounds__(256) ridge_atb_kernel(const float* __restrict_
     }
 }
 
-// In place: the lower triangle of M[g] (k x k) becomes its Cholesky factor L,
-// B[g] (k x d) becomes L^-1 A^T Y and Vc[g] = L^-T L^-1 A^T Y.  Blocked by
-// panels of kCholNb columns: the panel's diagonal block is factored by one warp
-// in shared memory, the rows below it are solved against it (one thread per
-// row, the row in registers) and kept in shared memory, and the trailing lower
-// triangle takes the panel's rank-32 update (one warp per row, one lane per
-// column).  The two triangular solves go panel by panel too: the block of 32
-// rows first takes the product with every solved row (thread = row x channel),
-// then its 32 x 32 triangle is solved in registers (one thread per channel).
-// A pivot that is not positive records KVS_ERR_RANGE and the head's values
-// are 0.
-constexpr int kCholNb = 32;
-constexpr int kCholLd = kCholNb + 1;  // panel row stride in shared memory (no bank conflicts)
+// ---- ridge solve across a cluster ---------------------------------------------
+// (A^T A + lam I) Vc = A^T Y for each head: a blocked Cholesky factorisation
+// L L^T and two blocked triangular solves, on a cluster of kRsCluster CTAs
+// per head that hold the matrix in their shared memory.  The k x k matrix is
+// padded with the identity to nblk <= 16 row blocks of 32 (a padded row
+// solves to 0); block i lives in CTA i (i < 8) or 15 - i (i >= 8): its rows,
+// columns 0 .. 32 i + 31 (the lower triangle up to its diagonal block), so
+// every CTA holds 17 blocks' worth of columns and the updates of one column
+// step are spread evenly.  Column step b:
+//   the owner of block b factors the diagonal block in one warp (L_bb) and
+//   inverts it, one lane per column; cluster barrier;
+//   every CTA turns its blocks i > b into L_ib = M_ib L_bb^-T (L_bb^-1 read
+//   from the owner); cluster barrier;
+//   every CTA copies the rows of the column panel L_jb (j > b) it needs from
+//   their owners and updates its blocks, M_ij -= L_ib L_jb^T for b < j <= i,
+//   8 x 4 outputs a thread.
+// The diagonal block is factored and inverted in registers (warp shuffles).
+// The two solves split the d channels over the cluster (CTA r takes
+// d / 8 of them for every row) and need no further barrier: the forward solve
+// L y = A^T Y takes y_b = L_bb^-1 (r_b - L_b,0:b y_0:b) block by block with
+// row block b of L read from its owner, the backward solve L^T x = y takes
+// x_b = L_bb^-T (y_b - sum_{i > b} L_ib^T x_i) from the last block up with
+// column block b read from the owners of the blocks below.  fp32 FMA
+// throughout.  A pivot that is not positive
+// records KVS_ERR_RANGE and the head's values are 0.
+constexpr int kRsCluster = 8;
+constexpr int kRsThreads = 512;
+constexpr int kRsMaxBlocks = kRidgeMaxK / 32;  // 16 = 2 kRsCluster
+constexpr int kRsLd = 33;                      // a 32 x 32 block in shared memory
+constexpr int kRsBlk = 32 * kRsLd;
+constexpr int kRsLdAt = 36;                        // a transposed panel block L_ib^T
+constexpr int kRsLdp = 32 * (kRsMaxBlocks - 1) + 4;  // the column panel, transposed: 32 x (rows below the diagonal)
+// shared memory layout (floats), the same in every CTA of the cluster
+constexpr int kRsOffB = 32 * (32 * (kRsMaxBlocks + 1) + 8);  // after the rows of the CTA's two blocks
+constexpr int kRsOffAt = kRsOffB + 2 * 32 * kRidgeMaxD;       // the solves' right-hand sides (the CTA's channels)
+constexpr int kRsOffPt = kRsOffAt + 2 * 32 * kRsLdAt;         // panel; in the solves a row or column block of L
+constexpr int kRsOffDinv = kRsOffPt + 32 * kRsLdp;            // L_bb^-1 of the two blocks
+constexpr int kRsOffTinv = kRsOffDinv + 2 * kRsBlk;           // a copy of the current L_bb^-1
+constexpr int kRsOffDiag = kRsOffTinv + kRsBlk;               // the diagonal block being factored
+constexpr int kRsOffFlag = kRsOffDiag + kRsBlk;               // a pivot was not positive
+constexpr size_t kRsSmemBytes = static_cast<size_t>(kRsOffFlag + 4) * sizeof(float);
+static_assert(kRidgeMaxK * (kRidgeMaxD / kRsCluster) <= 2 * 32 * kRidgeMaxD, "the channel slice fits");
+static_assert(32 * (kRidgeMaxK - 32) <= 32 * kRsLdp, "a row or column block of L fits in the panel's space");
+static_assert(kRsMaxBlocks == 2 * kRsCluster, "two blocks per CTA");
 
-inline size_t ridge_solve_smem(int k) { return static_cast<size_t>(k) * kCholLd * sizeof(float); }
+__device__ __forceinline__ int rs_owner(int i) { return i < kRsCluster ? i : 2 * kRsCluster - 1 - i; }
+__device__ __forceinline__ int rs_slot(int i) { return i < kRsCluster ? 0 : 1; }
+// row stride of block i's rows at its owner, and where they start there
+__device__ __forceinline__ int rs_ld(int i) { return 32 * (i + 1) + 4; }
+__device__ __forceinline__ int rs_off(int i) { return i < kRsCluster ? 0 : 32 * rs_ld(2 * kRsCluster - 1 - i); }
 
-__global__ void __launch_bounds__(kRidgeSolveThreads) ridge_solve_kernel(float* __restrict__ M, float* __restrict__ B,
-                                                                         int k, int d, float* __restrict__ Vc) {
+// grid (kRsCluster, Hkv), clusters of kRsCluster along x; kRsThreads threads.
+template <int DH>
+__global__ void __launch_bounds__(kRsThreads, 1)
+    ridge_solve_cluster_kernel(const float* __restrict__ M, const float* __restrict__ B, const int k,
+                               float* __restrict__ Vc) {
+  namespace cgr = cooperative_groups;
+  cgr::cluster_group cluster = cgr::this_cluster();
+  extern __shared__ float4 rs_smem4[];
+  float* sm = reinterpret_cast<float*>(rs_smem4);
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int g = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nblk = (k + 31) >> 5;
+  const float* Mg = M + static_cast<long long>(g) * k * k;
+  const float* Bg = B + static_cast<long long>(g) * k * DH;
+  float* Vg = Vc + static_cast<long long>(g) * k * DH;
+  float* PT = sm + kRsOffPt;
+  float* dinv = sm + kRsOffDinv;
+  float* tinv = sm + kRsOffTinv;
+  float* diag = sm + kRsOffDiag;
+  int* flag = reinterpret_cast<int*>(sm + kRsOffFlag);
+  const int own[2] = {rank, 2 * kRsCluster - 1 - rank};  // slot 0 holds the lower block
+  const bool has[2] = {own[0] < nblk, own[1] < nblk};
+  float* Ms[2] = {sm + rs_off(own[0]), sm + rs_off(own[1])};
+  const int lds[2] = {rs_ld(own[0]), rs_ld(own[1])};
+  float* At[2] = {sm + kRsOffAt, sm + kRsOffAt + 32 * kRsLdAt};
+  const int imax = has[1] ? own[1] : own[0];  // the CTA's last block (when it has one)
   pdl_wait();
-  extern __shared__ float s_panel[];  // [k][kCholLd]: the panel's rows below its diagonal block
-  __shared__ float s_diag[kCholNb][kCholLd];
-  __shared__ float s_y[kCholNb * kRidgeMaxD];  // a block of 32 solution rows, [row][channel]
-  __shared__ int s_bad;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  constexpr int kWarps = kRidgeSolveThreads / 32;
-  const int g = blockIdx.x;
-  float* Mg = M + static_cast<long long>(g) * k * k;
-  float* Bg = B + static_cast<long long>(g) * k * d;
-  float* Vg = Vc + static_cast<long long>(g) * k * d;
-  const int nd = d >> 5;  // channels per lane in the row-block products: 2 or 4
-  if (tid == 0) s_bad = 0;
-  __syncthreads();
+
+  // the CTA's rows of M (padded with the identity)
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    if (!has[s]) continue;
+    const int i = own[s], wdt = 32 * (i + 1);
+    for (int e = tid; e < 32 * wdt; e += kRsThreads) {
+      const int rr = e / wdt, c = e - rr * wdt, gr = 32 * i + rr;
+      Ms[s][rr * lds[s] + c] = (gr < k && c < k) ? __ldg(Mg + static_cast<long long>(gr) * k + c)
+                                                 : (gr == c ? 1.f : 0.f);
+    }
+  }
+  if (tid == 0) *flag = 0;
+  cluster.sync();
 
   // ---- factorisation ----
-  for (int J = 0; J < k; J += kCholNb) {
-    const int nb = min(kCholNb, k - J);
-    for (int e = tid; e < kCholNb * kCholNb; e += kRidgeSolveThreads) {
-      const int r = e / kCholNb, c = e % kCholNb;
-      s_diag[r][c] = (r < nb && c <= r) ? Mg[static_cast<long long>(J + r) * k + J + c] : 0.f;
-    }
-    __syncthreads();
-    if (warp == 0) {  // lane r owns row r of the diagonal block
-      for (int c = 0; c < nb; ++c) {
-        const float p = s_diag[c][c];
-        if (!(p > 0.f)) {  // the same value in every lane
-          if (lane == 0) s_bad = 1;
-          break;
-        }
+  bool bad = false;
+  for (int b = 0; b < nblk; ++b) {
+    const int ob = rs_owner(b), sb = rs_slot(b);
+    if (rank == ob && warp == 0) {  // L_bb in registers (lane = row), then L_bb^-1 (lane = column)
+      const float* Db = (sb ? Ms[1] : Ms[0]) + 32 * b;
+      const int ldb = sb ? lds[1] : lds[0];
+      for (int e = lane; e < 32 * 32; e += 32) diag[(e >> 5) * kRsLd + (e & 31)] = Db[(e >> 5) * ldb + (e & 31)];
+      __syncwarp();
+      float a[32];  // row `lane` of the block; the lower triangle becomes L_bb
+#pragma unroll
+      for (int c = 0; c < 32; ++c) a[c] = diag[lane * kRsLd + c];
+      bool ok = true;  // the same value in every lane (no early exit: a[] stays in registers)
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p = __shfl_sync(0xFFFFFFFFu, a[c], c);
+        ok = ok && p > 0.f;
         const float piv = sqrtf(p);
-        __syncwarp();
-        if (lane == c) s_diag[c][c] = piv;
-        if (lane > c && lane < nb) s_diag[lane][c] /= piv;
-        __syncwarp();
-        if (lane > c && lane < nb) {
-          const float lrc = s_diag[lane][c];
-          for (int c2 = c + 1; c2 <= lane; ++c2) s_diag[lane][c2] = fmaf(-lrc, s_diag[c2][c], s_diag[lane][c2]);
+        if (lane == c) a[c] = piv;
+        if (lane > c) a[c] /= piv;
+#pragma unroll
+        for (int c2 = 1; c2 < 32; ++c2) {  // row c2 > c of the trailing block, for the rows that reach it
+          if (c2 > c) {
+            const float l = __shfl_sync(0xFFFFFFFFu, a[c], c2);
+            if (lane >= c2) a[c2] = fmaf(-a[c], l, a[c2]);
+          }
         }
-        __syncwarp();
       }
-      if (lane < nb)
-        for (int c = 0; c <= lane; ++c) Mg[static_cast<long long>(J + lane) * k + J + c] = s_diag[lane][c];
-    }
-    __syncthreads();
-    if (s_bad) break;  // the same value in every thread after the barrier
-    const int t = k - J - nb;  // rows below the diagonal block (nb = kCholNb whenever t > 0)
-    for (int ii = tid; ii < t; ii += kRidgeSolveThreads) {  // x L_JJ^T = M[i, J:J+32], x kept in the panel
-      float* row = Mg + static_cast<long long>(J + nb + ii) * k + J;
-      float* x = s_panel + ii * kCholLd;
-      for (int c = 0; c < kCholNb; ++c) {
-        float v = row[c];
-        for (int c2 = 0; c2 < c; ++c2) v = fmaf(-x[c2], s_diag[c][c2], v);
-        v /= s_diag[c][c];
-        x[c] = v;
-        row[c] = v;
+      if (!ok) {
+        if (lane == 0) *flag = 1;
+      } else {
+        float x[32];  // column `lane` of L_bb^-1: L x = e_lane by forward substitution
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr) {
+          float v = rr == lane ? 1.f : 0.f;
+#pragma unroll
+          for (int q = 0; q < 31; ++q)
+            if (q < rr) v = fmaf(-__shfl_sync(0xFFFFFFFFu, a[q], rr), x[q], v);
+          x[rr] = v / __shfl_sync(0xFFFFFFFFu, a[rr], rr);
+        }
+        float* dv = dinv + sb * kRsBlk;
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr) dv[rr * kRsLd + lane] = x[rr];
       }
     }
-    __syncthreads();
-    for (int ii = warp; ii < t; ii += kWarps) {  // trailing lower triangle
-      const float* pi = s_panel + ii * kCholLd;
-      float* row = Mg + static_cast<long long>(J + nb + ii) * k + J + nb;
-      for (int cc = lane; cc <= ii; cc += 32) {
-        const float* pc = s_panel + cc * kCholLd;
-        float acc = 0.f;
+    cluster.sync();  // L_bb^-1, or the flag, at the owner
+    if (*cluster.map_shared_rank(flag, ob)) {  // the same value in every CTA
+      bad = true;
+      break;
+    }
+    const bool t0 = has[0] && own[0] > b, t1 = has[1] && own[1] > b;  // blocks below the diagonal block
+    if (t0 || t1) {  // L_ib = M_ib L_bb^-T
+      const float* src = cluster.map_shared_rank(dinv + sb * kRsBlk, ob);
+      for (int e = tid; e < kRsBlk; e += kRsThreads) tinv[e] = src[e];
+      __syncthreads();
+      const int rr = tid >> 4, c2 = tid & 15;
+      float a[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (!(s == 0 ? t0 : t1)) continue;
+        const float* mr = Ms[s] + rr * lds[s] + 32 * b;
 #pragma unroll 8
-        for (int q = 0; q < kCholNb; ++q) acc = fmaf(pi[q], pc[q], acc);
-        row[cc] -= acc;
+        for (int q = 0; q < 32; ++q) {
+          const float m = mr[q];
+          a[s][0] = fmaf(m, tinv[c2 * kRsLd + q], a[s][0]);
+          a[s][1] = fmaf(m, tinv[(c2 + 16) * kRsLd + q], a[s][1]);
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (!(s == 0 ? t0 : t1)) continue;
+        float* mr = Ms[s] + rr * lds[s] + 32 * b;
+        mr[c2] = a[s][0];
+        mr[c2 + 16] = a[s][1];
+        At[s][c2 * kRsLdAt + rr] = a[s][0];
+        At[s][(c2 + 16) * kRsLdAt + rr] = a[s][1];
       }
     }
-    __syncthreads();
-  }
-  if (s_bad) {
-    if (tid == 0) record_error(KVS_ERR_RANGE);
-    for (long long e = tid; e < static_cast<long long>(k) * d; e += kRidgeSolveThreads) Vg[e] = 0.f;
-    return;
+    cluster.sync();  // the column panel L_jb, j > b, at the blocks' owners
+    if (t0 || t1) {
+      const int np = (imax - b) * 32;  // the panel's rows this CTA needs (at most 480: one a thread)
+      if (tid < np) {
+        const int jb = b + 1 + (tid >> 5), rr = tid & 31;
+        const float4* src = reinterpret_cast<const float4*>(cluster.map_shared_rank(sm, rs_owner(jb)) + rs_off(jb) +
+                                                            rr * rs_ld(jb) + 32 * b);
+        float4 v[8];
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) v[q4] = src[q4];
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          PT[(4 * q4) * kRsLdp + tid] = v[q4].x;
+          PT[(4 * q4 + 1) * kRsLdp + tid] = v[q4].y;
+          PT[(4 * q4 + 2) * kRsLdp + tid] = v[q4].z;
+          PT[(4 * q4 + 3) * kRsLdp + tid] = v[q4].w;
+        }
+      }
+      __syncthreads();
+      const int cgi = tid & 127, rg = tid >> 7;  // columns 4 cgi .., rows 8 rg ..
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (!(s == 0 ? t0 : t1) || 4 * cgi >= 32 * (own[s] - b)) continue;
+        float acc[8][4];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
+#pragma unroll 4
+        for (int q = 0; q < 32; ++q) {
+          const float4 pv = *reinterpret_cast<const float4*>(PT + q * kRsLdp + 4 * cgi);
+          const float4 x0 = *reinterpret_cast<const float4*>(At[s] + q * kRsLdAt + 8 * rg);
+          const float4 x1 = *reinterpret_cast<const float4*>(At[s] + q * kRsLdAt + 8 * rg + 4);
+          const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            acc[u][0] = fmaf(xa[u], pv.x, acc[u][0]);
+            acc[u][1] = fmaf(xa[u], pv.y, acc[u][1]);
+            acc[u][2] = fmaf(xa[u], pv.z, acc[u][2]);
+            acc[u][3] = fmaf(xa[u], pv.w, acc[u][3]);
+          }
+        }
+        float* out = Ms[s] + 8 * rg * lds[s] + 32 * (b + 1) + 4 * cgi;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          float4* o = reinterpret_cast<float4*>(out + u * lds[s]);
+          float4 v = *o;
+          v.x -= acc[u][0];
+          v.y -= acc[u][1];
+          v.z -= acc[u][2];
+          v.w -= acc[u][3];
+          *o = v;
+        }
+      }
+      __syncthreads();
+    }
   }
 
-  // ---- L y = A^T Y (in B), then L^T x = y (into Vc) ----
-  for (int pass = 0; pass < 2; ++pass) {
-    const bool fwd = pass == 0;
-    const float* src = Bg;
-    float* dst = fwd ? Bg : Vg;
-    for (int jb = 0; jb < k; jb += kCholNb) {
-      const int J = fwd ? jb : ((k - 1) / kCholNb) * kCholNb - jb;
-      const int nb = min(kCholNb, k - J);
-      for (int e = tid; e < kCholNb * kCholNb; e += kRidgeSolveThreads) {
-        const int r = e / kCholNb, c = e % kCholNb;
-        s_diag[r][c] = (r < nb && c <= r) ? Mg[static_cast<long long>(J + r) * k + J + c] : (r == c ? 1.f : 0.f);
+  if (!bad) {
+    // ---- the two solves, CTA `rank` taking channels rank NCH .. + NCH - 1 of
+    // every row: L and the L_bb^-1 are final (read from their owners); no
+    // cluster barrier until the end ----
+    constexpr int NCH = DH / kRsCluster;  // 16 or 8
+    float* Yc = sm + kRsOffB;             // [32 nblk][NCH]: A^T Y, then y, then x
+    const int kp = 32 * nblk;
+    for (int e = tid; e < kp * NCH; e += kRsThreads) {
+      const int row = e / NCH, c = e % NCH;
+      Yc[e] = row < k ? __ldg(Bg + static_cast<long long>(row) * DH + rank * NCH + c) : 0.f;
+    }
+    const int orow = tid / NCH, oc = tid % NCH;  // this thread's output of a 32-row block (if orow < 32)
+    const bool active = tid < 32 * NCH;
+    float* lbuf = PT;  // pulled rows or columns of L
+    // L y = A^T Y: y_b = L_bb^-1 (r_b - L_b,0:b y_0:b)
+    for (int b = 0; b < nblk; ++b) {
+      const int ob = rs_owner(b), sb = rs_slot(b);
+      const float* ob_sm = cluster.map_shared_rank(sm, ob);
+      const int nq = 32 * b;  // columns left of the diagonal block
+      for (int e = tid; e < 32 * (nq / 4); e += kRsThreads) {  // row block b, columns 0 .. nq - 1
+        const int rr = e / (nq / 4), q4 = e % (nq / 4);
+        reinterpret_cast<float4*>(lbuf + rr * (nq + 4))[q4] =
+            reinterpret_cast<const float4*>(ob_sm + rs_off(b) + rr * rs_ld(b))[q4];
       }
-      for (int r = warp; r < nb; r += kWarps) {  // row J + r minus its product with the solved rows
+      for (int e = tid; e < kRsBlk; e += kRsThreads) tinv[e] = ob_sm[kRsOffDinv + sb * kRsBlk + e];
+      __syncthreads();
+      float r = 0.f;
+      if (active) {
+        const float* lr = lbuf + orow * (nq + 4);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const int p0 = fwd ? 0 : J + nb, p1 = fwd ? J : k;
-        for (int p = p0; p < p1; ++p) {
-          const float l = fwd ? Mg[static_cast<long long>(J + r) * k + p] : Mg[static_cast<long long>(p) * k + J + r];
-          const float* xp = dst + static_cast<long long>(p) * d + lane;
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (u < nd) acc[u] = fmaf(l, xp[32 * u], acc[u]);
+        for (int q = 0; q < nq; q += 4) {
+          const float4 l = *reinterpret_cast<const float4*>(lr + q);
+          acc[0] = fmaf(l.x, Yc[(q) * NCH + oc], acc[0]);
+          acc[1] = fmaf(l.y, Yc[(q + 1) * NCH + oc], acc[1]);
+          acc[2] = fmaf(l.z, Yc[(q + 2) * NCH + oc], acc[2]);
+          acc[3] = fmaf(l.w, Yc[(q + 3) * NCH + oc], acc[3]);
         }
-        float* out = dst + static_cast<long long>(J + r) * d + lane;
-        const float* in = src + static_cast<long long>(J + r) * d + lane;
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (u < nd) out[32 * u] = in[32 * u] - acc[u];
+        r = Yc[(nq + orow) * NCH + oc] - ((acc[0] + acc[1]) + (acc[2] + acc[3]));
       }
       __syncthreads();
-      if (tid < d) {  // the 32 x 32 triangle for channel tid, through shared memory
-        float* y = s_y + tid;  // y[r * kRidgeMaxD]
-        for (int r = 0; r < nb; ++r) y[r * kRidgeMaxD] = dst[static_cast<long long>(J + r) * d + tid];
-        if (fwd) {
-          for (int r = 0; r < nb; ++r) {
-            float v = y[r * kRidgeMaxD];
-            for (int r2 = 0; r2 < r; ++r2) v = fmaf(-s_diag[r][r2], y[r2 * kRidgeMaxD], v);
-            y[r * kRidgeMaxD] = v / s_diag[r][r];
-          }
-        } else {
-          for (int r = nb - 1; r >= 0; --r) {
-            float v = y[r * kRidgeMaxD];
-            for (int r2 = r + 1; r2 < nb; ++r2) v = fmaf(-s_diag[r2][r], y[r2 * kRidgeMaxD], v);
-            y[r * kRidgeMaxD] = v / s_diag[r][r];
-          }
-        }
-        for (int r = 0; r < nb; ++r) dst[static_cast<long long>(J + r) * d + tid] = y[r * kRidgeMaxD];
+      if (active) Yc[(nq + orow) * NCH + oc] = r;
+      __syncthreads();
+      float y = 0.f;
+      if (active) {
+#pragma unroll 8
+        for (int q = 0; q < 32; ++q) y = fmaf(tinv[orow * kRsLd + q], Yc[(nq + q) * NCH + oc], y);
       }
+      __syncthreads();
+      if (active) Yc[(nq + orow) * NCH + oc] = y;
       __syncthreads();
     }
+    // L^T x = y: x_b = L_bb^-T (y_b - sum_{i > b} L_ib^T x_i)
+    for (int b = nblk - 1; b >= 0; --b) {
+      const int ob = rs_owner(b), sb = rs_slot(b);
+      const int np = 32 * (nblk - 1 - b);  // rows below the diagonal block
+      for (int e = tid; e < np * 8; e += kRsThreads) {  // column block b of those rows: lbuf[p][0..31]
+        const int p = e >> 3, q4 = e & 7, ib = b + 1 + (p >> 5);
+        const float* src = cluster.map_shared_rank(sm, rs_owner(ib)) + rs_off(ib) + (p & 31) * rs_ld(ib) + 32 * b;
+        reinterpret_cast<float4*>(lbuf + p * 32)[q4] = reinterpret_cast<const float4*>(src)[q4];
+      }
+      const float* ob_sm = cluster.map_shared_rank(sm, ob);
+      for (int e = tid; e < kRsBlk; e += kRsThreads) tinv[e] = ob_sm[kRsOffDinv + sb * kRsBlk + e];
+      __syncthreads();
+      float r = 0.f;
+      const int nb0 = 32 * b;
+      if (active) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int p = 0; p < np; p += 4) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            acc[u] = fmaf(lbuf[(p + u) * 32 + orow], Yc[(nb0 + 32 + p + u) * NCH + oc], acc[u]);
+        }
+        r = Yc[(nb0 + orow) * NCH + oc] - ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+      }
+      __syncthreads();
+      if (active) Yc[(nb0 + orow) * NCH + oc] = r;
+      __syncthreads();
+      float x = 0.f;
+      if (active) {
+#pragma unroll 8
+        for (int q = 0; q < 32; ++q) x = fmaf(tinv[q * kRsLd + orow], Yc[(nb0 + q) * NCH + oc], x);
+      }
+      __syncthreads();
+      if (active) Yc[(nb0 + orow) * NCH + oc] = x;
+      __syncthreads();
+    }
+    for (int e = tid; e < k * NCH; e += kRsThreads)
+      Vg[static_cast<long long>(e / NCH) * DH + rank * NCH + e % NCH] = Yc[e];
+  } else {
+    if (rank == 0 && tid == 0) record_error(KVS_ERR_RANGE);
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      if (!has[s]) continue;
+      for (int e = tid; e < 32 * DH; e += kRsThreads) {
+        const int gr = 32 * own[s] + e / DH;
+        if (gr < k) Vg[static_cast<long long>(gr) * DH + e % DH] = 0.f;
+      }
+    }
   }
+  cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 }  // namespace kvs
