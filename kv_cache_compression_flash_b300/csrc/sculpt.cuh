@@ -843,9 +843,9 @@ __global__ void __launch_bounds__(kRsThreads, 1)
       for (int c = 0; c < 32; ++c) {
         const float p = __shfl_sync(0xFFFFFFFFu, a[c], c);
         ok = ok && p > 0.f;
-        const float piv = sqrtf(p);
-        if (lane == c) a[c] = piv;
-        if (lane > c) a[c] /= piv;
+        const float rp = __frsqrt_rn(p);  // 1 / L_cc
+        if (lane == c) a[c] = p * rp;
+        if (lane > c) a[c] *= rp;
 #pragma unroll
         for (int c2 = 1; c2 < 32; ++c2) {  // row c2 > c of the trailing block, for the rows that reach it
           if (c2 > c) {
@@ -857,6 +857,10 @@ __global__ void __launch_bounds__(kRsThreads, 1)
       if (!ok) {
         if (lane == 0) *flag = 1;
       } else {
+        float dl = a[0];
+#pragma unroll
+        for (int c = 1; c < 32; ++c) dl = lane == c ? a[c] : dl;
+        const float rd = __frcp_rn(dl);  // 1 / L_{lane, lane}
         float x[32];  // column `lane` of L_bb^-1: L x = e_lane by forward substitution
 #pragma unroll
         for (int rr = 0; rr < 32; ++rr) {
@@ -864,7 +868,7 @@ __global__ void __launch_bounds__(kRsThreads, 1)
 #pragma unroll
           for (int q = 0; q < 31; ++q)
             if (q < rr) v = fmaf(-__shfl_sync(0xFFFFFFFFu, a[q], rr), x[q], v);
-          x[rr] = v / __shfl_sync(0xFFFFFFFFu, a[rr], rr);
+          x[rr] = v * __shfl_sync(0xFFFFFFFFu, rd, rr);
         }
         float* dv = dinv + sb * kRsBlk;
 #pragma unroll
@@ -878,8 +882,8 @@ __global__ void __launch_bounds__(kRsThreads, 1)
     }
     const bool t0 = has[0] && own[0] > b, t1 = has[1] && own[1] > b;  // blocks below the diagonal block
     if (t0 || t1) {  // L_ib = M_ib L_bb^-T
-      const float* src = cluster.map_shared_rank(dinv + sb * kRsBlk, ob);
-      for (int e = tid; e < kRsBlk; e += kRsThreads) tinv[e] = src[e];
+      const float4* src = reinterpret_cast<const float4*>(cluster.map_shared_rank(dinv + sb * kRsBlk, ob));
+      if (tid < kRsBlk / 4) reinterpret_cast<float4*>(tinv)[tid] = src[tid];
       __syncthreads();
       const int rr = tid >> 4, c2 = tid & 15;
       float a[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
@@ -980,12 +984,25 @@ __global__ void __launch_bounds__(kRsThreads, 1)
       const int ob = rs_owner(b), sb = rs_slot(b);
       const float* ob_sm = cluster.map_shared_rank(sm, ob);
       const int nq = 32 * b;  // columns left of the diagonal block
-      for (int e = tid; e < 32 * (nq / 4); e += kRsThreads) {  // row block b, columns 0 .. nq - 1
-        const int rr = e / (nq / 4), q4 = e % (nq / 4);
-        reinterpret_cast<float4*>(lbuf + rr * (nq + 4))[q4] =
-            reinterpret_cast<const float4*>(ob_sm + rs_off(b) + rr * rs_ld(b))[q4];
+      {  // row block b, columns 0 .. nq - 1, and L_bb^-1: every remote load in flight at once
+        const int n4 = 32 * (nq / 4);  // at most 3840 = 7.5 a thread
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int e = tid + u * kRsThreads;
+          if (e < n4)
+            v[u] = reinterpret_cast<const float4*>(ob_sm + rs_off(b) + (e / (nq / 4)) * rs_ld(b))[e % (nq / 4)];
+        }
+        const float4 t = tid < kRsBlk / 4
+                             ? reinterpret_cast<const float4*>(ob_sm + kRsOffDinv + sb * kRsBlk)[tid]
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int e = tid + u * kRsThreads;
+          if (e < n4) reinterpret_cast<float4*>(lbuf + (e / (nq / 4)) * (nq + 4))[e % (nq / 4)] = v[u];
+        }
+        if (tid < kRsBlk / 4) reinterpret_cast<float4*>(tinv)[tid] = t;
       }
-      for (int e = tid; e < kRsBlk; e += kRsThreads) tinv[e] = ob_sm[kRsOffDinv + sb * kRsBlk + e];
       __syncthreads();
       float r = 0.f;
       if (active) {
@@ -1016,13 +1033,26 @@ __global__ void __launch_bounds__(kRsThreads, 1)
     for (int b = nblk - 1; b >= 0; --b) {
       const int ob = rs_owner(b), sb = rs_slot(b);
       const int np = 32 * (nblk - 1 - b);  // rows below the diagonal block
-      for (int e = tid; e < np * 8; e += kRsThreads) {  // column block b of those rows: lbuf[p][0..31]
-        const int p = e >> 3, q4 = e & 7, ib = b + 1 + (p >> 5);
-        const float* src = cluster.map_shared_rank(sm, rs_owner(ib)) + rs_off(ib) + (p & 31) * rs_ld(ib) + 32 * b;
-        reinterpret_cast<float4*>(lbuf + p * 32)[q4] = reinterpret_cast<const float4*>(src)[q4];
+      {  // column block b of those rows (lbuf[p][0..31]) and L_bb^-1: every remote load in flight at once
+        const float* ob_sm = cluster.map_shared_rank(sm, ob);
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int e = tid + u * kRsThreads, p = e >> 3, ib = b + 1 + (p >> 5);
+          if (e < np * 8)
+            v[u] = reinterpret_cast<const float4*>(cluster.map_shared_rank(sm, rs_owner(ib)) + rs_off(ib) +
+                                                   (p & 31) * rs_ld(ib) + 32 * b)[e & 7];
+        }
+        const float4 t = tid < kRsBlk / 4
+                             ? reinterpret_cast<const float4*>(ob_sm + kRsOffDinv + sb * kRsBlk)[tid]
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int e = tid + u * kRsThreads;
+          if (e < np * 8) reinterpret_cast<float4*>(lbuf + (e >> 3) * 32)[e & 7] = v[u];
+        }
+        if (tid < kRsBlk / 4) reinterpret_cast<float4*>(tinv)[tid] = t;
       }
-      const float* ob_sm = cluster.map_shared_rank(sm, ob);
-      for (int e = tid; e < kRsBlk; e += kRsThreads) tinv[e] = ob_sm[kRsOffDinv + sb * kRsBlk + e];
       __syncthreads();
       float r = 0.f;
       const int nb0 = 32 * b;
