@@ -439,7 +439,10 @@ int kvs_spectrum(const float* G, int64_t Hkv, int64_t d, float rtol, float* sigm
  * every pointer 16-byte aligned.  No workspace.  Tensor cores: the logits are
  * bf16 products summed in fp32; the weights enter the output product split
  * into two bf16 parts (16 significant bits), so Y keeps fp32-level error; an
- * online softmax over chunks of 64 keys.
+ * online softmax over tiles of 128 keys, the tiles taken alternately by two
+ * groups of warps whose partial results merge at the end.  Returns
+ * KVS_ERR_UNSUPPORTED (nothing launched) if the kernel's register split does
+ * not fit the registers it was built to launch with.
  *
  * kvs_ridge_values: per KV head g, the values of k compressed pairs whose keys
  * Kc[g] are fixed   [KVSculpt §2: with the keys fixed the values solve a
@@ -456,8 +459,9 @@ int kvs_spectrum(const float* G, int64_t Hkv, int64_t d, float rtol, float* sigm
  *   workspace: kvs_ridge_values_workspace_size(Hkv, R, k, d) bytes, 256-byte
  *        aligned.
  * The logits as in kvs_block_attention (bf16 products, fp32 sums), then fp32:
- * A, the lower triangle of A^T A + lam I, A^T Y, and a blocked Cholesky solve
- * (one CTA per head).  A pivot that is not positive (lam too small for fp32
+ * A, the lower triangle of A^T A + lam I and A^T Y (as two partial sums over
+ * the halves of R), and a blocked Cholesky solve on a cluster of 8 CTAs per
+ * head (one cluster per head at a time: about 187 KB of shared memory each).  A pivot that is not positive (lam too small for fp32
  * against |A^T A|) records KVS_ERR_RANGE in the error word and sets that
  * head's values to 0.  d in {64, 128}, else KVS_ERR_UNSUPPORTED; k > 512
  * gives KVS_ERR_UNSUPPORTED. */

@@ -1035,12 +1035,12 @@ int ridge_check(int64_t Hkv, int64_t R, int64_t k, int64_t d) {
   return KVS_OK;
 }
 
-// A [Hkv, R, k], then M [Hkv, k, k] and B [Hkv, k, d], each 256-byte aligned
+// A [Hkv, R, k], then M [kAtbSplit, Hkv, k, k] and B [kAtbSplit, Hkv, k, d], each 256-byte aligned
 size_t carve_ridge(int64_t Hkv, int64_t R, int64_t k, int64_t d, void* base, float** A, float** M, float** B) {
   WsCarver c{static_cast<char*>(base), 0, 0};
   *A = c.take<float>(static_cast<size_t>(Hkv * R * k));
-  *M = c.take<float>(static_cast<size_t>(Hkv * k * k));
-  *B = c.take<float>(static_cast<size_t>(Hkv * k * d));
+  *M = c.take<float>(static_cast<size_t>(kAtbSplit * Hkv * k * k));  // one partial sum per split of R
+  *B = c.take<float>(static_cast<size_t>(kAtbSplit * Hkv * k * d));
   return c.used;
 }
 }  // namespace
@@ -1077,19 +1077,19 @@ int kvs_ridge_values(const uint16_t* Qt, const uint16_t* Kc, const float* Y, int
                           c_log2, A));
   }
   const unsigned kt = static_cast<unsigned>(cdiv(k, kAtbTile)), dt = static_cast<unsigned>(cdiv(d, kAtbTile));
-  KVS_CUDA_TRY(launch_k(ridge_atb_kernel, dim3(kt, kt, static_cast<unsigned>(Hkv)), dim3(256), 0, st, 0,
-                        static_cast<const float*>(A), static_cast<const float*>(A), Ri, ki, ki, lam, 1, 1, M));
-  KVS_CUDA_TRY(launch_k(ridge_atb_kernel, dim3(dt, kt, static_cast<unsigned>(Hkv)), dim3(256), 0, st, 0,
-                        static_cast<const float*>(A), Y, Ri, ki, di, lam, 0, 0, B));
+  const long long mstride = Hkv * k * k, bstride = Hkv * k * d;  // between the partial sums
+  KVS_CUDA_TRY(launch_k(ridge_atb_kernel, dim3(kt * (kt + 1) / 2 + kt * dt, kAtbSplit, static_cast<unsigned>(Hkv)),
+                        dim3(256), 0, st, 0, static_cast<const float*>(A), Y, Ri, ki, di, lam, M, mstride, B,
+                        bstride));
   const dim3 gsolve(kRsCluster, static_cast<unsigned>(Hkv));  // a cluster of kRsCluster CTAs per head
   if (d == 64) {
     KVS_CUDA_TRY(allow_smem(ridge_solve_cluster_kernel<64>, kRsSmemBytes));
     KVS_CUDA_TRY(launch_k(ridge_solve_cluster_kernel<64>, gsolve, dim3(kRsThreads), kRsSmemBytes, st, kRsCluster,
-                          static_cast<const float*>(M), static_cast<const float*>(B), ki, Vc));
+                          static_cast<const float*>(M), mstride, static_cast<const float*>(B), bstride, ki, Vc));
   } else {
     KVS_CUDA_TRY(allow_smem(ridge_solve_cluster_kernel<128>, kRsSmemBytes));
     KVS_CUDA_TRY(launch_k(ridge_solve_cluster_kernel<128>, gsolve, dim3(kRsThreads), kRsSmemBytes, st, kRsCluster,
-                          static_cast<const float*>(M), static_cast<const float*>(B), ki, Vc));
+                          static_cast<const float*>(M), mstride, static_cast<const float*>(B), bstride, ki, Vc));
   }
   KVS_CUDA_TRY(cudaGetLastError());
   return KVS_OK;

@@ -10,9 +10,9 @@
 //       mask: every training query sees the whole compressed block), the
 //       logits on the tensor cores as in the block attention, in two sweeps
 //       over the keys (row max and sum, then the weights).
-//   ridge_atb_kernel            C = P^T Q (+ lam I), 64 x 64 output tiles with
-//       4 x 4 per thread over 16-row slices of P [R, m] and Q [R, n]: gives
-//       A^T A + lam I (lower triangle) and A^T Y.
+//   ridge_atb_kernel            A^T A + lam I (its lower 64 x 64 tiles) and
+//       A^T Y in one launch, 4 x 4 outputs a thread over 32-row slices of R,
+//       R split in two halves whose partial sums the solve adds.
 //   ridge_solve_cluster_kernel<DH>  a cluster of 8 CTAs per head: blocked
 //       Cholesky of A^T A + lam I and the forward and backward solves for
 //       the d right-hand sides, the matrix in the cluster's shared memory.
@@ -672,45 +672,67 @@ __global__ void __launch_bounds__(kBaThreads) ridge_softmax_kernel(const uint16_
 // the next slice's loads in flight while the current one is multiplied.  With
 // lower_only, tiles wholly above the diagonal are skipped: the solve reads only
 // the lower triangle of A^T A + lam I.
-constexpr int kAtbTile = 64, kAtbSlice = 16;
+constexpr int kAtbTile = 64, kAtbSlice = 32;
+constexpr int kAtbSplit = 2;  // partial sums over the halves of R, added by the solve as it loads them
 
-__global__ void __launch_bounds__(256) ridge_atb_kernel(const float* __restrict__ P, const float* __restrict__ Q,
-                                                        int R, int m, int n, float lam, int add_diag, int lower_only,
-                                                        float* __restrict__ C) {
+// One launch for both products of a head: tile t < kt (kt + 1) / 2 is a lower
+// tile of A^T A (+ lam I on the diagonal of split 0), the rest the tiles of
+// A^T Y; blockIdx.y = the split s (rows s Rs .. (s + 1) Rs - 1 of R), blockIdx.z
+// = the head.  Split s writes M + s mstride and B + s bstride.
+__global__ void __launch_bounds__(256) ridge_atb_kernel(const float* __restrict__ A, const float* __restrict__ Y,
+                                                        int R, int k, int d, float lam, float* __restrict__ M,
+                                                        long long mstride, float* __restrict__ B,
+                                                        long long bstride) {
   pdl_wait();
   pdl_trigger();
-  const int i0 = blockIdx.y * kAtbTile, j0 = blockIdx.x * kAtbTile;
-  if (lower_only != 0 && j0 > i0 + kAtbTile - 1) return;  // the whole CTA, before any barrier
+  const int kt = (k + kAtbTile - 1) / kAtbTile, nlow = kt * (kt + 1) / 2;
+  int t = blockIdx.x;
+  const bool gram = t < nlow;
+  int ti = 0, tj;
+  if (gram) {
+    while ((ti + 1) * (ti + 2) / 2 <= t) ++ti;
+    tj = t - ti * (ti + 1) / 2;
+  } else {
+    t -= nlow;
+    const int dt = (d + kAtbTile - 1) / kAtbTile;
+    ti = t / dt;
+    tj = t % dt;
+  }
+  const int n = gram ? k : d;
+  const int i0 = ti * kAtbTile, j0 = tj * kAtbTile;
+  const int split = blockIdx.y, g = blockIdx.z;
+  const int Rs = (R + kAtbSplit * kAtbSlice - 1) / (kAtbSplit * kAtbSlice) * kAtbSlice;  // rows of a split
+  const int rb = split * Rs, re = min(R, rb + Rs);
   __shared__ __align__(16) float ps[kAtbSlice][kAtbTile];
   __shared__ __align__(16) float qs[kAtbSlice][kAtbTile];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const int g = blockIdx.z;
-  const float* Pg = P + static_cast<long long>(g) * R * m;
-  const float* Qg = Q + static_cast<long long>(g) * R * n;
-  // this thread's four loads per slice: element e = tid + 256 u -> row e / 64, column e % 64
-  float pv[4], qv[4];
+  const float* Pg = A + static_cast<long long>(g) * R * k;
+  const float* Qg = gram ? Pg : Y + static_cast<long long>(g) * R * d;
+  // this thread's loads per slice: element e = tid + 256 u -> row e / 64, column e % 64
+  constexpr int kLoads = kAtbSlice * kAtbTile / 256;
+  float pv[kLoads], qv[kLoads];
   auto fetch = [&](int r0) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kLoads; ++u) {
       const int e = tid + 256 * u, rr = e >> 6, cc = e & 63, r = r0 + rr;
-      pv[u] = (r < R && i0 + cc < m) ? Pg[static_cast<long long>(r) * m + i0 + cc] : 0.f;
-      qv[u] = (r < R && j0 + cc < n) ? Qg[static_cast<long long>(r) * n + j0 + cc] : 0.f;
+      pv[u] = (r < re && i0 + cc < k) ? Pg[static_cast<long long>(r) * k + i0 + cc] : 0.f;
+      qv[u] = (r < re && j0 + cc < n) ? Qg[static_cast<long long>(r) * n + j0 + cc] : 0.f;
     }
   };
   float acc[4][4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
-  fetch(0);
-  for (int r0 = 0; r0 < R; r0 += kAtbSlice) {
+  fetch(rb);
+  for (int r0 = rb; r0 < re; r0 += kAtbSlice) {
     __syncthreads();  // the previous slice is consumed
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kLoads; ++u) {
       const int e = tid + 256 * u;
       ps[e >> 6][e & 63] = pv[u];
       qs[e >> 6][e & 63] = qv[u];
     }
     __syncthreads();
-    if (r0 + kAtbSlice < R) fetch(r0 + kAtbSlice);
+    if (r0 + kAtbSlice < re) fetch(r0 + kAtbSlice);
 #pragma unroll
     for (int rr = 0; rr < kAtbSlice; ++rr) {
       const float4 a = *reinterpret_cast<const float4*>(&ps[rr][4 * ty]);
@@ -722,13 +744,15 @@ __global__ void __launch_bounds__(256) ridge_atb_kernel(const float* __restrict_
         for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
     }
   }
+  float* C = gram ? M + split * mstride : B + split * bstride;
+  const bool diag = gram && split == 0;
 #pragma unroll
   for (int u = 0; u < 4; ++u)
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
       const int i = i0 + 4 * ty + u, j = j0 + 4 * tx + v;
-      if (i < m && j < n)
-        C[(static_cast<long long>(g) * m + i) * n + j] = acc[u][v] + ((add_diag != 0 && i == j) ? lam : 0.f);
+      if (i < k && j < n)
+        C[(static_cast<long long>(g) * k + i) * n + j] = acc[u][v] + ((diag && i == j) ? lam : 0.f);
     }
 }
 
@@ -786,8 +810,8 @@ __device__ __forceinline__ int rs_off(int i) { return i < kRsCluster ? 0 : 32 * 
 // grid (kRsCluster, Hkv), clusters of kRsCluster along x; kRsThreads threads.
 template <int DH>
 __global__ void __launch_bounds__(kRsThreads, 1)
-    ridge_solve_cluster_kernel(const float* __restrict__ M, const float* __restrict__ B, const int k,
-                               float* __restrict__ Vc) {
+    ridge_solve_cluster_kernel(const float* __restrict__ M, long long mstride, const float* __restrict__ B,
+                               long long bstride, const int k, float* __restrict__ Vc) {
   namespace cgr = cooperative_groups;
   cgr::cluster_group cluster = cgr::this_cluster();
   extern __shared__ float4 rs_smem4[];
@@ -819,8 +843,14 @@ __global__ void __launch_bounds__(kRsThreads, 1)
     const int i = own[s], wdt = 32 * (i + 1);
     for (int e = tid; e < 32 * wdt; e += kRsThreads) {
       const int rr = e / wdt, c = e - rr * wdt, gr = 32 * i + rr;
-      Ms[s][rr * lds[s] + c] = (gr < k && c < k) ? __ldg(Mg + static_cast<long long>(gr) * k + c)
-                                                 : (gr == c ? 1.f : 0.f);
+      float v = gr == c ? 1.f : 0.f;
+      if (gr < k && c < k) {
+        const long long o = static_cast<long long>(gr) * k + c;
+        v = __ldg(Mg + o);
+#pragma unroll
+        for (int sp = 1; sp < kAtbSplit; ++sp) v += __ldg(Mg + sp * mstride + o);
+      }
+      Ms[s][rr * lds[s] + c] = v;
     }
   }
   if (tid == 0) *flag = 0;
@@ -974,7 +1004,14 @@ __global__ void __launch_bounds__(kRsThreads, 1)
     const int kp = 32 * nblk;
     for (int e = tid; e < kp * NCH; e += kRsThreads) {
       const int row = e / NCH, c = e % NCH;
-      Yc[e] = row < k ? __ldg(Bg + static_cast<long long>(row) * DH + rank * NCH + c) : 0.f;
+      float v = 0.f;
+      if (row < k) {
+        const long long o = static_cast<long long>(row) * DH + rank * NCH + c;
+        v = __ldg(Bg + o);
+#pragma unroll
+        for (int sp = 1; sp < kAtbSplit; ++sp) v += __ldg(Bg + sp * bstride + o);
+      }
+      Yc[e] = v;
     }
     const int orow = tid / NCH, oc = tid % NCH;  // this thread's output of a 32-row block (if orow < 32)
     const bool active = tid < 32 * NCH;

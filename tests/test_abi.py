@@ -182,9 +182,11 @@ def test_block_lse_argument_errors(lib):
 
 
 def test_sculpt_sizes_and_argument_errors(lib):
-    # A [Hkv, R, k], A^T A [Hkv, k, k], A^T Y [Hkv, k, d], fp32, each 256-byte aligned
-    assert lib.kvs_ridge_values_workspace_size(8, 2048, 256, 128) == 4 * 8 * (2048 * 256 + 256 * 256 + 256 * 128)
-    assert lib.kvs_ridge_values_workspace_size(1, 3, 5, 64) == 256 + 256 + 4 * 5 * 64
+    # A [Hkv, R, k], then A^T A [2, Hkv, k, k] and A^T Y [2, Hkv, k, d] (partial sums over
+    # the two halves of R), fp32, each 256-byte aligned
+    assert lib.kvs_ridge_values_workspace_size(8, 2048, 256, 128) == 4 * 8 * (2048 * 256 + 2 * 256 * 256
+                                                                             + 2 * 256 * 128)
+    assert lib.kvs_ridge_values_workspace_size(1, 3, 5, 64) == 256 + 256 + 4 * 2 * 5 * 64
     assert lib.kvs_ridge_values_workspace_size(8, 2048, 513, 128) == 0     # k above 512
     assert lib.kvs_ridge_values_workspace_size(8, 2048, 256, 96) == 0      # d outside {64, 128}
     assert lib.kvs_ridge_values_workspace_size(8, 0, 256, 128) == 0
