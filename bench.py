@@ -900,11 +900,12 @@ def run_sculpt(args):
         "block_attention_us": attn_us, "ridge_values_us": ridge_us,
         "roofline": {"bound": "tensor", "achieved": attn_flops / (attn_us * 1e-6) / 1e12, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": attn_flops / (attn_us * 1e-6) / 1e12 / peak_tf,
-                     "peak_kind": f"{peak_kind} bf16 dense", "kernel": "block_attention_kernel",
+                     "peak_kind": f"{peak_kind} bf16 dense", "kernel": "block_attention_tc_kernel",
                      "algorithmic_flops": attn_flops},
         "ridge_tflops": ridge_flops / (ridge_us * 1e-6) / 1e12,
         "ridge_fma_frac": ridge_flops / (ridge_us * 1e-6) / (148 * 128 * 2 * fma_clock_mhz() * 1e6),
-        "gpu_launches": 5 * args.steps,
+        # block attention, then the ridge's softmax, A^T A + A^T Y and the cluster solve
+        "gpu_launches": 4 * args.steps,
     }))
     return 0
 
