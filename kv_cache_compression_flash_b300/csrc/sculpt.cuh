@@ -774,12 +774,12 @@ __global__ void __launch_bounds__(256) ridge_atb_kernel(const float* __restrict_
 //   8 x 4 outputs a thread.
 // The diagonal block is factored and inverted in registers (warp shuffles).
 // The two solves split the d channels over the cluster (CTA r takes
-// d / 8 of them for every row) and need no further barrier: the forward solve
-// L y = A^T Y takes y_b = L_bb^-1 (r_b - L_b,0:b y_0:b) block by block with
-// row block b of L read from its owner, the backward solve L^T x = y takes
-// x_b = L_bb^-T (y_b - sum_{i > b} L_ib^T x_i) from the last block up with
-// column block b read from the owners of the blocks below.  fp32 FMA
-// throughout.  A pivot that is not positive
+// d / 8 of them for every row) and need no further barrier; both are
+// right-looking: the forward solve L y = A^T Y takes y_b = L_bb^-1 r_b and
+// subtracts L_ib y_b from the rows below (column block b of L read from the
+// owners of those rows), the backward solve L^T x = y takes x_b = L_bb^-T y_b
+// from the last block up and subtracts L_bi^T x_b from the rows above (row
+// block b read from its owner).  fp32 FMA throughout.  A pivot that is not positive
 // records KVS_ERR_RANGE and the head's values are 0.
 constexpr int kRsCluster = 8;
 constexpr int kRsThreads = 512;
@@ -1016,103 +1016,90 @@ __global__ void __launch_bounds__(kRsThreads, 1)
     const int orow = tid / NCH, oc = tid % NCH;  // this thread's output of a 32-row block (if orow < 32)
     const bool active = tid < 32 * NCH;
     float* lbuf = PT;  // pulled rows or columns of L
-    // L y = A^T Y: y_b = L_bb^-1 (r_b - L_b,0:b y_0:b)
-    for (int b = 0; b < nblk; ++b) {
+    // pulls of step b from the owners, every remote load of a thread in flight
+    // at once: L_bb^-1 into tinv, and either column block b of the rows below
+    // it (lbuf[p][0..31], p < 32 (nblk - 1 - b)) or row block b left of its
+    // diagonal block (lbuf[q][0..32 b - 1], row stride 32 b + 4)
+    auto pull = [&](int b, bool column) {
       const int ob = rs_owner(b), sb = rs_slot(b);
       const float* ob_sm = cluster.map_shared_rank(sm, ob);
-      const int nq = 32 * b;  // columns left of the diagonal block
-      {  // row block b, columns 0 .. nq - 1, and L_bb^-1: every remote load in flight at once
-        const int n4 = 32 * (nq / 4);  // at most 3840 = 7.5 a thread
-        float4 v[8];
+      const int nq = 32 * b, np = 32 * (nblk - 1 - b);
+      const int n4 = column ? np * 8 : 32 * (nq / 4);  // at most 3840 = 7.5 a thread
+      float4 v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int e = tid + u * kRsThreads;
-          if (e < n4)
-            v[u] = reinterpret_cast<const float4*>(ob_sm + rs_off(b) + (e / (nq / 4)) * rs_ld(b))[e % (nq / 4)];
-        }
-        const float4 t = tid < kRsBlk / 4
-                             ? reinterpret_cast<const float4*>(ob_sm + kRsOffDinv + sb * kRsBlk)[tid]
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int e = tid + u * kRsThreads;
-          if (e < n4) reinterpret_cast<float4*>(lbuf + (e / (nq / 4)) * (nq + 4))[e % (nq / 4)] = v[u];
-        }
-        if (tid < kRsBlk / 4) reinterpret_cast<float4*>(tinv)[tid] = t;
-      }
-      __syncthreads();
-      float r = 0.f;
-      if (active) {
-        const float* lr = lbuf + orow * (nq + 4);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int q = 0; q < nq; q += 4) {
-          const float4 l = *reinterpret_cast<const float4*>(lr + q);
-          acc[0] = fmaf(l.x, Yc[(q) * NCH + oc], acc[0]);
-          acc[1] = fmaf(l.y, Yc[(q + 1) * NCH + oc], acc[1]);
-          acc[2] = fmaf(l.z, Yc[(q + 2) * NCH + oc], acc[2]);
-          acc[3] = fmaf(l.w, Yc[(q + 3) * NCH + oc], acc[3]);
-        }
-        r = Yc[(nq + orow) * NCH + oc] - ((acc[0] + acc[1]) + (acc[2] + acc[3]));
-      }
-      __syncthreads();
-      if (active) Yc[(nq + orow) * NCH + oc] = r;
-      __syncthreads();
-      float y = 0.f;
-      if (active) {
-#pragma unroll 8
-        for (int q = 0; q < 32; ++q) y = fmaf(tinv[orow * kRsLd + q], Yc[(nq + q) * NCH + oc], y);
-      }
-      __syncthreads();
-      if (active) Yc[(nq + orow) * NCH + oc] = y;
-      __syncthreads();
-    }
-    // L^T x = y: x_b = L_bb^-T (y_b - sum_{i > b} L_ib^T x_i)
-    for (int b = nblk - 1; b >= 0; --b) {
-      const int ob = rs_owner(b), sb = rs_slot(b);
-      const int np = 32 * (nblk - 1 - b);  // rows below the diagonal block
-      {  // column block b of those rows (lbuf[p][0..31]) and L_bb^-1: every remote load in flight at once
-        const float* ob_sm = cluster.map_shared_rank(sm, ob);
-        float4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int e = tid + u * kRsThreads, p = e >> 3, ib = b + 1 + (p >> 5);
-          if (e < np * 8)
+      for (int u = 0; u < 8; ++u) {
+        const int e = tid + u * kRsThreads;
+        if (e < n4) {
+          if (column) {
+            const int p = e >> 3, ib = b + 1 + (p >> 5);
             v[u] = reinterpret_cast<const float4*>(cluster.map_shared_rank(sm, rs_owner(ib)) + rs_off(ib) +
                                                    (p & 31) * rs_ld(ib) + 32 * b)[e & 7];
+          } else {
+            v[u] = reinterpret_cast<const float4*>(ob_sm + rs_off(b) + (e / (nq / 4)) * rs_ld(b))[e % (nq / 4)];
+          }
         }
-        const float4 t = tid < kRsBlk / 4
-                             ? reinterpret_cast<const float4*>(ob_sm + kRsOffDinv + sb * kRsBlk)[tid]
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int e = tid + u * kRsThreads;
-          if (e < np * 8) reinterpret_cast<float4*>(lbuf + (e >> 3) * 32)[e & 7] = v[u];
-        }
-        if (tid < kRsBlk / 4) reinterpret_cast<float4*>(tinv)[tid] = t;
       }
-      __syncthreads();
-      float r = 0.f;
-      const int nb0 = 32 * b;
-      if (active) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int p = 0; p < np; p += 4) {
+      const float4 t = tid < kRsBlk / 4 ? reinterpret_cast<const float4*>(ob_sm + kRsOffDinv + sb * kRsBlk)[tid]
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            acc[u] = fmaf(lbuf[(p + u) * 32 + orow], Yc[(nb0 + 32 + p + u) * NCH + oc], acc[u]);
+      for (int u = 0; u < 8; ++u) {
+        const int e = tid + u * kRsThreads;
+        if (e < n4) {
+          if (column)
+            reinterpret_cast<float4*>(lbuf + (e >> 3) * 32)[e & 7] = v[u];
+          else
+            reinterpret_cast<float4*>(lbuf + (e / (nq / 4)) * (nq + 4))[e % (nq / 4)] = v[u];
         }
-        r = Yc[(nb0 + orow) * NCH + oc] - ((acc[0] + acc[1]) + (acc[2] + acc[3]));
       }
-      __syncthreads();
-      if (active) Yc[(nb0 + orow) * NCH + oc] = r;
-      __syncthreads();
-      float x = 0.f;
+      if (tid < kRsBlk / 4) reinterpret_cast<float4*>(tinv)[tid] = t;
+    };
+    // block b's 32 x NCH solution in place: z = L_bb^-1 r (forward) or L_bb^-T r (backward)
+    auto solve_block = [&](int b, bool transposed) {
+      float z = 0.f;
       if (active) {
 #pragma unroll 8
-        for (int q = 0; q < 32; ++q) x = fmaf(tinv[q * kRsLd + orow], Yc[(nb0 + q) * NCH + oc], x);
+        for (int q = 0; q < 32; ++q)
+          z = fmaf(transposed ? tinv[q * kRsLd + orow] : tinv[orow * kRsLd + q], Yc[(32 * b + q) * NCH + oc], z);
       }
       __syncthreads();
-      if (active) Yc[(nb0 + orow) * NCH + oc] = x;
+      if (active) Yc[(32 * b + orow) * NCH + oc] = z;
       __syncthreads();
+    };
+    // rows p of the update (p < nrows, global row row0 + p) minus their products
+    // with block b's solution: coef(p, q) is the factor entry for row p, column q
+    // of the block; each thread keeps channel tid % NCH of the solution in registers
+    auto update = [&](int b, int row0, int nrows, auto coef) {
+      const int c = tid % NCH;
+      float z[32];
+#pragma unroll
+      for (int q = 0; q < 32; ++q) z[q] = Yc[(32 * b + q) * NCH + c];
+      for (int p = tid / NCH; p < nrows; p += kRsThreads / NCH) {
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int q = 0; q < 32; q += 4) {
+          a0 = fmaf(coef(p, q), z[q], a0);
+          a1 = fmaf(coef(p, q + 1), z[q + 1], a1);
+          a2 = fmaf(coef(p, q + 2), z[q + 2], a2);
+          a3 = fmaf(coef(p, q + 3), z[q + 3], a3);
+        }
+        Yc[(row0 + p) * NCH + c] -= (a0 + a1) + (a2 + a3);
+      }
+      __syncthreads();
+    };
+    // L y = A^T Y, right-looking: y_b = L_bb^-1 r_b, then r_i -= L_ib y_b for the rows below
+    for (int b = 0; b < nblk; ++b) {
+      pull(b, true);
+      __syncthreads();
+      solve_block(b, false);
+      update(b, 32 * (b + 1), 32 * (nblk - 1 - b), [&](int p, int q) { return lbuf[p * 32 + q]; });
+    }
+    // L^T x = y, from the last block up: x_b = L_bb^-T y_b, then y_i -= L_bi^T x_b for the rows above
+    for (int b = nblk - 1; b >= 0; --b) {
+      pull(b, false);
+      __syncthreads();
+      solve_block(b, true);
+      const int ld = 32 * b + 4;
+      update(b, 0, 32 * b, [&](int p, int q) { return lbuf[q * ld + p]; });
     }
     for (int e = tid; e < k * NCH; e += kRsThreads)
       Vg[static_cast<long long>(e / NCH) * DH + rank * NCH + e % NCH] = Yc[e];
