@@ -8,7 +8,7 @@
 //       keys t < n_block, t <= q_pos0 + r.
 //   ridge_softmax_kernel<DH>    A = softmax over all k compressed keys (no
 //       mask: every training query sees the whole compressed block), the
-//       logits on the tensor cores as in the block attention, in two sweeps
+//       logits by mma.sync m16n8k16 (bf16 products, fp32 sums), in two sweeps
 //       over the keys (row max and sum, then the weights).
 //   ridge_atb_kernel            A^T A + lam I (its lower 64 x 64 tiles) and
 //       A^T Y in one launch, 4 x 4 outputs a thread over 32-row slices of R,
