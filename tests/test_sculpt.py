@@ -79,6 +79,30 @@ def test_block_attention_vs_oracle(Hq, Hkv, W, N, d, q_pos0, n_block):
     assert (np.abs(lse_only - lse.cpu().numpy()) <= 2e-3 * np.maximum(1.0, np.abs(lser))).all()
 
 
+def test_block_attention_rising_logits_rescale():
+    """Keys scaled up along the block, so a tile's row max keeps passing the
+    running max by more than the lazy-rescale margin: both softmax groups
+    raise their max and scale their O again and again."""
+    Hq, Hkv, W, N, d, q_pos0, n_block = 8, 2, 64, 1200, 128, 1136, 1100
+    g = torch.Generator().manual_seed(77)
+    Q = torch.randn(Hq, W, d, generator=g).abs().bfloat16()
+    ramp = (torch.arange(N, dtype=torch.float32) / N * 6.0).view(1, N, 1)
+    K = (torch.randn(Hkv, N, d, generator=g).abs() * ramp).bfloat16()
+    V = torch.randn(Hkv, N, d, generator=g).bfloat16()
+    Y, lse = L.block_attention(Q.to(DEV), K.to(DEV), V.to(DEV), n_block, q_pos0=q_pos0)
+    torch.cuda.synchronize()
+    assert L.device_error() == 0
+    Q64, K64, V64 = Q.double().numpy(), K.double().numpy(), V.double().numpy()
+    Yr, lser = O.block_attention(Q64, K64, V64, q_pos0, n_block)
+    # every row's largest logit (log2 units) rises by more than two rescale
+    # margins (8 each) from the first key tile to the last
+    lg = Q64[0] @ K64[0, :n_block].T / math.sqrt(d) * 1.4426950408889634
+    assert (lg[:, 1024:].max(axis=1) - lg[:, :128].max(axis=1)).min() > 16
+    S = logit_scale(Q64, K64[:, :n_block])
+    check_block_attention(Y.cpu().numpy(), lse.cpu().numpy(), Yr, lser, d, S, n_block,
+                          np.abs(V64[:, :n_block]).max())
+
+
 def test_block_attention_without_lse_and_into_out():
     g = torch.Generator().manual_seed(11)
     Q = torch.randn(8, 64, 128, generator=g).bfloat16().to(DEV)
@@ -162,6 +186,26 @@ def test_ridge_values_vs_oracle(Hkv, R, k, d, lam_frac):
     torch.cuda.synchronize()
     assert L.device_error() == 0
     check_ridge(Vc.cpu().numpy(), Qt64, Kc64, Y64, lam, kappa)
+
+
+def test_ridge_values_nan_key_reports_range():
+    """A NaN among one head's compressed keys makes every pivot of that head's
+    factorisation NaN: the head's values are 0, KVS_ERR_RANGE is recorded, and
+    the other head (its own cluster) is unaffected."""
+    Hkv, R, k, d = 2, 40, 64, 128
+    g = torch.Generator().manual_seed(5)
+    Qt = torch.randn(Hkv, R, d, generator=g).bfloat16()
+    Kc = torch.randn(Hkv, k, d, generator=g).bfloat16()
+    Y = (0.3 * torch.randn(Hkv, R, d, generator=g)).float()
+    Kc[0, 3, 7] = float("nan")
+    Qt64, Kc64, Y64 = Qt.double().numpy(), Kc.double().numpy(), Y.double().numpy()
+    lam, kappa = lam_and_kappa(Qt64[1:], Kc64[1:], 0.05)
+    Vc = L.ridge_values(Qt.to(DEV), Kc.to(DEV), Y.to(DEV), lam)
+    torch.cuda.synchronize()
+    assert L.device_error() == 3                     # KVS_ERR_RANGE
+    out = Vc.cpu().numpy()
+    assert (out[0] == 0).all()
+    check_ridge(out[1:], Qt64[1:], Kc64[1:], Y64[1:], lam, kappa)
 
 
 def test_ridge_values_after_block_attention_llama3_8b_layer():
