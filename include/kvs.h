@@ -461,7 +461,7 @@ int kvs_spectrum(const float* G, int64_t Hkv, int64_t d, float rtol, float* sigm
  * The logits as in kvs_block_attention (bf16 products, fp32 sums), then fp32:
  * A, the lower triangle of A^T A + lam I and A^T Y (as two partial sums over
  * the halves of R), and a blocked Cholesky solve on a cluster of 8 CTAs per
- * head (one cluster per head at a time: about 187 KB of shared memory each).  A pivot that is not positive (lam too small for fp32
+ * head (one cluster per head at a time: about 183 KB of shared memory each).  A pivot that is not positive (lam too small for fp32
  * against |A^T A|) records KVS_ERR_RANGE in the error word and sets that
  * head's values to 0.  d in {64, 128}, else KVS_ERR_UNSUPPORTED; k > 512
  * gives KVS_ERR_UNSUPPORTED. */

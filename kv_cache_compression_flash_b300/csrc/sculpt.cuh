@@ -794,8 +794,7 @@ constexpr int kRsOffAt = kRsOffB + 2 * 32 * kRidgeMaxD;       // the solves' rig
 constexpr int kRsOffPt = kRsOffAt + 2 * 32 * kRsLdAt;         // panel; in the solves a row or column block of L
 constexpr int kRsOffDinv = kRsOffPt + 32 * kRsLdp;            // L_bb^-1 of the two blocks
 constexpr int kRsOffTinv = kRsOffDinv + 2 * kRsBlk;           // a copy of the current L_bb^-1
-constexpr int kRsOffDiag = kRsOffTinv + kRsBlk;               // the diagonal block being factored
-constexpr int kRsOffFlag = kRsOffDiag + kRsBlk;               // a pivot was not positive
+constexpr int kRsOffFlag = kRsOffTinv + kRsBlk;               // a pivot was not positive
 constexpr size_t kRsSmemBytes = static_cast<size_t>(kRsOffFlag + 4) * sizeof(float);
 static_assert(kRidgeMaxK * (kRidgeMaxD / kRsCluster) <= 2 * 32 * kRidgeMaxD, "the channel slice fits");
 static_assert(32 * (kRidgeMaxK - 32) <= 32 * kRsLdp, "a row or column block of L fits in the panel's space");
@@ -826,7 +825,6 @@ __global__ void __launch_bounds__(kRsThreads, 1)
   float* PT = sm + kRsOffPt;
   float* dinv = sm + kRsOffDinv;
   float* tinv = sm + kRsOffTinv;
-  float* diag = sm + kRsOffDiag;
   int* flag = reinterpret_cast<int*>(sm + kRsOffFlag);
   const int own[2] = {rank, 2 * kRsCluster - 1 - rank};  // slot 0 holds the lower block
   const bool has[2] = {own[0] < nblk, own[1] < nblk};
@@ -863,11 +861,9 @@ __global__ void __launch_bounds__(kRsThreads, 1)
     if (rank == ob && warp == 0) {  // L_bb in registers (lane = row), then L_bb^-1 (lane = column)
       const float* Db = (sb ? Ms[1] : Ms[0]) + 32 * b;
       const int ldb = sb ? lds[1] : lds[0];
-      for (int e = lane; e < 32 * 32; e += 32) diag[(e >> 5) * kRsLd + (e & 31)] = Db[(e >> 5) * ldb + (e & 31)];
-      __syncwarp();
-      float a[32];  // row `lane` of the block; the lower triangle becomes L_bb
+      float a[32];  // row `lane` of the block, straight from the CTA's rows; the lower triangle becomes L_bb
 #pragma unroll
-      for (int c = 0; c < 32; ++c) a[c] = diag[lane * kRsLd + c];
+      for (int c = 0; c < 32; ++c) a[c] = Db[lane * ldb + c];
       bool ok = true;  // the same value in every lane (no early exit: a[] stays in registers)
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
