@@ -1004,14 +1004,15 @@ int kvs_block_attention(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
   const dim3 grid(static_cast<unsigned>(Hkv * n_hc * n_pb));
   const int Wi = static_cast<int>(W), p0 = static_cast<int>(q_pos0), nb = static_cast<int>(n_block);
   // the kernel's register split must fit the registers it is launched with
-  // (otherwise the softmax warpgroups would wait for registers forever)
+  // (otherwise the softmax warpgroups would wait for registers forever);
+  // checked once per kernel: its attributes do not change
   auto split_fits = [](const void* kern) {
     cudaFuncAttributes fa{};
     return cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.numRegs * kBtThreads >= kBtRegPool;
   };
-  if (!split_fits(reinterpret_cast<const void*>(d == 64 ? block_attention_tc_kernel<64>
-                                                        : block_attention_tc_kernel<128>)))
-    return KVS_ERR_UNSUPPORTED;
+  static const bool fits64 = split_fits(reinterpret_cast<const void*>(block_attention_tc_kernel<64>));
+  static const bool fits128 = split_fits(reinterpret_cast<const void*>(block_attention_tc_kernel<128>));
+  if (!(d == 64 ? fits64 : fits128)) return KVS_ERR_UNSUPPORTED;
   if (d == 64) {
     const size_t smem = sizeof(BtSmem<64>) + 1024;
     KVS_CUDA_TRY(allow_smem(block_attention_tc_kernel<64>, smem));
